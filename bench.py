@@ -1,0 +1,426 @@
+"""Benchmark of libkda on one GB300 (or N replicas under torchrun).
+
+One step is one kda_prefill over the single-sequence prefill workload
+(B=1, H=32, T=4096, d_k=d_v=128, bf16 q/k/v, fp32 gates and state): every
+chunkwise row of the path (decay prefix, decayed operands, k-k and q-k
+matrices, UT solve, WY factors, output, state propagation).  The decode row is
+timed in the same run on its own workload (256 sequences x 32 heads, d=128,
+1000 in-place steps) and reported under "decode".
+
+value    prefill tokens/s with inputs resident in HBM (CUDA events, L2 flushed
+         between timed steps by writing a 256 MiB buffer, flush not timed);
+e2e      the same through the C ABI with pinned host buffers: host->device
+         copy of the step's inputs, kda_prefill, device->host copy of o and the
+         final state, all inside the timed region;
+roofline HBM-bound: algorithmic bytes of one prefill / its event-timed
+         duration, against the measured copy bandwidth in MEASURED_PEAKS.json;
+cpu_baseline  the fp64 oracle on the host cores (rank 0, N=1 only).
+
+`--impl reference` times the oracle itself (the only other implementation of
+the method here) on the same workload and prints the same line with
+"impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KDA prefill tokens/s & decode steps/s (H=32,d=128) and % of roofline"
+L2_FLUSH_BYTES = 256 << 20
+
+
+def _env_rank():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
+        int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def measured_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+def prefill_algorithmic_bytes(T, H, d, n_seqs, io_bytes, with_init):
+    per_token_head = (3 * d * io_bytes) + d * 4 + 4 + d * io_bytes  # q,k,v + log_alpha + beta + o
+    state = n_seqs * H * d * d * 4 * (2 if with_init else 1)
+    return T * H * per_token_head + state
+
+
+def prefill_flops(T, H, d, C=64):
+    # dense-tile count per token-head: 5 C x C x d products and 3 C x d x d products per chunk
+    return T * H * (10 * C * d + 6 * d * d)
+
+
+def decode_algorithmic_bytes(B, H, d, io_bytes):
+    return B * H * (2 * d * d * 4 + 3 * d * io_bytes + d * 4 + 4 + d * io_bytes)
+
+
+def source_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "kda_gated_delta_04_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        if f.endswith((".cu", ".cuh")):
+            h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel_key):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
+    current kernel sources; None otherwise."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    e = d.get(kernel_key)
+    if not e or e.get("source_sha") != source_sha():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, ValueError):
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in getattr(self, "lines", []):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax = float(parts[2])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- GPU arm
+def run_gpu(args):
+    import torch
+    from kda_gated_delta_04_gb300 import kda, synth
+
+    rank, world, local_rank = _env_rank()
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    w = synth.PREFILL_4K
+    seed = args.seed + rank  # each replica runs its own independent units
+    inp = synth.prefill_inputs(w, seed=seed)
+    T, H, d = inp["q"].shape
+    x = {k: inp[k].to(dev) for k in ("q", "k", "v", "log_alpha", "beta", "cu_seqlens")}
+    o = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
+    fs = torch.empty((1, H, d, d), dtype=torch.float32, device=dev)
+    ws = kda.workspace_for(1, T, H, d, kda.KDA_DTYPE_BF16, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    sh = stream.cuda_stream
+    launches_per_prefill = 2  # schedule/validation kernel + chunk kernel
+
+    def prefill_call():
+        st = kda.kda_prefill(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
+                             x["log_alpha"].data_ptr(), x["beta"].data_ptr(),
+                             x["cu_seqlens"].data_ptr(), 1, T, H, d, d, kda.KDA_DTYPE_BF16, None,
+                             o.data_ptr(), fs.data_ptr(), ws.data_ptr(), ws.numel(), sh)
+        if st != kda.KDA_OK:
+            raise kda.KdaError(st, "kda_prefill")
+
+    peaks = measured_peaks()
+    clocks = ClockSampler(local_rank)
+    with clocks:
+        # ------------------------------------------------ prefill, inputs resident in HBM
+        for _ in range(args.warmup):
+            flush.zero_()
+            prefill_call()
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        torch.cuda.synchronize()
+        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.steps)]
+        for a, b in ev:
+            flush.zero_()  # evict L2 between timed steps (not timed)
+            a.record(stream)
+            prefill_call()
+            b.record(stream)
+        torch.cuda.synchronize()
+        step_ms = [a.elapsed_time(b) for a, b in ev]
+        if dist:
+            dist.barrier()
+        total_ms = sum(step_ms)
+        st = kda.kda_read_device_status(ws.data_ptr(), sh)
+        if st != kda.KDA_OK:
+            raise kda.KdaError(st, "kda_prefill (device status)")
+
+        # ------------------------------------------------ prefill end to end from host
+        pin = {k: inp[k].pin_memory() for k in ("q", "k", "v", "log_alpha", "beta")}
+        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
+        fs_host = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        d2h = o_host.numel() * o_host.element_size() + fs_host.numel() * fs_host.element_size()
+
+        def e2e_step():
+            for k_, t in pin.items():
+                x[k_].copy_(t, non_blocking=True)
+            prefill_call()
+            o_host.copy_(o, non_blocking=True)
+            fs_host.copy_(fs, non_blocking=True)
+
+        for _ in range(max(1, args.warmup)):
+            e2e_step()
+        torch.cuda.synchronize()
+        e_ms = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            b.synchronize()
+            e_ms.append(a.elapsed_time(b))
+
+        # ------------------------------------------------ decode: 1000 in-place steps
+        dw = synth.DECODE_256
+        ring = [{k: t.to(dev) for k, t in synth.decode_inputs(dw, s, seed=seed).items()}
+                for s in range(16)]
+        state = synth.decode_state(dw, seed=seed).to(dev)
+        o_dec = torch.empty((dw.batch, dw.num_heads, dw.d), dtype=torch.bfloat16, device=dev)
+
+        def decode_call(s):
+            r = ring[s % len(ring)]
+            st = kda.kda_decode_step(r["q"].data_ptr(), r["k"].data_ptr(), r["v"].data_ptr(),
+                                     r["log_alpha"].data_ptr(), r["beta"].data_ptr(), dw.batch,
+                                     dw.num_heads, dw.d, dw.d, kda.KDA_DTYPE_BF16,
+                                     state.data_ptr(), o_dec.data_ptr(), sh)
+            if st != kda.KDA_OK:
+                raise kda.KdaError(st, "kda_decode_step")
+
+        for s in range(max(3, args.warmup)):
+            decode_call(s)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for s in range(dw.steps):
+            decode_call(s)
+        b.record(stream)
+        torch.cuda.synchronize()
+        if dist:
+            dist.barrier()
+        dec_ms = a.elapsed_time(b)
+
+    def max_over_ranks(v):
+        if not dist:
+            return v
+        t = torch.tensor([v], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    total_ms = max_over_ranks(total_ms)
+    e2e_total = max_over_ranks(sum(e_ms))
+    dec_ms = max_over_ranks(dec_ms)
+    mean_step_ms = total_ms / args.steps
+    tokens = T * world * args.steps
+    value = tokens / (total_ms / 1e3)
+    alg_bytes = prefill_algorithmic_bytes(T, H, d, 1, 2, False)
+    achieved = alg_bytes / (mean_step_ms / 1e3) / 1e9
+    dec_bytes = decode_algorithmic_bytes(dw.batch, dw.num_heads, dw.d, 2)
+    dec_step_ms = dec_ms / dw.steps
+    dec_achieved = dec_bytes / (dec_step_ms / 1e3) / 1e9
+    line = {
+        "metric": METRIC,
+        "value": value,
+        "unit": "tokens/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": mean_step_ms,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded counter-based generator; no dataset)",
+        "config": {"workload": w.name, "batch": 1, "num_heads": H, "seq_len": T, "d_k": d,
+                   "d_v": d, "chunk": 64, "io_dtype": "bf16", "gate_state_dtype": "f32",
+                   "l2": "flushed between timed steps (256 MiB write, untimed)",
+                   "parallelism": f"replicas x{world} (independent units, no collective)"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": profiled_traffic("prefill_4k"),
+                     "peak_source": peaks["source"],
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "tensor_frac_of_bf16_peak": prefill_flops(T, H, d) / (mean_step_ms / 1e3)
+                     / 1e12 / peaks["bf16_tflops"],
+                     "note": "duration from CUDA events around kda_prefill (its schedule kernel "
+                             "and the chunk kernel)"},
+        "e2e": {"value": T * world * args.steps / (e2e_total / 1e3), "unit": "tokens/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches_per_prefill * args.steps,
+        "clocks": clocks.summary(),
+        "decode": {"metric": "KDA decode steps/s", "workload": dw.name,
+                   "value": dw.steps * world / (dec_ms / 1e3), "unit": "steps/s",
+                   "ms_per_step": dec_step_ms, "steps": dw.steps, "gpu_launches": dw.steps,
+                   "tokens_per_s": dw.steps * dw.batch * world / (dec_ms / 1e3),
+                   "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"],
+                                "unit": "GB/s", "frac": dec_achieved / peaks["hbm_gbs"],
+                                "traffic": profiled_traffic("decode_256"),
+                                "algorithmic_bytes_per_launch": dec_bytes}},
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, inp)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.destroy_process_group()
+
+
+# ----------------------------------------------------------------------------- CPU arm
+def _oracle_inputs(inp):
+    from kda_gated_delta_04_gb300 import synth
+    return {k: synth.to_f64(inp[k]) for k in ("q", "k", "v", "log_alpha", "beta")}
+
+
+def cpu_baseline(w, inp, heads=None):
+    """The oracle as it stands, all host cores, on the whole prefill workload (or the
+    given heads); returns the cpu_baseline object (tokens/s of that sample)."""
+    import oracle
+    f = _oracle_inputs(inp)
+    if heads is not None:
+        f = {k: np.ascontiguousarray(v[:, heads]) for k, v in f.items()}
+    T, H = f["q"].shape[:2]
+    t0 = time.perf_counter()
+    _, _, used = oracle.prefill(f["q"], f["k"], f["v"], f["log_alpha"], f["beta"])
+    dt = time.perf_counter() - t0
+    return {"value": T * H / w.num_heads / dt, "unit": "tokens/s", "cores": used,
+            "kind": "oracle",
+            "sample": f"{w.name}: {H} of {w.num_heads} heads x {T} tokens, fp64 token-by-token, "
+                      f"{dt:.2f} s wall; tokens/s counts a token as all {w.num_heads} heads",
+            "cpu": _cpu_model(), "nproc": os.cpu_count()}
+
+
+def _cpu_model():
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part", "hardware")):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def run_reference(args):
+    rank, world, _ = _env_rank()
+    if rank != 0:
+        return
+    from kda_gated_delta_04_gb300 import synth
+    import oracle
+    w = synth.PREFILL_4K
+    inp = synth.prefill_inputs(w, seed=args.seed)
+    f = _oracle_inputs(inp)
+    # each step: the oracle on the whole workload (32 heads x 4096 tokens, ~1-2 s on
+    # 8-16 cores), so K steps stay within a few minutes
+    heads = list(range(w.num_heads))
+    fs = {k: np.ascontiguousarray(v[:, heads]) for k, v in f.items()}
+    T = fs["q"].shape[0]
+    used = 0
+    for _ in range(args.warmup):
+        oracle.prefill(fs["q"], fs["k"], fs["v"], fs["log_alpha"], fs["beta"])
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        _, _, used = oracle.prefill(fs["q"], fs["k"], fs["v"], fs["log_alpha"], fs["beta"])
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = T * len(heads) / w.num_heads * args.steps / total
+    sample = (f"{w.name}: all {len(heads)} heads x {T} tokens per step, fp64 token-by-token "
+              f"oracle on {used} threads")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": total / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded counter-based generator)",
+        "config": {"workload": w.name, "batch": 1, "num_heads": w.num_heads, "seq_len": T,
+                   "d_k": w.d, "d_v": w.d, "chunk": 64, "io_dtype": "bf16",
+                   "gate_state_dtype": "f32"},
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": used, "kind": "oracle",
+                         "sample": sample, "cpu": _cpu_model(), "nproc": os.cpu_count()},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

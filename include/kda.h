@@ -1,0 +1,140 @@
+/*
+ * kda.h -- C ABI of libkda: the Kimi Delta Attention (KDA) recurrence on one GPU.
+ *
+ * The operation (per sequence n, head h; key channel i < d_k, value channel j < d_v):
+ *
+ *     decayed   = Diag(alpha_t) S_{t-1}                 alpha_t = exp(log_alpha[t,h,:])
+ *     S_t       = decayed + beta_t k_t (v_t - decayed^T k_t)^T
+ *     o_t       = S_t^T q_t / sqrt(d_k)
+ *
+ * Sources: "Day 19, linear attention & KDA" (ai.air7.fun, k3-course-30), section 3:
+ * the update decays the state per channel first, then writes back only the
+ * prediction error scaled by beta_t; "K3 attention, three-piece set"
+ * (yeyulingfeng.com), KDA paragraphs: the (I - beta_t k_t k_t^T) factor, the
+ * per-key-channel gate Diag(alpha_t), a fixed-size d_k x d_v state per head,
+ * and the chunkwise-parallel deployment form; "From 124M to 2.8T"
+ * (ciyuanerhao.com), chapter 4: the gate has one value per key channel and
+ * scales the key rows of S.  The 1/sqrt(d_k) output scale is this library's
+ * definition (the pages state none).  q and k are expected to be L2-normalised
+ * by the caller (the pages normalise them inside the layer, before this step).
+ *
+ * Conventions shared by every call:
+ *  - All tensor pointers are DEVICE pointers owned by the caller, row-major and
+ *    contiguous (last dimension has stride 1), 16-byte aligned.  The library
+ *    allocates no device memory and keeps no mutable global state besides
+ *    cached device attributes.
+ *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*, NULL =
+ *    the legacy default stream) and never synchronise, except
+ *    kda_read_device_status.
+ *  - Argument errors are reported synchronously, before anything is enqueued.
+ *    A failed kernel launch returns KDA_ERR_CUDA.  Errors detected on the device
+ *    (see kda_prefill) are recorded in the workspace and read back with
+ *    kda_read_device_status.  Nothing aborts or throws across the ABI.
+ *  - Supported shapes: d_k == d_v == 64 or 128, with q/k/v/o stored as bf16 or
+ *    fp32 (kda_dtype_t); log_alpha, beta and every state are fp32.  Other shapes
+ *    return KDA_ERR_UNSUPPORTED.
+ */
+#ifndef LIBKDA_KDA_H
+#define LIBKDA_KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment, bad cu_seqlens  */
+    KDA_ERR_UNSUPPORTED = 2,  /* valid but not implemented shape / dtype / device       */
+    KDA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed            */
+    KDA_ERR_TIMEOUT = 4,      /* a bounded device-side wait expired (no hang, no trap)  */
+    KDA_ERR_DECAY_RANGE = 5   /* a chunk's cumulative log-decay left the supported range */
+} kda_status_t;
+
+typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_F32 = 1 } kda_dtype_t;
+
+/* Chunk length of the chunkwise prefill (tokens). */
+#define KDA_CHUNK 64
+/* Lower bound on sum(log_alpha) over any 64-token chunk, per key channel, that
+ * kda_prefill supports: its chunk factorisation forms exp(-g) for the in-chunk
+ * cumulative log-decay g, which must stay finite in fp32. */
+#define KDA_MIN_CHUNK_LOG_DECAY (-80.0f)
+
+/*
+ * Bytes of device workspace kda_prefill needs for this problem (a status word
+ * and a sequence schedule).  Pure host arithmetic; never fails (returns 0 only
+ * for num_seqs < 0).
+ */
+size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                                  int32_t d_k, int32_t d_v, kda_dtype_t dtype);
+
+/*
+ * Chunkwise prefill over packed variable-length sequences ("K3 attention,
+ * three-piece set": chunkwise-parallel form with WY representation and UT
+ * transform; "From 124M to 2.8T", chapter 3: parallel inside a chunk, serial
+ * across chunks).  Chunks of KDA_CHUNK tokens never cross a sequence boundary.
+ *
+ *  q, k        [total_tokens, num_heads, d_k]  dtype
+ *  v           [total_tokens, num_heads, d_v]  dtype
+ *  log_alpha   [total_tokens, num_heads, d_k]  fp32, finite, <= 0; per chunk and
+ *              channel its sum must be >= KDA_MIN_CHUNK_LOG_DECAY
+ *  beta        [total_tokens, num_heads]       fp32
+ *  cu_seqlens  [num_seqs + 1] int32 device offsets: 0 = cu[0] <= ... <= cu[num_seqs]
+ *              = total_tokens; NULL means one sequence of total_tokens tokens
+ *              (num_seqs must then be 1)
+ *  init_state  [num_seqs, num_heads, d_k, d_v] fp32, or NULL for zero states
+ *  o           [total_tokens, num_heads, d_v]  dtype (written for every token)
+ *  final_state [num_seqs, num_heads, d_k, d_v] fp32; may equal init_state
+ *              (in-place update); a zero-length sequence gets its initial state
+ *  workspace   device buffer of at least kda_prefill_workspace_size(...) bytes,
+ *              owned by the caller, 256-byte aligned; reused by every call
+ *  q, k, v, log_alpha, beta and o may be NULL when total_tokens == 0.
+ *
+ * Device-side errors (timeout of a bounded wait, a cu_seqlens array that is not
+ * a valid prefix sum, a decay outside the supported range) do not fault: the
+ * kernels clamp every access to the buffers, finish, and record the error in the
+ * workspace.  Each call clears the record first; read it with
+ * kda_read_device_status.  Calls that share a workspace must be ordered (same
+ * stream or synchronised).
+ */
+kda_status_t kda_prefill(const void *q, const void *k, const void *v, const float *log_alpha,
+                         const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                         int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                         kda_dtype_t dtype, const float *init_state, void *o, float *final_state,
+                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * One decode step for `batch` sequences x num_heads heads: the recurrence for a
+ * single new token per sequence, applied to the caller's state in place
+ * ("Day 19", section 2: constant memory and O(1) work per generated token;
+ * "K3 attention, three-piece set": fixed-size d_k x d_v state per KDA head).
+ *
+ *  q, k, log_alpha  [batch, num_heads, d_k]  (q, k dtype; log_alpha fp32)
+ *  v                [batch, num_heads, d_v]  dtype
+ *  beta             [batch, num_heads]       fp32
+ *  state            [batch, num_heads, d_k, d_v] fp32, read and overwritten
+ *  o                [batch, num_heads, d_v]  dtype
+ * No workspace; no device-side error conditions.  batch == 0 is a no-op that
+ * enqueues nothing (every pointer may then be NULL).
+ */
+kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
+                             const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
+                             int32_t d_v, kda_dtype_t dtype, float *state, void *o, void *stream);
+
+/*
+ * Synchronises `stream`, reads the device-side error record of the last
+ * kda_prefill that used `workspace`, clears it, and returns the first error
+ * found (KDA_OK when none).  Explicit synchronisation point.
+ */
+kda_status_t kda_read_device_status(void *workspace, void *stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+const char *kda_status_string(kda_status_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LIBKDA_KDA_H */

@@ -1,0 +1,93 @@
+// common.cuh -- internal definitions shared by libkda's CUDA translation units.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/kda.h"
+
+namespace kda {
+
+// Bits of the device-side error word at the head of the prefill workspace.
+enum : uint32_t {
+    DEV_ERR_SEQLENS = 1u,  // cu_seqlens is not a prefix sum ending at total_tokens
+    DEV_ERR_TIMEOUT = 2u,  // a bounded mbarrier / flag wait gave up
+    DEV_ERR_DECAY = 4u,    // |in-chunk cumulative log-decay| exceeded the supported range
+};
+
+constexpr int kChunk = KDA_CHUNK;
+constexpr size_t kWorkspaceHeader = 256;  // status word, padded
+
+// Everything a prefill launch needs, already validated on the host.
+struct PrefillProblem {
+    const void *q, *k, *v;
+    const float *log_alpha, *beta;
+    const int32_t *cu_seqlens;  // may be null: one sequence of total_tokens tokens
+    int num_seqs;
+    int64_t total_tokens;
+    int num_heads, d;           // d = d_k = d_v
+    kda_dtype_t dtype;
+    const float *init_state;    // may be null
+    void *o;
+    float *final_state;
+    uint32_t *status;           // workspace word
+    int32_t *order;             // workspace: sequence processing order (longest first)
+    cudaStream_t stream;
+};
+
+struct DecodeProblem {
+    const void *q, *k, *v;
+    const float *log_alpha, *beta;
+    int batch, num_heads, d;
+    kda_dtype_t dtype;
+    float *state;
+    void *o;
+    cudaStream_t stream;
+};
+
+// Launchers (each returns the launch error, cudaSuccess when enqueued).
+cudaError_t launch_prefill_prep(const PrefillProblem &p);
+cudaError_t launch_prefill_simt(const PrefillProblem &p);
+cudaError_t launch_decode(const DecodeProblem &p);
+
+// ---------------------------------------------------------------- device helpers
+__device__ __forceinline__ float load_io(const float *p) { return *p; }
+__device__ __forceinline__ float load_io(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
+__device__ __forceinline__ void store_io(float *p, float x) { *p = x; }
+__device__ __forceinline__ void store_io(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+
+// Four consecutive elements (16-byte aligned for fp32, 8-byte for bf16).
+__device__ __forceinline__ float4 load4_io(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 load4_io(const __nv_bfloat16 *p)
+{
+    const uint2 raw = *reinterpret_cast<const uint2 *>(p);
+    const __nv_bfloat162 a = *reinterpret_cast<const __nv_bfloat162 *>(&raw.x);
+    const __nv_bfloat162 b = *reinterpret_cast<const __nv_bfloat162 *>(&raw.y);
+    const float2 fa = __bfloat1622float2(a), fb = __bfloat1622float2(b);
+    return make_float4(fa.x, fa.y, fb.x, fb.y);
+}
+__device__ __forceinline__ void store4_io(float *p, float4 x) { *reinterpret_cast<float4 *>(p) = x; }
+__device__ __forceinline__ void store4_io(__nv_bfloat16 *p, float4 x)
+{
+    __nv_bfloat162 a = __floats2bfloat162_rn(x.x, x.y), b = __floats2bfloat162_rn(x.z, x.w);
+    uint2 raw;
+    raw.x = *reinterpret_cast<uint32_t *>(&a);
+    raw.y = *reinterpret_cast<uint32_t *>(&b);
+    *reinterpret_cast<uint2 *>(p) = raw;
+}
+
+// Token range [t0, t1) of sequence n, clamped to [0, total] so that a malformed
+// cu_seqlens can never send a kernel outside the buffers.
+__device__ __forceinline__ void seq_range(const int32_t *cu, int n, int64_t total, int64_t &t0,
+                                          int64_t &t1)
+{
+    if (!cu) { t0 = 0; t1 = total; return; }
+    int64_t a = cu[n], b = cu[n + 1];
+    a = a < 0 ? 0 : (a > total ? total : a);
+    b = b < a ? a : (b > total ? total : b);
+    t0 = a;
+    t1 = b;
+}
+
+}  // namespace kda

@@ -1,0 +1,149 @@
+// kda_api.cu -- the extern "C" boundary of libkda: argument validation, workspace
+// layout and kernel launches.  No compute happens here.
+#include <stdint.h>
+#include <string.h>
+
+#include "common.cuh"
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device check, cached per device (the only global state of the library):
+// 1 = supported (compute capability 10.3), -1 = not supported, 0 = unknown.
+int g_device_ok[kMaxDevices];
+
+kda_status_t check_device()
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return KDA_ERR_CUDA;
+    if (dev < 0 || dev >= kMaxDevices) return KDA_ERR_UNSUPPORTED;
+    if (g_device_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        g_device_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    return g_device_ok[dev] == 1 ? KDA_OK : KDA_ERR_UNSUPPORTED;
+}
+
+size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+kda_status_t check_shape(int32_t d_k, int32_t d_v, kda_dtype_t dtype)
+{
+    if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
+    if (d_k <= 0 || d_v <= 0) return KDA_ERR_INVALID_ARG;
+    if (d_k != d_v || (d_k != 64 && d_k != 128)) return KDA_ERR_UNSUPPORTED;
+    return KDA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                                  int32_t d_k, int32_t d_v, kda_dtype_t dtype)
+{
+    (void)total_tokens; (void)num_heads; (void)d_k; (void)d_v; (void)dtype;
+    if (num_seqs < 0) return 0;
+    return kda::kWorkspaceHeader + round_up((size_t)num_seqs * sizeof(int32_t) + 1, 256);
+}
+
+kda_status_t kda_prefill(const void *q, const void *k, const void *v, const float *log_alpha,
+                         const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                         int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                         kda_dtype_t dtype, const float *init_state, void *o, float *final_state,
+                         void *workspace, size_t workspace_bytes, void *stream)
+{
+    kda_status_t st = check_shape(d_k, d_v, dtype);
+    if (st != KDA_OK) return st;
+    if (num_seqs < 0 || total_tokens < 0 || num_heads <= 0) return KDA_ERR_INVALID_ARG;
+    if (num_seqs == 0 && total_tokens != 0) return KDA_ERR_INVALID_ARG;
+    if (!cu_seqlens && num_seqs != 1) return KDA_ERR_INVALID_ARG;
+    if (num_seqs > 65535) return KDA_ERR_UNSUPPORTED;  // grid z extent
+    if (num_heads > 65535) return KDA_ERR_UNSUPPORTED;  // grid y extent
+    // token tensors may be NULL only when there are no tokens
+    if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !o))
+        return KDA_ERR_INVALID_ARG;
+    if (!final_state || !workspace) return KDA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) ||
+        !aligned(o, 16) || !aligned(final_state, 16) || !aligned(beta, 4) ||
+        (init_state && !aligned(init_state, 16)) || (cu_seqlens && !aligned(cu_seqlens, 4)) ||
+        !aligned(workspace, 256))
+        return KDA_ERR_INVALID_ARG;
+    if (workspace_bytes < kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, d_k, d_v,
+                                                     dtype))
+        return KDA_ERR_INVALID_ARG;
+    st = check_device();
+    if (st != KDA_OK) return st;
+    if (num_seqs == 0) return KDA_OK;
+
+    kda::PrefillProblem p;
+    p.q = q; p.k = k; p.v = v; p.log_alpha = log_alpha; p.beta = beta;
+    p.cu_seqlens = cu_seqlens; p.num_seqs = num_seqs; p.total_tokens = total_tokens;
+    p.num_heads = num_heads; p.d = d_k; p.dtype = dtype; p.init_state = init_state;
+    p.o = o; p.final_state = final_state;
+    p.status = static_cast<uint32_t *>(workspace);
+    p.order = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + kda::kWorkspaceHeader);
+    p.stream = static_cast<cudaStream_t>(stream);
+
+    if (kda::launch_prefill_prep(p) != cudaSuccess) return KDA_ERR_CUDA;
+    if (kda::launch_prefill_simt(p) != cudaSuccess) return KDA_ERR_CUDA;
+    return KDA_OK;
+}
+
+kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
+                             const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
+                             int32_t d_v, kda_dtype_t dtype, float *state, void *o, void *stream)
+{
+    kda_status_t st = check_shape(d_k, d_v, dtype);
+    if (st != KDA_OK) return st;
+    if (batch < 0 || num_heads <= 0) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)batch * num_heads > INT32_MAX) return KDA_ERR_UNSUPPORTED;
+    if (batch == 0) return KDA_OK;  // nothing to read or write; pointers may be NULL
+    if (!q || !k || !v || !log_alpha || !beta || !state || !o) return KDA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) ||
+        !aligned(o, 16) || !aligned(state, 16) || !aligned(beta, 4))
+        return KDA_ERR_INVALID_ARG;
+    st = check_device();
+    if (st != KDA_OK) return st;
+    kda::DecodeProblem p;
+    p.q = q; p.k = k; p.v = v; p.log_alpha = log_alpha; p.beta = beta;
+    p.batch = batch; p.num_heads = num_heads; p.d = d_k; p.dtype = dtype;
+    p.state = state; p.o = o; p.stream = static_cast<cudaStream_t>(stream);
+    return kda::launch_decode(p) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_read_device_status(void *workspace, void *stream)
+{
+    if (!workspace || !aligned(workspace, 256)) return KDA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
+    if (word & kda::DEV_ERR_SEQLENS) return KDA_ERR_INVALID_ARG;
+    if (word & kda::DEV_ERR_TIMEOUT) return KDA_ERR_TIMEOUT;
+    if (word & kda::DEV_ERR_DECAY) return KDA_ERR_DECAY_RANGE;
+    return KDA_OK;
+}
+
+const char *kda_status_string(kda_status_t status)
+{
+    switch (status) {
+    case KDA_OK: return "KDA_OK";
+    case KDA_ERR_INVALID_ARG: return "KDA_ERR_INVALID_ARG: invalid argument";
+    case KDA_ERR_UNSUPPORTED: return "KDA_ERR_UNSUPPORTED: unsupported shape, dtype or device";
+    case KDA_ERR_CUDA: return "KDA_ERR_CUDA: CUDA runtime or launch failure";
+    case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device-side wait expired";
+    case KDA_ERR_DECAY_RANGE:
+        return "KDA_ERR_DECAY_RANGE: in-chunk cumulative log-decay outside the supported range";
+    }
+    return "KDA: unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,181 @@
+"""Python binding of libkda (ctypes).  Argument marshalling only.
+
+The raw functions ``kda_prefill``, ``kda_decode_step``,
+``kda_prefill_workspace_size``, ``kda_read_device_status`` and
+``kda_status_string`` are the C entry points of ``include/kda.h`` with the same
+names and arguments (pointers as integers).  ``prefill`` and ``decode_step``
+take torch CUDA tensors, allocate outputs with torch when none are given, and
+call the same entry points.  Every step of the computation runs in libkda's
+kernels; there is no fallback: if ``libkda.so`` is missing or the tensors are
+not on a CUDA device, these functions raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libkda.so")
+
+KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, \
+    KDA_ERR_DECAY_RANGE = range(6)
+KDA_DTYPE_BF16, KDA_DTYPE_F32 = 0, 1
+CHUNK = 64
+
+_lib = None
+_lock = threading.Lock()
+
+_c = ctypes
+_VP = _c.c_void_p
+_PREFILL_ARGS = [_VP, _VP, _VP, _VP, _VP, _VP, _c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
+                 _c.c_int32, _c.c_int, _VP, _VP, _VP, _VP, _c.c_size_t, _VP]
+_DECODE_ARGS = [_VP, _VP, _VP, _VP, _VP, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int,
+                _VP, _VP, _VP]
+EXPORTS = {
+    "kda_prefill_workspace_size": (_c.c_size_t, [_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
+                                                 _c.c_int32, _c.c_int]),
+    "kda_prefill": (_c.c_int, _PREFILL_ARGS),
+    "kda_decode_step": (_c.c_int, _DECODE_ARGS),
+    "kda_read_device_status": (_c.c_int, [_VP, _VP]),
+    "kda_status_string": (_c.c_char_p, [_c.c_int]),
+}
+
+
+class KdaError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {status_string(status)}")
+
+
+def lib():
+    """The loaded libkda (ctypes.CDLL).  Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"libkda.so not found at {LIB_PATH}; build it with "
+                                   "`python -c 'import __graft_entry__ as g; g.build()'`")
+            L = ctypes.CDLL(LIB_PATH)
+            for name, (res, args) in EXPORTS.items():
+                fn = getattr(L, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = L
+    return _lib
+
+
+# ------------------------------------------------------------------ raw C entry points
+def kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, d_k, d_v, dtype):
+    return lib().kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, d_k, d_v, dtype)
+
+
+def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
+                d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream):
+    return lib().kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens,
+                             num_heads, d_k, d_v, dtype, init_state, o, final_state, workspace,
+                             workspace_bytes, stream)
+
+
+def kda_decode_step(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype, state, o, stream):
+    return lib().kda_decode_step(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype,
+                                 state, o, stream)
+
+
+def kda_read_device_status(workspace, stream):
+    return lib().kda_read_device_status(workspace, stream)
+
+
+def status_string(status: int) -> str:
+    return lib().kda_status_string(int(status)).decode()
+
+
+kda_status_string = status_string
+
+
+# ------------------------------------------------------------------ torch convenience
+def _torch():
+    import torch
+    return torch
+
+
+def _dtype_code(t):
+    torch = _torch()
+    if t.dtype == torch.bfloat16:
+        return KDA_DTYPE_BF16
+    if t.dtype == torch.float32:
+        return KDA_DTYPE_F32
+    raise TypeError(f"q/k/v must be bf16 or fp32, got {t.dtype}")
+
+
+def _ptr(t, name, dtype=None):
+    torch = _torch()
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream_handle(stream, device):
+    torch = _torch()
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return s.cuda_stream
+
+
+def workspace_for(num_seqs, total_tokens, num_heads, d, dtype_code, device):
+    torch = _torch()
+    nbytes = kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, d, d, dtype_code)
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=None,
+            final_state=None, workspace=None, stream=None, check_status=False):
+    """KDA prefill over packed sequences.  q, k: [T, H, d]; v: [T, H, d]; log_alpha: [T, H, d]
+    fp32; beta: [T, H] fp32; cu_seqlens: int32 [N+1] CUDA tensor or None (one sequence);
+    init_state: [N, H, d, d] fp32 or None.  Returns (o, final_state)."""
+    torch = _torch()
+    T, H, d = q.shape
+    dt = _dtype_code(q)
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None:
+        o = torch.empty((T, H, v.shape[2]), dtype=q.dtype, device=q.device)
+    if final_state is None:
+        final_state = torch.empty((N, H, d, v.shape[2]), dtype=torch.float32, device=q.device)
+    if workspace is None:
+        workspace = workspace_for(N, T, H, d, dt, q.device)
+    st = kda_prefill(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
+                     _ptr(log_alpha, "log_alpha", torch.float32), _ptr(beta, "beta", torch.float32),
+                     _ptr(cu_seqlens, "cu_seqlens", torch.int32), N, T, H, d, v.shape[2], dt,
+                     _ptr(init_state, "init_state", torch.float32), _ptr(o, "o", q.dtype),
+                     _ptr(final_state, "final_state", torch.float32), _ptr(workspace, "workspace"),
+                     workspace.numel() * workspace.element_size(),
+                     _stream_handle(stream, q.device))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill")
+    if check_status:
+        st = kda_read_device_status(workspace.data_ptr(), _stream_handle(stream, q.device))
+        if st != KDA_OK:
+            raise KdaError(st, "kda_prefill (device)")
+    return o, final_state
+
+
+def decode_step(q, k, v, log_alpha, beta, state, *, o=None, stream=None):
+    """One decode step; state [B, H, d, d] fp32 is updated in place.  Returns o [B, H, d]."""
+    torch = _torch()
+    B, H, d = q.shape
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty((B, H, v.shape[2]), dtype=q.dtype, device=q.device)
+    st = kda_decode_step(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
+                         _ptr(log_alpha, "log_alpha", torch.float32),
+                         _ptr(beta, "beta", torch.float32), B, H, d, v.shape[2], dt,
+                         _ptr(state, "state", torch.float32), _ptr(o, "o", q.dtype),
+                         _stream_handle(stream, q.device))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_step")
+    return o

@@ -1,0 +1,106 @@
+"""The C-ABI library: builds, loads, exports every declared entry point, and
+rejects bad arguments on the host before touching any GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def kda():
+    from kda_gated_delta_04_gb300 import build
+    build.build()
+    from kda_gated_delta_04_gb300 import kda as binding
+    return binding
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for required in ("kda_prefill", "kda_decode_step", "kda_prefill_workspace_size",
+                     "kda_read_device_status", "kda_status_string"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(kda):
+    lib = ctypes.CDLL(kda.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(lib, name), f"libkda.so does not export {name}"
+    assert set(declared_functions()) == set(kda.EXPORTS)
+
+
+def test_status_strings(kda):
+    for code in range(6):
+        s = kda.status_string(code)
+        assert s.startswith("KDA_")
+    assert "unknown" in kda.status_string(99)
+
+
+def test_workspace_size(kda):
+    a = kda.kda_prefill_workspace_size(1, 4096, 32, 128, 128, 0)
+    b = kda.kda_prefill_workspace_size(16, 10, 32, 128, 128, 0)
+    assert a >= 256 + 4 and a % 256 == 0
+    assert b >= 256 + 64 and b % 256 == 0
+    assert kda.kda_prefill_workspace_size(-1, 0, 1, 64, 64, 1) == 0
+
+
+FAKE = 1 << 20  # 16-byte aligned dummy address; never dereferenced (rejected first)
+
+
+def _prefill_args(**over):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, log_alpha=FAKE, beta=FAKE, cu_seqlens=None, num_seqs=1,
+             total_tokens=64, num_heads=2, d_k=64, d_v=64, dtype=1, init_state=None, o=FAKE,
+             final_state=FAKE, workspace=FAKE, workspace_bytes=1 << 16, stream=None)
+    a.update(over)
+    return a
+
+
+@pytest.mark.parametrize("over,expected", [
+    (dict(q=None), 1), (dict(o=None), 1), (dict(final_state=None), 1), (dict(workspace=None), 1),
+    (dict(q=FAKE + 4), 1), (dict(workspace=FAKE + 16), 1), (dict(workspace_bytes=8), 1),
+    (dict(num_seqs=2), 1),                     # cu_seqlens required for several sequences
+    (dict(num_heads=0), 1), (dict(total_tokens=-1), 1), (dict(dtype=7), 1),
+    (dict(num_seqs=0, total_tokens=5, cu_seqlens=FAKE), 1),
+    (dict(d_k=96, d_v=96), 2), (dict(d_k=128, d_v=64), 2), (dict(d_k=256, d_v=256), 2),
+])
+def test_prefill_rejects_bad_arguments_on_host(kda, over, expected):
+    a = _prefill_args(**over)
+    assert kda.kda_prefill(*a.values()) == expected
+
+
+@pytest.mark.parametrize("over,expected", [
+    (dict(state=None), 1), (dict(beta=None), 1), (dict(o=FAKE + 8), 1), (dict(num_heads=0), 1),
+    (dict(batch=-1), 1), (dict(d_k=32, d_v=32), 2), (dict(dtype=3), 1),
+])
+def test_decode_rejects_bad_arguments_on_host(kda, over, expected):
+    a = dict(q=FAKE, k=FAKE, v=FAKE, log_alpha=FAKE, beta=FAKE, batch=4, num_heads=2, d_k=128,
+             d_v=128, dtype=0, state=FAKE, o=FAKE, stream=None)
+    a.update(over)
+    assert kda.kda_decode_step(*a.values()) == expected
+
+
+def test_binding_refuses_cpu_tensors(kda):
+    import torch
+    x = torch.zeros(4, 1, 64)
+    with pytest.raises(TypeError):
+        kda.decode_step(x, x, x, x, torch.zeros(4, 1), torch.zeros(4, 1, 64, 64))
+
+
+def test_product_path_does_not_import_the_oracle():
+    """The package and its native sources never reach the oracle or its sources."""
+    pkg = os.path.join(ROOT, "kda_gated_delta_04_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".c", ".h")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert "import oracle" not in text and "from oracle" not in text, f
+                assert "kda_oracle" not in text, f

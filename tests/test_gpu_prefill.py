@@ -1,0 +1,155 @@
+"""GPU parity of kda_prefill against the fp64 oracle (through the C ABI).
+
+Small problems are compared element by element; they span several chunks and
+ragged tails.  The full-size workloads run exactly as the benchmark launches
+them, and the oracle recomputes sampled (sequence, head) units, whose inputs
+the counter-based generator reproduces on their own.
+"""
+import numpy as np
+import pytest
+import torch
+
+from kda_gated_delta_04_gb300 import kda, synth
+from kda_gated_delta_04_gb300.synth import PrefillWorkload
+from parity_util import assert_parity, gpu_prefill, oracle_prefill, relF, to_device
+
+pytestmark = pytest.mark.gpu
+
+SMALL = [
+    synth.TINY,
+    PrefillWorkload("bf16_d128_T200_H3_state", 100, 3, 128, "bf16", (200,), 1, init_state=True),
+    PrefillWorkload("bf16_d128_varlen_edges", 101, 2, 128, "bf16", (0, 1, 63, 64, 65, 130), 6),
+    PrefillWorkload("f32_d128_T150_H2_state", 102, 2, 128, "f32", (150,), 1, init_state=True),
+    PrefillWorkload("bf16_d64_varlen_state", 103, 2, 64, "bf16", (5, 100, 64), 3, init_state=True),
+    PrefillWorkload("f32_d64_varlen", 104, 3, 64, "f32", (64, 1, 191), 3),
+]
+
+
+@pytest.mark.parametrize("w", SMALL, ids=lambda w: w.name)
+def test_small_problems_match_oracle(w):
+    inp = synth.prefill_inputs(w)
+    o, fs = gpu_prefill(inp)
+    o_ref, fs_ref = oracle_prefill(inp)
+    assert_parity(o, fs, o_ref, fs_ref, w.dtype, w.name)
+
+
+def _sampled_full_size(w, units):
+    """Run the whole workload on the GPU; recompute the listed (seq, head) units on the oracle."""
+    full = synth.prefill_inputs(w)
+    o, fs = gpu_prefill(full)
+    cu = full["cu_seqlens"].numpy()
+    for s, h in units:
+        sub = synth.prefill_inputs(w, heads=[h], seqs=[s])
+        t0, t1 = int(cu[s]), int(cu[s + 1])
+        # the generator reproduces the unit's inputs exactly
+        assert torch.equal(sub["q"][:, 0], full["q"][t0:t1, h])
+        o_ref, fs_ref = oracle_prefill(sub)
+        assert_parity(o[t0:t1, h], fs[s, h], o_ref[:, 0], fs_ref[0, 0], w.dtype,
+                      f"{w.name} seq {s} head {h}")
+    assert np.isfinite(o).all() and np.isfinite(fs).all()
+
+
+def test_prefill_4k_full_size_sampled():
+    _sampled_full_size(synth.PREFILL_4K, [(0, 0), (0, 13), (0, 31)])
+
+
+def test_prefill_64k_with_initial_state_full_size_sampled():
+    _sampled_full_size(synth.PREFILL_64K, [(0, 5), (0, 26)])
+
+
+def test_varlen16_full_size_sampled():
+    lens = synth.VARLEN_16.lengths()
+    longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
+    _sampled_full_size(synth.VARLEN_16, [(longest, 0), (shortest, 31), (3, 7)])
+
+
+def _custom(name, wid, lens, H=1, d=128, dtype="bf16", init_state=False, log_alpha=None):
+    w = PrefillWorkload(name, wid, H, d, dtype, tuple(lens), len(lens), init_state=init_state)
+    inp = synth.prefill_inputs(w)
+    if log_alpha is not None:
+        inp["log_alpha"] = torch.full_like(inp["log_alpha"], log_alpha)
+    return w, inp
+
+
+def test_strong_decay_near_the_supported_limit():
+    # -1.2 per token: a full chunk sums to -76.8, inside the supported range
+    w, inp = _custom("strong_decay", 110, [150], H=2, log_alpha=-1.2)
+    o, fs = gpu_prefill(inp)
+    o_ref, fs_ref = oracle_prefill(inp)
+    assert_parity(o, fs, o_ref, fs_ref, "bf16", "strong decay")
+
+
+def test_no_decay_and_zero_beta():
+    w, inp = _custom("no_decay", 111, [130], H=2, log_alpha=0.0, init_state=True)
+    inp["beta"][:] = 0.0
+    o, fs = gpu_prefill(inp)
+    o_ref, fs_ref = oracle_prefill(inp)
+    assert_parity(o, fs, o_ref, fs_ref, "bf16", "alpha=1, beta=0")
+    # beta = 0 and alpha = 1 leave the initial state untouched
+    np.testing.assert_allclose(fs, synth.to_f64(inp["init_state"]), rtol=0, atol=0)
+
+
+def test_decay_outside_range_is_reported_not_faulted():
+    w, inp = _custom("decay_out_of_range", 112, [100], log_alpha=-2.0)
+    d = to_device(inp)
+    ws = kda.workspace_for(1, 100, 1, 128, kda.KDA_DTYPE_BF16, "cuda")
+    kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], workspace=ws)
+    st = kda.kda_read_device_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == kda.KDA_ERR_DECAY_RANGE
+    # the record is cleared by the read
+    assert kda.kda_read_device_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+
+
+def test_malformed_cu_seqlens_is_reported_not_faulted():
+    w, inp = _custom("bad_cu", 113, [100, 50, 50], H=1)
+    d = to_device(inp)
+    d["cu_seqlens"] = torch.tensor([0, 100, 60, 200], dtype=torch.int32, device="cuda")
+    ws = kda.workspace_for(3, 200, 1, 128, kda.KDA_DTYPE_BF16, "cuda")
+    kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], workspace=ws)
+    st = kda.kda_read_device_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    assert st == kda.KDA_ERR_INVALID_ARG
+
+
+def test_final_state_may_alias_initial_state():
+    w, inp = _custom("inplace", 114, [90, 200], H=2, init_state=True)
+    o1, fs1 = gpu_prefill(inp)
+    o2, fs2 = gpu_prefill(inp, init_state_inplace=True)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(fs1, fs2)
+
+
+def test_zero_tokens_keeps_initial_states():
+    w, inp = _custom("empty", 115, [0, 0], H=2, init_state=True)
+    o, fs = gpu_prefill(inp)
+    assert o.size == 0
+    np.testing.assert_array_equal(fs, synth.to_f64(inp["init_state"]))
+
+
+def test_split_prefill_and_decode_continue_the_sequence():
+    w, inp = _custom("split", 116, [260], H=2, init_state=True)
+    o_all, fs_all = gpu_prefill(inp)
+    d = to_device(inp)
+    a, b = 130, 255
+    sl = lambda t, i, j: t[i:j].contiguous()
+    o1, f1 = kda.prefill(sl(d["q"], 0, a), sl(d["k"], 0, a), sl(d["v"], 0, a),
+                         sl(d["log_alpha"], 0, a), sl(d["beta"], 0, a), init_state=d["init_state"])
+    o2, f2 = kda.prefill(sl(d["q"], a, b), sl(d["k"], a, b), sl(d["v"], a, b),
+                         sl(d["log_alpha"], a, b), sl(d["beta"], a, b), init_state=f1)
+    state = f2.clone().view(1, 2, 128, 128)
+    outs = []
+    for t in range(b, 260):
+        x = lambda n: d[n][t:t + 1].contiguous()
+        outs.append(kda.decode_step(x("q"), x("k"), x("v"), x("log_alpha"), x("beta"), state))
+    torch.cuda.synchronize()
+    o_split = np.concatenate([synth.to_f64(o1), synth.to_f64(o2)] +
+                             [synth.to_f64(x) for x in outs])
+    assert np.abs(o_split - o_all).max() < 2e-2
+    assert relF(synth.to_f64(state), fs_all) < 1e-3
+
+
+def test_repeated_runs_are_bitwise_identical():
+    w, inp = _custom("determinism", 117, [300, 77], H=3, init_state=True)
+    o1, fs1 = gpu_prefill(inp)
+    o2, fs2 = gpu_prefill(inp)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(fs1, fs2)
