@@ -144,184 +144,229 @@ class ClockSampler:
                 "samples": len(sm)}
 
 
-# ----------------------------------------------------------------------------- GPU arm
-def run_gpu(args):
+def max_over_ranks(v, dist=None, device=None):
+    """Slowest replica's time: the job's time under weak scaling."""
+    if dist is None:
+        return v
     import torch
-    from kda_gated_delta_04_gb300 import kda, synth
+    t = torch.tensor([float(v)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
 
-    rank, world, local_rank = _env_rank()
-    torch.cuda.set_device(local_rank)
-    dev = torch.device("cuda", local_rank)
-    dist = None
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
 
-    w = synth.PREFILL_4K
-    seed = args.seed + rank  # each replica runs its own independent units
-    inp = synth.prefill_inputs(w, seed=seed)
-    T, H, d = inp["q"].shape
-    x = {k: inp[k].to(dev) for k in ("q", "k", "v", "log_alpha", "beta", "cu_seqlens")}
-    o = torch.empty((T, H, d), dtype=torch.bfloat16, device=dev)
-    fs = torch.empty((1, H, d, d), dtype=torch.float32, device=dev)
-    ws = kda.workspace_for(1, T, H, d, kda.KDA_DTYPE_BF16, dev)
-    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
-    stream = torch.cuda.current_stream(dev)
-    sh = stream.cuda_stream
-    launches_per_prefill = 2  # schedule/validation kernel + chunk kernel
+def aggregate_rate(units_per_step_per_rank, world, steps, total_ms):
+    """Whole-job throughput: units all ranks processed / the max-over-ranks time."""
+    return units_per_step_per_rank * world * steps / (total_ms / 1e3)
 
-    def prefill_call():
+
+# ----------------------------------------------------------------------------- GPU arm
+class _Gpu:
+    """Device buffers and the raw C-ABI calls of one replica."""
+
+    def __init__(self, args, rank, local_rank):
+        import torch
+        from kda_gated_delta_04_gb300 import kda, synth
+        self.torch, self.kda, self.synth = torch, kda, synth
+        self.dev = torch.device("cuda", local_rank)
+        self.stream = torch.cuda.current_stream(self.dev)
+        self.sh = self.stream.cuda_stream
+        self.seed = args.seed + rank  # each replica runs its own independent units
+        self.flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=self.dev)
+
+    def event(self):
+        return self.torch.cuda.Event(enable_timing=True)
+
+    # ------------------------------------------------------------------ prefill
+    def setup_prefill(self):
+        torch, kda = self.torch, self.kda
+        self.w = self.synth.PREFILL_4K
+        self.inp = self.synth.prefill_inputs(self.w, seed=self.seed)
+        self.T, self.H, self.d = self.inp["q"].shape
+        self.x = {k: self.inp[k].to(self.dev)
+                  for k in ("q", "k", "v", "log_alpha", "beta", "cu_seqlens")}
+        self.o = torch.empty((self.T, self.H, self.d), dtype=torch.bfloat16, device=self.dev)
+        self.fs = torch.empty((1, self.H, self.d, self.d), dtype=torch.float32, device=self.dev)
+        self.ws = kda.workspace_for(1, self.T, self.H, self.d, kda.KDA_DTYPE_BF16, self.dev)
+
+    def prefill_call(self):
+        kda, x = self.kda, self.x
         st = kda.kda_prefill(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
                              x["log_alpha"].data_ptr(), x["beta"].data_ptr(),
-                             x["cu_seqlens"].data_ptr(), 1, T, H, d, d, kda.KDA_DTYPE_BF16, None,
-                             o.data_ptr(), fs.data_ptr(), ws.data_ptr(), ws.numel(), sh)
+                             x["cu_seqlens"].data_ptr(), 1, self.T, self.H, self.d, self.d,
+                             kda.KDA_DTYPE_BF16, None, self.o.data_ptr(), self.fs.data_ptr(),
+                             self.ws.data_ptr(), self.ws.numel(), self.sh)
         if st != kda.KDA_OK:
             raise kda.KdaError(st, "kda_prefill")
 
-    peaks = measured_peaks()
-    clocks = ClockSampler(local_rank)
-    with clocks:
-        # ------------------------------------------------ prefill, inputs resident in HBM
-        for _ in range(args.warmup):
-            flush.zero_()
-            prefill_call()
+    def time_prefill(self, steps, warmup, barrier):
+        """Per-step event times (ms) of kda_prefill, L2 flushed (untimed) before each step."""
+        torch = self.torch
+        for _ in range(warmup):
+            self.flush.zero_()
+            self.prefill_call()
         torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
+        barrier()
         torch.cuda.synchronize()
-        ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-              for _ in range(args.steps)]
+        ev = [(self.event(), self.event()) for _ in range(steps)]
         for a, b in ev:
-            flush.zero_()  # evict L2 between timed steps (not timed)
-            a.record(stream)
-            prefill_call()
-            b.record(stream)
+            self.flush.zero_()
+            a.record(self.stream)
+            self.prefill_call()
+            b.record(self.stream)
         torch.cuda.synchronize()
-        step_ms = [a.elapsed_time(b) for a, b in ev]
-        if dist:
-            dist.barrier()
-        total_ms = sum(step_ms)
-        st = kda.kda_read_device_status(ws.data_ptr(), sh)
-        if st != kda.KDA_OK:
-            raise kda.KdaError(st, "kda_prefill (device status)")
+        barrier()
+        st = self.kda.kda_read_device_status(self.ws.data_ptr(), self.sh)
+        if st != self.kda.KDA_OK:
+            raise self.kda.KdaError(st, "kda_prefill (device status)")
+        return [a.elapsed_time(b) for a, b in ev]
 
-        # ------------------------------------------------ prefill end to end from host
-        pin = {k: inp[k].pin_memory() for k in ("q", "k", "v", "log_alpha", "beta")}
-        o_host = torch.empty(o.shape, dtype=o.dtype).pin_memory()
-        fs_host = torch.empty(fs.shape, dtype=fs.dtype).pin_memory()
-        h2d = sum(t.numel() * t.element_size() for t in pin.values())
-        d2h = o_host.numel() * o_host.element_size() + fs_host.numel() * fs_host.element_size()
+    def time_prefill_e2e(self, steps, warmup):
+        """Host-to-host: pinned inputs -> device, kda_prefill, o and final state -> host."""
+        torch = self.torch
+        pin = {k: self.inp[k].pin_memory() for k in ("q", "k", "v", "log_alpha", "beta")}
+        o_host = torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory()
+        fs_host = torch.empty(self.fs.shape, dtype=self.fs.dtype).pin_memory()
+        self.h2d = sum(t.numel() * t.element_size() for t in pin.values())
+        self.d2h = (o_host.numel() * o_host.element_size() +
+                    fs_host.numel() * fs_host.element_size())
 
-        def e2e_step():
+        def step():
             for k_, t in pin.items():
-                x[k_].copy_(t, non_blocking=True)
-            prefill_call()
-            o_host.copy_(o, non_blocking=True)
-            fs_host.copy_(fs, non_blocking=True)
+                self.x[k_].copy_(t, non_blocking=True)
+            self.prefill_call()
+            o_host.copy_(self.o, non_blocking=True)
+            fs_host.copy_(self.fs, non_blocking=True)
 
-        for _ in range(max(1, args.warmup)):
-            e2e_step()
+        for _ in range(warmup):
+            step()
         torch.cuda.synchronize()
-        e_ms = []
-        for _ in range(args.steps):
-            flush.zero_()
-            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            a.record(stream)
-            e2e_step()
-            b.record(stream)
+        out = []
+        for _ in range(steps):
+            self.flush.zero_()
+            a, b = self.event(), self.event()
+            a.record(self.stream)
+            step()
+            b.record(self.stream)
             b.synchronize()
-            e_ms.append(a.elapsed_time(b))
+            out.append(a.elapsed_time(b))
+        return out
 
-        # ------------------------------------------------ decode: 1000 in-place steps
-        dw = synth.DECODE_256
-        ring = [{k: t.to(dev) for k, t in synth.decode_inputs(dw, s, seed=seed).items()}
-                for s in range(16)]
-        state = synth.decode_state(dw, seed=seed).to(dev)
-        o_dec = torch.empty((dw.batch, dw.num_heads, dw.d), dtype=torch.bfloat16, device=dev)
+    # ------------------------------------------------------------------ decode
+    def setup_decode(self):
+        torch, synth = self.torch, self.synth
+        self.dw = dw = synth.DECODE_256
+        self.ring = [{k: t.to(self.dev) for k, t in synth.decode_inputs(dw, s, seed=self.seed).items()}
+                     for s in range(16)]
+        self.state = synth.decode_state(dw, seed=self.seed).to(self.dev)
+        self.o_dec = torch.empty((dw.batch, dw.num_heads, dw.d), dtype=torch.bfloat16,
+                                 device=self.dev)
 
-        def decode_call(s):
-            r = ring[s % len(ring)]
-            st = kda.kda_decode_step(r["q"].data_ptr(), r["k"].data_ptr(), r["v"].data_ptr(),
-                                     r["log_alpha"].data_ptr(), r["beta"].data_ptr(), dw.batch,
-                                     dw.num_heads, dw.d, dw.d, kda.KDA_DTYPE_BF16,
-                                     state.data_ptr(), o_dec.data_ptr(), sh)
-            if st != kda.KDA_OK:
-                raise kda.KdaError(st, "kda_decode_step")
+    def decode_call(self, s):
+        kda, dw, r = self.kda, self.dw, self.ring[s % len(self.ring)]
+        st = kda.kda_decode_step(r["q"].data_ptr(), r["k"].data_ptr(), r["v"].data_ptr(),
+                                 r["log_alpha"].data_ptr(), r["beta"].data_ptr(), dw.batch,
+                                 dw.num_heads, dw.d, dw.d, kda.KDA_DTYPE_BF16,
+                                 self.state.data_ptr(), self.o_dec.data_ptr(), self.sh)
+        if st != kda.KDA_OK:
+            raise kda.KdaError(st, "kda_decode_step")
 
-        for s in range(max(3, args.warmup)):
-            decode_call(s)
+    def time_decode(self, steps, warmup, barrier):
+        """Event time (ms) of `steps` back-to-back in-place decode steps (the 537 MB state
+        is larger than L2, so no flush is needed between steps)."""
+        torch = self.torch
+        for s in range(warmup):
+            self.decode_call(s)
         torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record(stream)
-        for s in range(dw.steps):
-            decode_call(s)
-        b.record(stream)
+        barrier()
+        a, b = self.event(), self.event()
+        a.record(self.stream)
+        for s in range(steps):
+            self.decode_call(s)
+        b.record(self.stream)
         torch.cuda.synchronize()
-        if dist:
-            dist.barrier()
-        dec_ms = a.elapsed_time(b)
+        barrier()
+        return a.elapsed_time(b)
 
-    def max_over_ranks(v):
-        if not dist:
-            return v
-        t = torch.tensor([v], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
 
-    total_ms = max_over_ranks(total_ms)
-    e2e_total = max_over_ranks(sum(e_ms))
-    dec_ms = max_over_ranks(dec_ms)
-    mean_step_ms = total_ms / args.steps
-    tokens = T * world * args.steps
-    value = tokens / (total_ms / 1e3)
-    alg_bytes = prefill_algorithmic_bytes(T, H, d, 1, 2, False)
-    achieved = alg_bytes / (mean_step_ms / 1e3) / 1e9
-    dec_bytes = decode_algorithmic_bytes(dw.batch, dw.num_heads, dw.d, 2)
-    dec_step_ms = dec_ms / dw.steps
-    dec_achieved = dec_bytes / (dec_step_ms / 1e3) / 1e9
-    line = {
-        "metric": METRIC,
-        "value": value,
-        "unit": "tokens/s",
-        "n_gpus": world,
-        "steps": args.steps,
-        "warmup": args.warmup,
-        "ms_per_step": mean_step_ms,
-        "higher_is_better": True,
-        "scaling": "weak",
-        "vs_baseline": None,
-        "dtype": "bf16",
-        "data": "synthetic (seeded counter-based generator; no dataset)",
-        "config": {"workload": w.name, "batch": 1, "num_heads": H, "seq_len": T, "d_k": d,
-                   "d_v": d, "chunk": 64, "io_dtype": "bf16", "gate_state_dtype": "f32",
-                   "l2": "flushed between timed steps (256 MiB write, untimed)",
-                   "parallelism": f"replicas x{world} (independent units, no collective)"},
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                     "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": profiled_traffic("prefill_4k"),
-                     "peak_source": peaks["source"],
-                     "algorithmic_bytes_per_launch": alg_bytes,
-                     "tensor_frac_of_bf16_peak": prefill_flops(T, H, d) / (mean_step_ms / 1e3)
-                     / 1e12 / peaks["bf16_tflops"],
-                     "note": "duration from CUDA events around kda_prefill (its schedule kernel "
-                             "and the chunk kernel)"},
-        "e2e": {"value": T * world * args.steps / (e2e_total / 1e3), "unit": "tokens/s",
-                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-        "gpu_launches": launches_per_prefill * args.steps,
-        "clocks": clocks.summary(),
-        "decode": {"metric": "KDA decode steps/s", "workload": dw.name,
-                   "value": dw.steps * world / (dec_ms / 1e3), "unit": "steps/s",
-                   "ms_per_step": dec_step_ms, "steps": dw.steps, "gpu_launches": dw.steps,
-                   "tokens_per_s": dw.steps * dw.batch * world / (dec_ms / 1e3),
-                   "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"],
-                                "unit": "GB/s", "frac": dec_achieved / peaks["hbm_gbs"],
-                                "traffic": profiled_traffic("decode_256"),
-                                "algorithmic_bytes_per_launch": dec_bytes}},
-    }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        line["cpu_baseline"] = cpu_baseline(w, inp)
+def run_gpu(args):
+    import torch
+
+    rank, world, local_rank = _env_rank()
+    torch.cuda.set_device(local_rank)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    barrier = (lambda: dist.barrier()) if dist else (lambda: None)
+
+    def reduce_max(v):
+        return max_over_ranks(v, dist, torch.device("cuda", local_rank))
+
+    g = _Gpu(args, rank, local_rank)
+    peaks = measured_peaks()
+    do_prefill = args.only in ("all", "prefill")
+    do_decode = args.only in ("all", "decode")
+    if do_prefill:
+        g.setup_prefill()
+    if do_decode:
+        g.setup_decode()
+    clocks = ClockSampler(local_rank)
+    line = {"metric": METRIC, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic (seeded counter-based generator; no dataset)"}
+    with clocks:
+        if do_prefill:
+            step_ms = g.time_prefill(args.steps, args.warmup, barrier)
+            e2e_ms = g.time_prefill_e2e(args.steps, args.warmup)
+        if do_decode:
+            dec_ms = g.time_decode(g.dw.steps, max(3, args.warmup), barrier)
+    if do_prefill:
+        total_ms = reduce_max(sum(step_ms))
+        e2e_total = reduce_max(sum(e2e_ms))
+        mean_step_ms = total_ms / args.steps
+        T, H, d = g.T, g.H, g.d
+        alg_bytes = prefill_algorithmic_bytes(T, H, d, 1, 2, False)
+        achieved = alg_bytes / (mean_step_ms / 1e3) / 1e9
+        line.update({
+            "value": aggregate_rate(T, world, args.steps, total_ms),
+            "ms_per_step": mean_step_ms,
+            "config": {"workload": g.w.name, "batch": 1, "num_heads": H, "seq_len": T,
+                       "d_k": d, "d_v": d, "chunk": 64, "io_dtype": "bf16",
+                       "gate_state_dtype": "f32",
+                       "l2": "flushed between timed steps (256 MiB write, untimed)",
+                       "parallelism": f"replicas x{world} (independent units, no collective)"},
+            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                         "traffic": profiled_traffic("prefill_4k"),
+                         "peak_source": peaks["source"],
+                         "algorithmic_bytes_per_launch": alg_bytes,
+                         "tensor_frac_of_bf16_peak": prefill_flops(T, H, d) /
+                         (mean_step_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
+                         "note": "duration from CUDA events around kda_prefill (its schedule "
+                                 "kernel and the chunk kernel)"},
+            "e2e": {"value": aggregate_rate(T, world, args.steps, e2e_total), "unit": "tokens/s",
+                    "h2d_bytes_per_step": g.h2d, "d2h_bytes_per_step": g.d2h},
+            "gpu_launches": 2 * args.steps,  # schedule/validation kernel + chunk kernel
+        })
+    line["clocks"] = clocks.summary()
+    if do_decode:
+        dw = g.dw
+        dec_ms = reduce_max(dec_ms)
+        dec_bytes = decode_algorithmic_bytes(dw.batch, dw.num_heads, dw.d, 2)
+        dec_step_ms = dec_ms / dw.steps
+        dec_achieved = dec_bytes / (dec_step_ms / 1e3) / 1e9
+        line["decode"] = {
+            "metric": "KDA decode steps/s", "workload": dw.name,
+            "value": aggregate_rate(1, world, dw.steps, dec_ms), "unit": "steps/s",
+            "ms_per_step": dec_step_ms, "steps": dw.steps, "gpu_launches": dw.steps,
+            "tokens_per_s": dw.steps * dw.batch * world / (dec_ms / 1e3),
+            "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": dec_achieved / peaks["hbm_gbs"],
+                         "traffic": profiled_traffic("decode_256"),
+                         "algorithmic_bytes_per_launch": dec_bytes}}
+    if do_prefill and rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(g.w, g.inp)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if dist:
@@ -413,6 +458,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+                    help="profiling aid: run only one part (the printed line is then partial)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
