@@ -130,6 +130,48 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const 
  */
 kda_status_t kda_read_device_status(void *workspace, void *stream);
 
+/*
+ * kda_prefill_no_alloc -- kda_prefill without a caller-provided workspace.
+ * The pages have no counterpart to this entry point; it is a library facility.
+ *
+ * Who it is for: callers that cannot allocate device memory when they call the
+ * prefill, so cannot hand kda_prefill its workspace.  Examples are a serving
+ * runtime that carves all GPU memory out of a pool sized at start-up and
+ * forbids allocations afterwards, and a latency-critical path that must not
+ * call cudaMalloc (which may synchronise the whole device).
+ *
+ * What it does: exactly what kda_prefill does, with the same arguments, checks,
+ * kernels and results, except that the workspace is a fixed device array built
+ * into libkda.  That array is KDA_NO_ALLOC_SCRATCH_BYTES bytes; every GPU that
+ * loads the library holds it until the process exits.  The call allocates
+ * nothing: no cudaMalloc, cudaFree or allocating library routine.
+ *
+ *  num_seqs      at most KDA_NO_ALLOC_MAX_SEQS; larger values return
+ *                KDA_ERR_UNSUPPORTED and enqueue nothing (use kda_prefill).
+ *  device_errors optional DEVICE pointer to one uint32; when not NULL it receives
+ *                this call's device-side error bits (0 = none, otherwise an OR of
+ *                KDA_DEVICE_ERR_*), copied on `stream` after the prefill.
+ *
+ * The first call on each device looks up the array's device address (with that
+ * device current) and caches it; make that first call before any stream capture
+ * begins.  All calls share the one array and each call reinitialises it (error
+ * word and schedule) before use, so calls ordered on one stream are fine, but
+ * calls whose work can overlap on the GPU (unordered streams) race on the array
+ * and must be serialised by the caller.
+ */
+#define KDA_NO_ALLOC_MAX_SEQS 4096
+#define KDA_NO_ALLOC_SCRATCH_BYTES (512 + 4 * KDA_NO_ALLOC_MAX_SEQS) /* 16,896 */
+#define KDA_DEVICE_ERR_SEQLENS 1u /* cu_seqlens is not a prefix sum ending at total_tokens */
+#define KDA_DEVICE_ERR_TIMEOUT 2u /* a bounded device-side wait expired                   */
+#define KDA_DEVICE_ERR_DECAY 4u   /* a chunk's cumulative log-decay left the supported range */
+kda_status_t kda_prefill_no_alloc(const void *q, const void *k, const void *v,
+                                  const float *log_alpha, const float *beta,
+                                  const int32_t *cu_seqlens, int32_t num_seqs,
+                                  int64_t total_tokens, int32_t num_heads, int32_t d_k,
+                                  int32_t d_v, kda_dtype_t dtype, const float *init_state,
+                                  void *o, float *final_state, uint32_t *device_errors,
+                                  void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *kda_status_string(kda_status_t status);
 

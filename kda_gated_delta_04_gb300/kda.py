@@ -39,6 +39,7 @@ EXPORTS = {
     "kda_decode_step": (_c.c_int, _DECODE_ARGS),
     "kda_read_device_status": (_c.c_int, [_VP, _VP]),
     "kda_status_string": (_c.c_char_p, [_c.c_int]),
+    "kda_prefill_no_alloc": (_c.c_int, _PREFILL_ARGS[:15] + [_VP, _VP]),
 }
 
 
@@ -80,6 +81,15 @@ def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, nu
 def kda_decode_step(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype, state, o, stream):
     return lib().kda_decode_step(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype,
                                  state, o, stream)
+
+
+def kda_prefill_no_alloc(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads,
+                         d_k, d_v, dtype, init_state, o, final_state, device_errors, stream):
+    """kda_prefill with its workspace in a fixed array inside libkda, for callers that
+    cannot allocate device memory at call time (see include/kda.h)."""
+    return lib().kda_prefill_no_alloc(q, k, v, log_alpha, beta, cu_seqlens, num_seqs,
+                                      total_tokens, num_heads, d_k, d_v, dtype, init_state, o,
+                                      final_state, device_errors, stream)
 
 
 def kda_read_device_status(workspace, stream):
