@@ -70,25 +70,24 @@ def decode_algorithmic_bytes(B, H, d, io_bytes):
     return B * H * (2 * d * d * 4 + 3 * d * io_bytes + d * 4 + 4 + d * io_bytes)
 
 
-def source_sha():
+def source_sha(files):
+    """Hash of the kernel sources a profile was taken on (paths relative to the repo)."""
     h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "kda_gated_delta_04_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            h.update(open(os.path.join(csrc, f), "rb").read())
+    for f in sorted(files):
+        h.update(open(os.path.join(ROOT, f), "rb").read())
     return h.hexdigest()[:16]
 
 
 def profiled_traffic(kernel_key):
-    """DRAM bytes per launch from the committed ncu summary, if it was taken on the
-    current kernel sources; None otherwise."""
+    """DRAM bytes per launch from the committed ncu summary (profiles/traffic.json), if it
+    was taken on the kernel's current sources; None otherwise."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
     with open(p) as f:
         d = json.load(f)
     e = d.get(kernel_key)
-    if not e or e.get("source_sha") != source_sha():
+    if not e or e.get("source_sha") != source_sha(e.get("sources", [])):
         return None
     return e.get("dram_bytes_per_launch")
 
