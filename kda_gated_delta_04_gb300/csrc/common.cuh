@@ -49,6 +49,8 @@ struct DecodeProblem {
 // Launchers (each returns the launch error, cudaSuccess when enqueued).
 cudaError_t launch_prefill_prep(const PrefillProblem &p);
 cudaError_t launch_prefill_simt(const PrefillProblem &p);
+bool prefill_tc_supported(const PrefillProblem &p);  // bf16, d = 128, 0 < total_tokens < 2^31
+cudaError_t launch_prefill_tc(const PrefillProblem &p);
 cudaError_t launch_decode(const DecodeProblem &p);
 
 // ---------------------------------------------------------------- device helpers

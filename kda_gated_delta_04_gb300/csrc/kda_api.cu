@@ -91,7 +91,11 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, const floa
     p.stream = static_cast<cudaStream_t>(stream);
 
     if (kda::launch_prefill_prep(p) != cudaSuccess) return KDA_ERR_CUDA;
-    if (kda::launch_prefill_simt(p) != cudaSuccess) return KDA_ERR_CUDA;
+    // bf16 at d = 128 runs on the tensor cores; fp32 I/O (the exact path) and d = 64 run
+    // the CUDA-core chunk kernel.
+    const cudaError_t err = kda::prefill_tc_supported(p) ? kda::launch_prefill_tc(p)
+                                                         : kda::launch_prefill_simt(p);
+    if (err != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }
 

@@ -1,0 +1,554 @@
+// prefill_tc.cu -- chunkwise KDA prefill on the 5th-generation tensor cores
+// (bf16 q/k/v, d_k = d_v = 128, fp32 state), sm_103a.
+//
+// One CTA owns one (sequence, head, 32-column value slice) and walks the
+// sequence's 64-token chunks in order (parallel inside a chunk, serial across
+// chunks: "From 124M to 2.8T", chapter 3; WY representation + UT transform:
+// "K3 attention, three-piece set", KDA engineering details).  Per chunk, with
+// g the in-chunk cumulative log-decay, Kg = k e^g, Ki = k e^-g, Qg = q e^g / sqrt(d):
+//
+//   TMA      q, k, log_alpha [64 x 128] and v [64 x 32] -> shared memory
+//   prep     g, Kg, Qg, Ki (bf16 and tf32 copies), V^T (tf32)             (a1, a2)
+//   G1 bf16  D1 = [Kg ; Qg] Ki^T   -> A = strict-lower(beta . D1[0:64]),
+//                                     Aqk = lower(D1[64:128])              (a3)
+//   solve    T' = (I + A)^-1 diag(beta), blocked 16 x 16 in shared memory (a4)
+//   GW bf16  W^T = Kg^T T'^T                                               (a5)
+//   GU tf32  D3  = [T' ; 0] V          (U~, the value part of the WY form)  (a5)
+//   G3 bf16  D3 += [-W ; Qg] S         rows 0-63: u, rows 64-127: Qg S      (a6)
+//   G4 bf16  D3 += [. ; Aqk] u         rows 64-127: o                       (a6)
+//   G5 tf32  D5  = Ki^T u
+//   state    S  <- e^{g_last} (S + D5)  (Kd = e^{g_last} Ki, so this is
+//            Diag(e^{g_last}) S + Kd^T u)                                   (a7)
+//
+// Precision: the products that produce u and the state (T' V, Ki^T u) take
+// tf32 operands; the k-k / q-k matrices, W S and Aqk u take bf16 operands;
+// all accumulate in fp32 in tensor memory and the state stays fp32 in registers.
+//
+// Every operand lives in shared memory in the K-major 128-byte-swizzled layout
+// the MMA descriptors expect; accumulators live in tensor memory (256 columns).
+// Every mbarrier wait is bounded by wall-clock time; on expiry the CTA records
+// KDA_DEVICE timeout in the workspace word, drains its own copies and MMAs
+// (bounded again), frees its tensor memory and returns.
+#include <cuda.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace kda {
+namespace {
+
+using namespace ptx;
+
+constexpr int kD = 128, kDV = 32, kC = 64, kTcThreads = 128;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
+
+// Dynamic shared memory map (byte offsets from a 1024-byte aligned base).
+constexpr uint32_t IN_Q = 0;        // q   [64][128] bf16 (TMA box, row-major)
+constexpr uint32_t IN_K = 16384;    // k   [64][128] bf16
+constexpr uint32_t IN_LA = 32768;   // log_alpha [64][128] fp32
+constexpr uint32_t IN_V = 65536;    // v slice [64][32] bf16
+constexpr uint32_t O1 = 69632;      // [Kg ; Qg] then [-W ; Qg]: bf16, 128 rows x K 128
+constexpr uint32_t O2 = 102400;     // Ki: bf16, 64 rows x K 128
+constexpr uint32_t O3 = 118784;     // Ki^T: tf32, 128 rows (i) x K 64 (r)
+constexpr uint32_t O4 = 151552;     // T': bf16, 64 rows x K 64
+constexpr uint32_t O8 = 159744;     // Aqk: bf16, 64 rows x K 64 (rows 64-127 of [T' ; Aqk])
+constexpr uint32_t O5 = 167936;     // [T' ; 0]: tf32, 128 rows x K 64
+constexpr uint32_t O6 = 200704;     // V^T: tf32, 32 rows (j) x K 64 (s)
+constexpr uint32_t O7 = 208896;     // S^T: bf16, 32 rows (j) x K 128 (i)
+constexpr uint32_t O9 = 217088;     // u^T: bf16, 32 rows (j) x K 64 (r)
+constexpr uint32_t O10 = 221184;    // u^T: tf32, 32 rows (j) x K 64 (r)
+constexpr uint32_t kSmemUsed = 229376;
+constexpr uint32_t kSmemDyn = kSmemUsed + 1024;  // slack to align the base to 1024 bytes
+// Solve scratch inside the input area (idle between the prep step and the next TMA).
+constexpr int LDA = kC + 1;
+constexpr uint32_t SOLVE_A = 0, SOLVE_T = 16640, SOLVE_X = 33280;  // fp32 [64][65], [64][65], [3][16][17]
+constexpr uint32_t kTxBytes = 16384 + 16384 + 32768 + 4096;
+static_assert(O8 == O4 + 8192, "[T' ; Aqk] must be one 128-row operand");
+static_assert(SOLVE_X + 3 * 16 * 17 * 4 <= O1, "solve scratch must fit in the input area");
+
+// Tensor-memory columns (one allocation of 256).
+constexpr uint32_t TM_D1 = 0, TM_DW = 64, TM_D3 = 128, TM_D5 = 160, kTmemCols = 256;
+
+constexpr uint32_t IDESC_G1 = idesc_bf16(128, 64, false, false);
+constexpr uint32_t IDESC_GW = idesc_bf16(128, 64, true, false);
+constexpr uint32_t IDESC_GU = idesc_tf32(128, 32, false, false);
+constexpr uint32_t IDESC_G3 = idesc_bf16(128, 32, false, false);
+constexpr uint32_t IDESC_G5 = idesc_tf32(128, 32, false, false);
+
+// Byte offset of element (row, col) of a K-major, 128-byte-swizzled operand
+// with `rows` rows per 64-element (bf16) or 32-element (tf32) column panel.
+__device__ __forceinline__ uint32_t km16(int row, int col, int rows)
+{
+    return (uint32_t)((col >> 6) * rows * 128 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
+                      ((col & 7) << 1));
+}
+__device__ __forceinline__ uint32_t km32(int row, int col, int rows)
+{
+    return (uint32_t)((col >> 5) * rows * 128 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4) +
+                      ((col & 3) << 2));
+}
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t addr) { return sdesc(addr, 16, 1024, kSw128B); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float bf16_at(const unsigned char *p)
+{
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
+}
+
+__device__ __forceinline__ void store_bf16(unsigned char *p, float x)
+{
+    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ void issue_chunk_loads(unsigned char *sm, const CUtensorMap *tq,
+                                                  const CUtensorMap *tk, const CUtensorMap *tla,
+                                                  const CUtensorMap *tv, uint64_t *bar, int h,
+                                                  int j0, int row)
+{
+    mbar_arrive_expect_tx(bar, kTxBytes);
+    tma_load_3d(sm + IN_Q, tq, bar, 0, h, row);
+    tma_load_3d(sm + IN_K, tk, bar, 0, h, row);
+    tma_load_3d(sm + IN_LA, tla, bar, 0, h, row);
+    tma_load_3d(sm + IN_V, tv, bar, j0, h, row);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                  const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_v,
+                  const float *__restrict__ beta, const int32_t *__restrict__ cu, int64_t total,
+                  int H, const float *init_state, __nv_bfloat16 *__restrict__ o,
+                  float *final_state, uint32_t *status, const int32_t *__restrict__ order)
+{
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bar_tma, bar_mma;
+    __shared__ uint32_t tmem_holder;
+    __shared__ float s_beta[kC];
+
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const int j0 = blockIdx.x * kDV, h = blockIdx.y, n = order[blockIdx.z];
+    int64_t t0, t1;
+    seq_range(cu, n, total, t0, t1);
+    const int nchunks = (int)((t1 - t0 + kC - 1) / kC);
+
+    if (tid == 0) {
+        mbar_init(&bar_tma, 1);
+        mbar_init(&bar_mma, 1);
+        fence_mbar_init();
+        prefetch_tmap(&tm_q);
+        prefetch_tmap(&tm_k);
+        prefetch_tmap(&tm_la);
+        prefetch_tmap(&tm_v);
+    }
+    if (warp == 0) {
+        tmem_alloc(&tmem_holder, kTmemCols);
+        tmem_relinquish();
+    }
+    // rows 64..127 of [T' ; 0] (both 32-column panels) stay zero for the whole kernel
+    for (int e = tid; e < 2 * 2048; e += kTcThreads)
+        *reinterpret_cast<uint32_t *>(sm + O5 + (e >> 11) * 16384 + 8192 + (e & 2047) * 4) = 0u;
+
+    // state row i = tid, columns j0 .. j0+31, fp32 in registers
+    float S[kDV];
+    const size_t st_off = (((size_t)n * H + h) * kD + tid) * kD + j0;
+    if (init_state) {
+#pragma unroll
+        for (int q = 0; q < kDV / 4; ++q) {
+            const float4 x = *reinterpret_cast<const float4 *>(init_state + st_off + 4 * q);
+            S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < kDV; ++j) S[j] = 0.f;
+    }
+#pragma unroll
+    for (int j = 0; j < kDV; ++j) store_bf16(sm + O7 + km16(j, tid, kDV), S[j]);
+
+    fence_proxy_async_smem();
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_holder;
+    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
+    const uint32_t tD1 = tmem + TM_D1 + lane_off, tDW = tmem + TM_DW + lane_off;
+    const uint32_t tD3 = tmem + TM_D3 + lane_off, tD5 = tmem + TM_D5 + lane_off;
+
+    uint32_t ph_tma = 0, ph_mma = 0;
+    bool tma_pending = nchunks > 0, mma_pending = false, timed_out = false, decay_bad = false;
+    if (tid == 0 && nchunks > 0)
+        issue_chunk_loads(sm, &tm_q, &tm_k, &tm_la, &tm_v, &bar_tma, h, j0, (int)t0);
+
+    for (int c = 0; c < nchunks; ++c) {
+        const int64_t c0 = t0 + (int64_t)c * kC;
+        const int len = (t1 - c0) < kC ? (int)(t1 - c0) : kC;
+
+        // ---------------------------------------------------------- inputs landed
+        bool ok = mbar_wait_ns(&bar_tma, ph_tma, kWaitNs);
+        if (__syncthreads_or(!ok)) { timed_out = true; break; }
+        ph_tma ^= 1;
+        tma_pending = false;
+
+        // ---------------------------------------------------------- a1, a2
+        float gamma_c;
+        {
+            const int i = tid;
+            const float scale = rsqrtf((float)kD);
+            float g = 0.f, gmin = 0.f, gmax = 0.f;
+            for (int r4 = 0; r4 < kC; r4 += 4) {
+                float ki4[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int r = r4 + u;
+                    const bool valid = r < len;
+                    const float la = valid ? *reinterpret_cast<const float *>(sm + IN_LA + (r * kD + i) * 4) : 0.f;
+                    g += la;
+                    gmin = fminf(gmin, g);
+                    gmax = fmaxf(gmax, g);
+                    const float qv = valid ? bf16_at(sm + IN_Q + (r * kD + i) * 2) : 0.f;
+                    const float kv = valid ? bf16_at(sm + IN_K + (r * kD + i) * 2) : 0.f;
+                    const float eg = __expf(g), egi = __expf(-g);
+                    store_bf16(sm + O1 + km16(r, i, 128), kv * eg);
+                    store_bf16(sm + O1 + km16(64 + r, i, 128), scale * qv * eg);
+                    const float kgi = kv * egi;
+                    store_bf16(sm + O2 + km16(r, i, 64), kgi);
+                    ki4[u] = to_tf32(kgi);
+                }
+                *reinterpret_cast<float4 *>(sm + O3 + km32(i, r4, 128)) =
+                    make_float4(ki4[0], ki4[1], ki4[2], ki4[3]);
+            }
+            gamma_c = __expf(g);
+            if (gmin < KDA_MIN_CHUNK_LOG_DECAY || gmax > -KDA_MIN_CHUNK_LOG_DECAY) decay_bad = true;
+        }
+        if (tid < kC) s_beta[tid] = tid < len ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
+        for (int e = tid; e < kDV * (kC / 4); e += kTcThreads) {
+            const int j = e % kDV, s4 = (e / kDV) * 4;
+            float x[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                x[u] = (s4 + u) < len ? bf16_at(sm + IN_V + ((s4 + u) * kDV + j) * 2) : 0.f;
+            *reinterpret_cast<float4 *>(sm + O6 + km32(j, s4, kDV)) = make_float4(x[0], x[1], x[2], x[3]);
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+
+        // ---------------------------------------------------------- a3: G1
+        if (tid == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t p = s >> 2, w = (s & 3) * 32;
+                mma_bf16(tmem + TM_D1, kdesc(sb + O1 + p * 16384 + w), kdesc(sb + O2 + p * 8192 + w),
+                         IDESC_G1, s > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        ok = mbar_wait_ns(&bar_mma, ph_mma, kWaitNs);
+        if (__syncthreads_or(!ok)) { timed_out = true; mma_pending = true; break; }
+        ph_mma ^= 1;
+        tc_fence_after_sync();
+
+        float *sA = reinterpret_cast<float *>(sm + SOLVE_A);
+        float *sT = reinterpret_cast<float *>(sm + SOLVE_T);
+        float *sX = reinterpret_cast<float *>(sm + SOLVE_X);
+        if (warp < 2) {  // lanes 0..63: rows of Kg Ki^T -> A
+            const int r = tid;
+            const float br = s_beta[r];
+            for (int cb = 0; cb < kC; cb += 16) {
+                float v[16];
+                tmem_ld16(tD1 + cb, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) sA[r * LDA + cb + u] = (cb + u) < r ? br * v[u] : 0.f;
+            }
+        } else {  // lanes 64..127: rows of Qg Ki^T -> Aqk (bf16)
+            const int r = tid - 64;
+            for (int cb = 0; cb < kC; cb += 16) {
+                float v[16];
+                tmem_ld16(tD1 + cb, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int half = 0; half < 2; ++half) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int s = cb + half * 8 + 2 * q;
+                        pk[q] = pack_bf16x2(s <= r ? v[half * 8 + 2 * q] : 0.f,
+                                            s + 1 <= r ? v[half * 8 + 2 * q + 1] : 0.f);
+                    }
+                    *reinterpret_cast<uint4 *>(sm + O8 + km16(r, cb + half * 8, 64)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+            }
+        }
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // ---------------------------------------------------------- a4: T = (I + A)^-1
+        if (tid < 64) {  // diagonal 16 x 16 blocks, one column per thread
+            const int b = (tid >> 4) * 16, cc = tid & 15;
+            float x[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) acc += sA[(b + r) * LDA + b + m] * x[m];
+                x[r] = r < cc ? 0.f : (r == cc ? 1.f : -acc);
+            }
+#pragma unroll
+            for (int r = 0; r < 16; ++r) sT[(b + r) * LDA + b + cc] = x[r];
+        }
+        __syncthreads();
+        for (int d = 1; d < 4; ++d) {  // off-diagonal blocks, by distance from the diagonal
+            const int nblk = 4 - d;
+            for (int e = tid; e < nblk * 256; e += kTcThreads) {  // X = sum_M A_RM T_MS
+                const int S0 = (e >> 8) * 16, R0 = S0 + d * 16, rr = (e >> 4) & 15, ss = e & 15;
+                float acc = 0.f;
+                for (int m = S0; m < R0; ++m) acc += sA[(R0 + rr) * LDA + m] * sT[m * LDA + S0 + ss];
+                sX[((e >> 8) * 16 + rr) * 17 + ss] = acc;
+            }
+            __syncthreads();
+            for (int e = tid; e < nblk * 256; e += kTcThreads) {  // T_RS = -T_RR X
+                const int S0 = (e >> 8) * 16, R0 = S0 + d * 16, rr = (e >> 4) & 15, ss = e & 15;
+                float acc = 0.f;
+                for (int m = 0; m <= rr; ++m)
+                    acc += sT[(R0 + rr) * LDA + R0 + m] * sX[((e >> 8) * 16 + m) * 17 + ss];
+                sT[(R0 + rr) * LDA + S0 + ss] = -acc;
+            }
+            __syncthreads();
+        }
+        // T' = T diag(beta): bf16 (for W) and tf32 (for U~)
+        for (int e = tid; e < kC * 8; e += kTcThreads) {
+            const int r = e >> 3, s8 = (e & 7) * 8;
+            float t[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int s = s8 + u;
+                t[u] = s <= r ? sT[r * LDA + s] * s_beta[s] : 0.f;
+            }
+            *reinterpret_cast<uint4 *>(sm + O4 + km16(r, s8, 64)) =
+                make_uint4(pack_bf16x2(t[0], t[1]), pack_bf16x2(t[2], t[3]), pack_bf16x2(t[4], t[5]),
+                           pack_bf16x2(t[6], t[7]));
+            *reinterpret_cast<float4 *>(sm + O5 + km32(r, s8, 128)) =
+                make_float4(to_tf32(t[0]), to_tf32(t[1]), to_tf32(t[2]), to_tf32(t[3]));
+            *reinterpret_cast<float4 *>(sm + O5 + km32(r, s8 + 4, 128)) =
+                make_float4(to_tf32(t[4]), to_tf32(t[5]), to_tf32(t[6]), to_tf32(t[7]));
+        }
+        fence_proxy_async_smem();
+        __syncthreads();
+
+        // ---------------------------------------------------------- a5: GW, GU; next inputs
+        if (tid == 0) {
+            if (c + 1 < nchunks)
+                issue_chunk_loads(sm, &tm_q, &tm_k, &tm_la, &tm_v, &bar_tma, h, j0,
+                                  (int)(c0 + kC));
+            tc_fence_after_sync();
+#pragma unroll
+            for (int s = 0; s < 4; ++s)  // W^T = Kg^T T'^T; Kg read MN-major from O1 rows 0-63
+                mma_bf16(tmem + TM_DW, sdesc(sb + O1 + s * 2048, 16384, 1024, kSw128B),
+                         kdesc(sb + O4 + s * 32), IDESC_GW, s > 0);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {  // U~ = [T' ; 0] V  (tf32)
+                const uint32_t p = s >> 2, w = (s & 3) * 32;
+                mma_tf32(tmem + TM_D3, kdesc(sb + O5 + p * 16384 + w), kdesc(sb + O6 + p * 4096 + w),
+                         IDESC_GU, s > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        tma_pending = c + 1 < nchunks;
+        ok = mbar_wait_ns(&bar_mma, ph_mma, kWaitNs);
+        if (__syncthreads_or(!ok)) { timed_out = true; mma_pending = true; break; }
+        ph_mma ^= 1;
+        tc_fence_after_sync();
+
+        {  // -W into rows 0-63 of O1 (Kg is no longer needed)
+            const int i = tid;
+            for (int cb = 0; cb < kC; cb += 16) {
+                float v[16];
+                tmem_ld16(tDW + cb, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) store_bf16(sm + O1 + km16(cb + u, i, 128), -v[u]);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // ---------------------------------------------------------- a6: G3 -> u, Qg S
+        if (tid == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t p = s >> 2, w = (s & 3) * 32;
+                mma_bf16(tmem + TM_D3, kdesc(sb + O1 + p * 16384 + w), kdesc(sb + O7 + p * 4096 + w),
+                         IDESC_G3, 1);
+            }
+            mma_commit(&bar_mma);
+        }
+        ok = mbar_wait_ns(&bar_mma, ph_mma, kWaitNs);
+        if (__syncthreads_or(!ok)) { timed_out = true; mma_pending = true; break; }
+        ph_mma ^= 1;
+        tc_fence_after_sync();
+
+        if (warp < 2) {  // u rows 0..63 -> bf16 and tf32 operands (u^T, K-major)
+            const int r = tid;
+            for (int cb = 0; cb < kDV; cb += 16) {
+                float v[16];
+                tmem_ld16(tD3 + cb, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int u = 0; u < 16; ++u) {
+                    store_bf16(sm + O9 + km16(cb + u, r, kDV), v[u]);
+                    *reinterpret_cast<float *>(sm + O10 + km32(cb + u, r, kDV)) = to_tf32(v[u]);
+                }
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+
+        // ---------------------------------------------------------- a6/a7: G4 -> o, G5
+        if (tid == 0) {
+            tc_fence_after_sync();
+#pragma unroll
+            for (int s = 0; s < 4; ++s)  // rows 64-127 of [T' ; Aqk] are Aqk
+                mma_bf16(tmem + TM_D3, kdesc(sb + O4 + s * 32), kdesc(sb + O9 + s * 32), IDESC_G3, 1);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t p = s >> 2, w = (s & 3) * 32;
+                mma_tf32(tmem + TM_D5, kdesc(sb + O3 + p * 16384 + w), kdesc(sb + O10 + p * 4096 + w),
+                         IDESC_G5, s > 0);
+            }
+            mma_commit(&bar_mma);
+        }
+        ok = mbar_wait_ns(&bar_mma, ph_mma, kWaitNs);
+        if (__syncthreads_or(!ok)) { timed_out = true; mma_pending = true; break; }
+        ph_mma ^= 1;
+        tc_fence_after_sync();
+
+        if (warp >= 2) {  // o rows 0..63 from lanes 64..127
+            const int r = tid - 64;
+            float v[32];
+            tmem_ld16(tD3, *reinterpret_cast<float(*)[16]>(v));
+            tmem_ld16(tD3 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+            tmem_ld_wait();
+            if (r < len) {
+                uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(c0 + r) * H + h) * kD + j0);
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    dst[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
+                                        pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+            }
+        }
+        {  // state rows: S <- gamma_c (S + Ki^T u)
+            float v[32];
+            tmem_ld16(tD5, *reinterpret_cast<float(*)[16]>(v));
+            tmem_ld16(tD5 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+            tmem_ld_wait();
+#pragma unroll
+            for (int j = 0; j < kDV; ++j) {
+                S[j] = gamma_c * (S[j] + v[j]);
+                store_bf16(sm + O7 + km16(j, tid, kDV), S[j]);
+            }
+        }
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        __syncthreads();
+    }
+
+    if (timed_out) {
+        if (tid == 0) atomicOr(status, DEV_ERR_TIMEOUT);
+        // drain our own copies and MMAs (bounded) before releasing shared and tensor memory
+        if (tma_pending) (void)mbar_wait_ns(&bar_tma, ph_tma, kWaitNs);
+        if (mma_pending) (void)mbar_wait_ns(&bar_mma, ph_mma, kWaitNs);
+    } else {
+        float *dst = final_state + st_off;
+#pragma unroll
+        for (int q = 0; q < kDV / 4; ++q)
+            *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
+    }
+    if (decay_bad) atomicOr(status, DEV_ERR_DECAY);
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [T, H, 128] token-major tensor; box = 64 tokens x 1 head x box_x channels.
+bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, int64_t T, int H,
+              uint32_t esz, uint32_t box_x)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)kD * esz, (cuuint64_t)H * kD * esz};
+    const cuuint32_t box[3] = {box_x, 1, (cuuint32_t)kC};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+bool prefill_tc_supported(const PrefillProblem &p)
+{
+    return p.dtype == KDA_DTYPE_BF16 && p.d == kD && p.total_tokens > 0 &&
+           p.total_tokens <= 0x7fffffffll;
+}
+
+cudaError_t launch_prefill_tc(const PrefillProblem &p)
+{
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (configured_device != dev) {
+        err = cudaFuncSetAttribute(prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kSmemDyn);
+        if (err != cudaSuccess) return err;
+        configured_device = dev;
+    }
+    CUtensorMap tq, tk, tla, tv;
+    if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, p.total_tokens, p.num_heads, 2, kD) ||
+        !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, p.total_tokens, p.num_heads, 2, kD) ||
+        !make_map(&tla, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.log_alpha, p.total_tokens, p.num_heads, 4,
+                  kD) ||
+        !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kDV))
+        return cudaErrorInvalidValue;
+    dim3 grid(kD / kDV, p.num_heads, p.num_seqs);
+    prefill_tc_kernel<<<grid, kTcThreads, kSmemDyn, p.stream>>>(
+        tq, tk, tla, tv, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.init_state,
+        static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.status, p.order);
+    return cudaGetLastError();
+}
+
+}  // namespace kda
