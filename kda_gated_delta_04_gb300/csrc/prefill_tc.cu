@@ -11,7 +11,7 @@
 //   prep     g, Kg, Qg, Ki (bf16 and tf32 copies), V^T (tf32)             (a1, a2)
 //   G1 bf16  D1 = [Kg ; Qg] Ki^T   -> A = strict-lower(beta . D1[0:64]),
 //                                     Aqk = lower(D1[64:128])              (a3)
-//   solve    T' = (I + A)^-1 diag(beta), blocked 16 x 16 in shared memory (a4)
+//   solve    T' = (I + A)^-1 diag(beta), recursive doubling over 16 x 16 blocks (a4)
 //   GW bf16  W^T = Kg^T T'^T                                               (a5)
 //   GU tf32  D3  = [T' ; 0] V          (U~, the value part of the WY form)  (a5)
 //   G3 bf16  D3 += [-W ; Qg] S         rows 0-63: u, rows 64-127: Qg S      (a6)
@@ -41,7 +41,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kD = 128, kDV = 32, kC = 64, kTcThreads = 128;
+constexpr int kD = 128, kDV = 32, kC = 64, kTcThreads = 256;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
 
 // Dynamic shared memory map (byte offsets from a 1024-byte aligned base).
@@ -61,12 +61,13 @@ constexpr uint32_t O9 = 217088;     // u^T: bf16, 32 rows (j) x K 64 (r)
 constexpr uint32_t O10 = 221184;    // u^T: tf32, 32 rows (j) x K 64 (r)
 constexpr uint32_t kSmemUsed = 229376;
 constexpr uint32_t kSmemDyn = kSmemUsed + 1024;  // slack to align the base to 1024 bytes
-// Solve scratch inside the input area (idle between the prep step and the next TMA).
-constexpr int LDA = kC + 1;
-constexpr uint32_t SOLVE_A = 0, SOLVE_T = 16640, SOLVE_X = 33280;  // fp32 [64][65], [64][65], [3][16][17]
+// Solve scratch inside the input area (idle between the operand prep and the next TMA).
+constexpr int kLdS = kC + 4;   // row stride (floats) of A and T
+constexpr int kLdX = 32 + 4;   // row stride of the block products X (up to 32 x 32)
+constexpr uint32_t SOLVE_A = 0, SOLVE_T = kC * kLdS * 4, SOLVE_X = 2 * kC * kLdS * 4;
 constexpr uint32_t kTxBytes = 16384 + 16384 + 32768 + 4096;
 static_assert(O8 == O4 + 8192, "[T' ; Aqk] must be one 128-row operand");
-static_assert(SOLVE_X + 3 * 16 * 17 * 4 <= O1, "solve scratch must fit in the input area");
+static_assert(SOLVE_X + 32 * kLdX * 4 <= IN_V, "solve scratch must fit in the input area");
 
 // Tensor-memory columns (one allocation of 256).
 constexpr uint32_t TM_D1 = 0, TM_DW = 64, TM_D3 = 128, TM_D5 = 160, kTmemCols = 256;
@@ -120,6 +121,23 @@ __device__ __forceinline__ void issue_chunk_loads(unsigned char *sm, const CUten
     tma_load_3d(sm + IN_V, tv, bar, j0, h, row);
 }
 
+__device__ __forceinline__ void unpack_bf16x8(uint4 raw, float (&x)[8])
+{
+    const uint32_t w[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+        const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&w[q]));
+        x[2 * q] = f.x;
+        x[2 * q + 1] = f.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[8])
+{
+    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                      pack_bf16x2(x[6], x[7]));
+}
+
 __global__ void __launch_bounds__(kTcThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_v,
@@ -131,10 +149,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     __shared__ __align__(8) uint64_t bar_tma, bar_mma;
     __shared__ uint32_t tmem_holder;
     __shared__ float s_beta[kC];
+    __shared__ float s_gam[kD];
+    __shared__ float s_tot[kD];
 
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
-    const int tid = threadIdx.x, warp = tid >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter; column half
     const int j0 = blockIdx.x * kDV, h = blockIdx.y, n = order[blockIdx.z];
     int64_t t0, t1;
     seq_range(cu, n, total, t0, t1);
@@ -157,34 +178,40 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     for (int e = tid; e < 2 * 2048; e += kTcThreads)
         *reinterpret_cast<uint32_t *>(sm + O5 + (e >> 11) * 16384 + 8192 + (e & 2047) * 4) = 0u;
 
-    // state row i = tid, columns j0 .. j0+31, fp32 in registers
-    float S[kDV];
-    const size_t st_off = (((size_t)n * H + h) * kD + tid) * kD + j0;
+    // State row i, columns j0 + 16*half .. +15, fp32 in registers.  The thread owns
+    // TMEM lane i of every 128-lane accumulator.
+    const int i_row = quarter * 32 + lane;
+    const int jh = half * 16;
+    float S[16];
+    const size_t st_off = (((size_t)n * H + h) * kD + i_row) * kD + j0 + jh;
     if (init_state) {
 #pragma unroll
-        for (int q = 0; q < kDV / 4; ++q) {
+        for (int q = 0; q < 4; ++q) {
             const float4 x = *reinterpret_cast<const float4 *>(init_state + st_off + 4 * q);
             S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < kDV; ++j) S[j] = 0.f;
+        for (int j = 0; j < 16; ++j) S[j] = 0.f;
     }
 #pragma unroll
-    for (int j = 0; j < kDV; ++j) store_bf16(sm + O7 + km16(j, tid, kDV), S[j]);
+    for (int j = 0; j < 16; ++j) store_bf16(sm + O7 + km16(jh + j, i_row, kDV), S[j]);
 
     fence_proxy_async_smem();
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_holder;
-    const uint32_t lane_off = (uint32_t)(warp * 32) << 16;
-    const uint32_t tD1 = tmem + TM_D1 + lane_off, tDW = tmem + TM_DW + lane_off;
-    const uint32_t tD3 = tmem + TM_D3 + lane_off, tD5 = tmem + TM_D5 + lane_off;
+    const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
 
     uint32_t ph_tma = 0, ph_mma = 0;
     bool tma_pending = nchunks > 0, mma_pending = false, timed_out = false, decay_bad = false;
     if (tid == 0 && nchunks > 0)
         issue_chunk_loads(sm, &tm_q, &tm_k, &tm_la, &tm_v, &bar_tma, h, j0, (int)t0);
+
+    float *sA = reinterpret_cast<float *>(sm + SOLVE_A);
+    float *sT = reinterpret_cast<float *>(sm + SOLVE_T);
+    float *sX = reinterpret_cast<float *>(sm + SOLVE_X);
+    const float *la_in = reinterpret_cast<const float *>(sm + IN_LA);
 
     for (int c = 0; c < nchunks; ++c) {
         const int64_t c0 = t0 + (int64_t)c * kC;
@@ -196,45 +223,68 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ph_tma ^= 1;
         tma_pending = false;
 
-        // ---------------------------------------------------------- a1, a2
-        float gamma_c;
+        // ---------------------------------------------------------- a1: prefix over rows
+        // Two threads per key channel i: rows 0-31 and rows 32-63.  Each scans its
+        // half in registers; the upper half adds the lower half's total.
+        const int ci = tid & (kD - 1), rh = tid >> 7;  // channel, row half
+        float gl[32], gmin = 0.f, gmax = 0.f;
         {
-            const int i = tid;
+            float g = 0.f;
+#pragma unroll
+            for (int rr = 0; rr < 32; ++rr) {
+                const int r = rh * 32 + rr;
+                g += r < len ? la_in[r * kD + ci] : 0.f;
+                gl[rr] = g;
+                gmin = fminf(gmin, g);
+                gmax = fmaxf(gmax, g);
+            }
+            if (rh == 0) s_tot[ci] = g;
+        }
+        if (tid >= kD) {  // beta and V^T (tf32, K-major [j][s]) by the upper-half threads
+            const int t2 = tid - kD;
+            if (t2 < kC) s_beta[t2] = t2 < len ? beta[(size_t)(c0 + t2) * H + h] : 0.f;
+            for (int e = t2; e < kDV * (kC / 4); e += kD) {
+                const int j = e % kDV, s4 = (e / kDV) * 4;
+                float x[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    x[u] = (s4 + u) < len ? bf16_at(sm + IN_V + ((s4 + u) * kDV + j) * 2) : 0.f;
+                *reinterpret_cast<float4 *>(sm + O6 + km32(j, s4, kDV)) =
+                    make_float4(x[0], x[1], x[2], x[3]);
+            }
+        }
+        __syncthreads();
+        // ---------------------------------------------------------- a2: decayed operands
+        {
+            const float off = rh ? s_tot[ci] : 0.f;
             const float scale = rsqrtf((float)kD);
-            float g = 0.f, gmin = 0.f, gmax = 0.f;
-            for (int r4 = 0; r4 < kC; r4 += 4) {
+            if (rh) s_gam[ci] = __expf(off + gl[31]);
+            if (off + gmin < KDA_MIN_CHUNK_LOG_DECAY || off + gmax > -KDA_MIN_CHUNK_LOG_DECAY)
+                decay_bad = true;
+            const uint32_t kbase = (uint32_t)((ci >> 6) * 16384 + ((ci & 7) << 1));
+            const uint32_t kbase2 = (uint32_t)((ci >> 6) * 8192 + ((ci & 7) << 1));
+            const uint32_t kchunk = (uint32_t)((ci & 63) >> 3);
+#pragma unroll
+            for (int r4 = 0; r4 < 32; r4 += 4) {
                 float ki4[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int r = r4 + u;
+                    const int rr = r4 + u, r = rh * 32 + rr;
                     const bool valid = r < len;
-                    const float la = valid ? *reinterpret_cast<const float *>(sm + IN_LA + (r * kD + i) * 4) : 0.f;
-                    g += la;
-                    gmin = fminf(gmin, g);
-                    gmax = fmaxf(gmax, g);
-                    const float qv = valid ? bf16_at(sm + IN_Q + (r * kD + i) * 2) : 0.f;
-                    const float kv = valid ? bf16_at(sm + IN_K + (r * kD + i) * 2) : 0.f;
+                    const float g = off + gl[rr];
                     const float eg = __expf(g), egi = __expf(-g);
-                    store_bf16(sm + O1 + km16(r, i, 128), kv * eg);
-                    store_bf16(sm + O1 + km16(64 + r, i, 128), scale * qv * eg);
+                    const float qv = valid ? bf16_at(sm + IN_Q + (r * kD + ci) * 2) : 0.f;
+                    const float kv = valid ? bf16_at(sm + IN_K + (r * kD + ci) * 2) : 0.f;
+                    const uint32_t sw = (kchunk ^ (uint32_t)(rr & 7)) << 4;  // (r & 7) == (rr & 7)
+                    store_bf16(sm + O1 + kbase + r * 128 + sw, kv * eg);
+                    store_bf16(sm + O1 + kbase + (64 + r) * 128 + sw, scale * qv * eg);
                     const float kgi = kv * egi;
-                    store_bf16(sm + O2 + km16(r, i, 64), kgi);
+                    store_bf16(sm + O2 + kbase2 + r * 128 + sw, kgi);
                     ki4[u] = to_tf32(kgi);
                 }
-                *reinterpret_cast<float4 *>(sm + O3 + km32(i, r4, 128)) =
+                *reinterpret_cast<float4 *>(sm + O3 + km32(ci, rh * 32 + r4, 128)) =
                     make_float4(ki4[0], ki4[1], ki4[2], ki4[3]);
             }
-            gamma_c = __expf(g);
-            if (gmin < KDA_MIN_CHUNK_LOG_DECAY || gmax > -KDA_MIN_CHUNK_LOG_DECAY) decay_bad = true;
-        }
-        if (tid < kC) s_beta[tid] = tid < len ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
-        for (int e = tid; e < kDV * (kC / 4); e += kTcThreads) {
-            const int j = e % kDV, s4 = (e / kDV) * 4;
-            float x[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                x[u] = (s4 + u) < len ? bf16_at(sm + IN_V + ((s4 + u) * kDV + j) * 2) : 0.f;
-            *reinterpret_cast<float4 *>(sm + O6 + km32(j, s4, kDV)) = make_float4(x[0], x[1], x[2], x[3]);
         }
         fence_proxy_async_smem();
         __syncthreads();
@@ -255,36 +305,35 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ph_mma ^= 1;
         tc_fence_after_sync();
 
-        float *sA = reinterpret_cast<float *>(sm + SOLVE_A);
-        float *sT = reinterpret_cast<float *>(sm + SOLVE_T);
-        float *sX = reinterpret_cast<float *>(sm + SOLVE_X);
-        if (warp < 2) {  // lanes 0..63: rows of Kg Ki^T -> A
-            const int r = tid;
+        if (quarter < 2) {  // lanes 0..63: rows of Kg Ki^T -> A (fp32, strict lower, beta rows)
+            const int r = quarter * 32 + lane;
             const float br = s_beta[r];
-            for (int cb = 0; cb < kC; cb += 16) {
+#pragma unroll
+            for (int cb = 0; cb < 32; cb += 16) {
                 float v[16];
-                tmem_ld16(tD1 + cb, v);
+                tmem_ld16(tmem + TM_D1 + lane_off + half * 32 + cb, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; ++u) sA[r * LDA + cb + u] = (cb + u) < r ? br * v[u] : 0.f;
+                for (int u = 0; u < 16; ++u) {
+                    const int col = half * 32 + cb + u;
+                    sA[r * kLdS + col] = col < r ? br * v[u] : 0.f;
+                }
             }
-        } else {  // lanes 64..127: rows of Qg Ki^T -> Aqk (bf16)
-            const int r = tid - 64;
-            for (int cb = 0; cb < kC; cb += 16) {
+        } else {  // lanes 64..127: rows of Qg Ki^T -> Aqk (bf16, lower incl. diagonal)
+            const int r = (quarter - 2) * 32 + lane;
+#pragma unroll
+            for (int cb = 0; cb < 32; cb += 16) {
                 float v[16];
-                tmem_ld16(tD1 + cb, v);
+                tmem_ld16(tmem + TM_D1 + lane_off + half * 32 + cb, v);
                 tmem_ld_wait();
 #pragma unroll
-                for (int half = 0; half < 2; ++half) {
-                    uint32_t pk[4];
+                for (int hh = 0; hh < 2; ++hh) {
+                    float x[8];
 #pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int s = cb + half * 8 + 2 * q;
-                        pk[q] = pack_bf16x2(s <= r ? v[half * 8 + 2 * q] : 0.f,
-                                            s + 1 <= r ? v[half * 8 + 2 * q + 1] : 0.f);
-                    }
-                    *reinterpret_cast<uint4 *>(sm + O8 + km16(r, cb + half * 8, 64)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                    for (int u = 0; u < 8; ++u)
+                        x[u] = (half * 32 + cb + hh * 8 + u) <= r ? v[hh * 8 + u] : 0.f;
+                    *reinterpret_cast<uint4 *>(sm + O8 + km16(r, half * 32 + cb + hh * 8, 64)) =
+                        pack_bf16x8(x);
                 }
             }
         }
@@ -292,38 +341,70 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         __syncthreads();
 
         // ---------------------------------------------------------- a4: T = (I + A)^-1
-        if (tid < 64) {  // diagonal 16 x 16 blocks, one column per thread
+        // Recursive doubling on the unit lower-triangular system: invert the four
+        // 16 x 16 diagonal blocks, then the two 16 x 16 blocks below them
+        // (T_10 = -T_11 A_10 T_00, T_32 = -T_33 A_32 T_22), then the 32 x 32
+        // block T_[2:4][0:2] = -T_[2:4][2:4] A_[2:4][0:2] T_[0:2][0:2].
+        if (tid < 64) {  // diagonal blocks, one column per thread
             const int b = (tid >> 4) * 16, cc = tid & 15;
             float x[16];
 #pragma unroll
             for (int r = 0; r < 16; ++r) {
                 float acc = 0.f;
 #pragma unroll
-                for (int m = 0; m < r; ++m) acc += sA[(b + r) * LDA + b + m] * x[m];
+                for (int m = 0; m < r; ++m) acc += sA[(b + r) * kLdS + b + m] * x[m];
                 x[r] = r < cc ? 0.f : (r == cc ? 1.f : -acc);
             }
 #pragma unroll
-            for (int r = 0; r < 16; ++r) sT[(b + r) * LDA + b + cc] = x[r];
+            for (int r = 0; r < 16; ++r) sT[(b + r) * kLdS + b + cc] = x[r];
         }
         __syncthreads();
-        for (int d = 1; d < 4; ++d) {  // off-diagonal blocks, by distance from the diagonal
-            const int nblk = 4 - d;
-            for (int e = tid; e < nblk * 256; e += kTcThreads) {  // X = sum_M A_RM T_MS
-                const int S0 = (e >> 8) * 16, R0 = S0 + d * 16, rr = (e >> 4) & 15, ss = e & 15;
-                float acc = 0.f;
-                for (int m = S0; m < R0; ++m) acc += sA[(R0 + rr) * LDA + m] * sT[m * LDA + S0 + ss];
-                sX[((e >> 8) * 16 + rr) * 17 + ss] = acc;
-            }
-            __syncthreads();
-            for (int e = tid; e < nblk * 256; e += kTcThreads) {  // T_RS = -T_RR X
-                const int S0 = (e >> 8) * 16, R0 = S0 + d * 16, rr = (e >> 4) & 15, ss = e & 15;
-                float acc = 0.f;
-                for (int m = 0; m <= rr; ++m)
-                    acc += sT[(R0 + rr) * LDA + R0 + m] * sX[((e >> 8) * 16 + m) * 17 + ss];
-                sT[(R0 + rr) * LDA + S0 + ss] = -acc;
-            }
-            __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {  // X = A_{R,R-1} T_{R-1,R-1} for (R0, C0) = (16, 0), (48, 32)
+            const int e = tid + q * kTcThreads, b = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+            const int R0 = 16 + 32 * b, C0 = 32 * b;
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                if (m >= cc) acc += sA[(R0 + rr) * kLdS + C0 + m] * sT[(C0 + m) * kLdS + C0 + cc];
+            sX[(b * 16 + rr) * kLdX + cc] = acc;
         }
+        __syncthreads();
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {  // T_{R,R-1} = -T_RR X
+            const int e = tid + q * kTcThreads, b = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+            const int R0 = 16 + 32 * b, C0 = 32 * b;
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < 16; ++m)
+                if (m <= rr) acc += sT[(R0 + rr) * kLdS + R0 + m] * sX[(b * 16 + m) * kLdX + cc];
+            sT[(R0 + rr) * kLdS + C0 + cc] = -acc;
+        }
+        __syncthreads();
+        {  // X2 = A[32:64][0:32] T[0:32][0:32]: row r, columns c..c+3 per thread
+            const int r = tid >> 3, c = (tid & 7) * 4, k0 = c & 16;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+            for (int k = k0; k < 32; ++k) {
+                const float a = sA[(32 + r) * kLdS + k];
+                const float4 t = *reinterpret_cast<const float4 *>(sT + k * kLdS + c);
+                acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
+            }
+            *reinterpret_cast<float4 *>(sX + r * kLdX + c) = acc;
+        }
+        __syncthreads();
+        {  // T[32:64][0:32] = -T[32:64][32:64] X2
+            const int r = tid >> 3, c = (tid & 7) * 4;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int m = 0; m <= r; ++m) {
+                const float t = sT[(32 + r) * kLdS + 32 + m];
+                const float4 x = *reinterpret_cast<const float4 *>(sX + m * kLdX + c);
+                acc.x += t * x.x; acc.y += t * x.y; acc.z += t * x.z; acc.w += t * x.w;
+            }
+            *reinterpret_cast<float4 *>(sT + (32 + r) * kLdS + c) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        }
+        __syncthreads();
         // T' = T diag(beta): bf16 (for W) and tf32 (for U~)
         for (int e = tid; e < kC * 8; e += kTcThreads) {
             const int r = e >> 3, s8 = (e & 7) * 8;
@@ -331,11 +412,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int s = s8 + u;
-                t[u] = s <= r ? sT[r * LDA + s] * s_beta[s] : 0.f;
+                t[u] = s <= r ? sT[r * kLdS + s] * s_beta[s] : 0.f;
             }
-            *reinterpret_cast<uint4 *>(sm + O4 + km16(r, s8, 64)) =
-                make_uint4(pack_bf16x2(t[0], t[1]), pack_bf16x2(t[2], t[3]), pack_bf16x2(t[4], t[5]),
-                           pack_bf16x2(t[6], t[7]));
+            *reinterpret_cast<uint4 *>(sm + O4 + km16(r, s8, 64)) = pack_bf16x8(t);
             *reinterpret_cast<float4 *>(sm + O5 + km32(r, s8, 128)) =
                 make_float4(to_tf32(t[0]), to_tf32(t[1]), to_tf32(t[2]), to_tf32(t[3]));
             *reinterpret_cast<float4 *>(sm + O5 + km32(r, s8 + 4, 128)) =
@@ -368,15 +447,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ph_mma ^= 1;
         tc_fence_after_sync();
 
-        {  // -W into rows 0-63 of O1 (Kg is no longer needed)
-            const int i = tid;
-            for (int cb = 0; cb < kC; cb += 16) {
-                float v[16];
-                tmem_ld16(tDW + cb, v);
-                tmem_ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; ++u) store_bf16(sm + O1 + km16(cb + u, i, 128), -v[u]);
-            }
+        for (int cb = 0; cb < 32; cb += 16) {  // -W into rows 0-63 of O1 (Kg no longer needed)
+            float v[16];
+            tmem_ld16(tmem + TM_DW + lane_off + half * 32 + cb, v);
+            tmem_ld_wait();
+#pragma unroll
+            for (int u = 0; u < 16; ++u) store_bf16(sm + O1 + km16(half * 32 + cb + u, i_row, 128), -v[u]);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -398,17 +475,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ph_mma ^= 1;
         tc_fence_after_sync();
 
-        if (warp < 2) {  // u rows 0..63 -> bf16 and tf32 operands (u^T, K-major)
-            const int r = tid;
-            for (int cb = 0; cb < kDV; cb += 16) {
-                float v[16];
-                tmem_ld16(tD3 + cb, v);
-                tmem_ld_wait();
+        if (quarter < 2) {  // u rows 0..63 -> bf16 and tf32 operands (u^T, K-major)
+            const int r = quarter * 32 + lane;
+            float v[16];
+            tmem_ld16(tmem + TM_D3 + lane_off + jh, v);
+            tmem_ld_wait();
 #pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    store_bf16(sm + O9 + km16(cb + u, r, kDV), v[u]);
-                    *reinterpret_cast<float *>(sm + O10 + km32(cb + u, r, kDV)) = to_tf32(v[u]);
-                }
+            for (int u = 0; u < 16; ++u) {
+                store_bf16(sm + O9 + km16(jh + u, r, kDV), v[u]);
+                *reinterpret_cast<float *>(sm + O10 + km32(jh + u, r, kDV)) = to_tf32(v[u]);
             }
         }
         fence_proxy_async_smem();
@@ -434,29 +509,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ph_mma ^= 1;
         tc_fence_after_sync();
 
-        if (warp >= 2) {  // o rows 0..63 from lanes 64..127
-            const int r = tid - 64;
-            float v[32];
-            tmem_ld16(tD3, *reinterpret_cast<float(*)[16]>(v));
-            tmem_ld16(tD3 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+        if (quarter >= 2) {  // o rows 0..63 from lanes 64..127
+            const int r = (quarter - 2) * 32 + lane;
+            float v[16];
+            tmem_ld16(tmem + TM_D3 + lane_off + jh, v);
             tmem_ld_wait();
             if (r < len) {
-                uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(c0 + r) * H + h) * kD + j0);
+                uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(c0 + r) * H + h) * kD + j0 + jh);
+                float a[8], b[8];
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
-                    dst[q] = make_uint4(pack_bf16x2(v[8 * q], v[8 * q + 1]), pack_bf16x2(v[8 * q + 2], v[8 * q + 3]),
-                                        pack_bf16x2(v[8 * q + 4], v[8 * q + 5]), pack_bf16x2(v[8 * q + 6], v[8 * q + 7]));
+                for (int u = 0; u < 8; ++u) { a[u] = v[u]; b[u] = v[8 + u]; }
+                dst[0] = pack_bf16x8(a);
+                dst[1] = pack_bf16x8(b);
             }
         }
         {  // state rows: S <- gamma_c (S + Ki^T u)
-            float v[32];
-            tmem_ld16(tD5, *reinterpret_cast<float(*)[16]>(v));
-            tmem_ld16(tD5 + 16, *reinterpret_cast<float(*)[16]>(v + 16));
+            float v[16];
+            tmem_ld16(tmem + TM_D5 + lane_off + jh, v);
             tmem_ld_wait();
+            const float gc = s_gam[i_row];
 #pragma unroll
-            for (int j = 0; j < kDV; ++j) {
-                S[j] = gamma_c * (S[j] + v[j]);
-                store_bf16(sm + O7 + km16(j, tid, kDV), S[j]);
+            for (int j = 0; j < 16; ++j) {
+                S[j] = gc * (S[j] + v[j]);
+                store_bf16(sm + O7 + km16(jh + j, i_row, kDV), S[j]);
             }
         }
         fence_proxy_async_smem();
@@ -472,7 +547,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     } else {
         float *dst = final_state + st_off;
 #pragma unroll
-        for (int q = 0; q < kDV / 4; ++q)
+        for (int q = 0; q < 4; ++q)
             *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
     }
     if (decay_bad) atomicOr(status, DEV_ERR_DECAY);
