@@ -41,7 +41,7 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kD = 128, kDV = 32, kC = 64, kTcThreads = 256;
+constexpr int kD = 128, kDV = 32, kC = 64, kTcThreads = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
 
 // Dynamic shared memory map (byte offsets from a 1024-byte aligned base).
@@ -70,10 +70,10 @@ static_assert(O8 == O4 + 8192, "[T' ; Aqk] must be one 128-row operand");
 static_assert(SOLVE_X + 32 * kLdX * 4 <= IN_V, "solve scratch must fit in the input area");
 
 // Tensor-memory columns (one allocation of 256).
-constexpr uint32_t TM_D1 = 0, TM_DW = 64, TM_D3 = 128, TM_D5 = 160, kTmemCols = 256;
+constexpr uint32_t TM_D1 = 0, TM_DW = 64, TM_D3 = 192, TM_D5 = 224, kTmemCols = 256;
 
 constexpr uint32_t IDESC_G1 = idesc_bf16(128, 64, false, false);
-constexpr uint32_t IDESC_GW = idesc_bf16(128, 64, true, false);
+constexpr uint32_t IDESC_GW = idesc_bf16(64, 128, false, true);  // W = T' Kg (Kg MN-major)
 constexpr uint32_t IDESC_GU = idesc_tf32(128, 32, false, false);
 constexpr uint32_t IDESC_G3 = idesc_bf16(128, 32, false, false);
 constexpr uint32_t IDESC_G5 = idesc_tf32(128, 32, false, false);
@@ -148,14 +148,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar_tma, bar_mma;
     __shared__ uint32_t tmem_holder;
-    __shared__ float s_beta[kC];
-    __shared__ float s_gam[kD];
-    __shared__ float s_tot[kD];
+    __shared__ __align__(16) float s_beta[kC];
+    __shared__ __align__(8) float s_gam[kD];
 
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, half = warp >> 2;  // TMEM lane quarter; column half
+    const int quarter = warp & 3, part = warp >> 2;  // TMEM lane quarter; column part (0..3)
     const int j0 = blockIdx.x * kDV, h = blockIdx.y, n = order[blockIdx.z];
     int64_t t0, t1;
     seq_range(cu, n, total, t0, t1);
@@ -175,27 +174,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tmem_relinquish();
     }
     // rows 64..127 of [T' ; 0] (both 32-column panels) stay zero for the whole kernel
-    for (int e = tid; e < 2 * 2048; e += kTcThreads)
+    for (int e = tid; e < 2 * 2048; e += kTcThreads)  // 2 panels x 64 rows x 32 words
         *reinterpret_cast<uint32_t *>(sm + O5 + (e >> 11) * 16384 + 8192 + (e & 2047) * 4) = 0u;
 
-    // State row i, columns j0 + 16*half .. +15, fp32 in registers.  The thread owns
+    // State row i, columns j0 + 8*part .. +7, fp32 in registers.  The thread owns
     // TMEM lane i of every 128-lane accumulator.
     const int i_row = quarter * 32 + lane;
-    const int jh = half * 16;
-    float S[16];
-    const size_t st_off = (((size_t)n * H + h) * kD + i_row) * kD + j0 + jh;
+    const int jp = part * 8;
+    float S[8];
+    const size_t st_off = (((size_t)n * H + h) * kD + i_row) * kD + j0 + jp;
     if (init_state) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
             const float4 x = *reinterpret_cast<const float4 *>(init_state + st_off + 4 * q);
             S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
         }
     } else {
 #pragma unroll
-        for (int j = 0; j < 16; ++j) S[j] = 0.f;
+        for (int j = 0; j < 8; ++j) S[j] = 0.f;
     }
 #pragma unroll
-    for (int j = 0; j < 16; ++j) store_bf16(sm + O7 + km16(jh + j, i_row, kDV), S[j]);
+    for (int j = 0; j < 8; ++j) store_bf16(sm + O7 + km16(jp + j, i_row, kDV), S[j]);
+    // beta of the next chunk is loaded one chunk ahead (hides the global-load latency)
+    float beta_next = (tid < kC && tid < t1 - t0) ? beta[(size_t)(t0 + tid) * H + h] : 0.f;
 
     fence_proxy_async_smem();
     __syncthreads();
@@ -212,6 +213,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     float *sT = reinterpret_cast<float *>(sm + SOLVE_T);
     float *sX = reinterpret_cast<float *>(sm + SOLVE_X);
     const float *la_in = reinterpret_cast<const float *>(sm + IN_LA);
+    // quarter totals of the prefix scan; the tf32 u operand area is idle during the prep
+    float *s_tot = reinterpret_cast<float *>(sm + O10);
 
     for (int c = 0; c < nchunks; ++c) {
         const int64_t c0 = t0 + (int64_t)c * kC;
@@ -224,66 +227,90 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tma_pending = false;
 
         // ---------------------------------------------------------- a1: prefix over rows
-        // Two threads per key channel i: rows 0-31 and rows 32-63.  Each scans its
-        // half in registers; the upper half adds the lower half's total.
-        const int ci = tid & (kD - 1), rh = tid >> 7;  // channel, row half
-        float gl[32], gmin = 0.f, gmax = 0.f;
+        // Thread = (channel pair cp: channels 2cp, 2cp+1; row group rg: rows
+        // 8rg .. 8rg+7).  Each scans its 8 rows in registers; group totals are
+        // combined through shared memory.
+        const int cp = tid & 63, rg = tid >> 6;
+        float2 gl[8];
+        float gmin = 0.f, gmax = 0.f;
         {
-            float g = 0.f;
+            float2 g = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int rr = 0; rr < 32; ++rr) {
-                const int r = rh * 32 + rr;
-                g += r < len ? la_in[r * kD + ci] : 0.f;
+            for (int rr = 0; rr < 8; ++rr) {
+                const int r = rg * 8 + rr;
+                const float2 la = r < len ? *reinterpret_cast<const float2 *>(la_in + r * kD + 2 * cp)
+                                          : make_float2(0.f, 0.f);
+                g.x += la.x;
+                g.y += la.y;
                 gl[rr] = g;
-                gmin = fminf(gmin, g);
-                gmax = fmaxf(gmax, g);
+                gmin = fminf(gmin, fminf(g.x, g.y));
+                gmax = fmaxf(gmax, fmaxf(g.x, g.y));
             }
-            if (rh == 0) s_tot[ci] = g;
+            *reinterpret_cast<float2 *>(&s_tot[rg * kD + 2 * cp]) = g;
         }
-        if (tid >= kD) {  // beta and V^T (tf32, K-major [j][s]) by the upper-half threads
-            const int t2 = tid - kD;
-            if (t2 < kC) s_beta[t2] = t2 < len ? beta[(size_t)(c0 + t2) * H + h] : 0.f;
-            for (int e = t2; e < kDV * (kC / 4); e += kD) {
-                const int j = e % kDV, s4 = (e / kDV) * 4;
-                float x[4];
+        if (tid < kC) {
+            s_beta[tid] = beta_next;
+            const int64_t cn = c0 + kC;  // next chunk
+            beta_next = (tid < t1 - cn) ? beta[(size_t)(cn + tid) * H + h] : 0.f;
+        }
+        {  // V^T (tf32, K-major [j][s]): one 4-row group of one column per thread
+            const int j = tid % kDV, s4 = (tid / kDV) * 4;
+            float x[4];
 #pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    x[u] = (s4 + u) < len ? bf16_at(sm + IN_V + ((s4 + u) * kDV + j) * 2) : 0.f;
-                *reinterpret_cast<float4 *>(sm + O6 + km32(j, s4, kDV)) =
-                    make_float4(x[0], x[1], x[2], x[3]);
-            }
+            for (int u = 0; u < 4; ++u)
+                x[u] = (s4 + u) < len ? bf16_at(sm + IN_V + ((s4 + u) * kDV + j) * 2) : 0.f;
+            *reinterpret_cast<float4 *>(sm + O6 + km32(j, s4, kDV)) = make_float4(x[0], x[1], x[2], x[3]);
         }
         __syncthreads();
         // ---------------------------------------------------------- a2: decayed operands
         {
-            const float off = rh ? s_tot[ci] : 0.f;
-            const float scale = rsqrtf((float)kD);
-            if (rh) s_gam[ci] = __expf(off + gl[31]);
-            if (off + gmin < KDA_MIN_CHUNK_LOG_DECAY || off + gmax > -KDA_MIN_CHUNK_LOG_DECAY)
+            float2 off = make_float2(0.f, 0.f);
+            for (int q = 0; q < rg; ++q) {
+                const float2 t = *reinterpret_cast<const float2 *>(&s_tot[q * kD + 2 * cp]);
+                off.x += t.x;
+                off.y += t.y;
+            }
+            if (rg == 7)
+                *reinterpret_cast<float2 *>(&s_gam[2 * cp]) =
+                    make_float2(__expf(off.x + gl[7].x), __expf(off.y + gl[7].y));
+            if (fminf(off.x, off.y) + gmin < KDA_MIN_CHUNK_LOG_DECAY ||
+                fmaxf(off.x, off.y) + gmax > -KDA_MIN_CHUNK_LOG_DECAY)
                 decay_bad = true;
-            const uint32_t kbase = (uint32_t)((ci >> 6) * 16384 + ((ci & 7) << 1));
-            const uint32_t kbase2 = (uint32_t)((ci >> 6) * 8192 + ((ci & 7) << 1));
-            const uint32_t kchunk = (uint32_t)((ci & 63) >> 3);
+            const float scale = rsqrtf((float)kD);
+            // K-major swizzled byte offset of channel 2cp in a row, less the row part
+            const uint32_t pbase1 = (uint32_t)((cp >> 5) * 16384 + ((cp & 3) << 2));
+            const uint32_t pbase2 = (uint32_t)((cp >> 5) * 8192 + ((cp & 3) << 2));
+            const uint32_t pchunk = (uint32_t)((cp & 31) >> 2);
 #pragma unroll
-            for (int r4 = 0; r4 < 32; r4 += 4) {
-                float ki4[4];
+            for (int r4 = 0; r4 < 8; r4 += 4) {
+                float ka[4], kb[4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u) {
-                    const int rr = r4 + u, r = rh * 32 + rr;
+                    const int rr = r4 + u, r = rg * 8 + rr;
                     const bool valid = r < len;
-                    const float g = off + gl[rr];
-                    const float eg = __expf(g), egi = __expf(-g);
-                    const float qv = valid ? bf16_at(sm + IN_Q + (r * kD + ci) * 2) : 0.f;
-                    const float kv = valid ? bf16_at(sm + IN_K + (r * kD + ci) * 2) : 0.f;
-                    const uint32_t sw = (kchunk ^ (uint32_t)(rr & 7)) << 4;  // (r & 7) == (rr & 7)
-                    store_bf16(sm + O1 + kbase + r * 128 + sw, kv * eg);
-                    store_bf16(sm + O1 + kbase + (64 + r) * 128 + sw, scale * qv * eg);
-                    const float kgi = kv * egi;
-                    store_bf16(sm + O2 + kbase2 + r * 128 + sw, kgi);
-                    ki4[u] = to_tf32(kgi);
+                    const float gx = off.x + gl[rr].x, gy = off.y + gl[rr].y;
+                    const float ex = __expf(gx), ey = __expf(gy);
+                    const float ix = __expf(-gx), iy = __expf(-gy);
+                    const uint32_t qraw = valid ? *reinterpret_cast<const uint32_t *>(sm + IN_Q + (r * kD + 2 * cp) * 2) : 0u;
+                    const uint32_t kraw = valid ? *reinterpret_cast<const uint32_t *>(sm + IN_K + (r * kD + 2 * cp) * 2) : 0u;
+                    const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qraw));
+                    const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kraw));
+                    const uint32_t sw = (pchunk ^ (uint32_t)(rr & 7)) << 4;  // (r & 7) == (rr & 7)
+                    *reinterpret_cast<uint32_t *>(sm + O1 + pbase1 + r * 128 + sw) = pack_bf16x2(kv.x * ex, kv.y * ey);
+                    *reinterpret_cast<uint32_t *>(sm + O1 + pbase1 + (64 + r) * 128 + sw) =
+                        pack_bf16x2(qv.x * (scale * ex), qv.y * (scale * ey));
+                    const float kix = kv.x * ix, kiy = kv.y * iy;
+                    *reinterpret_cast<uint32_t *>(sm + O2 + pbase2 + r * 128 + sw) = pack_bf16x2(kix, kiy);
+                    ka[u] = to_tf32(kix);
+                    kb[u] = to_tf32(kiy);
                 }
-                *reinterpret_cast<float4 *>(sm + O3 + km32(ci, rh * 32 + r4, 128)) =
-                    make_float4(ki4[0], ki4[1], ki4[2], ki4[3]);
+                // lanes 4-7 of every 8 store their odd channel first, so each store covers
+                // 8 distinct swizzle positions (no bank conflict)
+                const int rb = rg * 8 + r4, sel = (lane >> 2) & 1;
+                const float4 va = make_float4(ka[0], ka[1], ka[2], ka[3]);
+                const float4 vb = make_float4(kb[0], kb[1], kb[2], kb[3]);
+                *reinterpret_cast<float4 *>(sm + O3 + km32(2 * cp + sel, rb, 128)) = sel ? vb : va;
+                *reinterpret_cast<float4 *>(sm + O3 + km32(2 * cp + 1 - sel, rb, 128)) = sel ? va : vb;
             }
         }
         fence_proxy_async_smem();
@@ -308,33 +335,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (quarter < 2) {  // lanes 0..63: rows of Kg Ki^T -> A (fp32, strict lower, beta rows)
             const int r = quarter * 32 + lane;
             const float br = s_beta[r];
+            float v[16];
+            tmem_ld16(tmem + TM_D1 + lane_off + part * 16, v);
+            tmem_ld_wait();
 #pragma unroll
-            for (int cb = 0; cb < 32; cb += 16) {
-                float v[16];
-                tmem_ld16(tmem + TM_D1 + lane_off + half * 32 + cb, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int u = 0; u < 16; ++u) {
-                    const int col = half * 32 + cb + u;
-                    sA[r * kLdS + col] = col < r ? br * v[u] : 0.f;
-                }
+            for (int u = 0; u < 16; u += 4) {
+                const int col = part * 16 + u;
+                *reinterpret_cast<float4 *>(sA + r * kLdS + col) =
+                    make_float4(col < r ? br * v[u] : 0.f, col + 1 < r ? br * v[u + 1] : 0.f,
+                                col + 2 < r ? br * v[u + 2] : 0.f, col + 3 < r ? br * v[u + 3] : 0.f);
             }
         } else {  // lanes 64..127: rows of Qg Ki^T -> Aqk (bf16, lower incl. diagonal)
             const int r = (quarter - 2) * 32 + lane;
+            float v[16];
+            tmem_ld16(tmem + TM_D1 + lane_off + part * 16, v);
+            tmem_ld_wait();
 #pragma unroll
-            for (int cb = 0; cb < 32; cb += 16) {
-                float v[16];
-                tmem_ld16(tmem + TM_D1 + lane_off + half * 32 + cb, v);
-                tmem_ld_wait();
+            for (int hh = 0; hh < 2; ++hh) {
+                float x[8];
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
-                    float x[8];
-#pragma unroll
-                    for (int u = 0; u < 8; ++u)
-                        x[u] = (half * 32 + cb + hh * 8 + u) <= r ? v[hh * 8 + u] : 0.f;
-                    *reinterpret_cast<uint4 *>(sm + O8 + km16(r, half * 32 + cb + hh * 8, 64)) =
-                        pack_bf16x8(x);
-                }
+                for (int u = 0; u < 8; ++u) x[u] = (part * 16 + hh * 8 + u) <= r ? v[hh * 8 + u] : 0.f;
+                *reinterpret_cast<uint4 *>(sm + O8 + km16(r, part * 16 + hh * 8, 64)) = pack_bf16x8(x);
             }
         }
         tc_fence_before_sync();
@@ -359,61 +380,76 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             for (int r = 0; r < 16; ++r) sT[(b + r) * kLdS + b + cc] = x[r];
         }
         __syncthreads();
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {  // X = A_{R,R-1} T_{R-1,R-1} for (R0, C0) = (16, 0), (48, 32)
-            const int e = tid + q * kTcThreads, b = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+        {  // X = A_{R,R-1} T_{R-1,R-1} for (R0, C0) = (16, 0), (48, 32)
+            const int b = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
             const int R0 = 16 + 32 * b, C0 = 32 * b;
             float acc = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-                if (m >= cc) acc += sA[(R0 + rr) * kLdS + C0 + m] * sT[(C0 + m) * kLdS + C0 + cc];
+            for (int m = 0; m < 16; ++m) {
+                const float a = sA[(R0 + rr) * kLdS + C0 + m], t = sT[(C0 + m) * kLdS + C0 + cc];
+                acc += m >= cc ? a * t : 0.f;
+            }
             sX[(b * 16 + rr) * kLdX + cc] = acc;
         }
         __syncthreads();
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {  // T_{R,R-1} = -T_RR X
-            const int e = tid + q * kTcThreads, b = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
+        {  // T_{R,R-1} = -T_RR X
+            const int b = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
             const int R0 = 16 + 32 * b, C0 = 32 * b;
             float acc = 0.f;
 #pragma unroll
-            for (int m = 0; m < 16; ++m)
-                if (m <= rr) acc += sT[(R0 + rr) * kLdS + R0 + m] * sX[(b * 16 + m) * kLdX + cc];
+            for (int m = 0; m < 16; ++m) {
+                const float t = sT[(R0 + rr) * kLdS + R0 + m], x = sX[(b * 16 + m) * kLdX + cc];
+                acc += m <= rr ? t * x : 0.f;
+            }
             sT[(R0 + rr) * kLdS + C0 + cc] = -acc;
         }
         __syncthreads();
-        {  // X2 = A[32:64][0:32] T[0:32][0:32]: row r, columns c..c+3 per thread
+        if (tid < 256) {  // X2 = A[32:64][0:32] T[0:32][0:32]: row r, columns c..c+3 per thread
             const int r = tid >> 3, c = (tid & 7) * 4, k0 = c & 16;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int k = k0; k < 32; ++k) {
-                const float a = sA[(32 + r) * kLdS + k];
-                const float4 t = *reinterpret_cast<const float4 *>(sT + k * kLdS + c);
-                acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
+#pragma unroll
+            for (int k4 = 0; k4 < 32; k4 += 4) {
+                if (k4 < k0) continue;
+                const float4 a = *reinterpret_cast<const float4 *>(sA + (32 + r) * kLdS + k4);
+                const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 t = *reinterpret_cast<const float4 *>(sT + (k4 + u) * kLdS + c);
+                    acc.x += av[u] * t.x; acc.y += av[u] * t.y; acc.z += av[u] * t.z; acc.w += av[u] * t.w;
+                }
             }
             *reinterpret_cast<float4 *>(sX + r * kLdX + c) = acc;
         }
         __syncthreads();
-        {  // T[32:64][0:32] = -T[32:64][32:64] X2
+        if (tid < 256) {  // T[32:64][0:32] = -T[32:64][32:64] X2
             const int r = tid >> 3, c = (tid & 7) * 4;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int m = 0; m <= r; ++m) {
-                const float t = sT[(32 + r) * kLdS + 32 + m];
-                const float4 x = *reinterpret_cast<const float4 *>(sX + m * kLdX + c);
-                acc.x += t * x.x; acc.y += t * x.y; acc.z += t * x.z; acc.w += t * x.w;
+#pragma unroll
+            for (int m4 = 0; m4 < 32; m4 += 4) {
+                const float4 t = *reinterpret_cast<const float4 *>(sT + (32 + r) * kLdS + 32 + m4);
+                const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float tm = m4 + u <= r ? tv[u] : 0.f;  // T22 is lower triangular
+                    const float4 x = *reinterpret_cast<const float4 *>(sX + (m4 + u) * kLdX + c);
+                    acc.x += tm * x.x; acc.y += tm * x.y; acc.z += tm * x.z; acc.w += tm * x.w;
+                }
             }
-            *reinterpret_cast<float4 *>(sT + (32 + r) * kLdS + c) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            *reinterpret_cast<float4 *>(sT + (32 + r) * kLdS + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
         // T' = T diag(beta): bf16 (for W) and tf32 (for U~)
-        for (int e = tid; e < kC * 8; e += kTcThreads) {
-            const int r = e >> 3, s8 = (e & 7) * 8;
+        {
+            const int r = tid >> 3, s8 = (tid & 7) * 8;
+            const float4 ta = *reinterpret_cast<const float4 *>(sT + r * kLdS + s8);
+            const float4 tb = *reinterpret_cast<const float4 *>(sT + r * kLdS + s8 + 4);
+            const float4 ba = *reinterpret_cast<const float4 *>(s_beta + s8);
+            const float4 bb = *reinterpret_cast<const float4 *>(s_beta + s8 + 4);
+            const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
+            const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
             float t[8];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int s = s8 + u;
-                t[u] = s <= r ? sT[r * kLdS + s] * s_beta[s] : 0.f;
-            }
+            for (int u = 0; u < 8; ++u) t[u] = s8 + u <= r ? tv[u] * bv[u] : 0.f;
             *reinterpret_cast<uint4 *>(sm + O4 + km16(r, s8, 64)) = pack_bf16x8(t);
             *reinterpret_cast<float4 *>(sm + O5 + km32(r, s8, 128)) =
                 make_float4(to_tf32(t[0]), to_tf32(t[1]), to_tf32(t[2]), to_tf32(t[3]));
@@ -430,9 +466,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                                   (int)(c0 + kC));
             tc_fence_after_sync();
 #pragma unroll
-            for (int s = 0; s < 4; ++s)  // W^T = Kg^T T'^T; Kg read MN-major from O1 rows 0-63
-                mma_bf16(tmem + TM_DW, sdesc(sb + O1 + s * 2048, 16384, 1024, kSw128B),
-                         kdesc(sb + O4 + s * 32), IDESC_GW, s > 0);
+            for (int s = 0; s < 4; ++s)  // W = T' Kg (M = 64); Kg read MN-major from O1 rows 0-63
+                mma_bf16(tmem + TM_DW, kdesc(sb + O4 + s * 32),
+                         sdesc(sb + O1 + s * 2048, 16384, 1024, kSw128B), IDESC_GW, s > 0);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {  // U~ = [T' ; 0] V  (tf32)
                 const uint32_t p = s >> 2, w = (s & 3) * 32;
@@ -447,13 +483,26 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         ph_mma ^= 1;
         tc_fence_after_sync();
 
+        {  // -W into rows 0-63 of O1 (Kg no longer needed).  The M = 64 accumulator
+           // keeps row 16q + l in lane l < 16 of lane quarter q; this warp takes 32
+           // of the 128 columns.
+            const int r = quarter * 16 + (lane & 15);
 #pragma unroll
-        for (int cb = 0; cb < 32; cb += 16) {  // -W into rows 0-63 of O1 (Kg no longer needed)
-            float v[16];
-            tmem_ld16(tmem + TM_DW + lane_off + half * 32 + cb, v);
-            tmem_ld_wait();
+            for (int cb = 0; cb < 32; cb += 16) {
+                float v[16];
+                tmem_ld16(tmem + TM_DW + lane_off + part * 32 + cb, v);
+                tmem_ld_wait();
+                if (lane < 16) {
 #pragma unroll
-            for (int u = 0; u < 16; ++u) store_bf16(sm + O1 + km16(half * 32 + cb + u, i_row, 128), -v[u]);
+                    for (int hh = 0; hh < 2; ++hh) {
+                        float x[8];
+#pragma unroll
+                        for (int u = 0; u < 8; ++u) x[u] = -v[hh * 8 + u];
+                        *reinterpret_cast<uint4 *>(sm + O1 + km16(r, part * 32 + cb + hh * 8, 128)) =
+                            pack_bf16x8(x);
+                    }
+                }
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -476,14 +525,21 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         tc_fence_after_sync();
 
         if (quarter < 2) {  // u rows 0..63 -> bf16 and tf32 operands (u^T, K-major)
-            const int r = quarter * 32 + lane;
-            float v[16];
-            tmem_ld16(tmem + TM_D3 + lane_off + jh, v);
+            // Adjacent lanes (rows r, r^1) swap halves so each writes a row pair
+            // (2 x bf16, 2 x tf32) for 4 of the thread's 8 columns.
+            const int r = quarter * 32 + lane, odd = lane & 1, re = r & ~1;
+            float v[8];
+            tmem_ld8(tmem + TM_D3 + lane_off + jp, v);
             tmem_ld_wait();
 #pragma unroll
-            for (int u = 0; u < 16; ++u) {
-                store_bf16(sm + O9 + km16(jh + u, r, kDV), v[u]);
-                *reinterpret_cast<float *>(sm + O10 + km32(jh + u, r, kDV)) = to_tf32(v[u]);
+            for (int u = 0; u < 4; ++u) {
+                const float mine = odd ? v[4 + u] : v[u];
+                const float give = odd ? v[u] : v[4 + u];
+                const float other = __shfl_xor_sync(0xffffffffu, give, 1);
+                const float lo = odd ? other : mine, hi = odd ? mine : other;  // rows re, re+1
+                const int j = jp + 4 * odd + u;
+                *reinterpret_cast<uint32_t *>(sm + O9 + km16(j, re, kDV)) = pack_bf16x2(lo, hi);
+                *reinterpret_cast<float2 *>(sm + O10 + km32(j, re, kDV)) = make_float2(to_tf32(lo), to_tf32(hi));
             }
         }
         fence_proxy_async_smem();
@@ -511,27 +567,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
 
         if (quarter >= 2) {  // o rows 0..63 from lanes 64..127
             const int r = (quarter - 2) * 32 + lane;
-            float v[16];
-            tmem_ld16(tmem + TM_D3 + lane_off + jh, v);
+            float v[8];
+            tmem_ld8(tmem + TM_D3 + lane_off + jp, v);
             tmem_ld_wait();
-            if (r < len) {
-                uint4 *dst = reinterpret_cast<uint4 *>(o + ((size_t)(c0 + r) * H + h) * kD + j0 + jh);
-                float a[8], b[8];
-#pragma unroll
-                for (int u = 0; u < 8; ++u) { a[u] = v[u]; b[u] = v[8 + u]; }
-                dst[0] = pack_bf16x8(a);
-                dst[1] = pack_bf16x8(b);
-            }
+            if (r < len)
+                *reinterpret_cast<uint4 *>(o + ((size_t)(c0 + r) * H + h) * kD + j0 + jp) = pack_bf16x8(v);
         }
-        {  // state rows: S <- gamma_c (S + Ki^T u)
-            float v[16];
-            tmem_ld16(tmem + TM_D5 + lane_off + jh, v);
+        {  // state rows: S <- gamma_c (S + Ki^T u); S^T (bf16) for the next chunk, row pairs
+            float v[8];
+            tmem_ld8(tmem + TM_D5 + lane_off + jp, v);
             tmem_ld_wait();
             const float gc = s_gam[i_row];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-                S[j] = gc * (S[j] + v[j]);
-                store_bf16(sm + O7 + km16(jh + j, i_row, kDV), S[j]);
+            for (int j = 0; j < 8; ++j) S[j] = gc * (S[j] + v[j]);
+            const int odd = lane & 1, ie = i_row & ~1;
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float mine = odd ? S[4 + u] : S[u];
+                const float give = odd ? S[u] : S[4 + u];
+                const float other = __shfl_xor_sync(0xffffffffu, give, 1);
+                const float lo = odd ? other : mine, hi = odd ? mine : other;
+                *reinterpret_cast<uint32_t *>(sm + O7 + km16(jp + 4 * odd + u, ie, kDV)) = pack_bf16x2(lo, hi);
             }
         }
         fence_proxy_async_smem();
@@ -547,7 +603,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     } else {
         float *dst = final_state + st_off;
 #pragma unroll
-        for (int q = 0; q < 4; ++q)
+        for (int q = 0; q < 2; ++q)
             *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
     }
     if (decay_bad) atomicOr(status, DEV_ERR_DECAY);
