@@ -63,10 +63,16 @@ typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_F32 = 1 } kda_dtype_t;
 #define KDA_MIN_CHUNK_LOG_DECAY (-80.0f)
 
 /*
- * Bytes of device workspace kda_prefill needs for this problem (a status word
- * and a sequence schedule).  Pure host arithmetic; never fails (returns 0 only
- * for num_seqs < 0).
+ * Bytes of device workspace for the fastest kda_prefill path on this problem.
+ * For bf16 q/k/v at d_k = d_v = 128 that is the two-kernel tensor-core path: a
+ * status word, a sequence schedule, the first chunk of each sequence and one
+ * 90,624-byte record per (64-token chunk, head), at most
+ * (total_tokens / 64 + num_seqs) * num_heads records (about 1.4 KB per token
+ * per head).  For other shapes it equals KDA_PREFILL_MIN_WORKSPACE(num_seqs).
+ * Pure host arithmetic; returns 0 only for negative sizes.
  */
+#define KDA_PREFILL_MIN_WORKSPACE(num_seqs) \
+    (256u + ((((size_t)(num_seqs)) * 4u + 1u + 255u) / 256u) * 256u)
 size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
                                   int32_t d_k, int32_t d_v, kda_dtype_t dtype);
 
@@ -88,8 +94,13 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
  *  o           [total_tokens, num_heads, d_v]  dtype (written for every token)
  *  final_state [num_seqs, num_heads, d_k, d_v] fp32; may equal init_state
  *              (in-place update); a zero-length sequence gets its initial state
- *  workspace   device buffer of at least kda_prefill_workspace_size(...) bytes,
- *              owned by the caller, 256-byte aligned; reused by every call
+ *  workspace   device buffer owned by the caller, 256-byte aligned, reused by every
+ *              call.  With kda_prefill_workspace_size(...) bytes or more the bf16,
+ *              d = 128 prefill runs as two kernels (chunk-local products for all
+ *              chunks at once, then the serial state pass); with at least
+ *              KDA_PREFILL_MIN_WORKSPACE(num_seqs) bytes it runs as one fused
+ *              kernel (same results up to rounding order, slower).  Smaller
+ *              workspaces are rejected.
  *  q, k, v, log_alpha, beta and o may be NULL when total_tokens == 0.
  *
  * Device-side errors (timeout of a bounded wait, a cu_seqlens array that is not

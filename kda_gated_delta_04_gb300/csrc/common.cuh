@@ -33,6 +33,8 @@ struct PrefillProblem {
     float *final_state;
     uint32_t *status;           // workspace word
     int32_t *order;             // workspace: sequence processing order (longest first)
+    int32_t *cc;                // workspace: first chunk of each sequence [num_seqs + 1], or null
+    void *records;              // workspace: per chunk-head records of the two-kernel path, or null
     cudaStream_t stream;
 };
 
@@ -51,6 +53,9 @@ cudaError_t launch_prefill_prep(const PrefillProblem &p);
 cudaError_t launch_prefill_simt(const PrefillProblem &p);
 bool prefill_tc_supported(const PrefillProblem &p);  // bf16, d = 128, 0 < total_tokens < 2^31
 cudaError_t launch_prefill_tc(const PrefillProblem &p);
+// Two-kernel tensor-core prefill (needs p.cc and p.records).
+size_t prefill_split_records_bytes(int64_t total_tokens, int num_seqs, int num_heads);
+cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records);
 cudaError_t launch_decode(const DecodeProblem &p);
 
 // ---------------------------------------------------------------- device helpers

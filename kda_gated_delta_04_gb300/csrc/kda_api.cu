@@ -32,6 +32,22 @@ kda_status_t check_device()
 
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
+// Workspace layout: status header | sequence order | first chunk of each sequence
+// | per chunk-head records (the last two only for the two-kernel tensor-core path).
+size_t ws_order_bytes(int32_t num_seqs) { return round_up((size_t)num_seqs * sizeof(int32_t) + 1, 256); }
+size_t ws_min_bytes(int32_t num_seqs) { return kda::kWorkspaceHeader + ws_order_bytes(num_seqs); }
+size_t ws_cc_bytes(int32_t num_seqs) { return round_up(((size_t)num_seqs + 1) * sizeof(int32_t), 256); }
+bool split_shape(int64_t total_tokens, int32_t d_k, int32_t d_v, kda_dtype_t dtype)
+{
+    return dtype == KDA_DTYPE_BF16 && d_k == 128 && d_v == 128 && total_tokens > 0 &&
+           total_tokens <= 0x7fffffffll;
+}
+size_t ws_split_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
+{
+    return ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) +
+           kda::prefill_split_records_bytes(total_tokens, num_seqs, num_heads);
+}
+
 kda_status_t check_shape(int32_t d_k, int32_t d_v, kda_dtype_t dtype)
 {
     if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
@@ -47,9 +63,10 @@ extern "C" {
 size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
                                   int32_t d_k, int32_t d_v, kda_dtype_t dtype)
 {
-    (void)total_tokens; (void)num_heads; (void)d_k; (void)d_v; (void)dtype;
-    if (num_seqs < 0) return 0;
-    return kda::kWorkspaceHeader + round_up((size_t)num_seqs * sizeof(int32_t) + 1, 256);
+    if (num_seqs < 0 || total_tokens < 0 || num_heads < 0) return 0;
+    if (split_shape(total_tokens, d_k, d_v, dtype))
+        return ws_split_bytes(num_seqs, total_tokens, num_heads);
+    return ws_min_bytes(num_seqs);
 }
 
 kda_status_t kda_prefill(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -74,9 +91,7 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, const floa
         (init_state && !aligned(init_state, 16)) || (cu_seqlens && !aligned(cu_seqlens, 4)) ||
         !aligned(workspace, 256))
         return KDA_ERR_INVALID_ARG;
-    if (workspace_bytes < kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, d_k, d_v,
-                                                     dtype))
-        return KDA_ERR_INVALID_ARG;
+    if (workspace_bytes < ws_min_bytes(num_seqs)) return KDA_ERR_INVALID_ARG;
     st = check_device();
     if (st != KDA_OK) return st;
     if (num_seqs == 0) return KDA_OK;
@@ -87,14 +102,25 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, const floa
     p.num_heads = num_heads; p.d = d_k; p.dtype = dtype; p.init_state = init_state;
     p.o = o; p.final_state = final_state;
     p.status = static_cast<uint32_t *>(workspace);
-    p.order = reinterpret_cast<int32_t *>(static_cast<char *>(workspace) + kda::kWorkspaceHeader);
+    char *ws = static_cast<char *>(workspace);
+    p.order = reinterpret_cast<int32_t *>(ws + kda::kWorkspaceHeader);
     p.stream = static_cast<cudaStream_t>(stream);
+    // bf16 at d = 128 runs on the tensor cores: as the chunk / state kernel pair when the
+    // workspace holds the per-chunk records, else as the single fused kernel.  fp32 I/O
+    // (the exact path) and d = 64 run the CUDA-core chunk kernel.
+    const bool split = split_shape(total_tokens, d_k, d_v, dtype) &&
+                       workspace_bytes >= ws_split_bytes(num_seqs, total_tokens, num_heads);
+    p.cc = split ? reinterpret_cast<int32_t *>(ws + ws_min_bytes(num_seqs)) : nullptr;
+    p.records = split ? ws + ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) : nullptr;
 
     if (kda::launch_prefill_prep(p) != cudaSuccess) return KDA_ERR_CUDA;
-    // bf16 at d = 128 runs on the tensor cores; fp32 I/O (the exact path) and d = 64 run
-    // the CUDA-core chunk kernel.
-    const cudaError_t err = kda::prefill_tc_supported(p) ? kda::launch_prefill_tc(p)
-                                                         : kda::launch_prefill_simt(p);
+    cudaError_t err;
+    if (split)
+        err = kda::launch_prefill_split(p, p.cc, p.records);
+    else if (kda::prefill_tc_supported(p))
+        err = kda::launch_prefill_tc(p);
+    else
+        err = kda::launch_prefill_simt(p);
     if (err != cudaSuccess) return KDA_ERR_CUDA;
     return KDA_OK;
 }

@@ -29,10 +29,12 @@ namespace {
 constexpr int kThreads = 256;
 
 // ---------------------------------------------------------------- prep kernel
-// Clears the workspace error word, checks cu_seqlens and writes the order in
-// which sequences are processed (longest first, ties by index).
+// Clears the workspace error word, checks cu_seqlens, writes the order in
+// which sequences are processed (longest first, ties by index) and, when cc is
+// given, each sequence's first chunk in a packed chunk numbering
+// (cc[n] = sum over m < n of ceil(len_m / 64); cc[num_seqs] = all chunks).
 __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs, int64_t total,
-                                    uint32_t *status, int32_t *order)
+                                    uint32_t *status, int32_t *order, int32_t *cc)
 {
     __shared__ int bad;
     if (threadIdx.x == 0) bad = 0;
@@ -62,6 +64,40 @@ __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs
         }
         order[rank] = n;
     }
+    if (!cc) return;
+    __shared__ int warp_sums[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nwarps = blockDim.x >> 5;
+    int carry = 0;
+    for (int base = 0; base < num_seqs; base += blockDim.x) {
+        const int n = base + threadIdx.x;
+        int cnt = 0;
+        if (n < num_seqs) {
+            int64_t t0, t1;
+            seq_range(cu, n, total, t0, t1);
+            cnt = (int)((t1 - t0 + kChunk - 1) / kChunk);
+        }
+        int incl = cnt;  // inclusive scan inside the warp
+        for (int off = 1; off < 32; off <<= 1) {
+            const int t = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += t;
+        }
+        if (lane == 31) warp_sums[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            int w = lane < nwarps ? warp_sums[lane] : 0;
+            for (int off = 1; off < 32; off <<= 1) {
+                const int t = __shfl_up_sync(0xffffffffu, w, off);
+                if (lane >= off) w += t;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        const int before = warp > 0 ? warp_sums[warp - 1] : 0;
+        if (n < num_seqs) cc[n] = carry + before + incl - cnt;
+        carry += warp_sums[31];
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) cc[num_seqs] = carry;
 }
 
 // ---------------------------------------------------------------- SIMT chunk kernel
@@ -272,7 +308,7 @@ cudaError_t launch_simt(const PrefillProblem &p)
 cudaError_t launch_prefill_prep(const PrefillProblem &p)
 {
     prefill_prep_kernel<<<1, 1024, 0, p.stream>>>(p.cu_seqlens, p.num_seqs, p.total_tokens,
-                                                  p.status, p.order);
+                                                  p.status, p.order, p.cc);
     return cudaGetLastError();
 }
 

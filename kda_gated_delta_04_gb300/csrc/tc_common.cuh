@@ -1,0 +1,395 @@
+// tc_common.cuh -- pieces shared by the tensor-core prefill kernels (the fused
+// single-kernel prefill and the chunk / state kernel pair): shared-memory
+// operand layouts, packing helpers, the chunk-local phases (in-chunk decay
+// prefix, decayed operands, k-k / q-k matrices, UT solve, W epilogue) and the
+// tensor-map set-up.  Every device function here is called by all 512 threads
+// of the CTA.
+#pragma once
+
+#include <cuda.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "sm100_ptx.cuh"
+
+namespace kda {
+namespace tc {
+
+using namespace ptx;
+
+constexpr int kD = 128, kDV = 32, kC = 64, kThreads = 512;
+constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
+constexpr int kLdS = kC + 4;                 // row stride (floats) of A and T in the solve
+constexpr int kLdX = 32 + 4;                 // row stride of the block products X (<= 32 x 32)
+
+// Byte offset of element (row, col) of a K-major, 128-byte-swizzled operand
+// with `rows` rows per 64-element (bf16) or 32-element (tf32) column panel.
+__device__ __forceinline__ uint32_t km16(int row, int col, int rows)
+{
+    return (uint32_t)((col >> 6) * rows * 128 + row * 128 + ((((col & 63) >> 3) ^ (row & 7)) << 4) +
+                      ((col & 7) << 1));
+}
+__device__ __forceinline__ uint32_t km32(int row, int col, int rows)
+{
+    return (uint32_t)((col >> 5) * rows * 128 + row * 128 + ((((col & 31) >> 2) ^ (row & 7)) << 4) +
+                      ((col & 3) << 2));
+}
+
+__device__ __forceinline__ uint64_t kdesc(uint32_t addr) { return sdesc(addr, 16, 1024, kSw128B); }
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
+{
+    __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
+__device__ __forceinline__ float bf16_at(const unsigned char *p)
+{
+    return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
+}
+
+__device__ __forceinline__ void store_bf16(unsigned char *p, float x)
+{
+    *reinterpret_cast<__nv_bfloat16 *>(p) = __float2bfloat16_rn(x);
+}
+
+__device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[8])
+{
+    return make_uint4(pack_bf16x2(x[0], x[1]), pack_bf16x2(x[2], x[3]), pack_bf16x2(x[4], x[5]),
+                      pack_bf16x2(x[6], x[7]));
+}
+
+// A layout L provides byte offsets (from a 1024-aligned base) of:
+//   IN_Q, IN_K [64][128] bf16 and IN_LA [64][128] fp32 (the chunk's TMA boxes),
+//   O1  [Kg ; Qg] (later [-W ; Qg]) bf16 K-major, 128 rows x 128,
+//   O2  Ki bf16 K-major, 64 rows x 128,
+//   O3  Ki^T tf32 K-major, 128 rows (key channel) x 64,
+//   O4  T' bf16 K-major, 64 rows x 64,  AQ  Aqk bf16 K-major, 64 rows x 64,
+//   TT  T' tf32 K-major with TT_ROWS (64 or 128) rows per 32-column panel,
+//   SOLVE_A, SOLVE_T, SOLVE_X  fp32 scratch inside the input area.
+
+// ---------------------------------------------------------------- a1: prefix
+// Thread = (channel pair cp: channels 2cp, 2cp+1; row group rg: rows 8rg ..
+// 8rg+7).  Scans its 8 rows in registers and leaves the group totals in s_tot.
+template <class L>
+__device__ __forceinline__ void prefix_scan(const unsigned char *sm, int len, float *s_tot,
+                                            float2 (&gl)[8], float &gmin, float &gmax)
+{
+    const int tid = threadIdx.x, cp = tid & 63, rg = tid >> 6;
+    const float *la_in = reinterpret_cast<const float *>(sm + L::IN_LA);
+    float2 g = make_float2(0.f, 0.f);
+    gmin = 0.f;
+    gmax = 0.f;
+#pragma unroll
+    for (int rr = 0; rr < 8; ++rr) {
+        const int r = rg * 8 + rr;
+        const float2 la = r < len ? *reinterpret_cast<const float2 *>(la_in + r * kD + 2 * cp)
+                                  : make_float2(0.f, 0.f);
+        g.x += la.x;
+        g.y += la.y;
+        gl[rr] = g;
+        gmin = fminf(gmin, fminf(g.x, g.y));
+        gmax = fmaxf(gmax, fmaxf(g.x, g.y));
+    }
+    *reinterpret_cast<float2 *>(&s_tot[rg * kD + 2 * cp]) = g;
+}
+
+// ---------------------------------------------------------------- a2: operands
+// After a barrier following prefix_scan: Kg = k e^g and Qg = scale q e^g into
+// O1, Ki = k e^-g into O2 (bf16) and O3 (tf32, transposed), e^{g_last} into
+// s_gam.  Returns true when the in-chunk cumulative decay left the supported range.
+template <class L>
+__device__ __forceinline__ bool decayed_operands(unsigned char *sm, int len, const float *s_tot,
+                                                 float *s_gam, const float2 (&gl)[8], float gmin,
+                                                 float gmax)
+{
+    const int tid = threadIdx.x, lane = tid & 31, cp = tid & 63, rg = tid >> 6;
+    float2 off = make_float2(0.f, 0.f);
+    for (int q = 0; q < rg; ++q) {
+        const float2 t = *reinterpret_cast<const float2 *>(&s_tot[q * kD + 2 * cp]);
+        off.x += t.x;
+        off.y += t.y;
+    }
+    if (rg == 7)
+        *reinterpret_cast<float2 *>(&s_gam[2 * cp]) =
+            make_float2(__expf(off.x + gl[7].x), __expf(off.y + gl[7].y));
+    const bool bad = fminf(off.x, off.y) + gmin < KDA_MIN_CHUNK_LOG_DECAY ||
+                     fmaxf(off.x, off.y) + gmax > -KDA_MIN_CHUNK_LOG_DECAY;
+    const float scale = rsqrtf((float)kD);
+    // K-major swizzled byte offset of channel 2cp in a row, less the row part
+    const uint32_t pbase1 = (uint32_t)((cp >> 5) * 16384 + ((cp & 3) << 2));
+    const uint32_t pbase2 = (uint32_t)((cp >> 5) * 8192 + ((cp & 3) << 2));
+    const uint32_t pchunk = (uint32_t)((cp & 31) >> 2);
+#pragma unroll
+    for (int r4 = 0; r4 < 8; r4 += 4) {
+        float ka[4], kb[4];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const int rr = r4 + u, r = rg * 8 + rr;
+            const bool valid = r < len;
+            const float gx = off.x + gl[rr].x, gy = off.y + gl[rr].y;
+            const float ex = __expf(gx), ey = __expf(gy);
+            const float ix = __expf(-gx), iy = __expf(-gy);
+            const uint32_t qraw = valid ? *reinterpret_cast<const uint32_t *>(sm + L::IN_Q + (r * kD + 2 * cp) * 2) : 0u;
+            const uint32_t kraw = valid ? *reinterpret_cast<const uint32_t *>(sm + L::IN_K + (r * kD + 2 * cp) * 2) : 0u;
+            const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qraw));
+            const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kraw));
+            const uint32_t sw = (pchunk ^ (uint32_t)(rr & 7)) << 4;  // (r & 7) == (rr & 7)
+            *reinterpret_cast<uint32_t *>(sm + L::O1 + pbase1 + r * 128 + sw) = pack_bf16x2(kv.x * ex, kv.y * ey);
+            *reinterpret_cast<uint32_t *>(sm + L::O1 + pbase1 + (64 + r) * 128 + sw) =
+                pack_bf16x2(qv.x * (scale * ex), qv.y * (scale * ey));
+            const float kix = kv.x * ix, kiy = kv.y * iy;
+            *reinterpret_cast<uint32_t *>(sm + L::O2 + pbase2 + r * 128 + sw) = pack_bf16x2(kix, kiy);
+            ka[u] = to_tf32(kix);
+            kb[u] = to_tf32(kiy);
+        }
+        // lanes 4-7 of every 8 store their odd channel first, so each store covers
+        // 8 distinct swizzle positions (no bank conflict)
+        const int rb = rg * 8 + r4, sel = (lane >> 2) & 1;
+        const float4 va = make_float4(ka[0], ka[1], ka[2], ka[3]);
+        const float4 vb = make_float4(kb[0], kb[1], kb[2], kb[3]);
+        *reinterpret_cast<float4 *>(sm + L::O3 + km32(2 * cp + sel, rb, 128)) = sel ? vb : va;
+        *reinterpret_cast<float4 *>(sm + L::O3 + km32(2 * cp + 1 - sel, rb, 128)) = sel ? va : vb;
+    }
+    return bad;
+}
+
+// ---------------------------------------------------------------- a3: G1 + epilogue
+// D1 = [Kg ; Qg] Ki^T (M = 128, N = 64, K = 128); one thread issues.
+template <class L>
+__device__ __forceinline__ void issue_g1(uint32_t sb, uint32_t d1)
+{
+    constexpr uint32_t idesc = idesc_bf16(128, 64, false, false);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+        const uint32_t p = s >> 2, w = (s & 3) * 32;
+        mma_bf16(d1, kdesc(sb + L::O1 + p * 16384 + w), kdesc(sb + L::O2 + p * 8192 + w), idesc, s > 0);
+    }
+}
+
+// Lanes 0-63 of D1 -> A = strict-lower(beta_r . Kg Ki^T) (fp32, solve scratch);
+// lanes 64-127 -> Aqk = lower(Qg Ki^T) (bf16 operand).  16 columns per thread.
+template <class L>
+__device__ __forceinline__ void kk_epilogue(unsigned char *sm, uint32_t d1, const float *s_beta)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quarter = warp & 3, part = warp >> 2;
+    const uint32_t taddr = d1 + ((uint32_t)(quarter * 32) << 16) + part * 16;
+    float v[16];
+    tmem_ld16(taddr, v);
+    tmem_ld_wait();
+    if (quarter < 2) {
+        const int r = quarter * 32 + lane;
+        const float br = s_beta[r];
+        float *sA = reinterpret_cast<float *>(sm + L::SOLVE_A);
+#pragma unroll
+        for (int u = 0; u < 16; u += 4) {
+            const int col = part * 16 + u;
+            *reinterpret_cast<float4 *>(sA + r * kLdS + col) =
+                make_float4(col < r ? br * v[u] : 0.f, col + 1 < r ? br * v[u + 1] : 0.f,
+                            col + 2 < r ? br * v[u + 2] : 0.f, col + 3 < r ? br * v[u + 3] : 0.f);
+        }
+    } else {
+        const int r = (quarter - 2) * 32 + lane;
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[u] = (part * 16 + hh * 8 + u) <= r ? v[hh * 8 + u] : 0.f;
+            *reinterpret_cast<uint4 *>(sm + L::AQ + km16(r, part * 16 + hh * 8, 64)) = pack_bf16x8(x);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- a4: UT solve
+// T = (I + A)^-1 by recursive doubling on the unit lower-triangular system:
+// the four 16 x 16 diagonal blocks, then T_10 = -T_11 A_10 T_00 and
+// T_32 = -T_33 A_32 T_22, then T_[2:4][0:2] = -T_[2:4][2:4] A_[2:4][0:2] T_[0:2][0:2];
+// finally T' = T diag(beta) as bf16 (O4) and tf32 (TT).  Contains barriers.
+template <class L>
+__device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta)
+{
+    const int tid = threadIdx.x;
+    const float *sA = reinterpret_cast<const float *>(sm + L::SOLVE_A);
+    float *sT = reinterpret_cast<float *>(sm + L::SOLVE_T);
+    float *sX = reinterpret_cast<float *>(sm + L::SOLVE_X);
+    if (tid < 64) {  // diagonal blocks, one column per thread
+        const int b = (tid >> 4) * 16, cc = tid & 15;
+        float x[16];
+#pragma unroll
+        for (int r = 0; r < 16; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int m = 0; m < r; ++m) acc += sA[(b + r) * kLdS + b + m] * x[m];
+            x[r] = r < cc ? 0.f : (r == cc ? 1.f : -acc);
+        }
+#pragma unroll
+        for (int r = 0; r < 16; ++r) sT[(b + r) * kLdS + b + cc] = x[r];
+    }
+    __syncthreads();
+    {  // X = A_{R,R-1} T_{R-1,R-1} for (R0, C0) = (16, 0), (48, 32)
+        const int b = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
+        const int R0 = 16 + 32 * b, C0 = 32 * b;
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float a = sA[(R0 + rr) * kLdS + C0 + m], t = sT[(C0 + m) * kLdS + C0 + cc];
+            acc += m >= cc ? a * t : 0.f;
+        }
+        sX[(b * 16 + rr) * kLdX + cc] = acc;
+    }
+    __syncthreads();
+    {  // T_{R,R-1} = -T_RR X
+        const int b = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
+        const int R0 = 16 + 32 * b, C0 = 32 * b;
+        float acc = 0.f;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float t = sT[(R0 + rr) * kLdS + R0 + m], x = sX[(b * 16 + m) * kLdX + cc];
+            acc += m <= rr ? t * x : 0.f;
+        }
+        sT[(R0 + rr) * kLdS + C0 + cc] = -acc;
+    }
+    __syncthreads();
+    if (tid < 256) {  // X2 = A[32:64][0:32] T[0:32][0:32]: row r, columns c..c+3 per thread
+        const int r = tid >> 3, c = (tid & 7) * 4, k0 = c & 16;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int k4 = 0; k4 < 32; k4 += 4) {
+            if (k4 < k0) continue;
+            const float4 a = *reinterpret_cast<const float4 *>(sA + (32 + r) * kLdS + k4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 t = *reinterpret_cast<const float4 *>(sT + (k4 + u) * kLdS + c);
+                acc.x += av[u] * t.x; acc.y += av[u] * t.y; acc.z += av[u] * t.z; acc.w += av[u] * t.w;
+            }
+        }
+        *reinterpret_cast<float4 *>(sX + r * kLdX + c) = acc;
+    }
+    __syncthreads();
+    if (tid < 256) {  // T[32:64][0:32] = -T[32:64][32:64] X2
+        const int r = tid >> 3, c = (tid & 7) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int m4 = 0; m4 < 32; m4 += 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(sT + (32 + r) * kLdS + 32 + m4);
+            const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float tm = m4 + u <= r ? tv[u] : 0.f;  // T22 is lower triangular
+                const float4 x = *reinterpret_cast<const float4 *>(sX + (m4 + u) * kLdX + c);
+                acc.x += tm * x.x; acc.y += tm * x.y; acc.z += tm * x.z; acc.w += tm * x.w;
+            }
+        }
+        *reinterpret_cast<float4 *>(sT + (32 + r) * kLdS + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+    }
+    __syncthreads();
+    {  // T' = T diag(beta): bf16 (for W) and tf32 (for U~)
+        const int r = tid >> 3, s8 = (tid & 7) * 8;
+        const float4 ta = *reinterpret_cast<const float4 *>(sT + r * kLdS + s8);
+        const float4 tb = *reinterpret_cast<const float4 *>(sT + r * kLdS + s8 + 4);
+        const float4 ba = *reinterpret_cast<const float4 *>(s_beta + s8);
+        const float4 bb = *reinterpret_cast<const float4 *>(s_beta + s8 + 4);
+        const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
+        const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+        float t[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) t[u] = s8 + u <= r ? tv[u] * bv[u] : 0.f;
+        *reinterpret_cast<uint4 *>(sm + L::O4 + km16(r, s8, 64)) = pack_bf16x8(t);
+        *reinterpret_cast<float4 *>(sm + L::TT + km32(r, s8, L::TT_ROWS)) =
+            make_float4(to_tf32(t[0]), to_tf32(t[1]), to_tf32(t[2]), to_tf32(t[3]));
+        *reinterpret_cast<float4 *>(sm + L::TT + km32(r, s8 + 4, L::TT_ROWS)) =
+            make_float4(to_tf32(t[4]), to_tf32(t[5]), to_tf32(t[6]), to_tf32(t[7]));
+    }
+}
+
+// ---------------------------------------------------------------- a5: W
+// W = T' Kg (M = 64, N = 128, K = 64); Kg is read MN-major from O1 rows 0-63.
+template <class L>
+__device__ __forceinline__ void issue_gw(uint32_t sb, uint32_t dw)
+{
+    constexpr uint32_t idesc = idesc_bf16(64, 128, false, true);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+        mma_bf16(dw, kdesc(sb + L::O4 + s * 32), sdesc(sb + L::O1 + s * 2048, 16384, 1024, kSw128B),
+                 idesc, s > 0);
+}
+
+// -W into rows 0-63 of O1 (Kg no longer needed).  The M = 64 accumulator keeps
+// row 16q + l in lane l < 16 of lane quarter q; a warp takes 32 of 128 columns.
+template <class L>
+__device__ __forceinline__ void w_epilogue(unsigned char *sm, uint32_t dw)
+{
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quarter = warp & 3, part = warp >> 2;
+    const int r = quarter * 16 + (lane & 15);
+#pragma unroll
+    for (int cb = 0; cb < 32; cb += 16) {
+        float v[16];
+        tmem_ld16(dw + ((uint32_t)(quarter * 32) << 16) + part * 32 + cb, v);
+        tmem_ld_wait();
+        if (lane < 16) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = -v[hh * 8 + u];
+                *reinterpret_cast<uint4 *>(sm + L::O1 + km16(r, part * 32 + cb + hh * 8, 128)) = pack_bf16x8(x);
+            }
+        }
+    }
+}
+
+// ---------------------------------------------------------------- host side
+typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+inline EncodeTiledFn encode_fn()
+{
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// [T, H, 128] token-major tensor; box = 64 tokens x 1 head x box_x channels.
+inline bool make_map(CUtensorMap *m, CUtensorMapDataType dt, const void *ptr, int64_t T, int H,
+                     uint32_t esz, uint32_t box_x)
+{
+    EncodeTiledFn enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kD, (cuuint64_t)H, (cuuint64_t)T};
+    const cuuint64_t strides[2] = {(cuuint64_t)kD * esz, (cuuint64_t)H * kD * esz};
+    const cuuint32_t box[3] = {box_x, 1, (cuuint32_t)kC};
+    const cuuint32_t es[3] = {1, 1, 1};
+    return enc(m, dt, 3, const_cast<void *>(ptr), dims, strides, box, es,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Sets the dynamic shared memory limit of `kern` once per device.
+template <class K>
+inline cudaError_t allow_smem(K kern, int bytes, int *configured_device)
+{
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (*configured_device != dev) {
+        err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+        if (err != cudaSuccess) return err;
+        *configured_device = dev;
+    }
+    return cudaSuccess;
+}
+
+}  // namespace tc
+}  // namespace kda

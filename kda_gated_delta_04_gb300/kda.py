@@ -140,7 +140,14 @@ def _stream_handle(stream, device):
 def workspace_for(num_seqs, total_tokens, num_heads, d, dtype_code, device):
     torch = _torch()
     nbytes = kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, d, d, dtype_code)
-    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+    # every byte the kernels read is written first in the same call
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def min_workspace_bytes(num_seqs):
+    """KDA_PREFILL_MIN_WORKSPACE(num_seqs): the smallest workspace kda_prefill accepts
+    (it then runs the single fused kernel for bf16, d = 128)."""
+    return 256 + ((num_seqs * 4 + 1 + 255) // 256) * 256
 
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=None,

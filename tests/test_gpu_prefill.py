@@ -153,3 +153,21 @@ def test_repeated_runs_are_bitwise_identical():
     o2, fs2 = gpu_prefill(inp)
     np.testing.assert_array_equal(o1, o2)
     np.testing.assert_array_equal(fs1, fs2)
+
+
+@pytest.mark.parametrize("w", [SMALL[1], SMALL[2], synth.PREFILL_4K], ids=lambda w: w.name)
+def test_single_kernel_path_with_minimal_workspace(w):
+    """With only KDA_PREFILL_MIN_WORKSPACE bytes the bf16 d=128 prefill runs as one fused
+    kernel; it must meet the same bar, and agree with the two-kernel path."""
+    heads = None if w.num_heads <= 4 else [0, 17]
+    inp = synth.prefill_inputs(w, heads=heads)
+    d = to_device(inp)
+    N = d["cu_seqlens"].numel() - 1
+    ws = torch.empty(kda.min_workspace_bytes(N), dtype=torch.uint8, device="cuda")
+    o1, f1 = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
+                         d["init_state"], workspace=ws, check_status=True)
+    o2, f2 = gpu_prefill(inp)  # default (largest) workspace: two-kernel path
+    o1, f1 = synth.to_f64(o1), synth.to_f64(f1)
+    o_ref, fs_ref = oracle_prefill(inp)
+    assert_parity(o1, f1, o_ref, fs_ref, "bf16", w.name + " (single kernel)")
+    assert np.abs(o1 - o2).max() < 2e-3 and relF(f1, f2) < 2e-4
