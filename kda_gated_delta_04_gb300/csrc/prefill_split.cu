@@ -37,19 +37,20 @@ constexpr uint32_t R_GM = 90112;   // e^{g_last}, 128 fp32
 constexpr uint32_t kRecBytes = 90624;
 static_assert(kRecBytes % 16 == 0, "records are moved by bulk copies");
 
+// Chunk kernel: 256 threads and 89 KB of shared memory, so two CTAs share an SM
+// and hide each other's latencies.  Only the operands its own MMAs read live in
+// shared memory; Ki^T, Aqk, T' (tf32) and e^{g_last} go straight to the record.
+constexpr int kChunkThreads = 256;
 struct ChunkLayout {
-    static constexpr uint32_t IN_Q = 0, IN_K = 16384, IN_LA = 32768;  // TMA boxes
-    static constexpr uint32_t REC = 65536;                            // record image
-    static constexpr uint32_t O1 = REC + R_O1, O3 = REC + R_O3, TT = REC + R_TT, AQ = REC + R_AQ;
-    static constexpr uint32_t GM = REC + R_GM;
-    static constexpr int TT_ROWS = 64;
-    static constexpr uint32_t O2 = 156672;   // Ki bf16, 64 rows x 128
-    static constexpr uint32_t O4 = 172032;   // T' bf16, 64 rows x 64
+    static constexpr uint32_t IN_Q = 0, IN_K = 16384;  // TMA boxes
+    static constexpr uint32_t O2 = 32768;   // Ki bf16, 64 rows x 128
+    static constexpr uint32_t O1 = 49152;   // [Kg ; Qg] -> [-W ; Qg] (the record's first image)
+    static constexpr uint32_t O4 = 81920;   // T' bf16, 64 rows x 64 (prefix group totals before)
+    // solve scratch over the input boxes and O2, both dead by then
     static constexpr uint32_t SOLVE_A = 0, SOLVE_T = kC * kLdS * 4, SOLVE_X = 2 * kC * kLdS * 4;
-    static constexpr uint32_t USED = 180224;
+    static constexpr uint32_t USED = 90112;
 };
-static_assert(ChunkLayout::GM + 512 <= ChunkLayout::O2, "record image overlaps O2");
-static_assert(ChunkLayout::SOLVE_X + 32 * kLdX * 4 <= ChunkLayout::REC, "solve scratch in input area");
+static_assert(ChunkLayout::SOLVE_X + 32 * kLdX * 4 <= ChunkLayout::O1, "solve scratch overlaps O1");
 
 struct StateLayout {
     static constexpr uint32_t STAGE = 91136;  // record + padding to 1024 bytes
@@ -68,14 +69,15 @@ constexpr uint32_t kChunkSmem = ChunkLayout::USED + 1024;
 constexpr uint32_t kStateSmem = StateLayout::USED + 1024;
 
 // ============================================================== chunk kernel
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(kChunkThreads, 2)
 prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_la, const float *__restrict__ beta,
+                     const float *__restrict__ log_alpha, const float *__restrict__ beta,
                      const int32_t *__restrict__ cu, int64_t total, int H, int num_seqs,
                      const int32_t *__restrict__ cc, unsigned char *__restrict__ records,
                      uint32_t *status)
 {
     using L = ChunkLayout;
+    constexpr int NT = kChunkThreads;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar_tma, bar_mma;
     __shared__ uint32_t tmem_holder;
@@ -93,6 +95,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     seq_range(cu, n, total, t0, t1);
     const int64_t c0 = t0 + (int64_t)(g - cc[n]) * kC;
     const int len = (t1 - c0) < kC ? (int)(t1 - c0) : kC;
+    unsigned char *rec = records + ((size_t)g * H + h) * kRecBytes;
 
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
@@ -101,30 +104,31 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         mbar_init(&bar_tma, 1);
         mbar_init(&bar_mma, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&bar_tma, 16384 + 16384 + 32768);
+        mbar_arrive_expect_tx(&bar_tma, 16384 + 16384);
         tma_load_3d(sm + L::IN_Q, &tm_q, &bar_tma, 0, h, (int)c0);
         tma_load_3d(sm + L::IN_K, &tm_k, &bar_tma, 0, h, (int)c0);
-        tma_load_3d(sm + L::IN_LA, &tm_la, &bar_tma, 0, h, (int)c0);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_holder, 256);
         tmem_relinquish();
     }
     if (tid < kC) s_beta[tid] = tid < len ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
+    // a1: the in-chunk decay prefix reads log_alpha straight from global memory,
+    // overlapping the q/k copies
+    float *s_tot = reinterpret_cast<float *>(sm + L::O4);
+    float2 gl[4096 / NT];
+    float gmin, gmax;
+    prefix_scan<NT>(log_alpha + ((size_t)c0 * H + h) * kD, H * kD, len, s_tot, gl, gmin, gmax);
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_holder, tD1 = tmem, tDW = tmem + 64;
-    float *s_tot = reinterpret_cast<float *>(sm + L::O4);  // idle until the solve writes T'
     bool timed_out = false, tma_pending = true, mma_pending = false, decay_bad = false;
     do {
         bool ok = mbar_wait_ns(&bar_tma, 0, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tma_pending = false;
-        float2 gl[8];
-        float gmin, gmax;
-        prefix_scan<L>(sm, len, s_tot, gl, gmin, gmax);
-        __syncthreads();
-        decay_bad = decayed_operands<L>(sm, len, s_tot, reinterpret_cast<float *>(sm + L::GM), gl, gmin, gmax);
+        decay_bad = decayed_operands<L, NT>(sm, len, s_tot, rec + R_O3,
+                                            reinterpret_cast<float *>(rec + R_GM), gl, gmin, gmax);
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
@@ -137,10 +141,10 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         mma_pending = false;
         tc_fence_after_sync();
-        kk_epilogue<L>(sm, tD1, s_beta);
+        kk_epilogue<L, NT>(sm, tD1, s_beta, rec + R_AQ);
         tc_fence_before_sync();
         __syncthreads();
-        solve_ut<L>(sm, s_beta);
+        solve_ut<L, NT>(sm, s_beta, rec + R_TT, 64);
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
@@ -153,12 +157,12 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         mma_pending = false;
         tc_fence_after_sync();
-        w_epilogue<L>(sm, tDW);
+        w_epilogue<L, NT>(sm, tDW);
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
-        if (tid == 0) {  // the record: one bulk copy of the contiguous operand images
-            bulk_store(records + ((size_t)g * H + h) * kRecBytes, sm + L::REC, kRecBytes);
+        if (tid == 0) {  // [-W ; Qg] image of the record
+            bulk_store(rec + R_O1, sm + L::O1, 32768);
             bulk_commit();
             bulk_wait_all();
         }
@@ -402,17 +406,15 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     if (err != cudaSuccess) return err;
     err = allow_smem(prefill_state_kernel, (int)kStateSmem, &dev_state);
     if (err != cudaSuccess) return err;
-    CUtensorMap tq, tk, tla, tv;
+    CUtensorMap tq, tk, tv;
     if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, p.total_tokens, p.num_heads, 2, kD) ||
         !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, p.total_tokens, p.num_heads, 2, kD) ||
-        !make_map(&tla, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.log_alpha, p.total_tokens, p.num_heads, 4,
-                  kD) ||
         !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kDV))
         return cudaErrorInvalidValue;
     const int64_t chunk_bound = p.total_tokens / kC + p.num_seqs;
     dim3 grid_a((unsigned)chunk_bound, p.num_heads);
-    prefill_chunk_kernel<<<grid_a, kThreads, kChunkSmem, p.stream>>>(
-        tq, tk, tla, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.num_seqs, cc,
+    prefill_chunk_kernel<<<grid_a, kChunkThreads, kChunkSmem, p.stream>>>(
+        tq, tk, p.log_alpha, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.num_seqs, cc,
         static_cast<unsigned char *>(records), p.status);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;

@@ -168,7 +168,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // ---------------------------------------------------------- a1, a2
         float2 gl[8];
         float gmin, gmax;
-        prefix_scan<L>(sm, len, s_tot, gl, gmin, gmax);
+        prefix_scan<kThreads>(reinterpret_cast<const float *>(sm + L::IN_LA), kD, len, s_tot, gl, gmin, gmax);
         if (tid < kC) {
             s_beta[tid] = beta_next;
             const int64_t cn = c0 + kC;  // next chunk
@@ -183,7 +183,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             *reinterpret_cast<float4 *>(sm + L::O6 + km32(j, s4, kDV)) = make_float4(x[0], x[1], x[2], x[3]);
         }
         __syncthreads();
-        if (decayed_operands<L>(sm, len, s_tot, s_gam, gl, gmin, gmax)) decay_bad = true;
+        if (decayed_operands<L, kThreads>(sm, len, s_tot, sm + L::O3, s_gam, gl, gmin, gmax)) decay_bad = true;
         fence_proxy_async_smem();
         __syncthreads();
 
@@ -197,12 +197,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (__syncthreads_or(!ok)) { timed_out = true; mma_pending = true; break; }
         ph_mma ^= 1;
         tc_fence_after_sync();
-        kk_epilogue<L>(sm, tmem + TM_D1, s_beta);
+        kk_epilogue<L, kThreads>(sm, tmem + TM_D1, s_beta, sm + L::AQ);
         tc_fence_before_sync();
         __syncthreads();
 
         // ---------------------------------------------------------- a4: T = (I + A)^-1
-        solve_ut<L>(sm, s_beta);
+        solve_ut<L, kThreads>(sm, s_beta, sm + L::TT, L::TT_ROWS);
         fence_proxy_async_smem();
         __syncthreads();
 
@@ -226,7 +226,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (__syncthreads_or(!ok)) { timed_out = true; mma_pending = true; break; }
         ph_mma ^= 1;
         tc_fence_after_sync();
-        w_epilogue<L>(sm, tmem + TM_DW);
+        w_epilogue<L, kThreads>(sm, tmem + TM_DW);
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();

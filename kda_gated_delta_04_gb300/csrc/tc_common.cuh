@@ -2,8 +2,8 @@
 // single-kernel prefill and the chunk / state kernel pair): shared-memory
 // operand layouts, packing helpers, the chunk-local phases (in-chunk decay
 // prefix, decayed operands, k-k / q-k matrices, UT solve, W epilogue) and the
-// tensor-map set-up.  Every device function here is called by all 512 threads
-// of the CTA.
+// tensor-map set-up.  Every device function here is called by all threads of
+// the CTA (NT = 256 or 512).
 #pragma once
 
 #include <cuda.h>
@@ -61,33 +61,40 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[8])
 }
 
 // A layout L provides byte offsets (from a 1024-aligned base) of:
-//   IN_Q, IN_K [64][128] bf16 and IN_LA [64][128] fp32 (the chunk's TMA boxes),
+//   IN_Q, IN_K [64][128] bf16 (the chunk's TMA boxes),
 //   O1  [Kg ; Qg] (later [-W ; Qg]) bf16 K-major, 128 rows x 128,
 //   O2  Ki bf16 K-major, 64 rows x 128,
-//   O3  Ki^T tf32 K-major, 128 rows (key channel) x 64,
-//   O4  T' bf16 K-major, 64 rows x 64,  AQ  Aqk bf16 K-major, 64 rows x 64,
-//   TT  T' tf32 K-major with TT_ROWS (64 or 128) rows per 32-column panel,
-//   SOLVE_A, SOLVE_T, SOLVE_X  fp32 scratch inside the input area.
+//   O4  T' bf16 K-major, 64 rows x 64,
+//   SOLVE_A, SOLVE_T, SOLVE_X  fp32 scratch over buffers that are dead by the solve.
+// Operands that no MMA of the calling kernel reads (Ki^T tf32, Aqk, T' tf32,
+// e^{g_last}) go to caller-given generic pointers: shared memory in the fused
+// kernel, the chunk's record in global memory in the chunk kernel.  The byte
+// images are the same either way.  NT (256 or 512) is the CTA size.
 
 // ---------------------------------------------------------------- a1: prefix
-// Thread = (channel pair cp: channels 2cp, 2cp+1; row group rg: rows 8rg ..
-// 8rg+7).  Scans its 8 rows in registers and leaves the group totals in s_tot.
-template <class L>
-__device__ __forceinline__ void prefix_scan(const unsigned char *sm, int len, float *s_tot,
-                                            float2 (&gl)[8], float &gmin, float &gmax)
+// Thread = (channel pair cp: channels 2cp, 2cp+1; row group rg of R = 4096/NT
+// rows).  Scans its rows of log_alpha (row stride `la_stride` floats, shared or
+// global memory) in registers and leaves the group totals in s_tot.
+template <int NT>
+__device__ __forceinline__ void prefix_scan(const float *la, int la_stride, int len, float *s_tot,
+                                            float2 (&gl)[4096 / NT], float &gmin, float &gmax)
 {
+    constexpr int R = 4096 / NT;
     const int tid = threadIdx.x, cp = tid & 63, rg = tid >> 6;
-    const float *la_in = reinterpret_cast<const float *>(sm + L::IN_LA);
     float2 g = make_float2(0.f, 0.f);
     gmin = 0.f;
     gmax = 0.f;
+    float2 x[R];
 #pragma unroll
-    for (int rr = 0; rr < 8; ++rr) {
-        const int r = rg * 8 + rr;
-        const float2 la = r < len ? *reinterpret_cast<const float2 *>(la_in + r * kD + 2 * cp)
-                                  : make_float2(0.f, 0.f);
-        g.x += la.x;
-        g.y += la.y;
+    for (int rr = 0; rr < R; ++rr) {  // all loads first (they may come from global memory)
+        const int r = rg * R + rr;
+        x[rr] = r < len ? *reinterpret_cast<const float2 *>(la + (size_t)r * la_stride + 2 * cp)
+                        : make_float2(0.f, 0.f);
+    }
+#pragma unroll
+    for (int rr = 0; rr < R; ++rr) {
+        g.x += x[rr].x;
+        g.y += x[rr].y;
         gl[rr] = g;
         gmin = fminf(gmin, fminf(g.x, g.y));
         gmax = fmaxf(gmax, fmaxf(g.x, g.y));
@@ -97,13 +104,15 @@ __device__ __forceinline__ void prefix_scan(const unsigned char *sm, int len, fl
 
 // ---------------------------------------------------------------- a2: operands
 // After a barrier following prefix_scan: Kg = k e^g and Qg = scale q e^g into
-// O1, Ki = k e^-g into O2 (bf16) and O3 (tf32, transposed), e^{g_last} into
-// s_gam.  Returns true when the in-chunk cumulative decay left the supported range.
-template <class L>
+// O1, Ki = k e^-g into O2 (bf16) and into o3 (tf32, transposed, K-major
+// 128 rows x 64), e^{g_last} into gam[128].  Returns true when the in-chunk
+// cumulative decay left the supported range.
+template <class L, int NT>
 __device__ __forceinline__ bool decayed_operands(unsigned char *sm, int len, const float *s_tot,
-                                                 float *s_gam, const float2 (&gl)[8], float gmin,
-                                                 float gmax)
+                                                 unsigned char *o3, float *gam,
+                                                 const float2 (&gl)[4096 / NT], float gmin, float gmax)
 {
+    constexpr int R = 4096 / NT, G = NT / 64;
     const int tid = threadIdx.x, lane = tid & 31, cp = tid & 63, rg = tid >> 6;
     float2 off = make_float2(0.f, 0.f);
     for (int q = 0; q < rg; ++q) {
@@ -111,9 +120,9 @@ __device__ __forceinline__ bool decayed_operands(unsigned char *sm, int len, con
         off.x += t.x;
         off.y += t.y;
     }
-    if (rg == 7)
-        *reinterpret_cast<float2 *>(&s_gam[2 * cp]) =
-            make_float2(__expf(off.x + gl[7].x), __expf(off.y + gl[7].y));
+    if (rg == G - 1)
+        *reinterpret_cast<float2 *>(&gam[2 * cp]) =
+            make_float2(__expf(off.x + gl[R - 1].x), __expf(off.y + gl[R - 1].y));
     const bool bad = fminf(off.x, off.y) + gmin < KDA_MIN_CHUNK_LOG_DECAY ||
                      fmaxf(off.x, off.y) + gmax > -KDA_MIN_CHUNK_LOG_DECAY;
     const float scale = rsqrtf((float)kD);
@@ -122,11 +131,11 @@ __device__ __forceinline__ bool decayed_operands(unsigned char *sm, int len, con
     const uint32_t pbase2 = (uint32_t)((cp >> 5) * 8192 + ((cp & 3) << 2));
     const uint32_t pchunk = (uint32_t)((cp & 31) >> 2);
 #pragma unroll
-    for (int r4 = 0; r4 < 8; r4 += 4) {
+    for (int r4 = 0; r4 < R; r4 += 4) {
         float ka[4], kb[4];
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-            const int rr = r4 + u, r = rg * 8 + rr;
+            const int rr = r4 + u, r = rg * R + rr;
             const bool valid = r < len;
             const float gx = off.x + gl[rr].x, gy = off.y + gl[rr].y;
             const float ex = __expf(gx), ey = __expf(gy);
@@ -145,12 +154,12 @@ __device__ __forceinline__ bool decayed_operands(unsigned char *sm, int len, con
             kb[u] = to_tf32(kiy);
         }
         // lanes 4-7 of every 8 store their odd channel first, so each store covers
-        // 8 distinct swizzle positions (no bank conflict)
-        const int rb = rg * 8 + r4, sel = (lane >> 2) & 1;
+        // 8 distinct swizzle positions (no bank conflict in shared memory)
+        const int rb = rg * R + r4, sel = (lane >> 2) & 1;
         const float4 va = make_float4(ka[0], ka[1], ka[2], ka[3]);
         const float4 vb = make_float4(kb[0], kb[1], kb[2], kb[3]);
-        *reinterpret_cast<float4 *>(sm + L::O3 + km32(2 * cp + sel, rb, 128)) = sel ? vb : va;
-        *reinterpret_cast<float4 *>(sm + L::O3 + km32(2 * cp + 1 - sel, rb, 128)) = sel ? va : vb;
+        *reinterpret_cast<float4 *>(o3 + km32(2 * cp + sel, rb, 128)) = sel ? vb : va;
+        *reinterpret_cast<float4 *>(o3 + km32(2 * cp + 1 - sel, rb, 128)) = sel ? va : vb;
     }
     return bad;
 }
@@ -169,34 +178,39 @@ __device__ __forceinline__ void issue_g1(uint32_t sb, uint32_t d1)
 }
 
 // Lanes 0-63 of D1 -> A = strict-lower(beta_r . Kg Ki^T) (fp32, solve scratch);
-// lanes 64-127 -> Aqk = lower(Qg Ki^T) (bf16 operand).  16 columns per thread.
-template <class L>
-__device__ __forceinline__ void kk_epilogue(unsigned char *sm, uint32_t d1, const float *s_beta)
+// lanes 64-127 -> Aqk = lower(Qg Ki^T) (bf16 operand image at aq).
+template <class L, int NT>
+__device__ __forceinline__ void kk_epilogue(unsigned char *sm, uint32_t d1, const float *s_beta,
+                                            unsigned char *aq)
 {
+    constexpr int CW = 64 / (NT / 128);  // columns per thread
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quarter = warp & 3, part = warp >> 2;
-    const uint32_t taddr = d1 + ((uint32_t)(quarter * 32) << 16) + part * 16;
-    float v[16];
-    tmem_ld16(taddr, v);
-    tmem_ld_wait();
-    if (quarter < 2) {
-        const int r = quarter * 32 + lane;
-        const float br = s_beta[r];
-        float *sA = reinterpret_cast<float *>(sm + L::SOLVE_A);
 #pragma unroll
-        for (int u = 0; u < 16; u += 4) {
-            const int col = part * 16 + u;
-            *reinterpret_cast<float4 *>(sA + r * kLdS + col) =
-                make_float4(col < r ? br * v[u] : 0.f, col + 1 < r ? br * v[u + 1] : 0.f,
-                            col + 2 < r ? br * v[u + 2] : 0.f, col + 3 < r ? br * v[u + 3] : 0.f);
-        }
-    } else {
-        const int r = (quarter - 2) * 32 + lane;
+    for (int cb = 0; cb < CW; cb += 16) {
+        const int c0 = part * CW + cb;
+        float v[16];
+        tmem_ld16(d1 + ((uint32_t)(quarter * 32) << 16) + c0, v);
+        tmem_ld_wait();
+        if (quarter < 2) {
+            const int r = quarter * 32 + lane;
+            const float br = s_beta[r];
+            float *sA = reinterpret_cast<float *>(sm + L::SOLVE_A);
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            float x[8];
+            for (int u = 0; u < 16; u += 4) {
+                const int col = c0 + u;
+                *reinterpret_cast<float4 *>(sA + r * kLdS + col) =
+                    make_float4(col < r ? br * v[u] : 0.f, col + 1 < r ? br * v[u + 1] : 0.f,
+                                col + 2 < r ? br * v[u + 2] : 0.f, col + 3 < r ? br * v[u + 3] : 0.f);
+            }
+        } else {
+            const int r = (quarter - 2) * 32 + lane;
 #pragma unroll
-            for (int u = 0; u < 8; ++u) x[u] = (part * 16 + hh * 8 + u) <= r ? v[hh * 8 + u] : 0.f;
-            *reinterpret_cast<uint4 *>(sm + L::AQ + km16(r, part * 16 + hh * 8, 64)) = pack_bf16x8(x);
+            for (int hh = 0; hh < 2; ++hh) {
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = (c0 + hh * 8 + u) <= r ? v[hh * 8 + u] : 0.f;
+                *reinterpret_cast<uint4 *>(aq + km16(r, c0 + hh * 8, 64)) = pack_bf16x8(x);
+            }
         }
     }
 }
@@ -205,9 +219,11 @@ __device__ __forceinline__ void kk_epilogue(unsigned char *sm, uint32_t d1, cons
 // T = (I + A)^-1 by recursive doubling on the unit lower-triangular system:
 // the four 16 x 16 diagonal blocks, then T_10 = -T_11 A_10 T_00 and
 // T_32 = -T_33 A_32 T_22, then T_[2:4][0:2] = -T_[2:4][2:4] A_[2:4][0:2] T_[0:2][0:2];
-// finally T' = T diag(beta) as bf16 (O4) and tf32 (TT).  Contains barriers.
-template <class L>
-__device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta)
+// finally T' = T diag(beta) as bf16 (O4) and tf32 (image at tt with tt_rows rows
+// per 32-column panel).  Contains barriers.
+template <class L, int NT>
+__device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta, unsigned char *tt,
+                                         int tt_rows)
 {
     const int tid = threadIdx.x;
     const float *sA = reinterpret_cast<const float *>(sm + L::SOLVE_A);
@@ -227,8 +243,9 @@ __device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta)
         for (int r = 0; r < 16; ++r) sT[(b + r) * kLdS + b + cc] = x[r];
     }
     __syncthreads();
-    {  // X = A_{R,R-1} T_{R-1,R-1} for (R0, C0) = (16, 0), (48, 32)
-        const int b = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
+#pragma unroll
+    for (int e = tid; e < 512; e += NT) {  // X = A_{R,R-1} T_{R-1,R-1} for (R0, C0) = (16, 0), (48, 32)
+        const int b = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
         const int R0 = 16 + 32 * b, C0 = 32 * b;
         float acc = 0.f;
 #pragma unroll
@@ -239,8 +256,9 @@ __device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta)
         sX[(b * 16 + rr) * kLdX + cc] = acc;
     }
     __syncthreads();
-    {  // T_{R,R-1} = -T_RR X
-        const int b = tid >> 8, rr = (tid >> 4) & 15, cc = tid & 15;
+#pragma unroll
+    for (int e = tid; e < 512; e += NT) {  // T_{R,R-1} = -T_RR X
+        const int b = e >> 8, rr = (e >> 4) & 15, cc = e & 15;
         const int R0 = 16 + 32 * b, C0 = 32 * b;
         float acc = 0.f;
 #pragma unroll
@@ -285,8 +303,9 @@ __device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta)
         *reinterpret_cast<float4 *>(sT + (32 + r) * kLdS + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
-    {  // T' = T diag(beta): bf16 (for W) and tf32 (for U~)
-        const int r = tid >> 3, s8 = (tid & 7) * 8;
+#pragma unroll
+    for (int e = tid; e < 512; e += NT) {  // T' = T diag(beta): bf16 (for W) and tf32 (for U~)
+        const int r = e >> 3, s8 = (e & 7) * 8;
         const float4 ta = *reinterpret_cast<const float4 *>(sT + r * kLdS + s8);
         const float4 tb = *reinterpret_cast<const float4 *>(sT + r * kLdS + s8 + 4);
         const float4 ba = *reinterpret_cast<const float4 *>(s_beta + s8);
@@ -297,9 +316,9 @@ __device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta)
 #pragma unroll
         for (int u = 0; u < 8; ++u) t[u] = s8 + u <= r ? tv[u] * bv[u] : 0.f;
         *reinterpret_cast<uint4 *>(sm + L::O4 + km16(r, s8, 64)) = pack_bf16x8(t);
-        *reinterpret_cast<float4 *>(sm + L::TT + km32(r, s8, L::TT_ROWS)) =
+        *reinterpret_cast<float4 *>(tt + km32(r, s8, tt_rows)) =
             make_float4(to_tf32(t[0]), to_tf32(t[1]), to_tf32(t[2]), to_tf32(t[3]));
-        *reinterpret_cast<float4 *>(sm + L::TT + km32(r, s8 + 4, L::TT_ROWS)) =
+        *reinterpret_cast<float4 *>(tt + km32(r, s8 + 4, tt_rows)) =
             make_float4(to_tf32(t[4]), to_tf32(t[5]), to_tf32(t[6]), to_tf32(t[7]));
     }
 }
@@ -317,16 +336,17 @@ __device__ __forceinline__ void issue_gw(uint32_t sb, uint32_t dw)
 }
 
 // -W into rows 0-63 of O1 (Kg no longer needed).  The M = 64 accumulator keeps
-// row 16q + l in lane l < 16 of lane quarter q; a warp takes 32 of 128 columns.
-template <class L>
+// row 16q + l in lane l < 16 of lane quarter q; a warp takes 128/(NT/128) columns.
+template <class L, int NT>
 __device__ __forceinline__ void w_epilogue(unsigned char *sm, uint32_t dw)
 {
+    constexpr int CW = 128 / (NT / 128);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quarter = warp & 3, part = warp >> 2;
     const int r = quarter * 16 + (lane & 15);
 #pragma unroll
-    for (int cb = 0; cb < 32; cb += 16) {
+    for (int cb = 0; cb < CW; cb += 16) {
         float v[16];
-        tmem_ld16(dw + ((uint32_t)(quarter * 32) << 16) + part * 32 + cb, v);
+        tmem_ld16(dw + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
         tmem_ld_wait();
         if (lane < 16) {
 #pragma unroll
@@ -334,7 +354,7 @@ __device__ __forceinline__ void w_epilogue(unsigned char *sm, uint32_t dw)
                 float x[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) x[u] = -v[hh * 8 + u];
-                *reinterpret_cast<uint4 *>(sm + L::O1 + km16(r, part * 32 + cb + hh * 8, 128)) = pack_bf16x8(x);
+                *reinterpret_cast<uint4 *>(sm + L::O1 + km16(r, part * CW + cb + hh * 8, 128)) = pack_bf16x8(x);
             }
         }
     }
