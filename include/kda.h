@@ -50,7 +50,9 @@ typedef enum {
     KDA_ERR_UNSUPPORTED = 2,  /* valid but not implemented shape / dtype / device       */
     KDA_ERR_CUDA = 3,         /* a CUDA runtime call or kernel launch failed            */
     KDA_ERR_TIMEOUT = 4,      /* a bounded device-side wait expired (no hang, no trap)  */
-    KDA_ERR_DECAY_RANGE = 5   /* a chunk's cumulative log-decay left the supported range */
+    KDA_ERR_DECAY_RANGE = 5,  /* a chunk's cumulative log-decay left the supported range */
+    KDA_ERR_VALUE_RANGE = 6   /* a value the bf16 d = 128 fast path holds in fp16 left    */
+                              /* the fp16 range (|x| > 65504, or not finite)            */
 } kda_status_t;
 
 typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_F32 = 1 } kda_dtype_t;
@@ -66,8 +68,8 @@ typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_F32 = 1 } kda_dtype_t;
  * Bytes of device workspace for the fastest kda_prefill path on this problem.
  * For bf16 q/k/v at d_k = d_v = 128 that is the two-kernel tensor-core path: a
  * status word, a sequence schedule, the first chunk of each sequence and one
- * 90,624-byte record per (64-token chunk, head), at most
- * (total_tokens / 64 + num_seqs) * num_heads records (about 1.4 KB per token
+ * 74,240-byte record per (64-token chunk, head), at most
+ * (total_tokens / 64 + num_seqs) * num_heads records (about 1.2 KB per token
  * per head).  For other shapes it equals KDA_PREFILL_MIN_WORKSPACE(num_seqs).
  * Pure host arithmetic; returns 0 only for negative sizes.
  */
@@ -104,7 +106,9 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
  *  q, k, v, log_alpha, beta and o may be NULL when total_tokens == 0.
  *
  * Device-side errors (timeout of a bounded wait, a cu_seqlens array that is not
- * a valid prefix sum, a decay outside the supported range) do not fault: the
+ * a valid prefix sum, a decay outside the supported range, and on the two-kernel
+ * path a v value or a chunk-local product outside the fp16 range, which that
+ * path keeps in fp16) do not fault: the
  * kernels clamp every access to the buffers, finish, and record the error in the
  * workspace.  Each call clears the record first; read it with
  * kda_read_device_status.  Calls that share a workspace must be ordered (same
@@ -175,6 +179,7 @@ kda_status_t kda_read_device_status(void *workspace, void *stream);
 #define KDA_DEVICE_ERR_SEQLENS 1u /* cu_seqlens is not a prefix sum ending at total_tokens */
 #define KDA_DEVICE_ERR_TIMEOUT 2u /* a bounded device-side wait expired                   */
 #define KDA_DEVICE_ERR_DECAY 4u   /* a chunk's cumulative log-decay left the supported range */
+#define KDA_DEVICE_ERR_RANGE 8u   /* a value held in fp16 left the fp16 range (two-kernel path) */
 kda_status_t kda_prefill_no_alloc(const void *q, const void *k, const void *v,
                                   const float *log_alpha, const float *beta,
                                   const int32_t *cu_seqlens, int32_t num_seqs,

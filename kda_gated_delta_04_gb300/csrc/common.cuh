@@ -14,6 +14,7 @@ enum : uint32_t {
     DEV_ERR_SEQLENS = 1u,  // cu_seqlens is not a prefix sum ending at total_tokens
     DEV_ERR_TIMEOUT = 2u,  // a bounded mbarrier / flag wait gave up
     DEV_ERR_DECAY = 4u,    // |in-chunk cumulative log-decay| exceeded the supported range
+    DEV_ERR_RANGE = 8u,    // a value kept in fp16 left the fp16 range
 };
 
 constexpr int kChunk = KDA_CHUNK;

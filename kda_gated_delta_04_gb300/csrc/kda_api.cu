@@ -37,10 +37,13 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 size_t ws_order_bytes(int32_t num_seqs) { return round_up((size_t)num_seqs * sizeof(int32_t) + 1, 256); }
 size_t ws_min_bytes(int32_t num_seqs) { return kda::kWorkspaceHeader + ws_order_bytes(num_seqs); }
 size_t ws_cc_bytes(int32_t num_seqs) { return round_up(((size_t)num_seqs + 1) * sizeof(int32_t), 256); }
-bool split_shape(int64_t total_tokens, int32_t d_k, int32_t d_v, kda_dtype_t dtype)
+bool split_shape(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                 kda_dtype_t dtype)
 {
+    // the chunk kernel's one-dimensional grid holds (chunks + sequences) x heads CTAs
     return dtype == KDA_DTYPE_BF16 && d_k == 128 && d_v == 128 && total_tokens > 0 &&
-           total_tokens <= 0x7fffffffll;
+           total_tokens <= 0x7fffffffll &&
+           (total_tokens / KDA_CHUNK + num_seqs) * (int64_t)num_heads <= 0x7fffffffll;
 }
 size_t ws_split_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
 {
@@ -64,7 +67,7 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
                                   int32_t d_k, int32_t d_v, kda_dtype_t dtype)
 {
     if (num_seqs < 0 || total_tokens < 0 || num_heads < 0) return 0;
-    if (split_shape(total_tokens, d_k, d_v, dtype))
+    if (split_shape(num_seqs, total_tokens, num_heads, d_k, d_v, dtype))
         return ws_split_bytes(num_seqs, total_tokens, num_heads);
     return ws_min_bytes(num_seqs);
 }
@@ -108,7 +111,7 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, const floa
     // bf16 at d = 128 runs on the tensor cores: as the chunk / state kernel pair when the
     // workspace holds the per-chunk records, else as the single fused kernel.  fp32 I/O
     // (the exact path) and d = 64 run the CUDA-core chunk kernel.
-    const bool split = split_shape(total_tokens, d_k, d_v, dtype) &&
+    const bool split = split_shape(num_seqs, total_tokens, num_heads, d_k, d_v, dtype) &&
                        workspace_bytes >= ws_split_bytes(num_seqs, total_tokens, num_heads);
     p.cc = split ? reinterpret_cast<int32_t *>(ws + ws_min_bytes(num_seqs)) : nullptr;
     p.records = split ? ws + ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) : nullptr;
@@ -159,6 +162,7 @@ kda_status_t kda_read_device_status(void *workspace, void *stream)
     if (word & kda::DEV_ERR_SEQLENS) return KDA_ERR_INVALID_ARG;
     if (word & kda::DEV_ERR_TIMEOUT) return KDA_ERR_TIMEOUT;
     if (word & kda::DEV_ERR_DECAY) return KDA_ERR_DECAY_RANGE;
+    if (word & kda::DEV_ERR_RANGE) return KDA_ERR_VALUE_RANGE;
     return KDA_OK;
 }
 
@@ -172,6 +176,8 @@ const char *kda_status_string(kda_status_t status)
     case KDA_ERR_TIMEOUT: return "KDA_ERR_TIMEOUT: a bounded device-side wait expired";
     case KDA_ERR_DECAY_RANGE:
         return "KDA_ERR_DECAY_RANGE: in-chunk cumulative log-decay outside the supported range";
+    case KDA_ERR_VALUE_RANGE:
+        return "KDA_ERR_VALUE_RANGE: a value held in fp16 left the fp16 range";
     }
     return "KDA: unknown status";
 }

@@ -1,24 +1,28 @@
 // prefill_split.cu -- the tensor-core prefill as two kernels (bf16 q/k/v,
 // d_k = d_v = 128, fp32 state), sm_103a.
 //
-// Everything in a 64-token chunk that does not involve the running state (the
-// decay prefix, the decayed operands, the k-k / q-k matrices, the UT solve and
-// the WY factor W) is independent across chunks ("From 124M to 2.8T", chapter
-// 3: parallel inside a chunk; "K3 attention, three-piece set": WY
-// representation + UT transform).  So it runs in its own kernel, one CTA per
-// (chunk, head), over every chunk at once, and leaves a record per chunk-head in
-// the workspace.  The state kernel then only walks the serial part, one CTA per
-// (sequence, head, 32-column value slice), bulk-loading each record a chunk
-// ahead:
+// Everything in a 64-token chunk that does not involve the running state is
+// independent across chunks ("From 124M to 2.8T", chapter 3: parallel inside a
+// chunk; "K3 attention, three-piece set": WY representation + UT transform).
+// The chunk kernel, one CTA per (chunk, head) over every chunk at once, folds
+// all of it into four matrices per chunk-head, so that the serial walk over the
+// chunks is a single matrix product per chunk.  With g the in-chunk prefix of
+// log alpha, gamma = e^{g_last}, Kg = k e^g, Qg = scale q e^g, Kd = k e^{g_last - g},
+// Aqk = lower(Qg Ki^T), T' = (I + A)^-1 diag(beta) and W = T' Kg:
 //
-//   chunk kernel   (as in the fused kernel)  record = [-W ; Qg] bf16, Ki^T tf32,
-//                  T' = (I + A)^-1 diag(beta) tf32, Aqk bf16, e^{g_last}
-//   state kernel   D_u  = T' V (tf32) - W S (bf16)          = u       (M = 64)
-//                  D_o  = Qg S (bf16) + Aqk u (bf16)         = o       (M = 64)
-//                  D5   = Ki^T u (tf32);  S <- e^{g_last} (S + D5)     (M = 128)
+//   S_{c+1} = gamma . S_c + P V + N S_c      P  = Kd^T T'          (128 x 64)
+//                                            N  = -Kd^T W           (128 x 128)
+//   o_c     = Q' S_c + P2 V                  Q' = Qg - Aqk W        (64 x 128)
+//                                            P2 = Aqk T'            (64 x 64)
 //
-// Records are the chunk kernel's shared-memory operand images, byte for byte,
-// so the state kernel feeds them to the MMAs without re-packing.
+// (u = T'V - W S is substituted into S <- gamma.(S + Ki^T u) and o = Qg S + Aqk u.)
+// The record of a chunk-head holds N, Q' (bf16), P, P2 (fp16: the 10-bit
+// mantissa P needs, at half the bytes of tf32) and gamma as the state kernel's
+// MMA operand images, byte for byte.  P is formed from bf16 high/low splits of
+// Kd and T' (hi.hi + hi.lo + lo.hi), which is more accurate than one tf32 product.
+// The state kernel walks the chunks of one (sequence, head, 32-column value
+// slice): per chunk one MMA group P V + N S on the critical path and the output
+// group P2 V + Q' S beside it, issued by a second thread.
 #include "tc_common.cuh"
 
 namespace kda {
@@ -27,63 +31,269 @@ namespace {
 using namespace ptx;
 using namespace tc;
 
-// Record of one chunk-head (also the contiguous tail of the chunk kernel's
-// shared memory and the head of each state-kernel stage).
-constexpr uint32_t R_O1 = 0;       // [-W ; Qg] bf16 K-major, 2 panels x 128 rows
-constexpr uint32_t R_O3 = 32768;   // Ki^T tf32 K-major, 2 panels x 128 rows
-constexpr uint32_t R_TT = 65536;   // T' tf32 K-major, 2 panels x 64 rows
-constexpr uint32_t R_AQ = 81920;   // Aqk bf16 K-major, 64 rows
-constexpr uint32_t R_GM = 90112;   // e^{g_last}, 128 fp32
-constexpr uint32_t kRecBytes = 90624;
+// Record of one chunk-head.
+constexpr uint32_t R_N = 0;        // N  bf16 K-major, 2 panels x 128 rows (rows i, K = j)
+constexpr uint32_t R_P = 32768;    // P  fp16 K-major, 128 rows            (rows i, K = s)
+constexpr uint32_t R_Q = 49152;    // Q' bf16 K-major, 2 panels x 64 rows  (rows t, K = j)
+constexpr uint32_t R_P2 = 65536;   // P2 fp16 K-major, 64 rows             (rows t, K = s)
+constexpr uint32_t R_GM = 73728;   // gamma, 128 fp32
+constexpr uint32_t kRecBytes = 74240;
 static_assert(kRecBytes % 16 == 0, "records are moved by bulk copies");
 
-// Chunk kernel: 256 threads and 89 KB of shared memory, so two CTAs share an SM
-// and hide each other's latencies.  Only the operands its own MMAs read live in
-// shared memory; Ki^T, Aqk, T' (tf32) and e^{g_last} go straight to the record.
+// Chunk kernel: 256 threads and 105 KB of shared memory, so two CTAs share an
+// SM and hide each other's latencies.  CTAs take the chunks last to first, so
+// the records the serial pass reads first are the ones written last (most
+// likely still in L2).
 constexpr int kChunkThreads = 256;
 struct ChunkLayout {
-    static constexpr uint32_t IN_Q = 0, IN_K = 16384;  // TMA boxes
-    static constexpr uint32_t O2 = 32768;   // Ki bf16, 64 rows x 128
-    static constexpr uint32_t O1 = 49152;   // [Kg ; Qg] -> [-W ; Qg] (the record's first image)
-    static constexpr uint32_t O4 = 81920;   // T' bf16, 64 rows x 64 (prefix group totals before)
-    // solve scratch over the input boxes and O2, both dead by then
-    static constexpr uint32_t SOLVE_A = 0, SOLVE_T = kC * kLdS * 4, SOLVE_X = 2 * kC * kLdS * 4;
-    static constexpr uint32_t USED = 90112;
+    static constexpr uint32_t IN_K = 0, IN_Q = 16384;  // TMA boxes; k lives until the Kd build
+    static constexpr uint32_t O2 = 32768;   // Ki bf16, 64 rows x 128 (B of the k-k product)
+    static constexpr uint32_t O1 = 49152;   // [Kg ; Qg] -> [-W ; Qg] bf16, 128 rows x 128
+    static constexpr uint32_t AQ = 81920;   // Aqk bf16 K-major 64 x 64 (prefix group totals before)
+    static constexpr uint32_t O4 = 90112;   // T' high part bf16 [t][s]
+    static constexpr uint32_t TL = 98304;   // T' low part bf16 [t][s]
+    // in-place solve over the q box and Ki (both dead by then); Kd^T over the same bytes after it
+    static constexpr uint32_t SOLVE_A = 16384, SOLVE_T = 16384, SOLVE_X = 16384 + kC * kLdS * 4;
+    static constexpr uint32_t KDH = 16384, KDL = 32768;  // Kd^T high / low bf16 K-major, 128 rows x 64
+    static constexpr uint32_t USED = 106496;
 };
 static_assert(ChunkLayout::SOLVE_X + 32 * kLdX * 4 <= ChunkLayout::O1, "solve scratch overlaps O1");
 
+// State kernel (512 threads): two record stages, a ring of four v slices, the
+// V^T operand of two chunks and the S^T operand of two chunks.
+constexpr int kVRing = 4;
 struct StateLayout {
-    static constexpr uint32_t STAGE = 91136;  // record + padding to 1024 bytes
-    static constexpr uint32_t IN_V = 2 * STAGE;               // 2 x v slice [64][32] bf16
-    static constexpr uint32_t O6 = IN_V + 2 * 4096;           // V^T tf32, 32 rows x K 64
-    static constexpr uint32_t O7 = O6 + 8192;                 // S^T bf16, 32 rows x K 128
-    static constexpr uint32_t O9 = O7 + 8192;                 // u^T bf16, 32 rows x K 64
-    static constexpr uint32_t O10 = O9 + 4096;                // u^T tf32, 32 rows x K 64
-    static constexpr uint32_t USED = O10 + 8192;
+    static constexpr uint32_t STAGE = 75776;  // record + padding to 1024 bytes
+    static constexpr uint32_t VBOX = 2 * STAGE;               // kVRing x v slice [64][32] bf16
+    static constexpr uint32_t VIMG = VBOX + kVRing * 4096;    // 2 x V^T fp16, 32 rows x K 64
+    static constexpr uint32_t O7 = VIMG + 2 * 4096;           // 2 x S^T bf16, 32 rows x K 128
+    static constexpr uint32_t USED = O7 + 2 * 8192;
 };
 static_assert(StateLayout::STAGE % 1024 == 0 && StateLayout::STAGE >= kRecBytes, "stage size");
-static_assert(StateLayout::O6 % 1024 == 0 && StateLayout::O7 % 1024 == 0 &&
-              StateLayout::O9 % 1024 == 0 && StateLayout::O10 % 1024 == 0, "operand alignment");
+static_assert(StateLayout::VIMG % 1024 == 0 && StateLayout::O7 % 1024 == 0, "operand alignment");
 
 constexpr uint32_t kChunkSmem = ChunkLayout::USED + 1024;
 constexpr uint32_t kStateSmem = StateLayout::USED + 1024;
 
 // ============================================================== chunk kernel
+// TMEM columns: k-k / q-k product 0..63; then W 0..127, P2 128..191, P 192..255;
+// then N 0..127, Q'' = Aqk(-W) 128..255.
+constexpr uint32_t TC_W = 0, TC_P2 = 128, TC_P = 192, TC_N = 0, TC_Q = 128, kChunkTmem = 256;
+
+// MN-major bf16 operand of 64-row K panels (rows = K index, 128-byte swizzled rows)
+__device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t panel_stride)
+{
+    return sdesc(addr, panel_stride, 1024, kSw128B);
+}
+
+// T' = T diag(beta) split into bf16 high and low parts: [t][s] images at O4 and TL.
+template <class L, int NT>
+__device__ __forceinline__ void write_tprime_hilo(unsigned char *sm, const float *s_beta)
+{
+    const float *sT = reinterpret_cast<const float *>(sm + L::SOLVE_T);
+#pragma unroll
+    for (int e = threadIdx.x; e < 512; e += NT) {
+        const int r = e >> 3, s8 = (e & 7) * 8;
+        const float4 ta = *reinterpret_cast<const float4 *>(sT + r * kLdS + s8);
+        const float4 tb = *reinterpret_cast<const float4 *>(sT + r * kLdS + s8 + 4);
+        const float4 ba = *reinterpret_cast<const float4 *>(s_beta + s8);
+        const float4 bb = *reinterpret_cast<const float4 *>(s_beta + s8 + 4);
+        const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
+        const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
+        float hi[8], lo[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const float t = s8 + u <= r ? tv[u] * bv[u] : 0.f;
+            hi[u] = __bfloat162float(__float2bfloat16_rn(t));
+            lo[u] = t - hi[u];
+        }
+        *reinterpret_cast<uint4 *>(sm + L::O4 + km16(r, s8, 64)) = pack_bf16x8(hi);
+        *reinterpret_cast<uint4 *>(sm + L::TL + km16(r, s8, 64)) = pack_bf16x8(lo);
+    }
+}
+
+// Kd^T = (k e^{g_last - g})^T as bf16 high and low parts, K-major [i][s] at KDH
+// and KDL.  Thread = (channel pair cp, row group rg) as in decayed_operands.
+template <class L, int NT>
+__device__ __forceinline__ void build_kd(unsigned char *sm, int len, const float2 (&gl)[4096 / NT],
+                                         float2 off, float2 tot)
+{
+    constexpr int R = 4096 / NT;
+    static_assert(R % 8 == 0, "row groups cover whole 8-column chunks");
+    const int tid = threadIdx.x, lane = tid & 31, cp = tid & 63, rg = tid >> 6;
+    const int sel = lane & 1;  // odd lanes store their odd channel first (no bank conflicts)
+#pragma unroll
+    for (int r8 = 0; r8 < R; r8 += 8) {
+        float hx[8], lx[8], hy[8], ly[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            const int rr = r8 + u, r = rg * R + rr;
+            const bool valid = r < len;
+            const uint32_t kraw = valid ? *reinterpret_cast<const uint32_t *>(sm + L::IN_K + (r * kD + 2 * cp) * 2) : 0u;
+            const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kraw));
+            const float dx = kv.x * __expf(tot.x - (off.x + gl[rr].x));
+            const float dy = kv.y * __expf(tot.y - (off.y + gl[rr].y));
+            hx[u] = __bfloat162float(__float2bfloat16_rn(dx));
+            hy[u] = __bfloat162float(__float2bfloat16_rn(dy));
+            lx[u] = dx - hx[u];
+            ly[u] = dy - hy[u];
+        }
+        const int s0 = rg * R + r8;
+        const uint4 hxv = pack_bf16x8(hx), hyv = pack_bf16x8(hy), lxv = pack_bf16x8(lx), lyv = pack_bf16x8(ly);
+        *reinterpret_cast<uint4 *>(sm + L::KDH + km16(2 * cp + sel, s0, 128)) = sel ? hyv : hxv;
+        *reinterpret_cast<uint4 *>(sm + L::KDH + km16(2 * cp + 1 - sel, s0, 128)) = sel ? hxv : hyv;
+        *reinterpret_cast<uint4 *>(sm + L::KDL + km16(2 * cp + sel, s0, 128)) = sel ? lyv : lxv;
+        *reinterpret_cast<uint4 *>(sm + L::KDL + km16(2 * cp + 1 - sel, s0, 128)) = sel ? lxv : lyv;
+    }
+}
+
+// Round 2a: W = T' Kg (M = 64, N = 128) and P2 = Aqk T' (M = 64, N = 64).
+template <class L>
+__device__ __forceinline__ void issue_w_p2(uint32_t sb, uint32_t tmem)
+{
+    issue_gw<L>(sb, tmem + TC_W);
+    constexpr uint32_t idesc = idesc_bf16(64, 64, false, true);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+        mma_bf16(tmem + TC_P2, kdesc(sb + L::AQ + s * 32), mndesc(sb + L::O4 + s * 2048, 8192), idesc, s > 0);
+}
+
+// Round 2b: P = Kd^T T' (M = 128, N = 64) from the three leading terms of the
+// high/low split, hi.hi + hi.lo + lo.hi.
+template <class L>
+__device__ __forceinline__ void issue_p(uint32_t sb, uint32_t tmem)
+{
+    constexpr uint32_t idesc = idesc_bf16(128, 64, false, true);
+    const uint32_t a[3] = {L::KDH, L::KDH, L::KDL}, b[3] = {L::O4, L::TL, L::O4};
+#pragma unroll
+    for (int t = 0; t < 3; ++t)
+#pragma unroll
+        for (int s = 0; s < 4; ++s)
+            mma_bf16(tmem + TC_P, kdesc(sb + a[t] + s * 32), mndesc(sb + b[t] + s * 2048, 8192), idesc,
+                     (t | s) != 0);
+}
+
+// Round 3: N = Kd^T (-W) (M = 128, N = 128) and Q'' = Aqk (-W) (M = 64, N = 128).
+template <class L>
+__device__ __forceinline__ void issue_n_q(uint32_t sb, uint32_t tmem)
+{
+    constexpr uint32_t id_n = idesc_bf16(128, 128, false, true), id_q = idesc_bf16(64, 128, false, true);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+        mma_bf16(tmem + TC_N, kdesc(sb + L::KDH + s * 32), mndesc(sb + L::O1 + s * 2048, 16384), id_n, s > 0);
+#pragma unroll
+    for (int s = 0; s < 4; ++s)
+        mma_bf16(tmem + TC_Q, kdesc(sb + L::AQ + s * 32), mndesc(sb + L::O1 + s * 2048, 16384), id_q, s > 0);
+}
+
+// Epilogues straight into the record (global memory).  NT = 256: warp w reads
+// TMEM lane quarter w % 4 and column half w / 4.
+__device__ __forceinline__ void epi_p2(uint32_t tmem, unsigned char *rec, bool &ok)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
+    const int r = quarter * 16 + (lane & 15);  // M = 64: row 16q + l in lane l < 16
+#pragma unroll
+    for (int cb = 0; cb < 32; cb += 16) {
+        float v[16];
+        tmem_ld16(tmem + TC_P2 + ((uint32_t)(quarter * 32) << 16) + part * 32 + cb, v);
+        tmem_ld_wait();
+        if (lane < 16) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
+                *reinterpret_cast<uint4 *>(rec + R_P2 + km16(r, part * 32 + cb + hh * 8, 64)) = pack_f16x8(x, ok);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void epi_p(uint32_t tmem, unsigned char *rec, bool &ok)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
+    const int i = quarter * 32 + lane;
+#pragma unroll
+    for (int cb = 0; cb < 32; cb += 16) {
+        float v[16];
+        tmem_ld16(tmem + TC_P + ((uint32_t)(quarter * 32) << 16) + part * 32 + cb, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
+            *reinterpret_cast<uint4 *>(rec + R_P + km16(i, part * 32 + cb + hh * 8, 128)) = pack_f16x8(x, ok);
+        }
+    }
+}
+
+__device__ __forceinline__ void epi_n(uint32_t tmem, unsigned char *rec)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
+    const int i = quarter * 32 + lane;
+#pragma unroll
+    for (int cb = 0; cb < 64; cb += 16) {
+        float v[16];
+        tmem_ld16(tmem + TC_N + ((uint32_t)(quarter * 32) << 16) + part * 64 + cb, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
+            *reinterpret_cast<uint4 *>(rec + R_N + km16(i, part * 64 + cb + hh * 8, 128)) = pack_bf16x8(x);
+        }
+    }
+}
+
+// Q' = Qg + Aqk (-W); Qg from rows 64..127 of O1.
+template <class L>
+__device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, unsigned char *rec)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
+    const int r = quarter * 16 + (lane & 15);
+#pragma unroll
+    for (int cb = 0; cb < 64; cb += 16) {
+        float v[16];
+        tmem_ld16(tmem + TC_Q + ((uint32_t)(quarter * 32) << 16) + part * 64 + cb, v);
+        tmem_ld_wait();
+        if (lane < 16) {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int col = part * 64 + cb + hh * 8;
+                const uint4 qraw = *reinterpret_cast<const uint4 *>(sm + L::O1 + km16(64 + r, col, 128));
+                const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
+                float x[8];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qw[u]));
+                    x[2 * u] = qf.x + v[hh * 8 + 2 * u];
+                    x[2 * u + 1] = qf.y + v[hh * 8 + 2 * u + 1];
+                }
+                *reinterpret_cast<uint4 *>(rec + R_Q + km16(r, col, 64)) = pack_bf16x8(x);
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kChunkThreads, 2)
 prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const float *__restrict__ log_alpha, const float *__restrict__ beta,
                      const int32_t *__restrict__ cu, int64_t total, int H, int num_seqs,
-                     const int32_t *__restrict__ cc, unsigned char *__restrict__ records,
-                     uint32_t *status)
+                     int chunk_bound, const int32_t *__restrict__ cc,
+                     unsigned char *__restrict__ records, uint32_t *status)
 {
     using L = ChunkLayout;
     constexpr int NT = kChunkThreads;
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t bar_tma, bar_mma;
+    __shared__ __align__(8) uint64_t bar_tma, bar_mma, bar_p, bar_drain;
     __shared__ uint32_t tmem_holder;
     __shared__ __align__(16) float s_beta[kC];
 
-    const int g = blockIdx.x, h = blockIdx.y;
+    // one CTA per (chunk, head), heads fastest, chunks last to first
+    const int h = (int)(blockIdx.x % (unsigned)H);
+    const int g = chunk_bound - 1 - (int)(blockIdx.x / (unsigned)H);
     if (g >= cc[num_seqs]) return;  // past the last chunk (the grid is an upper bound)
     int lo = 0, hi = num_seqs;      // sequence n with cc[n] <= g < cc[n + 1]
     while (hi - lo > 1) {
@@ -103,97 +313,116 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     if (tid == 0) {
         mbar_init(&bar_tma, 1);
         mbar_init(&bar_mma, 1);
+        mbar_init(&bar_p, 1);
+        mbar_init(&bar_drain, 1);
         fence_mbar_init();
         mbar_arrive_expect_tx(&bar_tma, 16384 + 16384);
         tma_load_3d(sm + L::IN_Q, &tm_q, &bar_tma, 0, h, (int)c0);
         tma_load_3d(sm + L::IN_K, &tm_k, &bar_tma, 0, h, (int)c0);
     }
     if (warp == 0) {
-        tmem_alloc(&tmem_holder, 256);
+        tmem_alloc(&tmem_holder, kChunkTmem);
         tmem_relinquish();
     }
     if (tid < kC) s_beta[tid] = tid < len ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
-    // a1: the in-chunk decay prefix reads log_alpha straight from global memory,
+    // the in-chunk decay prefix reads log_alpha straight from global memory,
     // overlapping the q/k copies
-    float *s_tot = reinterpret_cast<float *>(sm + L::O4);
+    float *s_tot = reinterpret_cast<float *>(sm + L::AQ);
     float2 gl[4096 / NT];
     float gmin, gmax;
     prefix_scan<NT>(log_alpha + ((size_t)c0 * H + h) * kD, H * kD, len, s_tot, gl, gmin, gmax);
     __syncthreads();
     tc_fence_after_sync();
-    const uint32_t tmem = tmem_holder, tD1 = tmem, tDW = tmem + 64;
-    bool timed_out = false, tma_pending = true, mma_pending = false, decay_bad = false;
+    const uint32_t tmem = tmem_holder;
+    bool timed_out = false, tma_pending = true, decay_bad = false, range_ok = true;
     do {
         bool ok = mbar_wait_ns(&bar_tma, 0, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tma_pending = false;
-        decay_bad = decayed_operands<L, NT>(sm, len, s_tot, rec + R_O3,
-                                            reinterpret_cast<float *>(rec + R_GM), gl, gmin, gmax);
+        float2 ot[2];
+        decay_bad = decayed_operands<L, NT, false>(sm, len, s_tot, nullptr,
+                                                   reinterpret_cast<float *>(rec + R_GM), gl, gmin, gmax, ot);
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
             tc_fence_after_sync();
-            issue_g1<L>(sb, tD1);
+            issue_g1<L>(sb, tmem);
             mma_commit(&bar_mma);
         }
-        mma_pending = true;
         ok = mbar_wait_ns(&bar_mma, 0, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        mma_pending = false;
         tc_fence_after_sync();
-        kk_epilogue<L, NT>(sm, tD1, s_beta, rec + R_AQ);
+        kk_epilogue<L, NT>(sm, tmem, s_beta, sm + L::AQ);
         tc_fence_before_sync();
         __syncthreads();
-        solve_ut<L, NT>(sm, s_beta, rec + R_TT, 64);
+        solve_ut_core<L, NT, true>(sm);
+        write_tprime_hilo<L, NT>(sm, s_beta);
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
             tc_fence_after_sync();
-            issue_gw<L>(sb, tDW);
+            issue_w_p2<L>(sb, tmem);
             mma_commit(&bar_mma);
         }
-        mma_pending = true;
+        build_kd<L, NT>(sm, len, gl, ot[0], ot[1]);  // over the solve scratch, overlapping W and P2
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            tc_fence_after_sync();
+            issue_p<L>(sb, tmem);
+            mma_commit(&bar_p);
+        }
         ok = mbar_wait_ns(&bar_mma, 1, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        mma_pending = false;
         tc_fence_after_sync();
-        w_epilogue<L, NT>(sm, tDW);
+        w_epilogue<L, NT>(sm, tmem + TC_W);  // -W over Kg in O1
+        epi_p2(tmem, rec, range_ok);
+        ok = mbar_wait_ns(&bar_p, 0, kWaitNs);
+        if (__syncthreads_or(!ok)) { timed_out = true; break; }
+        tc_fence_after_sync();
+        epi_p(tmem, rec, range_ok);
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
-        if (tid == 0) {  // [-W ; Qg] image of the record
-            bulk_store(rec + R_O1, sm + L::O1, 32768);
-            bulk_commit();
-            bulk_wait_all();
+        if (tid == 0) {
+            tc_fence_after_sync();
+            issue_n_q<L>(sb, tmem);
+            mma_commit(&bar_mma);
         }
+        ok = mbar_wait_ns(&bar_mma, 0, kWaitNs);
+        if (__syncthreads_or(!ok)) { timed_out = true; break; }
+        tc_fence_after_sync();
+        epi_n(tmem, rec);
+        epi_q<L>(sm, tmem, rec);
     } while (false);
     if (timed_out) {
-        if (tid == 0) atomicOr(status, DEV_ERR_TIMEOUT);
+        if (tid == 0) {
+            atomicOr(status, DEV_ERR_TIMEOUT);
+            mma_commit(&bar_drain);  // completes once every MMA issued so far has
+        }
+        (void)mbar_wait_ns(&bar_drain, 0, kWaitNs);
         if (tma_pending) (void)mbar_wait_ns(&bar_tma, 0, kWaitNs);
-        if (mma_pending) (void)mbar_wait_ns(&bar_mma, 0, kWaitNs);
     }
     if (decay_bad) atomicOr(status, DEV_ERR_DECAY);
+    if (!range_ok) atomicOr(status, DEV_ERR_RANGE);
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, 256);
+    if (warp == 0) tmem_dealloc(tmem, kChunkTmem);
 }
 
 // ============================================================== state kernel
-constexpr uint32_t IDESC_U = idesc_tf32(64, 32, false, false);   // T' V
-constexpr uint32_t IDESC_WS = idesc_bf16(64, 32, false, false);  // -W S, Qg S, Aqk u
-constexpr uint32_t IDESC_K = idesc_tf32(128, 32, false, false);  // Ki^T u
-constexpr uint32_t TM_U = 0, TM_O = 32, TM_5 = 64, kStateTmem = 128;
+constexpr uint32_t IDESC_PV = idesc_f16(128, 32, false, false);   // P V
+constexpr uint32_t IDESC_NS = idesc_bf16(128, 32, false, false);  // N S
+constexpr uint32_t IDESC_P2V = idesc_f16(64, 32, false, false);   // P2 V
+constexpr uint32_t IDESC_QS = idesc_bf16(64, 32, false, false);   // Q' S
+// TMEM columns: state increment (M = 128), outputs of two chunks (M = 64)
+constexpr uint32_t TM_5 = 0, TM_O = 32, kStateTmem = 128;
 
-__device__ __forceinline__ void issue_state_loads(unsigned char *sm, const unsigned char *rec,
-                                                  const CUtensorMap *tv, uint64_t *bar, int st,
-                                                  int h, int j0, int row)
-{
-    using L = StateLayout;
-    mbar_arrive_expect_tx(bar, kRecBytes + 4096);
-    bulk_load(sm + st * L::STAGE, rec, kRecBytes, bar);
-    tma_load_3d(sm + L::IN_V + st * 4096, tv, bar, j0, h, row);
-}
-
+// The serial pass over the chunks of one (sequence, head, 32-column value slice).
+// Chunk c: thread 0 issues P V + N S_c (the critical chain) and thread 32 issues
+// P2 V + Q' S_c (the output); while they run, all threads write the outputs of
+// chunk c - 1 and convert the v slice of chunk c + 1; then S_{c+1} = gamma . S_c
+// + (P V + N S_c).  Records are copied one chunk ahead, v slices kVRing ahead.
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__restrict__ cu,
                      int64_t total, int H, const int32_t *__restrict__ cc,
@@ -203,7 +432,9 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
 {
     using L = StateLayout;
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t bar_ld[2], bar_mma;
+    // one output barrier per output buffer: chunk c commits to bar_o[c & 1] before
+    // chunk c - 1's outputs are awaited, so a single barrier could run two phases ahead
+    __shared__ __align__(8) uint64_t bar_rec[2], bar_v[kVRing], bar_s, bar_o[2], bar_drain;
     __shared__ uint32_t tmem_holder;
 
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -217,20 +448,37 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     const unsigned char *rec0 = records + ((size_t)cc[n] * H + h) * kRecBytes;
     const size_t rec_stride = (size_t)H * kRecBytes;
 
+    // copies, issued by thread 0 only (which alone keeps these counts exact)
+    int rec_issued = 0, v_issued = 0;
+    auto load_record = [&](int k) {
+        mbar_arrive_expect_tx(&bar_rec[k & 1], kRecBytes);
+        bulk_load(sm + (k & 1) * L::STAGE, rec0 + (size_t)k * rec_stride, kRecBytes, &bar_rec[k & 1]);
+        rec_issued = k + 1;
+    };
+    auto load_v = [&](int k) {
+        mbar_arrive_expect_tx(&bar_v[k % kVRing], 4096);
+        tma_load_3d(sm + L::VBOX + (k % kVRing) * 4096, &tm_v, &bar_v[k % kVRing], j0, h,
+                    (int)(t0 + (int64_t)k * kC));
+        v_issued = k + 1;
+    };
     if (tid == 0) {
-        mbar_init(&bar_ld[0], 1);
-        mbar_init(&bar_ld[1], 1);
-        mbar_init(&bar_mma, 1);
+        mbar_init(&bar_rec[0], 1);
+        mbar_init(&bar_rec[1], 1);
+        for (int k = 0; k < kVRing; ++k) mbar_init(&bar_v[k], 1);
+        mbar_init(&bar_s, 1);
+        mbar_init(&bar_o[0], 1);
+        mbar_init(&bar_o[1], 1);
+        mbar_init(&bar_drain, 2);  // both MMA-issuing threads commit to it on a timeout
         fence_mbar_init();
         prefetch_tmap(&tm_v);
-        for (int c = 0; c < 2 && c < nchunks; ++c)
-            issue_state_loads(sm, rec0 + c * rec_stride, &tm_v, &bar_ld[c], c, h, j0, (int)(t0 + c * kC));
+        for (int k = 0; k < 2 && k < nchunks; ++k) load_record(k);
+        for (int k = 0; k < kVRing && k < nchunks; ++k) load_v(k);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_holder, kStateTmem);
         tmem_relinquish();
     }
-    // state row i, columns j0 + 8*part .. +7 in registers; S^T (bf16) operand in O7
+    // state row i, columns j0 + 8*part .. +7 in registers; S^T (bf16) operands in O7
     const int i_row = quarter * 32 + lane, jp = part * 8;
     float S[8];
     const size_t st_off = (((size_t)n * H + h) * kD + i_row) * kD + j0 + jp;
@@ -252,141 +500,136 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     const uint32_t tmem = tmem_holder;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int r64 = quarter * 16 + (lane & 15);  // row held by this lane in an M = 64 accumulator
+    const int odd = lane & 1;
+    bool range_ok = true;
 
-    uint32_t ph_mma = 0;
-    bool timed_out = false, mma_pending = false;
-    int c = 0;
-    for (; c < nchunks; ++c) {
-        const int st = c & 1;
-        const int64_t c0 = t0 + (int64_t)c * kC;
-        const int len = (t1 - c0) < kC ? (int)(t1 - c0) : kC;
-        unsigned char *stg = sm + st * L::STAGE;
-        const uint32_t sg = sb + st * L::STAGE;
-
-        bool ok = mbar_wait_ns(&bar_ld[st], (uint32_t)((c >> 1) & 1), kWaitNs);
-        if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        {  // V^T (tf32, K-major [j][s]): one 4-row group of one column per thread
-            const int j = tid % kDV, s4 = (tid / kDV) * 4;
-            float x[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u)
-                x[u] = (s4 + u) < len ? bf16_at(sm + L::IN_V + st * 4096 + ((s4 + u) * kDV + j) * 2) : 0.f;
-            *reinterpret_cast<float4 *>(sm + L::O6 + km32(j, s4, kDV)) = make_float4(x[0], x[1], x[2], x[3]);
-        }
-        fence_proxy_async_smem();
-        __syncthreads();
-
-        // ------------------------------------------------------ u = T'V - WS, Qg S
-        if (tid == 0) {
-            tc_fence_after_sync();
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t p = s >> 2, w = (s & 3) * 32;
-                mma_tf32(tmem + TM_U, kdesc(sg + R_TT + p * 8192 + w), kdesc(sb + L::O6 + p * 4096 + w),
-                         IDESC_U, s > 0);
-            }
-#pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t p = s >> 2, w = (s & 3) * 32;
-                mma_bf16(tmem + TM_U, kdesc(sg + R_O1 + p * 16384 + w), kdesc(sb + L::O7 + p * 4096 + w),
-                         IDESC_WS, 1);
-                mma_bf16(tmem + TM_O, kdesc(sg + R_O1 + p * 16384 + 8192 + w),
-                         kdesc(sb + L::O7 + p * 4096 + w), IDESC_WS, s > 0);
-            }
-            mma_commit(&bar_mma);
-        }
-        mma_pending = true;
-        ok = mbar_wait_ns(&bar_mma, ph_mma, kWaitNs);
-        if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        mma_pending = false;
-        ph_mma ^= 1;
+    // o rows of chunk cp (M = 64 accumulator TM_O + 32*(cp&1)), once its MMAs finished
+    auto write_o = [&](int cp) -> bool {
+        if (!mbar_wait_ns(&bar_o[cp & 1], (uint32_t)((cp >> 1) & 1), kWaitNs)) return false;
         tc_fence_after_sync();
-        {  // u (M = 64 layout: row 16q + l in lane l < 16) -> u^T operands, row pairs
-            float v[8];
-            tmem_ld8(tmem + TM_U + lane_off + jp, v);
-            tmem_ld_wait();
-            const int odd = lane & 1, re = r64 & ~1;
+        float v[8];
+        tmem_ld8(tmem + TM_O + 32 * (cp & 1) + lane_off + jp, v);
+        tmem_ld_wait();
+        const int64_t cs = t0 + (int64_t)cp * kC;
+        if (lane < 16 && cs + r64 < t1)
+            *reinterpret_cast<uint4 *>(o + ((size_t)(cs + r64) * H + h) * kD + j0 + jp) = pack_bf16x8(v);
+        return true;
+    };
+    // v slice of chunk k -> V^T fp16 K-major in VIMG[k & 1]; one 4-row group of one column per thread
+    auto convert_v = [&](int k) -> bool {
+        if (!mbar_wait_ns(&bar_v[k % kVRing], (uint32_t)((k / kVRing) & 1), kWaitNs)) return false;
+        const int64_t ck = t0 + (int64_t)k * kC;
+        const int lenk = (t1 - ck) < kC ? (int)(t1 - ck) : kC;
+        const int j = tid % kDV, s4 = (tid / kDV) * 4;
+        float x[4];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float mine = odd ? v[4 + u] : v[u];
-                const float give = odd ? v[u] : v[4 + u];
-                const float other = __shfl_xor_sync(0xffffffffu, give, 1);
-                const float lo = odd ? other : mine, hi = odd ? mine : other;  // rows re, re+1
-                const int j = jp + 4 * odd + u;
-                if (lane < 16) {
-                    *reinterpret_cast<uint32_t *>(sm + L::O9 + km16(j, re, kDV)) = pack_bf16x2(lo, hi);
-                    *reinterpret_cast<float2 *>(sm + L::O10 + km32(j, re, kDV)) =
-                        make_float2(to_tf32(lo), to_tf32(hi));
-                }
-            }
+        for (int u = 0; u < 4; ++u) {
+            x[u] = (s4 + u) < lenk ? bf16_at(sm + L::VBOX + (k % kVRing) * 4096 + ((s4 + u) * kDV + j) * 2) : 0.f;
+            range_ok &= fabsf(x[u]) <= 65504.f;
         }
-        fence_proxy_async_smem();
-        tc_fence_before_sync();
-        __syncthreads();
+        __half2 a = __floats2half2_rn(x[0], x[1]), b = __floats2half2_rn(x[2], x[3]);
+        *reinterpret_cast<uint2 *>(sm + L::VIMG + (k & 1) * 4096 + km16(j, s4, kDV)) =
+            make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+        return true;
+    };
 
-        // ------------------------------------------------------ o += Aqk u, D5 = Ki^T u
-        if (tid == 0) {
+    bool timed_out = false;
+    {
+        const bool ok = nchunks == 0 || convert_v(0);
+        fence_proxy_async_smem();
+        if (__syncthreads_or(!ok)) timed_out = true;
+        else if (tid == 0 && kVRing < nchunks) load_v(kVRing);
+    }
+    int c = 0;
+    for (; c < nchunks && !timed_out; ++c) {
+        const int st = c & 1;
+        const uint32_t sg = sb + st * L::STAGE;
+        const uint32_t s_cur = sb + L::O7 + st * 8192, v_cur = sb + L::VIMG + st * 4096;
+
+        // chunk c - 1's MMAs have finished: its record stage takes chunk c + 1
+        if (tid == 0 && c >= 1 && c + 1 < nchunks &&
+            mbar_wait_ns(&bar_o[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1), kWaitNs))
+            load_record(c + 1);
+        bool ok = mbar_wait_ns(&bar_rec[st], (uint32_t)((c >> 1) & 1), kWaitNs);
+        if (__syncthreads_or(!ok)) { timed_out = true; break; }
+
+        if (tid == 0) {  // the chain: P V + N S_c
             tc_fence_after_sync();
 #pragma unroll
             for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem + TM_O, kdesc(sg + R_AQ + s * 32), kdesc(sb + L::O9 + s * 32), IDESC_WS, 1);
+                mma_bf16(tmem + TM_5, kdesc(sg + R_P + s * 32), kdesc(v_cur + s * 32), IDESC_PV, s > 0);
 #pragma unroll
             for (int s = 0; s < 8; ++s) {
                 const uint32_t p = s >> 2, w = (s & 3) * 32;
-                mma_tf32(tmem + TM_5, kdesc(sg + R_O3 + p * 16384 + w), kdesc(sb + L::O10 + p * 4096 + w),
-                         IDESC_K, s > 0);
+                mma_bf16(tmem + TM_5, kdesc(sg + R_N + p * 16384 + w), kdesc(s_cur + p * 4096 + w), IDESC_NS, 1);
             }
-            mma_commit(&bar_mma);
+            mma_commit(&bar_s);
+        } else if (tid == 32) {  // the output: P2 V + Q' S_c
+            tc_fence_after_sync();
+#pragma unroll
+            for (int s = 0; s < 4; ++s)
+                mma_bf16(tmem + TM_O + 32 * st, kdesc(sg + R_P2 + s * 32), kdesc(v_cur + s * 32), IDESC_P2V, s > 0);
+#pragma unroll
+            for (int s = 0; s < 8; ++s) {
+                const uint32_t p = s >> 2, w = (s & 3) * 32;
+                mma_bf16(tmem + TM_O + 32 * st, kdesc(sg + R_Q + p * 8192 + w), kdesc(s_cur + p * 4096 + w),
+                         IDESC_QS, 1);
+            }
+            mma_commit(&bar_o[st]);
         }
-        mma_pending = true;
-        ok = mbar_wait_ns(&bar_mma, ph_mma, kWaitNs);
+        // while they run: outputs of chunk c - 1 (which also frees V^T buffer (c + 1) & 1),
+        // then the v slice of chunk c + 1
+        ok = c < 1 || write_o(c - 1);
+        if (ok && c + 1 < nchunks) ok = convert_v(c + 1);
+        fence_proxy_async_smem();
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        mma_pending = false;
-        ph_mma ^= 1;
+        if (tid == 0 && c + 1 + kVRing < nchunks) load_v(c + 1 + kVRing);
+
+        ok = mbar_wait_ns(&bar_s, (uint32_t)(c & 1), kWaitNs);
+        if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
-        {  // o rows (M = 64 layout)
-            float v[8];
-            tmem_ld8(tmem + TM_O + lane_off + jp, v);
-            tmem_ld_wait();
-            if (lane < 16 && r64 < len)
-                *reinterpret_cast<uint4 *>(o + ((size_t)(c0 + r64) * H + h) * kD + j0 + jp) = pack_bf16x8(v);
-        }
-        {  // state rows: S <- gamma_c (S + Ki^T u); S^T (bf16) for the next chunk, row pairs
+        {  // S <- gamma . S + (P V + N S); S^T (bf16) for the next chunk, row pairs
             float v[8];
             tmem_ld8(tmem + TM_5 + lane_off + jp, v);
             tmem_ld_wait();
-            const float gc = reinterpret_cast<const float *>(stg + R_GM)[i_row];
+            const float gc = reinterpret_cast<const float *>(sm + st * L::STAGE + R_GM)[i_row];
 #pragma unroll
-            for (int j = 0; j < 8; ++j) S[j] = gc * (S[j] + v[j]);
-            const int odd = lane & 1, ie = i_row & ~1;
+            for (int j = 0; j < 8; ++j) S[j] = fmaf(gc, S[j], v[j]);
+            unsigned char *s_next = sm + L::O7 + (st ^ 1) * 8192;
+            const int ie = i_row & ~1;
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
                 const float mine = odd ? S[4 + u] : S[u];
                 const float give = odd ? S[u] : S[4 + u];
                 const float other = __shfl_xor_sync(0xffffffffu, give, 1);
                 const float lo = odd ? other : mine, hi = odd ? mine : other;
-                *reinterpret_cast<uint32_t *>(sm + L::O7 + km16(jp + 4 * odd + u, ie, kDV)) = pack_bf16x2(lo, hi);
+                *reinterpret_cast<uint32_t *>(s_next + km16(jp + 4 * odd + u, ie, kDV)) = pack_bf16x2(lo, hi);
             }
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
-        if (tid == 0 && c + 2 < nchunks)  // this stage is free: load chunk c + 2 into it
-            issue_state_loads(sm, rec0 + (size_t)(c + 2) * rec_stride, &tm_v, &bar_ld[st], st, h, j0,
-                              (int)(c0 + 2 * kC));
+    }
+    if (!timed_out && nchunks > 0) {
+        const bool ok = write_o(nchunks - 1);
+        if (__syncthreads_or(!ok)) timed_out = true;
     }
     if (timed_out) {
         if (tid == 0) atomicOr(status, DEV_ERR_TIMEOUT);
-        // drain our own loads and MMAs (bounded) before releasing shared and tensor memory
-        if (mma_pending) (void)mbar_wait_ns(&bar_mma, ph_mma, kWaitNs);
-        for (int k = c; k < c + 2 && k < nchunks; ++k)
-            (void)mbar_wait_ns(&bar_ld[k & 1], (uint32_t)((k >> 1) & 1), kWaitNs);
+        if (tid == 0 || tid == 32) mma_commit(&bar_drain);  // completes once both threads' MMAs have
+        (void)mbar_wait_ns(&bar_drain, 0, kWaitNs);
+        // our own copies still in flight (thread 0 issued them and knows how many)
+        for (int k = rec_issued > 2 ? rec_issued - 2 : 0; k < rec_issued; ++k)
+            (void)mbar_wait_ns(&bar_rec[k & 1], (uint32_t)((k >> 1) & 1), kWaitNs);
+        for (int k = v_issued > kVRing ? v_issued - kVRing : 0; k < v_issued; ++k)
+            (void)mbar_wait_ns(&bar_v[k % kVRing], (uint32_t)((k / kVRing) & 1), kWaitNs);
     } else {
         float *dst = final_state + st_off;
 #pragma unroll
         for (int q = 0; q < 2; ++q)
             *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
     }
+    if (!range_ok) atomicOr(status, DEV_ERR_RANGE);
     tc_fence_before_sync();
     __syncthreads();
     if (warp == 0) tmem_dealloc(tmem, kStateTmem);
@@ -412,10 +655,10 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
         !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kDV))
         return cudaErrorInvalidValue;
     const int64_t chunk_bound = p.total_tokens / kC + p.num_seqs;
-    dim3 grid_a((unsigned)chunk_bound, p.num_heads);
-    prefill_chunk_kernel<<<grid_a, kChunkThreads, kChunkSmem, p.stream>>>(
-        tq, tk, p.log_alpha, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.num_seqs, cc,
-        static_cast<unsigned char *>(records), p.status);
+    if (chunk_bound * p.num_heads > INT32_MAX) return cudaErrorInvalidValue;
+    prefill_chunk_kernel<<<(unsigned)(chunk_bound * p.num_heads), kChunkThreads, kChunkSmem, p.stream>>>(
+        tq, tk, p.log_alpha, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.num_seqs,
+        (int)chunk_bound, cc, static_cast<unsigned char *>(records), p.status);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     dim3 grid_b(kD / kDV, p.num_heads, p.num_seqs);

@@ -7,6 +7,7 @@
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 
 #include <mutex>
 
@@ -42,6 +43,20 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
 {
     __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
     return *reinterpret_cast<uint32_t *>(&v);
+}
+
+// Eight fp16 values (round to nearest even); `ok` is cleared when one of them
+// is outside the fp16 range or not finite.
+__device__ __forceinline__ uint4 pack_f16x8(const float (&x)[8], bool &ok)
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        ok &= fabsf(x[2 * u]) <= 65504.f && fabsf(x[2 * u + 1]) <= 65504.f;
+        __half2 h = __floats2half2_rn(x[2 * u], x[2 * u + 1]);
+        w[u] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
 __device__ __forceinline__ float bf16_at(const unsigned char *p)
@@ -104,21 +119,32 @@ __device__ __forceinline__ void prefix_scan(const float *la, int la_stride, int 
 
 // ---------------------------------------------------------------- a2: operands
 // After a barrier following prefix_scan: Kg = k e^g and Qg = scale q e^g into
-// O1, Ki = k e^-g into O2 (bf16) and into o3 (tf32, transposed, K-major
-// 128 rows x 64), e^{g_last} into gam[128].  Returns true when the in-chunk
-// cumulative decay left the supported range.
-template <class L, int NT>
+// O1, Ki = k e^-g into O2 (bf16) and, when KI_T, into o3 (tf32, transposed,
+// K-major 128 rows x 64), e^{g_last} into gam[128].  When off_tot is given it
+// receives this thread's group offset and the chunk total of g for its channel
+// pair.  Returns true when the in-chunk cumulative decay left the supported range.
+template <class L, int NT, bool KI_T = true>
 __device__ __forceinline__ bool decayed_operands(unsigned char *sm, int len, const float *s_tot,
                                                  unsigned char *o3, float *gam,
-                                                 const float2 (&gl)[4096 / NT], float gmin, float gmax)
+                                                 const float2 (&gl)[4096 / NT], float gmin, float gmax,
+                                                 float2 *off_tot = nullptr)
 {
     constexpr int R = 4096 / NT, G = NT / 64;
     const int tid = threadIdx.x, lane = tid & 31, cp = tid & 63, rg = tid >> 6;
-    float2 off = make_float2(0.f, 0.f);
-    for (int q = 0; q < rg; ++q) {
+    float2 off = make_float2(0.f, 0.f), tot = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int q = 0; q < G; ++q) {
         const float2 t = *reinterpret_cast<const float2 *>(&s_tot[q * kD + 2 * cp]);
-        off.x += t.x;
-        off.y += t.y;
+        if (q < rg) {
+            off.x += t.x;
+            off.y += t.y;
+        }
+        tot.x += t.x;
+        tot.y += t.y;
+    }
+    if (off_tot) {
+        off_tot[0] = off;
+        off_tot[1] = tot;
     }
     if (rg == G - 1)
         *reinterpret_cast<float2 *>(&gam[2 * cp]) =
@@ -153,6 +179,7 @@ __device__ __forceinline__ bool decayed_operands(unsigned char *sm, int len, con
             ka[u] = to_tf32(kix);
             kb[u] = to_tf32(kiy);
         }
+        if (!KI_T) continue;
         // lanes 4-7 of every 8 store their odd channel first, so each store covers
         // 8 distinct swizzle positions (no bank conflict in shared memory)
         const int rb = rg * R + r4, sel = (lane >> 2) & 1;
@@ -218,20 +245,23 @@ __device__ __forceinline__ void kk_epilogue(unsigned char *sm, uint32_t d1, cons
 // ---------------------------------------------------------------- a4: UT solve
 // T = (I + A)^-1 by recursive doubling on the unit lower-triangular system:
 // the four 16 x 16 diagonal blocks, then T_10 = -T_11 A_10 T_00 and
-// T_32 = -T_33 A_32 T_22, then T_[2:4][0:2] = -T_[2:4][2:4] A_[2:4][0:2] T_[0:2][0:2];
-// finally T' = T diag(beta) as bf16 (O4) and tf32 (image at tt with tt_rows rows
-// per 32-column panel).  Contains barriers.
-template <class L, int NT>
-__device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta, unsigned char *tt,
-                                         int tt_rows)
+// T_32 = -T_33 A_32 T_22, then T_[2:4][0:2] = -T_[2:4][2:4] A_[2:4][0:2] T_[0:2][0:2].
+// solve_ut_core leaves T (lower triangle, unit diagonal) in SOLVE_T.  With
+// INPLACE (SOLVE_T == SOLVE_A) each block of T overwrites the block of A it
+// replaces once no later step reads that block of A; the strictly upper blocks
+// of T are never read.  solve_ut then writes T' = T diag(beta) as bf16 (O4) and
+// tf32 (image at tt with tt_rows rows per 32-column panel).  Both contain barriers.
+template <class L, int NT, bool INPLACE>
+__device__ __forceinline__ void solve_ut_core(unsigned char *sm)
 {
+    static_assert(!INPLACE || L::SOLVE_A == L::SOLVE_T, "in-place solve needs SOLVE_A == SOLVE_T");
     const int tid = threadIdx.x;
     const float *sA = reinterpret_cast<const float *>(sm + L::SOLVE_A);
     float *sT = reinterpret_cast<float *>(sm + L::SOLVE_T);
     float *sX = reinterpret_cast<float *>(sm + L::SOLVE_X);
+    float x[16];
+    const int b = (tid >> 4) * 16, cc = tid & 15;
     if (tid < 64) {  // diagonal blocks, one column per thread
-        const int b = (tid >> 4) * 16, cc = tid & 15;
-        float x[16];
 #pragma unroll
         for (int r = 0; r < 16; ++r) {
             float acc = 0.f;
@@ -239,6 +269,9 @@ __device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta,
             for (int m = 0; m < r; ++m) acc += sA[(b + r) * kLdS + b + m] * x[m];
             x[r] = r < cc ? 0.f : (r == cc ? 1.f : -acc);
         }
+    }
+    if (INPLACE) __syncthreads();  // every column has read its diagonal block of A
+    if (tid < 64) {
 #pragma unroll
         for (int r = 0; r < 16; ++r) sT[(b + r) * kLdS + b + cc] = x[r];
     }
@@ -303,6 +336,15 @@ __device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta,
         *reinterpret_cast<float4 *>(sT + (32 + r) * kLdS + c) = make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
     }
     __syncthreads();
+}
+
+template <class L, int NT>
+__device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta, unsigned char *tt,
+                                         int tt_rows)
+{
+    solve_ut_core<L, NT, false>(sm);
+    const int tid = threadIdx.x;
+    const float *sT = reinterpret_cast<const float *>(sm + L::SOLVE_T);
 #pragma unroll
     for (int e = tid; e < 512; e += NT) {  // T' = T diag(beta): bf16 (for W) and tf32 (for U~)
         const int r = e >> 3, s8 = (e & 7) * 8;

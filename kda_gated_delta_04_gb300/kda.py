@@ -19,7 +19,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(PKG, "libkda.so")
 
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, \
-    KDA_ERR_DECAY_RANGE = range(6)
+    KDA_ERR_DECAY_RANGE, KDA_ERR_VALUE_RANGE = range(7)
 KDA_DTYPE_BF16, KDA_DTYPE_F32 = 0, 1
 CHUNK = 64
 

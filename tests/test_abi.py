@@ -39,7 +39,7 @@ def test_library_exports_every_declared_symbol(kda):
 
 
 def test_status_strings(kda):
-    for code in range(6):
+    for code in range(7):
         s = kda.status_string(code)
         assert s.startswith("KDA_")
     assert "unknown" in kda.status_string(99)
