@@ -417,13 +417,19 @@ constexpr uint32_t IDESC_P2V = idesc_f16(64, 32, false, false);   // P2 V
 constexpr uint32_t IDESC_QS = idesc_bf16(64, 32, false, false);   // Q' S
 // TMEM columns: state increment (M = 128), outputs of two chunks (M = 64)
 constexpr uint32_t TM_5 = 0, TM_O = 32, kStateTmem = 128;
+// Warps 0-15 hold the state; warp 16 issues the output MMAs; warp 17 copies and converts.
+constexpr int kStateWarps = 16, kOutWarp = 16, kCopyWarp = 17, kStateThreads = 18 * 32;
+constexpr int kL2Ahead = 3;  // records brought into L2 this many chunks ahead
 
 // The serial pass over the chunks of one (sequence, head, 32-column value slice).
-// Chunk c: thread 0 issues P V + N S_c (the critical chain) and thread 32 issues
-// P2 V + Q' S_c (the output); while they run, all threads write the outputs of
-// chunk c - 1 and convert the v slice of chunk c + 1; then S_{c+1} = gamma . S_c
-// + (P V + N S_c).  Records are copied one chunk ahead, v slices kVRing ahead.
-__global__ void __launch_bounds__(kThreads, 1)
+// One block-wide barrier per chunk c, after which
+//   thread 0       issues the chain P V + N S_c and commits it,
+//   warp 16        issues the output P2 V + Q' S_c right behind it,
+//   warp 17        copies record c + 1 (prefetching later ones into L2) and
+//                  converts the v slice of chunk c + 1,
+//   warps 0-15     write the outputs of chunk c - 1, then, once the chain is
+//                  done, S_{c+1} = gamma . S_c + (P V + N S_c).
+__global__ void __launch_bounds__(kStateThreads, 1)
 prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__restrict__ cu,
                      int64_t total, int H, const int32_t *__restrict__ cc,
                      const unsigned char *__restrict__ records, const float *init_state,
@@ -432,15 +438,16 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
 {
     using L = StateLayout;
     extern __shared__ unsigned char smem_raw[];
-    // one output barrier per output buffer: chunk c commits to bar_o[c & 1] before
-    // chunk c - 1's outputs are awaited, so a single barrier could run two phases ahead
-    __shared__ __align__(8) uint64_t bar_rec[2], bar_v[kVRing], bar_s, bar_o[2], bar_drain;
+    // one output barrier per output buffer, so that no barrier is ever waited on
+    // more than one phase behind
+    __shared__ __align__(8) uint64_t bar_rec[2], bar_v[kVRing], bar_s, bar_issued, bar_o[2], bar_drain;
     __shared__ uint32_t tmem_holder;
 
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int quarter = warp & 3, part = warp >> 2;
+    const bool state_warp = warp < kStateWarps;
+    const int quarter = warp & 3, part = (warp >> 2) & 3;
     const int j0 = blockIdx.x * kDV, h = blockIdx.y, n = order[blockIdx.z];
     int64_t t0, t1;
     seq_range(cu, n, total, t0, t1);
@@ -448,7 +455,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     const unsigned char *rec0 = records + ((size_t)cc[n] * H + h) * kRecBytes;
     const size_t rec_stride = (size_t)H * kRecBytes;
 
-    // copies, issued by thread 0 only (which alone keeps these counts exact)
+    // copies: issued by lane 0 of the copy warp only, which alone keeps these counts
     int rec_issued = 0, v_issued = 0;
     auto load_record = [&](int k) {
         mbar_arrive_expect_tx(&bar_rec[k & 1], kRecBytes);
@@ -461,18 +468,17 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
                     (int)(t0 + (int64_t)k * kC));
         v_issued = k + 1;
     };
+    const bool copier = warp == kCopyWarp && lane == 0;
     if (tid == 0) {
         mbar_init(&bar_rec[0], 1);
         mbar_init(&bar_rec[1], 1);
         for (int k = 0; k < kVRing; ++k) mbar_init(&bar_v[k], 1);
         mbar_init(&bar_s, 1);
+        mbar_init(&bar_issued, 1);
         mbar_init(&bar_o[0], 1);
         mbar_init(&bar_o[1], 1);
         mbar_init(&bar_drain, 2);  // both MMA-issuing threads commit to it on a timeout
         fence_mbar_init();
-        prefetch_tmap(&tm_v);
-        for (int k = 0; k < 2 && k < nchunks; ++k) load_record(k);
-        for (int k = 0; k < kVRing && k < nchunks; ++k) load_v(k);
     }
     if (warp == 0) {
         tmem_alloc(&tmem_holder, kStateTmem);
@@ -482,20 +488,22 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     const int i_row = quarter * 32 + lane, jp = part * 8;
     float S[8];
     const size_t st_off = (((size_t)n * H + h) * kD + i_row) * kD + j0 + jp;
-    if (init_state) {
+    if (state_warp) {
+        if (init_state) {
 #pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const float4 x = *reinterpret_cast<const float4 *>(init_state + st_off + 4 * q);
-            S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
+            for (int q = 0; q < 2; ++q) {
+                const float4 x = *reinterpret_cast<const float4 *>(init_state + st_off + 4 * q);
+                S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) S[j] = 0.f;
         }
-    } else {
 #pragma unroll
-        for (int j = 0; j < 8; ++j) S[j] = 0.f;
+        for (int j = 0; j < 8; ++j) store_bf16(sm + L::O7 + km16(jp + j, i_row, kDV), S[j]);
     }
-#pragma unroll
-    for (int j = 0; j < 8; ++j) store_bf16(sm + L::O7 + km16(jp + j, i_row, kDV), S[j]);
     fence_proxy_async_smem();
-    __syncthreads();
+    __syncthreads();  // barriers initialised, S_0^T written
     tc_fence_after_sync();
     const uint32_t tmem = tmem_holder;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
@@ -515,115 +523,146 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
             *reinterpret_cast<uint4 *>(o + ((size_t)(cs + r64) * H + h) * kD + j0 + jp) = pack_bf16x8(v);
         return true;
     };
-    // v slice of chunk k -> V^T fp16 K-major in VIMG[k & 1]; one 4-row group of one column per thread
+    // copy warp: the v slice of chunk k -> V^T fp16 K-major in VIMG[k & 1]; lane = column
     auto convert_v = [&](int k) -> bool {
         if (!mbar_wait_ns(&bar_v[k % kVRing], (uint32_t)((k / kVRing) & 1), kWaitNs)) return false;
         const int64_t ck = t0 + (int64_t)k * kC;
         const int lenk = (t1 - ck) < kC ? (int)(t1 - ck) : kC;
-        const int j = tid % kDV, s4 = (tid / kDV) * 4;
-        float x[4];
+        const unsigned char *box = sm + L::VBOX + (k % kVRing) * 4096;
+#pragma unroll 4
+        for (int s8 = 0; s8 < kC; s8 += 8) {
+            float x[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            x[u] = (s4 + u) < lenk ? bf16_at(sm + L::VBOX + (k % kVRing) * 4096 + ((s4 + u) * kDV + j) * 2) : 0.f;
-            range_ok &= fabsf(x[u]) <= 65504.f;
+            for (int u = 0; u < 8; ++u) {
+                x[u] = (s8 + u) < lenk ? bf16_at(box + ((s8 + u) * kDV + lane) * 2) : 0.f;
+            }
+            *reinterpret_cast<uint4 *>(sm + L::VIMG + (k & 1) * 4096 + km16(lane, s8, kDV)) = pack_f16x8(x, range_ok);
         }
-        __half2 a = __floats2half2_rn(x[0], x[1]), b = __floats2half2_rn(x[2], x[3]);
-        *reinterpret_cast<uint2 *>(sm + L::VIMG + (k & 1) * 4096 + km16(j, s4, kDV)) =
-            make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
         return true;
+    };
+    // the copy warp's share of an iteration: record c + 1 (chunk c - 1's MMAs are
+    // done with its stage), L2 prefetch, the v slice of chunk c + 1, the next v copy
+    auto copy_step = [&](int c) -> bool {
+        bool ok = true;
+        if (c >= 1) ok = mbar_wait_ns(&bar_o[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1), kWaitNs);
+        if (copier && ok) {
+            if (c >= 1 && c + 1 < nchunks) load_record(c + 1);
+            if (c + kL2Ahead < nchunks) bulk_prefetch_l2(rec0 + (size_t)(c + kL2Ahead) * rec_stride, kRecBytes);
+        }
+        if (ok && c + 1 < nchunks) ok = convert_v(c + 1);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (copier && ok && c + 1 + kVRing < nchunks) load_v(c + 1 + kVRing);
+        return ok;
     };
 
     bool timed_out = false;
-    {
-        const bool ok = nchunks == 0 || convert_v(0);
-        fence_proxy_async_smem();
+    {  // prologue: first copies, the v slice of chunk 0
+        bool ok = true;
+        if (warp == kCopyWarp) {
+            if (copier) {
+                for (int k = 0; k < 2 && k < nchunks; ++k) load_record(k);
+                for (int k = 2; k < kL2Ahead && k < nchunks; ++k)
+                    bulk_prefetch_l2(rec0 + (size_t)k * rec_stride, kRecBytes);
+                for (int k = 0; k < kVRing && k < nchunks; ++k) load_v(k);
+                prefetch_tmap(&tm_v);
+            }
+            __syncwarp();
+            if (nchunks > 0) ok = convert_v(0);
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (copier && ok && kVRing < nchunks) load_v(kVRing);
+        }
         if (__syncthreads_or(!ok)) timed_out = true;
-        else if (tid == 0 && kVRing < nchunks) load_v(kVRing);
     }
     int c = 0;
     for (; c < nchunks && !timed_out; ++c) {
         const int st = c & 1;
         const uint32_t sg = sb + st * L::STAGE;
         const uint32_t s_cur = sb + L::O7 + st * 8192, v_cur = sb + L::VIMG + st * 4096;
-
-        // chunk c - 1's MMAs have finished: its record stage takes chunk c + 1
-        if (tid == 0 && c >= 1 && c + 1 < nchunks &&
-            mbar_wait_ns(&bar_o[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1), kWaitNs))
-            load_record(c + 1);
-        bool ok = mbar_wait_ns(&bar_rec[st], (uint32_t)((c >> 1) & 1), kWaitNs);
-        if (__syncthreads_or(!ok)) { timed_out = true; break; }
-
-        if (tid == 0) {  // the chain: P V + N S_c
-            tc_fence_after_sync();
+        bool ok = true;
+        if (state_warp) {
+            if (tid == 0) {  // the chain: P V + N S_c
+                ok = mbar_wait_ns(&bar_rec[st], (uint32_t)((c >> 1) & 1), kWaitNs);
+                if (ok) {
+                    tc_fence_after_sync();
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem + TM_5, kdesc(sg + R_P + s * 32), kdesc(v_cur + s * 32), IDESC_PV, s > 0);
+                    for (int s = 0; s < 4; ++s)
+                        mma_bf16(tmem + TM_5, kdesc(sg + R_P + s * 32), kdesc(v_cur + s * 32), IDESC_PV, s > 0);
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t p = s >> 2, w = (s & 3) * 32;
-                mma_bf16(tmem + TM_5, kdesc(sg + R_N + p * 16384 + w), kdesc(s_cur + p * 4096 + w), IDESC_NS, 1);
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t p = s >> 2, w = (s & 3) * 32;
+                        mma_bf16(tmem + TM_5, kdesc(sg + R_N + p * 16384 + w), kdesc(s_cur + p * 4096 + w),
+                                 IDESC_NS, 1);
+                    }
+                    mma_commit(&bar_s);
+                    mbar_arrive(&bar_issued);
+                }
             }
-            mma_commit(&bar_s);
-        } else if (tid == 32) {  // the output: P2 V + Q' S_c
-            tc_fence_after_sync();
+            if (ok && c >= 1) ok = write_o(c - 1);
+            if (ok) ok = mbar_wait_ns(&bar_s, (uint32_t)(c & 1), kWaitNs);
+            // gamma is read from the record: observe its copy (long complete) here too
+            if (ok) ok = mbar_wait_ns(&bar_rec[st], (uint32_t)((c >> 1) & 1), kWaitNs);
+            if (ok) {  // S <- gamma . S + (P V + N S); S^T (bf16) for the next chunk, row pairs
+                tc_fence_after_sync();
+                float v[8];
+                tmem_ld8(tmem + TM_5 + lane_off + jp, v);
+                tmem_ld_wait();
+                const float gc = reinterpret_cast<const float *>(sm + st * L::STAGE + R_GM)[i_row];
 #pragma unroll
-            for (int s = 0; s < 4; ++s)
-                mma_bf16(tmem + TM_O + 32 * st, kdesc(sg + R_P2 + s * 32), kdesc(v_cur + s * 32), IDESC_P2V, s > 0);
+                for (int j = 0; j < 8; ++j) S[j] = fmaf(gc, S[j], v[j]);
+                unsigned char *s_next = sm + L::O7 + (st ^ 1) * 8192;
+                const int ie = i_row & ~1;
 #pragma unroll
-            for (int s = 0; s < 8; ++s) {
-                const uint32_t p = s >> 2, w = (s & 3) * 32;
-                mma_bf16(tmem + TM_O + 32 * st, kdesc(sg + R_Q + p * 8192 + w), kdesc(s_cur + p * 4096 + w),
-                         IDESC_QS, 1);
+                for (int u = 0; u < 4; ++u) {
+                    const float mine = odd ? S[4 + u] : S[u];
+                    const float give = odd ? S[u] : S[4 + u];
+                    const float other = __shfl_xor_sync(0xffffffffu, give, 1);
+                    const float lo = odd ? other : mine, hi = odd ? mine : other;
+                    *reinterpret_cast<uint32_t *>(s_next + km16(jp + 4 * odd + u, ie, kDV)) = pack_bf16x2(lo, hi);
+                }
             }
-            mma_commit(&bar_o[st]);
-        }
-        // while they run: outputs of chunk c - 1 (which also frees V^T buffer (c + 1) & 1),
-        // then the v slice of chunk c + 1
-        ok = c < 1 || write_o(c - 1);
-        if (ok && c + 1 < nchunks) ok = convert_v(c + 1);
-        fence_proxy_async_smem();
-        if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        if (tid == 0 && c + 1 + kVRing < nchunks) load_v(c + 1 + kVRing);
-
-        ok = mbar_wait_ns(&bar_s, (uint32_t)(c & 1), kWaitNs);
-        if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        tc_fence_after_sync();
-        {  // S <- gamma . S + (P V + N S); S^T (bf16) for the next chunk, row pairs
-            float v[8];
-            tmem_ld8(tmem + TM_5 + lane_off + jp, v);
-            tmem_ld_wait();
-            const float gc = reinterpret_cast<const float *>(sm + st * L::STAGE + R_GM)[i_row];
+        } else if (warp == kOutWarp) {  // the output: P2 V + Q' S_c, behind the chain
+            if (lane == 0) {
+                ok = mbar_wait_ns(&bar_issued, (uint32_t)(c & 1), kWaitNs);
+                if (ok) {
+                    tc_fence_after_sync();
 #pragma unroll
-            for (int j = 0; j < 8; ++j) S[j] = fmaf(gc, S[j], v[j]);
-            unsigned char *s_next = sm + L::O7 + (st ^ 1) * 8192;
-            const int ie = i_row & ~1;
+                    for (int s = 0; s < 4; ++s)
+                        mma_bf16(tmem + TM_O + 32 * st, kdesc(sg + R_P2 + s * 32), kdesc(v_cur + s * 32),
+                                 IDESC_P2V, s > 0);
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float mine = odd ? S[4 + u] : S[u];
-                const float give = odd ? S[u] : S[4 + u];
-                const float other = __shfl_xor_sync(0xffffffffu, give, 1);
-                const float lo = odd ? other : mine, hi = odd ? mine : other;
-                *reinterpret_cast<uint32_t *>(s_next + km16(jp + 4 * odd + u, ie, kDV)) = pack_bf16x2(lo, hi);
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t p = s >> 2, w = (s & 3) * 32;
+                        mma_bf16(tmem + TM_O + 32 * st, kdesc(sg + R_Q + p * 8192 + w),
+                                 kdesc(s_cur + p * 4096 + w), IDESC_QS, 1);
+                    }
+                    mma_commit(&bar_o[st]);
+                }
             }
+            __syncwarp();
+        } else {
+            ok = copy_step(c);
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
-        __syncthreads();
+        if (__syncthreads_or(!ok)) { timed_out = true; break; }
     }
     if (!timed_out && nchunks > 0) {
-        const bool ok = write_o(nchunks - 1);
+        const bool ok = !state_warp || write_o(nchunks - 1);
         if (__syncthreads_or(!ok)) timed_out = true;
     }
     if (timed_out) {
         if (tid == 0) atomicOr(status, DEV_ERR_TIMEOUT);
-        if (tid == 0 || tid == 32) mma_commit(&bar_drain);  // completes once both threads' MMAs have
+        // both MMA-issuing threads commit; completes once all their MMAs have
+        if (tid == 0 || (warp == kOutWarp && lane == 0)) mma_commit(&bar_drain);
         (void)mbar_wait_ns(&bar_drain, 0, kWaitNs);
-        // our own copies still in flight (thread 0 issued them and knows how many)
+        // our own copies still in flight (the copying thread knows how many)
         for (int k = rec_issued > 2 ? rec_issued - 2 : 0; k < rec_issued; ++k)
             (void)mbar_wait_ns(&bar_rec[k & 1], (uint32_t)((k >> 1) & 1), kWaitNs);
         for (int k = v_issued > kVRing ? v_issued - kVRing : 0; k < v_issued; ++k)
             (void)mbar_wait_ns(&bar_v[k % kVRing], (uint32_t)((k / kVRing) & 1), kWaitNs);
-    } else {
+    } else if (state_warp) {
         float *dst = final_state + st_off;
 #pragma unroll
         for (int q = 0; q < 2; ++q)
@@ -662,7 +701,7 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
     dim3 grid_b(kD / kDV, p.num_heads, p.num_seqs);
-    prefill_state_kernel<<<grid_b, kThreads, kStateSmem, p.stream>>>(
+    prefill_state_kernel<<<grid_b, kStateThreads, kStateSmem, p.stream>>>(
         tv, p.cu_seqlens, p.total_tokens, p.num_heads, cc,
         static_cast<const unsigned char *>(records), p.init_state,
         static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.status, p.order);
