@@ -417,18 +417,20 @@ constexpr uint32_t IDESC_P2V = idesc_f16(64, 32, false, false);   // P2 V
 constexpr uint32_t IDESC_QS = idesc_bf16(64, 32, false, false);   // Q' S
 // TMEM columns: state increment (M = 128), outputs of two chunks (M = 64)
 constexpr uint32_t TM_5 = 0, TM_O = 32, kStateTmem = 128;
-// Warps 0-15 hold the state; warp 16 issues the output MMAs; warp 17 copies and converts.
-constexpr int kStateWarps = 16, kOutWarp = 16, kCopyWarp = 17, kStateThreads = 18 * 32;
+// Warps 0-15 hold the state; warp 16 issues the MMAs; warp 17 copies and converts.
+constexpr int kStateWarps = 16, kIssueWarp = 16, kCopyWarp = 17, kStateThreads = 18 * 32;
 constexpr int kL2Ahead = 3;  // records brought into L2 this many chunks ahead
 
 // The serial pass over the chunks of one (sequence, head, 32-column value slice).
 // One block-wide barrier per chunk c, after which
-//   thread 0       issues the chain P V + N S_c and commits it,
-//   warp 16        issues the output P2 V + Q' S_c right behind it,
+//   warp 16        (one lane) issues the chain P V + N S_c, commits it, then
+//                  issues the output P2 V + Q' S_c behind it and commits that,
 //   warp 17        copies record c + 1 (prefetching later ones into L2) and
 //                  converts the v slice of chunk c + 1,
 //   warps 0-15     write the outputs of chunk c - 1, then, once the chain is
 //                  done, S_{c+1} = gamma . S_c + (P V + N S_c).
+// The issuing lane has a warp of its own: MMA issue slows down badly when the
+// rest of the issuing warp is busy with other work.
 __global__ void __launch_bounds__(kStateThreads, 1)
 prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__restrict__ cu,
                      int64_t total, int H, const int32_t *__restrict__ cc,
@@ -440,7 +442,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     extern __shared__ unsigned char smem_raw[];
     // one output barrier per output buffer, so that no barrier is ever waited on
     // more than one phase behind
-    __shared__ __align__(8) uint64_t bar_rec[2], bar_v[kVRing], bar_s, bar_issued, bar_o[2], bar_drain;
+    __shared__ __align__(8) uint64_t bar_rec[2], bar_v[kVRing], bar_s, bar_o[2], bar_drain;
     __shared__ uint32_t tmem_holder;
 
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -474,10 +476,9 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
         mbar_init(&bar_rec[1], 1);
         for (int k = 0; k < kVRing; ++k) mbar_init(&bar_v[k], 1);
         mbar_init(&bar_s, 1);
-        mbar_init(&bar_issued, 1);
         mbar_init(&bar_o[0], 1);
         mbar_init(&bar_o[1], 1);
-        mbar_init(&bar_drain, 2);  // both MMA-issuing threads commit to it on a timeout
+        mbar_init(&bar_drain, 1);
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -510,6 +511,8 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     const int r64 = quarter * 16 + (lane & 15);  // row held by this lane in an M = 64 accumulator
     const int odd = lane & 1;
     bool range_ok = true;
+    // operand descriptors of buffer 0; buffer 1 is a fixed byte distance further
+    const uint64_t d_rec0 = kdesc(sb), d_v0 = kdesc(sb + L::VIMG), d_s0 = kdesc(sb + L::O7);
 
     // o rows of chunk cp (M = 64 accumulator TM_O + 32*(cp&1)), once its MMAs finished
     auto write_o = [&](int cp) -> bool {
@@ -578,28 +581,9 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     int c = 0;
     for (; c < nchunks && !timed_out; ++c) {
         const int st = c & 1;
-        const uint32_t sg = sb + st * L::STAGE;
-        const uint32_t s_cur = sb + L::O7 + st * 8192, v_cur = sb + L::VIMG + st * 4096;
         bool ok = true;
         if (state_warp) {
-            if (tid == 0) {  // the chain: P V + N S_c
-                ok = mbar_wait_ns(&bar_rec[st], (uint32_t)((c >> 1) & 1), kWaitNs);
-                if (ok) {
-                    tc_fence_after_sync();
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma_bf16(tmem + TM_5, kdesc(sg + R_P + s * 32), kdesc(v_cur + s * 32), IDESC_PV, s > 0);
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t p = s >> 2, w = (s & 3) * 32;
-                        mma_bf16(tmem + TM_5, kdesc(sg + R_N + p * 16384 + w), kdesc(s_cur + p * 4096 + w),
-                                 IDESC_NS, 1);
-                    }
-                    mma_commit(&bar_s);
-                    mbar_arrive(&bar_issued);
-                }
-            }
-            if (ok && c >= 1) ok = write_o(c - 1);
+            if (c >= 1) ok = write_o(c - 1);
             if (ok) ok = mbar_wait_ns(&bar_s, (uint32_t)(c & 1), kWaitNs);
             // gamma is read from the record: observe its copy (long complete) here too
             if (ok) ok = mbar_wait_ns(&bar_rec[st], (uint32_t)((c >> 1) & 1), kWaitNs);
@@ -622,20 +606,31 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
                     *reinterpret_cast<uint32_t *>(s_next + km16(jp + 4 * odd + u, ie, kDV)) = pack_bf16x2(lo, hi);
                 }
             }
-        } else if (warp == kOutWarp) {  // the output: P2 V + Q' S_c, behind the chain
+        } else if (warp == kIssueWarp) {
             if (lane == 0) {
-                ok = mbar_wait_ns(&bar_issued, (uint32_t)(c & 1), kWaitNs);
+                ok = mbar_wait_ns(&bar_rec[st], (uint32_t)((c >> 1) & 1), kWaitNs);
                 if (ok) {
                     tc_fence_after_sync();
+                    // descriptors: base of each operand plus the constant byte offset >> 4
+                    const uint64_t dr = d_rec0 + st * (L::STAGE >> 4), dv = d_v0 + st * (4096 >> 4),
+                                   ds = d_s0 + st * (8192 >> 4);
 #pragma unroll
-                    for (int s = 0; s < 4; ++s)
-                        mma_bf16(tmem + TM_O + 32 * st, kdesc(sg + R_P2 + s * 32), kdesc(v_cur + s * 32),
+                    for (int s = 0; s < 4; ++s)  // the chain: P V + N S_c
+                        mma_bf16(tmem + TM_5, dr + ((R_P + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_PV, s > 0);
+#pragma unroll
+                    for (int s = 0; s < 8; ++s) {
+                        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32, offs = (s >> 2) * 4096 + (s & 3) * 32;
+                        mma_bf16(tmem + TM_5, dr + ((R_N + off) >> 4), ds + (offs >> 4), IDESC_NS, 1);
+                    }
+                    mma_commit(&bar_s);
+#pragma unroll
+                    for (int s = 0; s < 4; ++s)  // the output: P2 V + Q' S_c
+                        mma_bf16(tmem + TM_O + 32 * st, dr + ((R_P2 + s * 32) >> 4), dv + ((s * 32) >> 4),
                                  IDESC_P2V, s > 0);
 #pragma unroll
                     for (int s = 0; s < 8; ++s) {
-                        const uint32_t p = s >> 2, w = (s & 3) * 32;
-                        mma_bf16(tmem + TM_O + 32 * st, kdesc(sg + R_Q + p * 8192 + w),
-                                 kdesc(s_cur + p * 4096 + w), IDESC_QS, 1);
+                        const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32, offs = (s >> 2) * 4096 + (s & 3) * 32;
+                        mma_bf16(tmem + TM_O + 32 * st, dr + ((R_Q + off) >> 4), ds + (offs >> 4), IDESC_QS, 1);
                     }
                     mma_commit(&bar_o[st]);
                 }
@@ -654,8 +649,8 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     }
     if (timed_out) {
         if (tid == 0) atomicOr(status, DEV_ERR_TIMEOUT);
-        // both MMA-issuing threads commit; completes once all their MMAs have
-        if (tid == 0 || (warp == kOutWarp && lane == 0)) mma_commit(&bar_drain);
+        // completes once every MMA the issuing lane started has
+        if (warp == kIssueWarp && lane == 0) mma_commit(&bar_drain);
         (void)mbar_wait_ns(&bar_drain, 0, kWaitNs);
         // our own copies still in flight (the copying thread knows how many)
         for (int k = rec_issued > 2 ? rec_issued - 2 : 0; k < rec_issued; ++k)
