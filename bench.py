@@ -12,8 +12,11 @@ value    prefill tokens/s with inputs resident in HBM (CUDA events, L2 flushed
 e2e      the same through the C ABI with pinned host buffers: host->device
          copy of the step's inputs, kda_prefill, device->host copy of o and the
          final state, all inside the timed region;
-roofline HBM-bound: algorithmic bytes of one prefill / its event-timed
-         duration, against the measured copy bandwidth in MEASURED_PEAKS.json;
+roofline HBM-bound, for the dominant (longest) kernel of the prefill: its share
+         of the algorithmic bytes / its event-timed duration (four events that
+         kda_prefill_events records around the kernels on the launching stream),
+         against the measured copy bandwidth in MEASURED_PEAKS.json; the whole
+         call against all algorithmic bytes is reported beside it ("path");
 cpu_baseline  the fp64 oracle on the host cores (rank 0, N=1 only).
 
 `--impl reference` times the oracle itself (the only other implementation of
@@ -59,6 +62,15 @@ def prefill_algorithmic_bytes(T, H, d, n_seqs, io_bytes, with_init):
     per_token_head = (3 * d * io_bytes) + d * 4 + 4 + d * io_bytes  # q,k,v + log_alpha + beta + o
     state = n_seqs * H * d * d * 4 * (2 if with_init else 1)
     return T * H * per_token_head + state
+
+
+def prefill_stage_bytes(T, H, d, n_seqs, io_bytes, with_init):
+    """Each kernel's share of the algorithmic bytes: the chunk kernel reads q, k, log_alpha
+    and beta; the state kernel reads v (and S0), writes o and the final state.  The
+    per-chunk records the first hands to the second are not algorithmic bytes."""
+    chunk = T * H * (2 * d * io_bytes + d * 4 + 4)
+    state = T * H * (2 * d * io_bytes) + n_seqs * H * d * d * 4 * (2 if with_init else 1)
+    return {"prefill_chunk_kernel": chunk, "prefill_state_kernel": state}
 
 
 def prefill_flops(T, H, d, C=64):
@@ -187,18 +199,22 @@ class _Gpu:
         self.fs = torch.empty((1, self.H, self.d, self.d), dtype=torch.float32, device=self.dev)
         self.ws = kda.workspace_for(1, self.T, self.H, self.d, kda.KDA_DTYPE_BF16, self.dev)
 
-    def prefill_call(self):
+    def prefill_call(self, events=None):
+        """One kda_prefill through the C ABI; with `events` (four CUDA events) the
+        kda_prefill_events variant, which also marks the stages."""
         kda, x = self.kda, self.x
-        st = kda.kda_prefill(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
-                             x["log_alpha"].data_ptr(), x["beta"].data_ptr(),
-                             x["cu_seqlens"].data_ptr(), 1, self.T, self.H, self.d, self.d,
-                             kda.KDA_DTYPE_BF16, None, self.o.data_ptr(), self.fs.data_ptr(),
-                             self.ws.data_ptr(), self.ws.numel(), self.sh)
+        args = (x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), x["log_alpha"].data_ptr(),
+                x["beta"].data_ptr(), x["cu_seqlens"].data_ptr(), 1, self.T, self.H, self.d, self.d,
+                kda.KDA_DTYPE_BF16, None, self.o.data_ptr(), self.fs.data_ptr(), self.ws.data_ptr(),
+                self.ws.numel(), self.sh)
+        st = kda.kda_prefill(*args) if events is None else kda.kda_prefill_events(*args, events)
         if st != kda.KDA_OK:
             raise kda.KdaError(st, "kda_prefill")
 
     def time_prefill(self, steps, warmup, barrier):
-        """Per-step event times (ms) of kda_prefill, L2 flushed (untimed) before each step."""
+        """Per-step event times (ms) of kda_prefill, L2 flushed (untimed) before each step:
+        (whole call, [schedule, chunk kernel, state kernel]) from the four events that
+        kda_prefill_events records on the launching stream around its kernels."""
         torch = self.torch
         for _ in range(warmup):
             self.flush.zero_()
@@ -206,18 +222,22 @@ class _Gpu:
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
-        ev = [(self.event(), self.event()) for _ in range(steps)]
-        for a, b in ev:
+        ev = [[self.event() for _ in range(4)] for _ in range(steps)]
+        for e in ev:
+            for x in e:  # create the handles before they are passed down
+                x.record(self.stream)
+        torch.cuda.synchronize()
+        for e in ev:
             self.flush.zero_()
-            a.record(self.stream)
-            self.prefill_call()
-            b.record(self.stream)
+            self.prefill_call([x.cuda_event for x in e])
         torch.cuda.synchronize()
         barrier()
         st = self.kda.kda_read_device_status(self.ws.data_ptr(), self.sh)
         if st != self.kda.KDA_OK:
             raise self.kda.KdaError(st, "kda_prefill (device status)")
-        return [a.elapsed_time(b) for a, b in ev]
+        whole = [e[0].elapsed_time(e[3]) for e in ev]
+        stages = [[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev]
+        return whole, stages
 
     def time_prefill_e2e(self, steps, warmup):
         """Host-to-host: pinned inputs -> device, kda_prefill, o and final state -> host."""
@@ -316,7 +336,7 @@ def run_gpu(args):
             "data": "synthetic (seeded counter-based generator; no dataset)"}
     with clocks:
         if do_prefill:
-            step_ms = g.time_prefill(args.steps, args.warmup, barrier)
+            step_ms, stage_ms = g.time_prefill(args.steps, args.warmup, barrier)
             e2e_ms = g.time_prefill_e2e(args.steps, args.warmup)
         if do_decode:
             dec_ms = g.time_decode(g.dw.steps, max(3, args.warmup), barrier)
@@ -327,6 +347,19 @@ def run_gpu(args):
         T, H, d = g.T, g.H, g.d
         alg_bytes = prefill_algorithmic_bytes(T, H, d, 1, 2, False)
         achieved = alg_bytes / (mean_step_ms / 1e3) / 1e9
+        # per kernel: mean event time (max over ranks) and its share of the algorithmic bytes
+        names = ("prefill_prep_kernel", "prefill_chunk_kernel", "prefill_state_kernel")
+        stage_mean = [reduce_max(sum(s[i] for s in stage_ms)) / args.steps for i in range(3)]
+        stage_bytes = prefill_stage_bytes(T, H, d, 1, 2, False)
+        kernels = {}
+        for name, ms in zip(names, stage_mean):
+            kb = stage_bytes.get(name)
+            kernels[name] = {"ms_per_launch": ms}
+            if kb:
+                kernels[name].update({"algorithmic_bytes_per_launch": kb,
+                                      "achieved_gbs": kb / (ms / 1e3) / 1e9,
+                                      "frac": kb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]})
+        dom = max(stage_bytes, key=lambda n: kernels[n]["ms_per_launch"])
         line.update({
             "value": aggregate_rate(T, world, args.steps, total_ms),
             "ms_per_step": mean_step_ms,
@@ -335,18 +368,24 @@ def run_gpu(args):
                        "gate_state_dtype": "f32",
                        "l2": "flushed between timed steps (256 MiB write, untimed)",
                        "parallelism": f"replicas x{world} (independent units, no collective)"},
-            "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                         "traffic": profiled_traffic("prefill_4k"),
+            "roofline": {"bound": "hbm", "kernel": dom,
+                         "achieved": kernels[dom]["achieved_gbs"], "peak": peaks["hbm_gbs"],
+                         "unit": "GB/s", "frac": kernels[dom]["frac"],
+                         "traffic": profiled_traffic(dom + "_4k"),
                          "peak_source": peaks["source"],
-                         "algorithmic_bytes_per_launch": alg_bytes,
-                         "tensor_frac_of_bf16_peak": prefill_flops(T, H, d) /
-                         (mean_step_ms / 1e3) / 1e12 / peaks["bf16_tflops"],
-                         "note": "duration from CUDA events around kda_prefill (its schedule "
-                                 "kernel and the chunk kernel)"},
+                         "algorithmic_bytes_per_launch": stage_bytes[dom],
+                         "kernels": kernels,
+                         "path": {"achieved": achieved, "frac": achieved / peaks["hbm_gbs"],
+                                  "algorithmic_bytes_per_launch": alg_bytes,
+                                  "tensor_frac_of_bf16_peak": prefill_flops(T, H, d) /
+                                  (mean_step_ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
+                         "note": "durations from the four CUDA events kda_prefill_events records "
+                                 "on the launching stream around its kernels; the dominant "
+                                 "(longest) kernel is measured against its share of the path's "
+                                 "algorithmic bytes, the path against all of them"},
             "e2e": {"value": aggregate_rate(T, world, args.steps, e2e_total), "unit": "tokens/s",
                     "h2d_bytes_per_step": g.h2d, "d2h_bytes_per_step": g.d2h},
-            "gpu_launches": 2 * args.steps,  # schedule/validation kernel + chunk kernel
+            "gpu_launches": 3 * args.steps,  # schedule, chunk and state kernel per step
         })
     line["clocks"] = clocks.summary()
     if do_decode:

@@ -121,6 +121,25 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, const floa
                          void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kda_prefill with its stages marked, for measuring them: the same arguments and
+ * results, plus four CUDA events (cudaEvent_t handles passed as void*, created by
+ * the caller) recorded on `stream`:
+ *   events[0]  before the schedule kernel (cu_seqlens check, sequence order),
+ *   events[1]  after it,
+ *   events[2]  after the chunk-local kernel of the two-kernel path (on the
+ *              single-kernel paths directly after events[1]),
+ *   events[3]  after the last kernel.
+ * All four are recorded even when no kernel runs.  num_events must be 4 and no
+ * handle NULL, else KDA_ERR_INVALID_ARG before anything is enqueued.
+ */
+kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, const float *log_alpha,
+                                const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                                kda_dtype_t dtype, const float *init_state, void *o,
+                                float *final_state, void *workspace, size_t workspace_bytes,
+                                void *stream, void *const *events, int32_t num_events);
+
+/*
  * One decode step for `batch` sequences x num_heads heads: the recurrence for a
  * single new token per sequence, applied to the caller's state in place
  * ("Day 19", section 2: constant memory and O(1) work per generated token;

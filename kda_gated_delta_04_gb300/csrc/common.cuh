@@ -56,7 +56,9 @@ bool prefill_tc_supported(const PrefillProblem &p);  // bf16, d = 128, 0 < total
 cudaError_t launch_prefill_tc(const PrefillProblem &p);
 // Two-kernel tensor-core prefill (needs p.cc and p.records).
 size_t prefill_split_records_bytes(int64_t total_tokens, int num_seqs, int num_heads);
-cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records);
+// `mid` (may be null) is recorded on p.stream between the chunk kernel and the state kernel.
+cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records,
+                                 cudaEvent_t mid = nullptr);
 cudaError_t launch_decode(const DecodeProblem &p);
 
 // ---------------------------------------------------------------- device helpers

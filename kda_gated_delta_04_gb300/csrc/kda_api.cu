@@ -72,11 +72,14 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
     return ws_min_bytes(num_seqs);
 }
 
-kda_status_t kda_prefill(const void *q, const void *k, const void *v, const float *log_alpha,
-                         const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
-                         int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
-                         kda_dtype_t dtype, const float *init_state, void *o, float *final_state,
-                         void *workspace, size_t workspace_bytes, void *stream)
+namespace {
+
+// The prefill behind both entry points; ev (four events, or NULL) marks the stages.
+kda_status_t prefill_impl(const void *q, const void *k, const void *v, const float *log_alpha,
+                          const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                          int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                          kda_dtype_t dtype, const float *init_state, void *o, float *final_state,
+                          void *workspace, size_t workspace_bytes, void *stream, const cudaEvent_t *ev)
 {
     kda_status_t st = check_shape(d_k, d_v, dtype);
     if (st != KDA_OK) return st;
@@ -97,7 +100,9 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, const floa
     if (workspace_bytes < ws_min_bytes(num_seqs)) return KDA_ERR_INVALID_ARG;
     st = check_device();
     if (st != KDA_OK) return st;
-    if (num_seqs == 0) return KDA_OK;
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    auto mark = [&](int i) { return !ev || cudaEventRecord(ev[i], strm) == cudaSuccess; };
+    if (num_seqs == 0) return mark(0) && mark(1) && mark(2) && mark(3) ? KDA_OK : KDA_ERR_CUDA;
 
     kda::PrefillProblem p;
     p.q = q; p.k = k; p.v = v; p.log_alpha = log_alpha; p.beta = beta;
@@ -107,7 +112,7 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, const floa
     p.status = static_cast<uint32_t *>(workspace);
     char *ws = static_cast<char *>(workspace);
     p.order = reinterpret_cast<int32_t *>(ws + kda::kWorkspaceHeader);
-    p.stream = static_cast<cudaStream_t>(stream);
+    p.stream = strm;
     // bf16 at d = 128 runs on the tensor cores: as the chunk / state kernel pair when the
     // workspace holds the per-chunk records, else as the single fused kernel.  fp32 I/O
     // (the exact path) and d = 64 run the CUDA-core chunk kernel.
@@ -116,16 +121,49 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, const floa
     p.cc = split ? reinterpret_cast<int32_t *>(ws + ws_min_bytes(num_seqs)) : nullptr;
     p.records = split ? ws + ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) : nullptr;
 
+    if (!mark(0)) return KDA_ERR_CUDA;
     if (kda::launch_prefill_prep(p) != cudaSuccess) return KDA_ERR_CUDA;
+    if (!mark(1)) return KDA_ERR_CUDA;
     cudaError_t err;
-    if (split)
-        err = kda::launch_prefill_split(p, p.cc, p.records);
-    else if (kda::prefill_tc_supported(p))
-        err = kda::launch_prefill_tc(p);
-    else
-        err = kda::launch_prefill_simt(p);
+    if (split) {
+        err = kda::launch_prefill_split(p, p.cc, p.records, ev ? ev[2] : nullptr);
+    } else {
+        if (!mark(2)) return KDA_ERR_CUDA;
+        err = kda::prefill_tc_supported(p) ? kda::launch_prefill_tc(p) : kda::launch_prefill_simt(p);
+    }
     if (err != cudaSuccess) return KDA_ERR_CUDA;
+    if (!mark(3)) return KDA_ERR_CUDA;
     return KDA_OK;
+}
+
+}  // namespace
+
+kda_status_t kda_prefill(const void *q, const void *k, const void *v, const float *log_alpha,
+                         const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                         int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                         kda_dtype_t dtype, const float *init_state, void *o, float *final_state,
+                         void *workspace, size_t workspace_bytes, void *stream)
+{
+    return prefill_impl(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
+                        d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream,
+                        nullptr);
+}
+
+kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, const float *log_alpha,
+                                const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                                kda_dtype_t dtype, const float *init_state, void *o,
+                                float *final_state, void *workspace, size_t workspace_bytes,
+                                void *stream, void *const *events, int32_t num_events)
+{
+    if (!events || num_events != 4) return KDA_ERR_INVALID_ARG;
+    cudaEvent_t ev[4];
+    for (int i = 0; i < 4; ++i) {
+        if (!events[i]) return KDA_ERR_INVALID_ARG;
+        ev[i] = static_cast<cudaEvent_t>(events[i]);
+    }
+    return prefill_impl(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
+                        d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream, ev);
 }
 
 kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,

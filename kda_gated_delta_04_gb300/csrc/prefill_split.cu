@@ -676,7 +676,7 @@ size_t prefill_split_records_bytes(int64_t total_tokens, int num_seqs, int num_h
     return (size_t)(total_tokens / kC + num_seqs) * (size_t)num_heads * kRecBytes;
 }
 
-cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records)
+cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records, cudaEvent_t mid)
 {
     static int dev_chunk = -1, dev_state = -1;
     cudaError_t err = allow_smem(prefill_chunk_kernel, (int)kChunkSmem, &dev_chunk);
@@ -695,6 +695,7 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
         (int)chunk_bound, cc, static_cast<unsigned char *>(records), p.status);
     err = cudaGetLastError();
     if (err != cudaSuccess) return err;
+    if (mid && (err = cudaEventRecord(mid, p.stream)) != cudaSuccess) return err;
     dim3 grid_b(kD / kDV, p.num_heads, p.num_seqs);
     prefill_state_kernel<<<grid_b, kStateThreads, kStateSmem, p.stream>>>(
         tv, p.cu_seqlens, p.total_tokens, p.num_heads, cc,

@@ -40,6 +40,7 @@ EXPORTS = {
     "kda_read_device_status": (_c.c_int, [_VP, _VP]),
     "kda_status_string": (_c.c_char_p, [_c.c_int]),
     "kda_prefill_no_alloc": (_c.c_int, _PREFILL_ARGS[:15] + [_VP, _VP]),
+    "kda_prefill_events": (_c.c_int, _PREFILL_ARGS + [_c.POINTER(_VP), _c.c_int32]),
 }
 
 
@@ -90,6 +91,18 @@ def kda_prefill_no_alloc(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_t
     return lib().kda_prefill_no_alloc(q, k, v, log_alpha, beta, cu_seqlens, num_seqs,
                                       total_tokens, num_heads, d_k, d_v, dtype, init_state, o,
                                       final_state, device_errors, stream)
+
+
+def kda_prefill_events(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads,
+                       d_k, d_v, dtype, init_state, o, final_state, workspace, workspace_bytes,
+                       stream, events):
+    """kda_prefill that also records four CUDA events (handles as ints) on `stream` around
+    its stages: before the schedule kernel, after it, after the chunk-local kernel, after
+    the last kernel (see include/kda.h)."""
+    arr = (_VP * len(events))(*events)
+    return lib().kda_prefill_events(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens,
+                                    num_heads, d_k, d_v, dtype, init_state, o, final_state,
+                                    workspace, workspace_bytes, stream, arr, len(events))
 
 
 def kda_read_device_status(workspace, stream):

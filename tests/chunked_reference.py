@@ -41,6 +41,11 @@ def tf32_round(x: np.ndarray) -> np.ndarray:
     return u.astype(np.uint32).view(np.float32).astype(np.float64)
 
 
+def f16_round(x: np.ndarray) -> np.ndarray:
+    """Round to the nearest IEEE fp16 (10 explicit mantissa bits, ties to even)."""
+    return np.asarray(x, dtype=np.float32).astype(np.float16).astype(np.float64)
+
+
 def _ident(x):
     return x
 
@@ -111,3 +116,50 @@ def chunked_prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, 
                                                  log_alpha[t0:t1, h], beta[t0:t1, h], S0, C,
                                                  rnd, state_rnd)
     return o, fs
+
+
+def folded_unit(q, k, v, log_alpha, beta, S0=None, C=64, kernel_rounding=False):
+    """The same chunk update folded into four matrices per chunk, the form the
+    two-kernel tensor-core prefill uses.  Substituting U = U~ - W S0 into the
+    output and state lines above gives, with Kd = K*gamma_C/Gamma:
+
+      S_C = Diag(gamma_C) S0 + P V + N S0      P  = Kd^T T',  N = -Kd^T W
+      O   = Q' S0 + P2 V                       Q' = scale Q*Gamma - Aqk W,  P2 = Aqk T'
+
+    (T' = (I + A)^-1 diag(beta); Aqk as above).  With kernel_rounding the operands
+    are rounded where the kernels round them: bf16 Q*Gamma, K*Gamma, K/Gamma, Aqk,
+    W, N, Q' and the state operand of N S0 and Q' S0; T' and Kd each split into a
+    bf16 high part and a bf16 low part, P formed from hi.hi + hi.lo + lo.hi; fp16
+    P, P2 and V; W and P2 use the high part of T'; the state itself stays fp32.
+    Returns (o [T, dv], S_final)."""
+    B = bf16_round if kernel_rounding else _ident
+    F = f16_round if kernel_rounding else _ident
+    T, dk = q.shape
+    dv = v.shape[1]
+    scale = 1.0 / np.sqrt(dk)
+    S = np.zeros((dk, dv)) if S0 is None else np.array(S0, dtype=np.float64)
+    o = np.zeros((T, dv))
+    for c0 in range(0, T, C):
+        c1 = min(c0 + C, T)
+        n = c1 - c0
+        qc, kc, vc, bc = q[c0:c1], k[c0:c1], v[c0:c1], beta[c0:c1]
+        g = np.cumsum(log_alpha[c0:c1], axis=0)
+        Kg, Ki, Qg = B(kc * np.exp(g)), B(kc * np.exp(-g)), B(scale * qc * np.exp(g))
+        A = bc[:, None] * np.tril(Kg @ Ki.T, -1)
+        Aqk = B(np.tril(Qg @ Ki.T, 0))
+        Tp = np.linalg.solve(np.eye(n) + A, np.eye(n)) * bc[None, :]
+        Kd = kc * np.exp(g[-1] - g)
+        th, kh = B(Tp), B(Kd)
+        tl, kl = B(Tp - th), B(Kd - kh)
+        W = B(th @ Kg)
+        if kernel_rounding:
+            P = F(kh.T @ th + kh.T @ tl + kl.T @ th)
+        else:
+            P = Kd.T @ Tp
+        N = B(-(kh.T @ W))
+        Qp = B(Qg - Aqk @ W)
+        P2 = F(Aqk @ th)
+        Vr, Sr = F(vc), B(S)
+        o[c0:c1] = Qp @ Sr + P2 @ Vr
+        S = np.exp(g[-1])[:, None] * S + N @ Sr + P @ Vr
+    return o, S

@@ -184,3 +184,37 @@ def test_single_kernel_path_with_minimal_workspace(w):
     o_ref, fs_ref = oracle_prefill(inp)
     assert_parity(o1, f1, o_ref, fs_ref, "bf16", w.name + " (single kernel)")
     assert np.abs(o1 - o2).max() < 2e-3 and relF(f1, f2) < 1e-3
+
+
+def test_stage_events_bracket_the_kernels_and_change_nothing():
+    """kda_prefill_events gives the same results as kda_prefill and records its four
+    events in order around the stages."""
+    w, inp = _custom("events", 119, [300, 77], H=3, init_state=True)
+    o_ref, fs_ref = gpu_prefill(inp)
+    d = to_device(inp)
+    T, H, D = d["q"].shape
+    o = torch.empty_like(d["q"])
+    fs = torch.empty((2, H, D, D), dtype=torch.float32, device="cuda")
+    ws = kda.workspace_for(2, T, H, D, kda.KDA_DTYPE_BF16, "cuda")
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    s = torch.cuda.current_stream()
+    for e in ev:  # make sure every handle exists before it is passed down
+        e.record(s)
+    st = kda.kda_prefill_events(d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(),
+                                d["log_alpha"].data_ptr(), d["beta"].data_ptr(),
+                                d["cu_seqlens"].data_ptr(), 2, T, H, D, D, kda.KDA_DTYPE_BF16,
+                                d["init_state"].data_ptr(), o.data_ptr(), fs.data_ptr(),
+                                ws.data_ptr(), ws.numel(), s.cuda_stream,
+                                [e.cuda_event for e in ev])
+    assert st == kda.KDA_OK
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(synth.to_f64(o), o_ref)
+    np.testing.assert_array_equal(synth.to_f64(fs), fs_ref)
+    spans = [ev[i].elapsed_time(ev[i + 1]) for i in range(3)]
+    assert all(x >= 0 for x in spans) and spans[1] > 0 and spans[2] > 0
+    bad = kda.kda_prefill_events(d["q"].data_ptr(), d["k"].data_ptr(), d["v"].data_ptr(),
+                                 d["log_alpha"].data_ptr(), d["beta"].data_ptr(),
+                                 d["cu_seqlens"].data_ptr(), 2, T, H, D, D, kda.KDA_DTYPE_BF16,
+                                 None, o.data_ptr(), fs.data_ptr(), ws.data_ptr(), ws.numel(),
+                                 s.cuda_stream, [e.cuda_event for e in ev[:3]])
+    assert bad == kda.KDA_ERR_INVALID_ARG
