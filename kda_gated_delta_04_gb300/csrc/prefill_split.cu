@@ -355,7 +355,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         kk_epilogue<L, NT>(sm, tmem, s_beta, sm + L::AQ);
         tc_fence_before_sync();
         __syncthreads();
-        solve_ut_core<L, NT, true>(sm);
+        solve_ut_doubling<L, NT>(sm);
         write_tprime_hilo<L, NT>(sm, s_beta);
         fence_proxy_async_smem();
         __syncthreads();

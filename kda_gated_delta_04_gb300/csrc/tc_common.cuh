@@ -338,6 +338,72 @@ __device__ __forceinline__ void solve_ut_core(unsigned char *sm)
     __syncthreads();
 }
 
+// solve_ut_doubling: the same T, in place (SOLVE_T == SOLVE_A), by recursive
+// doubling all the way from 4 x 4 blocks: the sixteen 4 x 4 diagonal blocks by
+// substitution, then for block size b = 4, 8, 16, 32 and every pair of b x b
+// diagonal blocks, X = A_10 T_00 and T_10 = -T_11 X (X in SOLVE_X, row p*b + r).
+// Each output quad is one thread's float4; the strictly upper parts of A, which
+// the k-k epilogue zeroed, stand in for the zero upper parts of T, so no product
+// needs a mask.  Contains barriers.
+template <class L, int NT>
+__device__ __forceinline__ void solve_ut_doubling(unsigned char *sm)
+{
+    static_assert(L::SOLVE_A == L::SOLVE_T, "the doubling solve works in place");
+    const int tid = threadIdx.x;
+    float *sT = reinterpret_cast<float *>(sm + L::SOLVE_T);  // holds A until overwritten
+    float *sX = reinterpret_cast<float *>(sm + L::SOLVE_X);
+    {  // 4 x 4 diagonal blocks: thread (block j, column cc)
+        const int j4 = (tid >> 2) * 4, cc = tid & 3;
+        float x[4];
+        if (tid < 64) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) {
+                float acc = 0.f;
+#pragma unroll
+                for (int m = 0; m < r; ++m) acc += sT[(j4 + r) * kLdS + j4 + m] * x[m];
+                x[r] = r < cc ? 0.f : (r == cc ? 1.f : -acc);
+            }
+        }
+        __syncthreads();  // every column has read its block of A
+        if (tid < 64) {
+#pragma unroll
+            for (int r = 0; r < 4; ++r) sT[(j4 + r) * kLdS + j4 + cc] = x[r];
+        }
+        __syncthreads();
+    }
+#pragma unroll
+    for (int b = 4; b <= 32; b *= 2) {
+        const int quads = b / 4, items = 32 * quads;
+        for (int e = tid; e < items; e += NT) {  // X = A_10 T_00
+            const int xr = e / quads, cq = (e % quads) * 4, p = xr / b, rr = xr % b;
+            const int R0 = 2 * b * p + b, C0 = 2 * b * p;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int m = 0; m < b; ++m) {
+                const float a = sT[(R0 + rr) * kLdS + C0 + m];
+                const float4 t = *reinterpret_cast<const float4 *>(sT + (C0 + m) * kLdS + C0 + cq);
+                acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
+            }
+            *reinterpret_cast<float4 *>(sX + xr * kLdX + cq) = acc;
+        }
+        __syncthreads();
+        for (int e = tid; e < items; e += NT) {  // T_10 = -T_11 X, over A_10
+            const int xr = e / quads, cq = (e % quads) * 4, p = xr / b, rr = xr % b;
+            const int R0 = 2 * b * p + b, C0 = 2 * b * p;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 8
+            for (int m = 0; m < b; ++m) {
+                const float t = sT[(R0 + rr) * kLdS + R0 + m];
+                const float4 x = *reinterpret_cast<const float4 *>(sX + (p * b + m) * kLdX + cq);
+                acc.x += t * x.x; acc.y += t * x.y; acc.z += t * x.z; acc.w += t * x.w;
+            }
+            *reinterpret_cast<float4 *>(sT + (R0 + rr) * kLdS + C0 + cq) =
+                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+        }
+        __syncthreads();
+    }
+}
+
 template <class L, int NT>
 __device__ __forceinline__ void solve_ut(unsigned char *sm, const float *s_beta, unsigned char *tt,
                                          int tt_rows)
