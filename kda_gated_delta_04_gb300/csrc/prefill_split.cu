@@ -186,16 +186,18 @@ __device__ __forceinline__ void issue_n_q(uint32_t sb, uint32_t tmem)
         mma_bf16(tmem + TC_Q, kdesc(sb + L::AQ + s * 32), mndesc(sb + L::O1 + s * 2048, 16384), id_q, s > 0);
 }
 
-// Epilogues straight into the record (global memory).  NT = 256: warp w reads
-// TMEM lane quarter w % 4 and column half w / 4.
+// Epilogues straight into the record (global memory).  Warp w reads TMEM lane
+// quarter w % 4 and the (w / 4)-th of NT / 128 equal column ranges.
+template <int NT>
 __device__ __forceinline__ void epi_p2(uint32_t tmem, unsigned char *rec, bool &ok)
 {
+    constexpr int CW = 64 / (NT / 128);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
     const int r = quarter * 16 + (lane & 15);  // M = 64: row 16q + l in lane l < 16
 #pragma unroll
-    for (int cb = 0; cb < 32; cb += 16) {
+    for (int cb = 0; cb < CW; cb += 16) {
         float v[16];
-        tmem_ld16(tmem + TC_P2 + ((uint32_t)(quarter * 32) << 16) + part * 32 + cb, v);
+        tmem_ld16(tmem + TC_P2 + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
         tmem_ld_wait();
         if (lane < 16) {
 #pragma unroll
@@ -203,65 +205,70 @@ __device__ __forceinline__ void epi_p2(uint32_t tmem, unsigned char *rec, bool &
                 float x[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
-                *reinterpret_cast<uint4 *>(rec + R_P2 + km16(r, part * 32 + cb + hh * 8, 64)) = pack_f16x8(x, ok);
+                *reinterpret_cast<uint4 *>(rec + R_P2 + km16(r, part * CW + cb + hh * 8, 64)) = pack_f16x8(x, ok);
             }
         }
     }
 }
 
+template <int NT>
 __device__ __forceinline__ void epi_p(uint32_t tmem, unsigned char *rec, bool &ok)
 {
+    constexpr int CW = 64 / (NT / 128);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
     const int i = quarter * 32 + lane;
 #pragma unroll
-    for (int cb = 0; cb < 32; cb += 16) {
+    for (int cb = 0; cb < CW; cb += 16) {
         float v[16];
-        tmem_ld16(tmem + TC_P + ((uint32_t)(quarter * 32) << 16) + part * 32 + cb, v);
+        tmem_ld16(tmem + TC_P + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
         tmem_ld_wait();
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             float x[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
-            *reinterpret_cast<uint4 *>(rec + R_P + km16(i, part * 32 + cb + hh * 8, 128)) = pack_f16x8(x, ok);
+            *reinterpret_cast<uint4 *>(rec + R_P + km16(i, part * CW + cb + hh * 8, 128)) = pack_f16x8(x, ok);
         }
     }
 }
 
+template <int NT>
 __device__ __forceinline__ void epi_n(uint32_t tmem, unsigned char *rec)
 {
+    constexpr int CW = 128 / (NT / 128);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
     const int i = quarter * 32 + lane;
 #pragma unroll
-    for (int cb = 0; cb < 64; cb += 16) {
+    for (int cb = 0; cb < CW; cb += 16) {
         float v[16];
-        tmem_ld16(tmem + TC_N + ((uint32_t)(quarter * 32) << 16) + part * 64 + cb, v);
+        tmem_ld16(tmem + TC_N + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
         tmem_ld_wait();
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
             float x[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
-            *reinterpret_cast<uint4 *>(rec + R_N + km16(i, part * 64 + cb + hh * 8, 128)) = pack_bf16x8(x);
+            *reinterpret_cast<uint4 *>(rec + R_N + km16(i, part * CW + cb + hh * 8, 128)) = pack_bf16x8(x);
         }
     }
 }
 
 // Q' = Qg + Aqk (-W); Qg from rows 64..127 of O1.
-template <class L>
+template <class L, int NT>
 __device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, unsigned char *rec)
 {
+    constexpr int CW = 128 / (NT / 128);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
     const int r = quarter * 16 + (lane & 15);
 #pragma unroll
-    for (int cb = 0; cb < 64; cb += 16) {
+    for (int cb = 0; cb < CW; cb += 16) {
         float v[16];
-        tmem_ld16(tmem + TC_Q + ((uint32_t)(quarter * 32) << 16) + part * 64 + cb, v);
+        tmem_ld16(tmem + TC_Q + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
         tmem_ld_wait();
         if (lane < 16) {
 #pragma unroll
             for (int hh = 0; hh < 2; ++hh) {
-                const int col = part * 64 + cb + hh * 8;
+                const int col = part * CW + cb + hh * 8;
                 const uint4 qraw = *reinterpret_cast<const uint4 *>(sm + L::O1 + km16(64 + r, col, 128));
                 const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
                 float x[8];
@@ -376,11 +383,11 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
         w_epilogue<L, NT>(sm, tmem + TC_W);  // -W over Kg in O1
-        epi_p2(tmem, rec, range_ok);
+        epi_p2<NT>(tmem, rec, range_ok);
         ok = mbar_wait_ns(&bar_p, 0, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
-        epi_p(tmem, rec, range_ok);
+        epi_p<NT>(tmem, rec, range_ok);
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
@@ -392,8 +399,8 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         ok = mbar_wait_ns(&bar_mma, 0, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
-        epi_n(tmem, rec);
-        epi_q<L>(sm, tmem, rec);
+        epi_n<NT>(tmem, rec);
+        epi_q<L, NT>(sm, tmem, rec);
     } while (false);
     if (timed_out) {
         if (tid == 0) {
