@@ -33,8 +33,8 @@ using namespace tc;
 
 // Record of one chunk-head.
 constexpr uint32_t R_N = 0;        // N  bf16 K-major, 2 panels x 128 rows (rows i, K = j)
-constexpr uint32_t R_P = 32768;    // P  fp16 K-major, 128 rows            (rows i, K = s)
-constexpr uint32_t R_Q = 49152;    // Q' bf16 K-major, 2 panels x 64 rows  (rows t, K = j)
+constexpr uint32_t R_Q = 32768;    // Q' bf16 K-major, 2 panels x 64 rows  (rows t, K = j)
+constexpr uint32_t R_P = 49152;    // P  fp16 K-major, 128 rows            (rows i, K = s)
 constexpr uint32_t R_P2 = 65536;   // P2 fp16 K-major, 64 rows             (rows t, K = s)
 constexpr uint32_t R_GM = 73728;   // gamma, 128 fp32
 constexpr uint32_t kRecBytes = 74240;
@@ -55,8 +55,13 @@ struct ChunkLayout {
     // in-place solve over the q box and Ki (both dead by then); Kd^T over the same bytes after it
     static constexpr uint32_t SOLVE_A = 16384, SOLVE_T = 16384, SOLVE_X = 16384 + kC * kLdS * 4;
     static constexpr uint32_t KDH = 16384, KDL = 32768;  // Kd^T high / low bf16 K-major, 128 rows x 64
+    // record images staged for bulk stores, each over bytes dead by then:
+    static constexpr uint32_t ST_P = 0;        // P over the k box (after the Kd build)
+    static constexpr uint32_t ST_P2 = 90112;   // P2 over T' high (after the P products)
+    static constexpr uint32_t ST_NQ = 0;       // N | Q' over the P image and Kd^T (after N, Q'')
     static constexpr uint32_t USED = 106496;
 };
+static_assert(ChunkLayout::ST_NQ + 49152 <= ChunkLayout::O1, "N | Q' staging overlaps O1");
 static_assert(ChunkLayout::SOLVE_X + 32 * kLdX * 4 <= ChunkLayout::O1, "solve scratch overlaps O1");
 
 // State kernel (512 threads): two record stages, a ring of four v slices, the
@@ -186,10 +191,11 @@ __device__ __forceinline__ void issue_n_q(uint32_t sb, uint32_t tmem)
         mma_bf16(tmem + TC_Q, kdesc(sb + L::AQ + s * 32), mndesc(sb + L::O1 + s * 2048, 16384), id_q, s > 0);
 }
 
-// Epilogues straight into the record (global memory).  Warp w reads TMEM lane
-// quarter w % 4 and the (w / 4)-th of NT / 128 equal column ranges.
+// Epilogues into shared-memory images of the record's parts, which one thread
+// then bulk-copies to the record.  Warp w reads TMEM lane quarter w % 4 and the
+// (w / 4)-th of NT / 128 equal column ranges.
 template <int NT>
-__device__ __forceinline__ void epi_p2(uint32_t tmem, unsigned char *rec, bool &ok)
+__device__ __forceinline__ void epi_p2(uint32_t tmem, unsigned char *dst, bool &ok)
 {
     constexpr int CW = 64 / (NT / 128);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
@@ -205,14 +211,14 @@ __device__ __forceinline__ void epi_p2(uint32_t tmem, unsigned char *rec, bool &
                 float x[8];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
-                *reinterpret_cast<uint4 *>(rec + R_P2 + km16(r, part * CW + cb + hh * 8, 64)) = pack_f16x8(x, ok);
+                *reinterpret_cast<uint4 *>(dst + km16(r, part * CW + cb + hh * 8, 64)) = pack_f16x8(x, ok);
             }
         }
     }
 }
 
 template <int NT>
-__device__ __forceinline__ void epi_p(uint32_t tmem, unsigned char *rec, bool &ok)
+__device__ __forceinline__ void epi_p(uint32_t tmem, unsigned char *dst, bool &ok)
 {
     constexpr int CW = 64 / (NT / 128);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
@@ -227,13 +233,13 @@ __device__ __forceinline__ void epi_p(uint32_t tmem, unsigned char *rec, bool &o
             float x[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
-            *reinterpret_cast<uint4 *>(rec + R_P + km16(i, part * CW + cb + hh * 8, 128)) = pack_f16x8(x, ok);
+            *reinterpret_cast<uint4 *>(dst + km16(i, part * CW + cb + hh * 8, 128)) = pack_f16x8(x, ok);
         }
     }
 }
 
 template <int NT>
-__device__ __forceinline__ void epi_n(uint32_t tmem, unsigned char *rec)
+__device__ __forceinline__ void epi_n(uint32_t tmem, unsigned char *dst)
 {
     constexpr int CW = 128 / (NT / 128);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
@@ -248,14 +254,14 @@ __device__ __forceinline__ void epi_n(uint32_t tmem, unsigned char *rec)
             float x[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
-            *reinterpret_cast<uint4 *>(rec + R_N + km16(i, part * CW + cb + hh * 8, 128)) = pack_bf16x8(x);
+            *reinterpret_cast<uint4 *>(dst + km16(i, part * CW + cb + hh * 8, 128)) = pack_bf16x8(x);
         }
     }
 }
 
 // Q' = Qg + Aqk (-W); Qg from rows 64..127 of O1.
 template <class L, int NT>
-__device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, unsigned char *rec)
+__device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, unsigned char *dst)
 {
     constexpr int CW = 128 / (NT / 128);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
@@ -278,7 +284,7 @@ __device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, un
                     x[2 * u] = qf.x + v[hh * 8 + 2 * u];
                     x[2 * u + 1] = qf.y + v[hh * 8 + 2 * u + 1];
                 }
-                *reinterpret_cast<uint4 *>(rec + R_Q + km16(r, col, 64)) = pack_bf16x8(x);
+                *reinterpret_cast<uint4 *>(dst + km16(r, col, 64)) = pack_bf16x8(x);
             }
         }
     }
@@ -341,7 +347,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_holder;
-    bool timed_out = false, tma_pending = true, decay_bad = false, range_ok = true;
+    bool timed_out = false, tma_pending = true, decay_bad = false, range_ok = true, stores_pending = false;
     do {
         bool ok = mbar_wait_ns(&bar_tma, 0, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
@@ -383,11 +389,11 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
         w_epilogue<L, NT>(sm, tmem + TC_W);  // -W over Kg in O1
-        epi_p2<NT>(tmem, rec, range_ok);
         ok = mbar_wait_ns(&bar_p, 0, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
-        epi_p<NT>(tmem, rec, range_ok);
+        epi_p<NT>(tmem, sm + L::ST_P, range_ok);    // the k box is dead
+        epi_p2<NT>(tmem, sm + L::ST_P2, range_ok);  // T' (high) is dead: every product reading it is done
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
@@ -395,12 +401,23 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             tc_fence_after_sync();
             issue_n_q<L>(sb, tmem);
             mma_commit(&bar_mma);
+            bulk_store(rec + R_P, sm + L::ST_P, 16384);
+            bulk_store(rec + R_P2, sm + L::ST_P2, 8192);
+            bulk_commit();
+            stores_pending = true;
         }
         ok = mbar_wait_ns(&bar_mma, 0, kWaitNs);
+        if (tid == 0) bulk_wait_read();  // the P image is overwritten next
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
-        epi_n<NT>(tmem, rec);
-        epi_q<L, NT>(sm, tmem, rec);
+        epi_n<NT>(tmem, sm + L::ST_NQ);           // over the P image and Kd^T
+        epi_q<L, NT>(sm, tmem, sm + L::ST_NQ + 32768);
+        fence_proxy_async_smem();
+        __syncthreads();
+        if (tid == 0) {
+            bulk_store(rec + R_N, sm + L::ST_NQ, 49152);  // N | Q'
+            bulk_commit();
+        }
     } while (false);
     if (timed_out) {
         if (tid == 0) {
@@ -410,6 +427,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         (void)mbar_wait_ns(&bar_drain, 0, kWaitNs);
         if (tma_pending) (void)mbar_wait_ns(&bar_tma, 0, kWaitNs);
     }
+    if (tid == 0 && stores_pending) bulk_wait_all();  // record bulk stores complete before exit
     if (decay_bad) atomicOr(status, DEV_ERR_DECAY);
     if (!range_ok) atomicOr(status, DEV_ERR_RANGE);
     tc_fence_before_sync();

@@ -147,6 +147,10 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 // Wait until every bulk group this thread committed has completed (writes done).
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 
+// Wait until every bulk group this thread committed has finished reading its
+// shared-memory source (the source may then be overwritten).
+__device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
 // Bring a 16-byte aligned global range (size a multiple of 16) into L2, no completion.
 __device__ __forceinline__ void bulk_prefetch_l2(const void *src, uint32_t bytes)
 {
