@@ -374,28 +374,39 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm)
 #pragma unroll
     for (int b = 4; b <= 32; b *= 2) {
         const int quads = b / 4, items = 32 * quads;
-        for (int e = tid; e < items; e += NT) {  // X = A_10 T_00
-            const int xr = e / quads, cq = (e % quads) * 4, p = xr / b, rr = xr % b;
+        // X = A_10 T_00: a warp shares one column quad cq over the 32 rows of X, so
+        // the loop can start at m = cq (T_00[m][cq..cq+3] = 0 for m < cq); A is read
+        // four m at a time (rows 272 bytes apart: conflict-free float4 loads)
+        for (int e = tid; e < items; e += NT) {
+            const int xr = e & 31, cq = (e >> 5) * 4, p = xr / b, rr = xr % b;
             const int R0 = 2 * b * p + b, C0 = 2 * b * p;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int m = 0; m < b; ++m) {
-                const float a = sT[(R0 + rr) * kLdS + C0 + m];
-                const float4 t = *reinterpret_cast<const float4 *>(sT + (C0 + m) * kLdS + C0 + cq);
-                acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
+            for (int m4 = cq; m4 < b; m4 += 4) {
+                const float4 a = *reinterpret_cast<const float4 *>(sT + (R0 + rr) * kLdS + C0 + m4);
+                const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 t = *reinterpret_cast<const float4 *>(sT + (C0 + m4 + u) * kLdS + C0 + cq);
+                    acc.x += av[u] * t.x; acc.y += av[u] * t.y; acc.z += av[u] * t.z; acc.w += av[u] * t.w;
+                }
             }
             *reinterpret_cast<float4 *>(sX + xr * kLdX + cq) = acc;
         }
         __syncthreads();
-        for (int e = tid; e < items; e += NT) {  // T_10 = -T_11 X, over A_10
+        // T_10 = -T_11 X over A_10: row rr needs m <= rr only (T_11 is lower triangular);
+        // a warp covers few consecutive rows, so its trip counts stay close
+        for (int e = tid; e < items; e += NT) {
             const int xr = e / quads, cq = (e % quads) * 4, p = xr / b, rr = xr % b;
             const int R0 = 2 * b * p + b, C0 = 2 * b * p;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 8
-            for (int m = 0; m < b; ++m) {
-                const float t = sT[(R0 + rr) * kLdS + R0 + m];
-                const float4 x = *reinterpret_cast<const float4 *>(sX + (p * b + m) * kLdX + cq);
-                acc.x += t * x.x; acc.y += t * x.y; acc.z += t * x.z; acc.w += t * x.w;
+            for (int m4 = 0; m4 <= rr; m4 += 4) {
+                const float4 t = *reinterpret_cast<const float4 *>(sT + (R0 + rr) * kLdS + R0 + m4);
+                const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const float4 x = *reinterpret_cast<const float4 *>(sX + (p * b + m4 + u) * kLdX + cq);
+                    acc.x += tv[u] * x.x; acc.y += tv[u] * x.y; acc.z += tv[u] * x.z; acc.w += tv[u] * x.w;
+                }
             }
             *reinterpret_cast<float4 *>(sT + (R0 + rr) * kLdS + C0 + cq) =
                 make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
