@@ -442,20 +442,31 @@ constexpr uint32_t IDESC_P2V = idesc_f16(64, 32, false, false);   // P2 V
 constexpr uint32_t IDESC_QS = idesc_bf16(64, 32, false, false);   // Q' S
 // TMEM columns: state increment (M = 128), outputs of two chunks (M = 64)
 constexpr uint32_t TM_5 = 0, TM_O = 32, kStateTmem = 128;
-// Warps 0-15 hold the state; warp 16 issues the MMAs; warp 17 copies and converts.
-constexpr int kStateWarps = 16, kIssueWarp = 16, kCopyWarp = 17, kStateThreads = 18 * 32;
+// Warps 0-15 hold the state; warp 16 issues the chain MMAs; warp 17 copies and
+// converts; warp 18 issues the output MMAs.
+constexpr int kStateWarps = 16, kChainWarp = 16, kCopyWarp = 17, kOutWarp = 18;
+constexpr int kStateThreads = 19 * 32;
 constexpr int kL2Ahead = 3;  // records brought into L2 this many chunks ahead
 
-// The serial pass over the chunks of one (sequence, head, 32-column value slice).
-// One block-wide barrier per chunk c, after which
-//   warp 16        (one lane) issues the chain P V + N S_c, commits it, then
-//                  issues the output P2 V + Q' S_c behind it and commits that,
-//   warp 17        copies record c + 1 (prefetching later ones into L2) and
-//                  converts the v slice of chunk c + 1,
-//   warps 0-15     write the outputs of chunk c - 1, then, once the chain is
-//                  done, S_{c+1} = gamma . S_c + (P V + N S_c).
-// The issuing lane has a warp of its own: MMA issue slows down badly when the
-// rest of the issuing warp is busy with other work.
+// The serial pass over the chunks of one (sequence, head, 32-column value slice),
+// as four roles that meet only at mbarriers (no block-wide barrier per chunk):
+//   bar_ready[c&1]  S_c and V_c (both written by the 16 state warps) are in shared memory
+//   bar_rec[c&1]    record c has arrived
+//   bar_s           the chain of the latest chunk is done
+//   bar_o[c&1]      the output group of chunk c is done
+// Chunk c:
+//   warp 16 (one lane)   waits ready(c), record c; issues P V + N S_c; commits bar_s
+//   warp 18 (one lane)   waits ready(c), record c; issues P2 V + Q' S_c; commits bar_o
+//   warps 0-15           write the outputs of chunk c - 1 (waiting bar_o), convert the
+//                        v slice of chunk c + 1 over V_{c-1} while the chain runs, wait
+//                        bar_s, S_{c+1} = gamma . S_c + (P V + N S_c), arrive on ready(c + 1)
+//   warp 17              once ready(c) and bar_o(c - 1) hold, copies record c + 1 over
+//                        record c - 1, prefetches a later record into L2 and refills the
+//                        v slot of chunk c (converted by then) with chunk c + kVRing
+// Every producer runs at most one chunk ahead of the consumer of the buffer it
+// refills, and each ready / output barrier alternates with the chunk parity, so no
+// barrier is ever waited on more than one phase behind.  Each issuing lane has a
+// warp of its own: MMA issue slows down badly when the rest of its warp is busy.
 __global__ void __launch_bounds__(kStateThreads, 1)
 prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__restrict__ cu,
                      int64_t total, int H, const int32_t *__restrict__ cc,
@@ -465,9 +476,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
 {
     using L = StateLayout;
     extern __shared__ unsigned char smem_raw[];
-    // one output barrier per output buffer, so that no barrier is ever waited on
-    // more than one phase behind
-    __shared__ __align__(8) uint64_t bar_rec[2], bar_v[kVRing], bar_s, bar_o[2], bar_drain;
+    __shared__ __align__(8) uint64_t bar_rec[2], bar_v[kVRing], bar_s, bar_o[2], bar_ready[2], bar_drain;
     __shared__ uint32_t tmem_holder;
 
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -503,7 +512,9 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
         mbar_init(&bar_s, 1);
         mbar_init(&bar_o[0], 1);
         mbar_init(&bar_o[1], 1);
-        mbar_init(&bar_drain, 1);
+        mbar_init(&bar_ready[0], kStateWarps);
+        mbar_init(&bar_ready[1], kStateWarps);
+        mbar_init(&bar_drain, 2);  // both issuing lanes commit to it on a timeout
         fence_mbar_init();
     }
     if (warp == 0) {
@@ -538,6 +549,13 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     bool range_ok = true;
     // operand descriptors of buffer 0; buffer 1 is a fixed byte distance further
     const uint64_t d_rec0 = kdesc(sb), d_v0 = kdesc(sb + L::VIMG), d_s0 = kdesc(sb + L::O7);
+    // ready(c) for c >= 1 (chunk 0's operands are known ready from the first barrier)
+    auto wait_ready = [&](int c) -> bool {
+        return c < 1 || mbar_wait_ns(&bar_ready[c & 1], (uint32_t)(((c - 1) >> 1) & 1), kWaitNs);
+    };
+    auto wait_record = [&](int c) -> bool {
+        return mbar_wait_ns(&bar_rec[c & 1], (uint32_t)((c >> 1) & 1), kWaitNs);
+    };
 
     // o rows of chunk cp (M = 64 accumulator TM_O + 32*(cp&1)), once its MMAs finished
     auto write_o = [&](int cp) -> bool {
@@ -551,131 +569,136 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
             *reinterpret_cast<uint4 *>(o + ((size_t)(cs + r64) * H + h) * kD + j0 + jp) = pack_bf16x8(v);
         return true;
     };
-    // copy warp: the v slice of chunk k -> V^T fp16 K-major in VIMG[k & 1]; lane = column
+    // state warps: the v slice of chunk k -> V^T fp16 K-major in VIMG[k & 1]; one
+    // 4-row group of one column per thread
     auto convert_v = [&](int k) -> bool {
         if (!mbar_wait_ns(&bar_v[k % kVRing], (uint32_t)((k / kVRing) & 1), kWaitNs)) return false;
         const int64_t ck = t0 + (int64_t)k * kC;
         const int lenk = (t1 - ck) < kC ? (int)(t1 - ck) : kC;
         const unsigned char *box = sm + L::VBOX + (k % kVRing) * 4096;
-#pragma unroll 4
-        for (int s8 = 0; s8 < kC; s8 += 8) {
-            float x[8];
+        const int j = tid % kDV, s4 = (tid / kDV) * 4;
+        float x[4];
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                x[u] = (s8 + u) < lenk ? bf16_at(box + ((s8 + u) * kDV + lane) * 2) : 0.f;
-            }
-            *reinterpret_cast<uint4 *>(sm + L::VIMG + (k & 1) * 4096 + km16(lane, s8, kDV)) = pack_f16x8(x, range_ok);
+        for (int u = 0; u < 4; ++u) {
+            x[u] = (s4 + u) < lenk ? bf16_at(box + ((s4 + u) * kDV + j) * 2) : 0.f;
+            range_ok &= fabsf(x[u]) <= 65504.f;
         }
+        __half2 a = __floats2half2_rn(x[0], x[1]), b = __floats2half2_rn(x[2], x[3]);
+        *reinterpret_cast<uint2 *>(sm + L::VIMG + (k & 1) * 4096 + km16(j, s4, kDV)) =
+            make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
         return true;
     };
-    // the copy warp's share of an iteration: record c + 1 (chunk c - 1's MMAs are
-    // done with its stage), L2 prefetch, the v slice of chunk c + 1, the next v copy
-    auto copy_step = [&](int c) -> bool {
-        bool ok = true;
-        if (c >= 1) ok = mbar_wait_ns(&bar_o[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1), kWaitNs);
-        if (copier && ok) {
-            if (c >= 1 && c + 1 < nchunks) load_record(c + 1);
-            if (c + kL2Ahead < nchunks) bulk_prefetch_l2(rec0 + (size_t)(c + kL2Ahead) * rec_stride, kRecBytes);
-        }
-        if (ok && c + 1 < nchunks) ok = convert_v(c + 1);
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (copier && ok && c + 1 + kVRing < nchunks) load_v(c + 1 + kVRing);
-        return ok;
-    };
 
-    bool timed_out = false;
-    {  // prologue: first copies, the v slice of chunk 0
-        bool ok = true;
-        if (warp == kCopyWarp) {
-            if (copier) {
-                for (int k = 0; k < 2 && k < nchunks; ++k) load_record(k);
-                for (int k = 2; k < kL2Ahead && k < nchunks; ++k)
-                    bulk_prefetch_l2(rec0 + (size_t)k * rec_stride, kRecBytes);
-                for (int k = 0; k < kVRing && k < nchunks; ++k) load_v(k);
-                prefetch_tmap(&tm_v);
-            }
-            __syncwarp();
-            if (nchunks > 0) ok = convert_v(0);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (copier && ok && kVRing < nchunks) load_v(kVRing);
-        }
-        if (__syncthreads_or(!ok)) timed_out = true;
+    bool ok = true;
+    if (copier) {
+        for (int k = 0; k < 2 && k < nchunks; ++k) load_record(k);
+        for (int k = 2; k < kL2Ahead && k < nchunks; ++k) bulk_prefetch_l2(rec0 + (size_t)k * rec_stride, kRecBytes);
+        for (int k = 0; k < kVRing && k < nchunks; ++k) load_v(k);
+        prefetch_tmap(&tm_v);
     }
-    int c = 0;
-    for (; c < nchunks && !timed_out; ++c) {
-        const int st = c & 1;
-        bool ok = true;
-        if (state_warp) {
-            if (c >= 1) ok = write_o(c - 1);
-            if (ok) ok = mbar_wait_ns(&bar_s, (uint32_t)(c & 1), kWaitNs);
-            // gamma is read from the record: observe its copy (long complete) here too
-            if (ok) ok = mbar_wait_ns(&bar_rec[st], (uint32_t)((c >> 1) & 1), kWaitNs);
-            if (ok) {  // S <- gamma . S + (P V + N S); S^T (bf16) for the next chunk, row pairs
-                tc_fence_after_sync();
-                float v[8];
-                tmem_ld8(tmem + TM_5 + lane_off + jp, v);
-                tmem_ld_wait();
-                const float gc = reinterpret_cast<const float *>(sm + st * L::STAGE + R_GM)[i_row];
-#pragma unroll
-                for (int j = 0; j < 8; ++j) S[j] = fmaf(gc, S[j], v[j]);
-                unsigned char *s_next = sm + L::O7 + (st ^ 1) * 8192;
-                const int ie = i_row & ~1;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float mine = odd ? S[4 + u] : S[u];
-                    const float give = odd ? S[u] : S[4 + u];
-                    const float other = __shfl_xor_sync(0xffffffffu, give, 1);
-                    const float lo = odd ? other : mine, hi = odd ? mine : other;
-                    *reinterpret_cast<uint32_t *>(s_next + km16(jp + 4 * odd + u, ie, kDV)) = pack_bf16x2(lo, hi);
-                }
-            }
-        } else if (warp == kIssueWarp) {
-            if (lane == 0) {
-                ok = mbar_wait_ns(&bar_rec[st], (uint32_t)((c >> 1) & 1), kWaitNs);
-                if (ok) {
-                    tc_fence_after_sync();
-                    // descriptors: base of each operand plus the constant byte offset >> 4
-                    const uint64_t dr = d_rec0 + st * (L::STAGE >> 4), dv = d_v0 + st * (4096 >> 4),
-                                   ds = d_s0 + st * (8192 >> 4);
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)  // the chain: P V + N S_c
-                        mma_bf16(tmem + TM_5, dr + ((R_P + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_PV, s > 0);
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32, offs = (s >> 2) * 4096 + (s & 3) * 32;
-                        mma_bf16(tmem + TM_5, dr + ((R_N + off) >> 4), ds + (offs >> 4), IDESC_NS, 1);
-                    }
-                    mma_commit(&bar_s);
-#pragma unroll
-                    for (int s = 0; s < 4; ++s)  // the output: P2 V + Q' S_c
-                        mma_bf16(tmem + TM_O + 32 * st, dr + ((R_P2 + s * 32) >> 4), dv + ((s * 32) >> 4),
-                                 IDESC_P2V, s > 0);
-#pragma unroll
-                    for (int s = 0; s < 8; ++s) {
-                        const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32, offs = (s >> 2) * 4096 + (s & 3) * 32;
-                        mma_bf16(tmem + TM_O + 32 * st, dr + ((R_Q + off) >> 4), ds + (offs >> 4), IDESC_QS, 1);
-                    }
-                    mma_commit(&bar_o[st]);
-                }
-            }
-            __syncwarp();
-        } else {
-            ok = copy_step(c);
-        }
+    if (state_warp && nchunks > 0) {
+        ok = convert_v(0);
         fence_proxy_async_smem();
-        tc_fence_before_sync();
-        if (__syncthreads_or(!ok)) { timed_out = true; break; }
     }
-    if (!timed_out && nchunks > 0) {
-        const bool ok = !state_warp || write_o(nchunks - 1);
-        if (__syncthreads_or(!ok)) timed_out = true;
+    bool timed_out = __syncthreads_or(!ok);  // S_0 and V_0 are in place for every role
+    int c = 0;
+    if (!timed_out) {
+        if (state_warp) {
+            for (; ok && c < nchunks; ++c) {
+                const int st = c & 1;
+                if (c >= 1) ok = write_o(c - 1);  // also frees O7 and VIMG of chunk c - 1
+                if (ok && c + 1 < nchunks) {     // V_{c+1} while the chain of chunk c runs
+                    ok = convert_v(c + 1);
+                    fence_proxy_async_smem();
+                }
+                if (ok) ok = mbar_wait_ns(&bar_s, (uint32_t)(c & 1), kWaitNs);
+                // gamma is read from the record: observe its copy (long complete) here too
+                if (ok) ok = wait_record(c);
+                if (ok) {  // S <- gamma . S + (P V + N S); S^T (bf16) for the next chunk, row pairs
+                    tc_fence_after_sync();
+                    float v[8];
+                    tmem_ld8(tmem + TM_5 + lane_off + jp, v);
+                    tmem_ld_wait();
+                    const float gc = reinterpret_cast<const float *>(sm + st * L::STAGE + R_GM)[i_row];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) S[j] = fmaf(gc, S[j], v[j]);
+                    unsigned char *s_next = sm + L::O7 + (st ^ 1) * 8192;
+                    const int ie = i_row & ~1;
+#pragma unroll
+                    for (int u = 0; u < 4; ++u) {
+                        const float mine = odd ? S[4 + u] : S[u];
+                        const float give = odd ? S[u] : S[4 + u];
+                        const float other = __shfl_xor_sync(0xffffffffu, give, 1);
+                        const float lo = odd ? other : mine, hi = odd ? mine : other;
+                        *reinterpret_cast<uint32_t *>(s_next + km16(jp + 4 * odd + u, ie, kDV)) = pack_bf16x2(lo, hi);
+                    }
+                    fence_proxy_async_smem();
+                }
+                tc_fence_before_sync();  // this warp's TMEM reads precede the arrival
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok && lane == 0 && c + 1 < nchunks) mbar_arrive(&bar_ready[(c + 1) & 1]);  // S, V of c + 1
+            }
+            if (ok && nchunks > 0) ok = write_o(nchunks - 1);
+        } else if (warp == kChainWarp || warp == kOutWarp) {
+            const bool chain = warp == kChainWarp;
+            for (; ok && c < nchunks; ++c) {
+                const int st = c & 1;
+                if (lane == 0) {
+                    ok = wait_ready(c) && wait_record(c);
+                    if (ok) {
+                        tc_fence_after_sync();
+                        // descriptors: base of each operand plus the constant byte offset >> 4
+                        const uint64_t dr = d_rec0 + st * (L::STAGE >> 4), dv = d_v0 + st * (4096 >> 4),
+                                       ds = d_s0 + st * (8192 >> 4);
+                        if (chain) {
+#pragma unroll
+                            for (int s = 0; s < 4; ++s)  // P V (fp16)
+                                mma_bf16(tmem + TM_5, dr + ((R_P + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_PV,
+                                         s > 0);
+#pragma unroll
+                            for (int s = 0; s < 8; ++s) {  // + N S_c (bf16)
+                                const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32,
+                                               offs = (s >> 2) * 4096 + (s & 3) * 32;
+                                mma_bf16(tmem + TM_5, dr + ((R_N + off) >> 4), ds + (offs >> 4), IDESC_NS, 1);
+                            }
+                            mma_commit(&bar_s);
+                        } else {
+#pragma unroll
+                            for (int s = 0; s < 4; ++s)  // P2 V (fp16)
+                                mma_bf16(tmem + TM_O + 32 * st, dr + ((R_P2 + s * 32) >> 4), dv + ((s * 32) >> 4),
+                                         IDESC_P2V, s > 0);
+#pragma unroll
+                            for (int s = 0; s < 8; ++s) {  // + Q' S_c (bf16)
+                                const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32,
+                                               offs = (s >> 2) * 4096 + (s & 3) * 32;
+                                mma_bf16(tmem + TM_O + 32 * st, dr + ((R_Q + off) >> 4), ds + (offs >> 4),
+                                         IDESC_QS, 1);
+                            }
+                            mma_commit(&bar_o[st]);
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+        } else if (warp == kCopyWarp) {  // record c + 1, one chunk ahead of the state warps
+            for (; ok && c < nchunks; ++c) {
+                if (c >= 1) {  // the record stage of chunk c - 1 is free; V_c is converted
+                    ok = wait_ready(c) &&
+                         mbar_wait_ns(&bar_o[(c - 1) & 1], (uint32_t)(((c - 1) >> 1) & 1), kWaitNs);
+                    if (copier && ok && c + 1 < nchunks) load_record(c + 1);
+                }
+                if (copier && ok && c + kL2Ahead < nchunks)
+                    bulk_prefetch_l2(rec0 + (size_t)(c + kL2Ahead) * rec_stride, kRecBytes);
+                if (copier && ok && c + kVRing < nchunks) load_v(c + kVRing);  // V_c's slot
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+            }
+        }
     }
+    timed_out = __syncthreads_or(timed_out || !ok);  // every role has finished or given up
     if (timed_out) {
         if (tid == 0) atomicOr(status, DEV_ERR_TIMEOUT);
-        // completes once every MMA the issuing lane started has
-        if (warp == kIssueWarp && lane == 0) mma_commit(&bar_drain);
+        // completes once every MMA of both issuing lanes has
+        if ((warp == kChainWarp || warp == kOutWarp) && lane == 0) mma_commit(&bar_drain);
         (void)mbar_wait_ns(&bar_drain, 0, kWaitNs);
         // our own copies still in flight (the copying thread knows how many)
         for (int k = rec_issued > 2 ? rec_issued - 2 : 0; k < rec_issued; ++k)

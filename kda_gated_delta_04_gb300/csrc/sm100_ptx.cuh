@@ -56,6 +56,22 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
+// As mbar_try_wait, but a thread whose phase is not yet complete is suspended
+// until it completes or about `hint_ns` nanoseconds pass, instead of returning
+// at once: waiting warps then leave the issue slots to the warps doing work.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t *bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
+
 // Wait for the phase with the given parity, giving up after about `limit_ns`
 // nanoseconds of wall-clock time.  Returns false on give-up.
 __device__ __forceinline__ bool mbar_wait_ns(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
@@ -63,10 +79,23 @@ __device__ __forceinline__ bool mbar_wait_ns(uint64_t *bar, uint32_t parity, uin
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
     for (;;) {
-        for (int i = 0; i < 64; ++i)
-            if (mbar_try_wait(bar, parity)) return true;
+        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;  // sleeps <= 0.1 ms per try
         if (globaltimer_ns() - t0 > limit_ns) return false;
     }
+}
+
+// Named barrier `id` (1..15) over `count` threads (a multiple of 32) of the CTA;
+// returns true on every thread when `pred` is true on any of them.
+__device__ __forceinline__ bool bar_sync_or(uint32_t id, uint32_t count, bool pred)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\t"
+        "barrier.cta.red.or.pred q, %2, %3, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)pred), "r"(id), "r"(count)
+        : "memory");
+    return r != 0;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
