@@ -212,9 +212,11 @@ class _Gpu:
             raise kda.KdaError(st, "kda_prefill")
 
     def time_prefill(self, steps, warmup, barrier):
-        """Per-step event times (ms) of kda_prefill, L2 flushed (untimed) before each step:
-        (whole call, [schedule, chunk kernel, state kernel]) from the four events that
-        kda_prefill_events records on the launching stream around its kernels."""
+        """Per-step event times (ms), L2 flushed (untimed) before each step.  `whole`: one
+        kda_prefill bracketed by two events (the headline; its kernels overlap their launch
+        boundaries).  `stages`: the same number of kda_prefill_events calls, whose four events
+        on the launching stream split each call into schedule, chunk and state kernel (the
+        events between kernels keep them from overlapping, so these sum slightly higher)."""
         torch = self.torch
         for _ in range(warmup):
             self.flush.zero_()
@@ -222,6 +224,14 @@ class _Gpu:
         torch.cuda.synchronize()
         barrier()
         torch.cuda.synchronize()
+        outer = [(self.event(), self.event()) for _ in range(steps)]
+        for a, b in outer:
+            self.flush.zero_()
+            a.record(self.stream)
+            self.prefill_call()
+            b.record(self.stream)
+        torch.cuda.synchronize()
+        barrier()
         ev = [[self.event() for _ in range(4)] for _ in range(steps)]
         for e in ev:
             for x in e:  # create the handles before they are passed down
@@ -231,11 +241,10 @@ class _Gpu:
             self.flush.zero_()
             self.prefill_call([x.cuda_event for x in e])
         torch.cuda.synchronize()
-        barrier()
         st = self.kda.kda_read_device_status(self.ws.data_ptr(), self.sh)
         if st != self.kda.KDA_OK:
             raise self.kda.KdaError(st, "kda_prefill (device status)")
-        whole = [e[0].elapsed_time(e[3]) for e in ev]
+        whole = [a.elapsed_time(b) for a, b in outer]
         stages = [[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev]
         return whole, stages
 
@@ -379,10 +388,11 @@ def run_gpu(args):
                                   "algorithmic_bytes_per_launch": alg_bytes,
                                   "tensor_frac_of_bf16_peak": prefill_flops(T, H, d) /
                                   (mean_step_ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
-                         "note": "durations from the four CUDA events kda_prefill_events records "
-                                 "on the launching stream around its kernels; the dominant "
-                                 "(longest) kernel is measured against its share of the path's "
-                                 "algorithmic bytes, the path against all of them"},
+                         "note": "kernel durations from the four CUDA events kda_prefill_events "
+                                 "records on the launching stream around its kernels (a separate "
+                                 "timed pass); the dominant (longest) kernel is measured against "
+                                 "its share of the path's algorithmic bytes, the path (one "
+                                 "kda_prefill between two events) against all of them"},
             "e2e": {"value": aggregate_rate(T, world, args.steps, e2e_total), "unit": "tokens/s",
                     "h2d_bytes_per_step": g.h2d, "d2h_bytes_per_step": g.d2h},
             "gpu_launches": 3 * args.steps,  # schedule, chunk and state kernel per step

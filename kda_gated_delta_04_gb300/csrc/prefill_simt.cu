@@ -36,6 +36,8 @@ constexpr int kThreads = 256;
 __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs, int64_t total,
                                     uint32_t *status, int32_t *order, int32_t *cc)
 {
+    // the chunk kernel may be scheduled now; it waits for this kernel's results itself
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ int bad;
     if (threadIdx.x == 0) bad = 0;
     __syncthreads();

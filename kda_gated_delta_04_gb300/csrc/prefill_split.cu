@@ -304,6 +304,10 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     __shared__ uint32_t tmem_holder;
     __shared__ __align__(16) float s_beta[kC];
 
+    // launched with programmatic stream serialization behind the schedule kernel:
+    // nothing that kernel writes (cc, the status word) is touched before pdl_wait
+    pdl_launch_dependents();  // the state kernel may be scheduled as SMs free up
+    pdl_wait();
     // one CTA per (chunk, head), heads fastest, chunks last to first
     const int h = (int)(blockIdx.x % (unsigned)H);
     const int g = chunk_bound - 1 - (int)(blockIdx.x / (unsigned)H);
@@ -484,6 +488,9 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool state_warp = warp < kStateWarps;
     const int quarter = warp & 3, part = (warp >> 2) & 3;
+    // launched with programmatic stream serialization behind the chunk kernel: the
+    // schedule (order, cc) and the records are read only after pdl_wait
+    pdl_wait();
     const int j0 = blockIdx.x * kDV, h = blockIdx.y, n = order[blockIdx.z];
     int64_t t0, t1;
     seq_range(cu, n, total, t0, t1);
@@ -738,18 +745,30 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
         return cudaErrorInvalidValue;
     const int64_t chunk_bound = p.total_tokens / kC + p.num_seqs;
     if (chunk_bound * p.num_heads > INT32_MAX) return cudaErrorInvalidValue;
-    prefill_chunk_kernel<<<(unsigned)(chunk_bound * p.num_heads), kChunkThreads, kChunkSmem, p.stream>>>(
-        tq, tk, p.log_alpha, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.num_seqs,
-        (int)chunk_bound, cc, static_cast<unsigned char *>(records), p.status);
-    err = cudaGetLastError();
+    // both kernels may start while the kernel before them drains (programmatic
+    // dependent launch); each waits for its inputs with griddepcontrol.wait
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(chunk_bound * p.num_heads));
+    cfg.blockDim = dim3(kChunkThreads);
+    cfg.dynamicSmemBytes = kChunkSmem;
+    cfg.stream = p.stream;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    err = cudaLaunchKernelEx(&cfg, prefill_chunk_kernel, tq, tk, p.log_alpha, p.beta, p.cu_seqlens,
+                             p.total_tokens, p.num_heads, p.num_seqs, (int)chunk_bound, cc,
+                             static_cast<unsigned char *>(records), p.status);
     if (err != cudaSuccess) return err;
     if (mid && (err = cudaEventRecord(mid, p.stream)) != cudaSuccess) return err;
-    dim3 grid_b(kD / kDV, p.num_heads, p.num_seqs);
-    prefill_state_kernel<<<grid_b, kStateThreads, kStateSmem, p.stream>>>(
-        tv, p.cu_seqlens, p.total_tokens, p.num_heads, cc,
-        static_cast<const unsigned char *>(records), p.init_state,
-        static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.status, p.order);
-    return cudaGetLastError();
+    cfg.gridDim = dim3(kD / kDV, p.num_heads, p.num_seqs);
+    cfg.blockDim = dim3(kStateThreads);
+    cfg.dynamicSmemBytes = kStateSmem;
+    return cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, p.cu_seqlens, p.total_tokens, p.num_heads,
+                              static_cast<const int32_t *>(cc), static_cast<const unsigned char *>(records),
+                              p.init_state, static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.status,
+                              static_cast<const int32_t *>(p.order));
 }
 
 }  // namespace kda

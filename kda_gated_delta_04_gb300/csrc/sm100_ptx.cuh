@@ -98,6 +98,19 @@ __device__ __forceinline__ bool bar_sync_or(uint32_t id, uint32_t count, bool pr
     return r != 0;
 }
 
+// As mbar_wait_ns, but polling without suspending: for the one thread on a
+// latency-critical path, alone in its warp.
+__device__ __forceinline__ bool mbar_wait_spin_ns(uint64_t *bar, uint32_t parity, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        for (int i = 0; i < 64; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
+    }
+}
+
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
@@ -192,6 +205,13 @@ __device__ __forceinline__ void prefetch_tmap(const void *tmap)
 {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tmap)) : "memory");
 }
+
+// ------------------------------------------------------------------ dependent launch
+// Let the next kernel on the stream (launched with programmatic stream
+// serialization) be scheduled before this one finishes.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+// Wait until the kernels this one depends on have completed and their memory is visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // ------------------------------------------------------------------ tensor memory
 // Executed by one full warp.  Writes the allocated TMEM base address to *dst.
