@@ -341,7 +341,8 @@ __device__ __forceinline__ void solve_ut_core(unsigned char *sm)
 // solve_ut_doubling: the same T, in place (SOLVE_T == SOLVE_A), by recursive
 // doubling all the way from 4 x 4 blocks: the sixteen 4 x 4 diagonal blocks by
 // substitution, then for block size b = 4, 8, 16, 32 and every pair of b x b
-// diagonal blocks, X = A_10 T_00 and T_10 = -T_11 X (X in SOLVE_X, row p*b + r).
+// diagonal blocks, X = A_10 T_00 and T_10 = -T_11 X (X in SOLVE_X).  Up to b = 8
+// each 16 x 16 diagonal block is done by one warp with warp barriers only.
 // Each output quad is one thread's float4; the strictly upper parts of A, which
 // the k-k epilogue zeroed, stand in for the zero upper parts of T, so no product
 // needs a mask.  Contains barriers.
@@ -349,13 +350,18 @@ template <class L, int NT>
 __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm)
 {
     static_assert(L::SOLVE_A == L::SOLVE_T, "the doubling solve works in place");
-    const int tid = threadIdx.x;
+    static_assert(NT >= 128, "four warps take the diagonal 16 x 16 blocks");
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float *sT = reinterpret_cast<float *>(sm + L::SOLVE_T);  // holds A until overwritten
     float *sX = reinterpret_cast<float *>(sm + L::SOLVE_X);
-    {  // 4 x 4 diagonal blocks: thread (block j, column cc)
-        const int j4 = (tid >> 2) * 4, cc = tid & 3;
+    // 1. Warp w < 4 inverts the diagonal 16 x 16 block at 16w on its own (warp
+    //    barriers only): its four 4 x 4 blocks by substitution, then the 4 and 8
+    //    doubling levels inside the block.  X rows 8w .. 8w + 7 are the warp's.
+    if (warp < 4) {
+        const int w16 = warp * 16;
         float x[4];
-        if (tid < 64) {
+        const int j4 = w16 + (lane >> 2) * 4, cc = lane & 3;
+        if (lane < 16) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) {
                 float acc = 0.f;
@@ -364,15 +370,47 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm)
                 x[r] = r < cc ? 0.f : (r == cc ? 1.f : -acc);
             }
         }
-        __syncthreads();  // every column has read its block of A
-        if (tid < 64) {
+        __syncwarp();  // every column has read its block of A
+        if (lane < 16) {
 #pragma unroll
             for (int r = 0; r < 4; ++r) sT[(j4 + r) * kLdS + j4 + cc] = x[r];
         }
-        __syncthreads();
-    }
+        __syncwarp();
 #pragma unroll
-    for (int b = 4; b <= 32; b *= 2) {
+        for (int b = 4; b <= 8; b *= 2) {  // pairs of b x b blocks inside the 16 x 16 block
+            const int quads = b / 4;
+            const int nitems = (16 / (2 * b)) * b * quads;  // pairs x rows x quads: 8 (b = 4), 16 (b = 8)
+            const int xr = lane / quads, cq = (lane % quads) * 4, p = xr / b, rr = xr % b;
+            const int R0 = w16 + 2 * b * p + b, C0 = w16 + 2 * b * p;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (lane < nitems) {  // X = A_10 T_00
+#pragma unroll
+                for (int m = 0; m < b; ++m) {
+                    const float a = sT[(R0 + rr) * kLdS + C0 + m];
+                    const float4 t = *reinterpret_cast<const float4 *>(sT + (C0 + m) * kLdS + C0 + cq);
+                    acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
+                }
+                *reinterpret_cast<float4 *>(sX + (warp * 8 + xr) * kLdX + cq) = acc;
+            }
+            __syncwarp();
+            if (lane < nitems) {  // T_10 = -T_11 X over A_10
+                acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+                for (int m = 0; m < b; ++m) {
+                    const float t = sT[(R0 + rr) * kLdS + R0 + m];
+                    const float4 xv = *reinterpret_cast<const float4 *>(sX + (warp * 8 + p * b + m) * kLdX + cq);
+                    acc.x += t * xv.x; acc.y += t * xv.y; acc.z += t * xv.z; acc.w += t * xv.w;
+                }
+                *reinterpret_cast<float4 *>(sT + (R0 + rr) * kLdS + C0 + cq) =
+                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // 2. The 16 and 32 levels across the CTA.
+#pragma unroll
+    for (int b = 16; b <= 32; b *= 2) {
         const int quads = b / 4, items = 32 * quads;
         // X = A_10 T_00: a warp shares one column quad cq over the 32 rows of X, so
         // the loop can start at m = cq (T_00[m][cq..cq+3] = 0 for m < cq); A is read
