@@ -207,6 +207,19 @@ kda_status_t kda_prefill_no_alloc(const void *q, const void *k, const void *v,
                                   void *o, float *final_state, uint32_t *device_errors,
                                   void *stream);
 
+/*
+ * Self-test of the device-side failure path (the pages have no counterpart; it
+ * checks this library's own error handling).  Enqueues on `stream` one small
+ * kernel whose threads wait, one sleeping and one polling, on a barrier that
+ * nothing ever completes.  Each wait gives up after limit_ns nanoseconds of wall
+ * time (0 < limit_ns <= 1e9, else KDA_ERR_INVALID_ARG) exactly as every wait in
+ * the prefill kernels does, and the kernel records the give-up in the status
+ * word at the start of `workspace` (256-byte aligned device memory, at least 4
+ * bytes; the word is cleared first).  kda_read_device_status(workspace, stream)
+ * then returns KDA_ERR_TIMEOUT.  Nothing faults or hangs; the context stays usable.
+ */
+kda_status_t kda_selftest_bounded_wait(void *workspace, uint64_t limit_ns, void *stream);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *kda_status_string(kda_status_t status);
 

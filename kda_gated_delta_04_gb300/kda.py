@@ -41,6 +41,7 @@ EXPORTS = {
     "kda_status_string": (_c.c_char_p, [_c.c_int]),
     "kda_prefill_no_alloc": (_c.c_int, _PREFILL_ARGS[:15] + [_VP, _VP]),
     "kda_prefill_events": (_c.c_int, _PREFILL_ARGS + [_c.POINTER(_VP), _c.c_int32]),
+    "kda_selftest_bounded_wait": (_c.c_int, [_VP, _c.c_uint64, _VP]),
 }
 
 
@@ -103,6 +104,11 @@ def kda_prefill_events(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tok
     return lib().kda_prefill_events(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens,
                                     num_heads, d_k, d_v, dtype, init_state, o, final_state,
                                     workspace, workspace_bytes, stream, arr, len(events))
+
+
+def kda_selftest_bounded_wait(workspace, limit_ns, stream):
+    """Runs the device-side bounded-wait self-test (see include/kda.h)."""
+    return lib().kda_selftest_bounded_wait(workspace, limit_ns, stream)
 
 
 def kda_read_device_status(workspace, stream):

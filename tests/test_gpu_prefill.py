@@ -218,3 +218,22 @@ def test_stage_events_bracket_the_kernels_and_change_nothing():
                                  None, o.data_ptr(), fs.data_ptr(), ws.data_ptr(), ws.numel(),
                                  s.cuda_stream, [e.cuda_event for e in ev[:3]])
     assert bad == kda.KDA_ERR_INVALID_ARG
+
+
+def test_bounded_wait_gives_up_and_reports_without_a_fault():
+    """The failure path every prefill kernel uses: a wait on a barrier nothing
+    completes gives up after its limit (50 ms here), the kernel records
+    KDA_ERR_TIMEOUT and returns, and the context keeps working."""
+    import time
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    s = torch.cuda.current_stream().cuda_stream
+    t0 = time.time()
+    assert kda.kda_selftest_bounded_wait(ws.data_ptr(), 50_000_000, s) == kda.KDA_OK
+    assert kda.kda_read_device_status(ws.data_ptr(), s) == kda.KDA_ERR_TIMEOUT
+    assert time.time() - t0 < 10.0
+    assert kda.kda_selftest_bounded_wait(ws.data_ptr(), 0, s) == kda.KDA_ERR_INVALID_ARG
+    # the context is still usable: a prefill afterwards meets the bar
+    w, inp = _custom("after_timeout", 120, [130], H=2, init_state=True)
+    o, fs = gpu_prefill(inp)
+    o_ref, fs_ref = oracle_prefill(inp)
+    assert_parity(o, fs, o_ref, fs_ref, "bf16", "after the timeout self-test")
