@@ -431,7 +431,9 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         (void)mbar_wait_ns(&bar_drain, 0, kWaitNs);
         if (tma_pending) (void)mbar_wait_ns(&bar_tma, 0, kWaitNs);
     }
-    if (tid == 0 && stores_pending) bulk_wait_all();  // record bulk stores complete before exit
+    // the record stores must have read their shared-memory sources before the CTA exits
+    // and its shared memory is reused; their global writes complete before the kernel does
+    if (tid == 0 && stores_pending) bulk_wait_read();
     if (decay_bad) atomicOr(status, DEV_ERR_DECAY);
     if (!range_ok) atomicOr(status, DEV_ERR_RANGE);
     tc_fence_before_sync();

@@ -237,3 +237,19 @@ def test_bounded_wait_gives_up_and_reports_without_a_fault():
     o, fs = gpu_prefill(inp)
     o_ref, fs_ref = oracle_prefill(inp)
     assert_parity(o, fs, o_ref, fs_ref, "bf16", "after the timeout self-test")
+
+
+def test_many_tiny_ragged_sequences():
+    """The two-kernel path's schedule with hundreds of sequences, most shorter than one
+    chunk, some empty, some spanning a few chunks: every unit is checked against the
+    oracle (outputs element by element, states together)."""
+    rng = np.random.default_rng(121)
+    lens = rng.integers(0, 70, size=300)
+    lens[::37] = 0
+    lens[5], lens[200] = 190, 129
+    w = PrefillWorkload("tiny_ragged", 121, 2, 128, "bf16", tuple(int(x) for x in lens), len(lens),
+                        init_state=True)
+    inp = synth.prefill_inputs(w)
+    o, fs = gpu_prefill(inp)
+    o_ref, fs_ref = oracle_prefill(inp)
+    assert_parity(o, fs, o_ref, fs_ref, "bf16", "300 tiny ragged sequences")
