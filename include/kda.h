@@ -93,7 +93,9 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
  *              = total_tokens; NULL means one sequence of total_tokens tokens
  *              (num_seqs must then be 1)
  *  init_state  [num_seqs, num_heads, d_k, d_v] fp32, or NULL for zero states
- *  o           [total_tokens, num_heads, d_v]  dtype (written for every token)
+ *  o           [total_tokens, num_heads, d_v]  dtype (written for every token), or NULL
+ *              for a state-only prefill (final states only; the two-kernel path then
+ *              also skips the output products)
  *  final_state [num_seqs, num_heads, d_k, d_v] fp32; may equal init_state
  *              (in-place update); a zero-length sequence gets its initial state
  *  workspace   device buffer owned by the caller, 256-byte aligned, reused by every
@@ -103,7 +105,7 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
  *              KDA_PREFILL_MIN_WORKSPACE(num_seqs) bytes it runs as one fused
  *              kernel (same results up to rounding order, slower).  Smaller
  *              workspaces are rejected.
- *  q, k, v, log_alpha, beta and o may be NULL when total_tokens == 0.
+ *  q, k, v, log_alpha and beta may be NULL when total_tokens == 0.
  *
  * Device-side errors (timeout of a bounded wait, a cu_seqlens array that is not
  * a valid prefix sum, a decay outside the supported range, and on the two-kernel

@@ -88,8 +88,8 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     if (!cu_seqlens && num_seqs != 1) return KDA_ERR_INVALID_ARG;
     if (num_seqs > 65535) return KDA_ERR_UNSUPPORTED;  // grid z extent
     if (num_heads > 65535) return KDA_ERR_UNSUPPORTED;  // grid y extent
-    // token tensors may be NULL only when there are no tokens
-    if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta || !o))
+    // token tensors may be NULL only when there are no tokens; o may be NULL (final states only)
+    if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta))
         return KDA_ERR_INVALID_ARG;
     if (!final_state || !workspace) return KDA_ERR_INVALID_ARG;
     if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) ||

@@ -253,8 +253,8 @@ prefill_simt_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO
         }
         __syncthreads();
 
-        // ---- a6: output o = Qg S + Aqk U
-        {
+        // ---- a6: output o = Qg S + Aqk U (skipped when no outputs are wanted)
+        if (o) {
             const int j = tid % DV;
             for (int r = tid / DV; r < len; r += kThreads / DV) {
                 float acc = 0.f;

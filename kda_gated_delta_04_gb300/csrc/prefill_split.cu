@@ -152,11 +152,12 @@ __device__ __forceinline__ void build_kd(unsigned char *sm, int len, const float
     }
 }
 
-// Round 2a: W = T' Kg (M = 64, N = 128) and P2 = Aqk T' (M = 64, N = 64).
+// Round 2a: W = T' Kg (M = 64, N = 128) and, when outputs are wanted, P2 = Aqk T' (M = 64, N = 64).
 template <class L>
-__device__ __forceinline__ void issue_w_p2(uint32_t sb, uint32_t tmem)
+__device__ __forceinline__ void issue_w_p2(uint32_t sb, uint32_t tmem, bool with_o)
 {
     issue_gw<L>(sb, tmem + TC_W);
+    if (!with_o) return;
     constexpr uint32_t idesc = idesc_bf16(64, 64, false, true);
 #pragma unroll
     for (int s = 0; s < 4; ++s)
@@ -178,14 +179,15 @@ __device__ __forceinline__ void issue_p(uint32_t sb, uint32_t tmem)
                      (t | s) != 0);
 }
 
-// Round 3: N = Kd^T (-W) (M = 128, N = 128) and Q'' = Aqk (-W) (M = 64, N = 128).
+// Round 3: N = Kd^T (-W) (M = 128, N = 128) and, when outputs are wanted, Q'' = Aqk (-W) (M = 64, N = 128).
 template <class L>
-__device__ __forceinline__ void issue_n_q(uint32_t sb, uint32_t tmem)
+__device__ __forceinline__ void issue_n_q(uint32_t sb, uint32_t tmem, bool with_o)
 {
     constexpr uint32_t id_n = idesc_bf16(128, 128, false, true), id_q = idesc_bf16(64, 128, false, true);
 #pragma unroll
     for (int s = 0; s < 4; ++s)
         mma_bf16(tmem + TC_N, kdesc(sb + L::KDH + s * 32), mndesc(sb + L::O1 + s * 2048, 16384), id_n, s > 0);
+    if (!with_o) return;
 #pragma unroll
     for (int s = 0; s < 4; ++s)
         mma_bf16(tmem + TC_Q, kdesc(sb + L::AQ + s * 32), mndesc(sb + L::O1 + s * 2048, 16384), id_q, s > 0);
@@ -295,7 +297,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                      const float *__restrict__ log_alpha, const float *__restrict__ beta,
                      const int32_t *__restrict__ cu, int64_t total, int H, int num_seqs,
                      int chunk_bound, const int32_t *__restrict__ cc,
-                     unsigned char *__restrict__ records, uint32_t *status)
+                     unsigned char *__restrict__ records, uint32_t *status, bool with_o)
 {
     using L = ChunkLayout;
     constexpr int NT = kChunkThreads;
@@ -378,7 +380,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         __syncthreads();
         if (tid == 0) {
             tc_fence_after_sync();
-            issue_w_p2<L>(sb, tmem);
+            issue_w_p2<L>(sb, tmem, with_o);
             mma_commit(&bar_mma);
         }
         build_kd<L, NT>(sm, len, gl, ot[0], ot[1]);  // over the solve scratch, overlapping W and P2
@@ -397,16 +399,16 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
         epi_p<NT>(tmem, sm + L::ST_P, range_ok);    // the k box is dead
-        epi_p2<NT>(tmem, sm + L::ST_P2, range_ok);  // T' (high) is dead: every product reading it is done
+        if (with_o) epi_p2<NT>(tmem, sm + L::ST_P2, range_ok);  // T' (high) is dead: every product reading it is done
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
         if (tid == 0) {
             tc_fence_after_sync();
-            issue_n_q<L>(sb, tmem);
+            issue_n_q<L>(sb, tmem, with_o);
             mma_commit(&bar_mma);
             bulk_store(rec + R_P, sm + L::ST_P, 16384);
-            bulk_store(rec + R_P2, sm + L::ST_P2, 8192);
+            if (with_o) bulk_store(rec + R_P2, sm + L::ST_P2, 8192);
             bulk_commit();
             stores_pending = true;
         }
@@ -415,11 +417,11 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
         epi_n<NT>(tmem, sm + L::ST_NQ);           // over the P image and Kd^T
-        epi_q<L, NT>(sm, tmem, sm + L::ST_NQ + 32768);
+        if (with_o) epi_q<L, NT>(sm, tmem, sm + L::ST_NQ + 32768);
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
-            bulk_store(rec + R_N, sm + L::ST_NQ, 49152);  // N | Q'
+            bulk_store(rec + R_N, sm + L::ST_NQ, with_o ? 49152u : 32768u);  // N | Q'
             bulk_commit();
         }
     } while (false);
@@ -567,8 +569,10 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     };
 
     // o rows of chunk cp (M = 64 accumulator TM_O + 32*(cp&1)), once its MMAs finished
+    // (with no outputs wanted the barrier still marks the chunk's operands as released)
     auto write_o = [&](int cp) -> bool {
         if (!mbar_wait_ns(&bar_o[cp & 1], (uint32_t)((cp >> 1) & 1), kWaitNs)) return false;
+        if (!o) return true;
         tc_fence_after_sync();
         float v[8];
         tmem_ld8(tmem + TM_O + 32 * (cp & 1) + lane_off + jp, v);
@@ -672,18 +676,20 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
                             }
                             mma_commit(&bar_s);
                         } else {
+                            if (o) {  // no output products when no outputs are wanted
 #pragma unroll
-                            for (int s = 0; s < 4; ++s)  // P2 V (fp16)
-                                mma_bf16(tmem + TM_O + 32 * st, dr + ((R_P2 + s * 32) >> 4), dv + ((s * 32) >> 4),
-                                         IDESC_P2V, s > 0);
+                                for (int s = 0; s < 4; ++s)  // P2 V (fp16)
+                                    mma_bf16(tmem + TM_O + 32 * st, dr + ((R_P2 + s * 32) >> 4),
+                                             dv + ((s * 32) >> 4), IDESC_P2V, s > 0);
 #pragma unroll
-                            for (int s = 0; s < 8; ++s) {  // + Q' S_c (bf16)
-                                const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32,
-                                               offs = (s >> 2) * 4096 + (s & 3) * 32;
-                                mma_bf16(tmem + TM_O + 32 * st, dr + ((R_Q + off) >> 4), ds + (offs >> 4),
-                                         IDESC_QS, 1);
+                                for (int s = 0; s < 8; ++s) {  // + Q' S_c (bf16)
+                                    const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32,
+                                                   offs = (s >> 2) * 4096 + (s & 3) * 32;
+                                    mma_bf16(tmem + TM_O + 32 * st, dr + ((R_Q + off) >> 4), ds + (offs >> 4),
+                                             IDESC_QS, 1);
+                                }
                             }
-                            mma_commit(&bar_o[st]);
+                            mma_commit(&bar_o[st]);  // also marks chunk c's operands as released
                         }
                     }
                 }
@@ -761,7 +767,7 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     cfg.numAttrs = 1;
     err = cudaLaunchKernelEx(&cfg, prefill_chunk_kernel, tq, tk, p.log_alpha, p.beta, p.cu_seqlens,
                              p.total_tokens, p.num_heads, p.num_seqs, (int)chunk_bound, cc,
-                             static_cast<unsigned char *>(records), p.status);
+                             static_cast<unsigned char *>(records), p.status, p.o != nullptr);
     if (err != cudaSuccess) return err;
     if (mid && (err = cudaEventRecord(mid, p.stream)) != cudaSuccess) return err;
     cfg.gridDim = dim3(kD / kDV, p.num_heads, p.num_seqs);

@@ -293,7 +293,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             float v[8];
             tmem_ld8(tmem + TM_D3 + lane_off + jp, v);
             tmem_ld_wait();
-            if (r < len)
+            if (r < len && o)
                 *reinterpret_cast<uint4 *>(o + ((size_t)(c0 + r) * H + h) * kD + j0 + jp) = pack_bf16x8(v);
         }
         {  // state rows: S <- gamma_c (S + Ki^T u); S^T (bf16) for the next chunk, row pairs

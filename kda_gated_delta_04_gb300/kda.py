@@ -170,16 +170,19 @@ def min_workspace_bytes(num_seqs):
 
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=None,
-            final_state=None, workspace=None, stream=None, check_status=False):
+            final_state=None, workspace=None, stream=None, check_status=False, outputs=True):
     """KDA prefill over packed sequences.  q, k: [T, H, d]; v: [T, H, d]; log_alpha: [T, H, d]
     fp32; beta: [T, H] fp32; cu_seqlens: int32 [N+1] CUDA tensor or None (one sequence);
-    init_state: [N, H, d, d] fp32 or None.  Returns (o, final_state)."""
+    init_state: [N, H, d, d] fp32 or None.  Returns (o, final_state); with outputs=False
+    only the final states are computed and o is None."""
     torch = _torch()
     T, H, d = q.shape
     dt = _dtype_code(q)
     N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
-    if o is None:
+    if o is None and outputs:
         o = torch.empty((T, H, v.shape[2]), dtype=q.dtype, device=q.device)
+    if not outputs:
+        o = None
     if final_state is None:
         final_state = torch.empty((N, H, d, v.shape[2]), dtype=torch.float32, device=q.device)
     if workspace is None:
@@ -187,7 +190,8 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
     st = kda_prefill(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
                      _ptr(log_alpha, "log_alpha", torch.float32), _ptr(beta, "beta", torch.float32),
                      _ptr(cu_seqlens, "cu_seqlens", torch.int32), N, T, H, d, v.shape[2], dt,
-                     _ptr(init_state, "init_state", torch.float32), _ptr(o, "o", q.dtype),
+                     _ptr(init_state, "init_state", torch.float32),
+                     None if o is None else _ptr(o, "o", q.dtype),
                      _ptr(final_state, "final_state", torch.float32), _ptr(workspace, "workspace"),
                      workspace.numel() * workspace.element_size(),
                      _stream_handle(stream, q.device))

@@ -65,7 +65,7 @@ def _prefill_args(**over):
 
 
 @pytest.mark.parametrize("over,expected", [
-    (dict(q=None), 1), (dict(o=None), 1), (dict(final_state=None), 1), (dict(workspace=None), 1),
+    (dict(q=None), 1), (dict(o=FAKE + 8), 1), (dict(final_state=None), 1), (dict(workspace=None), 1),
     (dict(q=FAKE + 4), 1), (dict(workspace=FAKE + 16), 1), (dict(workspace_bytes=8), 1),
     (dict(num_seqs=2), 1),                     # cu_seqlens required for several sequences
     (dict(num_heads=0), 1), (dict(total_tokens=-1), 1), (dict(dtype=7), 1),

@@ -253,3 +253,24 @@ def test_many_tiny_ragged_sequences():
     o, fs = gpu_prefill(inp)
     o_ref, fs_ref = oracle_prefill(inp)
     assert_parity(o, fs, o_ref, fs_ref, "bf16", "300 tiny ragged sequences")
+
+
+@pytest.mark.parametrize("case", ["two_kernel", "fused", "fp32"])
+def test_state_only_prefill_gives_the_same_final_states(case):
+    """o = NULL: only the final states are computed (the two-kernel path also skips the
+    output products); they are bit for bit those of the full call."""
+    dtype = "f32" if case == "fp32" else "bf16"
+    w = PrefillWorkload("state_only_" + case, 122, 2, 128, dtype, (200, 0, 64, 97), 4, init_state=True)
+    inp = synth.prefill_inputs(w)
+    d = to_device(inp)
+    N = 4
+    ws = None
+    if case == "fused":
+        ws = torch.empty(kda.min_workspace_bytes(N), dtype=torch.uint8, device="cuda")
+    o_full, fs_full = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
+                                  d["init_state"], workspace=ws, check_status=True)
+    o_none, fs_only = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
+                                  d["init_state"], workspace=ws, check_status=True, outputs=False)
+    torch.cuda.synchronize()
+    assert o_none is None
+    np.testing.assert_array_equal(synth.to_f64(fs_only), synth.to_f64(fs_full))
