@@ -123,6 +123,23 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, const floa
                          void *workspace, size_t workspace_bytes, void *stream);
 
 /*
+ * kda_decode_step on a paged state cache: sequence b's state is slot slots[b] of
+ * state_pool ([num_slots, num_heads, d_k, d_v] fp32, read and overwritten in place),
+ * so a serving runtime can keep every live sequence's state in one pool and decode
+ * any subset of them in one call ("Day 19", section 2: constant memory per sequence).
+ *  slots          [batch] int32 device indices in [0, num_slots); they must be
+ *                 distinct within a call (two sequences on one slot race)
+ *  device_errors  NULL or a device uint32 that receives KDA_DEVICE_ERR_SLOT (or-ed)
+ *                 when a slot is out of range; that sequence is then skipped (its o
+ *                 and every pool slot are left untouched) and the others run
+ * Other arguments, layouts and errors as kda_decode_step.
+ */
+kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, const float *log_alpha,
+                                   const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
+                                   int32_t d_v, kda_dtype_t dtype, float *state_pool, int32_t num_slots,
+                                   const int32_t *slots, void *o, uint32_t *device_errors, void *stream);
+
+/*
  * kda_prefill with its stages marked, for measuring them: the same arguments and
  * results, plus four CUDA events (cudaEvent_t handles passed as void*, created by
  * the caller) recorded on `stream`:
@@ -201,6 +218,7 @@ kda_status_t kda_read_device_status(void *workspace, void *stream);
 #define KDA_DEVICE_ERR_TIMEOUT 2u /* a bounded device-side wait expired                   */
 #define KDA_DEVICE_ERR_DECAY 4u   /* a chunk's cumulative log-decay left the supported range */
 #define KDA_DEVICE_ERR_RANGE 8u   /* a value held in fp16 left the fp16 range (two-kernel path) */
+#define KDA_DEVICE_ERR_SLOT 16u   /* kda_decode_step_slots: a slot index out of range          */
 kda_status_t kda_prefill_no_alloc(const void *q, const void *k, const void *v,
                                   const float *log_alpha, const float *beta,
                                   const int32_t *cu_seqlens, int32_t num_seqs,

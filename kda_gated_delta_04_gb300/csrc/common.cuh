@@ -15,6 +15,7 @@ enum : uint32_t {
     DEV_ERR_TIMEOUT = 2u,  // a bounded mbarrier / flag wait gave up
     DEV_ERR_DECAY = 4u,    // |in-chunk cumulative log-decay| exceeded the supported range
     DEV_ERR_RANGE = 8u,    // a value kept in fp16 left the fp16 range
+    DEV_ERR_SLOT = 16u,    // a state-slot index outside [0, num_slots)
 };
 
 constexpr int kChunk = KDA_CHUNK;
@@ -47,6 +48,11 @@ struct DecodeProblem {
     float *state;
     void *o;
     cudaStream_t stream;
+    // paged state (optional): sequence b's state is slot slots[b] of `state`, which then
+    // holds num_slots x num_heads states; out-of-range slots are skipped and reported in *errors
+    const int32_t *slots = nullptr;
+    int num_slots = 0;
+    uint32_t *errors = nullptr;
 };
 
 // Launchers (each returns the launch error, cudaSuccess when enqueued).

@@ -26,7 +26,8 @@ template <int D, typename IO>
 __global__ void __launch_bounds__(256, 2)
 decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
               const float *__restrict__ log_alpha, const float *__restrict__ beta,
-              float *__restrict__ state, IO *__restrict__ o)
+              float *__restrict__ state, IO *__restrict__ o, const int32_t *__restrict__ slots,
+              int H, int num_slots, uint32_t *errors)
 {
     constexpr int TPR = D / 4;      // threads per state row
     constexpr int RPP = 256 / TPR;  // rows per pass
@@ -40,7 +41,16 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
     __shared__ __align__(16) float s_rk[RPP][D];
     __shared__ __align__(16) float s_rq[RPP][D];
 
-    float *S = state + (size_t)unit * D * D;
+    size_t sunit = (size_t)unit;  // the unit's state: its own, or its sequence's pool slot
+    if (slots) {
+        const int b = unit / H, slot = slots[b];
+        if (slot < 0 || slot >= num_slots) {
+            if (tid == 0 && errors) atomicOr(errors, DEV_ERR_SLOT);
+            return;
+        }
+        sunit = (size_t)slot * H + (unit - b * H);
+    }
+    float *S = state + sunit * D * D;
     float4 s[P];
 #pragma unroll
     for (int p = 0; p < P; ++p)
@@ -95,7 +105,7 @@ cudaError_t launch(const DecodeProblem &p)
     const int units = p.batch * p.num_heads;
     decode_kernel<D, IO><<<units, 256, 0, p.stream>>>(
         static_cast<const IO *>(p.q), static_cast<const IO *>(p.k), static_cast<const IO *>(p.v),
-        p.log_alpha, p.beta, p.state, static_cast<IO *>(p.o));
+        p.log_alpha, p.beta, p.state, static_cast<IO *>(p.o), p.slots, p.num_heads, p.num_slots, p.errors);
     return cudaGetLastError();
 }
 

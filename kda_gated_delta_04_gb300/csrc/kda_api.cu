@@ -166,6 +166,32 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
                         d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream, ev);
 }
 
+kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, const float *log_alpha,
+                                   const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
+                                   int32_t d_v, kda_dtype_t dtype, float *state_pool, int32_t num_slots,
+                                   const int32_t *slots, void *o, uint32_t *device_errors, void *stream)
+{
+    kda_status_t st = check_shape(d_k, d_v, dtype);
+    if (st != KDA_OK) return st;
+    if (batch < 0 || num_heads <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
+    if ((int64_t)batch * num_heads > INT32_MAX || (int64_t)num_slots * num_heads > INT32_MAX)
+        return KDA_ERR_UNSUPPORTED;
+    if (batch == 0) return KDA_OK;
+    if (!q || !k || !v || !log_alpha || !beta || !state_pool || !slots || !o) return KDA_ERR_INVALID_ARG;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) ||
+        !aligned(o, 16) || !aligned(state_pool, 16) || !aligned(beta, 4) || !aligned(slots, 4) ||
+        (device_errors && !aligned(device_errors, 4)))
+        return KDA_ERR_INVALID_ARG;
+    st = check_device();
+    if (st != KDA_OK) return st;
+    kda::DecodeProblem p;
+    p.q = q; p.k = k; p.v = v; p.log_alpha = log_alpha; p.beta = beta;
+    p.batch = batch; p.num_heads = num_heads; p.d = d_k; p.dtype = dtype;
+    p.state = state_pool; p.o = o; p.stream = static_cast<cudaStream_t>(stream);
+    p.slots = slots; p.num_slots = num_slots; p.errors = device_errors;
+    return kda::launch_decode(p) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
 kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
                              const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
                              int32_t d_v, kda_dtype_t dtype, float *state, void *o, void *stream)
@@ -197,7 +223,7 @@ kda_status_t kda_read_device_status(void *workspace, void *stream)
         return KDA_ERR_CUDA;
     if (cudaMemsetAsync(workspace, 0, sizeof(word), s) != cudaSuccess) return KDA_ERR_CUDA;
     if (cudaStreamSynchronize(s) != cudaSuccess) return KDA_ERR_CUDA;
-    if (word & kda::DEV_ERR_SEQLENS) return KDA_ERR_INVALID_ARG;
+    if (word & (kda::DEV_ERR_SEQLENS | kda::DEV_ERR_SLOT)) return KDA_ERR_INVALID_ARG;
     if (word & kda::DEV_ERR_TIMEOUT) return KDA_ERR_TIMEOUT;
     if (word & kda::DEV_ERR_DECAY) return KDA_ERR_DECAY_RANGE;
     if (word & kda::DEV_ERR_RANGE) return KDA_ERR_VALUE_RANGE;

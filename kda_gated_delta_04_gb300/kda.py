@@ -42,6 +42,8 @@ EXPORTS = {
     "kda_prefill_no_alloc": (_c.c_int, _PREFILL_ARGS[:15] + [_VP, _VP]),
     "kda_prefill_events": (_c.c_int, _PREFILL_ARGS + [_c.POINTER(_VP), _c.c_int32]),
     "kda_selftest_bounded_wait": (_c.c_int, [_VP, _c.c_uint64, _VP]),
+    "kda_decode_step_slots": (_c.c_int, [_VP, _VP, _VP, _VP, _VP, _c.c_int32, _c.c_int32, _c.c_int32,
+                                         _c.c_int32, _c.c_int, _VP, _c.c_int32, _VP, _VP, _VP, _VP]),
 }
 
 
@@ -104,6 +106,12 @@ def kda_prefill_events(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tok
     return lib().kda_prefill_events(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens,
                                     num_heads, d_k, d_v, dtype, init_state, o, final_state,
                                     workspace, workspace_bytes, stream, arr, len(events))
+
+
+def kda_decode_step_slots(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype, state_pool,
+                          num_slots, slots, o, device_errors, stream):
+    return lib().kda_decode_step_slots(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype,
+                                       state_pool, num_slots, slots, o, device_errors, stream)
 
 
 def kda_selftest_bounded_wait(workspace, limit_ns, stream):
@@ -202,6 +210,27 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
         if st != KDA_OK:
             raise KdaError(st, "kda_prefill (device)")
     return o, final_state
+
+
+def decode_step_slots(q, k, v, log_alpha, beta, state_pool, slots, *, o=None, errors=None,
+                      stream=None):
+    """One decode step on a paged state cache: state_pool [S, H, d, d] fp32 (updated in
+    place), slots int32 [B] CUDA tensor of distinct slot indices.  Returns o [B, H, d]."""
+    torch = _torch()
+    B, H, d = q.shape
+    dt = _dtype_code(q)
+    if o is None:
+        o = torch.empty((B, H, v.shape[2]), dtype=q.dtype, device=q.device)
+    st = kda_decode_step_slots(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
+                               _ptr(log_alpha, "log_alpha", torch.float32),
+                               _ptr(beta, "beta", torch.float32), B, H, d, v.shape[2], dt,
+                               _ptr(state_pool, "state_pool", torch.float32), state_pool.shape[0],
+                               _ptr(slots, "slots", torch.int32), _ptr(o, "o", q.dtype),
+                               None if errors is None else _ptr(errors, "errors", torch.int32),
+                               _stream_handle(stream, q.device))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_decode_step_slots")
+    return o
 
 
 def decode_step(q, k, v, log_alpha, beta, state, *, o=None, stream=None):

@@ -54,3 +54,48 @@ def test_empty_batch_is_a_no_op():
     st = kda.kda_decode_step(None, None, None, None, None, 0, 2, 64, 64, kda.KDA_DTYPE_F32, None,
                              None, None)
     assert st == kda.KDA_OK
+
+
+def test_paged_decode_matches_contiguous_decode_and_the_oracle():
+    """kda_decode_step_slots on a pool of 7 states x 3 heads, four sequences on slots
+    [5, 0, 3, 6], for several steps: bit for bit the contiguous decode of the gathered
+    states, within the bar of the oracle, and the slots nobody decodes are untouched."""
+    w = DecodeWorkload("decode_paged", 131, 4, 3, 128, "bf16", 6)
+    slots_h = [5, 0, 3, 6]
+    pool = torch.zeros((7, 3, 128, 128), dtype=torch.float32)
+    pool[1] = 1.0  # unused slots must stay as they are
+    pool[2] = -2.0
+    pool[4] = 3.0
+    state0 = synth.decode_state(w)
+    pool[slots_h] = state0
+    pool_d = pool.cuda()
+    slots = torch.tensor(slots_h, dtype=torch.int32, device="cuda")
+    contiguous = state0.clone().cuda()
+    ref_state = synth.to_f64(state0)
+    for s in range(w.steps):
+        x = {k: t.cuda() for k, t in synth.decode_inputs(w, s).items()}
+        o_paged = kda.decode_step_slots(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], pool_d, slots)
+        o_cont = kda.decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], contiguous)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(synth.to_f64(o_paged), synth.to_f64(o_cont))
+        r = {k: synth.to_f64(t) for k, t in synth.decode_inputs(w, s).items()}
+        o_ref, _ = oracle.decode_step(r["q"], r["k"], r["v"], r["log_alpha"], r["beta"], ref_state)
+        assert maxabs(synth.to_f64(o_paged), o_ref) <= TOL["bf16"]["o"]
+    np.testing.assert_array_equal(synth.to_f64(pool_d[slots_h].cpu()), synth.to_f64(contiguous.cpu()))
+    assert relF(synth.to_f64(pool_d[slots_h].cpu()), ref_state) <= TOL["bf16"]["state"]
+    for free, val in ((1, 1.0), (2, -2.0), (4, 3.0)):
+        assert bool((pool_d[free] == val).all())
+
+
+def test_paged_decode_reports_a_bad_slot_and_runs_the_rest():
+    w = DecodeWorkload("decode_bad_slot", 132, 3, 2, 64, "f32", 1)
+    pool = synth.decode_state(w).cuda()  # slots 0..2
+    before = pool.clone()
+    x = {k: t.cuda() for k, t in synth.decode_inputs(w, 0).items()}
+    slots = torch.tensor([0, 9, 2], dtype=torch.int32, device="cuda")  # 9 is out of range
+    errors = torch.zeros(1, dtype=torch.int32, device="cuda")
+    kda.decode_step_slots(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], pool, slots, errors=errors)
+    torch.cuda.synchronize()
+    assert errors.item() == 16  # KDA_DEVICE_ERR_SLOT
+    assert torch.equal(pool[1], before[1])          # slot 1: no sequence decodes it
+    assert not torch.equal(pool[0], before[0]) and not torch.equal(pool[2], before[2])
