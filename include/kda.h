@@ -159,6 +159,26 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
                                 void *stream, void *const *events, int32_t num_events);
 
 /*
+ * Options of kda_prefill_ex / kda_decode_step_ex (bitwise or; other bits are
+ * rejected with KDA_ERR_INVALID_ARG).
+ *  KDA_FLAG_SCALAR_GATE  scalar-gate (Gated DeltaNet) variant: log_alpha holds one
+ *                        value per token-head, [total_tokens, num_heads] fp32 (4-byte
+ *                        aligned; decode: [batch, num_heads]), the decay of every key
+ *                        channel ("From 124M to 2.8T", chapter 3: the scalar gate of
+ *                        Gated DeltaNet; "K3 attention, three-piece set": KDA makes the
+ *                        gate channel-wise).  Its chunk-prefix bound is the same.
+ */
+#define KDA_FLAG_SCALAR_GATE 1u
+
+/* kda_prefill with options (flags above); flags = 0 is kda_prefill.  With a scalar
+ * gate and only the minimal workspace, bf16 d = 128 runs the exact CUDA-core kernel. */
+kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                            const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                            int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                            kda_dtype_t dtype, const float *init_state, void *o, float *final_state,
+                            void *workspace, size_t workspace_bytes, void *stream, uint32_t flags);
+
+/*
  * One decode step for `batch` sequences x num_heads heads: the recurrence for a
  * single new token per sequence, applied to the caller's state in place
  * ("Day 19", section 2: constant memory and O(1) work per generated token;
@@ -175,6 +195,12 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
 kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
                              const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
                              int32_t d_v, kda_dtype_t dtype, float *state, void *o, void *stream);
+
+/* kda_decode_step with options (flags above); flags = 0 is kda_decode_step. */
+kda_status_t kda_decode_step_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                                const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
+                                int32_t d_v, kda_dtype_t dtype, float *state, void *o, void *stream,
+                                uint32_t flags);
 
 /*
  * Synchronises `stream`, reads the device-side error record of the last

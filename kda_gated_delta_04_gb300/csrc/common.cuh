@@ -37,6 +37,7 @@ struct PrefillProblem {
     int32_t *order;             // workspace: sequence processing order (longest first)
     int32_t *cc;                // workspace: first chunk of each sequence [num_seqs + 1], or null
     void *records;              // workspace: per chunk-head records of the two-kernel path, or null
+    bool scalar_gate = false;   // log_alpha is [T, H]: one decay per token-head for every key channel
     cudaStream_t stream;
 };
 
@@ -53,6 +54,7 @@ struct DecodeProblem {
     const int32_t *slots = nullptr;
     int num_slots = 0;
     uint32_t *errors = nullptr;
+    bool scalar_gate = false;   // log_alpha is [B, H]: one decay per sequence-head for every key channel
 };
 
 // Launchers (each returns the launch error, cudaSuccess when enqueued).

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256, 2)
 decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
               const float *__restrict__ log_alpha, const float *__restrict__ beta,
               float *__restrict__ state, IO *__restrict__ o, const int32_t *__restrict__ slots,
-              int H, int num_slots, uint32_t *errors)
+              int H, int num_slots, uint32_t *errors, bool scalar_gate)
 {
     constexpr int TPR = D / 4;      // threads per state row
     constexpr int RPP = 256 / TPR;  // rows per pass
@@ -57,7 +57,7 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
         s[p] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)(r0 + p * RPP) * D) + c4);
 
     if (tid < D) {
-        s_a[tid] = expf(log_alpha[(size_t)unit * D + tid]);
+        s_a[tid] = expf(scalar_gate ? log_alpha[unit] : log_alpha[(size_t)unit * D + tid]);
         s_k[tid] = load_io(k + (size_t)unit * D + tid);
         s_q[tid] = load_io(q + (size_t)unit * D + tid);
     }
@@ -105,7 +105,8 @@ cudaError_t launch(const DecodeProblem &p)
     const int units = p.batch * p.num_heads;
     decode_kernel<D, IO><<<units, 256, 0, p.stream>>>(
         static_cast<const IO *>(p.q), static_cast<const IO *>(p.k), static_cast<const IO *>(p.v),
-        p.log_alpha, p.beta, p.state, static_cast<IO *>(p.o), p.slots, p.num_heads, p.num_slots, p.errors);
+        p.log_alpha, p.beta, p.state, static_cast<IO *>(p.o), p.slots, p.num_heads, p.num_slots, p.errors,
+        p.scalar_gate);
     return cudaGetLastError();
 }
 

@@ -79,8 +79,11 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
                           const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
                           int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
                           kda_dtype_t dtype, const float *init_state, void *o, float *final_state,
-                          void *workspace, size_t workspace_bytes, void *stream, const cudaEvent_t *ev)
+                          void *workspace, size_t workspace_bytes, void *stream, const cudaEvent_t *ev,
+                          uint32_t flags)
 {
+    if (flags & ~(uint32_t)KDA_FLAG_SCALAR_GATE) return KDA_ERR_INVALID_ARG;
+    const bool scalar_gate = (flags & KDA_FLAG_SCALAR_GATE) != 0;
     kda_status_t st = check_shape(d_k, d_v, dtype);
     if (st != KDA_OK) return st;
     if (num_seqs < 0 || total_tokens < 0 || num_heads <= 0) return KDA_ERR_INVALID_ARG;
@@ -92,7 +95,7 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta))
         return KDA_ERR_INVALID_ARG;
     if (!final_state || !workspace) return KDA_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) ||
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, scalar_gate ? 4 : 16) ||
         !aligned(o, 16) || !aligned(final_state, 16) || !aligned(beta, 4) ||
         (init_state && !aligned(init_state, 16)) || (cu_seqlens && !aligned(cu_seqlens, 4)) ||
         !aligned(workspace, 256))
@@ -109,6 +112,7 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     p.cu_seqlens = cu_seqlens; p.num_seqs = num_seqs; p.total_tokens = total_tokens;
     p.num_heads = num_heads; p.d = d_k; p.dtype = dtype; p.init_state = init_state;
     p.o = o; p.final_state = final_state;
+    p.scalar_gate = scalar_gate;
     p.status = static_cast<uint32_t *>(workspace);
     char *ws = static_cast<char *>(workspace);
     p.order = reinterpret_cast<int32_t *>(ws + kda::kWorkspaceHeader);
@@ -146,7 +150,18 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, const floa
 {
     return prefill_impl(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
                         d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream,
-                        nullptr);
+                        nullptr, 0u);
+}
+
+kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                            const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                            int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                            kda_dtype_t dtype, const float *init_state, void *o, float *final_state,
+                            void *workspace, size_t workspace_bytes, void *stream, uint32_t flags)
+{
+    return prefill_impl(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
+                        d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream,
+                        nullptr, flags);
 }
 
 kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -163,7 +178,7 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
         ev[i] = static_cast<cudaEvent_t>(events[i]);
     }
     return prefill_impl(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
-                        d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream, ev);
+                        d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream, ev, 0u);
 }
 
 kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -192,17 +207,20 @@ kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, 
     return kda::launch_decode(p) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
-kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
-                             const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
-                             int32_t d_v, kda_dtype_t dtype, float *state, void *o, void *stream)
+kda_status_t kda_decode_step_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                                const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
+                                int32_t d_v, kda_dtype_t dtype, float *state, void *o, void *stream,
+                                uint32_t flags)
 {
+    if (flags & ~(uint32_t)KDA_FLAG_SCALAR_GATE) return KDA_ERR_INVALID_ARG;
+    const bool scalar_gate = (flags & KDA_FLAG_SCALAR_GATE) != 0;
     kda_status_t st = check_shape(d_k, d_v, dtype);
     if (st != KDA_OK) return st;
     if (batch < 0 || num_heads <= 0) return KDA_ERR_INVALID_ARG;
     if ((int64_t)batch * num_heads > INT32_MAX) return KDA_ERR_UNSUPPORTED;
     if (batch == 0) return KDA_OK;  // nothing to read or write; pointers may be NULL
     if (!q || !k || !v || !log_alpha || !beta || !state || !o) return KDA_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) ||
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, scalar_gate ? 4 : 16) ||
         !aligned(o, 16) || !aligned(state, 16) || !aligned(beta, 4))
         return KDA_ERR_INVALID_ARG;
     st = check_device();
@@ -211,7 +229,16 @@ kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const 
     p.q = q; p.k = k; p.v = v; p.log_alpha = log_alpha; p.beta = beta;
     p.batch = batch; p.num_heads = num_heads; p.d = d_k; p.dtype = dtype;
     p.state = state; p.o = o; p.stream = static_cast<cudaStream_t>(stream);
+    p.scalar_gate = scalar_gate;
     return kda::launch_decode(p) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+kda_status_t kda_decode_step(const void *q, const void *k, const void *v, const float *log_alpha,
+                             const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
+                             int32_t d_v, kda_dtype_t dtype, float *state, void *o, void *stream)
+{
+    return kda_decode_step_ex(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype, state, o,
+                              stream, 0u);
 }
 
 kda_status_t kda_read_device_status(void *workspace, void *stream)

@@ -125,7 +125,7 @@ prefill_simt_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO
                     const float *__restrict__ log_alpha, const float *__restrict__ beta,
                     const int32_t *__restrict__ cu, int64_t total, int H,
                     const float *init_state, IO *__restrict__ o, float *final_state,
-                    uint32_t *status, const int32_t *__restrict__ order)
+                    uint32_t *status, const int32_t *__restrict__ order, bool scalar_gate)
 {
     using Sm = SimtSmem<D, DV>;
     constexpr int LD = Sm::LD, LA = Sm::LA;
@@ -159,7 +159,12 @@ prefill_simt_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO
                 const size_t row = ((size_t)(c0 + r) * H + h) * D + i4;
                 a = load4_io(q + row);
                 b = load4_io(k + row);
-                c = *reinterpret_cast<const float4 *>(log_alpha + row);
+                if (scalar_gate) {  // log_alpha [T, H]: one decay for every key channel
+                    const float x = log_alpha[(size_t)(c0 + r) * H + h];
+                    c = make_float4(x, x, x, x);
+                } else {
+                    c = *reinterpret_cast<const float4 *>(log_alpha + row);
+                }
             }
             *reinterpret_cast<float4 *>(&sm.q[r * LD + i4]) = a;
             *reinterpret_cast<float4 *>(&sm.k[r * LD + i4]) = b;
@@ -301,7 +306,7 @@ cudaError_t launch_simt(const PrefillProblem &p)
     kern<<<grid, kThreads, smem, p.stream>>>(
         static_cast<const IO *>(p.q), static_cast<const IO *>(p.k), static_cast<const IO *>(p.v),
         p.log_alpha, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.init_state,
-        static_cast<IO *>(p.o), p.final_state, p.status, p.order);
+        static_cast<IO *>(p.o), p.final_state, p.status, p.order, p.scalar_gate);
     return cudaGetLastError();
 }
 

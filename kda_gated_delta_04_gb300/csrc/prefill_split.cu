@@ -297,7 +297,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                      const float *__restrict__ log_alpha, const float *__restrict__ beta,
                      const int32_t *__restrict__ cu, int64_t total, int H, int num_seqs,
                      int chunk_bound, const int32_t *__restrict__ cc,
-                     unsigned char *__restrict__ records, uint32_t *status, bool with_o)
+                     unsigned char *__restrict__ records, uint32_t *status, bool with_o, bool scalar_gate)
 {
     using L = ChunkLayout;
     constexpr int NT = kChunkThreads;
@@ -349,7 +349,10 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     float *s_tot = reinterpret_cast<float *>(sm + L::AQ);
     float2 gl[4096 / NT];
     float gmin, gmax;
-    prefix_scan<NT>(log_alpha + ((size_t)c0 * H + h) * kD, H * kD, len, s_tot, gl, gmin, gmax);
+    if (scalar_gate)  // log_alpha [T, H]: one decay per token-head
+        prefix_scan<NT>(log_alpha + (size_t)c0 * H + h, H, len, s_tot, gl, gmin, gmax, true);
+    else
+        prefix_scan<NT>(log_alpha + ((size_t)c0 * H + h) * kD, H * kD, len, s_tot, gl, gmin, gmax);
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_holder;
@@ -767,7 +770,8 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     cfg.numAttrs = 1;
     err = cudaLaunchKernelEx(&cfg, prefill_chunk_kernel, tq, tk, p.log_alpha, p.beta, p.cu_seqlens,
                              p.total_tokens, p.num_heads, p.num_seqs, (int)chunk_bound, cc,
-                             static_cast<unsigned char *>(records), p.status, p.o != nullptr);
+                             static_cast<unsigned char *>(records), p.status, p.o != nullptr,
+                             p.scalar_gate);
     if (err != cudaSuccess) return err;
     if (mid && (err = cudaEventRecord(mid, p.stream)) != cudaSuccess) return err;
     cfg.gridDim = dim3(kD / kDV, p.num_heads, p.num_seqs);

@@ -60,7 +60,8 @@ struct FusedLayout {
 };
 using L = FusedLayout;
 constexpr uint32_t kSmemDyn = L::USED + 1024;  // slack to align the base to 1024 bytes
-constexpr uint32_t kTxBytes = 16384 + 16384 + 32768 + 4096;
+constexpr uint32_t kLaBoxBytes = kC * kD * 4;  // log_alpha [64 x 128] fp32
+constexpr uint32_t kTxBytes = 16384 + 16384 + kLaBoxBytes + 4096;
 static_assert(L::AQ == L::O4 + 8192, "[T' ; Aqk] must be one 128-row operand");
 static_assert(L::SOLVE_X + 32 * kLdX * 4 <= L::IN_V, "solve scratch must fit in the input area");
 
@@ -74,12 +75,13 @@ constexpr uint32_t IDESC_G5 = idesc_tf32(128, 32, false, false);
 __device__ __forceinline__ void issue_chunk_loads(unsigned char *sm, const CUtensorMap *tq,
                                                   const CUtensorMap *tk, const CUtensorMap *tla,
                                                   const CUtensorMap *tv, uint64_t *bar, int h,
-                                                  int j0, int row)
+                                                  int j0, int row, bool scalar_gate)
 {
-    mbar_arrive_expect_tx(bar, kTxBytes);
+    // a scalar gate is read from global memory by the prefix scan: no log_alpha box
+    mbar_arrive_expect_tx(bar, scalar_gate ? kTxBytes - kLaBoxBytes : kTxBytes);
     tma_load_3d(sm + L::IN_Q, tq, bar, 0, h, row);
     tma_load_3d(sm + L::IN_K, tk, bar, 0, h, row);
-    tma_load_3d(sm + L::IN_LA, tla, bar, 0, h, row);
+    if (!scalar_gate) tma_load_3d(sm + L::IN_LA, tla, bar, 0, h, row);
     tma_load_3d(sm + L::IN_V, tv, bar, j0, h, row);
 }
 
@@ -88,7 +90,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_v,
                   const float *__restrict__ beta, const int32_t *__restrict__ cu, int64_t total,
                   int H, const float *init_state, __nv_bfloat16 *__restrict__ o,
-                  float *final_state, uint32_t *status, const int32_t *__restrict__ order)
+                  float *final_state, uint32_t *status, const int32_t *__restrict__ order,
+                  const float *__restrict__ la_scalar)
 {
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar_tma, bar_mma;
@@ -151,7 +154,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     uint32_t ph_tma = 0, ph_mma = 0;
     bool tma_pending = nchunks > 0, mma_pending = false, timed_out = false, decay_bad = false;
     if (tid == 0 && nchunks > 0)
-        issue_chunk_loads(sm, &tm_q, &tm_k, &tm_la, &tm_v, &bar_tma, h, j0, (int)t0);
+        issue_chunk_loads(sm, &tm_q, &tm_k, &tm_la, &tm_v, &bar_tma, h, j0, (int)t0, la_scalar);
     // group totals of the prefix scan; the tf32 u operand area is idle during the prep
     float *s_tot = reinterpret_cast<float *>(sm + L::O10);
 
@@ -168,7 +171,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // ---------------------------------------------------------- a1, a2
         float2 gl[8];
         float gmin, gmax;
-        prefix_scan<kThreads>(reinterpret_cast<const float *>(sm + L::IN_LA), kD, len, s_tot, gl, gmin, gmax);
+        if (la_scalar)  // log_alpha [T, H]: one decay per token-head
+            prefix_scan<kThreads>(la_scalar + (size_t)c0 * H + h, H, len, s_tot, gl, gmin, gmax, true);
+        else
+            prefix_scan<kThreads>(reinterpret_cast<const float *>(sm + L::IN_LA), kD, len, s_tot, gl,
+                                  gmin, gmax);
         if (tid < kC) {
             s_beta[tid] = beta_next;
             const int64_t cn = c0 + kC;  // next chunk
@@ -210,7 +217,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (tid == 0) {
             if (c + 1 < nchunks)
                 issue_chunk_loads(sm, &tm_q, &tm_k, &tm_la, &tm_v, &bar_tma, h, j0,
-                                  (int)(c0 + kC));
+                                  (int)(c0 + kC), la_scalar);
             tc_fence_after_sync();
             issue_gw<L>(sb, tmem + TM_DW);
 #pragma unroll
@@ -351,14 +358,19 @@ cudaError_t launch_prefill_tc(const PrefillProblem &p)
     CUtensorMap tq, tk, tla, tv;
     if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, p.total_tokens, p.num_heads, 2, kD) ||
         !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, p.total_tokens, p.num_heads, 2, kD) ||
-        !make_map(&tla, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.log_alpha, p.total_tokens, p.num_heads, 4,
-                  kD) ||
         !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kDV))
+        return cudaErrorInvalidValue;
+    // a scalar gate ([T, H]) is read by the prefix scan, never by TMA: its map slot repeats q's
+    if (p.scalar_gate)
+        tla = tq;
+    else if (!make_map(&tla, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.log_alpha, p.total_tokens,
+                       p.num_heads, 4, kD))
         return cudaErrorInvalidValue;
     dim3 grid(kD / kDV, p.num_heads, p.num_seqs);
     prefill_tc_kernel<<<grid, kThreads, kSmemDyn, p.stream>>>(
         tq, tk, tla, tv, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.init_state,
-        static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.status, p.order);
+        static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.status, p.order,
+        p.scalar_gate ? p.log_alpha : nullptr);
     return cudaGetLastError();
 }
 

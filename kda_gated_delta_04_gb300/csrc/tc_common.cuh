@@ -89,10 +89,11 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[8])
 // ---------------------------------------------------------------- a1: prefix
 // Thread = (channel pair cp: channels 2cp, 2cp+1; row group rg of R = 4096/NT
 // rows).  Scans its rows of log_alpha (row stride `la_stride` floats, shared or
-// global memory) in registers and leaves the group totals in s_tot.
+// global memory) in registers and leaves the group totals in s_tot.  With `scalar`
+// each row holds one value, the decay of every key channel (scalar gate).
 template <int NT>
 __device__ __forceinline__ void prefix_scan(const float *la, int la_stride, int len, float *s_tot,
-                                            float2 (&gl)[4096 / NT], float &gmin, float &gmax)
+                                            float2 (&gl)[4096 / NT], float &gmin, float &gmax, bool scalar = false)
 {
     constexpr int R = 4096 / NT;
     const int tid = threadIdx.x, cp = tid & 63, rg = tid >> 6;
@@ -103,8 +104,13 @@ __device__ __forceinline__ void prefix_scan(const float *la, int la_stride, int 
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {  // all loads first (they may come from global memory)
         const int r = rg * R + rr;
-        x[rr] = r < len ? *reinterpret_cast<const float2 *>(la + (size_t)r * la_stride + 2 * cp)
-                        : make_float2(0.f, 0.f);
+        if (scalar) {
+            const float a = r < len ? la[(size_t)r * la_stride] : 0.f;
+            x[rr] = make_float2(a, a);
+        } else {
+            x[rr] = r < len ? *reinterpret_cast<const float2 *>(la + (size_t)r * la_stride + 2 * cp)
+                            : make_float2(0.f, 0.f);
+        }
     }
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {

@@ -21,6 +21,7 @@ LIB_PATH = os.path.join(PKG, "libkda.so")
 KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, \
     KDA_ERR_DECAY_RANGE, KDA_ERR_VALUE_RANGE = range(7)
 KDA_DTYPE_BF16, KDA_DTYPE_F32 = 0, 1
+KDA_FLAG_SCALAR_GATE = 1
 CHUNK = 64
 
 _lib = None
@@ -42,6 +43,8 @@ EXPORTS = {
     "kda_prefill_no_alloc": (_c.c_int, _PREFILL_ARGS[:15] + [_VP, _VP]),
     "kda_prefill_events": (_c.c_int, _PREFILL_ARGS + [_c.POINTER(_VP), _c.c_int32]),
     "kda_selftest_bounded_wait": (_c.c_int, [_VP, _c.c_uint64, _VP]),
+    "kda_prefill_ex": (_c.c_int, _PREFILL_ARGS + [_c.c_uint32]),
+    "kda_decode_step_ex": (_c.c_int, _DECODE_ARGS + [_c.c_uint32]),
     "kda_decode_step_slots": (_c.c_int, [_VP, _VP, _VP, _VP, _VP, _c.c_int32, _c.c_int32, _c.c_int32,
                                          _c.c_int32, _c.c_int, _VP, _c.c_int32, _VP, _VP, _VP, _VP]),
 }
@@ -80,6 +83,19 @@ def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, nu
     return lib().kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens,
                              num_heads, d_k, d_v, dtype, init_state, o, final_state, workspace,
                              workspace_bytes, stream)
+
+
+def kda_prefill_ex(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
+                   d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream, flags):
+    return lib().kda_prefill_ex(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens,
+                                num_heads, d_k, d_v, dtype, init_state, o, final_state, workspace,
+                                workspace_bytes, stream, flags)
+
+
+def kda_decode_step_ex(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype, state, o, stream,
+                       flags):
+    return lib().kda_decode_step_ex(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype,
+                                    state, o, stream, flags)
 
 
 def kda_decode_step(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype, state, o, stream):
@@ -182,7 +198,8 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
     """KDA prefill over packed sequences.  q, k: [T, H, d]; v: [T, H, d]; log_alpha: [T, H, d]
     fp32; beta: [T, H] fp32; cu_seqlens: int32 [N+1] CUDA tensor or None (one sequence);
     init_state: [N, H, d, d] fp32 or None.  Returns (o, final_state); with outputs=False
-    only the final states are computed and o is None."""
+    only the final states are computed and o is None.  A log_alpha of shape [T, H] is the
+    scalar-gate (Gated DeltaNet) variant: one decay per token-head for every key channel."""
     torch = _torch()
     T, H, d = q.shape
     dt = _dtype_code(q)
@@ -195,14 +212,15 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
         final_state = torch.empty((N, H, d, v.shape[2]), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = workspace_for(N, T, H, d, dt, q.device)
-    st = kda_prefill(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
+    flags = KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0
+    st = kda_prefill_ex(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
                      _ptr(log_alpha, "log_alpha", torch.float32), _ptr(beta, "beta", torch.float32),
                      _ptr(cu_seqlens, "cu_seqlens", torch.int32), N, T, H, d, v.shape[2], dt,
                      _ptr(init_state, "init_state", torch.float32),
                      None if o is None else _ptr(o, "o", q.dtype),
                      _ptr(final_state, "final_state", torch.float32), _ptr(workspace, "workspace"),
                      workspace.numel() * workspace.element_size(),
-                     _stream_handle(stream, q.device))
+                     _stream_handle(stream, q.device), flags)
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill")
     if check_status:
@@ -234,17 +252,19 @@ def decode_step_slots(q, k, v, log_alpha, beta, state_pool, slots, *, o=None, er
 
 
 def decode_step(q, k, v, log_alpha, beta, state, *, o=None, stream=None):
-    """One decode step; state [B, H, d, d] fp32 is updated in place.  Returns o [B, H, d]."""
+    """One decode step; state [B, H, d, d] fp32 is updated in place.  Returns o [B, H, d].
+    A log_alpha of shape [B, H] is the scalar-gate variant."""
     torch = _torch()
     B, H, d = q.shape
     dt = _dtype_code(q)
     if o is None:
         o = torch.empty((B, H, v.shape[2]), dtype=q.dtype, device=q.device)
-    st = kda_decode_step(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
-                         _ptr(log_alpha, "log_alpha", torch.float32),
-                         _ptr(beta, "beta", torch.float32), B, H, d, v.shape[2], dt,
-                         _ptr(state, "state", torch.float32), _ptr(o, "o", q.dtype),
-                         _stream_handle(stream, q.device))
+    flags = KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0
+    st = kda_decode_step_ex(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
+                            _ptr(log_alpha, "log_alpha", torch.float32),
+                            _ptr(beta, "beta", torch.float32), B, H, d, v.shape[2], dt,
+                            _ptr(state, "state", torch.float32), _ptr(o, "o", q.dtype),
+                            _stream_handle(stream, q.device), flags)
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_step")
     return o

@@ -104,3 +104,9 @@ def test_product_path_does_not_import_the_oracle():
                 text = open(os.path.join(dirpath, f)).read()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "kda_oracle" not in text, f
+
+
+def test_unknown_flags_are_rejected_on_host(kda):
+    a = _prefill_args()
+    assert kda.kda_prefill_ex(*a.values(), 1 << 7) == 1
+    assert kda.kda_decode_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 128, 0, FAKE, FAKE, None, 4) == 1

@@ -99,3 +99,27 @@ def test_paged_decode_reports_a_bad_slot_and_runs_the_rest():
     assert errors.item() == 16  # KDA_DEVICE_ERR_SLOT
     assert torch.equal(pool[1], before[1])          # slot 1: no sequence decodes it
     assert not torch.equal(pool[0], before[0]) and not torch.equal(pool[2], before[2])
+
+
+
+def test_scalar_gate_decode():
+    """KDA_FLAG_SCALAR_GATE in decode: log_alpha [B, H]; bit for bit the per-channel call on
+    the broadcast gate, and within the bar of the oracle."""
+    w = DecodeWorkload("decode_scalar_gate", 133, 3, 4, 128, "bf16", 3)
+    st_s = synth.decode_state(w).cuda()
+    st_f = st_s.clone()
+    ref_state = synth.to_f64(synth.decode_state(w))
+    g = torch.Generator().manual_seed(133)
+    for s in range(w.steps):
+        x = {k: t.cuda() for k, t in synth.decode_inputs(w, s).items()}
+        la = (-0.05 * torch.nn.functional.softplus(torch.randn(3, 4, generator=g))).float()
+        la_full = la[:, :, None].expand(3, 4, 128).contiguous()
+        o_s = kda.decode_step(x["q"], x["k"], x["v"], la.cuda(), x["beta"], st_s)
+        o_f = kda.decode_step(x["q"], x["k"], x["v"], la_full.cuda(), x["beta"], st_f)
+        torch.cuda.synchronize()
+        np.testing.assert_array_equal(synth.to_f64(o_s), synth.to_f64(o_f))
+        r = {k: synth.to_f64(t) for k, t in synth.decode_inputs(w, s).items()}
+        o_ref, _ = oracle.decode_step(r["q"], r["k"], r["v"], synth.to_f64(la_full), r["beta"], ref_state)
+        assert maxabs(synth.to_f64(o_s), o_ref) <= TOL["bf16"]["o"]
+    np.testing.assert_array_equal(synth.to_f64(st_s), synth.to_f64(st_f))
+    assert relF(synth.to_f64(st_s), ref_state) <= TOL["bf16"]["state"]

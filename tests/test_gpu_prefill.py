@@ -274,3 +274,36 @@ def test_state_only_prefill_gives_the_same_final_states(case):
     torch.cuda.synchronize()
     assert o_none is None
     np.testing.assert_array_equal(synth.to_f64(fs_only), synth.to_f64(fs_full))
+
+
+def _scalar_gate(inp, seed):
+    """Scalar-gate inputs: one log_alpha per token-head ([T, H]) and its broadcast [T, H, d]."""
+    g = torch.Generator().manual_seed(seed)
+    T, H, d = inp["q"].shape
+    la = -0.05 * torch.nn.functional.softplus(torch.randn(T, H, generator=g))
+    return la.float().contiguous(), la[:, :, None].expand(T, H, d).float().contiguous()
+
+
+@pytest.mark.parametrize("case", ["two_kernel", "fp32_d64", "single_kernel"])
+def test_scalar_gate_variant(case):
+    """KDA_FLAG_SCALAR_GATE (Gated DeltaNet): one decay per token-head.  Within the bar of the
+    oracle run on the broadcast gate, and bit for bit the per-channel call on that gate."""
+    dtype, d = ("f32", 64) if case == "fp32_d64" else ("bf16", 128)
+    w = PrefillWorkload("scalar_gate_" + case, 123, 2, d, dtype, (150, 0, 64, 97), 4, init_state=True)
+    inp = synth.prefill_inputs(w)
+    la_s, la_full = _scalar_gate(inp, 123)
+    d_ = to_device(inp)
+    ws = None
+    if case == "single_kernel":  # minimal workspace: bf16 d=128 takes the fused tcgen05 kernel
+        ws = torch.empty(kda.min_workspace_bytes(4), dtype=torch.uint8, device="cuda")
+    o_s, fs_s = kda.prefill(d_["q"], d_["k"], d_["v"], la_s.cuda(), d_["beta"], d_["cu_seqlens"],
+                            d_["init_state"], workspace=ws, check_status=True)
+    o_f, fs_f = kda.prefill(d_["q"], d_["k"], d_["v"], la_full.cuda(), d_["beta"], d_["cu_seqlens"],
+                            d_["init_state"], workspace=ws, check_status=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(synth.to_f64(o_s), synth.to_f64(o_f))
+    np.testing.assert_array_equal(synth.to_f64(fs_s), synth.to_f64(fs_f))
+    ref = dict(inp)
+    ref["log_alpha"] = la_full
+    o_ref, fs_ref = oracle_prefill(ref)
+    assert_parity(synth.to_f64(o_s), synth.to_f64(fs_s), o_ref, fs_ref, dtype, "scalar gate " + case)
