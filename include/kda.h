@@ -132,12 +132,14 @@ kda_status_t kda_prefill(const void *q, const void *k, const void *v, const floa
  *  device_errors  NULL or a device uint32 that receives KDA_DEVICE_ERR_SLOT (or-ed)
  *                 when a slot is out of range; that sequence is then skipped (its o
  *                 and every pool slot are left untouched) and the others run
+ *  flags          as kda_decode_step_ex (KDA_FLAG_SCALAR_GATE below)
  * Other arguments, layouts and errors as kda_decode_step.
  */
 kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, const float *log_alpha,
                                    const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
                                    int32_t d_v, kda_dtype_t dtype, float *state_pool, int32_t num_slots,
-                                   const int32_t *slots, void *o, uint32_t *device_errors, void *stream);
+                                   const int32_t *slots, void *o, uint32_t *device_errors, void *stream,
+                                   uint32_t flags);
 
 /*
  * kda_prefill with its stages marked, for measuring them: the same arguments and
@@ -170,13 +172,37 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
  */
 #define KDA_FLAG_SCALAR_GATE 1u
 
-/* kda_prefill with options (flags above); flags = 0 is kda_prefill.  With a scalar
- * gate and only the minimal workspace, bf16 d = 128 runs the exact CUDA-core kernel. */
+/* kda_prefill with options (flags above); flags = 0 is kda_prefill. */
 kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, const float *log_alpha,
                             const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
                             int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
                             kda_dtype_t dtype, const float *init_state, void *o, float *final_state,
                             void *workspace, size_t workspace_bytes, void *stream, uint32_t flags);
+
+/*
+ * kda_prefill against the paged state cache of kda_decode_step_slots: sequence n
+ * starts from slot init_slots[n] of state_pool and its final state is written to
+ * slot final_slots[n], so a prompt is prefilled straight into the pool that decode
+ * then continues from ("Day 19", section 2: a fixed-size state per sequence carried
+ * from the prompt into generation).
+ *  state_pool   [num_slots, num_heads, d_k, d_v] fp32, 16-byte aligned
+ *  init_slots   [num_seqs] int32 device, or NULL (every sequence starts from zero);
+ *               an entry -1 starts that sequence from zero
+ *  final_slots  [num_seqs] int32 device, required
+ * A sequence may read and write the same slot (it is updated in place).  Final
+ * slots must be distinct, and no sequence may start from another sequence's final
+ * slot (the two would race).  A slot outside [0, num_slots) (init: also -1) is a
+ * device-side error (KDA_DEVICE_ERR_SLOT; kda_read_device_status returns
+ * KDA_ERR_INVALID_ARG): that sequence starts from zero, its outputs are computed
+ * and its final state is not written; the other sequences are not affected.
+ * Other arguments (flags included), layouts and errors as kda_prefill_ex.
+ */
+kda_status_t kda_prefill_slots(const void *q, const void *k, const void *v, const float *log_alpha,
+                               const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                               int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                               kda_dtype_t dtype, float *state_pool, int32_t num_slots,
+                               const int32_t *init_slots, const int32_t *final_slots, void *o,
+                               void *workspace, size_t workspace_bytes, void *stream, uint32_t flags);
 
 /*
  * One decode step for `batch` sequences x num_heads heads: the recurrence for a
@@ -244,7 +270,7 @@ kda_status_t kda_read_device_status(void *workspace, void *stream);
 #define KDA_DEVICE_ERR_TIMEOUT 2u /* a bounded device-side wait expired                   */
 #define KDA_DEVICE_ERR_DECAY 4u   /* a chunk's cumulative log-decay left the supported range */
 #define KDA_DEVICE_ERR_RANGE 8u   /* a value held in fp16 left the fp16 range (two-kernel path) */
-#define KDA_DEVICE_ERR_SLOT 16u   /* kda_decode_step_slots: a slot index out of range          */
+#define KDA_DEVICE_ERR_SLOT 16u   /* a state-pool slot index out of range (the _slots calls)   */
 kda_status_t kda_prefill_no_alloc(const void *q, const void *k, const void *v,
                                   const float *log_alpha, const float *beta,
                                   const int32_t *cu_seqlens, int32_t num_seqs,

@@ -22,6 +22,14 @@ constexpr int kChunk = KDA_CHUNK;
 constexpr size_t kWorkspaceHeader = 256;  // status word, padded
 
 // Everything a prefill launch needs, already validated on the host.
+// Where each sequence's states live.  Dense (fin == null): entry n of init_state and of
+// final_state.  A state pool of num entries: init[n] (-1, or init == null: start from zero)
+// and fin[n].
+struct StateSlots {
+    const int32_t *init = nullptr, *fin = nullptr;
+    int64_t num = 0;
+};
+
 struct PrefillProblem {
     const void *q, *k, *v;
     const float *log_alpha, *beta;
@@ -38,6 +46,7 @@ struct PrefillProblem {
     int32_t *cc;                // workspace: first chunk of each sequence [num_seqs + 1], or null
     void *records;              // workspace: per chunk-head records of the two-kernel path, or null
     bool scalar_gate = false;   // log_alpha is [T, H]: one decay per token-head for every key channel
+    StateSlots slots;           // state pool indices, or none (dense states)
     cudaStream_t stream;
 };
 
@@ -106,6 +115,24 @@ __device__ __forceinline__ void seq_range(const int32_t *cu, int n, int64_t tota
     b = b < a ? a : (b > total ? total : b);
     t0 = a;
     t1 = b;
+}
+
+// Sequence n's initial-state entry si (-1: zero) and final-state entry sf (-1: not written).
+// Returns false for a pool slot out of range; the sequence then starts from zero and its final
+// state is not written.
+__device__ __forceinline__ bool state_entries(const StateSlots &s, int n, bool has_init, int64_t &si,
+                                              int64_t &sf)
+{
+    if (!s.fin) {
+        si = has_init ? n : -1;
+        sf = n;
+        return true;
+    }
+    si = s.init ? s.init[n] : -1;
+    sf = s.fin[n];
+    if (si >= -1 && si < s.num && sf >= 0 && sf < s.num) return true;
+    si = sf = -1;
+    return false;
 }
 
 }  // namespace kda

@@ -80,7 +80,7 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
                           int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
                           kda_dtype_t dtype, const float *init_state, void *o, float *final_state,
                           void *workspace, size_t workspace_bytes, void *stream, const cudaEvent_t *ev,
-                          uint32_t flags)
+                          uint32_t flags, const kda::StateSlots *slots = nullptr)
 {
     if (flags & ~(uint32_t)KDA_FLAG_SCALAR_GATE) return KDA_ERR_INVALID_ARG;
     const bool scalar_gate = (flags & KDA_FLAG_SCALAR_GATE) != 0;
@@ -113,6 +113,7 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     p.num_heads = num_heads; p.d = d_k; p.dtype = dtype; p.init_state = init_state;
     p.o = o; p.final_state = final_state;
     p.scalar_gate = scalar_gate;
+    if (slots) p.slots = *slots;
     p.status = static_cast<uint32_t *>(workspace);
     char *ws = static_cast<char *>(workspace);
     p.order = reinterpret_cast<int32_t *>(ws + kda::kWorkspaceHeader);
@@ -164,6 +165,24 @@ kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, const f
                         nullptr, flags);
 }
 
+kda_status_t kda_prefill_slots(const void *q, const void *k, const void *v, const float *log_alpha,
+                               const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                               int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                               kda_dtype_t dtype, float *state_pool, int32_t num_slots,
+                               const int32_t *init_slots, const int32_t *final_slots, void *o,
+                               void *workspace, size_t workspace_bytes, void *stream, uint32_t flags)
+{
+    if (num_slots < 0 || !state_pool || !final_slots || !aligned(init_slots, 4) || !aligned(final_slots, 4))
+        return KDA_ERR_INVALID_ARG;
+    kda::StateSlots slots;
+    slots.init = init_slots;
+    slots.fin = final_slots;
+    slots.num = num_slots;
+    return prefill_impl(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
+                        d_v, dtype, init_slots ? state_pool : nullptr, o, state_pool, workspace,
+                        workspace_bytes, stream, nullptr, flags, &slots);
+}
+
 kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, const float *log_alpha,
                                 const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
                                 int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
@@ -184,8 +203,11 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
 kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, const float *log_alpha,
                                    const float *beta, int32_t batch, int32_t num_heads, int32_t d_k,
                                    int32_t d_v, kda_dtype_t dtype, float *state_pool, int32_t num_slots,
-                                   const int32_t *slots, void *o, uint32_t *device_errors, void *stream)
+                                   const int32_t *slots, void *o, uint32_t *device_errors, void *stream,
+                                   uint32_t flags)
 {
+    if (flags & ~(uint32_t)KDA_FLAG_SCALAR_GATE) return KDA_ERR_INVALID_ARG;
+    const bool scalar_gate = (flags & KDA_FLAG_SCALAR_GATE) != 0;
     kda_status_t st = check_shape(d_k, d_v, dtype);
     if (st != KDA_OK) return st;
     if (batch < 0 || num_heads <= 0 || num_slots < 0) return KDA_ERR_INVALID_ARG;
@@ -193,7 +215,7 @@ kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, 
         return KDA_ERR_UNSUPPORTED;
     if (batch == 0) return KDA_OK;
     if (!q || !k || !v || !log_alpha || !beta || !state_pool || !slots || !o) return KDA_ERR_INVALID_ARG;
-    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, 16) ||
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(log_alpha, scalar_gate ? 4 : 16) ||
         !aligned(o, 16) || !aligned(state_pool, 16) || !aligned(beta, 4) || !aligned(slots, 4) ||
         (device_errors && !aligned(device_errors, 4)))
         return KDA_ERR_INVALID_ARG;
@@ -204,6 +226,7 @@ kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, 
     p.batch = batch; p.num_heads = num_heads; p.d = d_k; p.dtype = dtype;
     p.state = state_pool; p.o = o; p.stream = static_cast<cudaStream_t>(stream);
     p.slots = slots; p.num_slots = num_slots; p.errors = device_errors;
+    p.scalar_gate = scalar_gate;
     return kda::launch_decode(p) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

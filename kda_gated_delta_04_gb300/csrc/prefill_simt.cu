@@ -125,7 +125,8 @@ prefill_simt_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO
                     const float *__restrict__ log_alpha, const float *__restrict__ beta,
                     const int32_t *__restrict__ cu, int64_t total, int H,
                     const float *init_state, IO *__restrict__ o, float *final_state,
-                    uint32_t *status, const int32_t *__restrict__ order, bool scalar_gate)
+                    uint32_t *status, const int32_t *__restrict__ order, bool scalar_gate,
+                    StateSlots slots)
 {
     using Sm = SimtSmem<D, DV>;
     constexpr int LD = Sm::LD, LA = Sm::LA;
@@ -141,10 +142,12 @@ prefill_simt_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO
     const float scale = rsqrtf((float)D);
 
     // state slice S[i][j0 .. j0+DV)
-    const size_t st_off = ((size_t)n * H + h) * D * D;
+    int64_t si, sf;
+    if (!state_entries(slots, n, init_state != nullptr, si, sf) && tid == 0) atomicOr(status, DEV_ERR_SLOT);
+    const size_t head_off = (size_t)h * D * D, st_entry = (size_t)H * D * D;
     for (int e = tid; e < D * DV; e += kThreads) {
         const int i = e / DV, j = e % DV;
-        sm.S[e] = init_state ? init_state[st_off + (size_t)i * D + j0 + j] : 0.f;
+        sm.S[e] = si >= 0 ? init_state[si * st_entry + head_off + (size_t)i * D + j0 + j] : 0.f;
     }
     bool decay_bad = false;
 
@@ -281,9 +284,9 @@ prefill_simt_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO
         }
     }
     __syncthreads();
-    for (int e = tid; e < D * DV; e += kThreads) {
+    for (int e = tid; e < D * DV && sf >= 0; e += kThreads) {
         const int i = e / DV, j = e % DV;
-        final_state[st_off + (size_t)i * D + j0 + j] = sm.S[e];
+        final_state[sf * st_entry + head_off + (size_t)i * D + j0 + j] = sm.S[e];
     }
     if (decay_bad) atomicOr(status, DEV_ERR_DECAY);
 }
@@ -306,7 +309,7 @@ cudaError_t launch_simt(const PrefillProblem &p)
     kern<<<grid, kThreads, smem, p.stream>>>(
         static_cast<const IO *>(p.q), static_cast<const IO *>(p.k), static_cast<const IO *>(p.v),
         p.log_alpha, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.init_state,
-        static_cast<IO *>(p.o), p.final_state, p.status, p.order, p.scalar_gate);
+        static_cast<IO *>(p.o), p.final_state, p.status, p.order, p.scalar_gate, p.slots);
     return cudaGetLastError();
 }
 

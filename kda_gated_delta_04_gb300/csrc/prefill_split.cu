@@ -483,7 +483,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
                      int64_t total, int H, const int32_t *__restrict__ cc,
                      const unsigned char *__restrict__ records, const float *init_state,
                      __nv_bfloat16 *__restrict__ o, float *final_state, uint32_t *status,
-                     const int32_t *__restrict__ order)
+                     const int32_t *__restrict__ order, StateSlots slots)
 {
     using L = StateLayout;
     extern __shared__ unsigned char smem_raw[];
@@ -538,12 +538,14 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     // state row i, columns j0 + 8*part .. +7 in registers; S^T (bf16) operands in O7
     const int i_row = quarter * 32 + lane, jp = part * 8;
     float S[8];
-    const size_t st_off = (((size_t)n * H + h) * kD + i_row) * kD + j0 + jp;
+    int64_t si, sf;
+    if (!state_entries(slots, n, init_state != nullptr, si, sf) && tid == 0) atomicOr(status, DEV_ERR_SLOT);
+    const size_t st_off = ((size_t)h * kD + i_row) * kD + j0 + jp, st_entry = (size_t)H * kD * kD;
     if (state_warp) {
-        if (init_state) {
+        if (si >= 0) {
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
-                const float4 x = *reinterpret_cast<const float4 *>(init_state + st_off + 4 * q);
+                const float4 x = *reinterpret_cast<const float4 *>(init_state + si * st_entry + st_off + 4 * q);
                 S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
             }
         } else {
@@ -723,8 +725,8 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
             (void)mbar_wait_ns(&bar_rec[k & 1], (uint32_t)((k >> 1) & 1), kWaitNs);
         for (int k = v_issued > kVRing ? v_issued - kVRing : 0; k < v_issued; ++k)
             (void)mbar_wait_ns(&bar_v[k % kVRing], (uint32_t)((k / kVRing) & 1), kWaitNs);
-    } else if (state_warp) {
-        float *dst = final_state + st_off;
+    } else if (state_warp && sf >= 0) {
+        float *dst = final_state + sf * st_entry + st_off;
 #pragma unroll
         for (int q = 0; q < 2; ++q)
             *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
@@ -780,7 +782,7 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     return cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, p.cu_seqlens, p.total_tokens, p.num_heads,
                               static_cast<const int32_t *>(cc), static_cast<const unsigned char *>(records),
                               p.init_state, static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.status,
-                              static_cast<const int32_t *>(p.order));
+                              static_cast<const int32_t *>(p.order), p.slots);
 }
 
 }  // namespace kda

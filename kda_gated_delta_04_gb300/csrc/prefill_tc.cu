@@ -91,7 +91,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   const float *__restrict__ beta, const int32_t *__restrict__ cu, int64_t total,
                   int H, const float *init_state, __nv_bfloat16 *__restrict__ o,
                   float *final_state, uint32_t *status, const int32_t *__restrict__ order,
-                  const float *__restrict__ la_scalar)
+                  const float *__restrict__ la_scalar, StateSlots slots)
 {
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar_tma, bar_mma;
@@ -129,11 +129,13 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
     const int i_row = quarter * 32 + lane;
     const int jp = part * 8;
     float S[8];
-    const size_t st_off = (((size_t)n * H + h) * kD + i_row) * kD + j0 + jp;
-    if (init_state) {
+    int64_t si, sf;
+    if (!state_entries(slots, n, init_state != nullptr, si, sf) && tid == 0) atomicOr(status, DEV_ERR_SLOT);
+    const size_t st_off = ((size_t)h * kD + i_row) * kD + j0 + jp, st_entry = (size_t)H * kD * kD;
+    if (si >= 0) {
 #pragma unroll
         for (int q = 0; q < 2; ++q) {
-            const float4 x = *reinterpret_cast<const float4 *>(init_state + st_off + 4 * q);
+            const float4 x = *reinterpret_cast<const float4 *>(init_state + si * st_entry + st_off + 4 * q);
             S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
         }
     } else {
@@ -330,8 +332,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         // drain our own copies and MMAs (bounded) before releasing shared and tensor memory
         if (tma_pending) (void)mbar_wait_ns(&bar_tma, ph_tma, kWaitNs);
         if (mma_pending) (void)mbar_wait_ns(&bar_mma, ph_mma, kWaitNs);
-    } else {
-        float *dst = final_state + st_off;
+    } else if (sf >= 0) {
+        float *dst = final_state + sf * st_entry + st_off;
 #pragma unroll
         for (int q = 0; q < 2; ++q)
             *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
@@ -370,7 +372,7 @@ cudaError_t launch_prefill_tc(const PrefillProblem &p)
     prefill_tc_kernel<<<grid, kThreads, kSmemDyn, p.stream>>>(
         tq, tk, tla, tv, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.init_state,
         static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.status, p.order,
-        p.scalar_gate ? p.log_alpha : nullptr);
+        p.scalar_gate ? p.log_alpha : nullptr, p.slots);
     return cudaGetLastError();
 }
 

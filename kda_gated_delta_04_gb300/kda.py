@@ -46,7 +46,10 @@ EXPORTS = {
     "kda_prefill_ex": (_c.c_int, _PREFILL_ARGS + [_c.c_uint32]),
     "kda_decode_step_ex": (_c.c_int, _DECODE_ARGS + [_c.c_uint32]),
     "kda_decode_step_slots": (_c.c_int, [_VP, _VP, _VP, _VP, _VP, _c.c_int32, _c.c_int32, _c.c_int32,
-                                         _c.c_int32, _c.c_int, _VP, _c.c_int32, _VP, _VP, _VP, _VP]),
+                                         _c.c_int32, _c.c_int, _VP, _c.c_int32, _VP, _VP, _VP, _VP,
+                                         _c.c_uint32]),
+    "kda_prefill_slots": (_c.c_int, _PREFILL_ARGS[:12] + [_VP, _c.c_int32, _VP, _VP, _VP, _VP,
+                                                          _c.c_size_t, _VP, _c.c_uint32]),
 }
 
 
@@ -125,9 +128,17 @@ def kda_prefill_events(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tok
 
 
 def kda_decode_step_slots(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype, state_pool,
-                          num_slots, slots, o, device_errors, stream):
+                          num_slots, slots, o, device_errors, stream, flags):
     return lib().kda_decode_step_slots(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype,
-                                       state_pool, num_slots, slots, o, device_errors, stream)
+                                       state_pool, num_slots, slots, o, device_errors, stream, flags)
+
+
+def kda_prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
+                      d_v, dtype, state_pool, num_slots, init_slots, final_slots, o, workspace,
+                      workspace_bytes, stream, flags):
+    return lib().kda_prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens,
+                                   num_heads, d_k, d_v, dtype, state_pool, num_slots, init_slots,
+                                   final_slots, o, workspace, workspace_bytes, stream, flags)
 
 
 def kda_selftest_bounded_wait(workspace, limit_ns, stream):
@@ -230,22 +241,60 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
     return o, final_state
 
 
+def prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, state_pool, final_slots, init_slots=None, *,
+                  o=None, workspace=None, stream=None, check_status=False, outputs=True):
+    """Prefill into a paged state cache: sequence n starts from state_pool[init_slots[n]]
+    (zero when init_slots is None or the entry is -1) and its final state is written to
+    state_pool[final_slots[n]].  state_pool [S, H, d, d] fp32; slots int32 CUDA tensors [N].
+    Other arguments as prefill.  Returns o (None with outputs=False)."""
+    torch = _torch()
+    T, H, d = q.shape
+    dt = _dtype_code(q)
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    if o is None and outputs:
+        o = torch.empty((T, H, v.shape[2]), dtype=q.dtype, device=q.device)
+    if not outputs:
+        o = None
+    if workspace is None:
+        workspace = workspace_for(N, T, H, d, dt, q.device)
+    flags = KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0
+    st = kda_prefill_slots(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
+                           _ptr(log_alpha, "log_alpha", torch.float32),
+                           _ptr(beta, "beta", torch.float32),
+                           _ptr(cu_seqlens, "cu_seqlens", torch.int32), N, T, H, d, v.shape[2], dt,
+                           _ptr(state_pool, "state_pool", torch.float32), state_pool.shape[0],
+                           _ptr(init_slots, "init_slots", torch.int32),
+                           _ptr(final_slots, "final_slots", torch.int32),
+                           None if o is None else _ptr(o, "o", q.dtype), _ptr(workspace, "workspace"),
+                           workspace.numel() * workspace.element_size(),
+                           _stream_handle(stream, q.device), flags)
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_slots")
+    if check_status:
+        st = kda_read_device_status(workspace.data_ptr(), _stream_handle(stream, q.device))
+        if st != KDA_OK:
+            raise KdaError(st, "kda_prefill_slots (device)")
+    return o
+
+
 def decode_step_slots(q, k, v, log_alpha, beta, state_pool, slots, *, o=None, errors=None,
                       stream=None):
     """One decode step on a paged state cache: state_pool [S, H, d, d] fp32 (updated in
-    place), slots int32 [B] CUDA tensor of distinct slot indices.  Returns o [B, H, d]."""
+    place), slots int32 [B] CUDA tensor of distinct slot indices.  Returns o [B, H, d].
+    A log_alpha of shape [B, H] is the scalar-gate variant."""
     torch = _torch()
     B, H, d = q.shape
     dt = _dtype_code(q)
     if o is None:
         o = torch.empty((B, H, v.shape[2]), dtype=q.dtype, device=q.device)
+    flags = KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0
     st = kda_decode_step_slots(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
                                _ptr(log_alpha, "log_alpha", torch.float32),
                                _ptr(beta, "beta", torch.float32), B, H, d, v.shape[2], dt,
                                _ptr(state_pool, "state_pool", torch.float32), state_pool.shape[0],
                                _ptr(slots, "slots", torch.int32), _ptr(o, "o", q.dtype),
                                None if errors is None else _ptr(errors, "errors", torch.int32),
-                               _stream_handle(stream, q.device))
+                               _stream_handle(stream, q.device), flags)
     if st != KDA_OK:
         raise KdaError(st, "kda_decode_step_slots")
     return o

@@ -110,3 +110,18 @@ def test_unknown_flags_are_rejected_on_host(kda):
     a = _prefill_args()
     assert kda.kda_prefill_ex(*a.values(), 1 << 7) == 1
     assert kda.kda_decode_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 128, 0, FAKE, FAKE, None, 4) == 1
+
+
+def test_slot_calls_reject_bad_arguments_on_host(kda):
+    head = list(_prefill_args().values())[:12]
+
+    def prefill_slots(pool=FAKE, num_slots=4, init_slots=None, final_slots=FAKE, flags=1):
+        return kda.kda_prefill_slots(*head, pool, num_slots, init_slots, final_slots, FAKE, FAKE,
+                                     1 << 16, None, flags)
+    assert prefill_slots(pool=None) == 1
+    assert prefill_slots(final_slots=None) == 1
+    assert prefill_slots(num_slots=-1) == 1
+    assert prefill_slots(init_slots=FAKE + 2) == 1      # misaligned
+    assert prefill_slots(flags=8) == 1                  # unknown flag
+    dec = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 128, 0, FAKE, 8, FAKE, FAKE, None, None]
+    assert kda.kda_decode_step_slots(*dec, 2) == 1      # unknown flag

@@ -9,9 +9,10 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 from kda_gated_delta_04_gb300 import kda, synth
 from kda_gated_delta_04_gb300.synth import PrefillWorkload
-from parity_util import assert_parity, gpu_prefill, oracle_prefill, relF, to_device
+from parity_util import TOL, assert_parity, gpu_prefill, maxabs, oracle_prefill, relF, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -307,3 +308,88 @@ def test_scalar_gate_variant(case):
     ref["log_alpha"] = la_full
     o_ref, fs_ref = oracle_prefill(ref)
     assert_parity(synth.to_f64(o_s), synth.to_f64(fs_s), o_ref, fs_ref, dtype, "scalar gate " + case)
+
+
+@pytest.mark.parametrize("case", ["two_kernel", "single_kernel", "fp32_d64"])
+def test_prefill_into_a_state_pool_then_decode_from_it(case):
+    """kda_prefill_slots on a pool of 9 states: sequence 0 continues from its slot in place,
+    sequence 1 starts from zero, sequences 2 and 3 move from one slot to another.  The outputs
+    and final states are bit for bit those of kda_prefill on the gathered states, slots that no
+    sequence writes are untouched, and one decode step on the pool continues every sequence
+    within the bar of the oracle."""
+    dtype, d = ("f32", 64) if case == "fp32_d64" else ("bf16", 128)
+    H = 2
+    w = PrefillWorkload("pool_" + case, 124, H, d, dtype, (130, 64, 0, 97), 4, init_state=True)
+    inp = synth.prefill_inputs(w)
+    init_h, final_h = [3, -1, 5, 7], [3, 2, 6, 0]
+    pool = torch.zeros((9, H, d, d), dtype=torch.float32)
+    for s in range(9):
+        pool[s] = 0.01 * (s + 1)
+    for n, s in enumerate(init_h):
+        if s >= 0:
+            pool[s] = inp["init_state"][n]
+    init_dense = inp["init_state"].clone()
+    init_dense[1] = 0.0
+    pool_before = pool.clone()
+    dev = to_device(inp)
+    pool_d = pool.cuda()
+    ws = None
+    if case == "single_kernel":
+        ws = torch.empty(kda.min_workspace_bytes(4), dtype=torch.uint8, device="cuda")
+    i_slots = torch.tensor(init_h, dtype=torch.int32, device="cuda")
+    f_slots = torch.tensor(final_h, dtype=torch.int32, device="cuda")
+    o_pool = kda.prefill_slots(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"],
+                               dev["cu_seqlens"], pool_d, f_slots, i_slots, workspace=ws,
+                               check_status=True)
+    o_dense, fs_dense = kda.prefill(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"],
+                                    dev["cu_seqlens"], init_dense.cuda(), workspace=ws, check_status=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(synth.to_f64(o_pool), synth.to_f64(o_dense))
+    np.testing.assert_array_equal(synth.to_f64(pool_d[final_h].cpu()), synth.to_f64(fs_dense.cpu()))
+    for s in (1, 4, 8):  # read by nobody (slot 5 and 7 are read, not written) or untouched
+        assert torch.equal(pool_d[s].cpu(), pool_before[s])
+    for s in (5, 7):
+        assert torch.equal(pool_d[s].cpu(), pool_before[s])
+    # the oracle on the same problem (sequence 1 from zero)
+    ref = dict(inp)
+    ref["init_state"] = init_dense
+    o_ref, fs_ref = oracle_prefill(ref)
+    assert_parity(synth.to_f64(o_pool), synth.to_f64(pool_d[final_h].cpu()), o_ref, fs_ref, dtype,
+                  "prefill into a pool " + case)
+    # decode continues each sequence from its final slot
+    g = torch.Generator().manual_seed(125)
+    io = torch.float32 if dtype == "f32" else torch.bfloat16
+    x = {
+        "q": torch.nn.functional.normalize(torch.randn(4, H, d, generator=g), dim=-1).to(io),
+        "k": torch.nn.functional.normalize(torch.randn(4, H, d, generator=g), dim=-1).to(io),
+        "v": torch.randn(4, H, d, generator=g).to(io),
+        "log_alpha": (-0.05 * torch.nn.functional.softplus(torch.randn(4, H, d, generator=g))).float(),
+        "beta": torch.sigmoid(torch.randn(4, H, generator=g)).float(),
+    }
+    o_dec = kda.decode_step_slots(*(x[k].cuda() for k in ("q", "k", "v", "log_alpha", "beta")),
+                                  pool_d, f_slots)
+    torch.cuda.synchronize()
+    r = {k: synth.to_f64(t) for k, t in x.items()}
+    od_ref, _ = oracle.decode_step(r["q"], r["k"], r["v"], r["log_alpha"], r["beta"], fs_ref.copy())
+    assert maxabs(synth.to_f64(o_dec), od_ref) <= TOL[dtype]["o"]
+
+
+def test_prefill_into_a_pool_reports_a_bad_slot_and_runs_the_rest():
+    """A final slot out of range: KDA_DEVICE_ERR_SLOT is reported (KDA_ERR_INVALID_ARG), that
+    sequence's state is written nowhere, and the other sequences are unaffected."""
+    w = PrefillWorkload("pool_bad_slot", 126, 2, 128, "bf16", (70, 40), 2)
+    inp = synth.prefill_inputs(w)
+    dev = to_device(inp)
+    pool_d = torch.full((4, 2, 128, 128), 5.0, dtype=torch.float32, device="cuda")
+    f_slots = torch.tensor([1, 4], dtype=torch.int32, device="cuda")  # 4 is out of range
+    ws = kda.workspace_for(2, 110, 2, 128, kda.KDA_DTYPE_BF16, torch.device("cuda"))
+    kda.prefill_slots(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"], dev["cu_seqlens"],
+                      pool_d, f_slots, workspace=ws)
+    st = kda.kda_read_device_status(ws.data_ptr(), kda._stream_handle(None, ws.device))
+    assert st == kda.KDA_ERR_INVALID_ARG
+    _, fs = kda.prefill(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"], dev["cu_seqlens"],
+                        check_status=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(synth.to_f64(pool_d[1].cpu()), synth.to_f64(fs[0].cpu()))
+    for s in (0, 2, 3):
+        assert bool((pool_d[s] == 5.0).all())
