@@ -171,6 +171,14 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
  *                        gate channel-wise).  Its chunk-prefix bound is the same.
  */
 #define KDA_FLAG_SCALAR_GATE 1u
+/*  KDA_FLAG_QK_L2NORM    q and k are raw (the layer's activations before their L2
+ *                        normalisation): the kernels normalise every q and k row over
+ *                        d_k in fp32, x / max(||x||_2, 1e-12), before the recurrence
+ *                        ("K3 attention, three-piece set", KDA engineering notes: q and
+ *                        k pass a short causal convolution and then L2 normalisation;
+ *                        "From 124M to 2.8T", chapter 3 code: the normalisation over the
+ *                        channel axis).  The 1/sqrt(d_k) output scale is unchanged. */
+#define KDA_FLAG_QK_L2NORM 2u
 
 /* kda_prefill with options (flags above); flags = 0 is kda_prefill. */
 kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, const float *log_alpha,

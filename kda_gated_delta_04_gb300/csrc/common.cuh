@@ -20,6 +20,7 @@ enum : uint32_t {
 
 constexpr int kChunk = KDA_CHUNK;
 constexpr size_t kWorkspaceHeader = 256;  // status word, padded
+constexpr float kQkNormEps = 1e-12f;       // floor of the q / k row norm (KDA_FLAG_QK_L2NORM)
 
 // Everything a prefill launch needs, already validated on the host.
 // Where each sequence's states live.  Dense (fin == null): entry n of init_state and of
@@ -47,6 +48,7 @@ struct PrefillProblem {
     void *records;              // workspace: per chunk-head records of the two-kernel path, or null
     bool scalar_gate = false;   // log_alpha is [T, H]: one decay per token-head for every key channel
     StateSlots slots;           // state pool indices, or none (dense states)
+    bool qk_l2norm = false;     // q, k rows are normalised in the kernels
     cudaStream_t stream;
 };
 
@@ -64,6 +66,7 @@ struct DecodeProblem {
     int num_slots = 0;
     uint32_t *errors = nullptr;
     bool scalar_gate = false;   // log_alpha is [B, H]: one decay per sequence-head for every key channel
+    bool qk_l2norm = false;     // q, k rows are normalised in the kernel
 };
 
 // Launchers (each returns the launch error, cudaSuccess when enqueued).

@@ -27,7 +27,7 @@ __global__ void __launch_bounds__(256, 2)
 decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
               const float *__restrict__ log_alpha, const float *__restrict__ beta,
               float *__restrict__ state, IO *__restrict__ o, const int32_t *__restrict__ slots,
-              int H, int num_slots, uint32_t *errors, bool scalar_gate)
+              int H, int num_slots, uint32_t *errors, bool scalar_gate, bool qk_norm)
 {
     constexpr int TPR = D / 4;      // threads per state row
     constexpr int RPP = 256 / TPR;  // rows per pass
@@ -78,14 +78,22 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
 
     if (tid < D) {
         const int j = tid;
-        float sk = 0.f, sq = 0.f, kq = 0.f;
+        float sk = 0.f, sq = 0.f, kq = 0.f, kk = 0.f, qq = 0.f;
 #pragma unroll
         for (int r = 0; r < RPP; ++r) { sk += s_rk[r][j]; sq += s_rq[r][j]; }
         for (int i = 0; i < D; ++i) kq += s_k[i] * s_q[i];
+        // raw q, k (qk_norm): every term is linear in q and in k, so the reciprocal norms
+        // scale the reductions instead of the vectors (no extra barrier)
+        float nk = 1.f, nq = 1.f;
+        if (qk_norm) {
+            for (int i = 0; i < D; ++i) { kk += s_k[i] * s_k[i]; qq += s_q[i] * s_q[i]; }
+            nk = 1.f / fmaxf(sqrtf(kk), kQkNormEps);
+            nq = 1.f / fmaxf(sqrtf(qq), kQkNormEps);
+        }
         const float scale = rsqrtf((float)D);
-        const float d = beta[unit] * (load_io(v + (size_t)unit * D + j) - sk);
-        s_d[j] = d;
-        store_io(o + (size_t)unit * D + j, scale * (sq + kq * d));
+        const float d = beta[unit] * (load_io(v + (size_t)unit * D + j) - sk * nk);
+        s_d[j] = d * nk;  // the write k^ d^T = k (nk d)^T
+        store_io(o + (size_t)unit * D + j, scale * (sq * nq + kq * (nk * nq) * d));
     }
     __syncthreads();
 
@@ -106,7 +114,7 @@ cudaError_t launch(const DecodeProblem &p)
     decode_kernel<D, IO><<<units, 256, 0, p.stream>>>(
         static_cast<const IO *>(p.q), static_cast<const IO *>(p.k), static_cast<const IO *>(p.v),
         p.log_alpha, p.beta, p.state, static_cast<IO *>(p.o), p.slots, p.num_heads, p.num_slots, p.errors,
-        p.scalar_gate);
+        p.scalar_gate, p.qk_l2norm);
     return cudaGetLastError();
 }
 

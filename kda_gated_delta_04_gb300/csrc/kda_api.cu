@@ -61,6 +61,9 @@ kda_status_t check_shape(int32_t d_k, int32_t d_v, kda_dtype_t dtype)
 
 }  // namespace
 
+// every option bit of the _ex / _slots calls
+constexpr uint32_t kKnownFlags = KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM;
+
 extern "C" {
 
 size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
@@ -82,7 +85,7 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
                           void *workspace, size_t workspace_bytes, void *stream, const cudaEvent_t *ev,
                           uint32_t flags, const kda::StateSlots *slots = nullptr)
 {
-    if (flags & ~(uint32_t)KDA_FLAG_SCALAR_GATE) return KDA_ERR_INVALID_ARG;
+    if (flags & ~kKnownFlags) return KDA_ERR_INVALID_ARG;
     const bool scalar_gate = (flags & KDA_FLAG_SCALAR_GATE) != 0;
     kda_status_t st = check_shape(d_k, d_v, dtype);
     if (st != KDA_OK) return st;
@@ -113,6 +116,7 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     p.num_heads = num_heads; p.d = d_k; p.dtype = dtype; p.init_state = init_state;
     p.o = o; p.final_state = final_state;
     p.scalar_gate = scalar_gate;
+    p.qk_l2norm = (flags & KDA_FLAG_QK_L2NORM) != 0;
     if (slots) p.slots = *slots;
     p.status = static_cast<uint32_t *>(workspace);
     char *ws = static_cast<char *>(workspace);
@@ -206,7 +210,7 @@ kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, 
                                    const int32_t *slots, void *o, uint32_t *device_errors, void *stream,
                                    uint32_t flags)
 {
-    if (flags & ~(uint32_t)KDA_FLAG_SCALAR_GATE) return KDA_ERR_INVALID_ARG;
+    if (flags & ~kKnownFlags) return KDA_ERR_INVALID_ARG;
     const bool scalar_gate = (flags & KDA_FLAG_SCALAR_GATE) != 0;
     kda_status_t st = check_shape(d_k, d_v, dtype);
     if (st != KDA_OK) return st;
@@ -227,6 +231,7 @@ kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, 
     p.state = state_pool; p.o = o; p.stream = static_cast<cudaStream_t>(stream);
     p.slots = slots; p.num_slots = num_slots; p.errors = device_errors;
     p.scalar_gate = scalar_gate;
+    p.qk_l2norm = (flags & KDA_FLAG_QK_L2NORM) != 0;
     return kda::launch_decode(p) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 
@@ -235,7 +240,7 @@ kda_status_t kda_decode_step_ex(const void *q, const void *k, const void *v, con
                                 int32_t d_v, kda_dtype_t dtype, float *state, void *o, void *stream,
                                 uint32_t flags)
 {
-    if (flags & ~(uint32_t)KDA_FLAG_SCALAR_GATE) return KDA_ERR_INVALID_ARG;
+    if (flags & ~kKnownFlags) return KDA_ERR_INVALID_ARG;
     const bool scalar_gate = (flags & KDA_FLAG_SCALAR_GATE) != 0;
     kda_status_t st = check_shape(d_k, d_v, dtype);
     if (st != KDA_OK) return st;
@@ -253,6 +258,7 @@ kda_status_t kda_decode_step_ex(const void *q, const void *k, const void *v, con
     p.batch = batch; p.num_heads = num_heads; p.d = d_k; p.dtype = dtype;
     p.state = state; p.o = o; p.stream = static_cast<cudaStream_t>(stream);
     p.scalar_gate = scalar_gate;
+    p.qk_l2norm = (flags & KDA_FLAG_QK_L2NORM) != 0;
     return kda::launch_decode(p) == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }
 

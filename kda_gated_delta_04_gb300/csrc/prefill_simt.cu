@@ -126,7 +126,7 @@ prefill_simt_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO
                     const int32_t *__restrict__ cu, int64_t total, int H,
                     const float *init_state, IO *__restrict__ o, float *final_state,
                     uint32_t *status, const int32_t *__restrict__ order, bool scalar_gate,
-                    StateSlots slots)
+                    StateSlots slots, bool qk_norm)
 {
     using Sm = SimtSmem<D, DV>;
     constexpr int LD = Sm::LD, LA = Sm::LA;
@@ -181,6 +181,21 @@ prefill_simt_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO
         }
         if (tid < kChunk) sm.beta[tid] = tid < len ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
         __syncthreads();
+
+        // ---- q / k L2 normalisation, in place in fp32 (one warp per row); nothing below
+        // reads q or k before the barrier after a1
+        if (qk_norm) {
+            const int warp = tid >> 5, lane = tid & 31;
+            for (int row = warp; row < 2 * kChunk; row += kThreads / 32) {
+                float *x = row < kChunk ? &sm.q[row * LD] : &sm.k[(row - kChunk) * LD];
+                float ss = 0.f;
+                for (int i = lane; i < D; i += 32) ss += x[i] * x[i];
+#pragma unroll
+                for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+                const float inv = 1.f / fmaxf(sqrtf(ss), kQkNormEps);
+                for (int i = lane; i < D; i += 32) x[i] *= inv;
+            }
+        }
 
         // ---- a1: in-chunk cumulative log-decay per channel
         if (tid < D) {
@@ -309,7 +324,7 @@ cudaError_t launch_simt(const PrefillProblem &p)
     kern<<<grid, kThreads, smem, p.stream>>>(
         static_cast<const IO *>(p.q), static_cast<const IO *>(p.k), static_cast<const IO *>(p.v),
         p.log_alpha, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.init_state,
-        static_cast<IO *>(p.o), p.final_state, p.status, p.order, p.scalar_gate, p.slots);
+        static_cast<IO *>(p.o), p.final_state, p.status, p.order, p.scalar_gate, p.slots, p.qk_l2norm);
     return cudaGetLastError();
 }
 

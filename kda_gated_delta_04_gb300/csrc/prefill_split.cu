@@ -119,9 +119,9 @@ __device__ __forceinline__ void write_tprime_hilo(unsigned char *sm, const float
 
 // Kd^T = (k e^{g_last - g})^T as bf16 high and low parts, K-major [i][s] at KDH
 // and KDL.  Thread = (channel pair cp, row group rg) as in decayed_operands.
-template <class L, int NT>
+template <class L, int NT, bool NORM>
 __device__ __forceinline__ void build_kd(unsigned char *sm, int len, const float2 (&gl)[4096 / NT],
-                                         float2 off, float2 tot)
+                                         float2 off, float2 tot, const float *rn)
 {
     constexpr int R = 4096 / NT;
     static_assert(R % 8 == 0, "row groups cover whole 8-column chunks");
@@ -135,7 +135,11 @@ __device__ __forceinline__ void build_kd(unsigned char *sm, int len, const float
             const int rr = r8 + u, r = rg * R + rr;
             const bool valid = r < len;
             const uint32_t kraw = valid ? *reinterpret_cast<const uint32_t *>(sm + L::IN_K + (r * kD + 2 * cp) * 2) : 0u;
-            const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kraw));
+            float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kraw));
+            if (NORM) {  // normalised k (KDA_FLAG_QK_L2NORM)
+                kv.x *= rn[r];
+                kv.y *= rn[r];
+            }
             const float dx = kv.x * __expf(tot.x - (off.x + gl[rr].x));
             const float dy = kv.y * __expf(tot.y - (off.y + gl[rr].y));
             hx[u] = __bfloat162float(__float2bfloat16_rn(dx));
@@ -292,6 +296,8 @@ __device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, un
     }
 }
 
+// NORM: q and k arrive raw and are L2-normalised here (KDA_FLAG_QK_L2NORM).
+template <bool NORM>
 __global__ void __launch_bounds__(kChunkThreads, 2)
 prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const float *__restrict__ log_alpha, const float *__restrict__ beta,
@@ -305,6 +311,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     __shared__ __align__(8) uint64_t bar_tma, bar_mma, bar_p, bar_drain;
     __shared__ uint32_t tmem_holder;
     __shared__ __align__(16) float s_beta[kC];
+    __shared__ float s_rn[2 * kC];  // reciprocal k, q row norms (NORM)
 
     // launched with programmatic stream serialization behind the schedule kernel:
     // nothing that kernel writes (cc, the status word) is touched before pdl_wait
@@ -361,9 +368,14 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         bool ok = mbar_wait_ns(&bar_tma, 0, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tma_pending = false;
+        if (NORM) {
+            qk_row_inv_norms<NT>(sm + L::IN_K, sm + L::IN_Q, s_rn);
+            __syncthreads();
+        }
         float2 ot[2];
-        decay_bad = decayed_operands<L, NT, false>(sm, len, s_tot, nullptr,
-                                                   reinterpret_cast<float *>(rec + R_GM), gl, gmin, gmax, ot);
+        decay_bad = decayed_operands<L, NT, false, NORM>(sm, len, s_tot, nullptr,
+                                                   reinterpret_cast<float *>(rec + R_GM), gl, gmin, gmax, ot,
+                                                   s_rn);
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
@@ -386,7 +398,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             issue_w_p2<L>(sb, tmem, with_o);
             mma_commit(&bar_mma);
         }
-        build_kd<L, NT>(sm, len, gl, ot[0], ot[1]);  // over the solve scratch, overlapping W and P2
+        build_kd<L, NT, NORM>(sm, len, gl, ot[0], ot[1], s_rn);  // over the solve scratch, overlapping W and P2
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
@@ -746,8 +758,9 @@ size_t prefill_split_records_bytes(int64_t total_tokens, int num_seqs, int num_h
 
 cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records, cudaEvent_t mid)
 {
-    static int dev_chunk = -1, dev_state = -1;
-    cudaError_t err = allow_smem(prefill_chunk_kernel, (int)kChunkSmem, &dev_chunk);
+    static int dev_chunk = -1, dev_chunk_norm = -1, dev_state = -1;
+    auto chunk_kernel = p.qk_l2norm ? prefill_chunk_kernel<true> : prefill_chunk_kernel<false>;
+    cudaError_t err = allow_smem(chunk_kernel, (int)kChunkSmem, p.qk_l2norm ? &dev_chunk_norm : &dev_chunk);
     if (err != cudaSuccess) return err;
     err = allow_smem(prefill_state_kernel, (int)kStateSmem, &dev_state);
     if (err != cudaSuccess) return err;
@@ -770,7 +783,7 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     cfg.stream = p.stream;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, prefill_chunk_kernel, tq, tk, p.log_alpha, p.beta, p.cu_seqlens,
+    err = cudaLaunchKernelEx(&cfg, chunk_kernel, tq, tk, p.log_alpha, p.beta, p.cu_seqlens,
                              p.total_tokens, p.num_heads, p.num_seqs, (int)chunk_bound, cc,
                              static_cast<unsigned char *>(records), p.status, p.o != nullptr,
                              p.scalar_gate);

@@ -91,13 +91,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
                   const float *__restrict__ beta, const int32_t *__restrict__ cu, int64_t total,
                   int H, const float *init_state, __nv_bfloat16 *__restrict__ o,
                   float *final_state, uint32_t *status, const int32_t *__restrict__ order,
-                  const float *__restrict__ la_scalar, StateSlots slots)
+                  const float *__restrict__ la_scalar, StateSlots slots, bool qk_norm)
 {
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar_tma, bar_mma;
     __shared__ uint32_t tmem_holder;
     __shared__ __align__(16) float s_beta[kC];
     __shared__ __align__(8) float s_gam[kD];
+    __shared__ float s_rn[2 * kC];  // reciprocal k, q row norms (qk_norm)
 
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
@@ -169,6 +170,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         ph_tma ^= 1;
         tma_pending = false;
+        if (qk_norm) qk_row_inv_norms<kThreads>(sm + L::IN_K, sm + L::IN_Q, s_rn);  // read after the barrier below
 
         // ---------------------------------------------------------- a1, a2
         float2 gl[8];
@@ -192,7 +194,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constan
             *reinterpret_cast<float4 *>(sm + L::O6 + km32(j, s4, kDV)) = make_float4(x[0], x[1], x[2], x[3]);
         }
         __syncthreads();
-        if (decayed_operands<L, kThreads>(sm, len, s_tot, sm + L::O3, s_gam, gl, gmin, gmax)) decay_bad = true;
+        if (decayed_operands<L, kThreads, true, true>(sm, len, s_tot, sm + L::O3, s_gam, gl, gmin, gmax,
+                                                      nullptr, qk_norm ? s_rn : nullptr))
+            decay_bad = true;
         fence_proxy_async_smem();
         __syncthreads();
 
@@ -372,7 +376,7 @@ cudaError_t launch_prefill_tc(const PrefillProblem &p)
     prefill_tc_kernel<<<grid, kThreads, kSmemDyn, p.stream>>>(
         tq, tk, tla, tv, p.beta, p.cu_seqlens, p.total_tokens, p.num_heads, p.init_state,
         static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.status, p.order,
-        p.scalar_gate ? p.log_alpha : nullptr, p.slots);
+        p.scalar_gate ? p.log_alpha : nullptr, p.slots, p.qk_l2norm);
     return cudaGetLastError();
 }
 

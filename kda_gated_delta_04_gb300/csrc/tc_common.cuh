@@ -123,17 +123,41 @@ __device__ __forceinline__ void prefix_scan(const float *la, int la_stride, int 
     *reinterpret_cast<float2 *>(&s_tot[rg * kD + 2 * cp]) = g;
 }
 
+// ---------------------------------------------------------------- q/k L2 normalisation
+// Reciprocal row norms of the chunk's raw q and k boxes (bf16 [64][128], row-major):
+// rn[r] = 1 / max(|k_r|_2, eps) and rn[64 + r] the same for q_r.  The operand builders
+// scale the raw values by them in fp32, so the normalised q, k are never rounded on
+// their own.  One warp per row; each lane sums four channels.
+template <int NT>
+__device__ __forceinline__ void qk_row_inv_norms(const unsigned char *k_box, const unsigned char *q_box,
+                                                 float *rn)
+{
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int row = warp; row < 2 * kC; row += NT / 32) {
+        const unsigned char *box = row < kC ? k_box : q_box;
+        const uint2 raw = *reinterpret_cast<const uint2 *>(box + ((row & (kC - 1)) * kD + 4 * lane) * 2);
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+        float ss = a.x * a.x + a.y * a.y + b.x * b.x + b.y * b.y;
+#pragma unroll
+        for (int m = 16; m; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
+        if (lane == 0) rn[row] = 1.f / fmaxf(sqrtf(ss), kQkNormEps);
+    }
+}
+
 // ---------------------------------------------------------------- a2: operands
 // After a barrier following prefix_scan: Kg = k e^g and Qg = scale q e^g into
 // O1, Ki = k e^-g into O2 (bf16) and, when KI_T, into o3 (tf32, transposed,
 // K-major 128 rows x 64), e^{g_last} into gam[128].  When off_tot is given it
 // receives this thread's group offset and the chunk total of g for its channel
-// pair.  Returns true when the in-chunk cumulative decay left the supported range.
-template <class L, int NT, bool KI_T = true>
+// pair.  With NORM and rn (qk_row_inv_norms, after a barrier) q and k rows are normalised
+// first; without NORM rn is ignored and the code is the plain operand build.
+// Returns true when the in-chunk cumulative decay left the supported range.
+template <class L, int NT, bool KI_T = true, bool NORM = false>
 __device__ __forceinline__ bool decayed_operands(unsigned char *sm, int len, const float *s_tot,
                                                  unsigned char *o3, float *gam,
                                                  const float2 (&gl)[4096 / NT], float gmin, float gmax,
-                                                 float2 *off_tot = nullptr)
+                                                 float2 *off_tot = nullptr, const float *rn = nullptr)
 {
     constexpr int R = 4096 / NT, G = NT / 64;
     const int tid = threadIdx.x, lane = tid & 31, cp = tid & 63, rg = tid >> 6;
@@ -174,8 +198,13 @@ __device__ __forceinline__ bool decayed_operands(unsigned char *sm, int len, con
             const float ix = __expf(-gx), iy = __expf(-gy);
             const uint32_t qraw = valid ? *reinterpret_cast<const uint32_t *>(sm + L::IN_Q + (r * kD + 2 * cp) * 2) : 0u;
             const uint32_t kraw = valid ? *reinterpret_cast<const uint32_t *>(sm + L::IN_K + (r * kD + 2 * cp) * 2) : 0u;
-            const float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qraw));
-            const float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kraw));
+            float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qraw));
+            float2 kv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&kraw));
+            if (NORM && rn) {
+                const float kn = rn[r], qn = rn[kC + r];
+                kv.x *= kn; kv.y *= kn;
+                qv.x *= qn; qv.y *= qn;
+            }
             const uint32_t sw = (pchunk ^ (uint32_t)(rr & 7)) << 4;  // (r & 7) == (rr & 7)
             *reinterpret_cast<uint32_t *>(sm + L::O1 + pbase1 + r * 128 + sw) = pack_bf16x2(kv.x * ex, kv.y * ey);
             *reinterpret_cast<uint32_t *>(sm + L::O1 + pbase1 + (64 + r) * 128 + sw) =

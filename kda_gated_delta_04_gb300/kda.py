@@ -22,6 +22,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT,
     KDA_ERR_DECAY_RANGE, KDA_ERR_VALUE_RANGE = range(7)
 KDA_DTYPE_BF16, KDA_DTYPE_F32 = 0, 1
 KDA_FLAG_SCALAR_GATE = 1
+KDA_FLAG_QK_L2NORM = 2
 CHUNK = 64
 
 _lib = None
@@ -185,6 +186,12 @@ def _ptr(t, name, dtype=None):
     return t.data_ptr()
 
 
+def _flags(log_alpha, qk_l2norm):
+    """Option bits: a log_alpha without a channel axis is the scalar gate."""
+    return ((KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0) |
+            (KDA_FLAG_QK_L2NORM if qk_l2norm else 0))
+
+
 def _stream_handle(stream, device):
     torch = _torch()
     s = stream if stream is not None else torch.cuda.current_stream(device)
@@ -205,12 +212,14 @@ def min_workspace_bytes(num_seqs):
 
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=None,
-            final_state=None, workspace=None, stream=None, check_status=False, outputs=True):
+            final_state=None, workspace=None, stream=None, check_status=False, outputs=True,
+            qk_l2norm=False):
     """KDA prefill over packed sequences.  q, k: [T, H, d]; v: [T, H, d]; log_alpha: [T, H, d]
     fp32; beta: [T, H] fp32; cu_seqlens: int32 [N+1] CUDA tensor or None (one sequence);
     init_state: [N, H, d, d] fp32 or None.  Returns (o, final_state); with outputs=False
     only the final states are computed and o is None.  A log_alpha of shape [T, H] is the
-    scalar-gate (Gated DeltaNet) variant: one decay per token-head for every key channel."""
+    scalar-gate (Gated DeltaNet) variant: one decay per token-head for every key channel.
+    qk_l2norm=True: q and k are raw and the kernels L2-normalise their rows."""
     torch = _torch()
     T, H, d = q.shape
     dt = _dtype_code(q)
@@ -223,7 +232,7 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
         final_state = torch.empty((N, H, d, v.shape[2]), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = workspace_for(N, T, H, d, dt, q.device)
-    flags = KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0
+    flags = _flags(log_alpha, qk_l2norm)
     st = kda_prefill_ex(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
                      _ptr(log_alpha, "log_alpha", torch.float32), _ptr(beta, "beta", torch.float32),
                      _ptr(cu_seqlens, "cu_seqlens", torch.int32), N, T, H, d, v.shape[2], dt,
@@ -242,7 +251,8 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
 
 
 def prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, state_pool, final_slots, init_slots=None, *,
-                  o=None, workspace=None, stream=None, check_status=False, outputs=True):
+                  o=None, workspace=None, stream=None, check_status=False, outputs=True,
+                  qk_l2norm=False):
     """Prefill into a paged state cache: sequence n starts from state_pool[init_slots[n]]
     (zero when init_slots is None or the entry is -1) and its final state is written to
     state_pool[final_slots[n]].  state_pool [S, H, d, d] fp32; slots int32 CUDA tensors [N].
@@ -257,7 +267,7 @@ def prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, state_pool, final_slots,
         o = None
     if workspace is None:
         workspace = workspace_for(N, T, H, d, dt, q.device)
-    flags = KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0
+    flags = _flags(log_alpha, qk_l2norm)
     st = kda_prefill_slots(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
                            _ptr(log_alpha, "log_alpha", torch.float32),
                            _ptr(beta, "beta", torch.float32),
@@ -278,7 +288,7 @@ def prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, state_pool, final_slots,
 
 
 def decode_step_slots(q, k, v, log_alpha, beta, state_pool, slots, *, o=None, errors=None,
-                      stream=None):
+                      stream=None, qk_l2norm=False):
     """One decode step on a paged state cache: state_pool [S, H, d, d] fp32 (updated in
     place), slots int32 [B] CUDA tensor of distinct slot indices.  Returns o [B, H, d].
     A log_alpha of shape [B, H] is the scalar-gate variant."""
@@ -287,7 +297,7 @@ def decode_step_slots(q, k, v, log_alpha, beta, state_pool, slots, *, o=None, er
     dt = _dtype_code(q)
     if o is None:
         o = torch.empty((B, H, v.shape[2]), dtype=q.dtype, device=q.device)
-    flags = KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0
+    flags = _flags(log_alpha, qk_l2norm)
     st = kda_decode_step_slots(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
                                _ptr(log_alpha, "log_alpha", torch.float32),
                                _ptr(beta, "beta", torch.float32), B, H, d, v.shape[2], dt,
@@ -300,7 +310,7 @@ def decode_step_slots(q, k, v, log_alpha, beta, state_pool, slots, *, o=None, er
     return o
 
 
-def decode_step(q, k, v, log_alpha, beta, state, *, o=None, stream=None):
+def decode_step(q, k, v, log_alpha, beta, state, *, o=None, stream=None, qk_l2norm=False):
     """One decode step; state [B, H, d, d] fp32 is updated in place.  Returns o [B, H, d].
     A log_alpha of shape [B, H] is the scalar-gate variant."""
     torch = _torch()
@@ -308,7 +318,7 @@ def decode_step(q, k, v, log_alpha, beta, state, *, o=None, stream=None):
     dt = _dtype_code(q)
     if o is None:
         o = torch.empty((B, H, v.shape[2]), dtype=q.dtype, device=q.device)
-    flags = KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0
+    flags = _flags(log_alpha, qk_l2norm)
     st = kda_decode_step_ex(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
                             _ptr(log_alpha, "log_alpha", torch.float32),
                             _ptr(beta, "beta", torch.float32), B, H, d, v.shape[2], dt,

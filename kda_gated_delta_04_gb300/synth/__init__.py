@@ -120,6 +120,7 @@ class PrefillWorkload:
     num_seqs: int
     varlen_range: tuple | None = None
     init_state: bool = False
+    raw_qk: bool = False     # q, k as raw N(0, 1) rows (not unit rows), for in-kernel normalisation
 
     def lengths(self, seed: int = 0) -> np.ndarray:
         if self.seq_lens is not None:
@@ -137,6 +138,7 @@ class DecodeWorkload:
     d: int
     dtype: str
     steps: int
+    raw_qk: bool = False     # q, k as raw N(0, 1) rows (not unit rows)
 
 
 TINY = PrefillWorkload("tiny_f32_T256_H2_d64", 10, 2, 64, "f32", (256,), 1)
@@ -192,8 +194,9 @@ def prefill_inputs(w: PrefillWorkload, seed: int = 0, heads=None, seqs=None):
                     dst.copy_(val.reshape(dst.shape))
                 else:
                     dst[:, hsel].copy_(val.reshape(dst[:, hsel].shape))
-            put("q", _qkv_rows(w.dtype, UNIT_ROWS, key[T_Q], row0, step, nrows, D))
-            put("k", _qkv_rows(w.dtype, UNIT_ROWS, key[T_K], row0, step, nrows, D))
+            qk_kind = NORMAL if w.raw_qk else UNIT_ROWS
+            put("q", _qkv_rows(w.dtype, qk_kind, key[T_Q], row0, step, nrows, D))
+            put("k", _qkv_rows(w.dtype, qk_kind, key[T_K], row0, step, nrows, D))
             put("v", _qkv_rows(w.dtype, NORMAL, key[T_V], row0, step, nrows, D))
             put("log_alpha", torch.from_numpy(
                 rows(NEG_SOFTPLUS, key[T_LOG_ALPHA], row0, step, nrows, D, scale=0.05)))
@@ -244,8 +247,9 @@ def decode_inputs(w: DecodeWorkload, step: int, seed: int = 0, batch=None):
     for sel, row0, nrows in spans:
         def put(name, val):
             out[name][sel].copy_(val.reshape(out[name][sel].shape))
-        put("q", _qkv_rows(w.dtype, UNIT_ROWS, key[T_Q], row0, 1, nrows, D))
-        put("k", _qkv_rows(w.dtype, UNIT_ROWS, key[T_K], row0, 1, nrows, D))
+        qk_kind = NORMAL if w.raw_qk else UNIT_ROWS
+        put("q", _qkv_rows(w.dtype, qk_kind, key[T_Q], row0, 1, nrows, D))
+        put("k", _qkv_rows(w.dtype, qk_kind, key[T_K], row0, 1, nrows, D))
         put("v", _qkv_rows(w.dtype, NORMAL, key[T_V], row0, 1, nrows, D))
         put("log_alpha", torch.from_numpy(rows(NEG_SOFTPLUS, key[T_LOG_ALPHA], row0, 1, nrows, D,
                                                scale=0.05)))

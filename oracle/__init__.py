@@ -112,6 +112,19 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, want_out
     return o, fs, used
 
 
+def l2_normalize(x, eps: float = 1e-12):
+    """Rows of x (last axis) divided by max(their Euclidean norm, eps), in float64.
+
+    The q / k normalisation that precedes the recurrence in the layer ("K3 attention,
+    three-piece set", KDA engineering notes: short causal convolution, then L2
+    normalisation; "From 124M to 2.8T", chapter 3 code: normalisation over the channel
+    axis).  The floor eps = 1e-12 is the usual library default; the pages state none.
+    """
+    x = np.asarray(x, dtype=np.float64)
+    n = np.sqrt(np.sum(x * x, axis=-1, keepdims=True))
+    return x / np.maximum(n, eps)
+
+
 def decode_step(q, k, v, log_alpha, beta, state, nthreads: int = 0):
     """One KDA token for B x H independent units; state [B,H,dk,dv] updated IN PLACE.
 

@@ -109,7 +109,8 @@ def test_product_path_does_not_import_the_oracle():
 def test_unknown_flags_are_rejected_on_host(kda):
     a = _prefill_args()
     assert kda.kda_prefill_ex(*a.values(), 1 << 7) == 1
-    assert kda.kda_decode_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 128, 0, FAKE, FAKE, None, 4) == 1
+    assert kda.kda_decode_step_ex(FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 128, 0, FAKE, FAKE, None,
+                                  1 << 7) == 1
 
 
 def test_slot_calls_reject_bad_arguments_on_host(kda):
@@ -122,6 +123,6 @@ def test_slot_calls_reject_bad_arguments_on_host(kda):
     assert prefill_slots(final_slots=None) == 1
     assert prefill_slots(num_slots=-1) == 1
     assert prefill_slots(init_slots=FAKE + 2) == 1      # misaligned
-    assert prefill_slots(flags=8) == 1                  # unknown flag
+    assert prefill_slots(flags=1 << 7) == 1             # unknown flag
     dec = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 128, 0, FAKE, 8, FAKE, FAKE, None, None]
-    assert kda.kda_decode_step_slots(*dec, 2) == 1      # unknown flag
+    assert kda.kda_decode_step_slots(*dec, 1 << 7) == 1  # unknown flag

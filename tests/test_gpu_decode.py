@@ -123,3 +123,22 @@ def test_scalar_gate_decode():
         assert maxabs(synth.to_f64(o_s), o_ref) <= TOL["bf16"]["o"]
     np.testing.assert_array_equal(synth.to_f64(st_s), synth.to_f64(st_f))
     assert relF(synth.to_f64(st_s), ref_state) <= TOL["bf16"]["state"]
+
+
+@pytest.mark.parametrize("d,dtype", [(128, "bf16"), (64, "f32")])
+def test_in_kernel_qk_l2_normalisation_decode(d, dtype):
+    """KDA_FLAG_QK_L2NORM in decode: raw q, k rows over several steps, within the bar of the
+    oracle run on the fp64-normalised rows."""
+    w = DecodeWorkload("decode_qk_norm", 134, 3, 4, d, dtype, 4, raw_qk=True)
+    state = synth.decode_state(w).cuda()
+    ref_state = synth.to_f64(synth.decode_state(w))
+    for s in range(w.steps):
+        x_h = synth.decode_inputs(w, s)
+        x = {k: t.cuda() for k, t in x_h.items()}
+        o = kda.decode_step(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], state, qk_l2norm=True)
+        torch.cuda.synchronize()
+        r = {k: synth.to_f64(t) for k, t in x_h.items()}
+        o_ref, _ = oracle.decode_step(oracle.l2_normalize(r["q"]), oracle.l2_normalize(r["k"]), r["v"],
+                                      r["log_alpha"], r["beta"], ref_state)
+        assert maxabs(synth.to_f64(o), o_ref) <= TOL[dtype]["o"]
+    assert relF(synth.to_f64(state), ref_state) <= TOL[dtype]["state"]

@@ -393,3 +393,26 @@ def test_prefill_into_a_pool_reports_a_bad_slot_and_runs_the_rest():
     np.testing.assert_array_equal(synth.to_f64(pool_d[1].cpu()), synth.to_f64(fs[0].cpu()))
     for s in (0, 2, 3):
         assert bool((pool_d[s] == 5.0).all())
+
+
+@pytest.mark.parametrize("case", ["two_kernel", "single_kernel", "fp32_d64", "bf16_d64"])
+def test_in_kernel_qk_l2_normalisation(case):
+    """KDA_FLAG_QK_L2NORM: raw N(0, 1) q and k rows (norms near sqrt(d)); the kernels normalise
+    them.  Within the bar of the oracle run on the fp64-normalised rows."""
+    dtype = "f32" if case == "fp32_d64" else "bf16"
+    d = 64 if case in ("fp32_d64", "bf16_d64") else 128
+    w = PrefillWorkload("qk_norm_" + case, 127, 2, d, dtype, (150, 0, 64, 97), 4, init_state=True,
+                        raw_qk=True)
+    inp = synth.prefill_inputs(w)
+    dev = to_device(inp)
+    ws = None
+    if case == "single_kernel":
+        ws = torch.empty(kda.min_workspace_bytes(4), dtype=torch.uint8, device="cuda")
+    o, fs = kda.prefill(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"], dev["cu_seqlens"],
+                        dev["init_state"], workspace=ws, check_status=True, qk_l2norm=True)
+    torch.cuda.synchronize()
+    ref = dict(inp)
+    ref["q"] = oracle.l2_normalize(synth.to_f64(inp["q"]))
+    ref["k"] = oracle.l2_normalize(synth.to_f64(inp["k"]))
+    o_ref, fs_ref = oracle_prefill(ref)
+    assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, dtype, "q/k L2 norm " + case)

@@ -323,3 +323,28 @@ def test_threads_do_not_change_results():
     assert n1 == 1 and n4 == 4
     np.testing.assert_array_equal(o1, o4)
     np.testing.assert_array_equal(f1, f4)
+
+
+# ---------------------------------------------------------------- q / k L2 normalisation
+def test_l2_normalize_worked_rows_and_the_floor():
+    """Rows over the last axis: (3, 4) -> (0.6, 0.8) (a 3-4-5 triangle), a zero row stays
+    zero, and a row shorter than the floor is divided by the floor, not by its norm."""
+    x = np.array([[[3.0, 4.0, 0.0], [0.0, 0.0, 0.0]], [[1e-13, 0.0, 0.0], [0.0, -2.0, 0.0]]])
+    y = oracle.l2_normalize(x)
+    assert y.shape == x.shape
+    np.testing.assert_allclose(y[0, 0], [0.6, 0.8, 0.0], rtol=0, atol=1e-15)
+    assert np.all(y[0, 1] == 0.0)
+    np.testing.assert_allclose(y[1, 0], [0.1, 0.0, 0.0], rtol=1e-12)
+    np.testing.assert_array_equal(y[1, 1], [0.0, -1.0, 0.0])
+
+
+def test_l2_normalize_gives_unit_rows_in_the_same_direction():
+    """Every row of a [T, H, d] array comes out with norm 1 and the same direction (its
+    cosine with the input row is 1); scaling a row by c > 0 changes nothing."""
+    rng = np.random.default_rng(7)
+    x = 3.0 * rng.standard_normal((5, 3, 16))
+    y = oracle.l2_normalize(x)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), 1.0, rtol=1e-14)
+    cos = np.sum(x * y, axis=-1) / np.linalg.norm(x, axis=-1)
+    np.testing.assert_allclose(cos, 1.0, rtol=1e-14)
+    np.testing.assert_allclose(oracle.l2_normalize(x * 17.5), y, rtol=1e-14, atol=1e-16)
