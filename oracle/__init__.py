@@ -14,7 +14,8 @@ Parity status: every part of the recurrence is pinned by closed forms and
 invariants in ``tests/test_oracle_pins.py`` (pure decay, exact retrieval,
 overwrite, geometric convergence, DeltaNet and Gated DeltaNet reductions,
 linearity, column permutation, chunked restatement, an exact-rational worked
-example).  The pages print no numeric output for the method, so no value here
+example); ``l2_normalize`` by a worked 3-4-5 row, its floor, unit norm and
+direction.  The pages print no numeric output for the method, so no value here
 is compared with a printed number.
 """
 from __future__ import annotations
