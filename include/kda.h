@@ -179,6 +179,17 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
  *                        "From 124M to 2.8T", chapter 3 code: the normalisation over the
  *                        channel axis).  The 1/sqrt(d_k) output scale is unchanged. */
 #define KDA_FLAG_QK_L2NORM 2u
+/*  KDA_FLAG_NO_SEQ_SPLIT  keep each sequence's serial state pass in one piece.  By
+ *                        default, when a bf16 d = 128 problem has so few (sequence,
+ *                        head) units that the state pass would leave most SMs idle, and
+ *                        the workspace was sized by kda_prefill_workspace_size for that
+ *                        shape, every sequence is cut into segments of whole chunks: a
+ *                        transition pass gives each segment its affine map (the
+ *                        chunkwise form makes every chunk's update affine in its start
+ *                        state), the maps are chained in fp32 into each segment's start
+ *                        state, and the segments then run at once.  The results agree
+ *                        with the unsplit pass to within rounding, not bit for bit. */
+#define KDA_FLAG_NO_SEQ_SPLIT 4u
 
 /* kda_prefill with options (flags above); flags = 0 is kda_prefill. */
 kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -196,7 +207,8 @@ kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, const f
  *  state_pool   [num_slots, num_heads, d_k, d_v] fp32, 16-byte aligned
  *  init_slots   [num_seqs] int32 device, or NULL (every sequence starts from zero);
  *               an entry -1 starts that sequence from zero
- *  final_slots  [num_seqs] int32 device, required
+ *  final_slots  [num_seqs] int32 device, required; an entry -1 stores no final
+ *               state for that sequence
  * A sequence may read and write the same slot (it is updated in place).  Final
  * slots must be distinct, and no sequence may start from another sequence's final
  * slot (the two would race).  A slot outside [0, num_slots) (init: also -1) is a

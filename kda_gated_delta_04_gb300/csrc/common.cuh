@@ -25,10 +25,30 @@ constexpr float kQkNormEps = 1e-12f;       // floor of the q / k row norm (KDA_F
 // Everything a prefill launch needs, already validated on the host.
 // Where each sequence's states live.  Dense (fin == null): entry n of init_state and of
 // final_state.  A state pool of num entries: init[n] (-1, or init == null: start from zero)
-// and fin[n].
+// and fin[n] (-1: not stored).
 struct StateSlots {
     const int32_t *init = nullptr, *fin = nullptr;
     int64_t num = 0;
+};
+
+// Sequence-split state pass (bf16, d = 128, few (sequence, head) units): every sequence's
+// chunks are cut into segments of lseg chunks, each a "virtual sequence" v.  A transition
+// pass gives each segment but the last its affine map S_end = M_v S_start + R_v, a combine
+// kernel chains the maps into every segment's true start state, and the state pass then
+// runs all segments at once.  lseg == 0: no split.  Every pointer is workspace.
+struct SeqSplit {
+    int lseg = 0;                // chunks per segment
+    int nv_max = 0;              // bound on the number of segments (grid extent)
+    int32_t *vcu = nullptr;      // [nv_max + 2] token start of each segment (then the end)
+    int32_t *vcc = nullptr;      // [nv_max + 2] first global chunk of each segment
+    int32_t *vorder = nullptr;   // [nv_max]     segment processed by grid index z
+    int32_t *seg_first = nullptr;  // [num_seqs + 1] first segment of each sequence
+    int32_t *init_src = nullptr;   // [num_seqs]   the sequence's initial-state entry, -1 = zero
+    int32_t *fin_a = nullptr;    // [nv_max + 1] transition-pass store slot (-1: last segment)
+    int32_t *init_c = nullptr;   // [nv_max + 1] state-pass start slot in `start`
+    int32_t *fin_c = nullptr;    // [nv_max + 1] state-pass final slot (the sequence's, last segment only)
+    float *R = nullptr, *M = nullptr, *start = nullptr;  // [nv_max, H, d, d] fp32 each
+    void *vzero = nullptr;       // [H, d] bf16 zeros: the value rows of the transition pass
 };
 
 struct PrefillProblem {
@@ -48,6 +68,7 @@ struct PrefillProblem {
     void *records;              // workspace: per chunk-head records of the two-kernel path, or null
     bool scalar_gate = false;   // log_alpha is [T, H]: one decay per token-head for every key channel
     StateSlots slots;           // state pool indices, or none (dense states)
+    SeqSplit split;             // sequence-split state pass, or none
     bool qk_l2norm = false;     // q, k rows are normalised in the kernels
     cudaStream_t stream;
 };
@@ -80,6 +101,15 @@ size_t prefill_split_records_bytes(int64_t total_tokens, int num_seqs, int num_h
 cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records,
                                  cudaEvent_t mid = nullptr);
 cudaError_t launch_decode(const DecodeProblem &p);
+// Sequence-split state pass: segment length for a problem shape (0: no split), the bound on
+// its segment count, the workspace it needs, and its two small kernels (segment tables after
+// the schedule kernel; start states after the transition pass).
+int seqsplit_lseg(int num_seqs, int64_t total_tokens, int num_heads);
+int seqsplit_nv_max(int lseg, int num_seqs, int64_t total_tokens);
+size_t seqsplit_bytes(int num_seqs, int64_t total_tokens, int num_heads);
+void seqsplit_carve(SeqSplit &s, int num_seqs, int64_t total_tokens, int num_heads, char *ws);
+cudaError_t launch_seqsplit_plan(const PrefillProblem &p);
+cudaError_t launch_seqsplit_combine(const PrefillProblem &p);
 
 // ---------------------------------------------------------------- device helpers
 __device__ __forceinline__ float load_io(const float *p) { return *p; }
@@ -120,7 +150,7 @@ __device__ __forceinline__ void seq_range(const int32_t *cu, int n, int64_t tota
     t1 = b;
 }
 
-// Sequence n's initial-state entry si (-1: zero) and final-state entry sf (-1: not written).
+// Sequence n's initial-state entry si (-1: zero) and final-state entry sf (-1: not stored).
 // Returns false for a pool slot out of range; the sequence then starts from zero and its final
 // state is not written.
 __device__ __forceinline__ bool state_entries(const StateSlots &s, int n, bool has_init, int64_t &si,
@@ -133,7 +163,7 @@ __device__ __forceinline__ bool state_entries(const StateSlots &s, int n, bool h
     }
     si = s.init ? s.init[n] : -1;
     sf = s.fin[n];
-    if (si >= -1 && si < s.num && sf >= 0 && sf < s.num) return true;
+    if (si >= -1 && si < s.num && sf >= -1 && sf < s.num) return true;
     si = sf = -1;
     return false;
 }

@@ -45,10 +45,17 @@ bool split_shape(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int3
            total_tokens <= 0x7fffffffll &&
            (total_tokens / KDA_CHUNK + num_seqs) * (int64_t)num_heads <= 0x7fffffffll;
 }
-size_t ws_split_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
+// the two-kernel path: schedule, chunk numbering and records
+size_t ws_records_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
 {
     return ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) +
            kda::prefill_split_records_bytes(total_tokens, num_seqs, num_heads);
+}
+// ... plus the sequence-split state pass where the shape calls for it
+size_t ws_split_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
+{
+    return ws_records_bytes(num_seqs, total_tokens, num_heads) +
+           kda::seqsplit_bytes(num_seqs, total_tokens, num_heads);
 }
 
 kda_status_t check_shape(int32_t d_k, int32_t d_v, kda_dtype_t dtype)
@@ -62,7 +69,7 @@ kda_status_t check_shape(int32_t d_k, int32_t d_v, kda_dtype_t dtype)
 }  // namespace
 
 // every option bit of the _ex / _slots calls
-constexpr uint32_t kKnownFlags = KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM;
+constexpr uint32_t kKnownFlags = KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM | KDA_FLAG_NO_SEQ_SPLIT;
 
 extern "C" {
 
@@ -126,9 +133,15 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     // workspace holds the per-chunk records, else as the single fused kernel.  fp32 I/O
     // (the exact path) and d = 64 run the CUDA-core chunk kernel.
     const bool split = split_shape(num_seqs, total_tokens, num_heads, d_k, d_v, dtype) &&
-                       workspace_bytes >= ws_split_bytes(num_seqs, total_tokens, num_heads);
+                       workspace_bytes >= ws_records_bytes(num_seqs, total_tokens, num_heads);
     p.cc = split ? reinterpret_cast<int32_t *>(ws + ws_min_bytes(num_seqs)) : nullptr;
     p.records = split ? ws + ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) : nullptr;
+    // few (sequence, head) units: the state pass runs each sequence in segments
+    if (split && !(flags & KDA_FLAG_NO_SEQ_SPLIT) &&
+        workspace_bytes >= ws_split_bytes(num_seqs, total_tokens, num_heads))
+        kda::seqsplit_carve(p.split, num_seqs, total_tokens, num_heads,
+                            static_cast<char *>(p.records) +
+                                kda::prefill_split_records_bytes(total_tokens, num_seqs, num_heads));
 
     if (!mark(0)) return KDA_ERR_CUDA;
     if (kda::launch_prefill_prep(p) != cudaSuccess) return KDA_ERR_CUDA;

@@ -23,6 +23,8 @@
 // The state kernel walks the chunks of one (sequence, head, 32-column value
 // slice): per chunk one MMA group P V + N S on the critical path and the output
 // group P2 V + Q' S beside it, issued by a second thread.
+#include <climits>
+
 #include "tc_common.cuh"
 
 namespace kda {
@@ -490,12 +492,18 @@ constexpr int kL2Ahead = 3;  // records brought into L2 this many chunks ahead
 // refills, and each ready / output barrier alternates with the chunk parity, so no
 // barrier is ever waited on more than one phase behind.  Each issuing lane has a
 // warp of its own: MMA issue slows down badly when the rest of its warp is busy.
+//
+// CTAs with blockIdx.z >= z_ident run the transition pass of the sequence-split prefill:
+// the state starts as the identity, every value row reads as zero (tm_v_zero maps one
+// zero row, so every box past it is filled with zeros), and the final state goes to
+// final_ident.  Their result is the linear map of the sequence's chunks.  A CTA whose
+// sequence has no final state to store and no outputs to write returns at once.
 __global__ void __launch_bounds__(kStateThreads, 1)
-prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__restrict__ cu,
-                     int64_t total, int H, const int32_t *__restrict__ cc,
+prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_v_zero,
+                     const int32_t *__restrict__ cu, int64_t total, int H, const int32_t *__restrict__ cc,
                      const unsigned char *__restrict__ records, const float *init_state,
                      __nv_bfloat16 *__restrict__ o, float *final_state, uint32_t *status,
-                     const int32_t *__restrict__ order, StateSlots slots)
+                     const int32_t *__restrict__ order, StateSlots slots, int z_ident, float *final_ident)
 {
     using L = StateLayout;
     extern __shared__ unsigned char smem_raw[];
@@ -510,10 +518,18 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     // launched with programmatic stream serialization behind the chunk kernel: the
     // schedule (order, cc) and the records are read only after pdl_wait
     pdl_wait();
-    const int j0 = blockIdx.x * kDV, h = blockIdx.y, n = order[blockIdx.z];
+    const bool ident = (int)blockIdx.z >= z_ident;
+    const int j0 = blockIdx.x * kDV, h = blockIdx.y, n = order[ident ? blockIdx.z - z_ident : blockIdx.z];
     int64_t t0, t1;
     seq_range(cu, n, total, t0, t1);
     const int nchunks = (int)((t1 - t0 + kC - 1) / kC);
+    int64_t si, sf;
+    if (!state_entries(slots, n, !ident && init_state != nullptr, si, sf) && tid == 0)
+        atomicOr(status, DEV_ERR_SLOT);
+    if (ident) o = nullptr;
+    if (sf < 0 && (o == nullptr || nchunks == 0)) return;  // nothing to store or write
+    float *const fpool = ident ? final_ident : final_state;
+    const CUtensorMap *const tmv = ident ? &tm_v_zero : &tm_v;
     const unsigned char *rec0 = records + ((size_t)cc[n] * H + h) * kRecBytes;
     const size_t rec_stride = (size_t)H * kRecBytes;
 
@@ -526,7 +542,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     };
     auto load_v = [&](int k) {
         mbar_arrive_expect_tx(&bar_v[k % kVRing], 4096);
-        tma_load_3d(sm + L::VBOX + (k % kVRing) * 4096, &tm_v, &bar_v[k % kVRing], j0, h,
+        tma_load_3d(sm + L::VBOX + (k % kVRing) * 4096, tmv, &bar_v[k % kVRing], j0, h,
                     (int)(t0 + (int64_t)k * kC));
         v_issued = k + 1;
     };
@@ -550,11 +566,12 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
     // state row i, columns j0 + 8*part .. +7 in registers; S^T (bf16) operands in O7
     const int i_row = quarter * 32 + lane, jp = part * 8;
     float S[8];
-    int64_t si, sf;
-    if (!state_entries(slots, n, init_state != nullptr, si, sf) && tid == 0) atomicOr(status, DEV_ERR_SLOT);
     const size_t st_off = ((size_t)h * kD + i_row) * kD + j0 + jp, st_entry = (size_t)H * kD * kD;
     if (state_warp) {
-        if (si >= 0) {
+        if (ident) {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) S[j] = i_row == j0 + jp + j ? 1.f : 0.f;
+        } else if (si >= 0) {
 #pragma unroll
             for (int q = 0; q < 2; ++q) {
                 const float4 x = *reinterpret_cast<const float4 *>(init_state + si * st_entry + st_off + 4 * q);
@@ -624,7 +641,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
         for (int k = 0; k < 2 && k < nchunks; ++k) load_record(k);
         for (int k = 2; k < kL2Ahead && k < nchunks; ++k) bulk_prefetch_l2(rec0 + (size_t)k * rec_stride, kRecBytes);
         for (int k = 0; k < kVRing && k < nchunks; ++k) load_v(k);
-        prefetch_tmap(&tm_v);
+        prefetch_tmap(tmv);
     }
     if (state_warp && nchunks > 0) {
         ok = convert_v(0);
@@ -738,7 +755,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const int32_t *__
         for (int k = v_issued > kVRing ? v_issued - kVRing : 0; k < v_issued; ++k)
             (void)mbar_wait_ns(&bar_v[k % kVRing], (uint32_t)((k / kVRing) & 1), kWaitNs);
     } else if (state_warp && sf >= 0) {
-        float *dst = final_state + sf * st_entry + st_off;
+        float *dst = fpool + sf * st_entry + st_off;
 #pragma unroll
         for (int q = 0; q < 2; ++q)
             *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
@@ -773,6 +790,7 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     if (chunk_bound * p.num_heads > INT32_MAX) return cudaErrorInvalidValue;
     // both kernels may start while the kernel before them drains (programmatic
     // dependent launch); each waits for its inputs with griddepcontrol.wait
+    if (p.split.lseg > 0 && (err = launch_seqsplit_plan(p)) != cudaSuccess) return err;
     cudaLaunchAttribute pdl;
     pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl.val.programmaticStreamSerializationAllowed = 1;
@@ -789,13 +807,39 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
                              p.scalar_gate);
     if (err != cudaSuccess) return err;
     if (mid && (err = cudaEventRecord(mid, p.stream)) != cudaSuccess) return err;
-    cfg.gridDim = dim3(kD / kDV, p.num_heads, p.num_seqs);
     cfg.blockDim = dim3(kStateThreads);
     cfg.dynamicSmemBytes = kStateSmem;
-    return cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, p.cu_seqlens, p.total_tokens, p.num_heads,
-                              static_cast<const int32_t *>(cc), static_cast<const unsigned char *>(records),
-                              p.init_state, static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.status,
-                              static_cast<const int32_t *>(p.order), p.slots);
+    const unsigned char *rec = static_cast<const unsigned char *>(records);
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+    if (p.split.lseg == 0) {
+        cfg.gridDim = dim3(kD / kDV, p.num_heads, p.num_seqs);
+        return cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, tv, p.cu_seqlens, p.total_tokens, p.num_heads,
+                                  static_cast<const int32_t *>(cc), rec, p.init_state, o, p.final_state, p.status,
+                                  static_cast<const int32_t *>(p.order), p.slots, INT_MAX, (float *)nullptr);
+    }
+    // sequence split: transition pass (R for grid z < nv_max, M above), start states, state pass
+    const SeqSplit &s = p.split;
+    CUtensorMap tz;  // one zero value row: every box of the transition pass reads zeros
+    if (!make_map(&tz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s.vzero, 1, p.num_heads, 2, kDV))
+        return cudaErrorInvalidValue;
+    StateSlots sa;
+    sa.fin = s.fin_a;
+    sa.num = (int64_t)s.nv_max + 1;
+    cfg.gridDim = dim3(kD / kDV, p.num_heads, 2 * s.nv_max);
+    err = cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, tz, (const int32_t *)s.vcu, p.total_tokens,
+                             p.num_heads, (const int32_t *)s.vcc, rec, (const float *)nullptr,
+                             (__nv_bfloat16 *)nullptr, s.R, p.status, (const int32_t *)s.vorder, sa, s.nv_max, s.M);
+    if (err != cudaSuccess) return err;
+    if ((err = launch_seqsplit_combine(p)) != cudaSuccess) return err;
+    StateSlots sc;
+    sc.init = s.init_c;
+    sc.fin = s.fin_c;
+    const int64_t user_entries = p.slots.fin ? p.slots.num : p.num_seqs;
+    sc.num = user_entries > (int64_t)s.nv_max + 1 ? user_entries : (int64_t)s.nv_max + 1;
+    cfg.gridDim = dim3(kD / kDV, p.num_heads, s.nv_max);
+    return cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, tv, (const int32_t *)s.vcu, p.total_tokens,
+                              p.num_heads, (const int32_t *)s.vcc, rec, (const float *)s.start, o, p.final_state,
+                              p.status, (const int32_t *)s.vorder, sc, INT_MAX, (float *)nullptr);
 }
 
 }  // namespace kda

@@ -23,6 +23,7 @@ KDA_OK, KDA_ERR_INVALID_ARG, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT,
 KDA_DTYPE_BF16, KDA_DTYPE_F32 = 0, 1
 KDA_FLAG_SCALAR_GATE = 1
 KDA_FLAG_QK_L2NORM = 2
+KDA_FLAG_NO_SEQ_SPLIT = 4
 CHUNK = 64
 
 _lib = None
@@ -186,10 +187,10 @@ def _ptr(t, name, dtype=None):
     return t.data_ptr()
 
 
-def _flags(log_alpha, qk_l2norm):
+def _flags(log_alpha, qk_l2norm, seq_split=True):
     """Option bits: a log_alpha without a channel axis is the scalar gate."""
     return ((KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0) |
-            (KDA_FLAG_QK_L2NORM if qk_l2norm else 0))
+            (KDA_FLAG_QK_L2NORM if qk_l2norm else 0) | (0 if seq_split else KDA_FLAG_NO_SEQ_SPLIT))
 
 
 def _stream_handle(stream, device):
@@ -213,13 +214,14 @@ def min_workspace_bytes(num_seqs):
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=None,
             final_state=None, workspace=None, stream=None, check_status=False, outputs=True,
-            qk_l2norm=False):
+            qk_l2norm=False, seq_split=True):
     """KDA prefill over packed sequences.  q, k: [T, H, d]; v: [T, H, d]; log_alpha: [T, H, d]
     fp32; beta: [T, H] fp32; cu_seqlens: int32 [N+1] CUDA tensor or None (one sequence);
     init_state: [N, H, d, d] fp32 or None.  Returns (o, final_state); with outputs=False
     only the final states are computed and o is None.  A log_alpha of shape [T, H] is the
     scalar-gate (Gated DeltaNet) variant: one decay per token-head for every key channel.
-    qk_l2norm=True: q and k are raw and the kernels L2-normalise their rows."""
+    qk_l2norm=True: q and k are raw and the kernels L2-normalise their rows.  seq_split=False
+    keeps each sequence's state pass in one piece (KDA_FLAG_NO_SEQ_SPLIT)."""
     torch = _torch()
     T, H, d = q.shape
     dt = _dtype_code(q)
@@ -232,7 +234,7 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
         final_state = torch.empty((N, H, d, v.shape[2]), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = workspace_for(N, T, H, d, dt, q.device)
-    flags = _flags(log_alpha, qk_l2norm)
+    flags = _flags(log_alpha, qk_l2norm, seq_split)
     st = kda_prefill_ex(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
                      _ptr(log_alpha, "log_alpha", torch.float32), _ptr(beta, "beta", torch.float32),
                      _ptr(cu_seqlens, "cu_seqlens", torch.int32), N, T, H, d, v.shape[2], dt,
@@ -252,7 +254,7 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
 
 def prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, state_pool, final_slots, init_slots=None, *,
                   o=None, workspace=None, stream=None, check_status=False, outputs=True,
-                  qk_l2norm=False):
+                  qk_l2norm=False, seq_split=True):
     """Prefill into a paged state cache: sequence n starts from state_pool[init_slots[n]]
     (zero when init_slots is None or the entry is -1) and its final state is written to
     state_pool[final_slots[n]].  state_pool [S, H, d, d] fp32; slots int32 CUDA tensors [N].
@@ -267,7 +269,7 @@ def prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, state_pool, final_slots,
         o = None
     if workspace is None:
         workspace = workspace_for(N, T, H, d, dt, q.device)
-    flags = _flags(log_alpha, qk_l2norm)
+    flags = _flags(log_alpha, qk_l2norm, seq_split)
     st = kda_prefill_slots(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
                            _ptr(log_alpha, "log_alpha", torch.float32),
                            _ptr(beta, "beta", torch.float32),

@@ -416,3 +416,64 @@ def test_in_kernel_qk_l2_normalisation(case):
     ref["k"] = oracle.l2_normalize(synth.to_f64(inp["k"]))
     o_ref, fs_ref = oracle_prefill(ref)
     assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, dtype, "q/k L2 norm " + case)
+
+
+SPLIT_CASES = [  # few (sequence, head) units: the state pass runs in segments
+    PrefillWorkload("split_H2_T2000_state", 128, 2, 128, "bf16", (2000,), 1, init_state=True),
+    PrefillWorkload("split_H1_varlen_state", 129, 1, 128, "bf16", (2000, 0, 3000, 64, 1), 5,
+                    init_state=True),
+]
+
+
+@pytest.mark.parametrize("w", SPLIT_CASES, ids=lambda w: w.name)
+def test_sequence_split_state_pass(w):
+    """The segmented state pass (transition maps, fp32 chaining, all segments at once) is
+    within the bar of the oracle, differs from the unsplit pass only by rounding (so it did
+    run), and its state-only and state-pool forms give bit for bit the same final states."""
+    inp = synth.prefill_inputs(w)
+    d = to_device(inp)
+    args = (d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"])
+    o_s, fs_s = kda.prefill(*args, check_status=True)
+    o_n, fs_n = kda.prefill(*args, check_status=True, seq_split=False)
+    _, fs_only = kda.prefill(*args, check_status=True, outputs=False)
+    torch.cuda.synchronize()
+    o_ref, fs_ref = oracle_prefill(inp)
+    assert_parity(synth.to_f64(o_s), synth.to_f64(fs_s), o_ref, fs_ref, "bf16", "split " + w.name)
+    assert_parity(synth.to_f64(o_n), synth.to_f64(fs_n), o_ref, fs_ref, "bf16", "unsplit " + w.name)
+    assert not np.array_equal(synth.to_f64(fs_s), synth.to_f64(fs_n))
+    np.testing.assert_array_equal(synth.to_f64(fs_only), synth.to_f64(fs_s))
+    # the same problem against a state pool: start slots reversed, one sequence from zero
+    N, H = len(w.seq_lens), w.num_heads
+    pool = torch.zeros((2 * N + 1, H, 128, 128), dtype=torch.float32)
+    init_h = [2 * N - n for n in range(N)]
+    init_h[0] = -1
+    init_dense = inp["init_state"].clone()
+    init_dense[0] = 0.0
+    for n, s in enumerate(init_h):
+        if s >= 0:
+            pool[s] = inp["init_state"][n]
+    pool_d = pool.cuda()
+    final_h = list(range(N))
+    o_p = kda.prefill_slots(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], pool_d,
+                            torch.tensor(final_h, dtype=torch.int32, device="cuda"),
+                            torch.tensor(init_h, dtype=torch.int32, device="cuda"), check_status=True)
+    o_d, fs_d = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
+                            init_dense.cuda(), check_status=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(synth.to_f64(o_p), synth.to_f64(o_d))
+    np.testing.assert_array_equal(synth.to_f64(pool_d[final_h].cpu()), synth.to_f64(fs_d.cpu()))
+
+
+def test_sequence_split_long_context_few_heads_sampled():
+    """T = 65536, H = 4, one sequence (the segmented pass with 5 segments of 205 chunks):
+    head 2 against the oracle, outputs and final state."""
+    w = PrefillWorkload("long_T65536_H4_state", 130, 4, 128, "bf16", (65536,), 1, init_state=True)
+    inp = synth.prefill_inputs(w)
+    d = to_device(inp)
+    o, fs = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
+                        d["init_state"], check_status=True)
+    torch.cuda.synchronize()
+    sub = synth.prefill_inputs(w, heads=[2])
+    o_ref, fs_ref = oracle_prefill(sub)
+    assert_parity(synth.to_f64(o[:, 2:3]), synth.to_f64(fs[:, 2:3]), o_ref, fs_ref, "bf16",
+                  "split T=65536 H=4 head 2")
