@@ -5,7 +5,9 @@ One step is one kda_prefill over the single-sequence prefill workload
 chunkwise row of the path (decay prefix, decayed operands, k-k and q-k
 matrices, UT solve, WY factors, output, state propagation).  The decode row is
 timed in the same run on its own workload (256 sequences x 32 heads, d=128,
-1000 in-place steps) and reported under "decode".
+1000 in-place steps) and reported under "decode".  A long single sequence with
+few heads (T=65536, H=4), where the serial state pass would leave most SMs idle,
+is timed with and without the sequence-split state pass under "long_context".
 
 value    prefill tokens/s with inputs resident in HBM (CUDA events, L2 flushed
          between timed steps by writing a 256 MiB buffer, flush not timed);
@@ -280,6 +282,51 @@ class _Gpu:
         return out
 
     # ------------------------------------------------------------------ decode
+    # ------------------------------------------------------------------ long context
+    def setup_long(self):
+        torch, kda, synth = self.torch, self.kda, self.synth
+        self.lw = lw = synth.PrefillWorkload("prefill_bf16_T65536_H4_d128_state", 15, 4, 128, "bf16",
+                                             (65536,), 1, init_state=True)
+        inp = synth.prefill_inputs(lw, seed=self.seed)
+        self.lx = {k: inp[k].to(self.dev)
+                   for k in ("q", "k", "v", "log_alpha", "beta", "cu_seqlens", "init_state")}
+        T, H, d = inp["q"].shape
+        self.lo = torch.empty((T, H, d), dtype=torch.bfloat16, device=self.dev)
+        self.lfs = torch.empty((1, H, d, d), dtype=torch.float32, device=self.dev)
+        self.lws = kda.workspace_for(1, T, H, d, kda.KDA_DTYPE_BF16, self.dev)
+
+    def long_call(self, split):
+        kda, x = self.kda, self.lx
+        T, H, d = x["q"].shape
+        st = kda.kda_prefill_ex(x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(),
+                                x["log_alpha"].data_ptr(), x["beta"].data_ptr(),
+                                x["cu_seqlens"].data_ptr(), 1, T, H, d, d, kda.KDA_DTYPE_BF16,
+                                x["init_state"].data_ptr(), self.lo.data_ptr(), self.lfs.data_ptr(),
+                                self.lws.data_ptr(), self.lws.numel(), self.sh,
+                                0 if split else kda.KDA_FLAG_NO_SEQ_SPLIT)
+        if st != kda.KDA_OK:
+            raise kda.KdaError(st, "kda_prefill_ex")
+
+    def time_long(self, steps, warmup):
+        """Event time (ms per call) of the long-context prefill, split and unsplit (its 470 MB
+        of inputs exceed L2, so no flush is needed)."""
+        torch, out = self.torch, {}
+        for split in (True, False):
+            for _ in range(warmup):
+                self.long_call(split)
+            torch.cuda.synchronize()
+            a, b = self.event(), self.event()
+            a.record(self.stream)
+            for _ in range(steps):
+                self.long_call(split)
+            b.record(self.stream)
+            torch.cuda.synchronize()
+            out[split] = a.elapsed_time(b) / steps
+        st = self.kda.kda_read_device_status(self.lws.data_ptr(), self.sh)
+        if st != self.kda.KDA_OK:
+            raise self.kda.KdaError(st, "kda_prefill_ex (device status)")
+        return out
+
     def setup_decode(self):
         torch, synth = self.torch, self.synth
         self.dw = dw = synth.DECODE_256
@@ -334,8 +381,11 @@ def run_gpu(args):
     peaks = measured_peaks()
     do_prefill = args.only in ("all", "prefill")
     do_decode = args.only in ("all", "decode")
+    do_long = args.only in ("all", "long")
     if do_prefill:
         g.setup_prefill()
+    if do_long:
+        g.setup_long()
     if do_decode:
         g.setup_decode()
     clocks = ClockSampler(local_rank)
@@ -349,6 +399,8 @@ def run_gpu(args):
             e2e_ms = g.time_prefill_e2e(args.steps, args.warmup)
         if do_decode:
             dec_ms = g.time_decode(g.dw.steps, max(3, args.warmup), barrier)
+        if do_long:
+            long_ms = g.time_long(5, max(3, args.warmup))
     if do_prefill:
         total_ms = reduce_max(sum(step_ms))
         e2e_total = reduce_max(sum(e2e_ms))
@@ -413,6 +465,16 @@ def run_gpu(args):
                          "unit": "GB/s", "frac": dec_achieved / peaks["hbm_gbs"],
                          "traffic": profiled_traffic("decode_256"),
                          "algorithmic_bytes_per_launch": dec_bytes}}
+    if do_long:
+        T = g.lw.seq_lens[0]
+        split_ms, unsplit_ms = reduce_max(long_ms[True]), reduce_max(long_ms[False])
+        line["long_context"] = {
+            "metric": "KDA prefill tokens/s, one long sequence with few heads",
+            "workload": g.lw.name, "unit": "tokens/s",
+            "value": aggregate_rate(T, world, 1, split_ms), "ms_per_call": split_ms,
+            "unsplit_value": aggregate_rate(T, world, 1, unsplit_ms), "unsplit_ms_per_call": unsplit_ms,
+            "speedup_of_sequence_split": unsplit_ms / split_ms, "steps": 5,
+            "note": "default call (sequence-split state pass) against KDA_FLAG_NO_SEQ_SPLIT"}
     if do_prefill and rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(g.w, g.inp)
     if rank == 0:
@@ -506,7 +568,7 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "long"], default="all",
                     help="profiling aid: run only one part (the printed line is then partial)")
     args = ap.parse_args()
     if args.warmup < 3:
