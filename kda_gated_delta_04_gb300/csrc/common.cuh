@@ -65,6 +65,8 @@ struct PrefillProblem {
     uint32_t *status;           // workspace word
     int32_t *order;             // workspace: sequence processing order (longest first)
     int32_t *cc;                // workspace: first chunk of each sequence [num_seqs + 1], or null
+    int2 *desc = nullptr;       // workspace: per packed chunk g < chunk_bound, (first token, rows); or null
+    int chunk_bound = 0;        // total_tokens / 64 + num_seqs, a bound on the packed chunk count
     void *records;              // workspace: per chunk-head records of the two-kernel path, or null
     bool scalar_gate = false;   // log_alpha is [T, H]: one decay per token-head for every key channel
     StateSlots slots;           // state pool indices, or none (dense states)

@@ -37,6 +37,12 @@ size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 size_t ws_order_bytes(int32_t num_seqs) { return round_up((size_t)num_seqs * sizeof(int32_t) + 1, 256); }
 size_t ws_min_bytes(int32_t num_seqs) { return kda::kWorkspaceHeader + ws_order_bytes(num_seqs); }
 size_t ws_cc_bytes(int32_t num_seqs) { return round_up(((size_t)num_seqs + 1) * sizeof(int32_t), 256); }
+// one (first token, rows) pair per packed chunk, bounded by total_tokens / 64 + num_seqs
+int64_t chunk_bound(int32_t num_seqs, int64_t total_tokens) { return total_tokens / kda::kChunk + num_seqs; }
+size_t ws_desc_bytes(int32_t num_seqs, int64_t total_tokens)
+{
+    return round_up((size_t)chunk_bound(num_seqs, total_tokens) * 2 * sizeof(int32_t), 256);
+}
 bool split_shape(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
                  kda_dtype_t dtype)
 {
@@ -48,7 +54,7 @@ bool split_shape(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int3
 // the two-kernel path: schedule, chunk numbering and records
 size_t ws_records_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
 {
-    return ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) +
+    return ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) + ws_desc_bytes(num_seqs, total_tokens) +
            kda::prefill_split_records_bytes(total_tokens, num_seqs, num_heads);
 }
 // ... plus the sequence-split state pass where the shape calls for it
@@ -135,7 +141,10 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     const bool split = split_shape(num_seqs, total_tokens, num_heads, d_k, d_v, dtype) &&
                        workspace_bytes >= ws_records_bytes(num_seqs, total_tokens, num_heads);
     p.cc = split ? reinterpret_cast<int32_t *>(ws + ws_min_bytes(num_seqs)) : nullptr;
-    p.records = split ? ws + ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) : nullptr;
+    p.desc = split ? reinterpret_cast<int2 *>(ws + ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs)) : nullptr;
+    p.chunk_bound = split ? (int)chunk_bound(num_seqs, total_tokens) : 0;
+    p.records = split ? ws + ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) + ws_desc_bytes(num_seqs, total_tokens)
+                      : nullptr;
     // few (sequence, head) units: the state pass runs each sequence in segments
     if (split && !(flags & KDA_FLAG_NO_SEQ_SPLIT) &&
         workspace_bytes >= ws_split_bytes(num_seqs, total_tokens, num_heads))

@@ -32,9 +32,12 @@ constexpr int kThreads = 256;
 // Clears the workspace error word, checks cu_seqlens, writes the order in
 // which sequences are processed (longest first, ties by index) and, when cc is
 // given, each sequence's first chunk in a packed chunk numbering
-// (cc[n] = sum over m < n of ceil(len_m / 64); cc[num_seqs] = all chunks).
+// (cc[n] = sum over m < n of ceil(len_m / 64); cc[num_seqs] = all chunks) and, when desc
+// is given, every packed chunk's first token and row count (0 rows past the last chunk),
+// so that a chunk CTA finds its rows with one load.
 __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs, int64_t total,
-                                    uint32_t *status, int32_t *order, int32_t *cc)
+                                    uint32_t *status, int32_t *order, int32_t *cc, int2 *desc,
+                                    int chunk_bound)
 {
     // the chunk kernel may be scheduled now; it waits for this kernel's results itself
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
@@ -100,6 +103,23 @@ __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs
         __syncthreads();
     }
     if (threadIdx.x == 0) cc[num_seqs] = carry;
+    if (!desc) return;
+    __syncthreads();  // cc complete (global writes of this block are visible to it after the barrier)
+    for (int g = threadIdx.x; g < chunk_bound; g += blockDim.x) {
+        int2 d = make_int2(0, 0);
+        if (g < carry) {
+            int lo = 0, hi = num_seqs;  // the sequence n with cc[n] <= g < cc[n + 1]
+            while (hi - lo > 1) {
+                const int mid = (lo + hi) >> 1;
+                if (cc[mid] <= g) lo = mid; else hi = mid;
+            }
+            int64_t t0, t1;
+            seq_range(cu, lo, total, t0, t1);
+            const int64_t c0 = t0 + (int64_t)(g - cc[lo]) * kChunk;
+            d = make_int2((int)c0, (int)((t1 - c0) < kChunk ? (t1 - c0) : kChunk));
+        }
+        desc[g] = d;
+    }
 }
 
 // ---------------------------------------------------------------- SIMT chunk kernel
@@ -333,7 +353,7 @@ cudaError_t launch_simt(const PrefillProblem &p)
 cudaError_t launch_prefill_prep(const PrefillProblem &p)
 {
     prefill_prep_kernel<<<1, 1024, 0, p.stream>>>(p.cu_seqlens, p.num_seqs, p.total_tokens,
-                                                  p.status, p.order, p.cc);
+                                                  p.status, p.order, p.cc, p.desc, p.chunk_bound);
     return cudaGetLastError();
 }
 

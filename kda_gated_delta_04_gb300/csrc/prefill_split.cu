@@ -303,8 +303,7 @@ template <bool NORM>
 __global__ void __launch_bounds__(kChunkThreads, 2)
 prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const float *__restrict__ log_alpha, const float *__restrict__ beta,
-                     const int32_t *__restrict__ cu, int64_t total, int H, int num_seqs,
-                     int chunk_bound, const int32_t *__restrict__ cc,
+                     const int2 *__restrict__ desc, int H, int chunk_bound,
                      unsigned char *__restrict__ records, uint32_t *status, bool with_o, bool scalar_gate)
 {
     using L = ChunkLayout;
@@ -322,17 +321,10 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     // one CTA per (chunk, head), heads fastest, chunks last to first
     const int h = (int)(blockIdx.x % (unsigned)H);
     const int g = chunk_bound - 1 - (int)(blockIdx.x / (unsigned)H);
-    if (g >= cc[num_seqs]) return;  // past the last chunk (the grid is an upper bound)
-    int lo = 0, hi = num_seqs;      // sequence n with cc[n] <= g < cc[n + 1]
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cc[mid] <= g) lo = mid; else hi = mid;
-    }
-    const int n = lo;
-    int64_t t0, t1;
-    seq_range(cu, n, total, t0, t1);
-    const int64_t c0 = t0 + (int64_t)(g - cc[n]) * kC;
-    const int len = (t1 - c0) < kC ? (int)(t1 - c0) : kC;
+    const int2 dsc = desc[g];     // first token and row count of packed chunk g
+    if (dsc.y <= 0) return;       // past the last chunk (the grid is an upper bound)
+    const int64_t c0 = dsc.x;
+    const int len = dsc.y;
     unsigned char *rec = records + ((size_t)g * H + h) * kRecBytes;
 
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -787,7 +779,8 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
         !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kDV))
         return cudaErrorInvalidValue;
     const int64_t chunk_bound = p.total_tokens / kC + p.num_seqs;
-    if (chunk_bound * p.num_heads > INT32_MAX) return cudaErrorInvalidValue;
+    if (chunk_bound * p.num_heads > INT32_MAX || !p.desc || p.chunk_bound != chunk_bound)
+        return cudaErrorInvalidValue;
     // both kernels may start while the kernel before them drains (programmatic
     // dependent launch); each waits for its inputs with griddepcontrol.wait
     if (p.split.lseg > 0 && (err = launch_seqsplit_plan(p)) != cudaSuccess) return err;
@@ -801,9 +794,8 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     cfg.stream = p.stream;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, chunk_kernel, tq, tk, p.log_alpha, p.beta, p.cu_seqlens,
-                             p.total_tokens, p.num_heads, p.num_seqs, (int)chunk_bound, cc,
-                             static_cast<unsigned char *>(records), p.status, p.o != nullptr,
+    err = cudaLaunchKernelEx(&cfg, chunk_kernel, tq, tk, p.log_alpha, p.beta, (const int2 *)p.desc,
+                             p.num_heads, (int)chunk_bound, static_cast<unsigned char *>(records), p.status, p.o != nullptr,
                              p.scalar_gate);
     if (err != cudaSuccess) return err;
     if (mid && (err = cudaEventRecord(mid, p.stream)) != cudaSuccess) return err;

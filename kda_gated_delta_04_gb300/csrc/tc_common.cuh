@@ -373,6 +373,17 @@ __device__ __forceinline__ void solve_ut_core(unsigned char *sm)
     __syncthreads();
 }
 
+// Sum of a float4 over the two lanes of an adjacent pair (lane ^ 1); every lane of the
+// warp takes part.
+__device__ __forceinline__ float4 add_pair_lanes(float4 a)
+{
+    a.x += __shfl_xor_sync(0xffffffffu, a.x, 1);
+    a.y += __shfl_xor_sync(0xffffffffu, a.y, 1);
+    a.z += __shfl_xor_sync(0xffffffffu, a.z, 1);
+    a.w += __shfl_xor_sync(0xffffffffu, a.w, 1);
+    return a;
+}
+
 // solve_ut_doubling: the same T, in place (SOLVE_T == SOLVE_A), by recursive
 // doubling all the way from 4 x 4 blocks: the sixteen 4 x 4 diagonal blocks by
 // substitution, then for block size b = 4, 8, 16, 32 and every pair of b x b
@@ -443,18 +454,22 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm)
         }
     }
     __syncthreads();
-    // 2. The 16 and 32 levels across the CTA.
+    // 2. The 16 and 32 levels across the CTA.  Where a level has fewer output quads than
+    //    the CTA has threads, two adjacent lanes share a quad: each takes every other
+    //    group of four m and a shuffle adds the halves.
 #pragma unroll
     for (int b = 16; b <= 32; b *= 2) {
         const int quads = b / 4, items = 32 * quads;
+        const int P = NT >= 2 * items ? 2 : 1;  // threads per output quad (warp-uniform loops)
         // X = A_10 T_00: a warp shares one column quad cq over the 32 rows of X, so
         // the loop can start at m = cq (T_00[m][cq..cq+3] = 0 for m < cq); A is read
         // four m at a time (rows 272 bytes apart: conflict-free float4 loads)
-        for (int e = tid; e < items; e += NT) {
+        for (int it = tid; it < items * P; it += NT) {
+            const int e = it / P, half = it % P;
             const int xr = e & 31, cq = (e >> 5) * 4, p = xr / b, rr = xr % b;
             const int R0 = 2 * b * p + b, C0 = 2 * b * p;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int m4 = cq; m4 < b; m4 += 4) {
+            for (int m4 = cq + 4 * half; m4 < b; m4 += 4 * P) {
                 const float4 a = *reinterpret_cast<const float4 *>(sT + (R0 + rr) * kLdS + C0 + m4);
                 const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
@@ -463,16 +478,18 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm)
                     acc.x += av[u] * t.x; acc.y += av[u] * t.y; acc.z += av[u] * t.z; acc.w += av[u] * t.w;
                 }
             }
-            *reinterpret_cast<float4 *>(sX + xr * kLdX + cq) = acc;
+            if (P == 2) acc = add_pair_lanes(acc);
+            if (half == 0) *reinterpret_cast<float4 *>(sX + xr * kLdX + cq) = acc;
         }
         __syncthreads();
         // T_10 = -T_11 X over A_10: row rr needs m <= rr only (T_11 is lower triangular);
         // a warp covers few consecutive rows, so its trip counts stay close
-        for (int e = tid; e < items; e += NT) {
+        for (int it = tid; it < items * P; it += NT) {
+            const int e = it / P, half = it % P;
             const int xr = e / quads, cq = (e % quads) * 4, p = xr / b, rr = xr % b;
             const int R0 = 2 * b * p + b, C0 = 2 * b * p;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int m4 = 0; m4 <= rr; m4 += 4) {
+            for (int m4 = 4 * half; m4 <= rr; m4 += 4 * P) {
                 const float4 t = *reinterpret_cast<const float4 *>(sT + (R0 + rr) * kLdS + R0 + m4);
                 const float tv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
@@ -481,8 +498,10 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm)
                     acc.x += tv[u] * x.x; acc.y += tv[u] * x.y; acc.z += tv[u] * x.z; acc.w += tv[u] * x.w;
                 }
             }
-            *reinterpret_cast<float4 *>(sT + (R0 + rr) * kLdS + C0 + cq) =
-                make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
+            if (P == 2) acc = add_pair_lanes(acc);
+            if (half == 0)
+                *reinterpret_cast<float4 *>(sT + (R0 + rr) * kLdS + C0 + cq) =
+                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
     }
