@@ -112,63 +112,75 @@ seqsplit_plan_kernel(const int32_t *__restrict__ cu, const int32_t *__restrict__
     for (int e = threadIdx.x; e < H * kD / 2; e += blockDim.x) z[e] = 0u;
 }
 
-// One CTA per (32-column slice, head, sequence): the start state of every segment,
+// One CTA per (8-column slice, head, sequence): the start state of every segment,
 // S_start(0) = the sequence's initial state, S_start(k + 1) = M_k S_start(k) + R_k (fp32).
-constexpr int kCombThreads = 256, kSlice = 32;
+// M_k is staged transposed in shared memory (a warp loads 32 rows of one column quad, so
+// the transposing stores are conflict-free) while the registers already hold M_{k+1}'s
+// loads in flight.  Thread: rows 4ib .. 4ib + 3 of column j.
+constexpr int kCombThreads = 256, kCols = 8;
 __global__ void __launch_bounds__(kCombThreads)
 seqsplit_combine_kernel(SeqSplit s, const float *init_state, int H)
 {
-    __shared__ __align__(16) float S[kD][kSlice];
-    const int j0 = blockIdx.x * kSlice, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
-    const int v0 = s.seg_first[n], nseg = s.seg_first[n + 1] - v0;
+    extern __shared__ __align__(16) float comb_smem[];
+    float *MT = comb_smem;            // [kD][kD]: MT[m][i] = M[i][m]
+    float *S = comb_smem + kD * kD;   // [kD][kCols]
+    const int j0 = blockIdx.x * kCols, h = blockIdx.y, n = blockIdx.z, tid = threadIdx.x;
+    const int v0 = s.seg_first[n];
+    const int nseg = min(s.seg_first[n + 1], s.seg_first[gridDim.z]) - v0;
     const int si = s.init_src[n];
     const size_t entry = (size_t)H * kD * kD, head = (size_t)h * kD * kD;
-    for (int e = tid; e < kD * kSlice / 4; e += kCombThreads) {
-        const int i = e / (kSlice / 4), j4 = (e % (kSlice / 4)) * 4;
-        float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (init_state && si >= 0) x = *reinterpret_cast<const float4 *>(init_state + si * entry + head + (size_t)i * kD + j0 + j4);
-        *reinterpret_cast<float4 *>(&S[i][j4]) = x;
-        if (nseg > 0) *reinterpret_cast<float4 *>(s.start + v0 * entry + head + (size_t)i * kD + j0 + j4) = x;
+    const int ib = tid >> 3, j = tid & 7;          // compute: rows 4ib.., column j
+    const int li = tid & 31, lq = tid >> 5;        // staging: row li + 32 (r & 3), quad lq + 8 (r >> 2)
+    for (int e = tid; e < kD * kCols; e += kCombThreads) {
+        const int i = e / kCols, c = e % kCols;
+        const float x = (init_state && si >= 0) ? init_state[si * entry + head + (size_t)i * kD + j0 + c] : 0.f;
+        S[i * kCols + c] = x;
+        if (nseg > 0) s.start[v0 * entry + head + (size_t)i * kD + j0 + c] = x;
     }
-    __syncthreads();
-    // thread: row i, 16 columns c0 .. c0 + 15 of the slice
-    const int i = tid >> 1, c0 = (tid & 1) * 16;
+    float4 mr[16];
+    auto load_m = [&](size_t v) {
+        const float *Mv = s.M + v * entry + head;
+#pragma unroll
+        for (int r = 0; r < 16; ++r)
+            mr[r] = *reinterpret_cast<const float4 *>(Mv + (size_t)(li + 32 * (r & 3)) * kD + 4 * (lq + 8 * (r >> 2)));
+    };
+    if (nseg > 1) load_m((size_t)v0);
     for (int k = 0; k + 1 < nseg; ++k) {
         const size_t v = (size_t)(v0 + k);
-        const float *Mi = s.M + v * entry + head + (size_t)i * kD;
-        const float *Ri = s.R + v * entry + head + (size_t)i * kD + j0 + c0;
-        float acc[16];
+        __syncthreads();  // the previous step has finished reading MT and S
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const float4 r = *reinterpret_cast<const float4 *>(Ri + 4 * q);
-            acc[4 * q] = r.x; acc[4 * q + 1] = r.y; acc[4 * q + 2] = r.z; acc[4 * q + 3] = r.w;
+        for (int r = 0; r < 16; ++r) {
+            const int i = li + 32 * (r & 3), m = 4 * (lq + 8 * (r >> 2));
+            MT[(m + 0) * kD + i] = mr[r].x;
+            MT[(m + 1) * kD + i] = mr[r].y;
+            MT[(m + 2) * kD + i] = mr[r].z;
+            MT[(m + 3) * kD + i] = mr[r].w;
         }
-        for (int m4 = 0; m4 < kD; m4 += 4) {
-            const float4 a = *reinterpret_cast<const float4 *>(Mi + m4);
-            const float av[4] = {a.x, a.y, a.z, a.w};
+        if (k + 2 < nseg) load_m(v + 1);  // in flight during this step's products
+        float acc[4];
+        const float *Rv = s.R + v * entry + head + j0 + j;
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    const float4 b = *reinterpret_cast<const float4 *>(&S[m4 + u][c0 + 4 * q]);
-                    acc[4 * q] = fmaf(av[u], b.x, acc[4 * q]);
-                    acc[4 * q + 1] = fmaf(av[u], b.y, acc[4 * q + 1]);
-                    acc[4 * q + 2] = fmaf(av[u], b.z, acc[4 * q + 2]);
-                    acc[4 * q + 3] = fmaf(av[u], b.w, acc[4 * q + 3]);
-                }
-            }
+        for (int q = 0; q < 4; ++q) acc[q] = Rv[(size_t)(4 * ib + q) * kD];
+        __syncthreads();
+#pragma unroll 8
+        for (int m = 0; m < kD; ++m) {
+            const float4 a = *reinterpret_cast<const float4 *>(MT + m * kD + 4 * ib);
+            const float b = S[m * kCols + j];
+            acc[0] = fmaf(a.x, b, acc[0]);
+            acc[1] = fmaf(a.y, b, acc[1]);
+            acc[2] = fmaf(a.z, b, acc[2]);
+            acc[3] = fmaf(a.w, b, acc[3]);
         }
         __syncthreads();  // every thread has read S_start(k)
-        float *dst = s.start + (v + 1) * entry + head + (size_t)i * kD + j0 + c0;
+        float *dst = s.start + (v + 1) * entry + head + j0 + j;
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const float4 x = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
-            *reinterpret_cast<float4 *>(&S[i][c0 + 4 * q]) = x;
-            *reinterpret_cast<float4 *>(dst + 4 * q) = x;
+            S[(4 * ib + q) * kCols + j] = acc[q];
+            dst[(size_t)(4 * ib + q) * kD] = acc[q];
         }
-        __syncthreads();
     }
 }
+constexpr size_t kCombSmem = (size_t)(kD * kD + kD * kCols) * sizeof(float);
 
 }  // namespace
 
@@ -242,8 +254,18 @@ cudaError_t launch_seqsplit_plan(const PrefillProblem &p)
 
 cudaError_t launch_seqsplit_combine(const PrefillProblem &p)
 {
-    dim3 grid(kD / kSlice, p.num_heads, p.num_seqs);
-    seqsplit_combine_kernel<<<grid, kCombThreads, 0, p.stream>>>(p.split, p.init_state, p.num_heads);
+    static int configured_device = -1;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (configured_device != dev) {
+        err = cudaFuncSetAttribute(seqsplit_combine_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)kCombSmem);
+        if (err != cudaSuccess) return err;
+        configured_device = dev;
+    }
+    dim3 grid(kD / kCols, p.num_heads, p.num_seqs);
+    seqsplit_combine_kernel<<<grid, kCombThreads, kCombSmem, p.stream>>>(p.split, p.init_state, p.num_heads);
     return cudaGetLastError();
 }
 
