@@ -477,3 +477,69 @@ def test_sequence_split_long_context_few_heads_sampled():
     o_ref, fs_ref = oracle_prefill(sub)
     assert_parity(synth.to_f64(o[:, 2:3]), synth.to_f64(fs[:, 2:3]), o_ref, fs_ref, "bf16",
                   "split T=65536 H=4 head 2")
+
+
+def test_options_together_on_a_split_problem():
+    """Scalar gate, in-kernel q/k normalisation, a state pool with a discarded final state
+    (slot -1) and the sequence-split pass in one call (H = 2, ragged lengths): the outputs
+    are bit for bit those of the same options on a dense call, the discarded sequence's
+    slot is untouched, and the stored states are within the bar of the oracle run on the
+    broadcast gate and fp64-normalised q, k."""
+    H = 2
+    w = PrefillWorkload("options_split", 135, H, 128, "bf16", (1500, 900, 40), 3, init_state=True,
+                        raw_qk=True)
+    inp = synth.prefill_inputs(w)
+    la_s, la_full = _scalar_gate(inp, 135)
+    dev = to_device(inp)
+    la_d = la_s.cuda()
+    pool = torch.full((5, H, 128, 128), 0.25, dtype=torch.float32)
+    pool[4] = inp["init_state"][0]
+    pool[3] = inp["init_state"][2]
+    pool_before = pool.clone()
+    pool_d = pool.cuda()
+    init_h, final_h = [4, -1, 3], [0, -1, 3]  # sequence 1: from zero, final state discarded
+    o_p = kda.prefill_slots(dev["q"], dev["k"], dev["v"], la_d, dev["beta"], dev["cu_seqlens"], pool_d,
+                            torch.tensor(final_h, dtype=torch.int32, device="cuda"),
+                            torch.tensor(init_h, dtype=torch.int32, device="cuda"), check_status=True,
+                            qk_l2norm=True)
+    init_dense = inp["init_state"].clone()
+    init_dense[1] = 0.0
+    o_d, fs_d = kda.prefill(dev["q"], dev["k"], dev["v"], la_d, dev["beta"], dev["cu_seqlens"],
+                            init_dense.cuda(), check_status=True, qk_l2norm=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(synth.to_f64(o_p), synth.to_f64(o_d))
+    np.testing.assert_array_equal(synth.to_f64(pool_d[0].cpu()), synth.to_f64(fs_d[0].cpu()))
+    np.testing.assert_array_equal(synth.to_f64(pool_d[3].cpu()), synth.to_f64(fs_d[2].cpu()))
+    for s in (1, 2, 4):
+        assert torch.equal(pool_d[s].cpu(), pool_before[s])
+    ref = dict(inp)
+    ref["log_alpha"] = la_full
+    ref["init_state"] = init_dense
+    ref["q"] = oracle.l2_normalize(synth.to_f64(inp["q"]))
+    ref["k"] = oracle.l2_normalize(synth.to_f64(inp["k"]))
+    o_ref, fs_ref = oracle_prefill(ref)
+    assert_parity(synth.to_f64(o_p), synth.to_f64(fs_d), o_ref, fs_ref, "bf16", "options together, split")
+
+
+def test_split_prefill_into_a_pool_then_paged_decode():
+    """A long prompt with few heads goes through the sequence-split pass straight into a
+    state pool; paged decode continues from it within the bar of the oracle."""
+    H = 2
+    w = PrefillWorkload("handoff_split", 136, H, 128, "bf16", (2500,), 1, init_state=False)
+    inp = synth.prefill_inputs(w)
+    dev = to_device(inp)
+    pool_d = torch.zeros((3, H, 128, 128), dtype=torch.float32, device="cuda")
+    f_slots = torch.tensor([2], dtype=torch.int32, device="cuda")
+    kda.prefill_slots(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"], dev["cu_seqlens"], pool_d,
+                      f_slots, check_status=True, outputs=False)
+    _, fs_ref = oracle_prefill(inp)
+    ref_state = fs_ref.copy()
+    dw = synth.DecodeWorkload("handoff_split_decode", 137, 1, H, 128, "bf16", 4)
+    for s in range(dw.steps):
+        x = synth.decode_inputs(dw, s)
+        o = kda.decode_step_slots(*(x[k].cuda() for k in ("q", "k", "v", "log_alpha", "beta")), pool_d, f_slots)
+        torch.cuda.synchronize()
+        r = {k: synth.to_f64(t) for k, t in x.items()}
+        o_ref, _ = oracle.decode_step(r["q"], r["k"], r["v"], r["log_alpha"], r["beta"], ref_state)
+        assert maxabs(synth.to_f64(o), o_ref) <= TOL["bf16"]["o"]
+    assert relF(synth.to_f64(pool_d[2:3].cpu()), ref_state) <= TOL["bf16"]["state"]
