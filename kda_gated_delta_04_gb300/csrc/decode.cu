@@ -22,13 +22,17 @@
 namespace kda {
 namespace {
 
-template <int D, typename IO>
+// SCALAR: log_alpha holds one value per unit (scalar gate); QKN: q, k arrive raw and are
+// L2-normalised here.  Both are template parameters so that the plain kernel carries
+// none of their code.
+template <int D, typename IO, bool SCALAR, bool QKN>
 __global__ void __launch_bounds__(256, 2)
 decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__restrict__ v,
               const float *__restrict__ log_alpha, const float *__restrict__ beta,
               float *__restrict__ state, IO *__restrict__ o, const int32_t *__restrict__ slots,
-              int H, int num_slots, uint32_t *errors, bool scalar_gate, bool qk_norm)
+              int H, int num_slots, uint32_t *errors)
 {
+    constexpr bool scalar_gate = SCALAR, qk_norm = QKN;
     constexpr int TPR = D / 4;      // threads per state row
     constexpr int RPP = 256 / TPR;  // rows per pass
     constexpr int P = D / RPP;      // rows per thread
@@ -107,15 +111,20 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
     }
 }
 
+template <int D, typename IO, bool SCALAR, bool QKN>
+cudaError_t launch_v(const DecodeProblem &p)
+{
+    const int units = p.batch * p.num_heads;
+    decode_kernel<D, IO, SCALAR, QKN><<<units, 256, 0, p.stream>>>(
+        static_cast<const IO *>(p.q), static_cast<const IO *>(p.k), static_cast<const IO *>(p.v),
+        p.log_alpha, p.beta, p.state, static_cast<IO *>(p.o), p.slots, p.num_heads, p.num_slots, p.errors);
+    return cudaGetLastError();
+}
 template <int D, typename IO>
 cudaError_t launch(const DecodeProblem &p)
 {
-    const int units = p.batch * p.num_heads;
-    decode_kernel<D, IO><<<units, 256, 0, p.stream>>>(
-        static_cast<const IO *>(p.q), static_cast<const IO *>(p.k), static_cast<const IO *>(p.v),
-        p.log_alpha, p.beta, p.state, static_cast<IO *>(p.o), p.slots, p.num_heads, p.num_slots, p.errors,
-        p.scalar_gate, p.qk_l2norm);
-    return cudaGetLastError();
+    if (p.scalar_gate) return p.qk_l2norm ? launch_v<D, IO, true, true>(p) : launch_v<D, IO, true, false>(p);
+    return p.qk_l2norm ? launch_v<D, IO, false, true>(p) : launch_v<D, IO, false, false>(p);
 }
 
 }  // namespace
