@@ -41,7 +41,8 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
     const int c4 = tid % TPR;
     const int r0 = tid / TPR;
 
-    __shared__ float s_a[D], s_k[D], s_q[D], s_d[D];
+    __shared__ float s_a[D], s_k[D], s_q[D];
+    __shared__ __align__(16) float s_d[D];  // read as float4
     __shared__ __align__(16) float s_rk[RPP][D];
     __shared__ __align__(16) float s_rq[RPP][D];
 
