@@ -397,6 +397,9 @@ def run_gpu(args):
         if do_prefill:
             step_ms, stage_ms = g.time_prefill(args.steps, args.warmup, barrier)
             e2e_ms = g.time_prefill_e2e(args.steps, args.warmup)
+            # the prefill kernels' tensor-core product groups on their own (resident operands)
+            phase_tflops = {name: g.kda.diag_tensor_phases(i, 2000, g.ws)
+                            for i, name in enumerate(("chunk_kernel_products", "state_kernel_products"))}
         if do_decode:
             dec_ms = g.time_decode(g.dw.steps, max(3, args.warmup), barrier)
         if do_long:
@@ -440,6 +443,12 @@ def run_gpu(args):
                                   "algorithmic_bytes_per_launch": alg_bytes,
                                   "tensor_frac_of_bf16_peak": prefill_flops(T, H, d) /
                                   (mean_step_ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
+                         "gemm_phases": dict(
+                             {name: {"achieved": tf, "unit": "TFLOP/s", "peak": peaks["bf16_tflops"],
+                                     "frac": tf / peaks["bf16_tflops"]} for name, tf in phase_tflops.items()},
+                             note="kda_diag_tensor_phases: each kernel's product groups issued back to back by "
+                                  "its own issue routines on operands resident in shared memory (executed "
+                                  "FLOPs, bf16/fp16 inputs, fp32 accumulate), 2000 repetitions per CTA"),
                          "note": "kernel durations from the four CUDA events kda_prefill_events "
                                  "records on the launching stream around its kernels (a separate "
                                  "timed pass); the dominant (longest) kernel is measured against "

@@ -312,6 +312,23 @@ kda_status_t kda_prefill_no_alloc(const void *q, const void *k, const void *v,
  */
 kda_status_t kda_selftest_bounded_wait(void *workspace, uint64_t limit_ns, void *stream);
 
+/*
+ * Measurement only (no counterpart on the pages): the tensor-core product groups of one
+ * two-kernel-path prefill kernel, issued back to back by the kernel's own issue routines
+ * on a constant operand image resident in shared memory, with no epilogues, no waits
+ * between groups and no global traffic.  It isolates how fast the tensor pipe runs the
+ * prefill's GEMM phases, apart from the work between them.
+ *  pass  0: the chunk kernel's groups of one (chunk, head) item (k-k and q-k, W, P2, the
+ *           three-term P, N, Q''), 9,961,472 executed FLOP per repetition, two CTAs per SM;
+ *        1: the state kernel's chain and output groups of one chunk and 32-column value
+ *           slice (P V, N S, P2 V, Q' S), 2,359,296 FLOP per repetition, one CTA per SM
+ *  reps      repetitions per CTA, 1 .. 2^20
+ *  workspace 256-byte aligned device memory of at least 4 bytes (status word, cleared)
+ *  tflops    receives the executed TFLOP/s over the whole GPU (CUDA events on `stream`)
+ * Synchronises `stream`.  KDA_ERR_TIMEOUT if a bounded wait gave up.
+ */
+kda_status_t kda_diag_tensor_phases(int32_t pass, int32_t reps, void *workspace, void *stream, double *tflops);
+
 /* Static, human-readable name of a status code (never NULL). */
 const char *kda_status_string(kda_status_t status);
 

@@ -103,6 +103,9 @@ size_t prefill_split_records_bytes(int64_t total_tokens, int num_seqs, int num_h
 cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records,
                                  cudaEvent_t mid = nullptr);
 cudaError_t launch_decode(const DecodeProblem &p);
+// Measurement only: the tensor-core product groups of the chunk kernel (pass 0) or the state
+// kernel (pass 1) back to back on resident operands; synchronises `stream`; executed TFLOP/s.
+cudaError_t diag_tensor_phases(int pass, int reps, uint32_t *status, cudaStream_t stream, double *tflops);
 // Sequence-split state pass: segment length for a problem shape (0: no split), the bound on
 // its segment count, the workspace it needs, and its two small kernels (segment tables after
 // the schedule kernel; start states after the transition pass).

@@ -465,6 +465,33 @@ constexpr int kStateWarps = 16, kChainWarp = 16, kCopyWarp = 17, kOutWarp = 18;
 constexpr int kStateThreads = 19 * 32;
 constexpr int kL2Ahead = 3;  // records brought into L2 this many chunks ahead
 
+// The chain group of one chunk: P V (fp16) + N S_c (bf16) into the M = 128 accumulator.
+// dr, dv, ds: descriptors of the record, the V^T image and the S^T image in use.
+__device__ __forceinline__ void issue_chain(uint32_t acc, uint64_t dr, uint64_t dv, uint64_t ds)
+{
+#pragma unroll
+    for (int s = 0; s < 4; ++s)  // P V (fp16)
+        mma_bf16(acc, dr + ((R_P + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_PV, s > 0);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {  // + N S_c (bf16)
+        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32, offs = (s >> 2) * 4096 + (s & 3) * 32;
+        mma_bf16(acc, dr + ((R_N + off) >> 4), ds + (offs >> 4), IDESC_NS, 1);
+    }
+}
+
+// The output group of one chunk: P2 V (fp16) + Q' S_c (bf16) into an M = 64 accumulator.
+__device__ __forceinline__ void issue_out(uint32_t acc, uint64_t dr, uint64_t dv, uint64_t ds)
+{
+#pragma unroll
+    for (int s = 0; s < 4; ++s)  // P2 V (fp16)
+        mma_bf16(acc, dr + ((R_P2 + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_P2V, s > 0);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {  // + Q' S_c (bf16)
+        const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32, offs = (s >> 2) * 4096 + (s & 3) * 32;
+        mma_bf16(acc, dr + ((R_Q + off) >> 4), ds + (offs >> 4), IDESC_QS, 1);
+    }
+}
+
 // The serial pass over the chunks of one (sequence, head, 32-column value slice),
 // as four roles that meet only at mbarriers (no block-wide barrier per chunk):
 //   bar_ready[c&1]  S_c and V_c (both written by the 16 state warps) are in shared memory
@@ -690,31 +717,10 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
                         const uint64_t dr = d_rec0 + st * (L::STAGE >> 4), dv = d_v0 + st * (4096 >> 4),
                                        ds = d_s0 + st * (8192 >> 4);
                         if (chain) {
-#pragma unroll
-                            for (int s = 0; s < 4; ++s)  // P V (fp16)
-                                mma_bf16(tmem + TM_5, dr + ((R_P + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_PV,
-                                         s > 0);
-#pragma unroll
-                            for (int s = 0; s < 8; ++s) {  // + N S_c (bf16)
-                                const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32,
-                                               offs = (s >> 2) * 4096 + (s & 3) * 32;
-                                mma_bf16(tmem + TM_5, dr + ((R_N + off) >> 4), ds + (offs >> 4), IDESC_NS, 1);
-                            }
+                            issue_chain(tmem + TM_5, dr, dv, ds);
                             mma_commit(&bar_s);
                         } else {
-                            if (o) {  // no output products when no outputs are wanted
-#pragma unroll
-                                for (int s = 0; s < 4; ++s)  // P2 V (fp16)
-                                    mma_bf16(tmem + TM_O + 32 * st, dr + ((R_P2 + s * 32) >> 4),
-                                             dv + ((s * 32) >> 4), IDESC_P2V, s > 0);
-#pragma unroll
-                                for (int s = 0; s < 8; ++s) {  // + Q' S_c (bf16)
-                                    const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32,
-                                                   offs = (s >> 2) * 4096 + (s & 3) * 32;
-                                    mma_bf16(tmem + TM_O + 32 * st, dr + ((R_Q + off) >> 4), ds + (offs >> 4),
-                                             IDESC_QS, 1);
-                                }
-                            }
+                            if (o) issue_out(tmem + TM_O + 32 * st, dr, dv, ds);  // none when no outputs are wanted
                             mma_commit(&bar_o[st]);  // also marks chunk c's operands as released
                         }
                     }
@@ -758,7 +764,113 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     if (warp == 0) tmem_dealloc(tmem, kStateTmem);
 }
 
+// ============================================================== product-group diagnostic
+// Measurement only.  The tensor-core product groups of one prefill kernel, issued back to
+// back `reps` times per CTA by the same routines the kernels use, on a constant operand
+// image resident in shared memory: no epilogues, no waits between groups, no global
+// traffic.  PASS 0: the chunk kernel's groups of one (chunk, head) item (k-k and q-k, W,
+// P2, the three-term P, N, Q''), two CTAs per SM as that kernel runs.  PASS 1: the state
+// kernel's chain and output groups of one chunk and 32-column slice, one CTA per SM.
+constexpr uint64_t kDiagFlops[2] = {
+    2ull * (128 * 64 * 128 + 64 * 128 * 64 + 64 * 64 * 64 + 3 * 128 * 64 * 64 + 128 * 128 * 64 + 64 * 128 * 64),
+    2ull * (128 * 32 * 64 + 128 * 32 * 128 + 64 * 32 * 64 + 64 * 32 * 128)};
+
+template <int PASS>
+__global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(int reps, uint32_t *status)
+{
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t bar, bar_drain;
+    __shared__ uint32_t tmem_holder;
+    constexpr uint32_t used = PASS == 0 ? ChunkLayout::USED : StateLayout::USED;
+    constexpr uint32_t cols = PASS == 0 ? kChunkTmem : kStateTmem;
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x;
+    // 0x3c00: 2^-7 as bf16, 1.0 as fp16; finite products and sums in every group
+    for (uint32_t e = tid; e < used / 16; e += blockDim.x)
+        reinterpret_cast<uint4 *>(sm)[e] = make_uint4(0x3c003c00u, 0x3c003c00u, 0x3c003c00u, 0x3c003c00u);
+    fence_proxy_async_smem();
+    if (tid == 0) {
+        mbar_init(&bar, 1);
+        mbar_init(&bar_drain, 1);
+        fence_mbar_init();
+    }
+    if (tid < 32) {
+        tmem_alloc(&tmem_holder, cols);
+        tmem_relinquish();
+    }
+    __syncthreads();
+    tc_fence_after_sync();
+    const uint32_t tmem = tmem_holder;
+    if (tid == 0) {
+        bool ok = true;
+        for (int r = 0; r < reps && ok; ++r) {
+            if (PASS == 0) {
+                issue_g1<ChunkLayout>(sb, tmem);
+                issue_w_p2<ChunkLayout>(sb, tmem, true);
+                issue_p<ChunkLayout>(sb, tmem);
+                issue_n_q<ChunkLayout>(sb, tmem, true);
+            } else {
+                const uint64_t dr = kdesc(sb), dv = kdesc(sb + StateLayout::VIMG), ds = kdesc(sb + StateLayout::O7);
+                issue_chain(tmem + TM_5, dr, dv, ds);
+                issue_out(tmem + TM_O, dr, dv, ds);
+            }
+            mma_commit(&bar);
+            ok = mbar_wait_ns(&bar, (uint32_t)(r & 1), kWaitNs);
+            tc_fence_after_sync();
+        }
+        if (!ok) {
+            atomicOr(status, DEV_ERR_TIMEOUT);
+            mma_commit(&bar_drain);  // every MMA issued so far completes before the drain barrier
+            (void)mbar_wait_ns(&bar_drain, 0, kWaitNs);
+        }
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    if (tid < 32) tmem_dealloc(tmem, cols);
+}
+
+template <int PASS>
+cudaError_t run_tensor_phases(int reps, uint32_t *status, cudaStream_t stream, double *tflops)
+{
+    static int configured = -1, num_sms = 0;
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const int smem = PASS == 0 ? (int)kChunkSmem : (int)kStateSmem;
+    if (configured != dev) {
+        if ((err = cudaFuncSetAttribute(tensor_phase_kernel<PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        smem)) != cudaSuccess ||
+            (err = cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+            return err;
+        configured = dev;
+    }
+    const int grid = (PASS == 0 ? 2 : 1) * num_sms;
+    cudaEvent_t a, b;
+    if ((err = cudaEventCreate(&a)) != cudaSuccess) return err;
+    if ((err = cudaEventCreate(&b)) != cudaSuccess) { cudaEventDestroy(a); return err; }
+    err = cudaEventRecord(a, stream);
+    if (err == cudaSuccess) {
+        tensor_phase_kernel<PASS><<<grid, 256, smem, stream>>>(reps, status);
+        err = cudaGetLastError();
+    }
+    if (err == cudaSuccess) err = cudaEventRecord(b, stream);
+    if (err == cudaSuccess) err = cudaEventSynchronize(b);
+    float ms = 0.f;
+    if (err == cudaSuccess) err = cudaEventElapsedTime(&ms, a, b);
+    cudaEventDestroy(a);
+    cudaEventDestroy(b);
+    if (err == cudaSuccess) *tflops = (double)grid * reps * (double)kDiagFlops[PASS] / (ms * 1e9);
+    return err;
+}
+
 }  // namespace
+
+cudaError_t diag_tensor_phases(int pass, int reps, uint32_t *status, cudaStream_t stream, double *tflops)
+{
+    return pass == 0 ? run_tensor_phases<0>(reps, status, stream, tflops)
+                     : run_tensor_phases<1>(reps, status, stream, tflops);
+}
 
 size_t prefill_split_records_bytes(int64_t total_tokens, int num_seqs, int num_heads)
 {

@@ -1,8 +1,10 @@
-// selftest.cu -- kda_selftest_bounded_wait: exercises the kernels' failure path
-// on the device without a fault.  The pages have no counterpart; it checks the
-// library's own bounded waits: a wait on an mbarrier that nothing ever arrives
-// on must give up after its limit, record KDA_DEVICE_ERR_TIMEOUT in the status
-// word and return, leaving the context usable.
+// selftest.cu -- the library's diagnostics (the pages have no counterpart):
+//  kda_selftest_bounded_wait  exercises the kernels' failure path on the device without a
+//      fault: a wait on an mbarrier that nothing ever arrives on must give up after its
+//      limit, record KDA_DEVICE_ERR_TIMEOUT in the status word and return, leaving the
+//      context usable;
+//  kda_diag_tensor_phases     measures the prefill kernels' tensor-core product groups on
+//      their own (the kernel is in prefill_split.cu, beside the routines it reuses).
 #include "common.cuh"
 #include "sm100_ptx.cuh"
 
@@ -38,4 +40,23 @@ extern "C" kda_status_t kda_selftest_bounded_wait(void *workspace, uint64_t limi
     if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return KDA_ERR_CUDA;
     kda::bounded_wait_selftest_kernel<<<1, 64, 0, s>>>(static_cast<uint32_t *>(workspace), limit_ns);
     return cudaGetLastError() == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
+}
+
+extern "C" kda_status_t kda_diag_tensor_phases(int32_t pass, int32_t reps, void *workspace, void *stream,
+                                               double *tflops)
+{
+    if ((pass != 0 && pass != 1) || reps < 1 || reps > (1 << 20) || !tflops) return KDA_ERR_INVALID_ARG;
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return KDA_ERR_CUDA;
+    double t = 0.0;
+    if (kda::diag_tensor_phases(pass, reps, static_cast<uint32_t *>(workspace), s, &t) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+        cudaStreamSynchronize(s) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    if (word) return KDA_ERR_TIMEOUT;
+    *tflops = t;
+    return KDA_OK;
 }

@@ -46,6 +46,7 @@ EXPORTS = {
     "kda_prefill_events": (_c.c_int, _PREFILL_ARGS + [_c.POINTER(_VP), _c.c_int32]),
     "kda_selftest_bounded_wait": (_c.c_int, [_VP, _c.c_uint64, _VP]),
     "kda_prefill_ex": (_c.c_int, _PREFILL_ARGS + [_c.c_uint32]),
+    "kda_diag_tensor_phases": (_c.c_int, [_c.c_int32, _c.c_int32, _VP, _VP, _c.POINTER(_c.c_double)]),
     "kda_decode_step_ex": (_c.c_int, _DECODE_ARGS + [_c.c_uint32]),
     "kda_decode_step_slots": (_c.c_int, [_VP, _VP, _VP, _VP, _VP, _c.c_int32, _c.c_int32, _c.c_int32,
                                          _c.c_int32, _c.c_int, _VP, _c.c_int32, _VP, _VP, _VP, _VP,
@@ -141,6 +142,21 @@ def kda_prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_toke
     return lib().kda_prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens,
                                    num_heads, d_k, d_v, dtype, state_pool, num_slots, init_slots,
                                    final_slots, o, workspace, workspace_bytes, stream, flags)
+
+
+def kda_diag_tensor_phases(pass_, reps, workspace, stream, tflops):
+    return lib().kda_diag_tensor_phases(pass_, reps, workspace, stream, tflops)
+
+
+def diag_tensor_phases(pass_, reps, workspace, stream=None):
+    """Executed TFLOP/s of the chunk kernel's (pass_ = 0) or state kernel's (pass_ = 1)
+    tensor-core product groups run on their own (see include/kda.h)."""
+    out = _c.c_double(0.0)
+    st = lib().kda_diag_tensor_phases(pass_, reps, _ptr(workspace, "workspace"),
+                                      _stream_handle(stream, workspace.device), _c.byref(out))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_diag_tensor_phases")
+    return out.value
 
 
 def kda_selftest_bounded_wait(workspace, limit_ns, stream):

@@ -126,3 +126,13 @@ def test_slot_calls_reject_bad_arguments_on_host(kda):
     assert prefill_slots(flags=1 << 7) == 1             # unknown flag
     dec = [FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 128, 0, FAKE, 8, FAKE, FAKE, None, None]
     assert kda.kda_decode_step_slots(*dec, 1 << 7) == 1  # unknown flag
+
+
+def test_diag_tensor_phases_rejects_bad_arguments_on_host(kda):
+    import ctypes
+    out = ctypes.c_double(0.0)
+    assert kda.kda_diag_tensor_phases(2, 10, FAKE, None, ctypes.byref(out)) == 1    # no such pass
+    assert kda.kda_diag_tensor_phases(0, 0, FAKE, None, ctypes.byref(out)) == 1     # no repetition
+    assert kda.kda_diag_tensor_phases(0, 10, FAKE + 16, None, ctypes.byref(out)) == 1  # misaligned
+    assert kda.kda_diag_tensor_phases(1, 10, None, None, ctypes.byref(out)) == 1    # no workspace
+    assert kda.kda_diag_tensor_phases(0, 10, FAKE, None, None) == 1                 # no result

@@ -543,3 +543,12 @@ def test_split_prefill_into_a_pool_then_paged_decode():
         o_ref, _ = oracle.decode_step(r["q"], r["k"], r["v"], r["log_alpha"], r["beta"], ref_state)
         assert maxabs(synth.to_f64(o), o_ref) <= TOL["bf16"]["o"]
     assert relF(synth.to_f64(pool_d[2:3].cpu()), ref_state) <= TOL["bf16"]["state"]
+
+
+def test_tensor_phase_diagnostic_runs_clean():
+    """kda_diag_tensor_phases: both passes finish with a clean status word and a plausible
+    executed rate (above zero, below the nominal dense bf16 peak of the GPU with margin)."""
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    for p in (0, 1):
+        tf = kda.diag_tensor_phases(p, 50, ws)
+        assert 1.0 < tf < 3000.0, (p, tf)
