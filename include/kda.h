@@ -313,6 +313,50 @@ kda_status_t kda_prefill_no_alloc(const void *q, const void *k, const void *v,
 kda_status_t kda_selftest_bounded_wait(void *workspace, uint64_t limit_ns, void *stream);
 
 /*
+ * kda_prefill from host buffers, for a caller whose inputs and outputs live in host memory:
+ * the prompt is cut into up to four segments at chunk boundaries (64-token multiples from the
+ * start of the sequence a cut falls in; prompts under 2,048 tokens are not cut), and the
+ * host->device copies of later segments, the prefill of earlier ones and the device->host
+ * copies of their outputs overlap on two internal streams.  Because every chunk and every
+ * serial state step is the one kda_prefill would run, o and the final states are bit for bit
+ * those of kda_prefill_ex with the same flags on the same shape of problem per segment (with
+ * KDA_FLAG_NO_SEQ_SPLIT, or a problem too large for the sequence split, on every shape).
+ *  q, k, v, log_alpha, beta, o   host memory, the layouts of kda_prefill; page-locked
+ *                                memory lets the copies overlap (pageable memory works, slower)
+ *  cu_seqlens                    HOST int32 [num_seqs + 1] (checked on the host), or NULL for
+ *                                one sequence
+ *  init_state                    host [num_seqs, H, d, d] fp32, or NULL (zero)
+ *  final_state                   host [num_seqs, H, d, d] fp32, required
+ *  o                             may be NULL (final states only)
+ *  device_buffer, device_bytes   256-byte aligned device memory of at least
+ *                                kda_prefill_host_buffer_size(...) bytes; its first word
+ *                                collects the device-side errors of the call: read it with
+ *                                kda_read_device_status(device_buffer, stream)
+ *  flags                         KDA_FLAG_QK_L2NORM and KDA_FLAG_NO_SEQ_SPLIT
+ *                                (KDA_FLAG_SCALAR_GATE: KDA_ERR_UNSUPPORTED)
+ * Asynchronous on `stream`: the host buffers must stay valid, and the outputs unread, until
+ * the stream is synchronised.  Calls from several host threads are serialised while they
+ * enqueue.  Errors as kda_prefill; a cu_seqlens that is not a prefix sum from 0 to
+ * total_tokens is KDA_ERR_INVALID_ARG here (it is on the host).
+ */
+kda_status_t kda_prefill_host(const void *q, const void *k, const void *v, const float *log_alpha,
+                              const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                              int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                              kda_dtype_t dtype, const float *init_state, void *o, float *final_state,
+                              void *device_buffer, size_t device_bytes, void *stream, uint32_t flags);
+
+/* Device bytes kda_prefill_host needs for this problem (cu_seqlens on the host, or NULL for
+ * one sequence); 0 for invalid arguments. */
+size_t kda_prefill_host_buffer_size(const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                    int32_t num_heads, int32_t d_k, int32_t d_v, kda_dtype_t dtype);
+
+/* The segment boundaries kda_prefill_host uses: writes bounds[0] = 0 < ... < bounds[n] =
+ * total_tokens and returns n (0 for no tokens), or -1 for invalid arguments.  max_bounds
+ * must be at least 5. */
+int32_t kda_prefill_host_segments(const int32_t *cu_seqlens, int32_t num_seqs, int64_t total_tokens,
+                                  int64_t *bounds, int32_t max_bounds);
+
+/*
  * Measurement only (no counterpart on the pages): the tensor-core product groups of one
  * two-kernel-path prefill kernel, issued back to back by the kernel's own issue routines
  * on a constant operand image resident in shared memory, with no epilogues, no waits

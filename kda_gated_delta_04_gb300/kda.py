@@ -47,6 +47,10 @@ EXPORTS = {
     "kda_selftest_bounded_wait": (_c.c_int, [_VP, _c.c_uint64, _VP]),
     "kda_prefill_ex": (_c.c_int, _PREFILL_ARGS + [_c.c_uint32]),
     "kda_diag_tensor_phases": (_c.c_int, [_c.c_int32, _c.c_int32, _VP, _VP, _c.POINTER(_c.c_double)]),
+    "kda_prefill_host": (_c.c_int, _PREFILL_ARGS + [_c.c_uint32]),
+    "kda_prefill_host_buffer_size": (_c.c_size_t, [_VP, _c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
+                                                   _c.c_int32, _c.c_int]),
+    "kda_prefill_host_segments": (_c.c_int32, [_VP, _c.c_int32, _c.c_int64, _VP, _c.c_int32]),
     "kda_decode_step_ex": (_c.c_int, _DECODE_ARGS + [_c.c_uint32]),
     "kda_decode_step_slots": (_c.c_int, [_VP, _VP, _VP, _VP, _VP, _c.c_int32, _c.c_int32, _c.c_int32,
                                          _c.c_int32, _c.c_int, _VP, _c.c_int32, _VP, _VP, _VP, _VP,
@@ -142,6 +146,21 @@ def kda_prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_toke
     return lib().kda_prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens,
                                    num_heads, d_k, d_v, dtype, state_pool, num_slots, init_slots,
                                    final_slots, o, workspace, workspace_bytes, stream, flags)
+
+
+def kda_prefill_host(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k, d_v,
+                     dtype, init_state, o, final_state, device_buffer, device_bytes, stream, flags):
+    return lib().kda_prefill_host(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads,
+                                  d_k, d_v, dtype, init_state, o, final_state, device_buffer, device_bytes,
+                                  stream, flags)
+
+
+def kda_prefill_host_buffer_size(cu_seqlens, num_seqs, total_tokens, num_heads, d_k, d_v, dtype):
+    return lib().kda_prefill_host_buffer_size(cu_seqlens, num_seqs, total_tokens, num_heads, d_k, d_v, dtype)
+
+
+def kda_prefill_host_segments(cu_seqlens, num_seqs, total_tokens, bounds, max_bounds):
+    return lib().kda_prefill_host_segments(cu_seqlens, num_seqs, total_tokens, bounds, max_bounds)
 
 
 def kda_diag_tensor_phases(pass_, reps, workspace, stream, tflops):
@@ -303,6 +322,54 @@ def prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, state_pool, final_slots,
         if st != KDA_OK:
             raise KdaError(st, "kda_prefill_slots (device)")
     return o
+
+
+def _hptr(t, name, dtype=None):
+    """Address of a contiguous CPU tensor (None passes through)."""
+    torch = _torch()
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or t.is_cuda:
+        raise TypeError(f"{name} must be a CPU tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def prefill_host(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=None, final_state=None,
+                 device_buffer=None, device=None, stream=None, outputs=True, qk_l2norm=False, seq_split=True):
+    """kda_prefill_host: q, k, v, log_alpha, beta, cu_seqlens (int32), init_state and the outputs
+    in host memory (pin them for the copies to overlap with the prefill).  Returns (o, final_state)
+    as host tensors, valid once `stream` has been synchronised."""
+    torch = _torch()
+    T, H, d = q.shape
+    dt = _dtype_code(q)
+    N = 1 if cu_seqlens is None else cu_seqlens.numel() - 1
+    device = device or torch.device("cuda", torch.cuda.current_device())
+    if o is None and outputs:
+        o = torch.empty((T, H, v.shape[2]), dtype=q.dtype).pin_memory()
+    if not outputs:
+        o = None
+    if final_state is None:
+        final_state = torch.empty((N, H, d, v.shape[2]), dtype=torch.float32).pin_memory()
+    cu = _hptr(cu_seqlens, "cu_seqlens", torch.int32)
+    if device_buffer is None:
+        nbytes = kda_prefill_host_buffer_size(cu, N, T, H, d, v.shape[2], dt)
+        if nbytes == 0:
+            raise KdaError(KDA_ERR_INVALID_ARG, "kda_prefill_host_buffer_size")
+        device_buffer = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    st = kda_prefill_host(_hptr(q, "q", q.dtype), _hptr(k, "k", q.dtype), _hptr(v, "v", q.dtype),
+                          _hptr(log_alpha, "log_alpha", torch.float32), _hptr(beta, "beta", torch.float32),
+                          cu, N, T, H, d, v.shape[2], dt, _hptr(init_state, "init_state", torch.float32),
+                          _hptr(o, "o", q.dtype), _hptr(final_state, "final_state", torch.float32),
+                          _ptr(device_buffer, "device_buffer"),
+                          device_buffer.numel() * device_buffer.element_size(),
+                          _stream_handle(stream, device_buffer.device), _flags(log_alpha, qk_l2norm, seq_split))
+    if st != KDA_OK:
+        raise KdaError(st, "kda_prefill_host")
+    return o, final_state
 
 
 def decode_step_slots(q, k, v, log_alpha, beta, state_pool, slots, *, o=None, errors=None,

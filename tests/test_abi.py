@@ -136,3 +136,52 @@ def test_diag_tensor_phases_rejects_bad_arguments_on_host(kda):
     assert kda.kda_diag_tensor_phases(0, 10, FAKE + 16, None, ctypes.byref(out)) == 1  # misaligned
     assert kda.kda_diag_tensor_phases(1, 10, None, None, ctypes.byref(out)) == 1    # no workspace
     assert kda.kda_diag_tensor_phases(0, 10, FAKE, None, None) == 1                 # no result
+
+
+def _segments(kda, cu, N, T):
+    import ctypes
+    bounds = (ctypes.c_int64 * 8)()
+    arr = None if cu is None else (ctypes.c_int32 * len(cu))(*cu)
+    n = kda.kda_prefill_host_segments(None if arr is None else ctypes.addressof(arr), N, T,
+                                      ctypes.addressof(bounds), 8)
+    return n, [bounds[i] for i in range(max(n, 0) + 1)]
+
+
+@pytest.mark.parametrize("cu,T", [
+    (None, 4096), (None, 1500), (None, 2048), (None, 100000),
+    ([0, 700, 700, 3000, 3064, 3065, 9000], 9000), ([0, 5000], 5000), ([0, 1, 2, 3, 4096], 4096),
+])
+def test_host_prefill_segments_fall_on_chunk_boundaries(kda, cu, T):
+    """kda_prefill_host's cuts: at most four segments, strictly increasing from 0 to T, prompts
+    under 2,048 tokens uncut, and every cut a 64-token multiple from the start of the
+    sequence it falls in (so every chunk is the one a single kda_prefill runs)."""
+    N = 1 if cu is None else len(cu) - 1
+    n, b = _segments(kda, cu, N, T)
+    assert 1 <= n <= 4 and b[0] == 0 and b[n] == T
+    assert all(b[i] < b[i + 1] for i in range(n))
+    if T < 2048:
+        assert n == 1
+    starts = [0] if cu is None else cu[:-1]
+    for cut in b[1:n]:
+        start = max(s for s in starts if s <= cut)
+        assert (cut - start) % 64 == 0, (cut, start)
+
+
+def test_host_prefill_sizes_and_host_side_checks(kda):
+    import ctypes
+    assert kda.kda_prefill_host_buffer_size(None, 1, 4096, 32, 128, 128, 0) > 4096 * 32 * 128 * 2
+    assert kda.kda_prefill_host_buffer_size(None, 2, 4096, 32, 128, 128, 0) == 0    # cu_seqlens needed
+    assert kda.kda_prefill_host_buffer_size(None, 1, 4096, 32, 128, 64, 0) == 0     # d_k != d_v
+    n, _ = _segments(kda, None, 1, 0)
+    assert n == 0
+    bad_cu = (ctypes.c_int32 * 3)(0, 10, 9)                                           # not a prefix sum
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, ctypes.addressof(bad_cu), 2, 9, 2, 128, 128, 0, None, FAKE,
+            FAKE, FAKE, 1 << 30, None, 0]
+    assert kda.kda_prefill_host(*args) == 1
+    good_cu = (ctypes.c_int32 * 3)(0, 4, 9)
+    args[5] = ctypes.addressof(good_cu)
+    args[15] = FAKE + 16                                                              # misaligned buffer
+    assert kda.kda_prefill_host(*args) == 1
+    args[15] = FAKE
+    args[9], args[10] = 96, 96                                                        # unsupported d
+    assert kda.kda_prefill_host(*args) == 2

@@ -552,3 +552,42 @@ def test_tensor_phase_diagnostic_runs_clean():
     for p in (0, 1):
         tf = kda.diag_tensor_phases(p, 50, ws)
         assert 1.0 < tf < 3000.0, (p, tf)
+
+
+def _pinned(t):
+    return None if t is None else t.contiguous().pin_memory()
+
+
+HOST_CASES = [
+    ("bench_shape", synth.PREFILL_4K, True),
+    ("varlen_state", PrefillWorkload("host_varlen", 138, 2, 128, "bf16", (700, 0, 2300, 64, 1, 1900), 6,
+                                     init_state=True), False),
+    ("fp32_d64", PrefillWorkload("host_f32", 139, 2, 64, "f32", (3000, 500), 2, init_state=True), False),
+]
+
+
+@pytest.mark.parametrize("name,w,outputs", HOST_CASES, ids=[c[0] for c in HOST_CASES])
+def test_host_buffer_prefill_is_bit_for_bit_kda_prefill(name, w, outputs):
+    """kda_prefill_host (pinned host buffers, prompt cut at chunk boundaries into overlapped
+    segments) gives bit for bit the o and final states of one kda_prefill, with the sequence
+    split off in both (the segments are separate, smaller problems); state-only for varlen."""
+    inp = synth.prefill_inputs(w)
+    dev = to_device(inp)
+    o_d, fs_d = kda.prefill(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"], dev["cu_seqlens"],
+                            dev["init_state"], check_status=True, seq_split=False)
+    host = {k: _pinned(inp[k]) for k in ("q", "k", "v", "log_alpha", "beta", "init_state")}
+    buf = torch.empty(kda.kda_prefill_host_buffer_size(inp["cu_seqlens"].data_ptr(), len(w.seq_lens),
+                                                       inp["q"].shape[0], w.num_heads, w.d, w.d,
+                                                       kda.KDA_DTYPE_BF16 if w.dtype == "bf16" else kda.KDA_DTYPE_F32),
+                      dtype=torch.uint8, device="cuda")
+    o_h, fs_h = kda.prefill_host(host["q"], host["k"], host["v"], host["log_alpha"], host["beta"],
+                                 inp["cu_seqlens"], host["init_state"], device_buffer=buf, seq_split=False,
+                                 outputs=outputs)
+    torch.cuda.synchronize()
+    st = kda.kda_read_device_status(buf.data_ptr(), kda._stream_handle(None, buf.device))
+    assert st == kda.KDA_OK
+    np.testing.assert_array_equal(synth.to_f64(fs_h), synth.to_f64(fs_d.cpu()))
+    if outputs:
+        np.testing.assert_array_equal(synth.to_f64(o_h), synth.to_f64(o_d.cpu()))
+    else:
+        assert o_h is None
