@@ -11,9 +11,10 @@ is timed with and without the sequence-split state pass under "long_context".
 
 value    prefill tokens/s with inputs resident in HBM (CUDA events, L2 flushed
          between timed steps by writing a 256 MiB buffer, flush not timed);
-e2e      the same through the C ABI with pinned host buffers: host->device
-         copy of the step's inputs, kda_prefill, device->host copy of o and the
-         final state, all inside the timed region;
+e2e      the same through the C ABI from pinned host buffers (kda_prefill_host):
+         host->device copies of the step's inputs, the prefill and the device->host
+         copies of o and the final state, all inside the timed region (the library
+         overlaps the copies of later segments with the prefill of earlier ones);
 roofline HBM-bound, for the dominant (longest) kernel of the prefill: its share
          of the algorithmic bytes / its event-timed duration (four events that
          kda_prefill_events records around the kernels on the launching stream),
@@ -251,21 +252,29 @@ class _Gpu:
         return whole, stages
 
     def time_prefill_e2e(self, steps, warmup):
-        """Host-to-host: pinned inputs -> device, kda_prefill, o and final state -> host."""
-        torch = self.torch
+        """Host-to-host through kda_prefill_host: pinned inputs in, o and the final state out,
+        the copies of later segments overlapped with the prefill of earlier ones."""
+        torch, kda = self.torch, self.kda
         pin = {k: self.inp[k].pin_memory() for k in ("q", "k", "v", "log_alpha", "beta")}
+        cu_host = self.inp["cu_seqlens"].contiguous()
         o_host = torch.empty(self.o.shape, dtype=self.o.dtype).pin_memory()
         fs_host = torch.empty(self.fs.shape, dtype=self.fs.dtype).pin_memory()
         self.h2d = sum(t.numel() * t.element_size() for t in pin.values())
         self.d2h = (o_host.numel() * o_host.element_size() +
                     fs_host.numel() * fs_host.element_size())
+        nbytes = kda.kda_prefill_host_buffer_size(cu_host.data_ptr(), 1, self.T, self.H, self.d, self.d,
+                                                  kda.KDA_DTYPE_BF16)
+        dbuf = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
+        bounds = torch.zeros(8, dtype=torch.int64)  # kept alive across the call that fills it
+        self.e2e_launches = kda.kda_prefill_host_segments(cu_host.data_ptr(), 1, self.T, bounds.data_ptr(), 8) * 4
 
         def step():
-            for k_, t in pin.items():
-                self.x[k_].copy_(t, non_blocking=True)
-            self.prefill_call()
-            o_host.copy_(self.o, non_blocking=True)
-            fs_host.copy_(self.fs, non_blocking=True)
+            st = kda.kda_prefill_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(),
+                                      pin["log_alpha"].data_ptr(), pin["beta"].data_ptr(), cu_host.data_ptr(),
+                                      1, self.T, self.H, self.d, self.d, kda.KDA_DTYPE_BF16, None,
+                                      o_host.data_ptr(), fs_host.data_ptr(), dbuf.data_ptr(), nbytes, self.sh, 0)
+            if st != kda.KDA_OK:
+                raise kda.KdaError(st, "kda_prefill_host")
 
         for _ in range(warmup):
             step()
@@ -455,7 +464,11 @@ def run_gpu(args):
                                  "its share of the path's algorithmic bytes, the path (one "
                                  "kda_prefill between two events) against all of them"},
             "e2e": {"value": aggregate_rate(T, world, args.steps, e2e_total), "unit": "tokens/s",
-                    "h2d_bytes_per_step": g.h2d, "d2h_bytes_per_step": g.d2h},
+                    "h2d_bytes_per_step": g.h2d, "d2h_bytes_per_step": g.d2h,
+                    "call": "kda_prefill_host: pinned host buffers, the prompt cut into segments whose "
+                            "copies overlap the prefill of the segments before (results bit for bit "
+                            "those of kda_prefill)",
+                    "gpu_launches_per_step": g.e2e_launches},
             "gpu_launches": 3 * args.steps,  # schedule, chunk and state kernel per step
         })
     line["clocks"] = clocks.summary()
