@@ -265,8 +265,11 @@ class _Gpu:
         nbytes = kda.kda_prefill_host_buffer_size(cu_host.data_ptr(), 1, self.T, self.H, self.d, self.d,
                                                   kda.KDA_DTYPE_BF16)
         dbuf = torch.empty(nbytes, dtype=torch.uint8, device=self.dev)
-        bounds = torch.zeros(8, dtype=torch.int64)  # kept alive across the call that fills it
-        self.e2e_launches = kda.kda_prefill_host_segments(cu_host.data_ptr(), 1, self.T, bounds.data_ptr(), 8) * 4
+        bounds = torch.zeros(64, dtype=torch.int64)  # kept alive across the call that fills it
+        nseg = kda.kda_prefill_host_segments(cu_host.data_ptr(), 1, self.T, bounds.data_ptr(), 64)
+        if nseg < 1:
+            raise kda.KdaError(kda.KDA_ERR_INVALID_ARG, "kda_prefill_host_segments")
+        self.e2e_launches = 4 * nseg  # per segment: schedule, chunk, state kernel and the error word
 
         def step():
             st = kda.kda_prefill_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(),
