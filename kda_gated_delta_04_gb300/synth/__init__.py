@@ -179,8 +179,10 @@ def prefill_inputs(w: PrefillWorkload, seed: int = 0, heads=None, seqs=None):
         "beta": torch.empty((T, Hs), dtype=torch.float32),
     }
     full_heads = heads == list(range(H))
+    all_seqs = seqs == list(range(len(lens)))
     t_out = 0
-    for s in seqs:
+    # every sequence and head: one contiguous run of global rows (the same values, one call each)
+    for s in ([] if (full_heads and all_seqs) else seqs):
         t0, n = int(cu_full[s]), int(lens[s])
         if full_heads:
             # rows t*H + h for t in [t0, t0+n): one contiguous run
@@ -202,9 +204,21 @@ def prefill_inputs(w: PrefillWorkload, seed: int = 0, heads=None, seqs=None):
                 rows(NEG_SOFTPLUS, key[T_LOG_ALPHA], row0, step, nrows, D, scale=0.05)))
             put("beta", torch.from_numpy(rows(SIGMOID, key[T_BETA], row0, step, nrows, 1)))
         t_out += n
+    if full_heads and all_seqs and T > 0:
+        qk_kind = NORMAL if w.raw_qk else UNIT_ROWS
+        n_rows = T * H
+        out["q"].copy_(_qkv_rows(w.dtype, qk_kind, key[T_Q], 0, 1, n_rows, D).reshape(T, H, D))
+        out["k"].copy_(_qkv_rows(w.dtype, qk_kind, key[T_K], 0, 1, n_rows, D).reshape(T, H, D))
+        out["v"].copy_(_qkv_rows(w.dtype, NORMAL, key[T_V], 0, 1, n_rows, D).reshape(T, H, D))
+        out["log_alpha"].copy_(torch.from_numpy(
+            rows(NEG_SOFTPLUS, key[T_LOG_ALPHA], 0, 1, n_rows, D, scale=0.05)).reshape(T, H, D))
+        out["beta"].copy_(torch.from_numpy(rows(SIGMOID, key[T_BETA], 0, 1, n_rows, 1)).reshape(T, H))
     out["cu_seqlens"] = torch.from_numpy(
         np.concatenate([[0], np.cumsum(sel_lens)]).astype(np.int32))
-    if w.init_state:
+    if w.init_state and full_heads and all_seqs:  # rows (s * H + h) * D .. in order: one run
+        out["init_state"] = torch.from_numpy(
+            rows(NORMAL, key[T_STATE], 0, 1, len(seqs) * H * D, D, scale=0.02)).reshape(len(seqs), H, D, D)
+    elif w.init_state:
         st = torch.empty((len(seqs), Hs, D, D), dtype=torch.float32)
         for a, s in enumerate(seqs):
             for b, h in enumerate(heads):

@@ -97,3 +97,4 @@ def test_rounding_budget_of_the_folded_form():
                        kernel_rounding=True)
     assert np.linalg.norm(f - f_ref[0, 0]) / np.linalg.norm(f_ref[0, 0]) < 7e-4
     assert np.abs(o - o_ref[:, 0]).max() < 2e-3
+

@@ -591,3 +591,18 @@ def test_host_buffer_prefill_is_bit_for_bit_kda_prefill(name, w, outputs):
         np.testing.assert_array_equal(synth.to_f64(o_h), synth.to_f64(o_d.cpu()))
     else:
         assert o_h is None
+
+
+def test_maximum_sequence_count():
+    """65,535 sequences (the grid limit) of 0, 1 and 2 tokens at H = 1: past the sorted-schedule
+    limit, every packed chunk a one- or two-token tail, zero-length sequences in between.  All
+    outputs and final states against the oracle."""
+    lens = tuple(i % 3 for i in range(65535))
+    w = PrefillWorkload("max_seqs", 140, 1, 128, "bf16", lens, len(lens), init_state=True)
+    inp = synth.prefill_inputs(w)
+    d = to_device(inp)
+    o, fs = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"],
+                        check_status=True)
+    torch.cuda.synchronize()
+    o_ref, fs_ref = oracle_prefill(inp)
+    assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, "bf16", "65,535 sequences")
