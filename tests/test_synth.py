@@ -1,5 +1,6 @@
 """The seeded input generator: its whole-problem path against unit-by-unit generation."""
 
+
 def test_generator_full_problem_equals_unit_by_unit_generation():
     """The input generator's one-run path (all sequences, all heads) gives exactly the values
     generating each sequence, or each head, on its own gives: the sampled parity tests
