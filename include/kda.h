@@ -315,7 +315,8 @@ kda_status_t kda_selftest_bounded_wait(void *workspace, uint64_t limit_ns, void 
 /*
  * kda_prefill from host buffers, for a caller whose inputs and outputs live in host memory:
  * the prompt is cut into up to four segments at chunk boundaries (64-token multiples from the
- * start of the sequence a cut falls in; prompts under 2,048 tokens are not cut), and the
+ * start of the sequence a cut falls in; prompts under 2,048 tokens are not cut; the last
+ * segment is about 1/16 of the prompt, so little follows the last upload), and the
  * host->device copies of later segments, the prefill of earlier ones and the device->host
  * copies of their outputs overlap on two internal streams.  Because every chunk and every
  * serial state step is the one kda_prefill would run, o and the final states are bit for bit

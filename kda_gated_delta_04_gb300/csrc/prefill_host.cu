@@ -28,6 +28,9 @@ size_t round256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Segment boundaries bounds[0] = 0 < ... < bounds[n] = total, each one at a 64-token multiple
 // from the start of the sequence it falls in.  cu: host [num_seqs + 1] (NULL: one sequence).
+// The host->device copies are the critical path and run back to back; what follows the last
+// one (that segment's prefill, the copies of its outputs and of the final states) is the only
+// exposed part, so the last segment gets 1/16 of the tokens and the others share the rest.
 int plan_segments(const int32_t *cu, int num_seqs, int64_t total, int64_t *bounds)
 {
     int n = 0;
@@ -35,7 +38,7 @@ int plan_segments(const int32_t *cu, int num_seqs, int64_t total, int64_t *bound
     int k = (int)(total / kMinSegmentTokens);
     if (k > kMaxSegments) k = kMaxSegments;
     for (int s = 1; s < k; ++s) {
-        const int64_t t = total * s / k;
+        const int64_t t = total * 15 * s / (16 * (k - 1));
         int64_t start = 0;  // start of the sequence holding token t
         if (cu) {
             int lo = 0, hi = num_seqs;  // cu[lo] <= t < cu[lo + 1]
