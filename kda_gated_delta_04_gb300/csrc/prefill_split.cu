@@ -315,9 +315,11 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     __shared__ float s_rn[2 * kC];  // reciprocal k, q row norms (NORM)
 
     // launched with programmatic stream serialization behind the schedule kernel:
-    // nothing that kernel writes (cc, the status word) is touched before pdl_wait
-    pdl_launch_dependents();  // the state kernel may be scheduled as SMs free up
+    // nothing that kernel writes (cc, the status word) is touched before pdl_wait.  The
+    // state kernel may be scheduled once every CTA is past this point, so it can read the
+    // schedule (complete by then) before it waits for this kernel's records.
     pdl_wait();
+    pdl_launch_dependents();
     // one CTA per (chunk, head), heads fastest, chunks last to first
     const int h = (int)(blockIdx.x % (unsigned)H);
     const int g = chunk_bound - 1 - (int)(blockIdx.x / (unsigned)H);
@@ -534,9 +536,10 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool state_warp = warp < kStateWarps;
     const int quarter = warp & 3, part = (warp >> 2) & 3;
-    // launched with programmatic stream serialization behind the chunk kernel: the
-    // schedule (order, cc) and the records are read only after pdl_wait
-    pdl_wait();
+    // launched with programmatic stream serialization behind the chunk kernel, which signals
+    // only once the schedule kernel is complete: the schedule (order, cc, descriptors), the
+    // initial states and the value rows are read at once, the records only after pdl_wait
+    // (the chunk kernel's completion), so this prologue overlaps that kernel's last CTAs
     const bool ident = (int)blockIdx.z >= z_ident;
     const int j0 = blockIdx.x * kDV, h = blockIdx.y, n = order[ident ? blockIdx.z - z_ident : blockIdx.z];
     int64_t t0, t1;
@@ -657,10 +660,13 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
 
     bool ok = true;
     if (copier) {
-        for (int k = 0; k < 2 && k < nchunks; ++k) load_record(k);
-        for (int k = 2; k < kL2Ahead && k < nchunks; ++k) bulk_prefetch_l2(rec0 + (size_t)k * rec_stride, kRecBytes);
         for (int k = 0; k < kVRing && k < nchunks; ++k) load_v(k);
         prefetch_tmap(tmv);
+    }
+    pdl_wait();  // the chunk kernel has completed: its records are visible
+    if (copier) {
+        for (int k = 0; k < 2 && k < nchunks; ++k) load_record(k);
+        for (int k = 2; k < kL2Ahead && k < nchunks; ++k) bulk_prefetch_l2(rec0 + (size_t)k * rec_stride, kRecBytes);
     }
     if (state_warp && nchunks > 0) {
         ok = convert_v(0);
