@@ -606,3 +606,44 @@ def test_maximum_sequence_count():
     torch.cuda.synchronize()
     o_ref, fs_ref = oracle_prefill(inp)
     assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, "bf16", "65,535 sequences")
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_randomized_problems(seed):
+    """Seeded random small problems mixing everything the prefill accepts: 1-3 heads, d = 64 or
+    128, bf16 or fp32, 1-6 ragged sequences (zero-length ones included), initial states or
+    none, the scalar gate, in-kernel q/k normalisation, state-only calls, the minimal or the
+    full workspace, with and without the sequence split.  Each against the oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    H = int(rng.integers(1, 4))
+    d = int(rng.choice([64, 128]))
+    dtype = str(rng.choice(["bf16", "f32"]))
+    N = int(rng.integers(1, 7))
+    lens = tuple(int(x) for x in rng.integers(0, 300, size=N))
+    if sum(lens) == 0:
+        lens = (1,) + lens[1:]
+    scalar, qkn, outputs = bool(rng.integers(2)), bool(rng.integers(2)), bool(rng.integers(2))
+    minimal_ws, split = bool(rng.integers(2)), bool(rng.integers(2))
+    w = PrefillWorkload(f"random_{seed}", 2000 + seed, H, d, dtype, lens, N, init_state=bool(rng.integers(2)),
+                        raw_qk=qkn)
+    inp = synth.prefill_inputs(w)
+    dev = to_device(inp)
+    la = dev["log_alpha"]
+    ref = dict(inp)
+    if scalar:
+        la_s, la_full = _scalar_gate(inp, 3000 + seed)
+        la, ref["log_alpha"] = la_s.cuda(), la_full
+    if qkn:
+        ref["q"] = oracle.l2_normalize(synth.to_f64(inp["q"]))
+        ref["k"] = oracle.l2_normalize(synth.to_f64(inp["k"]))
+    ws = torch.empty(kda.min_workspace_bytes(N), dtype=torch.uint8, device="cuda") if minimal_ws else None
+    o, fs = kda.prefill(dev["q"], dev["k"], dev["v"], la, dev["beta"], dev["cu_seqlens"], dev["init_state"],
+                        workspace=ws, check_status=True, outputs=outputs, qk_l2norm=qkn, seq_split=split)
+    torch.cuda.synchronize()
+    o_ref, fs_ref = oracle_prefill(ref)
+    label = f"random {seed}: H={H} d={d} {dtype} lens={lens} scalar={scalar} qkn={qkn} out={outputs} min_ws={minimal_ws}"
+    if outputs:
+        assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, dtype, label)
+    else:
+        assert o is None
+        assert_parity(np.zeros(1), synth.to_f64(fs), np.zeros(1), fs_ref, dtype, label)
