@@ -16,13 +16,15 @@
  * (ciyuanerhao.com), chapter 4: the gate has one value per key channel and
  * scales the key rows of S.  The 1/sqrt(d_k) output scale is this library's
  * definition (the pages state none).  q and k are expected to be L2-normalised
- * by the caller (the pages normalise them inside the layer, before this step).
+ * by the caller (the pages normalise them inside the layer, before this step),
+ * unless KDA_FLAG_QK_L2NORM asks the kernels to do it.
  *
  * Conventions shared by every call:
  *  - All tensor pointers are DEVICE pointers owned by the caller, row-major and
- *    contiguous (last dimension has stride 1), 16-byte aligned.  The library
- *    allocates no device memory and keeps no mutable global state besides
- *    cached device attributes.
+ *    contiguous (last dimension has stride 1), 16-byte aligned; kda_prefill_host
+ *    alone takes host buffers.  The library allocates no device memory; its only
+ *    global state is cached device attributes and, for kda_prefill_host, two
+ *    streams and a few events per device.
  *  - Calls are asynchronous on `stream` (a cudaStream_t passed as void*, NULL =
  *    the legacy default stream) and never synchronise, except
  *    kda_read_device_status.
@@ -67,10 +69,13 @@ typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_F32 = 1 } kda_dtype_t;
 /*
  * Bytes of device workspace for the fastest kda_prefill path on this problem.
  * For bf16 q/k/v at d_k = d_v = 128 that is the two-kernel tensor-core path: a
- * status word, a sequence schedule, the first chunk of each sequence and one
- * 74,240-byte record per (64-token chunk, head), at most
- * (total_tokens / 64 + num_seqs) * num_heads records (about 1.2 KB per token
- * per head).  For other shapes it equals KDA_PREFILL_MIN_WORKSPACE(num_seqs).
+ * status word, a sequence schedule, the first chunk of each sequence, one 8-byte
+ * descriptor per chunk and one 74,240-byte record per (64-token chunk, head), at
+ * most (total_tokens / 64 + num_seqs) * num_heads records (about 1.2 KB per
+ * token per head); when the problem has so few (sequence, head) units that the
+ * state pass runs in segments (KDA_FLAG_NO_SEQ_SPLIT), also three fp32 states
+ * per segment and head.  For other shapes it equals
+ * KDA_PREFILL_MIN_WORKSPACE(num_seqs).
  * Pure host arithmetic; returns 0 only for negative sizes.
  */
 #define KDA_PREFILL_MIN_WORKSPACE(num_seqs) \
