@@ -81,6 +81,17 @@ def prefill_flops(T, H, d, C=64):
     return T * H * (10 * C * d + 6 * d * d)
 
 
+def executed_tensor_flops(T, H, d, C=64):
+    """Tensor-core FLOPs the two-kernel path executes on one sequence of T tokens: per (chunk,
+    head) the chunk kernel's groups (k-k and q-k, W, P2, three-term P, N, Q'') and, per chunk and
+    each of the four 32-column value slices, the state kernel's groups (P V, N S, P2 V, Q' S)."""
+    chunks = -(-T // C)
+    chunk_groups = 2 * (128 * 64 * 128 + 64 * 128 * 64 + 64 * 64 * 64 + 3 * 128 * 64 * 64
+                        + 128 * 128 * 64 + 64 * 128 * 64)
+    state_groups = 2 * (128 * 32 * 64 + 128 * 32 * 128 + 64 * 32 * 64 + 64 * 32 * 128) * (d // 32)
+    return chunks * H * (chunk_groups + state_groups)
+
+
 def decode_algorithmic_bytes(B, H, d, io_bytes):
     return B * H * (2 * d * d * 4 + 3 * d * io_bytes + d * 4 + 4 + d * io_bytes)
 
@@ -348,27 +359,33 @@ class _Gpu:
         self.o_dec = torch.empty((dw.batch, dw.num_heads, dw.d), dtype=torch.bfloat16,
                                  device=self.dev)
 
-    def decode_call(self, s):
+    def decode_call(self, s, stream_handle=None):
         kda, dw, r = self.kda, self.dw, self.ring[s % len(self.ring)]
         st = kda.kda_decode_step(r["q"].data_ptr(), r["k"].data_ptr(), r["v"].data_ptr(),
                                  r["log_alpha"].data_ptr(), r["beta"].data_ptr(), dw.batch,
                                  dw.num_heads, dw.d, dw.d, kda.KDA_DTYPE_BF16,
-                                 self.state.data_ptr(), self.o_dec.data_ptr(), self.sh)
+                                 self.state.data_ptr(), self.o_dec.data_ptr(),
+                                 self.sh if stream_handle is None else stream_handle)
         if st != kda.KDA_OK:
             raise kda.KdaError(st, "kda_decode_step")
 
     def time_decode(self, steps, warmup, barrier):
-        """Event time (ms) of `steps` back-to-back in-place decode steps (the 537 MB state
-        is larger than L2, so no flush is needed between steps)."""
+        """Event time (ms) of `steps` in-place decode steps, captured once as a CUDA graph
+        of `steps` kernel launches and replayed (the 537 MB state is larger than L2, so no
+        flush is needed between steps)."""
         torch = self.torch
         for s in range(warmup):
             self.decode_call(s)
         torch.cuda.synchronize()
+        graph, side = torch.cuda.CUDAGraph(), torch.cuda.Stream(self.dev)
+        with torch.cuda.graph(graph, stream=side):
+            for s in range(steps):
+                self.decode_call(s, side.cuda_stream)
+        torch.cuda.synchronize()
         barrier()
         a, b = self.event(), self.event()
         a.record(self.stream)
-        for s in range(steps):
-            self.decode_call(s)
+        graph.replay()
         b.record(self.stream)
         torch.cuda.synchronize()
         barrier()
@@ -453,6 +470,8 @@ def run_gpu(args):
                          "kernels": kernels,
                          "path": {"achieved": achieved, "frac": achieved / peaks["hbm_gbs"],
                                   "algorithmic_bytes_per_launch": alg_bytes,
+                                  "algorithmic_flops_per_call": prefill_flops(T, H, d),
+                                  "executed_tensor_flops_per_call": executed_tensor_flops(T, H, d),
                                   "tensor_frac_of_bf16_peak": prefill_flops(T, H, d) /
                                   (mean_step_ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
                          "gemm_phases": dict(
@@ -485,6 +504,7 @@ def run_gpu(args):
             "metric": "KDA decode steps/s", "workload": dw.name,
             "value": aggregate_rate(1, world, dw.steps, dec_ms), "unit": "steps/s",
             "ms_per_step": dec_step_ms, "steps": dw.steps, "gpu_launches": dw.steps,
+            "timing": "one CUDA graph of the steps' launches, replayed once between two events",
             "tokens_per_s": dw.steps * dw.batch * world / (dec_ms / 1e3),
             "roofline": {"bound": "hbm", "achieved": dec_achieved, "peak": peaks["hbm_gbs"],
                          "unit": "GB/s", "frac": dec_achieved / peaks["hbm_gbs"],
