@@ -647,3 +647,44 @@ def test_randomized_problems(seed):
     else:
         assert o is None
         assert_parity(np.zeros(1), synth.to_f64(fs), np.zeros(1), fs_ref, dtype, label)
+
+
+def test_concurrent_prefills_on_two_streams_match_sequential_runs():
+    """Two prefills of different problems on two streams at once (each with its own workspace)
+    give bit for bit what each gives alone: no state is shared between calls."""
+    wa = PrefillWorkload("conc_a", 143, 4, 128, "bf16", (900, 130), 2, init_state=True)
+    wb = PrefillWorkload("conc_b", 144, 2, 128, "bf16", (2000,), 1)
+    da, db = to_device(synth.prefill_inputs(wa)), to_device(synth.prefill_inputs(wb))
+    args = lambda d: (d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"])
+    oa, fa = kda.prefill(*args(da), check_status=True)
+    ob, fb = kda.prefill(*args(db), check_status=True)
+    torch.cuda.synchronize()
+    sa, sb = torch.cuda.Stream(), torch.cuda.Stream()
+    outs = []
+    for _ in range(3):
+        with torch.cuda.stream(sa):
+            ra = kda.prefill(*args(da), stream=sa)
+        with torch.cuda.stream(sb):
+            rb = kda.prefill(*args(db), stream=sb)
+        outs.append((ra, rb))
+    torch.cuda.synchronize()
+    for (oa2, fa2), (ob2, fb2) in outs:
+        assert torch.equal(oa2, oa) and torch.equal(fa2, fa)
+        assert torch.equal(ob2, ob) and torch.equal(fb2, fb)
+
+
+def test_host_buffer_prefill_from_pageable_memory():
+    """kda_prefill_host with ordinary (pageable) host tensors: the copies cannot overlap the
+    prefill, but the results are the same, bit for bit."""
+    w = PrefillWorkload("host_pageable", 145, 2, 128, "bf16", (2500, 300), 2, init_state=True)
+    inp = synth.prefill_inputs(w)
+    dev = to_device(inp)
+    o_d, fs_d = kda.prefill(dev["q"], dev["k"], dev["v"], dev["log_alpha"], dev["beta"], dev["cu_seqlens"],
+                            dev["init_state"], check_status=True, seq_split=False)
+    o_h = torch.empty_like(inp["v"])
+    fs_h = torch.empty_like(inp["init_state"])
+    kda.prefill_host(inp["q"], inp["k"], inp["v"], inp["log_alpha"], inp["beta"], inp["cu_seqlens"],
+                     inp["init_state"], o=o_h, final_state=fs_h, seq_split=False)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(synth.to_f64(o_h), synth.to_f64(o_d.cpu()))
+    np.testing.assert_array_equal(synth.to_f64(fs_h), synth.to_f64(fs_d.cpu()))
