@@ -67,13 +67,13 @@ static_assert(ChunkLayout::ST_NQ + 49152 <= ChunkLayout::O1, "N | Q' staging ove
 static_assert(ChunkLayout::SOLVE_X + 32 * kLdX * 4 <= ChunkLayout::O1, "solve scratch overlaps O1");
 
 // State kernel (512 threads): two record stages, a ring of four v slices, the
-// V^T operand of two chunks and the S^T operand of two chunks.
+// V^T operand of two chunks and the S operand of two chunks.
 constexpr int kVRing = 4;
 struct StateLayout {
     static constexpr uint32_t STAGE = 75776;  // record + padding to 1024 bytes
     static constexpr uint32_t VBOX = 2 * STAGE;               // kVRing x v slice [64][32] bf16
     static constexpr uint32_t VIMG = VBOX + kVRing * 4096;    // 2 x V^T fp16, 32 rows x K 64
-    static constexpr uint32_t O7 = VIMG + 2 * 4096;           // 2 x S^T bf16, 32 rows x K 128
+    static constexpr uint32_t O7 = VIMG + 2 * 4096;           // 2 x S bf16, MN-major, K 128 x 32 columns
     static constexpr uint32_t USED = O7 + 2 * 8192;
 };
 static_assert(StateLayout::STAGE % 1024 == 0 && StateLayout::STAGE >= kRecBytes, "stage size");
@@ -456,9 +456,9 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 
 // ============================================================== state kernel
 constexpr uint32_t IDESC_PV = idesc_f16(128, 32, false, false);   // P V
-constexpr uint32_t IDESC_NS = idesc_bf16(128, 32, false, false);  // N S
+constexpr uint32_t IDESC_NS = idesc_bf16(128, 32, false, true);   // N S (S MN-major)
 constexpr uint32_t IDESC_P2V = idesc_f16(64, 32, false, false);   // P2 V
-constexpr uint32_t IDESC_QS = idesc_bf16(64, 32, false, false);   // Q' S
+constexpr uint32_t IDESC_QS = idesc_bf16(64, 32, false, true);    // Q' S (S MN-major)
 // TMEM columns: state increment (M = 128), outputs of two chunks (M = 64)
 constexpr uint32_t TM_5 = 0, TM_O = 32, kStateTmem = 128;
 // Warps 0-15 hold the state; warp 16 issues the chain MMAs; warp 17 copies and
@@ -467,8 +467,16 @@ constexpr int kStateWarps = 16, kChainWarp = 16, kCopyWarp = 17, kOutWarp = 18;
 constexpr int kStateThreads = 19 * 32;
 constexpr int kL2Ahead = 3;  // records brought into L2 this many chunks ahead
 
+// The state operand S (K = state row i, N = value column j, 32 columns): MN-major, rows of
+// 64 bytes, 64-byte swizzle (8-row atoms of 512 bytes); one K step of 16 rows is 1024 bytes.
+__device__ __forceinline__ uint32_t mn64(int i, int j)
+{
+    return (uint32_t)(i * 64 + ((((j >> 3) ^ (i >> 1)) & 3) << 4) + ((j & 7) << 1));
+}
+__device__ __forceinline__ uint64_t sdesc_s(uint32_t addr) { return sdesc(addr, 512, 512, kSw64B); }
+
 // The chain group of one chunk: P V (fp16) + N S_c (bf16) into the M = 128 accumulator.
-// dr, dv, ds: descriptors of the record, the V^T image and the S^T image in use.
+// dr, dv, ds: descriptors of the record, the V^T image and the S image in use.
 __device__ __forceinline__ void issue_chain(uint32_t acc, uint64_t dr, uint64_t dv, uint64_t ds)
 {
 #pragma unroll
@@ -476,7 +484,7 @@ __device__ __forceinline__ void issue_chain(uint32_t acc, uint64_t dr, uint64_t 
         mma_bf16(acc, dr + ((R_P + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_PV, s > 0);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {  // + N S_c (bf16)
-        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32, offs = (s >> 2) * 4096 + (s & 3) * 32;
+        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32, offs = s * 1024;
         mma_bf16(acc, dr + ((R_N + off) >> 4), ds + (offs >> 4), IDESC_NS, 1);
     }
 }
@@ -489,7 +497,7 @@ __device__ __forceinline__ void issue_out(uint32_t acc, uint64_t dr, uint64_t dv
         mma_bf16(acc, dr + ((R_P2 + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_P2V, s > 0);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {  // + Q' S_c (bf16)
-        const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32, offs = (s >> 2) * 4096 + (s & 3) * 32;
+        const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32, offs = s * 1024;
         mma_bf16(acc, dr + ((R_Q + off) >> 4), ds + (offs >> 4), IDESC_QS, 1);
     }
 }
@@ -585,7 +593,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
         tmem_alloc(&tmem_holder, kStateTmem);
         tmem_relinquish();
     }
-    // state row i, columns j0 + 8*part .. +7 in registers; S^T (bf16) operands in O7
+    // state row i, columns j0 + 8*part .. +7 in registers; S (bf16) operands in O7
     const int i_row = quarter * 32 + lane, jp = part * 8;
     float S[8];
     const size_t st_off = ((size_t)h * kD + i_row) * kD + j0 + jp, st_entry = (size_t)H * kD * kD;
@@ -603,19 +611,17 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
 #pragma unroll
             for (int j = 0; j < 8; ++j) S[j] = 0.f;
         }
-#pragma unroll
-        for (int j = 0; j < 8; ++j) store_bf16(sm + L::O7 + km16(jp + j, i_row, kDV), S[j]);
+        *reinterpret_cast<uint4 *>(sm + L::O7 + mn64(i_row, jp)) = pack_bf16x8(S);
     }
     fence_proxy_async_smem();
-    __syncthreads();  // barriers initialised, S_0^T written
+    __syncthreads();  // barriers initialised, S_0 written
     tc_fence_after_sync();
     const uint32_t tmem = tmem_holder;
     const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
     const int r64 = quarter * 16 + (lane & 15);  // row held by this lane in an M = 64 accumulator
-    const int odd = lane & 1;
     bool range_ok = true;
     // operand descriptors of buffer 0; buffer 1 is a fixed byte distance further
-    const uint64_t d_rec0 = kdesc(sb), d_v0 = kdesc(sb + L::VIMG), d_s0 = kdesc(sb + L::O7);
+    const uint64_t d_rec0 = kdesc(sb), d_v0 = kdesc(sb + L::VIMG), d_s0 = sdesc_s(sb + L::O7);
     // ready(c) for c >= 1 (chunk 0's operands are known ready from the first barrier)
     auto wait_ready = [&](int c) -> bool {
         return c < 1 || mbar_wait_ns(&bar_ready[c & 1], (uint32_t)(((c - 1) >> 1) & 1), kWaitNs);
@@ -683,27 +689,18 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
                     ok = convert_v(c + 1);
                     fence_proxy_async_smem();
                 }
-                if (ok) ok = mbar_wait_ns(&bar_s, (uint32_t)(c & 1), kWaitNs);
-                // gamma is read from the record: observe its copy (long complete) here too
+                // gamma comes from the record (its copy long complete): read before the chain's wait
                 if (ok) ok = wait_record(c);
-                if (ok) {  // S <- gamma . S + (P V + N S); S^T (bf16) for the next chunk, row pairs
+                const float gc = ok ? reinterpret_cast<const float *>(sm + st * L::STAGE + R_GM)[i_row] : 0.f;
+                if (ok) ok = mbar_wait_ns(&bar_s, (uint32_t)(c & 1), kWaitNs);
+                if (ok) {  // S <- gamma . S + (P V + N S); its bf16 operand image for the next chunk
                     tc_fence_after_sync();
                     float v[8];
                     tmem_ld8(tmem + TM_5 + lane_off + jp, v);
                     tmem_ld_wait();
-                    const float gc = reinterpret_cast<const float *>(sm + st * L::STAGE + R_GM)[i_row];
 #pragma unroll
                     for (int j = 0; j < 8; ++j) S[j] = fmaf(gc, S[j], v[j]);
-                    unsigned char *s_next = sm + L::O7 + (st ^ 1) * 8192;
-                    const int ie = i_row & ~1;
-#pragma unroll
-                    for (int u = 0; u < 4; ++u) {
-                        const float mine = odd ? S[4 + u] : S[u];
-                        const float give = odd ? S[u] : S[4 + u];
-                        const float other = __shfl_xor_sync(0xffffffffu, give, 1);
-                        const float lo = odd ? other : mine, hi = odd ? mine : other;
-                        *reinterpret_cast<uint32_t *>(s_next + km16(jp + 4 * odd + u, ie, kDV)) = pack_bf16x2(lo, hi);
-                    }
+                    *reinterpret_cast<uint4 *>(sm + L::O7 + (st ^ 1) * 8192 + mn64(i_row, jp)) = pack_bf16x8(S);
                     fence_proxy_async_smem();
                 }
                 tc_fence_before_sync();  // this warp's TMEM reads precede the arrival
@@ -817,7 +814,7 @@ __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(in
                 issue_p<ChunkLayout>(sb, tmem);
                 issue_n_q<ChunkLayout>(sb, tmem, true);
             } else {
-                const uint64_t dr = kdesc(sb), dv = kdesc(sb + StateLayout::VIMG), ds = kdesc(sb + StateLayout::O7);
+                const uint64_t dr = kdesc(sb), dv = kdesc(sb + StateLayout::VIMG), ds = sdesc_s(sb + StateLayout::O7);
                 issue_chain(tmem + TM_5, dr, dv, ds);
                 issue_out(tmem + TM_O, dr, dv, ds);
             }
