@@ -66,8 +66,9 @@ struct ChunkLayout {
 static_assert(ChunkLayout::ST_NQ + 49152 <= ChunkLayout::O1, "N | Q' staging overlaps O1");
 static_assert(ChunkLayout::SOLVE_X + 32 * kLdX * 4 <= ChunkLayout::O1, "solve scratch overlaps O1");
 
-// State kernel (512 threads): two record stages, a ring of four v slices, the
-// V^T operand of two chunks and the S operand of two chunks.
+// State kernel (608 threads: sixteen state warps, two issuing warps, a copy warp): two
+// record stages, a ring of four v slices, the V^T operand of two chunks and the S operand
+// of two chunks.
 constexpr int kVRing = 4;
 struct StateLayout {
     static constexpr uint32_t STAGE = 75776;  // record + padding to 1024 bytes
