@@ -280,11 +280,14 @@ kda_status_t kda_read_device_status(void *workspace, void *stream);
  *                KDA_ERR_UNSUPPORTED and enqueue nothing (use kda_prefill).
  *  device_errors optional DEVICE pointer to one uint32; when not NULL it receives
  *                this call's device-side error bits (0 = none, otherwise an OR of
- *                KDA_DEVICE_ERR_*), copied on `stream` after the prefill.
+ *                KDA_DEVICE_ERR_*), copied on `stream` after the prefill; a call
+ *                with num_seqs == 0 runs no kernel and writes 0 there.
  *
  * The first call on each device looks up the array's device address (with that
  * device current) and caches it; make that first call before any stream capture
- * begins.  All calls share the one array and each call reinitialises it (error
+ * begins.  The cached address is not valid across cudaDeviceReset (the library's
+ * module, and with it the array, may come back at another address): do not call
+ * this entry point on a device after resetting it in the same process.  All calls share the one array and each call reinitialises it (error
  * word and schedule) before use, so calls ordered on one stream are fine, but
  * calls whose work can overlap on the GPU (unordered streams) race on the array
  * and must be serialised by the caller.

@@ -31,7 +31,9 @@ void *g_scratch_addr[kMaxDevices];  // device address of g_prefill_scratch, per 
 std::mutex g_scratch_mutex;
 
 // Device address of the scratch on the current device, looked up once per device
-// (with that device current) and cached.
+// (with that device current) and cached.  The cache outlives a cudaDeviceReset, after
+// which the module, and so the array, may be loaded at another address: a process
+// that resets a device must not call kda_prefill_no_alloc on it again.
 kda_status_t scratch_on_current_device(void **out)
 {
     int dev = 0;
@@ -65,9 +67,13 @@ extern "C" kda_status_t kda_prefill_no_alloc(
     st = kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
                      d_v, dtype, init_state, o, final_state, scratch, kScratchBytes, stream);
     if (st != KDA_OK) return st;
-    if (device_errors &&
-        cudaMemcpyAsync(device_errors, scratch, sizeof(uint32_t), cudaMemcpyDeviceToDevice,
-                        static_cast<cudaStream_t>(stream)) != cudaSuccess)
-        return KDA_ERR_CUDA;
-    return KDA_OK;
+    if (!device_errors) return KDA_OK;
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    // With no sequences kda_prefill enqueues no kernel, so the scratch still holds the
+    // error word of whichever call used it last: report this call's (none) instead.
+    const cudaError_t e =
+        num_seqs == 0 ? cudaMemsetAsync(device_errors, 0, sizeof(uint32_t), strm)
+                      : cudaMemcpyAsync(device_errors, scratch, sizeof(uint32_t),
+                                        cudaMemcpyDeviceToDevice, strm);
+    return e == cudaSuccess ? KDA_OK : KDA_ERR_CUDA;
 }

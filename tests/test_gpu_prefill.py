@@ -2,8 +2,8 @@
 
 Small problems are compared element by element; they span several chunks and
 ragged tails.  The full-size workloads run exactly as the benchmark launches
-them, and the oracle recomputes sampled (sequence, head) units, whose inputs
-the counter-based generator reproduces on their own.
+them, and the oracle recomputes every (sequence, head) unit: the whole output
+element by element and the whole final-state tensor.
 """
 import numpy as np
 import pytest
@@ -34,34 +34,65 @@ def test_small_problems_match_oracle(w):
     assert_parity(o, fs, o_ref, fs_ref, w.dtype, w.name)
 
 
-def _sampled_full_size(w, units):
-    """Run the whole workload on the GPU; recompute the listed (seq, head) units on the oracle."""
+def _whole_tensor_parity(w, group):
+    """Run the whole workload on the GPU exactly as the benchmark launches it, then check
+    every (sequence, head) unit against the oracle, `group` heads at a time (so host memory
+    stays bounded): o element by element (max-abs over the whole output), the final state by
+    relative Frobenius over the whole [N, H, d, d] tensor.  Per-unit maxima are printed as
+    diagnostics only; the stated bounds gate."""
     full = synth.prefill_inputs(w)
-    o, fs = gpu_prefill(full)
-    cu = full["cu_seqlens"].numpy()
-    for s, h in units:
-        sub = synth.prefill_inputs(w, heads=[h], seqs=[s])
-        t0, t1 = int(cu[s]), int(cu[s + 1])
-        # the generator reproduces the unit's inputs exactly
-        assert torch.equal(sub["q"][:, 0], full["q"][t0:t1, h])
+    d = to_device(full)
+    o_d, fs_d = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
+                            cu_seqlens=d["cu_seqlens"], init_state=d["init_state"],
+                            check_status=True)
+    torch.cuda.synchronize()
+    o, fs = o_d.cpu(), fs_d.cpu()
+    del d, o_d, fs_d
+    cu = full["cu_seqlens"].numpy().astype(np.int64)
+    N, H = len(cu) - 1, w.num_heads
+    unit_o = np.zeros((N, H))
+    unit_s = np.zeros((N, H))
+    err2 = ref2 = 0.0
+    for h0 in range(0, H, group):
+        hs = slice(h0, min(H, h0 + group))
+        sub = {key: full[key][:, hs].contiguous() for key in ("q", "k", "v", "log_alpha", "beta")}
+        sub["cu_seqlens"] = full["cu_seqlens"]
+        sub["init_state"] = None if full["init_state"] is None else full["init_state"][:, hs].contiguous()
         o_ref, fs_ref = oracle_prefill(sub)
-        assert_parity(o[t0:t1, h], fs[s, h], o_ref[:, 0], fs_ref[0, 0], w.dtype,
-                      f"{w.name} seq {s} head {h}")
-    assert np.isfinite(o).all() and np.isfinite(fs).all()
+        diff = np.abs(synth.to_f64(o[:, hs]) - o_ref).max(axis=2)  # [T, heads]
+        del o_ref
+        for n in range(N):
+            if cu[n + 1] > cu[n]:
+                unit_o[n, hs] = diff[cu[n]:cu[n + 1]].max(axis=0)
+        del diff
+        fs_g = synth.to_f64(fs[:, hs])
+        assert np.isfinite(fs_g).all()
+        e = np.square(fs_g - fs_ref).sum(axis=(2, 3))
+        r = np.square(fs_ref).sum(axis=(2, 3))
+        unit_s[:, hs] = np.sqrt(e / np.where(r > 0, r, 1.0))
+        err2 += float(e.sum())
+        ref2 += float(r.sum())
+    eo = float(unit_o.max())
+    es = float(np.sqrt(err2 / ref2)) if ref2 > 0 else float(np.sqrt(err2))
+    wo, ws_ = np.unravel_index(np.argmax(unit_o), unit_o.shape), np.unravel_index(np.argmax(unit_s), unit_s.shape)
+    print(f"[parity] {w.name}: all {N} x {H} units; max|do| = {eo:.3e} (tol {TOL[w.dtype]['o']:.0e}, "
+          f"worst unit seq {wo[0]} head {wo[1]}), relF(whole final state) = {es:.3e} "
+          f"(tol {TOL[w.dtype]['state']:.0e}; worst unit {unit_s.max():.3e} at seq {ws_[0]} head {ws_[1]})")
+    assert bool(torch.isfinite(o.float()).all())
+    assert eo <= TOL[w.dtype]["o"], f"{w.name}: output max-abs error {eo:.3e}"
+    assert es <= TOL[w.dtype]["state"], f"{w.name}: final-state relative error {es:.3e}"
 
 
-def test_prefill_4k_full_size_sampled():
-    _sampled_full_size(synth.PREFILL_4K, [(0, 0), (0, 13), (0, 31)])
+def test_prefill_4k_full_size_every_unit():
+    _whole_tensor_parity(synth.PREFILL_4K, group=32)
 
 
-def test_prefill_64k_with_initial_state_full_size_sampled():
-    _sampled_full_size(synth.PREFILL_64K, [(0, 5), (0, 26)])
+def test_prefill_64k_with_initial_state_full_size_every_unit():
+    _whole_tensor_parity(synth.PREFILL_64K, group=8)
 
 
-def test_varlen16_full_size_sampled():
-    lens = synth.VARLEN_16.lengths()
-    longest, shortest = int(np.argmax(lens)), int(np.argmin(lens))
-    _sampled_full_size(synth.VARLEN_16, [(longest, 0), (shortest, 31), (3, 7)])
+def test_varlen16_full_size_every_unit():
+    _whole_tensor_parity(synth.VARLEN_16, group=4)
 
 
 def _custom(name, wid, lens, H=1, d=128, dtype="bf16", init_state=False, log_alpha=None):
@@ -464,19 +495,11 @@ def test_sequence_split_state_pass(w):
     np.testing.assert_array_equal(synth.to_f64(pool_d[final_h].cpu()), synth.to_f64(fs_d.cpu()))
 
 
-def test_sequence_split_long_context_few_heads_sampled():
+def test_sequence_split_long_context_few_heads_every_unit():
     """T = 65536, H = 4, one sequence (the segmented pass with 5 segments of 205 chunks):
-    head 2 against the oracle, outputs and final state."""
+    every head against the oracle, the whole output and the whole final state."""
     w = PrefillWorkload("long_T65536_H4_state", 130, 4, 128, "bf16", (65536,), 1, init_state=True)
-    inp = synth.prefill_inputs(w)
-    d = to_device(inp)
-    o, fs = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
-                        d["init_state"], check_status=True)
-    torch.cuda.synchronize()
-    sub = synth.prefill_inputs(w, heads=[2])
-    o_ref, fs_ref = oracle_prefill(sub)
-    assert_parity(synth.to_f64(o[:, 2:3]), synth.to_f64(fs[:, 2:3]), o_ref, fs_ref, "bf16",
-                  "split T=65536 H=4 head 2")
+    _whole_tensor_parity(w, group=4)
 
 
 def test_options_together_on_a_split_problem():

@@ -78,6 +78,14 @@ def test_no_alloc_reports_device_errors_and_rejects_too_many_sequences():
     assert st == kda.KDA_OK
     torch.cuda.synchronize()
     assert err.item() == 1  # KDA_DEVICE_ERR_SEQLENS
+    # the scratch still holds that error; an empty call must report its own (none)
+    err.fill_(0xFFFF)
+    st = kda.kda_prefill_no_alloc(None, None, None, None, None, d["cu_seqlens"].data_ptr(), 0, 0,
+                                  dims[2], dims[3], dims[3], kda.KDA_DTYPE_BF16, None, None,
+                                  fs.data_ptr(), err.data_ptr(), stream)
+    assert st == kda.KDA_OK
+    torch.cuda.synchronize()
+    assert err.item() == 0
     too_many = list(_args(d, o, fs, dims))
     too_many[6] = 4097
     assert kda.kda_prefill_no_alloc(*too_many, None, stream) == kda.KDA_ERR_UNSUPPORTED
