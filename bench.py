@@ -5,9 +5,13 @@ One step is one kda_prefill over the single-sequence prefill workload
 chunkwise row of the path (decay prefix, decayed operands, k-k and q-k
 matrices, UT solve, WY factors, output, state propagation).  The decode row is
 timed in the same run on its own workload (256 sequences x 32 heads, d=128,
-1000 in-place steps) and reported under "decode".  A long single sequence with
-few heads (T=65536, H=4), where the serial state pass would leave most SMs idle,
-is timed with and without the sequence-split state pass under "long_context".
+1000 in-place steps) and reported under "decode".  The two larger prefill
+workloads are timed in the same run, each with its own roofline and oracle
+baseline: one sequence of T=65536 tokens from a nonzero initial state under
+"long_prefill", and 16 packed sequences of 512..16384 tokens (168,023 in all)
+under "varlen_prefill".  A long single sequence with few heads (T=65536, H=4),
+where the serial state pass would leave most SMs idle, is timed with and
+without the sequence-split state pass under "long_context".
 
 value    prefill tokens/s with inputs resident in HBM (CUDA events, L2 flushed
          between timed steps by writing a 256 MiB buffer, flush not timed);
@@ -20,7 +24,9 @@ roofline HBM-bound, for the dominant (longest) kernel of the prefill: its share
          kda_prefill_events records around the kernels on the launching stream),
          against the measured copy bandwidth in MEASURED_PEAKS.json; the whole
          call against all algorithmic bytes is reported beside it ("path");
-cpu_baseline  the fp64 oracle on the host cores (rank 0, N=1 only).
+cpu_baseline  the fp64 oracle on the host cores (rank 0, N=1 only); the decode,
+         long_prefill and varlen_prefill blocks carry their own, each on a
+         bounded sample of its workload that the block states.
 
 `--impl reference` times the oracle itself (the only other implementation of
 the method here) on the same workload and prints the same line with
@@ -44,6 +50,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "KDA prefill tokens/s & decode steps/s (H=32,d=128) and % of roofline"
 L2_FLUSH_BYTES = 256 << 20
+CASE_STEPS = 5  # timed calls of each further prefill workload (2.5 to 10 ms each)
 
 
 def _env_rank():
@@ -90,6 +97,38 @@ def executed_tensor_flops(T, H, d, C=64):
                         + 128 * 128 * 64 + 64 * 128 * 64)
     state_groups = 2 * (128 * 32 * 64 + 128 * 32 * 128 + 64 * 32 * 64 + 64 * 32 * 128) * (d // 32)
     return chunks * H * (chunk_groups + state_groups)
+
+
+def prefill_roofline(T, H, d, N, with_init, call_ms, stage_ms, peaks, traffic_key):
+    """Roofline object of one prefill workload: the dominant (longest) kernel against its
+    share of the algorithmic bytes, and the whole call against all of them.  call_ms: mean
+    event time of one kda_prefill; stage_ms: mean event times of schedule, chunk and state
+    kernel from kda_prefill_events."""
+    alg_bytes = prefill_algorithmic_bytes(T, H, d, N, 2, with_init)
+    achieved = alg_bytes / (call_ms / 1e3) / 1e9
+    names = ("prefill_prep_kernel", "prefill_chunk_kernel", "prefill_state_kernel")
+    stage_bytes = prefill_stage_bytes(T, H, d, N, 2, with_init)
+    kernels = {}
+    for name, ms in zip(names, stage_ms):
+        kb = stage_bytes.get(name)
+        kernels[name] = {"ms_per_launch": ms}
+        if kb:
+            kernels[name].update({"algorithmic_bytes_per_launch": kb,
+                                  "achieved_gbs": kb / (ms / 1e3) / 1e9,
+                                  "frac": kb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]})
+    dom = max(stage_bytes, key=lambda n: kernels[n]["ms_per_launch"])
+    return {"bound": "hbm", "kernel": dom,
+            "achieved": kernels[dom]["achieved_gbs"], "peak": peaks["hbm_gbs"],
+            "unit": "GB/s", "frac": kernels[dom]["frac"],
+            "traffic": profiled_traffic(dom + "_" + traffic_key),
+            "peak_source": peaks["source"],
+            "algorithmic_bytes_per_launch": stage_bytes[dom],
+            "kernels": kernels,
+            "path": {"achieved": achieved, "frac": achieved / peaks["hbm_gbs"],
+                     "algorithmic_bytes_per_launch": alg_bytes,
+                     "algorithmic_flops_per_call": prefill_flops(T, H, d),
+                     "tensor_frac_of_bf16_peak": prefill_flops(T, H, d) /
+                     (call_ms / 1e3) / 1e12 / peaks["bf16_tflops"]}}
 
 
 def decode_algorithmic_bytes(B, H, d, io_bytes):
@@ -350,6 +389,61 @@ class _Gpu:
             raise self.kda.KdaError(st, "kda_prefill_ex (device status)")
         return out
 
+    # ------------------------------------------------------------------ more prefill workloads
+    def setup_case(self, w):
+        """Device buffers of one more prefill workload (the long single sequence with an
+        initial state, or the 16-sequence varlen pack)."""
+        torch, kda = self.torch, self.kda
+        inp = self.synth.prefill_inputs(w, seed=self.seed)
+        x = {k: (None if inp[k] is None else inp[k].to(self.dev))
+             for k in ("q", "k", "v", "log_alpha", "beta", "cu_seqlens", "init_state")}
+        T, H, d = inp["q"].shape
+        N = inp["cu_seqlens"].numel() - 1
+        c = {"w": w, "inp": inp, "x": x, "T": T, "H": H, "d": d, "N": N,
+             "o": torch.empty((T, H, d), dtype=torch.bfloat16, device=self.dev),
+             "fs": torch.empty((N, H, d, d), dtype=torch.float32, device=self.dev),
+             "ws": kda.workspace_for(N, T, H, d, kda.KDA_DTYPE_BF16, self.dev)}
+        return c
+
+    def case_call(self, c, events=None):
+        kda, x = self.kda, c["x"]
+        s0 = None if x["init_state"] is None else x["init_state"].data_ptr()
+        args = (x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), x["log_alpha"].data_ptr(),
+                x["beta"].data_ptr(), x["cu_seqlens"].data_ptr(), c["N"], c["T"], c["H"], c["d"],
+                c["d"], kda.KDA_DTYPE_BF16, s0, c["o"].data_ptr(), c["fs"].data_ptr(),
+                c["ws"].data_ptr(), c["ws"].numel(), self.sh)
+        st = kda.kda_prefill(*args) if events is None else kda.kda_prefill_events(*args, events)
+        if st != kda.KDA_OK:
+            raise kda.KdaError(st, "kda_prefill")
+
+    def time_case(self, c, steps, warmup):
+        """Per-call event times (ms) of kda_prefill on one workload, and the per-kernel split
+        from the same number of kda_prefill_events calls.  The inputs (over 1 GB) are far
+        larger than L2, so no flush runs between calls."""
+        torch = self.torch
+        for _ in range(warmup):
+            self.case_call(c)
+        torch.cuda.synchronize()
+        outer = [(self.event(), self.event()) for _ in range(steps)]
+        for a, b in outer:
+            a.record(self.stream)
+            self.case_call(c)
+            b.record(self.stream)
+        torch.cuda.synchronize()
+        ev = [[self.event() for _ in range(4)] for _ in range(steps)]
+        for e in ev:
+            for x in e:
+                x.record(self.stream)
+        torch.cuda.synchronize()
+        for e in ev:
+            self.case_call(c, [x.cuda_event for x in e])
+        torch.cuda.synchronize()
+        st = self.kda.kda_read_device_status(c["ws"].data_ptr(), self.sh)
+        if st != self.kda.KDA_OK:
+            raise self.kda.KdaError(st, "kda_prefill (device status)")
+        return ([a.elapsed_time(b) for a, b in outer],
+                [[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev])
+
     def setup_decode(self):
         torch, synth = self.torch, self.synth
         self.dw = dw = synth.DECODE_256
@@ -411,6 +505,9 @@ def run_gpu(args):
     do_prefill = args.only in ("all", "prefill")
     do_decode = args.only in ("all", "decode")
     do_long = args.only in ("all", "long")
+    # the long single sequence with an initial state, and the 16-sequence varlen pack
+    case_ws = {"long_prefill": (g.synth.PREFILL_64K, "64k"), "varlen_prefill": (g.synth.VARLEN_16, "varlen16")}
+    do_cases = [n for n in case_ws if args.only in ("all", n)]
     if do_prefill:
         g.setup_prefill()
     if do_long:
@@ -422,6 +519,7 @@ def run_gpu(args):
             "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16",
             "data": "synthetic (seeded counter-based generator; no dataset)"}
+    case_ms = {}
     with clocks:
         if do_prefill:
             step_ms, stage_ms = g.time_prefill(args.steps, args.warmup, barrier)
@@ -429,6 +527,17 @@ def run_gpu(args):
             # the prefill kernels' tensor-core product groups on their own (resident operands)
             phase_tflops = {name: g.kda.diag_tensor_phases(i, 2000, g.ws)
                             for i, name in enumerate(("chunk_kernel_products", "state_kernel_products"))}
+        for name in do_cases:
+            # one workload on the device at a time (the varlen pack holds about 20 GB)
+            c = g.setup_case(case_ws[name][0])
+            barrier()
+            case_ms[name] = (c, g.time_case(c, CASE_STEPS, max(3, args.warmup)))
+            c["with_init"] = c["inp"]["init_state"] is not None
+            # the oracle's sample is cut out now; the full host inputs are dropped
+            c["cpu_sample"] = case_sample(c["w"], c["inp"])
+            for key in ("x", "o", "fs", "ws", "inp"):
+                c.pop(key)
+            torch.cuda.empty_cache()
         if do_decode:
             dec_ms = g.time_decode(g.dw.steps, max(3, args.warmup), barrier)
         if do_long:
@@ -438,21 +547,21 @@ def run_gpu(args):
         e2e_total = reduce_max(sum(e2e_ms))
         mean_step_ms = total_ms / args.steps
         T, H, d = g.T, g.H, g.d
-        alg_bytes = prefill_algorithmic_bytes(T, H, d, 1, 2, False)
-        achieved = alg_bytes / (mean_step_ms / 1e3) / 1e9
         # per kernel: mean event time (max over ranks) and its share of the algorithmic bytes
-        names = ("prefill_prep_kernel", "prefill_chunk_kernel", "prefill_state_kernel")
         stage_mean = [reduce_max(sum(s[i] for s in stage_ms)) / args.steps for i in range(3)]
-        stage_bytes = prefill_stage_bytes(T, H, d, 1, 2, False)
-        kernels = {}
-        for name, ms in zip(names, stage_mean):
-            kb = stage_bytes.get(name)
-            kernels[name] = {"ms_per_launch": ms}
-            if kb:
-                kernels[name].update({"algorithmic_bytes_per_launch": kb,
-                                      "achieved_gbs": kb / (ms / 1e3) / 1e9,
-                                      "frac": kb / (ms / 1e3) / 1e9 / peaks["hbm_gbs"]})
-        dom = max(stage_bytes, key=lambda n: kernels[n]["ms_per_launch"])
+        roof = prefill_roofline(T, H, d, 1, False, mean_step_ms, stage_mean, peaks, "4k")
+        roof["path"]["executed_tensor_flops_per_call"] = executed_tensor_flops(T, H, d)
+        roof["gemm_phases"] = dict(
+            {name: {"achieved": tf, "unit": "TFLOP/s", "peak": peaks["bf16_tflops"],
+                    "frac": tf / peaks["bf16_tflops"]} for name, tf in phase_tflops.items()},
+            note="kda_diag_tensor_phases: each kernel's product groups issued back to back by "
+                 "its own issue routines on operands resident in shared memory (executed "
+                 "FLOPs, bf16/fp16 inputs, fp32 accumulate), 2000 repetitions per CTA")
+        roof["note"] = ("kernel durations from the four CUDA events kda_prefill_events records on "
+                        "the launching stream around its kernels (a separate timed pass); the "
+                        "dominant (longest) kernel is measured against its share of the path's "
+                        "algorithmic bytes, the path (one kda_prefill between two events) against "
+                        "all of them")
         line.update({
             "value": aggregate_rate(T, world, args.steps, total_ms),
             "ms_per_step": mean_step_ms,
@@ -461,39 +570,32 @@ def run_gpu(args):
                        "gate_state_dtype": "f32",
                        "l2": "flushed between timed steps (256 MiB write, untimed)",
                        "parallelism": f"replicas x{world} (independent units, no collective)"},
-            "roofline": {"bound": "hbm", "kernel": dom,
-                         "achieved": kernels[dom]["achieved_gbs"], "peak": peaks["hbm_gbs"],
-                         "unit": "GB/s", "frac": kernels[dom]["frac"],
-                         "traffic": profiled_traffic(dom + "_4k"),
-                         "peak_source": peaks["source"],
-                         "algorithmic_bytes_per_launch": stage_bytes[dom],
-                         "kernels": kernels,
-                         "path": {"achieved": achieved, "frac": achieved / peaks["hbm_gbs"],
-                                  "algorithmic_bytes_per_launch": alg_bytes,
-                                  "algorithmic_flops_per_call": prefill_flops(T, H, d),
-                                  "executed_tensor_flops_per_call": executed_tensor_flops(T, H, d),
-                                  "tensor_frac_of_bf16_peak": prefill_flops(T, H, d) /
-                                  (mean_step_ms / 1e3) / 1e12 / peaks["bf16_tflops"]},
-                         "gemm_phases": dict(
-                             {name: {"achieved": tf, "unit": "TFLOP/s", "peak": peaks["bf16_tflops"],
-                                     "frac": tf / peaks["bf16_tflops"]} for name, tf in phase_tflops.items()},
-                             note="kda_diag_tensor_phases: each kernel's product groups issued back to back by "
-                                  "its own issue routines on operands resident in shared memory (executed "
-                                  "FLOPs, bf16/fp16 inputs, fp32 accumulate), 2000 repetitions per CTA"),
-                         "note": "kernel durations from the four CUDA events kda_prefill_events "
-                                 "records on the launching stream around its kernels (a separate "
-                                 "timed pass); the dominant (longest) kernel is measured against "
-                                 "its share of the path's algorithmic bytes, the path (one "
-                                 "kda_prefill between two events) against all of them"},
+            "roofline": roof,
             "e2e": {"value": aggregate_rate(T, world, args.steps, e2e_total), "unit": "tokens/s",
                     "h2d_bytes_per_step": g.h2d, "d2h_bytes_per_step": g.d2h,
                     "call": "kda_prefill_host: pinned host buffers, the prompt cut into segments whose "
                             "copies overlap the prefill of the segments before (results bit for bit "
                             "those of kda_prefill)",
+                    "link_gbs": (g.h2d + g.d2h) / (e2e_total / args.steps / 1e3) / 1e9,
                     "gpu_launches_per_step": g.e2e_launches},
             "gpu_launches": 3 * args.steps,  # schedule, chunk and state kernel per step
         })
     line["clocks"] = clocks.summary()
+    for name, (c, (call_ms, stages)) in case_ms.items():
+        w, T, H, d, N = c["w"], c["T"], c["H"], c["d"], c["N"]
+        ms = reduce_max(sum(call_ms)) / len(call_ms)
+        stage_mean = [reduce_max(sum(st[i] for st in stages)) / len(stages) for i in range(3)]
+        blk = {"metric": "KDA prefill tokens/s", "workload": w.name, "unit": "tokens/s",
+               "value": aggregate_rate(T, world, 1, ms), "ms_per_call": ms, "steps": len(call_ms),
+               "num_seqs": N, "total_tokens": T, "num_heads": H, "d_k": d, "d_v": d,
+               "init_state": c["with_init"],
+               "l2": "inputs larger than L2 (no flush)",
+               "gpu_launches": 3 * len(call_ms),
+               "roofline": prefill_roofline(T, H, d, N, c["with_init"], ms,
+                                            stage_mean, peaks, case_ws[name][1])}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            blk["cpu_baseline"] = cpu_baseline_case(w, c["cpu_sample"])
+        line[name] = blk
     if do_decode:
         dw = g.dw
         dec_ms = reduce_max(dec_ms)
@@ -510,6 +612,8 @@ def run_gpu(args):
                          "unit": "GB/s", "frac": dec_achieved / peaks["hbm_gbs"],
                          "traffic": profiled_traffic("decode_256"),
                          "algorithmic_bytes_per_launch": dec_bytes}}
+        if rank == 0 and world == 1 and not args.no_cpu_baseline:
+            line["decode"]["cpu_baseline"] = cpu_baseline_decode(dw, g.seed)
     if do_long:
         T = g.lw.seq_lens[0]
         split_ms, unsplit_ms = reduce_max(long_ms[True]), reduce_max(long_ms[False])
@@ -555,6 +659,72 @@ def cpu_baseline(w, inp, heads=None):
             "sample": f"{w.name}: {H} of {w.num_heads} heads x {T} tokens, fp64 token-by-token, "
                       f"{reps} passes in {dt:.2f} s wall on {used} threads (about {dt * used:.0f} s of CPU "
                       f"time); tokens/s counts a token as all {w.num_heads} heads",
+            "cpu": _cpu_model(), "nproc": os.cpu_count()}
+
+
+CASE_SAMPLE_TOKENS = {"prefill_bf16_T65536_H32_d128_state": 2048, "varlen16_bf16_T512-16384_H32_d128": 256}
+
+
+def case_sample(w, inp):
+    """The oracle's bounded sample of a larger prefill workload: every sequence and head,
+    each sequence cut to its first few tokens (with its initial state, if any).  The
+    oracle's cost per token-head does not depend on the position, so the rate carries over."""
+    from kda_gated_delta_04_gb300 import synth
+    n = CASE_SAMPLE_TOKENS[w.name]
+    cu = inp["cu_seqlens"].numpy().astype(np.int64)
+    idx = np.concatenate([np.arange(cu[i], min(cu[i + 1], cu[i] + n)) for i in range(len(cu) - 1)])
+    lens = np.minimum(np.diff(cu), n)
+    import torch
+    sel = torch.from_numpy(idx)
+    f = {k: np.ascontiguousarray(synth.to_f64(inp[k].index_select(0, sel)))
+         for k in ("q", "k", "v", "log_alpha", "beta")}
+    f["cu_seqlens"] = np.concatenate([[0], np.cumsum(lens)]).astype(np.int64)
+    f["init_state"] = None if inp["init_state"] is None else synth.to_f64(inp["init_state"])
+    f["desc"] = (f"{w.name}: the first {n} tokens of each of its {len(lens)} sequence(s) x all "
+                 f"{w.num_heads} heads" + (" from the initial states" if inp["init_state"] is not None else ""))
+    return f
+
+
+def cpu_baseline_case(w, f):
+    """The oracle as it stands, all host cores, on the sample case_sample() cut out."""
+    import oracle
+    T, H = f["q"].shape[:2]
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        _, _, used = oracle.prefill(f["q"], f["k"], f["v"], f["log_alpha"], f["beta"],
+                                    cu_seqlens=f["cu_seqlens"], init_state=f["init_state"])
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt * used >= 12.0 or reps >= 50:
+            break
+    return {"value": reps * T / dt, "unit": "tokens/s", "cores": used, "kind": "oracle",
+            "sample": f"{f['desc']} ({T} tokens), fp64 token-by-token, {reps} passes in {dt:.2f} s "
+                      f"wall on {used} threads (about {dt * used:.0f} s of CPU time); tokens/s counts "
+                      f"a token as all {H} heads",
+            "cpu": _cpu_model(), "nproc": os.cpu_count()}
+
+
+def cpu_baseline_decode(dw, seed):
+    """The oracle's decode step as it stands, all host cores, on the full batch (every
+    sequence and head of the decode workload, the same state and per-step inputs), for as
+    many of the workload's steps as fit about 12 s of CPU time; steps/s over those steps."""
+    import oracle
+    from kda_gated_delta_04_gb300 import synth
+    state = synth.to_f64(synth.decode_state(dw, seed=seed))
+    ring = [{k: synth.to_f64(t) for k, t in synth.decode_inputs(dw, s, seed=seed).items()}
+            for s in range(16)]
+    steps, t0 = 0, time.perf_counter()
+    while True:
+        r = ring[steps % len(ring)]
+        _, used = oracle.decode_step(r["q"], r["k"], r["v"], r["log_alpha"], r["beta"], state)
+        steps += 1
+        dt = time.perf_counter() - t0
+        if (dt * used >= 12.0 and steps >= 3) or steps >= dw.steps:
+            break
+    return {"value": steps / dt, "unit": "steps/s", "cores": used, "kind": "oracle",
+            "sample": f"{dw.name}: the first {steps} of its {dw.steps} steps over all {dw.batch} x "
+                      f"{dw.num_heads} units (fp64 state, in place), {dt:.2f} s wall on {used} threads "
+                      f"(about {dt * used:.0f} s of CPU time); measured over those steps, not extrapolated",
             "cpu": _cpu_model(), "nproc": os.cpu_count()}
 
 
@@ -619,7 +789,8 @@ def main():
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", choices=["gb300", "reference"], default="gb300")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--only", choices=["all", "prefill", "decode", "long"], default="all",
+    ap.add_argument("--only", choices=["all", "prefill", "decode", "long", "long_prefill",
+                                       "varlen_prefill"], default="all",
                     help="profiling aid: run only one part (the printed line is then partial)")
     args = ap.parse_args()
     if args.warmup < 3:

@@ -121,6 +121,28 @@ __device__ __forceinline__ float load_io(const float *p) { return *p; }
 __device__ __forceinline__ float load_io(const __nv_bfloat16 *p) { return __bfloat162float(*p); }
 __device__ __forceinline__ void store_io(float *p, float x) { *p = x; }
 __device__ __forceinline__ void store_io(__nv_bfloat16 *p, float x) { *p = __float2bfloat16_rn(x); }
+// four consecutive values (p 16-byte aligned for fp32, 8-byte aligned for bf16)
+__device__ __forceinline__ void load_io4(const float *p, float (&x)[4])
+{
+    const float4 a = *reinterpret_cast<const float4 *>(p);
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+}
+__device__ __forceinline__ void load_io4(const __nv_bfloat16 *p, float (&x)[4])
+{
+    const uint2 a = *reinterpret_cast<const uint2 *>(p);
+    const float2 lo = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&a.x));
+    const float2 hi = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&a.y));
+    x[0] = lo.x; x[1] = lo.y; x[2] = hi.x; x[3] = hi.y;
+}
+__device__ __forceinline__ void store_io4(float *p, const float (&x)[4])
+{
+    *reinterpret_cast<float4 *>(p) = make_float4(x[0], x[1], x[2], x[3]);
+}
+__device__ __forceinline__ void store_io4(__nv_bfloat16 *p, const float (&x)[4])
+{
+    __nv_bfloat162 lo = __floats2bfloat162_rn(x[0], x[1]), hi = __floats2bfloat162_rn(x[2], x[3]);
+    *reinterpret_cast<uint2 *>(p) = make_uint2(*reinterpret_cast<uint32_t *>(&lo), *reinterpret_cast<uint32_t *>(&hi));
+}
 
 // Four consecutive elements (16-byte aligned for fp32, 8-byte for bf16).
 __device__ __forceinline__ float4 load4_io(const float *p) { return *reinterpret_cast<const float4 *>(p); }

@@ -13,10 +13,14 @@
 // work per token, decay first and then the delta write; "K3 attention,
 // three-piece set": fixed d_k x d_v state per KDA head).
 //
-// Layout: 256 threads; each thread owns a float4 column quad of P rows; a warp
-// reads whole 512-byte (d = 128) or 256-byte (d = 64) rows with 128-bit loads.
-// The reduction over rows is done in registers, then across the rows-per-pass
-// groups through shared memory.
+// Layout: 256 threads, 8 warps; warp w owns the value columns [D/8 w, D/8 (w+1)) over
+// all D key rows.  Lane = (row lane rl, column quad cq) with CQ = D/32 quads per warp
+// and RL = 32/CQ row lanes, so one 128-bit load per lane covers RL whole rows of the
+// warp's stripe; a thread keeps the float4 quad of P = D/RL rows (rl, rl + RL, ...).
+// Both reductions over the key rows end in the warp: a lane sums its P rows in
+// registers, then a butterfly of warp shuffles over the row lanes leaves every lane
+// with its columns' S~^T k and S~^T q, so delta, o and the write need no further
+// barrier.  k.q is a butterfly over the whole warp.
 #include "common.cuh"
 
 namespace kda {
@@ -33,18 +37,15 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
               int H, int num_slots, uint32_t *errors)
 {
     constexpr bool scalar_gate = SCALAR, qk_norm = QKN;
-    constexpr int TPR = D / 4;      // threads per state row
-    constexpr int RPP = 256 / TPR;  // rows per pass
-    constexpr int P = D / RPP;      // rows per thread
+    constexpr int CQ = D / 32;   // column quads per warp (8 warps x CQ quads = D / 4)
+    constexpr int RL = 32 / CQ;  // row lanes
+    constexpr int P = D / RL;    // rows per thread
     const int unit = blockIdx.x;
-    const int tid = threadIdx.x;
-    const int c4 = tid % TPR;
-    const int r0 = tid / TPR;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int rl = lane / CQ;
+    const int c4 = warp * CQ + lane % CQ;  // this thread's column quad
 
     __shared__ float s_a[D], s_k[D], s_q[D];
-    __shared__ __align__(16) float s_d[D];  // read as float4
-    __shared__ __align__(16) float s_rk[RPP][D];
-    __shared__ __align__(16) float s_rq[RPP][D];
 
     size_t sunit = (size_t)unit;  // the unit's state: its own, or its sequence's pool slot
     if (slots) {
@@ -59,7 +60,7 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
     float4 s[P];
 #pragma unroll
     for (int p = 0; p < P; ++p)
-        s[p] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)(r0 + p * RPP) * D) + c4);
+        s[p] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)(rl + p * RL) * D) + c4);
 
     if (tid < D) {
         s_a[tid] = expf(scalar_gate ? log_alpha[unit] : log_alpha[(size_t)unit * D + tid]);
@@ -71,44 +72,62 @@ decode_kernel(const IO *__restrict__ q, const IO *__restrict__ k, const IO *__re
     float4 rk = make_float4(0.f, 0.f, 0.f, 0.f), rq = rk;
 #pragma unroll
     for (int p = 0; p < P; ++p) {
-        const int i = r0 + p * RPP;
+        const int i = rl + p * RL;
         const float a = s_a[i], ki = s_k[i], qi = s_q[i];
         s[p].x *= a; s[p].y *= a; s[p].z *= a; s[p].w *= a;
         rk.x += s[p].x * ki; rk.y += s[p].y * ki; rk.z += s[p].z * ki; rk.w += s[p].w * ki;
         rq.x += s[p].x * qi; rq.y += s[p].y * qi; rq.z += s[p].z * qi; rq.w += s[p].w * qi;
     }
-    reinterpret_cast<float4 *>(&s_rk[r0][0])[c4] = rk;
-    reinterpret_cast<float4 *>(&s_rq[r0][0])[c4] = rq;
-    __syncthreads();
-
-    if (tid < D) {
-        const int j = tid;
-        float sk = 0.f, sq = 0.f, kq = 0.f, kk = 0.f, qq = 0.f;
+    // k.q (and the squared norms for raw q, k): lane l sums rows l, l + 32, ...
+    float kq = 0.f, kk = 0.f, qq = 0.f;
 #pragma unroll
-        for (int r = 0; r < RPP; ++r) { sk += s_rk[r][j]; sq += s_rq[r][j]; }
-        for (int i = 0; i < D; ++i) kq += s_k[i] * s_q[i];
-        // raw q, k (qk_norm): every term is linear in q and in k, so the reciprocal norms
-        // scale the reductions instead of the vectors (no extra barrier)
-        float nk = 1.f, nq = 1.f;
-        if (qk_norm) {
-            for (int i = 0; i < D; ++i) { kk += s_k[i] * s_k[i]; qq += s_q[i] * s_q[i]; }
-            nk = 1.f / fmaxf(sqrtf(kk), kQkNormEps);
-            nq = 1.f / fmaxf(sqrtf(qq), kQkNormEps);
-        }
-        const float scale = rsqrtf((float)D);
-        const float d = beta[unit] * (load_io(v + (size_t)unit * D + j) - sk * nk);
-        s_d[j] = d * nk;  // the write k^ d^T = k (nk d)^T
-        store_io(o + (size_t)unit * D + j, scale * (sq * nq + kq * (nk * nq) * d));
+    for (int i = lane; i < D; i += 32) {
+        const float ki = s_k[i], qi = s_q[i];
+        kq += ki * qi;
+        if (qk_norm) { kk += ki * ki; qq += qi * qi; }
     }
-    __syncthreads();
+#pragma unroll
+    for (int m = CQ; m < 32; m <<= 1) {  // over the row lanes: the column sums
+        rk.x += __shfl_xor_sync(0xffffffffu, rk.x, m); rk.y += __shfl_xor_sync(0xffffffffu, rk.y, m);
+        rk.z += __shfl_xor_sync(0xffffffffu, rk.z, m); rk.w += __shfl_xor_sync(0xffffffffu, rk.w, m);
+        rq.x += __shfl_xor_sync(0xffffffffu, rq.x, m); rq.y += __shfl_xor_sync(0xffffffffu, rq.y, m);
+        rq.z += __shfl_xor_sync(0xffffffffu, rq.z, m); rq.w += __shfl_xor_sync(0xffffffffu, rq.w, m);
+    }
+#pragma unroll
+    for (int m = 1; m < 32; m <<= 1) {  // over the whole warp: the dot products
+        kq += __shfl_xor_sync(0xffffffffu, kq, m);
+        if (qk_norm) {
+            kk += __shfl_xor_sync(0xffffffffu, kk, m);
+            qq += __shfl_xor_sync(0xffffffffu, qq, m);
+        }
+    }
+    // raw q, k (qk_norm): every term is linear in q and in k, so the reciprocal norms
+    // scale the reductions instead of the vectors
+    float nk = 1.f, nq = 1.f;
+    if (qk_norm) {
+        nk = 1.f / fmaxf(sqrtf(kk), kQkNormEps);
+        nq = 1.f / fmaxf(sqrtf(qq), kQkNormEps);
+    }
+    const float scale = rsqrtf((float)D), b = beta[unit];
+    const int j = 4 * c4;
+    float vj[4];
+    load_io4(v + (size_t)unit * D + j, vj);
+    const float rkv[4] = {rk.x, rk.y, rk.z, rk.w}, rqv[4] = {rq.x, rq.y, rq.z, rq.w};
+    float dl[4], ov[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        const float d = b * (vj[u] - rkv[u] * nk);
+        ov[u] = scale * (rqv[u] * nq + kq * (nk * nq) * d);
+        dl[u] = d * nk;  // the write k^ d^T = k (nk d)^T
+    }
+    if (rl == 0) store_io4(o + (size_t)unit * D + j, ov);
 
-    const float4 d4 = reinterpret_cast<const float4 *>(s_d)[c4];
 #pragma unroll
     for (int p = 0; p < P; ++p) {
-        const float ki = s_k[r0 + p * RPP];
+        const float ki = s_k[rl + p * RL];
         float4 x = s[p];
-        x.x += ki * d4.x; x.y += ki * d4.y; x.z += ki * d4.z; x.w += ki * d4.w;
-        __stcs(reinterpret_cast<float4 *>(S + (size_t)(r0 + p * RPP) * D) + c4, x);
+        x.x += ki * dl[0]; x.y += ki * dl[1]; x.z += ki * dl[2]; x.w += ki * dl[3];
+        __stcs(reinterpret_cast<float4 *>(S + (size_t)(rl + p * RL) * D) + c4, x);
     }
 }
 
