@@ -188,8 +188,8 @@ int seqsplit_lseg(int num_seqs, int64_t total_tokens, int num_heads)
 {
     if (num_seqs <= 0 || num_heads <= 0 || total_tokens <= 0) return 0;
     const int64_t units = (int64_t)num_seqs * num_heads;
-    // the transition pass runs 8 CTAs (R and M, four slices each) per segment and head
-    const int64_t kmax = 1 + kSplitSMs / (8 * units);
+    // the transition pass runs 4 CTAs (R and M, two 64-column slices each) per segment and head
+    const int64_t kmax = 1 + kSplitSMs / (4 * units);
     const int64_t avg = (total_tokens / kChunk + num_seqs) / num_seqs;  // chunks per sequence
     int64_t k = avg / kMinSegChunks;
     if (k > kmax) k = kmax;

@@ -66,19 +66,24 @@ struct ChunkLayout {
 static_assert(ChunkLayout::ST_NQ + 49152 <= ChunkLayout::O1, "N | Q' staging overlaps O1");
 static_assert(ChunkLayout::SOLVE_X + 32 * kLdX * 4 <= ChunkLayout::O1, "solve scratch overlaps O1");
 
-// State kernel (608 threads: sixteen state warps, two issuing warps, a copy warp): two
-// record stages, a ring of four v slices, the V^T operand of two chunks and the S operand
-// of two chunks.
-constexpr int kVRing = 4;
+// State kernel (608 threads: sixteen state warps, two issuing warps, a copy warp) over a
+// 64-column value slice: two record stages, a ring of three v slices, the V^T operand of
+// two chunks and the S operand of two chunks.
+constexpr int kSV = 64;                         // value columns per state CTA
+constexpr uint32_t kVBytes = kC * kSV * 2;      // one v slice [64 tokens][64] bf16, and V^T fp16
+constexpr uint32_t kSBytes = kD * kSV * 2;      // the S operand, bf16
+constexpr int kVRing = 3;
 struct StateLayout {
     static constexpr uint32_t STAGE = 75776;  // record + padding to 1024 bytes
-    static constexpr uint32_t VBOX = 2 * STAGE;               // kVRing x v slice [64][32] bf16
-    static constexpr uint32_t VIMG = VBOX + kVRing * 4096;    // 2 x V^T fp16, 32 rows x K 64
-    static constexpr uint32_t O7 = VIMG + 2 * 4096;           // 2 x S bf16, MN-major, K 128 x 32 columns
-    static constexpr uint32_t USED = O7 + 2 * 8192;
+    static constexpr uint32_t VBOX = 2 * STAGE;                 // kVRing x v slice [64][64] bf16
+    static constexpr uint32_t VIMG = VBOX + kVRing * kVBytes;   // 2 x V^T fp16, 64 rows x K 64
+    static constexpr uint32_t O7 = VIMG + 2 * kVBytes;          // 2 x S bf16, MN-major, K 128 x 64 columns
+    static constexpr uint32_t USED = O7 + 2 * kSBytes;
 };
 static_assert(StateLayout::STAGE % 1024 == 0 && StateLayout::STAGE >= kRecBytes, "stage size");
 static_assert(StateLayout::VIMG % 1024 == 0 && StateLayout::O7 % 1024 == 0, "operand alignment");
+static_assert(StateLayout::USED + 1024 <= 232448, "state kernel shared memory over the per-CTA limit");
+static_assert(kSV / 4 == 16, "a state warp's output columns are two 8-column halves");
 
 constexpr uint32_t kChunkSmem = ChunkLayout::USED + 1024;
 constexpr uint32_t kStateSmem = StateLayout::USED + 1024;
@@ -92,32 +97,6 @@ constexpr uint32_t TC_W = 0, TC_P2 = 128, TC_P = 192, TC_N = 0, TC_Q = 128, kChu
 __device__ __forceinline__ uint64_t mndesc(uint32_t addr, uint32_t panel_stride)
 {
     return sdesc(addr, panel_stride, 1024, kSw128B);
-}
-
-// T' = T diag(beta) split into bf16 high and low parts: [t][s] images at O4 and TL.
-template <class L, int NT>
-__device__ __forceinline__ void write_tprime_hilo(unsigned char *sm, const float *s_beta)
-{
-    const float *sT = reinterpret_cast<const float *>(sm + L::SOLVE_T);
-#pragma unroll
-    for (int e = threadIdx.x; e < 512; e += NT) {
-        const int r = e >> 3, s8 = (e & 7) * 8;
-        const float4 ta = *reinterpret_cast<const float4 *>(sT + r * kLdS + s8);
-        const float4 tb = *reinterpret_cast<const float4 *>(sT + r * kLdS + s8 + 4);
-        const float4 ba = *reinterpret_cast<const float4 *>(s_beta + s8);
-        const float4 bb = *reinterpret_cast<const float4 *>(s_beta + s8 + 4);
-        const float tv[8] = {ta.x, ta.y, ta.z, ta.w, tb.x, tb.y, tb.z, tb.w};
-        const float bv[8] = {ba.x, ba.y, ba.z, ba.w, bb.x, bb.y, bb.z, bb.w};
-        float hi[8], lo[8];
-#pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            const float t = s8 + u <= r ? tv[u] * bv[u] : 0.f;
-            hi[u] = __bfloat162float(__float2bfloat16_rn(t));
-            lo[u] = t - hi[u];
-        }
-        *reinterpret_cast<uint4 *>(sm + L::O4 + km16(r, s8, 64)) = pack_bf16x8(hi);
-        *reinterpret_cast<uint4 *>(sm + L::TL + km16(r, s8, 64)) = pack_bf16x8(lo);
-    }
 }
 
 // Kd^T = (k e^{g_last - g})^T as bf16 high and low parts, K-major [i][s] at KDH
@@ -206,22 +185,20 @@ __device__ __forceinline__ void issue_n_q(uint32_t sb, uint32_t tmem, bool with_
 template <int NT>
 __device__ __forceinline__ void epi_p2(uint32_t tmem, unsigned char *dst, bool &ok)
 {
-    constexpr int CW = 64 / (NT / 128);
+    constexpr int CW = 64 / (NT / 128), HW = CW / 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
-    const int r = quarter * 16 + (lane & 15);  // M = 64: row 16q + l in lane l < 16
+    const int r = quarter * 16 + (lane & 15), c0 = part * CW + (lane >> 4) * HW;  // M = 64: 16-lane loads
 #pragma unroll
-    for (int cb = 0; cb < CW; cb += 16) {
+    for (int cb = 0; cb < HW; cb += 16) {
         float v[16];
-        tmem_ld16(tmem + TC_P2 + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
+        tmem_ld16x2_x16<HW>(tmem + TC_P2 + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
         tmem_ld_wait();
-        if (lane < 16) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float x[8];
+        for (int hh = 0; hh < 2; ++hh) {
+            float x[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
-                *reinterpret_cast<uint4 *>(dst + km16(r, part * CW + cb + hh * 8, 64)) = pack_f16x8(x, ok);
-            }
+            for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
+            *reinterpret_cast<uint4 *>(dst + km16(r, c0 + cb + hh * 8, 64)) = pack_f16x8(x, ok);
         }
     }
 }
@@ -268,33 +245,31 @@ __device__ __forceinline__ void epi_n(uint32_t tmem, unsigned char *dst)
     }
 }
 
-// Q' = Qg + Aqk (-W); Qg from rows 64..127 of O1.
+// Q' = Qg + Aqk (-W); Qg from rows 64..127 of O1.  M = 64: 16-lane loads, as in w_epilogue.
 template <class L, int NT>
 __device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, unsigned char *dst)
 {
-    constexpr int CW = 128 / (NT / 128);
+    constexpr int CW = 128 / (NT / 128), HW = CW / 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
-    const int r = quarter * 16 + (lane & 15);
+    const int r = quarter * 16 + (lane & 15), c0 = part * CW + (lane >> 4) * HW;
 #pragma unroll
-    for (int cb = 0; cb < CW; cb += 16) {
+    for (int cb = 0; cb < HW; cb += 16) {
         float v[16];
-        tmem_ld16(tmem + TC_Q + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
+        tmem_ld16x2_x16<HW>(tmem + TC_Q + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
         tmem_ld_wait();
-        if (lane < 16) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                const int col = part * CW + cb + hh * 8;
-                const uint4 qraw = *reinterpret_cast<const uint4 *>(sm + L::O1 + km16(64 + r, col, 128));
-                const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
-                float x[8];
+        for (int hh = 0; hh < 2; ++hh) {
+            const int col = c0 + cb + hh * 8;
+            const uint4 qraw = *reinterpret_cast<const uint4 *>(sm + L::O1 + km16(64 + r, col, 128));
+            const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
+            float x[8];
 #pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qw[u]));
-                    x[2 * u] = qf.x + v[hh * 8 + 2 * u];
-                    x[2 * u + 1] = qf.y + v[hh * 8 + 2 * u + 1];
-                }
-                *reinterpret_cast<uint4 *>(dst + km16(r, col, 64)) = pack_bf16x8(x);
+            for (int u = 0; u < 4; ++u) {
+                const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qw[u]));
+                x[2 * u] = qf.x + v[hh * 8 + 2 * u];
+                x[2 * u + 1] = qf.y + v[hh * 8 + 2 * u + 1];
             }
+            *reinterpret_cast<uint4 *>(dst + km16(r, col, 64)) = pack_bf16x8(x);
         }
     }
 }
@@ -386,8 +361,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         kk_epilogue<L, NT>(sm, tmem, s_beta, sm + L::AQ);
         tc_fence_before_sync();
         __syncthreads();
-        solve_ut_doubling<L, NT>(sm);
-        write_tprime_hilo<L, NT>(sm, s_beta);
+        solve_ut_doubling<L, NT>(sm, s_beta);  // T' high / low images straight from the last level
         fence_proxy_async_smem();
         __syncthreads();
         if (tid == 0) {
@@ -456,25 +430,35 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 }
 
 // ============================================================== state kernel
-constexpr uint32_t IDESC_PV = idesc_f16(128, 32, false, false);   // P V
-constexpr uint32_t IDESC_NS = idesc_bf16(128, 32, false, true);   // N S (S MN-major)
-constexpr uint32_t IDESC_P2V = idesc_f16(64, 32, false, false);   // P2 V
-constexpr uint32_t IDESC_QS = idesc_bf16(64, 32, false, true);    // Q' S (S MN-major)
+constexpr uint32_t IDESC_PV = idesc_f16(128, kSV, false, false);   // P V
+constexpr uint32_t IDESC_NS = idesc_bf16(128, kSV, false, true);   // N S (S MN-major)
+constexpr uint32_t IDESC_P2V = idesc_f16(64, kSV, false, false);   // P2 V
+constexpr uint32_t IDESC_QS = idesc_bf16(64, kSV, false, true);    // Q' S (S MN-major)
 // TMEM columns: state increment (M = 128), outputs of two chunks (M = 64)
-constexpr uint32_t TM_5 = 0, TM_O = 32, kStateTmem = 128;
+constexpr uint32_t TM_5 = 0, TM_O = kSV, kStateTmem = 256;
+static_assert(TM_O + 2 * kSV <= kStateTmem, "state kernel TMEM map");
 // Warps 0-15 hold the state; warp 16 issues the chain MMAs; warp 17 copies and
 // converts; warp 18 issues the output MMAs.
 constexpr int kStateWarps = 16, kChainWarp = 16, kCopyWarp = 17, kOutWarp = 18;
 constexpr int kStateThreads = 19 * 32;
 constexpr int kL2Ahead = 3;  // records brought into L2 this many chunks ahead
+constexpr int kSCols = kSV / 4;  // state columns per state-warp thread (a row of a quarter of the slice)
 
-// The state operand S (K = state row i, N = value column j, 32 columns): MN-major, rows of
-// 64 bytes, 64-byte swizzle (8-row atoms of 512 bytes); one K step of 16 rows is 1024 bytes.
-__device__ __forceinline__ uint32_t mn64(int i, int j)
+// The state operand S (K = state row i, N = value column j, 64 columns): MN-major, rows of
+// 128 bytes, 128-byte swizzle (8-row atoms of 1024 bytes); one K step of 16 rows is 2048 bytes.
+__device__ __forceinline__ uint32_t mn_s(int i, int j) { return km16(i, j, kD); }
+__device__ __forceinline__ uint64_t sdesc_s(uint32_t addr) { return sdesc(addr, kSBytes, 1024, kSw128B); }
+// A state-warp thread's kSCols columns of state row i, as bf16, into the S operand image.
+__device__ __forceinline__ void store_s_operand(unsigned char *img, int i, int jp, const float (&S)[kSCols])
 {
-    return (uint32_t)(i * 64 + ((((j >> 3) ^ (i >> 1)) & 3) << 4) + ((j & 7) << 1));
+#pragma unroll
+    for (int q = 0; q < kSCols / 8; ++q) {
+        float x[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) x[u] = S[8 * q + u];
+        *reinterpret_cast<uint4 *>(img + mn_s(i, jp + 8 * q)) = pack_bf16x8(x);
+    }
 }
-__device__ __forceinline__ uint64_t sdesc_s(uint32_t addr) { return sdesc(addr, 512, 512, kSw64B); }
 
 // The chain group of one chunk: P V (fp16) + N S_c (bf16) into the M = 128 accumulator.
 // dr, dv, ds: descriptors of the record, the V^T image and the S image in use.
@@ -485,7 +469,7 @@ __device__ __forceinline__ void issue_chain(uint32_t acc, uint64_t dr, uint64_t 
         mma_bf16(acc, dr + ((R_P + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_PV, s > 0);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {  // + N S_c (bf16)
-        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32, offs = s * 1024;
+        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32, offs = s * 2048;
         mma_bf16(acc, dr + ((R_N + off) >> 4), ds + (offs >> 4), IDESC_NS, 1);
     }
 }
@@ -498,12 +482,12 @@ __device__ __forceinline__ void issue_out(uint32_t acc, uint64_t dr, uint64_t dv
         mma_bf16(acc, dr + ((R_P2 + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_P2V, s > 0);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {  // + Q' S_c (bf16)
-        const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32, offs = s * 1024;
+        const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32, offs = s * 2048;
         mma_bf16(acc, dr + ((R_Q + off) >> 4), ds + (offs >> 4), IDESC_QS, 1);
     }
 }
 
-// The serial pass over the chunks of one (sequence, head, 32-column value slice),
+// The serial pass over the chunks of one (sequence, head, 64-column value slice),
 // as four roles that meet only at mbarriers (no block-wide barrier per chunk):
 //   bar_ready[c&1]  S_c and V_c (both written by the 16 state warps) are in shared memory
 //   bar_rec[c&1]    record c has arrived
@@ -550,7 +534,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     // initial states and the value rows are read at once, the records only after pdl_wait
     // (the chunk kernel's completion), so this prologue overlaps that kernel's last CTAs
     const bool ident = (int)blockIdx.z >= z_ident;
-    const int j0 = blockIdx.x * kDV, h = blockIdx.y, n = order[ident ? blockIdx.z - z_ident : blockIdx.z];
+    const int j0 = blockIdx.x * kSV, h = blockIdx.y, n = order[ident ? blockIdx.z - z_ident : blockIdx.z];
     int64_t t0, t1;
     seq_range(cu, n, total, t0, t1);
     const int nchunks = (int)((t1 - t0 + kC - 1) / kC);
@@ -572,8 +556,8 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
         rec_issued = k + 1;
     };
     auto load_v = [&](int k) {
-        mbar_arrive_expect_tx(&bar_v[k % kVRing], 4096);
-        tma_load_3d(sm + L::VBOX + (k % kVRing) * 4096, tmv, &bar_v[k % kVRing], j0, h,
+        mbar_arrive_expect_tx(&bar_v[k % kVRing], kVBytes);
+        tma_load_3d(sm + L::VBOX + (k % kVRing) * kVBytes, tmv, &bar_v[k % kVRing], j0, h,
                     (int)(t0 + (int64_t)k * kC));
         v_issued = k + 1;
     };
@@ -594,25 +578,25 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
         tmem_alloc(&tmem_holder, kStateTmem);
         tmem_relinquish();
     }
-    // state row i, columns j0 + 8*part .. +7 in registers; S (bf16) operands in O7
-    const int i_row = quarter * 32 + lane, jp = part * 8;
-    float S[8];
+    // state row i, columns j0 + jp .. jp + kSCols - 1 in registers; S (bf16) operands in O7
+    const int i_row = quarter * 32 + lane, jp = part * kSCols;
+    float S[kSCols];
     const size_t st_off = ((size_t)h * kD + i_row) * kD + j0 + jp, st_entry = (size_t)H * kD * kD;
     if (state_warp) {
         if (ident) {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) S[j] = i_row == j0 + jp + j ? 1.f : 0.f;
+            for (int j = 0; j < kSCols; ++j) S[j] = i_row == j0 + jp + j ? 1.f : 0.f;
         } else if (si >= 0) {
 #pragma unroll
-            for (int q = 0; q < 2; ++q) {
+            for (int q = 0; q < kSCols / 4; ++q) {
                 const float4 x = *reinterpret_cast<const float4 *>(init_state + si * st_entry + st_off + 4 * q);
                 S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
             }
         } else {
 #pragma unroll
-            for (int j = 0; j < 8; ++j) S[j] = 0.f;
+            for (int j = 0; j < kSCols; ++j) S[j] = 0.f;
         }
-        *reinterpret_cast<uint4 *>(sm + L::O7 + mn64(i_row, jp)) = pack_bf16x8(S);
+        store_s_operand(sm + L::O7, i_row, jp, S);
     }
     fence_proxy_async_smem();
     __syncthreads();  // barriers initialised, S_0 written
@@ -631,37 +615,37 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
         return mbar_wait_ns(&bar_rec[c & 1], (uint32_t)((c >> 1) & 1), kWaitNs);
     };
 
-    // o rows of chunk cp (M = 64 accumulator TM_O + 32*(cp&1)), once its MMAs finished
+    // o rows of chunk cp (M = 64 accumulator TM_O + kSV*(cp&1)), once its MMAs finished
     // (with no outputs wanted the barrier still marks the chunk's operands as released)
     auto write_o = [&](int cp) -> bool {
         if (!mbar_wait_ns(&bar_o[cp & 1], (uint32_t)((cp >> 1) & 1), kWaitNs)) return false;
         if (!o) return true;
         tc_fence_after_sync();
+        // the warp's kSCols columns: eight per half-warp, one 16-byte store per thread
         float v[8];
-        tmem_ld8(tmem + TM_O + 32 * (cp & 1) + lane_off + jp, v);
+        tmem_ld16x2_x8<8>(tmem + TM_O + kSV * (cp & 1) + lane_off + jp, v);
         tmem_ld_wait();
         const int64_t cs = t0 + (int64_t)cp * kC;
-        if (lane < 16 && cs + r64 < t1)
-            *reinterpret_cast<uint4 *>(o + ((size_t)(cs + r64) * H + h) * kD + j0 + jp) = pack_bf16x8(v);
+        if (cs + r64 < t1)
+            *reinterpret_cast<uint4 *>(o + ((size_t)(cs + r64) * H + h) * kD + j0 + jp + 8 * (lane >> 4)) =
+                pack_bf16x8(v);
         return true;
     };
     // state warps: the v slice of chunk k -> V^T fp16 K-major in VIMG[k & 1]; one
-    // 4-row group of one column per thread
+    // 8-row group of one column per thread
     auto convert_v = [&](int k) -> bool {
         if (!mbar_wait_ns(&bar_v[k % kVRing], (uint32_t)((k / kVRing) & 1), kWaitNs)) return false;
         const int64_t ck = t0 + (int64_t)k * kC;
         const int lenk = (t1 - ck) < kC ? (int)(t1 - ck) : kC;
-        const unsigned char *box = sm + L::VBOX + (k % kVRing) * 4096;
-        const int j = tid % kDV, s4 = (tid / kDV) * 4;
-        float x[4];
+        const unsigned char *box = sm + L::VBOX + (k % kVRing) * kVBytes;
+        const int j = tid % kSV, s8 = (tid / kSV) * 8;
+        float x[8];
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-            x[u] = (s4 + u) < lenk ? bf16_at(box + ((s4 + u) * kDV + j) * 2) : 0.f;
+        for (int u = 0; u < 8; ++u) {
+            x[u] = (s8 + u) < lenk ? bf16_at(box + ((s8 + u) * kSV + j) * 2) : 0.f;
             range_ok &= fabsf(x[u]) <= 65504.f;
         }
-        __half2 a = __floats2half2_rn(x[0], x[1]), b = __floats2half2_rn(x[2], x[3]);
-        *reinterpret_cast<uint2 *>(sm + L::VIMG + (k & 1) * 4096 + km16(j, s4, kDV)) =
-            make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+        *reinterpret_cast<uint4 *>(sm + L::VIMG + (k & 1) * kVBytes + km16(j, s8, kSV)) = pack_f16x8_plain(x);
         return true;
     };
 
@@ -696,12 +680,12 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
                 if (ok) ok = mbar_wait_ns(&bar_s, (uint32_t)(c & 1), kWaitNs);
                 if (ok) {  // S <- gamma . S + (P V + N S); its bf16 operand image for the next chunk
                     tc_fence_after_sync();
-                    float v[8];
-                    tmem_ld8(tmem + TM_5 + lane_off + jp, v);
+                    float v[kSCols];
+                    tmem_ld16(tmem + TM_5 + lane_off + jp, v);
                     tmem_ld_wait();
 #pragma unroll
-                    for (int j = 0; j < 8; ++j) S[j] = fmaf(gc, S[j], v[j]);
-                    *reinterpret_cast<uint4 *>(sm + L::O7 + (st ^ 1) * 8192 + mn64(i_row, jp)) = pack_bf16x8(S);
+                    for (int j = 0; j < kSCols; ++j) S[j] = fmaf(gc, S[j], v[j]);
+                    store_s_operand(sm + L::O7 + (st ^ 1) * kSBytes, i_row, jp, S);
                     fence_proxy_async_smem();
                 }
                 tc_fence_before_sync();  // this warp's TMEM reads precede the arrival
@@ -718,13 +702,13 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
                     if (ok) {
                         tc_fence_after_sync();
                         // descriptors: base of each operand plus the constant byte offset >> 4
-                        const uint64_t dr = d_rec0 + st * (L::STAGE >> 4), dv = d_v0 + st * (4096 >> 4),
-                                       ds = d_s0 + st * (8192 >> 4);
+                        const uint64_t dr = d_rec0 + st * (L::STAGE >> 4), dv = d_v0 + st * (kVBytes >> 4),
+                                       ds = d_s0 + st * (kSBytes >> 4);
                         if (chain) {
                             issue_chain(tmem + TM_5, dr, dv, ds);
                             mma_commit(&bar_s);
                         } else {
-                            if (o) issue_out(tmem + TM_O + 32 * st, dr, dv, ds);  // none when no outputs are wanted
+                            if (o) issue_out(tmem + TM_O + kSV * st, dr, dv, ds);  // none when no outputs are wanted
                             mma_commit(&bar_o[st]);  // also marks chunk c's operands as released
                         }
                     }
@@ -759,7 +743,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     } else if (state_warp && sf >= 0) {
         float *dst = fpool + sf * st_entry + st_off;
 #pragma unroll
-        for (int q = 0; q < 2; ++q)
+        for (int q = 0; q < kSCols / 4; ++q)
             *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
     }
     if (!range_ok) atomicOr(status, DEV_ERR_RANGE);
@@ -773,17 +757,18 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
 // back `reps` times per CTA by the same routines the kernels use, on a constant operand
 // image resident in shared memory: no epilogues, no waits between groups, no global
 // traffic.  PASS 0: the chunk kernel's groups of one (chunk, head) item (k-k and q-k, W,
-// P2, the three-term P, N, Q''), two CTAs per SM as that kernel runs.  PASS 1: the state
-// kernel's chain and output groups of one chunk and 32-column slice, one CTA per SM.
+// P2, the three-term P, N, Q''), issued by one thread, two CTAs per SM as that kernel runs.
+// PASS 1: the state kernel's chain and output groups of one chunk and 64-column slice,
+// one CTA per SM, each group issued by a thread of its own warp as in that kernel.
 constexpr uint64_t kDiagFlops[2] = {
     2ull * (128 * 64 * 128 + 64 * 128 * 64 + 64 * 64 * 64 + 3 * 128 * 64 * 64 + 128 * 128 * 64 + 64 * 128 * 64),
-    2ull * (128 * 32 * 64 + 128 * 32 * 128 + 64 * 32 * 64 + 64 * 32 * 128)};
+    2ull * (128 * kSV * 64 + 128 * kSV * 128 + 64 * kSV * 64 + 64 * kSV * 128)};
 
 template <int PASS>
 __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(int reps, uint32_t *status)
 {
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t bar, bar_drain;
+    __shared__ __align__(8) uint64_t bar[2], bar_drain;
     __shared__ uint32_t tmem_holder;
     constexpr uint32_t used = PASS == 0 ? ChunkLayout::USED : StateLayout::USED;
     constexpr uint32_t cols = PASS == 0 ? kChunkTmem : kStateTmem;
@@ -795,8 +780,9 @@ __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(in
         reinterpret_cast<uint4 *>(sm)[e] = make_uint4(0x3c003c00u, 0x3c003c00u, 0x3c003c00u, 0x3c003c00u);
     fence_proxy_async_smem();
     if (tid == 0) {
-        mbar_init(&bar, 1);
-        mbar_init(&bar_drain, 1);
+        mbar_init(&bar[0], 1);
+        mbar_init(&bar[1], 1);
+        mbar_init(&bar_drain, PASS == 0 ? 1 : 2);
         fence_mbar_init();
     }
     if (tid < 32) {
@@ -806,7 +792,10 @@ __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(in
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_holder;
-    if (tid == 0) {
+    // PASS 0: thread 0 issues everything; PASS 1: thread 0 the chain group, thread 128 the
+    // output group
+    const int issuer = tid == 0 ? 0 : (PASS == 1 && tid == 128 ? 1 : -1);
+    if (issuer >= 0) {
         bool ok = true;
         for (int r = 0; r < reps && ok; ++r) {
             if (PASS == 0) {
@@ -816,19 +805,20 @@ __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(in
                 issue_n_q<ChunkLayout>(sb, tmem, true);
             } else {
                 const uint64_t dr = kdesc(sb), dv = kdesc(sb + StateLayout::VIMG), ds = sdesc_s(sb + StateLayout::O7);
-                issue_chain(tmem + TM_5, dr, dv, ds);
-                issue_out(tmem + TM_O, dr, dv, ds);
+                if (issuer == 0)
+                    issue_chain(tmem + TM_5, dr, dv, ds);
+                else
+                    issue_out(tmem + TM_O, dr, dv, ds);
             }
-            mma_commit(&bar);
-            ok = mbar_wait_ns(&bar, (uint32_t)(r & 1), kWaitNs);
+            mma_commit(&bar[issuer]);
+            ok = mbar_wait_ns(&bar[issuer], (uint32_t)(r & 1), kWaitNs);
             tc_fence_after_sync();
         }
-        if (!ok) {
-            atomicOr(status, DEV_ERR_TIMEOUT);
-            mma_commit(&bar_drain);  // every MMA issued so far completes before the drain barrier
-            (void)mbar_wait_ns(&bar_drain, 0, kWaitNs);
-        }
+        if (!ok) atomicOr(status, DEV_ERR_TIMEOUT);
     }
+    // a drain barrier that every issuer commits to: all MMAs complete before TMEM is freed
+    if (issuer >= 0) mma_commit(&bar_drain);
+    if (tid == 0) (void)mbar_wait_ns(&bar_drain, 0, kWaitNs);
     tc_fence_before_sync();
     __syncthreads();
     if (tid < 32) tmem_dealloc(tmem, cols);
@@ -892,7 +882,7 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     CUtensorMap tq, tk, tv;
     if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, p.total_tokens, p.num_heads, 2, kD) ||
         !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, p.total_tokens, p.num_heads, 2, kD) ||
-        !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kDV))
+        !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kSV))
         return cudaErrorInvalidValue;
     const int64_t chunk_bound = p.total_tokens / kC + p.num_seqs;
     if (chunk_bound * p.num_heads > INT32_MAX || !p.desc || p.chunk_bound != chunk_bound)
@@ -920,7 +910,7 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     const unsigned char *rec = static_cast<const unsigned char *>(records);
     __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
     if (p.split.lseg == 0) {
-        cfg.gridDim = dim3(kD / kDV, p.num_heads, p.num_seqs);
+        cfg.gridDim = dim3(kD / kSV, p.num_heads, p.num_seqs);
         return cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, tv, p.cu_seqlens, p.total_tokens, p.num_heads,
                                   static_cast<const int32_t *>(cc), rec, p.init_state, o, p.final_state, p.status,
                                   static_cast<const int32_t *>(p.order), p.slots, INT_MAX, (float *)nullptr);
@@ -928,12 +918,12 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     // sequence split: transition pass (R for grid z < nv_max, M above), start states, state pass
     const SeqSplit &s = p.split;
     CUtensorMap tz;  // one zero value row: every box of the transition pass reads zeros
-    if (!make_map(&tz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s.vzero, 1, p.num_heads, 2, kDV))
+    if (!make_map(&tz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s.vzero, 1, p.num_heads, 2, kSV))
         return cudaErrorInvalidValue;
     StateSlots sa;
     sa.fin = s.fin_a;
     sa.num = (int64_t)s.nv_max + 1;
-    cfg.gridDim = dim3(kD / kDV, p.num_heads, 2 * s.nv_max);
+    cfg.gridDim = dim3(kD / kSV, p.num_heads, 2 * s.nv_max);
     err = cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, tz, (const int32_t *)s.vcu, p.total_tokens,
                              p.num_heads, (const int32_t *)s.vcc, rec, (const float *)nullptr,
                              (__nv_bfloat16 *)nullptr, s.R, p.status, (const int32_t *)s.vorder, sa, s.nv_max, s.M);
@@ -944,7 +934,7 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     sc.fin = s.fin_c;
     const int64_t user_entries = p.slots.fin ? p.slots.num : p.num_seqs;
     sc.num = user_entries > (int64_t)s.nv_max + 1 ? user_entries : (int64_t)s.nv_max + 1;
-    cfg.gridDim = dim3(kD / kDV, p.num_heads, s.nv_max);
+    cfg.gridDim = dim3(kD / kSV, p.num_heads, s.nv_max);
     return cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, tv, (const int32_t *)s.vcu, p.total_tokens,
                               p.num_heads, (const int32_t *)s.vcc, rec, (const float *)s.start, o, p.final_state,
                               p.status, (const int32_t *)s.vorder, sc, INT_MAX, (float *)nullptr);

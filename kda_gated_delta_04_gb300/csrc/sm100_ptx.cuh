@@ -258,6 +258,32 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8])
                  : "r"(taddr));
 }
 
+// An M = 64 accumulator keeps its rows in lanes 0-15 of each lane quarter.  These loads
+// read 16 lanes with every thread of the warp: thread t < 16 gets lane (quarter base + t)
+// at columns [c, c + N), thread t >= 16 gets lane (quarter base + t - 16) at columns
+// [c + HALF, c + HALF + N) (the 16x32bx2 shape; HALF is the immediate half-split offset).
+template <int HALF>
+__device__ __forceinline__ void tmem_ld16x2_x8(uint32_t taddr, float (&r)[8])
+{
+    uint32_t *u = reinterpret_cast<uint32_t *>(r);
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8], %9;"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]),
+                   "=r"(u[6]), "=r"(u[7])
+                 : "r"(taddr), "n"(HALF));
+}
+template <int HALF>
+__device__ __forceinline__ void tmem_ld16x2_x16(uint32_t taddr, float (&r)[16])
+{
+    uint32_t *u = reinterpret_cast<uint32_t *>(r);
+    asm volatile(
+        "tcgen05.ld.sync.aligned.16x32bx2.x16.b32 "
+        "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16], %17;"
+        : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3]), "=r"(u[4]), "=r"(u[5]), "=r"(u[6]),
+          "=r"(u[7]), "=r"(u[8]), "=r"(u[9]), "=r"(u[10]), "=r"(u[11]), "=r"(u[12]),
+          "=r"(u[13]), "=r"(u[14]), "=r"(u[15])
+        : "r"(taddr), "n"(HALF));
+}
+
 __device__ __forceinline__ void tmem_ld_wait()
 {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");

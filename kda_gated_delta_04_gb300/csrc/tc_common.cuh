@@ -59,6 +59,18 @@ __device__ __forceinline__ uint4 pack_f16x8(const float (&x)[8], bool &ok)
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// Eight fp16 values (round to nearest even), no range check.
+__device__ __forceinline__ uint4 pack_f16x8_plain(const float (&x)[8])
+{
+    uint32_t w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        __half2 h = __floats2half2_rn(x[2 * u], x[2 * u + 1]);
+        w[u] = *reinterpret_cast<uint32_t *>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
 __device__ __forceinline__ float bf16_at(const unsigned char *p)
 {
     return __bfloat162float(*reinterpret_cast<const __nv_bfloat16 *>(p));
@@ -384,6 +396,23 @@ __device__ __forceinline__ float4 add_pair_lanes(float4 a)
     return a;
 }
 
+// T' = T diag(beta) for one quad of four columns of row r, as bf16 high and low parts
+// into the [t][s] images at L::O4 and L::TL (8 bytes each).
+template <class L>
+__device__ __forceinline__ void store_tprime_quad(unsigned char *sm, int r, int c, float4 t, const float *s_beta)
+{
+    const float4 bq = *reinterpret_cast<const float4 *>(s_beta + c);
+    const float tv[4] = {t.x * bq.x, t.y * bq.y, t.z * bq.z, t.w * bq.w};
+    float hi[4], lo[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+        hi[u] = __bfloat162float(__float2bfloat16_rn(tv[u]));
+        lo[u] = tv[u] - hi[u];
+    }
+    *reinterpret_cast<uint2 *>(sm + L::O4 + km16(r, c, 64)) = make_uint2(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]));
+    *reinterpret_cast<uint2 *>(sm + L::TL + km16(r, c, 64)) = make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
+}
+
 // solve_ut_doubling: the same T, in place (SOLVE_T == SOLVE_A), by recursive
 // doubling all the way from 4 x 4 blocks: the sixteen 4 x 4 diagonal blocks by
 // substitution, then for block size b = 4, 8, 16, 32 and every pair of b x b
@@ -391,12 +420,16 @@ __device__ __forceinline__ float4 add_pair_lanes(float4 a)
 // each 16 x 16 diagonal block is done by one warp with warp barriers only.
 // Each output quad is one thread's float4; the strictly upper parts of A, which
 // the k-k epilogue zeroed, stand in for the zero upper parts of T, so no product
-// needs a mask.  Contains barriers.
+// needs a mask.  The last level writes T' = T diag(beta) straight into its bf16
+// high and low images (L::O4, L::TL): the diagonal 32 x 32 quadrants while X is
+// formed, the lower-left one as it is formed, zeros above; T itself is not
+// completed in fp32.  Contains barriers; the caller fences and synchronises
+// before the images are read.
 template <class L, int NT>
-__device__ __forceinline__ void solve_ut_doubling(unsigned char *sm)
+__device__ __forceinline__ void solve_ut_doubling(unsigned char *sm, const float *s_beta)
 {
     static_assert(L::SOLVE_A == L::SOLVE_T, "the doubling solve works in place");
-    static_assert(NT >= 128, "four warps take the diagonal 16 x 16 blocks");
+    static_assert(NT == 256, "the last level maps one output quad to each thread");
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float *sT = reinterpret_cast<float *>(sm + L::SOLVE_T);  // holds A until overwritten
     float *sX = reinterpret_cast<float *>(sm + L::SOLVE_X);
@@ -454,22 +487,20 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm)
         }
     }
     __syncthreads();
-    // 2. The 16 and 32 levels across the CTA.  Where a level has fewer output quads than
-    //    the CTA has threads, two adjacent lanes share a quad: each takes every other
-    //    group of four m and a shuffle adds the halves.
-#pragma unroll
-    for (int b = 16; b <= 32; b *= 2) {
-        const int quads = b / 4, items = 32 * quads;
-        const int P = NT >= 2 * items ? 2 : 1;  // threads per output quad (warp-uniform loops)
-        // X = A_10 T_00: a warp shares one column quad cq over the 32 rows of X, so
-        // the loop can start at m = cq (T_00[m][cq..cq+3] = 0 for m < cq); A is read
-        // four m at a time (rows 272 bytes apart: conflict-free float4 loads)
-        for (int it = tid; it < items * P; it += NT) {
-            const int e = it / P, half = it % P;
+    // 2. The 16 level across the CTA: two pairs of 16 x 16 blocks, 128 output quads, two
+    //    adjacent lanes per quad (each takes every other group of four m; a shuffle adds
+    //    the halves).
+    {
+        constexpr int b = 16, quads = 4, items = 32 * quads;
+        // X = A_10 T_00: a warp shares one column quad cq over the 32 rows of X, so the
+        // loop can start at m = cq (T_00[m][cq..cq+3] = 0 for m < cq); A is read four m at
+        // a time (rows 272 bytes apart: conflict-free float4 loads)
+        for (int it = tid; it < items * 2; it += NT) {
+            const int e = it / 2, half = it % 2;
             const int xr = e & 31, cq = (e >> 5) * 4, p = xr / b, rr = xr % b;
             const int R0 = 2 * b * p + b, C0 = 2 * b * p;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int m4 = cq + 4 * half; m4 < b; m4 += 4 * P) {
+            for (int m4 = cq + 4 * half; m4 < b; m4 += 8) {
                 const float4 a = *reinterpret_cast<const float4 *>(sT + (R0 + rr) * kLdS + C0 + m4);
                 const float av[4] = {a.x, a.y, a.z, a.w};
 #pragma unroll
@@ -478,18 +509,18 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm)
                     acc.x += av[u] * t.x; acc.y += av[u] * t.y; acc.z += av[u] * t.z; acc.w += av[u] * t.w;
                 }
             }
-            if (P == 2) acc = add_pair_lanes(acc);
+            acc = add_pair_lanes(acc);
             if (half == 0) *reinterpret_cast<float4 *>(sX + xr * kLdX + cq) = acc;
         }
         __syncthreads();
         // T_10 = -T_11 X over A_10: row rr needs m <= rr only (T_11 is lower triangular);
         // a warp covers few consecutive rows, so its trip counts stay close
-        for (int it = tid; it < items * P; it += NT) {
-            const int e = it / P, half = it % P;
+        for (int it = tid; it < items * 2; it += NT) {
+            const int e = it / 2, half = it % 2;
             const int xr = e / quads, cq = (e % quads) * 4, p = xr / b, rr = xr % b;
             const int R0 = 2 * b * p + b, C0 = 2 * b * p;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int m4 = 4 * half; m4 <= rr; m4 += 4 * P) {
+            for (int m4 = 4 * half; m4 <= rr; m4 += 8) {
                 const float4 t = *reinterpret_cast<const float4 *>(sT + (R0 + rr) * kLdS + R0 + m4);
                 const float tv[4] = {t.x, t.y, t.z, t.w};
 #pragma unroll
@@ -498,12 +529,51 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm)
                     acc.x += tv[u] * x.x; acc.y += tv[u] * x.y; acc.z += tv[u] * x.z; acc.w += tv[u] * x.w;
                 }
             }
-            if (P == 2) acc = add_pair_lanes(acc);
+            acc = add_pair_lanes(acc);
             if (half == 0)
                 *reinterpret_cast<float4 *>(sT + (R0 + rr) * kLdS + C0 + cq) =
                     make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
         __syncthreads();
+    }
+    // 3. The 32 level: one pair of 32 x 32 blocks, one output quad per thread.  T_00 and
+    //    T_11 are final now: each thread also sends one quad of each to the T' images and
+    //    zeros one quad of the upper-right quadrant.
+    {
+        const int xr = tid & 31, cq = (tid >> 5) * 4;  // X = A_10 T_00 (rows 32.., columns 0..31)
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int m4 = cq; m4 < 32; m4 += 4) {
+            const float4 a = *reinterpret_cast<const float4 *>(sT + (32 + xr) * kLdS + m4);
+            const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 t = *reinterpret_cast<const float4 *>(sT + (m4 + u) * kLdS + cq);
+                acc.x += av[u] * t.x; acc.y += av[u] * t.y; acc.z += av[u] * t.z; acc.w += av[u] * t.w;
+            }
+        }
+        *reinterpret_cast<float4 *>(sX + xr * kLdX + cq) = acc;
+        const int r = tid >> 3, c = (tid & 7) * 4;  // this thread's quad of each 32 x 32 quadrant
+        store_tprime_quad<L>(sm, r, c, *reinterpret_cast<const float4 *>(sT + r * kLdS + c), s_beta);
+        store_tprime_quad<L>(sm, 32 + r, 32 + c, *reinterpret_cast<const float4 *>(sT + (32 + r) * kLdS + 32 + c),
+                             s_beta);
+        *reinterpret_cast<uint2 *>(sm + L::O4 + km16(r, 32 + c, 64)) = make_uint2(0u, 0u);
+        *reinterpret_cast<uint2 *>(sm + L::TL + km16(r, 32 + c, 64)) = make_uint2(0u, 0u);
+    }
+    __syncthreads();
+    {
+        // T_10 = -T_11 X straight into the T' images (row 32 + rr, columns cq..cq+3)
+        const int rr = tid >> 3, cq = (tid & 7) * 4;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int m4 = 0; m4 <= rr; m4 += 4) {
+            const float4 t = *reinterpret_cast<const float4 *>(sT + (32 + rr) * kLdS + 32 + m4);
+            const float tv[4] = {t.x, t.y, t.z, t.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float4 x = *reinterpret_cast<const float4 *>(sX + (m4 + u) * kLdX + cq);
+                acc.x += tv[u] * x.x; acc.y += tv[u] * x.y; acc.z += tv[u] * x.z; acc.w += tv[u] * x.w;
+            }
+        }
+        store_tprime_quad<L>(sm, 32 + rr, cq, make_float4(-acc.x, -acc.y, -acc.z, -acc.w), s_beta);
     }
 }
 
@@ -546,27 +616,26 @@ __device__ __forceinline__ void issue_gw(uint32_t sb, uint32_t dw)
                  idesc, s > 0);
 }
 
-// -W into rows 0-63 of O1 (Kg no longer needed).  The M = 64 accumulator keeps
-// row 16q + l in lane l < 16 of lane quarter q; a warp takes 128/(NT/128) columns.
+// -W into rows 0-63 of O1 (Kg no longer needed).  The M = 64 accumulator keeps row
+// 16q + l in lane l < 16 of lane quarter q; a warp takes 128/(NT/128) columns, its two
+// half-warps one half each (16-lane loads, so every thread of the warp works).
 template <class L, int NT>
 __device__ __forceinline__ void w_epilogue(unsigned char *sm, uint32_t dw)
 {
-    constexpr int CW = 128 / (NT / 128);
+    constexpr int CW = 128 / (NT / 128), HW = CW / 2;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, quarter = warp & 3, part = warp >> 2;
-    const int r = quarter * 16 + (lane & 15);
+    const int r = quarter * 16 + (lane & 15), c0 = part * CW + (lane >> 4) * HW;
 #pragma unroll
-    for (int cb = 0; cb < CW; cb += 16) {
+    for (int cb = 0; cb < HW; cb += 16) {
         float v[16];
-        tmem_ld16(dw + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
+        tmem_ld16x2_x16<HW>(dw + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
         tmem_ld_wait();
-        if (lane < 16) {
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float x[8];
+        for (int hh = 0; hh < 2; ++hh) {
+            float x[8];
 #pragma unroll
-                for (int u = 0; u < 8; ++u) x[u] = -v[hh * 8 + u];
-                *reinterpret_cast<uint4 *>(sm + L::O1 + km16(r, part * CW + cb + hh * 8, 128)) = pack_bf16x8(x);
-            }
+            for (int u = 0; u < 8; ++u) x[u] = -v[hh * 8 + u];
+            *reinterpret_cast<uint4 *>(sm + L::O1 + km16(r, c0 + cb + hh * 8, 128)) = pack_bf16x8(x);
         }
     }
 }
