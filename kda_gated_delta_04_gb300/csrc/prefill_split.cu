@@ -42,11 +42,15 @@ constexpr uint32_t R_GM = 73728;   // gamma, 128 fp32
 constexpr uint32_t kRecBytes = 74240;
 static_assert(kRecBytes % 16 == 0, "records are moved by bulk copies");
 
-// Chunk kernel: 256 threads and 105 KB of shared memory, so two CTAs share an
-// SM and hide each other's latencies.  CTAs take the chunks last to first, so
-// the records the serial pass reads first are the ones written last (most
-// likely still in L2).
-constexpr int kChunkThreads = 256;
+// Chunk kernel: eight compute warps and one issuing warp (288 threads) and 105 KB
+// of shared memory, so two CTAs share an SM and hide each other's latencies.  The
+// issuing warp owns the barriers, the TMEM allocation, every MMA group and every
+// bulk store, so the compute warps go on to their next phase as soon as a group is
+// handed off.  CTAs take the chunks last to first, so the records the serial pass
+// reads first are the ones written last (most likely still in L2).
+constexpr int kChunkCompute = 256;                  // compute threads (warps 0-7)
+constexpr int kChunkThreads = kChunkCompute + 32;   // + the issuing warp
+constexpr int kChunkIssuer = kChunkCompute;         // its lane 0 issues
 struct ChunkLayout {
     static constexpr uint32_t IN_K = 0, IN_Q = 16384;  // TMA boxes; k lives until the Kd build
     static constexpr uint32_t O2 = 32768;   // Ki bf16, 64 rows x 128 (B of the k-k product)
@@ -283,7 +287,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                      unsigned char *__restrict__ records, uint32_t *status, bool with_o, bool scalar_gate)
 {
     using L = ChunkLayout;
-    constexpr int NT = kChunkThreads;
+    constexpr int NT = kChunkCompute;  // the compute threads' mappings are over 256 threads
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar_tma, bar_mma, bar_p, bar_drain;
     __shared__ uint32_t tmem_holder;
@@ -308,7 +312,9 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5;
-    if (tid == 0) {
+    const bool compute = tid < kChunkCompute, issuer = tid == kChunkIssuer;
+    constexpr int kIssueWarp = kChunkIssuer / 32;
+    if (issuer) {
         mbar_init(&bar_tma, 1);
         mbar_init(&bar_mma, 1);
         mbar_init(&bar_p, 1);
@@ -318,7 +324,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         tma_load_3d(sm + L::IN_Q, &tm_q, &bar_tma, 0, h, (int)c0);
         tma_load_3d(sm + L::IN_K, &tm_k, &bar_tma, 0, h, (int)c0);
     }
-    if (warp == 0) {
+    if (warp == kIssueWarp) {
         tmem_alloc(&tmem_holder, kChunkTmem);
         tmem_relinquish();
     }
@@ -327,30 +333,33 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     // overlapping the q/k copies
     float *s_tot = reinterpret_cast<float *>(sm + L::AQ);
     float2 gl[4096 / NT];
-    float gmin, gmax;
-    if (scalar_gate)  // log_alpha [T, H]: one decay per token-head
-        prefix_scan<NT>(log_alpha + (size_t)c0 * H + h, H, len, s_tot, gl, gmin, gmax, true);
-    else
-        prefix_scan<NT>(log_alpha + ((size_t)c0 * H + h) * kD, H * kD, len, s_tot, gl, gmin, gmax);
+    float gmin = 0.f, gmax = 0.f;
+    if (compute) {
+        if (scalar_gate)  // log_alpha [T, H]: one decay per token-head
+            prefix_scan<NT>(log_alpha + (size_t)c0 * H + h, H, len, s_tot, gl, gmin, gmax, true);
+        else
+            prefix_scan<NT>(log_alpha + ((size_t)c0 * H + h) * kD, H * kD, len, s_tot, gl, gmin, gmax);
+    }
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_holder;
     bool timed_out = false, tma_pending = true, decay_bad = false, range_ok = true, stores_pending = false;
     do {
-        bool ok = mbar_wait_ns(&bar_tma, 0, kWaitNs);
+        bool ok = !compute || mbar_wait_ns(&bar_tma, 0, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tma_pending = false;
         if (NORM) {
-            qk_row_inv_norms<NT>(sm + L::IN_K, sm + L::IN_Q, s_rn);
+            if (compute) qk_row_inv_norms<NT>(sm + L::IN_K, sm + L::IN_Q, s_rn);
             __syncthreads();
         }
         float2 ot[2];
-        decay_bad = decayed_operands<L, NT, false, NORM>(sm, len, s_tot, nullptr,
-                                                   reinterpret_cast<float *>(rec + R_GM), gl, gmin, gmax, ot,
-                                                   s_rn);
+        if (compute)
+            decay_bad = decayed_operands<L, NT, false, NORM>(sm, len, s_tot, nullptr,
+                                                       reinterpret_cast<float *>(rec + R_GM), gl, gmin, gmax, ot,
+                                                       s_rn);
         fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0) {
+        if (issuer) {
             tc_fence_after_sync();
             issue_g1<L>(sb, tmem);
             mma_commit(&bar_mma);
@@ -358,21 +367,23 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         ok = mbar_wait_ns(&bar_mma, 0, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
-        kk_epilogue<L, NT>(sm, tmem, s_beta, sm + L::AQ);
-        tc_fence_before_sync();
-        __syncthreads();
-        solve_ut_doubling<L, NT>(sm, s_beta);  // T' high / low images straight from the last level
+        if (compute) {
+            kk_epilogue<L, NT>(sm, tmem, s_beta, sm + L::AQ);
+            tc_fence_before_sync();
+            asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");  // A complete for the solve
+            solve_ut_doubling<L, NT>(sm, s_beta);  // T' high / low images straight from the last level
+        }
         fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0) {
+        if (issuer) {
             tc_fence_after_sync();
             issue_w_p2<L>(sb, tmem, with_o);
             mma_commit(&bar_mma);
         }
-        build_kd<L, NT, NORM>(sm, len, gl, ot[0], ot[1], s_rn);  // over the solve scratch, overlapping W and P2
+        if (compute) build_kd<L, NT, NORM>(sm, len, gl, ot[0], ot[1], s_rn);  // over the solve scratch, overlapping W and P2
         fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0) {
+        if (issuer) {
             tc_fence_after_sync();
             issue_p<L>(sb, tmem);
             mma_commit(&bar_p);
@@ -380,16 +391,18 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         ok = mbar_wait_ns(&bar_mma, 1, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
-        w_epilogue<L, NT>(sm, tmem + TC_W);  // -W over Kg in O1
+        if (compute) w_epilogue<L, NT>(sm, tmem + TC_W);  // -W over Kg in O1
         ok = mbar_wait_ns(&bar_p, 0, kWaitNs);
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
-        epi_p<NT>(tmem, sm + L::ST_P, range_ok);    // the k box is dead
-        if (with_o) epi_p2<NT>(tmem, sm + L::ST_P2, range_ok);  // T' (high) is dead: every product reading it is done
+        if (compute) {
+            epi_p<NT>(tmem, sm + L::ST_P, range_ok);    // the k box is dead
+            if (with_o) epi_p2<NT>(tmem, sm + L::ST_P2, range_ok);  // T' (high) is dead: every product reading it is done
+        }
         fence_proxy_async_smem();
         tc_fence_before_sync();
         __syncthreads();
-        if (tid == 0) {
+        if (issuer) {
             tc_fence_after_sync();
             issue_n_q<L>(sb, tmem, with_o);
             mma_commit(&bar_mma);
@@ -399,20 +412,22 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             stores_pending = true;
         }
         ok = mbar_wait_ns(&bar_mma, 0, kWaitNs);
-        if (tid == 0) bulk_wait_read();  // the P image is overwritten next
+        if (issuer) bulk_wait_read();  // the P image is overwritten next
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
-        epi_n<NT>(tmem, sm + L::ST_NQ);           // over the P image and Kd^T
-        if (with_o) epi_q<L, NT>(sm, tmem, sm + L::ST_NQ + 32768);
+        if (compute) {
+            epi_n<NT>(tmem, sm + L::ST_NQ);           // over the P image and Kd^T
+            if (with_o) epi_q<L, NT>(sm, tmem, sm + L::ST_NQ + 32768);
+        }
         fence_proxy_async_smem();
         __syncthreads();
-        if (tid == 0) {
+        if (issuer) {
             bulk_store(rec + R_N, sm + L::ST_NQ, with_o ? 49152u : 32768u);  // N | Q'
             bulk_commit();
         }
     } while (false);
     if (timed_out) {
-        if (tid == 0) {
+        if (issuer) {
             atomicOr(status, DEV_ERR_TIMEOUT);
             mma_commit(&bar_drain);  // completes once every MMA issued so far has
         }
@@ -421,12 +436,12 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     }
     // the record stores must have read their shared-memory sources before the CTA exits
     // and its shared memory is reused; their global writes complete before the kernel does
-    if (tid == 0 && stores_pending) bulk_wait_read();
+    if (issuer && stores_pending) bulk_wait_read();
     if (decay_bad) atomicOr(status, DEV_ERR_DECAY);
     if (!range_ok) atomicOr(status, DEV_ERR_RANGE);
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kChunkTmem);
+    if (warp == kIssueWarp) tmem_dealloc(tmem, kChunkTmem);
 }
 
 // ============================================================== state kernel

@@ -423,13 +423,16 @@ __device__ __forceinline__ void store_tprime_quad(unsigned char *sm, int r, int 
 // needs a mask.  The last level writes T' = T diag(beta) straight into its bf16
 // high and low images (L::O4, L::TL): the diagonal 32 x 32 quadrants while X is
 // formed, the lower-left one as it is formed, zeros above; T itself is not
-// completed in fp32.  Contains barriers; the caller fences and synchronises
-// before the images are read.
+// completed in fp32.  Called by the NT compute threads only; they synchronise at
+// named barrier 1, and the caller fences and synchronises before the images are read.
 template <class L, int NT>
 __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm, const float *s_beta)
 {
     static_assert(L::SOLVE_A == L::SOLVE_T, "the doubling solve works in place");
     static_assert(NT == 256, "the last level maps one output quad to each thread");
+    // the NT compute threads (warps 0 .. NT/32 - 1) meet at named barrier 1; a CTA's
+    // other warps do not take part in the solve
+    auto sync = [] { asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory"); };
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float *sT = reinterpret_cast<float *>(sm + L::SOLVE_T);  // holds A until overwritten
     float *sX = reinterpret_cast<float *>(sm + L::SOLVE_X);
@@ -486,7 +489,7 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm, const float
             __syncwarp();
         }
     }
-    __syncthreads();
+    sync();
     // 2. The 16 level across the CTA: two pairs of 16 x 16 blocks, 128 output quads, two
     //    adjacent lanes per quad (each takes every other group of four m; a shuffle adds
     //    the halves).
@@ -512,7 +515,7 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm, const float
             acc = add_pair_lanes(acc);
             if (half == 0) *reinterpret_cast<float4 *>(sX + xr * kLdX + cq) = acc;
         }
-        __syncthreads();
+        sync();
         // T_10 = -T_11 X over A_10: row rr needs m <= rr only (T_11 is lower triangular);
         // a warp covers few consecutive rows, so its trip counts stay close
         for (int it = tid; it < items * 2; it += NT) {
@@ -534,7 +537,7 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm, const float
                 *reinterpret_cast<float4 *>(sT + (R0 + rr) * kLdS + C0 + cq) =
                     make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
         }
-        __syncthreads();
+        sync();
     }
     // 3. The 32 level: one pair of 32 x 32 blocks, one output quad per thread.  T_00 and
     //    T_11 are final now: each thread also sends one quad of each to the T' images and
@@ -559,7 +562,7 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm, const float
         *reinterpret_cast<uint2 *>(sm + L::O4 + km16(r, 32 + c, 64)) = make_uint2(0u, 0u);
         *reinterpret_cast<uint2 *>(sm + L::TL + km16(r, 32 + c, 64)) = make_uint2(0u, 0u);
     }
-    __syncthreads();
+    sync();
     {
         // T_10 = -T_11 X straight into the T' images (row 32 + rr, columns cq..cq+3)
         const int rr = tid >> 3, cq = (tid & 7) * 4;
