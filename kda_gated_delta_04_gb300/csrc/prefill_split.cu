@@ -126,8 +126,8 @@ __device__ __forceinline__ void build_kd(unsigned char *sm, int len, const float
                 kv.x *= rn[r];
                 kv.y *= rn[r];
             }
-            const float dx = kv.x * __expf(tot.x - (off.x + gl[rr].x));
-            const float dy = kv.y * __expf(tot.y - (off.y + gl[rr].y));
+            const float dx = kv.x * exp2_approx(tot.x - (off.x + gl[rr].x));  // log2 units
+            const float dy = kv.y * exp2_approx(tot.y - (off.y + gl[rr].y));
             hx[u] = __bfloat162float(__float2bfloat16_rn(dx));
             hy[u] = __bfloat162float(__float2bfloat16_rn(dy));
             lx[u] = dx - hx[u];

@@ -23,6 +23,17 @@ constexpr int kD = 128, kDV = 32, kC = 64, kThreads = 512;
 constexpr uint64_t kWaitNs = 2000000000ull;  // 2 s per wait before giving up
 constexpr int kLdS = kC + 4;                 // row stride (floats) of A and T in the solve
 constexpr int kLdX = 32 + 4;                 // row stride of the block products X (<= 32 x 32)
+constexpr float kLog2e = 1.4426950408889634f;  // log2(e): e^x = 2^(x log2 e)
+
+// 2^x by the hardware's approximate base-2 exponential (relative error about 2^-22;
+// subnormal results flush to zero).  The in-chunk decay prefix is kept in log2 units,
+// so each decay factor is this one instruction.
+__device__ __forceinline__ float exp2_approx(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
 // Byte offset of element (row, col) of a K-major, 128-byte-swizzled operand
 // with `rows` rows per 64-element (bf16) or 32-element (tf32) column panel.
@@ -102,7 +113,9 @@ __device__ __forceinline__ uint4 pack_bf16x8(const float (&x)[8])
 // Thread = (channel pair cp: channels 2cp, 2cp+1; row group rg of R = 4096/NT
 // rows).  Scans its rows of log_alpha (row stride `la_stride` floats, shared or
 // global memory) in registers and leaves the group totals in s_tot.  With `scalar`
-// each row holds one value, the decay of every key channel (scalar gate).
+// each row holds one value, the decay of every key channel (scalar gate).  The
+// prefix is kept in log2 units, g = log2(e) * sum(log alpha) (each add is one FMA),
+// so that every decay factor e^(sum log alpha) = 2^g is a single exp2_approx.
 template <int NT>
 __device__ __forceinline__ void prefix_scan(const float *la, int la_stride, int len, float *s_tot,
                                             float2 (&gl)[4096 / NT], float &gmin, float &gmax, bool scalar = false)
@@ -126,8 +139,8 @@ __device__ __forceinline__ void prefix_scan(const float *la, int la_stride, int 
     }
 #pragma unroll
     for (int rr = 0; rr < R; ++rr) {
-        g.x += x[rr].x;
-        g.y += x[rr].y;
+        g.x = fmaf(x[rr].x, kLog2e, g.x);
+        g.y = fmaf(x[rr].y, kLog2e, g.y);
         gl[rr] = g;
         gmin = fminf(gmin, fminf(g.x, g.y));
         gmax = fmaxf(gmax, fmaxf(g.x, g.y));
@@ -158,7 +171,8 @@ __device__ __forceinline__ void qk_row_inv_norms(const unsigned char *k_box, con
 }
 
 // ---------------------------------------------------------------- a2: operands
-// After a barrier following prefix_scan: Kg = k e^g and Qg = scale q e^g into
+// After a barrier following prefix_scan (g in log2 units, e^g below meaning
+// 2^g): Kg = k e^g and Qg = scale q e^g into
 // O1, Ki = k e^-g into O2 (bf16) and, when KI_T, into o3 (tf32, transposed,
 // K-major 128 rows x 64), e^{g_last} into gam[128].  When off_tot is given it
 // receives this thread's group offset and the chunk total of g for its channel
@@ -190,9 +204,10 @@ __device__ __forceinline__ bool decayed_operands(unsigned char *sm, int len, con
     }
     if (rg == G - 1)
         *reinterpret_cast<float2 *>(&gam[2 * cp]) =
-            make_float2(__expf(off.x + gl[R - 1].x), __expf(off.y + gl[R - 1].y));
-    const bool bad = fminf(off.x, off.y) + gmin < KDA_MIN_CHUNK_LOG_DECAY ||
-                     fmaxf(off.x, off.y) + gmax > -KDA_MIN_CHUNK_LOG_DECAY;
+            make_float2(exp2_approx(off.x + gl[R - 1].x), exp2_approx(off.y + gl[R - 1].y));
+    // the supported range of the cumulative log-decay, in the prefix's log2 units
+    const bool bad = fminf(off.x, off.y) + gmin < KDA_MIN_CHUNK_LOG_DECAY * kLog2e ||
+                     fmaxf(off.x, off.y) + gmax > -KDA_MIN_CHUNK_LOG_DECAY * kLog2e;
     const float scale = rsqrtf((float)kD);
     // K-major swizzled byte offset of channel 2cp in a row, less the row part
     const uint32_t pbase1 = (uint32_t)((cp >> 5) * 16384 + ((cp & 3) << 2));
@@ -205,9 +220,9 @@ __device__ __forceinline__ bool decayed_operands(unsigned char *sm, int len, con
         for (int u = 0; u < 4; ++u) {
             const int rr = r4 + u, r = rg * R + rr;
             const bool valid = r < len;
-            const float gx = off.x + gl[rr].x, gy = off.y + gl[rr].y;
-            const float ex = __expf(gx), ey = __expf(gy);
-            const float ix = __expf(-gx), iy = __expf(-gy);
+            const float gx = off.x + gl[rr].x, gy = off.y + gl[rr].y;  // log2 units
+            const float ex = exp2_approx(gx), ey = exp2_approx(gy);
+            const float ix = exp2_approx(-gx), iy = exp2_approx(-gy);
             const uint32_t qraw = valid ? *reinterpret_cast<const uint32_t *>(sm + L::IN_Q + (r * kD + 2 * cp) * 2) : 0u;
             const uint32_t kraw = valid ? *reinterpret_cast<const uint32_t *>(sm + L::IN_K + (r * kD + 2 * cp) * 2) : 0u;
             float2 qv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qraw));
