@@ -282,7 +282,8 @@ __device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, un
 template <bool NORM>
 __global__ void __launch_bounds__(kChunkThreads, 2)
 prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const float *__restrict__ log_alpha, const float *__restrict__ beta,
+                     const __grid_constant__ CUtensorMap tm_la, const float *__restrict__ log_alpha,
+                     const float *__restrict__ beta,
                      const int2 *__restrict__ desc, int H, int chunk_bound,
                      unsigned char *__restrict__ records, uint32_t *status, bool with_o, bool scalar_gate)
 {
@@ -320,32 +321,34 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         mbar_init(&bar_p, 1);
         mbar_init(&bar_drain, 1);
         fence_mbar_init();
-        mbar_arrive_expect_tx(&bar_tma, 16384 + 16384);
+        // q and k boxes, and (per-channel gate) the log_alpha box into O1, free until the
+        // decayed operands are written there
+        mbar_arrive_expect_tx(&bar_tma, 16384 + 16384 + (scalar_gate ? 0u : 32768u));
         tma_load_3d(sm + L::IN_Q, &tm_q, &bar_tma, 0, h, (int)c0);
         tma_load_3d(sm + L::IN_K, &tm_k, &bar_tma, 0, h, (int)c0);
+        if (!scalar_gate) tma_load_3d(sm + L::O1, &tm_la, &bar_tma, 0, h, (int)c0);
     }
     if (warp == kIssueWarp) {
         tmem_alloc(&tmem_holder, kChunkTmem);
         tmem_relinquish();
     }
     if (tid < kC) s_beta[tid] = tid < len ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
-    // the in-chunk decay prefix reads log_alpha straight from global memory,
-    // overlapping the q/k copies
     float *s_tot = reinterpret_cast<float *>(sm + L::AQ);
     float2 gl[4096 / NT];
     float gmin = 0.f, gmax = 0.f;
-    if (compute) {
-        if (scalar_gate)  // log_alpha [T, H]: one decay per token-head
-            prefix_scan<NT>(log_alpha + (size_t)c0 * H + h, H, len, s_tot, gl, gmin, gmax, true);
-        else
-            prefix_scan<NT>(log_alpha + ((size_t)c0 * H + h) * kD, H * kD, len, s_tot, gl, gmin, gmax);
-    }
-    __syncthreads();
+    // scalar gate (log_alpha [T, H], one decay per token-head): the prefix reads its 64
+    // values straight from global memory while the boxes fly
+    if (compute && scalar_gate)
+        prefix_scan<NT>(log_alpha + (size_t)c0 * H + h, H, len, s_tot, gl, gmin, gmax, true);
+    __syncthreads();  // barriers initialised, TMEM allocated
     tc_fence_after_sync();
     const uint32_t tmem = tmem_holder;
     bool timed_out = false, tma_pending = true, decay_bad = false, range_ok = true, stores_pending = false;
     do {
         bool ok = !compute || mbar_wait_ns(&bar_tma, 0, kWaitNs);
+        if (compute && !scalar_gate && ok)  // the per-channel prefix from the log_alpha box
+            prefix_scan<NT>(reinterpret_cast<const float *>(sm + L::O1), kD, len, s_tot, gl, gmin, gmax);
+        // every thread is past its reads of the log_alpha box and s_tot is complete
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tma_pending = false;
         if (NORM) {
@@ -364,17 +367,21 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             issue_g1<L>(sb, tmem);
             mma_commit(&bar_mma);
         }
-        ok = mbar_wait_ns(&bar_mma, 0, kWaitNs);
-        if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        tc_fence_after_sync();
+        // From here the compute warps wait for their products themselves; whether any wait
+        // gave up is agreed on at the next block-wide barrier, so the issuing warp never
+        // holds them up while it issues.
+        bool late = false;
         if (compute) {
-            kk_epilogue<L, NT>(sm, tmem, s_beta, sm + L::AQ);
+            late = !mbar_wait_ns(&bar_mma, 0, kWaitNs);
+            tc_fence_after_sync();
+            if (!late) kk_epilogue<L, NT>(sm, tmem, s_beta, sm + L::AQ);
             tc_fence_before_sync();
-            asm volatile("bar.sync 1, %0;" ::"n"(NT) : "memory");  // A complete for the solve
-            solve_ut_doubling<L, NT>(sm, s_beta);  // T' high / low images straight from the last level
+            // A complete for the solve; the compute warps enter it all or none
+            late = bar_sync_or(1, NT, late);
+            if (!late) solve_ut_doubling<L, NT>(sm, s_beta);  // T' high / low images straight from the last level
         }
         fence_proxy_async_smem();
-        __syncthreads();
+        if (__syncthreads_or(late)) { timed_out = true; break; }
         if (issuer) {
             tc_fence_after_sync();
             issue_w_p2<L>(sb, tmem, with_o);
@@ -388,20 +395,20 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             issue_p<L>(sb, tmem);
             mma_commit(&bar_p);
         }
-        ok = mbar_wait_ns(&bar_mma, 1, kWaitNs);
-        if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        tc_fence_after_sync();
-        if (compute) w_epilogue<L, NT>(sm, tmem + TC_W);  // -W over Kg in O1
-        ok = mbar_wait_ns(&bar_p, 0, kWaitNs);
-        if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        tc_fence_after_sync();
-        if (compute) {
-            epi_p<NT>(tmem, sm + L::ST_P, range_ok);    // the k box is dead
-            if (with_o) epi_p2<NT>(tmem, sm + L::ST_P2, range_ok);  // T' (high) is dead: every product reading it is done
+        if (compute) {  // the issuing warp is still issuing P meanwhile
+            late = !mbar_wait_ns(&bar_mma, 1, kWaitNs);
+            tc_fence_after_sync();
+            if (!late) w_epilogue<L, NT>(sm, tmem + TC_W);  // -W over Kg in O1
+            late = late || !mbar_wait_ns(&bar_p, 0, kWaitNs);
+            tc_fence_after_sync();
+            if (!late) {
+                epi_p<NT>(tmem, sm + L::ST_P, range_ok);    // the k box is dead
+                if (with_o) epi_p2<NT>(tmem, sm + L::ST_P2, range_ok);  // T' (high) is dead: every product reading it is done
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
-        __syncthreads();
+        if (__syncthreads_or(late)) { timed_out = true; break; }
         if (issuer) {
             tc_fence_after_sync();
             issue_n_q<L>(sb, tmem, with_o);
@@ -894,10 +901,15 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     if (err != cudaSuccess) return err;
     err = allow_smem(prefill_state_kernel, (int)kStateSmem, &dev_state);
     if (err != cudaSuccess) return err;
-    CUtensorMap tq, tk, tv;
+    CUtensorMap tq, tk, tla, tv;
     if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, p.total_tokens, p.num_heads, 2, kD) ||
         !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, p.total_tokens, p.num_heads, 2, kD) ||
         !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kSV))
+        return cudaErrorInvalidValue;
+    // a scalar gate ([T, H]) is read by the prefix scan, never by TMA: its map slot repeats q's
+    if (p.scalar_gate)
+        tla = tq;
+    else if (!make_map(&tla, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, p.log_alpha, p.total_tokens, p.num_heads, 4, kD))
         return cudaErrorInvalidValue;
     const int64_t chunk_bound = p.total_tokens / kC + p.num_seqs;
     if (chunk_bound * p.num_heads > INT32_MAX || !p.desc || p.chunk_bound != chunk_bound)
@@ -915,7 +927,7 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     cfg.stream = p.stream;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, chunk_kernel, tq, tk, p.log_alpha, p.beta, (const int2 *)p.desc,
+    err = cudaLaunchKernelEx(&cfg, chunk_kernel, tq, tk, tla, p.log_alpha, p.beta, (const int2 *)p.desc,
                              p.num_heads, (int)chunk_bound, static_cast<unsigned char *>(records), p.status, p.o != nullptr,
                              p.scalar_gate);
     if (err != cudaSuccess) return err;
