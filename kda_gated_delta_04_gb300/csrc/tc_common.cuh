@@ -428,11 +428,10 @@ __device__ __forceinline__ void store_tprime_quad(unsigned char *sm, int r, int 
     *reinterpret_cast<uint2 *>(sm + L::TL + km16(r, c, 64)) = make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
 }
 
-// solve_ut_doubling: the same T, in place (SOLVE_T == SOLVE_A), by recursive
-// doubling all the way from 4 x 4 blocks: the sixteen 4 x 4 diagonal blocks by
-// substitution, then for block size b = 4, 8, 16, 32 and every pair of b x b
-// diagonal blocks, X = A_10 T_00 and T_10 = -T_11 X (X in SOLVE_X).  Up to b = 8
-// each 16 x 16 diagonal block is done by one warp with warp barriers only.
+// solve_ut_doubling: the same T, in place (SOLVE_T == SOLVE_A): the four 16 x 16
+// diagonal blocks by column-parallel forward substitution (one warp per block, one
+// lane per column), then recursive doubling: for block size b = 16, 32 and every
+// pair of b x b diagonal blocks, X = A_10 T_00 and T_10 = -T_11 X (X in SOLVE_X).
 // Each output quad is one thread's float4; the strictly upper parts of A, which
 // the k-k epilogue zeroed, stand in for the zero upper parts of T, so no product
 // needs a mask.  The last level writes T' = T diag(beta) straight into its bf16
@@ -451,58 +450,24 @@ __device__ __forceinline__ void solve_ut_doubling(unsigned char *sm, const float
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     float *sT = reinterpret_cast<float *>(sm + L::SOLVE_T);  // holds A until overwritten
     float *sX = reinterpret_cast<float *>(sm + L::SOLVE_X);
-    // 1. Warp w < 4 inverts the diagonal 16 x 16 block at 16w on its own (warp
-    //    barriers only): its four 4 x 4 blocks by substitution, then the 4 and 8
-    //    doubling levels inside the block.  X rows 8w .. 8w + 7 are the warp's.
-    if (warp < 4) {
-        const int w16 = warp * 16;
-        float x[4];
-        const int j4 = w16 + (lane >> 2) * 4, cc = lane & 3;
-        if (lane < 16) {
+    // 1. Warp w < 4 inverts the diagonal 16 x 16 block at 16w on its own: lane c < 16 forms
+    //    column c by forward substitution, updating every later row's sum as soon as x[m]
+    //    is known (the sixteen steps each add one FMA to the dependency chain).  The block of
+    //    A is read in full before any lane overwrites it with its column of T.
+    if (warp < 4 && lane < 16) {
+        const int b0 = warp * 16, cc = lane;
+        float acc[16], x[16];
 #pragma unroll
-            for (int r = 0; r < 4; ++r) {
-                float acc = 0.f;
+        for (int r = 0; r < 16; ++r) acc[r] = 0.f;
 #pragma unroll
-                for (int m = 0; m < r; ++m) acc += sT[(j4 + r) * kLdS + j4 + m] * x[m];
-                x[r] = r < cc ? 0.f : (r == cc ? 1.f : -acc);
-            }
+        for (int m = 0; m < 16; ++m) {
+            x[m] = m < cc ? 0.f : (m == cc ? 1.f : -acc[m]);
+#pragma unroll
+            for (int r = m + 1; r < 16; ++r) acc[r] = fmaf(sT[(b0 + r) * kLdS + b0 + m], x[m], acc[r]);
         }
-        __syncwarp();  // every column has read its block of A
-        if (lane < 16) {
+        __syncwarp(0xffffu);  // every column has read the block of A
 #pragma unroll
-            for (int r = 0; r < 4; ++r) sT[(j4 + r) * kLdS + j4 + cc] = x[r];
-        }
-        __syncwarp();
-#pragma unroll
-        for (int b = 4; b <= 8; b *= 2) {  // pairs of b x b blocks inside the 16 x 16 block
-            const int quads = b / 4;
-            const int nitems = (16 / (2 * b)) * b * quads;  // pairs x rows x quads: 8 (b = 4), 16 (b = 8)
-            const int xr = lane / quads, cq = (lane % quads) * 4, p = xr / b, rr = xr % b;
-            const int R0 = w16 + 2 * b * p + b, C0 = w16 + 2 * b * p;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-            if (lane < nitems) {  // X = A_10 T_00
-#pragma unroll
-                for (int m = 0; m < b; ++m) {
-                    const float a = sT[(R0 + rr) * kLdS + C0 + m];
-                    const float4 t = *reinterpret_cast<const float4 *>(sT + (C0 + m) * kLdS + C0 + cq);
-                    acc.x += a * t.x; acc.y += a * t.y; acc.z += a * t.z; acc.w += a * t.w;
-                }
-                *reinterpret_cast<float4 *>(sX + (warp * 8 + xr) * kLdX + cq) = acc;
-            }
-            __syncwarp();
-            if (lane < nitems) {  // T_10 = -T_11 X over A_10
-                acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-                for (int m = 0; m < b; ++m) {
-                    const float t = sT[(R0 + rr) * kLdS + R0 + m];
-                    const float4 xv = *reinterpret_cast<const float4 *>(sX + (warp * 8 + p * b + m) * kLdX + cq);
-                    acc.x += t * xv.x; acc.y += t * xv.y; acc.z += t * xv.z; acc.w += t * xv.w;
-                }
-                *reinterpret_cast<float4 *>(sT + (R0 + rr) * kLdS + C0 + cq) =
-                    make_float4(-acc.x, -acc.y, -acc.z, -acc.w);
-            }
-            __syncwarp();
-        }
+        for (int r = 0; r < 16; ++r) sT[(b0 + r) * kLdS + b0 + cc] = x[r];
     }
     sync();
     // 2. The 16 level across the CTA: two pairs of 16 x 16 blocks, 128 output quads, two
