@@ -71,26 +71,50 @@ static_assert(ChunkLayout::ST_NQ + 49152 <= ChunkLayout::O1, "N | Q' staging ove
 static_assert(ChunkLayout::SOLVE_X + 32 * kLdX * 4 <= ChunkLayout::O1, "solve scratch overlaps O1");
 
 // State kernel (608 threads: sixteen state warps, two issuing warps, a copy warp) over a
-// 64-column value slice: two record stages, a ring of three v slices, the V^T operand of
-// two chunks and the S operand of two chunks.
-constexpr int kSV = 64;                         // value columns per state CTA
-constexpr uint32_t kVBytes = kC * kSV * 2;      // one v slice [64 tokens][64] bf16, and V^T fp16
-constexpr uint32_t kSBytes = kD * kSV * 2;      // the S operand, bf16
-constexpr int kVRing = 3;
-struct StateLayout {
-    static constexpr uint32_t STAGE = 75776;  // record + padding to 1024 bytes
-    static constexpr uint32_t VBOX = 2 * STAGE;                 // kVRing x v slice [64][64] bf16
-    static constexpr uint32_t VIMG = VBOX + kVRing * kVBytes;   // 2 x V^T fp16, 64 rows x K 64
-    static constexpr uint32_t O7 = VIMG + 2 * kVBytes;          // 2 x S bf16, MN-major, K 128 x 64 columns
+// value slice of SV = 32 or 64 columns: two record stages, a ring of v slices, the V^T
+// operand of two chunks and the S operand of two chunks.  The 32-column form has the
+// shorter chain per chunk; the 64-column form halves the CTA count (and doubles the width
+// of every tensor-core product group), which wins once the slices no longer fit in one
+// wave of SMs.
+template <int SV>
+struct StateShape {
+    static_assert(SV == 32 || SV == 64, "value slices of 32 or 64 columns");
+    static constexpr uint32_t kVBytes = kC * SV * 2;    // one v slice [64 tokens][SV] bf16, and V^T fp16
+    static constexpr uint32_t kSBytes = kD * SV * 2;    // the S operand, bf16
+    static constexpr int kVRing = SV == 32 ? 4 : 3;     // v slices in flight
+    static constexpr int kSCols = SV / 4;               // state columns per state-warp thread
+    static constexpr uint32_t STAGE = 75776;            // record + padding to 1024 bytes
+    static constexpr uint32_t VBOX = 2 * STAGE;         // kVRing x v slice
+    static constexpr uint32_t VIMG = VBOX + kVRing * kVBytes;  // 2 x V^T fp16, SV rows x K 64
+    static constexpr uint32_t O7 = VIMG + 2 * kVBytes;  // 2 x S bf16, MN-major, K 128 x SV columns
     static constexpr uint32_t USED = O7 + 2 * kSBytes;
+    static constexpr uint32_t SMEM = USED + 1024;
+    // TMEM columns: state increment (M = 128), outputs of two chunks (M = 64)
+    static constexpr uint32_t TM_5 = 0, TM_O = SV, TMEM = SV == 32 ? 128 : 256;
+    // The S operand (K = state row i, N = value column j): MN-major.  64 columns: rows of
+    // 128 bytes, 128-byte swizzle (8-row atoms of 1024 bytes); 32 columns: rows of 64 bytes,
+    // 64-byte swizzle (8-row atoms of 512 bytes).  SK: bytes per K step of 16 rows.
+    static constexpr uint32_t SK = SV * 32;
+    __device__ static uint32_t mn(int i, int j)
+    {
+        if (SV == 64) return km16(i, j, kD);
+        return (uint32_t)(i * 64 + ((((j >> 3) ^ (i >> 1)) & 3) << 4) + ((j & 7) << 1));
+    }
+    __device__ static uint64_t sdesc_s(uint32_t addr)
+    {
+        return SV == 64 ? sdesc(addr, kSBytes, 1024, kSw128B) : sdesc(addr, 512, 512, kSw64B);
+    }
+    static constexpr uint32_t IDESC_PV = idesc_f16(128, SV, false, false);   // P V
+    static constexpr uint32_t IDESC_NS = idesc_bf16(128, SV, false, true);   // N S (S MN-major)
+    static constexpr uint32_t IDESC_P2V = idesc_f16(64, SV, false, false);   // P2 V
+    static constexpr uint32_t IDESC_QS = idesc_bf16(64, SV, false, true);    // Q' S (S MN-major)
+    static_assert(STAGE % 1024 == 0 && STAGE >= kRecBytes, "stage size");
+    static_assert(VIMG % 1024 == 0 && O7 % 1024 == 0, "operand alignment");
+    static_assert(SMEM <= 232448, "state kernel shared memory over the per-CTA limit");
+    static_assert(TM_O + 2 * SV <= TMEM, "state kernel TMEM map");
 };
-static_assert(StateLayout::STAGE % 1024 == 0 && StateLayout::STAGE >= kRecBytes, "stage size");
-static_assert(StateLayout::VIMG % 1024 == 0 && StateLayout::O7 % 1024 == 0, "operand alignment");
-static_assert(StateLayout::USED + 1024 <= 232448, "state kernel shared memory over the per-CTA limit");
-static_assert(kSV / 4 == 16, "a state warp's output columns are two 8-column halves");
 
 constexpr uint32_t kChunkSmem = ChunkLayout::USED + 1024;
-constexpr uint32_t kStateSmem = StateLayout::USED + 1024;
 
 // ============================================================== chunk kernel
 // TMEM columns: k-k / q-k product 0..63; then W 0..127, P2 128..191, P 192..255;
@@ -452,64 +476,55 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
 }
 
 // ============================================================== state kernel
-constexpr uint32_t IDESC_PV = idesc_f16(128, kSV, false, false);   // P V
-constexpr uint32_t IDESC_NS = idesc_bf16(128, kSV, false, true);   // N S (S MN-major)
-constexpr uint32_t IDESC_P2V = idesc_f16(64, kSV, false, false);   // P2 V
-constexpr uint32_t IDESC_QS = idesc_bf16(64, kSV, false, true);    // Q' S (S MN-major)
-// TMEM columns: state increment (M = 128), outputs of two chunks (M = 64)
-constexpr uint32_t TM_5 = 0, TM_O = kSV, kStateTmem = 256;
-static_assert(TM_O + 2 * kSV <= kStateTmem, "state kernel TMEM map");
 // Warps 0-15 hold the state; warp 16 issues the chain MMAs; warp 17 copies and
 // converts; warp 18 issues the output MMAs.
 constexpr int kStateWarps = 16, kChainWarp = 16, kCopyWarp = 17, kOutWarp = 18;
 constexpr int kStateThreads = 19 * 32;
 constexpr int kL2Ahead = 3;  // records brought into L2 this many chunks ahead
-constexpr int kSCols = kSV / 4;  // state columns per state-warp thread (a row of a quarter of the slice)
 
-// The state operand S (K = state row i, N = value column j, 64 columns): MN-major, rows of
-// 128 bytes, 128-byte swizzle (8-row atoms of 1024 bytes); one K step of 16 rows is 2048 bytes.
-__device__ __forceinline__ uint32_t mn_s(int i, int j) { return km16(i, j, kD); }
-__device__ __forceinline__ uint64_t sdesc_s(uint32_t addr) { return sdesc(addr, kSBytes, 1024, kSw128B); }
 // A state-warp thread's kSCols columns of state row i, as bf16, into the S operand image.
-__device__ __forceinline__ void store_s_operand(unsigned char *img, int i, int jp, const float (&S)[kSCols])
+template <class Sh>
+__device__ __forceinline__ void store_s_operand(unsigned char *img, int i, int jp, const float (&S)[Sh::kSCols])
 {
 #pragma unroll
-    for (int q = 0; q < kSCols / 8; ++q) {
+    for (int q = 0; q < Sh::kSCols / 8; ++q) {
         float x[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) x[u] = S[8 * q + u];
-        *reinterpret_cast<uint4 *>(img + mn_s(i, jp + 8 * q)) = pack_bf16x8(x);
+        *reinterpret_cast<uint4 *>(img + Sh::mn(i, jp + 8 * q)) = pack_bf16x8(x);
     }
 }
 
 // The chain group of one chunk: P V (fp16) + N S_c (bf16) into the M = 128 accumulator.
 // dr, dv, ds: descriptors of the record, the V^T image and the S image in use.
+template <class Sh>
 __device__ __forceinline__ void issue_chain(uint32_t acc, uint64_t dr, uint64_t dv, uint64_t ds)
 {
 #pragma unroll
     for (int s = 0; s < 4; ++s)  // P V (fp16)
-        mma_bf16(acc, dr + ((R_P + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_PV, s > 0);
+        mma_bf16(acc, dr + ((R_P + s * 32) >> 4), dv + ((s * 32) >> 4), Sh::IDESC_PV, s > 0);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {  // + N S_c (bf16)
-        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32, offs = s * 2048;
-        mma_bf16(acc, dr + ((R_N + off) >> 4), ds + (offs >> 4), IDESC_NS, 1);
+        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32, offs = s * Sh::SK;
+        mma_bf16(acc, dr + ((R_N + off) >> 4), ds + (offs >> 4), Sh::IDESC_NS, 1);
     }
 }
 
 // The output group of one chunk: P2 V (fp16) + Q' S_c (bf16) into an M = 64 accumulator.
+template <class Sh>
 __device__ __forceinline__ void issue_out(uint32_t acc, uint64_t dr, uint64_t dv, uint64_t ds)
 {
 #pragma unroll
     for (int s = 0; s < 4; ++s)  // P2 V (fp16)
-        mma_bf16(acc, dr + ((R_P2 + s * 32) >> 4), dv + ((s * 32) >> 4), IDESC_P2V, s > 0);
+        mma_bf16(acc, dr + ((R_P2 + s * 32) >> 4), dv + ((s * 32) >> 4), Sh::IDESC_P2V, s > 0);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {  // + Q' S_c (bf16)
-        const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32, offs = s * 2048;
-        mma_bf16(acc, dr + ((R_Q + off) >> 4), ds + (offs >> 4), IDESC_QS, 1);
+        const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32, offs = s * Sh::SK;
+        mma_bf16(acc, dr + ((R_Q + off) >> 4), ds + (offs >> 4), Sh::IDESC_QS, 1);
     }
 }
 
-// The serial pass over the chunks of one (sequence, head, 64-column value slice),
+// The serial pass over the chunks of one (sequence, head, SV-column value slice),
 // as four roles that meet only at mbarriers (no block-wide barrier per chunk):
 //   bar_ready[c&1]  S_c and V_c (both written by the 16 state warps) are in shared memory
 //   bar_rec[c&1]    record c has arrived
@@ -534,6 +549,7 @@ __device__ __forceinline__ void issue_out(uint32_t acc, uint64_t dr, uint64_t dv
 // zero row, so every box past it is filled with zeros), and the final state goes to
 // final_ident.  Their result is the linear map of the sequence's chunks.  A CTA whose
 // sequence has no final state to store and no outputs to write returns at once.
+template <int SV>
 __global__ void __launch_bounds__(kStateThreads, 1)
 prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_v_zero,
                      const int32_t *__restrict__ cu, int64_t total, int H, const int32_t *__restrict__ cc,
@@ -541,7 +557,10 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
                      __nv_bfloat16 *__restrict__ o, float *final_state, uint32_t *status,
                      const int32_t *__restrict__ order, StateSlots slots, int z_ident, float *final_ident)
 {
-    using L = StateLayout;
+    using Sh = StateShape<SV>;
+    using L = Sh;
+    constexpr int kVRing = Sh::kVRing, kSCols = Sh::kSCols;
+    constexpr uint32_t kVBytes = Sh::kVBytes, kSBytes = Sh::kSBytes, TM_5 = Sh::TM_5, TM_O = Sh::TM_O;
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar_rec[2], bar_v[kVRing], bar_s, bar_o[2], bar_ready[2], bar_drain;
     __shared__ uint32_t tmem_holder;
@@ -556,7 +575,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     // initial states and the value rows are read at once, the records only after pdl_wait
     // (the chunk kernel's completion), so this prologue overlaps that kernel's last CTAs
     const bool ident = (int)blockIdx.z >= z_ident;
-    const int j0 = blockIdx.x * kSV, h = blockIdx.y, n = order[ident ? blockIdx.z - z_ident : blockIdx.z];
+    const int j0 = blockIdx.x * SV, h = blockIdx.y, n = order[ident ? blockIdx.z - z_ident : blockIdx.z];
     int64_t t0, t1;
     seq_range(cu, n, total, t0, t1);
     const int nchunks = (int)((t1 - t0 + kC - 1) / kC);
@@ -597,7 +616,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
         fence_mbar_init();
     }
     if (warp == 0) {
-        tmem_alloc(&tmem_holder, kStateTmem);
+        tmem_alloc(&tmem_holder, Sh::TMEM);
         tmem_relinquish();
     }
     // state row i, columns j0 + jp .. jp + kSCols - 1 in registers; S (bf16) operands in O7
@@ -618,7 +637,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
 #pragma unroll
             for (int j = 0; j < kSCols; ++j) S[j] = 0.f;
         }
-        store_s_operand(sm + L::O7, i_row, jp, S);
+        store_s_operand<Sh>(sm + L::O7, i_row, jp, S);
     }
     fence_proxy_async_smem();
     __syncthreads();  // barriers initialised, S_0 written
@@ -628,7 +647,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     const int r64 = quarter * 16 + (lane & 15);  // row held by this lane in an M = 64 accumulator
     bool range_ok = true;
     // operand descriptors of buffer 0; buffer 1 is a fixed byte distance further
-    const uint64_t d_rec0 = kdesc(sb), d_v0 = kdesc(sb + L::VIMG), d_s0 = sdesc_s(sb + L::O7);
+    const uint64_t d_rec0 = kdesc(sb), d_v0 = kdesc(sb + L::VIMG), d_s0 = Sh::sdesc_s(sb + L::O7);
     // ready(c) for c >= 1 (chunk 0's operands are known ready from the first barrier)
     auto wait_ready = [&](int c) -> bool {
         return c < 1 || mbar_wait_ns(&bar_ready[c & 1], (uint32_t)(((c - 1) >> 1) & 1), kWaitNs);
@@ -637,37 +656,50 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
         return mbar_wait_ns(&bar_rec[c & 1], (uint32_t)((c >> 1) & 1), kWaitNs);
     };
 
-    // o rows of chunk cp (M = 64 accumulator TM_O + kSV*(cp&1)), once its MMAs finished
+    // o rows of chunk cp (M = 64 accumulator TM_O + SV*(cp&1)), once its MMAs finished
     // (with no outputs wanted the barrier still marks the chunk's operands as released)
     auto write_o = [&](int cp) -> bool {
         if (!mbar_wait_ns(&bar_o[cp & 1], (uint32_t)((cp >> 1) & 1), kWaitNs)) return false;
         if (!o) return true;
         tc_fence_after_sync();
-        // the warp's kSCols columns: eight per half-warp, one 16-byte store per thread
-        float v[8];
-        tmem_ld16x2_x8<8>(tmem + TM_O + kSV * (cp & 1) + lane_off + jp, v);
-        tmem_ld_wait();
+        // the warp's kSCols columns, half to each half-warp (16-lane load of the M = 64 rows)
         const int64_t cs = t0 + (int64_t)cp * kC;
-        if (cs + r64 < t1)
-            *reinterpret_cast<uint4 *>(o + ((size_t)(cs + r64) * H + h) * kD + j0 + jp + 8 * (lane >> 4)) =
-                pack_bf16x8(v);
+        __nv_bfloat16 *dst = o + ((size_t)(cs + r64) * H + h) * kD + j0 + jp + (kSCols / 2) * (lane >> 4);
+        if constexpr (SV == 64) {
+            float v[8];
+            tmem_ld16x2_x8<8>(tmem + TM_O + SV * (cp & 1) + lane_off + jp, v);
+            tmem_ld_wait();
+            if (cs + r64 < t1) *reinterpret_cast<uint4 *>(dst) = pack_bf16x8(v);
+        } else {
+            float v[4];
+            tmem_ld16x2_x4<4>(tmem + TM_O + SV * (cp & 1) + lane_off + jp, v);
+            tmem_ld_wait();
+            if (cs + r64 < t1) *reinterpret_cast<uint2 *>(dst) = make_uint2(pack_bf16x2(v[0], v[1]), pack_bf16x2(v[2], v[3]));
+        }
         return true;
     };
     // state warps: the v slice of chunk k -> V^T fp16 K-major in VIMG[k & 1]; one
-    // 8-row group of one column per thread
+    // group of RV rows of one column per thread
     auto convert_v = [&](int k) -> bool {
+        constexpr int RV = SV / 8;  // 512 state threads cover 64 rows x SV columns
         if (!mbar_wait_ns(&bar_v[k % kVRing], (uint32_t)((k / kVRing) & 1), kWaitNs)) return false;
         const int64_t ck = t0 + (int64_t)k * kC;
         const int lenk = (t1 - ck) < kC ? (int)(t1 - ck) : kC;
         const unsigned char *box = sm + L::VBOX + (k % kVRing) * kVBytes;
-        const int j = tid % kSV, s8 = (tid / kSV) * 8;
-        float x[8];
+        const int j = tid % SV, s0 = (tid / SV) * RV;
+        float x[RV];
 #pragma unroll
-        for (int u = 0; u < 8; ++u) {
-            x[u] = (s8 + u) < lenk ? bf16_at(box + ((s8 + u) * kSV + j) * 2) : 0.f;
+        for (int u = 0; u < RV; ++u) {
+            x[u] = (s0 + u) < lenk ? bf16_at(box + ((s0 + u) * SV + j) * 2) : 0.f;
             range_ok &= fabsf(x[u]) <= 65504.f;
         }
-        *reinterpret_cast<uint4 *>(sm + L::VIMG + (k & 1) * kVBytes + km16(j, s8, kSV)) = pack_f16x8_plain(x);
+        unsigned char *img = sm + L::VIMG + (k & 1) * kVBytes + km16(j, s0, SV);
+        if constexpr (RV == 8) {
+            *reinterpret_cast<uint4 *>(img) = pack_f16x8_plain(x);
+        } else {
+            __half2 a = __floats2half2_rn(x[0], x[1]), b = __floats2half2_rn(x[2], x[3]);
+            *reinterpret_cast<uint2 *>(img) = make_uint2(*reinterpret_cast<uint32_t *>(&a), *reinterpret_cast<uint32_t *>(&b));
+        }
         return true;
     };
 
@@ -703,11 +735,14 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
                 if (ok) {  // S <- gamma . S + (P V + N S); its bf16 operand image for the next chunk
                     tc_fence_after_sync();
                     float v[kSCols];
-                    tmem_ld16(tmem + TM_5 + lane_off + jp, v);
+                    if constexpr (kSCols == 16)
+                        tmem_ld16(tmem + TM_5 + lane_off + jp, v);
+                    else
+                        tmem_ld8(tmem + TM_5 + lane_off + jp, v);
                     tmem_ld_wait();
 #pragma unroll
                     for (int j = 0; j < kSCols; ++j) S[j] = fmaf(gc, S[j], v[j]);
-                    store_s_operand(sm + L::O7 + (st ^ 1) * kSBytes, i_row, jp, S);
+                    store_s_operand<Sh>(sm + L::O7 + (st ^ 1) * kSBytes, i_row, jp, S);
                     fence_proxy_async_smem();
                 }
                 tc_fence_before_sync();  // this warp's TMEM reads precede the arrival
@@ -727,10 +762,10 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
                         const uint64_t dr = d_rec0 + st * (L::STAGE >> 4), dv = d_v0 + st * (kVBytes >> 4),
                                        ds = d_s0 + st * (kSBytes >> 4);
                         if (chain) {
-                            issue_chain(tmem + TM_5, dr, dv, ds);
+                            issue_chain<Sh>(tmem + TM_5, dr, dv, ds);
                             mma_commit(&bar_s);
                         } else {
-                            if (o) issue_out(tmem + TM_O + kSV * st, dr, dv, ds);  // none when no outputs are wanted
+                            if (o) issue_out<Sh>(tmem + TM_O + SV * st, dr, dv, ds);  // none when no outputs are wanted
                             mma_commit(&bar_o[st]);  // also marks chunk c's operands as released
                         }
                     }
@@ -771,7 +806,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     if (!range_ok) atomicOr(status, DEV_ERR_RANGE);
     tc_fence_before_sync();
     __syncthreads();
-    if (warp == 0) tmem_dealloc(tmem, kStateTmem);
+    if (warp == 0) tmem_dealloc(tmem, Sh::TMEM);
 }
 
 // ============================================================== product-group diagnostic
@@ -784,7 +819,8 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
 // one CTA per SM, each group issued by a thread of its own warp as in that kernel.
 constexpr uint64_t kDiagFlops[2] = {
     2ull * (128 * 64 * 128 + 64 * 128 * 64 + 64 * 64 * 64 + 3 * 128 * 64 * 64 + 128 * 128 * 64 + 64 * 128 * 64),
-    2ull * (128 * kSV * 64 + 128 * kSV * 128 + 64 * kSV * 64 + 64 * kSV * 128)};
+    2ull * (128 * 64 * 64 + 128 * 64 * 128 + 64 * 64 * 64 + 64 * 64 * 128)};
+using DiagState = StateShape<64>;  // pass 1 measures the 64-column groups
 
 template <int PASS>
 __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(int reps, uint32_t *status)
@@ -792,8 +828,8 @@ __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(in
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar[2], bar_drain;
     __shared__ uint32_t tmem_holder;
-    constexpr uint32_t used = PASS == 0 ? ChunkLayout::USED : StateLayout::USED;
-    constexpr uint32_t cols = PASS == 0 ? kChunkTmem : kStateTmem;
+    constexpr uint32_t used = PASS == 0 ? ChunkLayout::USED : DiagState::USED;
+    constexpr uint32_t cols = PASS == 0 ? kChunkTmem : DiagState::TMEM;
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x;
@@ -826,11 +862,11 @@ __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(in
                 issue_p<ChunkLayout>(sb, tmem);
                 issue_n_q<ChunkLayout>(sb, tmem, true);
             } else {
-                const uint64_t dr = kdesc(sb), dv = kdesc(sb + StateLayout::VIMG), ds = sdesc_s(sb + StateLayout::O7);
+                const uint64_t dr = kdesc(sb), dv = kdesc(sb + DiagState::VIMG), ds = DiagState::sdesc_s(sb + DiagState::O7);
                 if (issuer == 0)
-                    issue_chain(tmem + TM_5, dr, dv, ds);
+                    issue_chain<DiagState>(tmem + DiagState::TM_5, dr, dv, ds);
                 else
-                    issue_out(tmem + TM_O, dr, dv, ds);
+                    issue_out<DiagState>(tmem + DiagState::TM_O, dr, dv, ds);
             }
             mma_commit(&bar[issuer]);
             ok = mbar_wait_ns(&bar[issuer], (uint32_t)(r & 1), kWaitNs);
@@ -853,7 +889,7 @@ cudaError_t run_tensor_phases(int reps, uint32_t *status, cudaStream_t stream, d
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int smem = PASS == 0 ? (int)kChunkSmem : (int)kStateSmem;
+    const int smem = PASS == 0 ? (int)kChunkSmem : (int)DiagState::SMEM;
     if (configured != dev) {
         if ((err = cudaFuncSetAttribute(tensor_phase_kernel<PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         smem)) != cudaSuccess ||
@@ -893,18 +929,76 @@ size_t prefill_split_records_bytes(int64_t total_tokens, int num_seqs, int num_h
     return (size_t)(total_tokens / kC + num_seqs) * (size_t)num_heads * kRecBytes;
 }
 
+namespace {
+
+// The state pass with SV-column value slices (the chunk kernel has run before it).
+template <int SV>
+cudaError_t launch_state_pass(const PrefillProblem &p, const int32_t *cc, const unsigned char *rec,
+                              cudaLaunchConfig_t cfg)
+{
+    using Sh = StateShape<SV>;
+    static int dev_state = -1;
+    cudaError_t err = allow_smem(prefill_state_kernel<SV>, (int)Sh::SMEM, &dev_state);
+    if (err != cudaSuccess) return err;
+    CUtensorMap tv;
+    if (!make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, SV))
+        return cudaErrorInvalidValue;
+    cfg.blockDim = dim3(kStateThreads);
+    cfg.dynamicSmemBytes = Sh::SMEM;
+    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
+    if (p.split.lseg == 0) {
+        cfg.gridDim = dim3(kD / SV, p.num_heads, p.num_seqs);
+        return cudaLaunchKernelEx(&cfg, prefill_state_kernel<SV>, tv, tv, p.cu_seqlens, p.total_tokens, p.num_heads,
+                                  cc, rec, p.init_state, o, p.final_state, p.status,
+                                  static_cast<const int32_t *>(p.order), p.slots, INT_MAX, (float *)nullptr);
+    }
+    // sequence split: transition pass (R for grid z < nv_max, M above), start states, state pass
+    const SeqSplit &s = p.split;
+    CUtensorMap tz;  // one zero value row: every box of the transition pass reads zeros
+    if (!make_map(&tz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s.vzero, 1, p.num_heads, 2, SV))
+        return cudaErrorInvalidValue;
+    StateSlots sa;
+    sa.fin = s.fin_a;
+    sa.num = (int64_t)s.nv_max + 1;
+    cfg.gridDim = dim3(kD / SV, p.num_heads, 2 * s.nv_max);
+    err = cudaLaunchKernelEx(&cfg, prefill_state_kernel<SV>, tv, tz, (const int32_t *)s.vcu, p.total_tokens,
+                             p.num_heads, (const int32_t *)s.vcc, rec, (const float *)nullptr,
+                             (__nv_bfloat16 *)nullptr, s.R, p.status, (const int32_t *)s.vorder, sa, s.nv_max, s.M);
+    if (err != cudaSuccess) return err;
+    if ((err = launch_seqsplit_combine(p)) != cudaSuccess) return err;
+    StateSlots sc;
+    sc.init = s.init_c;
+    sc.fin = s.fin_c;
+    const int64_t user_entries = p.slots.fin ? p.slots.num : p.num_seqs;
+    sc.num = user_entries > (int64_t)s.nv_max + 1 ? user_entries : (int64_t)s.nv_max + 1;
+    cfg.gridDim = dim3(kD / SV, p.num_heads, s.nv_max);
+    return cudaLaunchKernelEx(&cfg, prefill_state_kernel<SV>, tv, tv, (const int32_t *)s.vcu, p.total_tokens,
+                              p.num_heads, (const int32_t *)s.vcc, rec, (const float *)s.start, o, p.final_state,
+                              p.status, (const int32_t *)s.vorder, sc, INT_MAX, (float *)nullptr);
+}
+
+// SMs of the current device (cached per device).
+int sm_count()
+{
+    static int count[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+    if (!count[dev] && cudaDeviceGetAttribute(&count[dev], cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+        count[dev] = 0;
+    return count[dev];
+}
+
+}  // namespace
+
 cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records, cudaEvent_t mid)
 {
-    static int dev_chunk = -1, dev_chunk_norm = -1, dev_state = -1;
+    static int dev_chunk = -1, dev_chunk_norm = -1;
     auto chunk_kernel = p.qk_l2norm ? prefill_chunk_kernel<true> : prefill_chunk_kernel<false>;
     cudaError_t err = allow_smem(chunk_kernel, (int)kChunkSmem, p.qk_l2norm ? &dev_chunk_norm : &dev_chunk);
     if (err != cudaSuccess) return err;
-    err = allow_smem(prefill_state_kernel, (int)kStateSmem, &dev_state);
-    if (err != cudaSuccess) return err;
-    CUtensorMap tq, tk, tla, tv;
+    CUtensorMap tq, tk, tla;
     if (!make_map(&tq, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.q, p.total_tokens, p.num_heads, 2, kD) ||
-        !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, p.total_tokens, p.num_heads, 2, kD) ||
-        !make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kSV))
+        !make_map(&tk, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.k, p.total_tokens, p.num_heads, 2, kD))
         return cudaErrorInvalidValue;
     // a scalar gate ([T, H]) is read by the prefix scan, never by TMA: its map slot repeats q's
     if (p.scalar_gate)
@@ -932,39 +1026,13 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
                              p.scalar_gate);
     if (err != cudaSuccess) return err;
     if (mid && (err = cudaEventRecord(mid, p.stream)) != cudaSuccess) return err;
-    cfg.blockDim = dim3(kStateThreads);
-    cfg.dynamicSmemBytes = kStateSmem;
+    // 32-column slices while every (sequence, head, slice) of the pass fits in one wave of
+    // SMs (their chain per chunk is shorter); 64-column slices beyond that, and for the
+    // sequence split, whose transition pass is sized for them
     const unsigned char *rec = static_cast<const unsigned char *>(records);
-    __nv_bfloat16 *o = static_cast<__nv_bfloat16 *>(p.o);
-    if (p.split.lseg == 0) {
-        cfg.gridDim = dim3(kD / kSV, p.num_heads, p.num_seqs);
-        return cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, tv, p.cu_seqlens, p.total_tokens, p.num_heads,
-                                  static_cast<const int32_t *>(cc), rec, p.init_state, o, p.final_state, p.status,
-                                  static_cast<const int32_t *>(p.order), p.slots, INT_MAX, (float *)nullptr);
-    }
-    // sequence split: transition pass (R for grid z < nv_max, M above), start states, state pass
-    const SeqSplit &s = p.split;
-    CUtensorMap tz;  // one zero value row: every box of the transition pass reads zeros
-    if (!make_map(&tz, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, s.vzero, 1, p.num_heads, 2, kSV))
-        return cudaErrorInvalidValue;
-    StateSlots sa;
-    sa.fin = s.fin_a;
-    sa.num = (int64_t)s.nv_max + 1;
-    cfg.gridDim = dim3(kD / kSV, p.num_heads, 2 * s.nv_max);
-    err = cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, tz, (const int32_t *)s.vcu, p.total_tokens,
-                             p.num_heads, (const int32_t *)s.vcc, rec, (const float *)nullptr,
-                             (__nv_bfloat16 *)nullptr, s.R, p.status, (const int32_t *)s.vorder, sa, s.nv_max, s.M);
-    if (err != cudaSuccess) return err;
-    if ((err = launch_seqsplit_combine(p)) != cudaSuccess) return err;
-    StateSlots sc;
-    sc.init = s.init_c;
-    sc.fin = s.fin_c;
-    const int64_t user_entries = p.slots.fin ? p.slots.num : p.num_seqs;
-    sc.num = user_entries > (int64_t)s.nv_max + 1 ? user_entries : (int64_t)s.nv_max + 1;
-    cfg.gridDim = dim3(kD / kSV, p.num_heads, s.nv_max);
-    return cudaLaunchKernelEx(&cfg, prefill_state_kernel, tv, tv, (const int32_t *)s.vcu, p.total_tokens,
-                              p.num_heads, (const int32_t *)s.vcc, rec, (const float *)s.start, o, p.final_state,
-                              p.status, (const int32_t *)s.vorder, sc, INT_MAX, (float *)nullptr);
+    const int64_t slices32 = (int64_t)p.num_seqs * p.num_heads * (kD / 32);
+    if (p.split.lseg == 0 && slices32 <= sm_count()) return launch_state_pass<32>(p, cc, rec, cfg);
+    return launch_state_pass<64>(p, cc, rec, cfg);
 }
 
 }  // namespace kda

@@ -263,6 +263,14 @@ __device__ __forceinline__ void tmem_ld8(uint32_t taddr, float (&r)[8])
 // at columns [c, c + N), thread t >= 16 gets lane (quarter base + t - 16) at columns
 // [c + HALF, c + HALF + N) (the 16x32bx2 shape; HALF is the immediate half-split offset).
 template <int HALF>
+__device__ __forceinline__ void tmem_ld16x2_x4(uint32_t taddr, float (&r)[4])
+{
+    uint32_t *u = reinterpret_cast<uint32_t *>(r);
+    asm volatile("tcgen05.ld.sync.aligned.16x32bx2.x4.b32 {%0,%1,%2,%3}, [%4], %5;"
+                 : "=r"(u[0]), "=r"(u[1]), "=r"(u[2]), "=r"(u[3])
+                 : "r"(taddr), "n"(HALF));
+}
+template <int HALF>
 __device__ __forceinline__ void tmem_ld16x2_x8(uint32_t taddr, float (&r)[8])
 {
     uint32_t *u = reinterpret_cast<uint32_t *>(r);

@@ -95,6 +95,21 @@ def test_varlen16_full_size_every_unit():
     _whole_tensor_parity(synth.VARLEN_16, group=4)
 
 
+@pytest.mark.parametrize("H", [1, 2], ids=["32_column_slices", "64_column_slices"])
+def test_state_pass_slice_widths(H):
+    """The state pass takes 32-column value slices while all of them fit in one wave of
+    SMs and 64-column slices beyond that: 20 ragged sequences from initial states give
+    20 x H x 4 = 80 slices at H = 1 and 160 at H = 2 (a GB300 has 152 SMs).  Every unit
+    against the oracle."""
+    rng = np.random.default_rng(150 + H)
+    lens = tuple(int(x) for x in rng.integers(0, 300, size=20))
+    w = PrefillWorkload(f"slices_H{H}", 150 + H, H, 128, "bf16", lens, len(lens), init_state=True)
+    inp = synth.prefill_inputs(w)
+    o, fs = gpu_prefill(inp)
+    o_ref, fs_ref = oracle_prefill(inp)
+    assert_parity(o, fs, o_ref, fs_ref, "bf16", w.name)
+
+
 def _custom(name, wid, lens, H=1, d=128, dtype="bf16", init_state=False, log_alpha=None):
     w = PrefillWorkload(name, wid, H, d, dtype, tuple(lens), len(lens), init_state=init_state)
     inp = synth.prefill_inputs(w)
