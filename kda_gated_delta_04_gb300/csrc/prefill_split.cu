@@ -434,13 +434,14 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         tc_fence_before_sync();
         if (__syncthreads_or(late)) { timed_out = true; break; }
         if (issuer) {
-            tc_fence_after_sync();
-            issue_n_q<L>(sb, tmem, with_o);
-            mma_commit(&bar_mma);
+            // the P and P2 images go out first, so their reads overlap the N, Q'' issue
             bulk_store(rec + R_P, sm + L::ST_P, 16384);
             if (with_o) bulk_store(rec + R_P2, sm + L::ST_P2, 8192);
             bulk_commit();
             stores_pending = true;
+            tc_fence_after_sync();
+            issue_n_q<L>(sb, tmem, with_o);
+            mma_commit(&bar_mma);
         }
         ok = mbar_wait_ns(&bar_mma, 0, kWaitNs);
         if (issuer) bulk_wait_read();  // the P image is overwritten next
