@@ -325,65 +325,83 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     // schedule (complete by then) before it waits for this kernel's records.
     pdl_wait();
     pdl_launch_dependents();
-    // one CTA per (chunk, head), heads fastest, chunks last to first
-    const int h = (int)(blockIdx.x % (unsigned)H);
-    const int g = chunk_bound - 1 - (int)(blockIdx.x / (unsigned)H);
-    const int2 dsc = desc[g];     // first token and row count of packed chunk g
-    if (dsc.y <= 0) return;       // past the last chunk (the grid is an upper bound)
-    const int64_t c0 = dsc.x;
-    const int len = dsc.y;
-    unsigned char *rec = records + ((size_t)g * H + h) * kRecBytes;
-
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5;
     const bool compute = tid < kChunkCompute, issuer = tid == kChunkIssuer;
     constexpr int kIssueWarp = kChunkIssuer / 32;
+    // Persistent: item = (chunk, head), heads fastest, chunks last to first; this CTA takes
+    // items blockIdx.x, blockIdx.x + gridDim.x, ...  Items past the last packed chunk (the
+    // chunk count is an upper bound) are skipped.
+    const int items = chunk_bound * H;
+    auto next_item = [&](int it, int &h, int &g, int2 &dsc) -> int {
+        for (; it < items; it += (int)gridDim.x) {
+            h = it % H;
+            g = chunk_bound - 1 - it / H;
+            dsc = desc[g];  // first token and row count of packed chunk g
+            if (dsc.y > 0) break;
+        }
+        return it;
+    };
+    int h = 0, g = 0;
+    int2 dsc = make_int2(0, 0);
+    int it = next_item((int)blockIdx.x, h, g, dsc);
+    // q and k boxes, and (per-channel gate) the log_alpha box into O1, which is free until
+    // the decayed operands are written there
+    const uint32_t tma_bytes = 16384 + 16384 + (scalar_gate ? 0u : 32768u);
     if (issuer) {
         mbar_init(&bar_tma, 1);
         mbar_init(&bar_mma, 1);
         mbar_init(&bar_p, 1);
         mbar_init(&bar_drain, 1);
         fence_mbar_init();
-        // q and k boxes, and (per-channel gate) the log_alpha box into O1, free until the
-        // decayed operands are written there
-        mbar_arrive_expect_tx(&bar_tma, 16384 + 16384 + (scalar_gate ? 0u : 32768u));
-        tma_load_3d(sm + L::IN_Q, &tm_q, &bar_tma, 0, h, (int)c0);
-        tma_load_3d(sm + L::IN_K, &tm_k, &bar_tma, 0, h, (int)c0);
-        if (!scalar_gate) tma_load_3d(sm + L::O1, &tm_la, &bar_tma, 0, h, (int)c0);
+        if (it < items) {
+            mbar_arrive_expect_tx(&bar_tma, tma_bytes);
+            if (!scalar_gate) tma_load_3d(sm + L::O1, &tm_la, &bar_tma, 0, h, dsc.x);
+            tma_load_3d(sm + L::IN_Q, &tm_q, &bar_tma, 0, h, dsc.x);
+            tma_load_3d(sm + L::IN_K, &tm_k, &bar_tma, 0, h, dsc.x);
+        }
     }
     if (warp == kIssueWarp) {
         tmem_alloc(&tmem_holder, kChunkTmem);
         tmem_relinquish();
     }
-    if (tid < kC) s_beta[tid] = tid < len ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
-    float *s_tot = reinterpret_cast<float *>(sm + L::AQ);
-    float2 gl[4096 / NT];
-    float gmin = 0.f, gmax = 0.f;
-    // scalar gate (log_alpha [T, H], one decay per token-head): the prefix reads its 64
-    // values straight from global memory while the boxes fly
-    if (compute && scalar_gate)
-        prefix_scan<NT>(log_alpha + (size_t)c0 * H + h, H, len, s_tot, gl, gmin, gmax, true);
     __syncthreads();  // barriers initialised, TMEM allocated
     tc_fence_after_sync();
     const uint32_t tmem = tmem_holder;
-    bool timed_out = false, tma_pending = true, decay_bad = false, range_ok = true, stores_pending = false;
-    do {
-        bool ok = !compute || mbar_wait_ns(&bar_tma, 0, kWaitNs);
+    float *s_tot = reinterpret_cast<float *>(sm + L::AQ);
+    bool timed_out = false, decay_bad = false, range_ok = true, stores_pending = false;
+    uint32_t n = 0;  // items done by this CTA: the barriers' phase parities follow it
+    for (; it < items; ++n) {
+        const int64_t c0 = dsc.x;
+        const int len = dsc.y;
+        unsigned char *rec = records + ((size_t)g * H + h) * kRecBytes;
+        // the next item, so that its descriptor load overlaps this item's work
+        int hn = 0, gn = 0;
+        int2 dn = make_int2(0, 0);
+        const int itn = next_item(it + (int)gridDim.x, hn, gn, dn);
+        const uint32_t pm = (3u * n) & 1u;  // bar_mma completes three times per item
+        if (tid < kC) s_beta[tid] = tid < len ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
+        float2 gl[4096 / NT];
+        float gmin = 0.f, gmax = 0.f;
+        // scalar gate (log_alpha [T, H], one decay per token-head): the prefix reads its 64
+        // values straight from global memory while the boxes fly
+        if (compute && scalar_gate)
+            prefix_scan<NT>(log_alpha + (size_t)c0 * H + h, H, len, s_tot, gl, gmin, gmax, true);
+        bool ok = !compute || mbar_wait_ns(&bar_tma, n & 1u, kWaitNs);
         if (compute && !scalar_gate && ok)  // the per-channel prefix from the log_alpha box
             prefix_scan<NT>(reinterpret_cast<const float *>(sm + L::O1), kD, len, s_tot, gl, gmin, gmax);
         // every thread is past its reads of the log_alpha box and s_tot is complete
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        tma_pending = false;
         if (NORM) {
             if (compute) qk_row_inv_norms<NT>(sm + L::IN_K, sm + L::IN_Q, s_rn);
             __syncthreads();
         }
         float2 ot[2];
         if (compute)
-            decay_bad = decayed_operands<L, NT, false, NORM>(sm, len, s_tot, nullptr,
-                                                       reinterpret_cast<float *>(rec + R_GM), gl, gmin, gmax, ot,
-                                                       s_rn);
+            decay_bad |= decayed_operands<L, NT, false, NORM>(sm, len, s_tot, nullptr,
+                                                        reinterpret_cast<float *>(rec + R_GM), gl, gmin, gmax, ot,
+                                                        s_rn);
         fence_proxy_async_smem();
         __syncthreads();
         if (issuer) {
@@ -396,7 +414,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // holds them up while it issues.
         bool late = false;
         if (compute) {
-            late = !mbar_wait_ns(&bar_mma, 0, kWaitNs);
+            late = !mbar_wait_ns(&bar_mma, pm, kWaitNs);
             tc_fence_after_sync();
             if (!late) kk_epilogue<L, NT>(sm, tmem, s_beta, sm + L::AQ);
             tc_fence_before_sync();
@@ -420,10 +438,10 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             mma_commit(&bar_p);
         }
         if (compute) {  // the issuing warp is still issuing P meanwhile
-            late = !mbar_wait_ns(&bar_mma, 1, kWaitNs);
+            late = !mbar_wait_ns(&bar_mma, pm ^ 1u, kWaitNs);
             tc_fence_after_sync();
             if (!late) w_epilogue<L, NT>(sm, tmem + TC_W);  // -W over Kg in O1
-            late = late || !mbar_wait_ns(&bar_p, 0, kWaitNs);
+            late = late || !mbar_wait_ns(&bar_p, n & 1u, kWaitNs);
             tc_fence_after_sync();
             if (!late) {
                 epi_p<NT>(tmem, sm + L::ST_P, range_ok);    // the k box is dead
@@ -443,7 +461,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             issue_n_q<L>(sb, tmem, with_o);
             mma_commit(&bar_mma);
         }
-        ok = mbar_wait_ns(&bar_mma, 0, kWaitNs);
+        ok = mbar_wait_ns(&bar_mma, pm, kWaitNs);
         if (issuer) bulk_wait_read();  // the P image is overwritten next
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
@@ -452,19 +470,34 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             if (with_o) epi_q<L, NT>(sm, tmem, sm + L::ST_NQ + 32768);
         }
         fence_proxy_async_smem();
+        tc_fence_before_sync();  // this item's TMEM reads precede the next item's products
         __syncthreads();
         if (issuer) {
             bulk_store(rec + R_N, sm + L::ST_NQ, with_o ? 49152u : 32768u);  // N | Q'
             bulk_commit();
+            if (itn < items) {
+                // the next item's boxes: log_alpha into O1 at once (free after Q'), q and k
+                // once the store has read [0, 48 KB), where they land
+                mbar_arrive_expect_tx(&bar_tma, tma_bytes);
+                if (!scalar_gate) tma_load_3d(sm + L::O1, &tm_la, &bar_tma, 0, hn, dn.x);
+                bulk_wait_read();
+                tma_load_3d(sm + L::IN_Q, &tm_q, &bar_tma, 0, hn, dn.x);
+                tma_load_3d(sm + L::IN_K, &tm_k, &bar_tma, 0, hn, dn.x);
+            }
         }
-    } while (false);
+        it = itn;
+        h = hn;
+        g = gn;
+        dsc = dn;
+    }
     if (timed_out) {
         if (issuer) {
             atomicOr(status, DEV_ERR_TIMEOUT);
             mma_commit(&bar_drain);  // completes once every MMA issued so far has
         }
         (void)mbar_wait_ns(&bar_drain, 0, kWaitNs);
-        if (tma_pending) (void)mbar_wait_ns(&bar_tma, 0, kWaitNs);
+        // the item that gave up may still have its boxes in flight
+        (void)mbar_wait_ns(&bar_tma, n & 1u, kWaitNs);
     }
     // the record stores must have read their shared-memory sources before the CTA exits
     // and its shared memory is reused; their global writes complete before the kernel does
@@ -1016,7 +1049,9 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl.val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(chunk_bound * p.num_heads));
+    // persistent: two CTAs per SM (or one per item when there are fewer)
+    const int64_t items = chunk_bound * p.num_heads, slots = 2 * (int64_t)sm_count();
+    cfg.gridDim = dim3((unsigned)(items < slots || slots <= 0 ? items : slots));
     cfg.blockDim = dim3(kChunkThreads);
     cfg.dynamicSmemBytes = kChunkSmem;
     cfg.stream = p.stream;

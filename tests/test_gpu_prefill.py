@@ -559,6 +559,33 @@ def test_options_together_on_a_split_problem():
     assert_parity(synth.to_f64(o_p), synth.to_f64(fs_d), o_ref, fs_ref, "bf16", "options together, split")
 
 
+@pytest.mark.parametrize("scalar,qkn", [(False, False), (True, True)], ids=["plain", "scalar_gate_qk_norm"])
+def test_more_items_than_resident_chunk_ctas(scalar, qkn):
+    """The chunk kernel keeps two CTAs per SM and each walks several (chunk, head) items:
+    8 heads over 3,100 ragged tokens in 7 sequences give 440 items against 304 CTA slots,
+    with initial states, and with or without the scalar gate and in-kernel q/k
+    normalisation.  Every unit against the oracle."""
+    H = 8
+    w = PrefillWorkload(f"persistent_{int(scalar)}{int(qkn)}", 160 + 2 * scalar + qkn, H, 128, "bf16",
+                        (700, 513, 64, 1, 900, 455, 467), 7, init_state=True, raw_qk=qkn)
+    inp = synth.prefill_inputs(w)
+    dev = to_device(inp)
+    ref = dict(inp)
+    la = dev["log_alpha"]
+    if scalar:
+        la_s, la_full = _scalar_gate(inp, 160)
+        la = la_s.cuda()
+        ref["log_alpha"] = la_full
+    if qkn:
+        ref["q"] = oracle.l2_normalize(synth.to_f64(inp["q"]))
+        ref["k"] = oracle.l2_normalize(synth.to_f64(inp["k"]))
+    o, fs = kda.prefill(dev["q"], dev["k"], dev["v"], la, dev["beta"], dev["cu_seqlens"], dev["init_state"],
+                        check_status=True, qk_l2norm=qkn)
+    torch.cuda.synchronize()
+    o_ref, fs_ref = oracle_prefill(ref)
+    assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, "bf16", w.name)
+
+
 def test_split_prefill_into_a_pool_then_paged_decode():
     """A long prompt with few heads goes through the sequence-split pass straight into a
     state pool; paged decode continues from it within the bar of the oracle."""
