@@ -35,6 +35,8 @@ constexpr int kThreads = 256;
 // (cc[n] = sum over m < n of ceil(len_m / 64); cc[num_seqs] = all chunks) and, when desc
 // is given, every packed chunk's first token and row count (0 rows past the last chunk),
 // so that a chunk CTA finds its rows with one load.
+constexpr int kPrepStaged = 4096;  // sequences whose boundaries and chunk offsets live in shared memory
+
 __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs, int64_t total,
                                     uint32_t *status, int32_t *order, int32_t *cc, int2 *desc,
                                     int chunk_bound)
@@ -42,6 +44,11 @@ __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs
     // the chunk kernel may be scheduled now; it waits for this kernel's results itself
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     __shared__ int bad;
+    // up to kPrepStaged sequences: cu (clamped as seq_range clamps it) and the chunk offsets
+    // cc are kept here, so the sort and the descriptor search read no global memory
+    __shared__ int32_t s_cu[kPrepStaged + 1];
+    __shared__ int32_t s_cc[kPrepStaged + 1];
+    const bool staged = cu && num_seqs <= kPrepStaged;
     if (threadIdx.x == 0) bad = 0;
     __syncthreads();
     if (cu) {
@@ -50,20 +57,30 @@ __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs
             if (n == 0 && c != 0) bad = 1;
             if (n == num_seqs && c != total) bad = 1;
             if (n < num_seqs && cu[n + 1] < c) bad = 1;
+            if (staged) s_cu[n] = c;
         }
     }
     __syncthreads();
     if (threadIdx.x == 0) *status = bad ? DEV_ERR_SEQLENS : 0u;
-    const bool sort = cu && num_seqs <= 4096;
+    // the range [t0, t1) of sequence n, clamped exactly as seq_range clamps it
+    auto range = [&](int n, int64_t &t0, int64_t &t1) {
+        if (!staged) { seq_range(cu, n, total, t0, t1); return; }
+        int64_t a = s_cu[n], b = s_cu[n + 1];
+        a = a < 0 ? 0 : (a > total ? total : a);
+        b = b < a ? a : (b > total ? total : b);
+        t0 = a;
+        t1 = b;
+    };
+    const bool sort = cu && num_seqs <= kPrepStaged;
     for (int n = threadIdx.x; n < num_seqs; n += blockDim.x) {
         if (!sort) { order[n] = n; continue; }
         int64_t t0, t1;
-        seq_range(cu, n, total, t0, t1);
+        range(n, t0, t1);
         const int64_t len = t1 - t0;
         int rank = 0;
         for (int m = 0; m < num_seqs; ++m) {
             int64_t a0, a1;
-            seq_range(cu, m, total, a0, a1);
+            range(m, a0, a1);
             const int64_t lm = a1 - a0;
             rank += (lm > len) || (lm == len && m < n);
         }
@@ -78,7 +95,7 @@ __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs
         int cnt = 0;
         if (n < num_seqs) {
             int64_t t0, t1;
-            seq_range(cu, n, total, t0, t1);
+            range(n, t0, t1);
             cnt = (int)((t1 - t0 + kChunk - 1) / kChunk);
         }
         int incl = cnt;  // inclusive scan inside the warp
@@ -98,12 +115,16 @@ __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs
         }
         __syncthreads();
         const int before = warp > 0 ? warp_sums[warp - 1] : 0;
-        if (n < num_seqs) cc[n] = carry + before + incl - cnt;
+        if (n < num_seqs) {
+            cc[n] = carry + before + incl - cnt;
+            if (staged || !cu) s_cc[n] = carry + before + incl - cnt;
+        }
         carry += warp_sums[31];
         __syncthreads();
     }
     if (threadIdx.x == 0) cc[num_seqs] = carry;
     if (!desc) return;
+    const bool cc_shared = staged || !cu;  // (without cu_seqlens there is one sequence)
     __syncthreads();  // cc complete (global writes of this block are visible to it after the barrier)
     for (int g = threadIdx.x; g < chunk_bound; g += blockDim.x) {
         int2 d = make_int2(0, 0);
@@ -111,11 +132,11 @@ __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs
             int lo = 0, hi = num_seqs;  // the sequence n with cc[n] <= g < cc[n + 1]
             while (hi - lo > 1) {
                 const int mid = (lo + hi) >> 1;
-                if (cc[mid] <= g) lo = mid; else hi = mid;
+                if ((cc_shared ? s_cc[mid] : cc[mid]) <= g) lo = mid; else hi = mid;
             }
             int64_t t0, t1;
-            seq_range(cu, lo, total, t0, t1);
-            const int64_t c0 = t0 + (int64_t)(g - cc[lo]) * kChunk;
+            range(lo, t0, t1);
+            const int64_t c0 = t0 + (int64_t)(g - (cc_shared ? s_cc[lo] : cc[lo])) * kChunk;
             d = make_int2((int)c0, (int)((t1 - c0) < kChunk ? (t1 - c0) : kChunk));
         }
         desc[g] = d;
