@@ -8,8 +8,9 @@ timed in the same run on its own workload (256 sequences x 32 heads, d=128,
 1000 in-place steps) and reported under "decode".  The two larger prefill
 workloads are timed in the same run, each with its own roofline and oracle
 baseline: one sequence of T=65536 tokens from a nonzero initial state under
-"long_prefill", and 16 packed sequences of 512..16384 tokens (168,023 in all)
-under "varlen_prefill".  A long single sequence with few heads (T=65536, H=4),
+"long_prefill" (beside it, "bounded_records": the same call with a workspace whose
+per-chunk records cover 128 chunks at a time), and 16 packed sequences of
+512..16384 tokens (168,023 in all) under "varlen_prefill".  A long single sequence with few heads (T=65536, H=4),
 where the serial state pass would leave most SMs idle, is timed with and
 without the sequence-split state pass under "long_context".
 
@@ -51,6 +52,7 @@ sys.path.insert(0, ROOT)
 METRIC = "KDA prefill tokens/s & decode steps/s (H=32,d=128) and % of roofline"
 L2_FLUSH_BYTES = 256 << 20
 CASE_STEPS = 5  # timed calls of each further prefill workload (2.5 to 10 ms each)
+BOUNDED_CHUNKS = 128  # packed chunks per segment of the bounded-records measurement (T=65536: 8 segments)
 
 
 def _env_rank():
@@ -405,16 +407,38 @@ class _Gpu:
              "ws": kda.workspace_for(N, T, H, d, kda.KDA_DTYPE_BF16, self.dev)}
         return c
 
-    def case_call(self, c, events=None):
+    def case_call(self, c, events=None, ws=None):
         kda, x = self.kda, c["x"]
+        ws = c["ws"] if ws is None else ws
         s0 = None if x["init_state"] is None else x["init_state"].data_ptr()
         args = (x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), x["log_alpha"].data_ptr(),
                 x["beta"].data_ptr(), x["cu_seqlens"].data_ptr(), c["N"], c["T"], c["H"], c["d"],
                 c["d"], kda.KDA_DTYPE_BF16, s0, c["o"].data_ptr(), c["fs"].data_ptr(),
-                c["ws"].data_ptr(), c["ws"].numel(), self.sh)
+                ws.data_ptr(), ws.numel(), self.sh)
         st = kda.kda_prefill(*args) if events is None else kda.kda_prefill_events(*args, events)
         if st != kda.KDA_OK:
             raise kda.KdaError(st, "kda_prefill")
+
+    def time_bounded(self, c, segment_chunks, steps, warmup):
+        """Event time (ms per call) of the same prefill with a workspace whose per-chunk
+        records cover only `segment_chunks` packed chunks (the pass then runs in segments);
+        returns (ms, workspace bytes)."""
+        torch = self.torch
+        ws = self.kda.segmented_workspace_for(c["N"], c["T"], c["H"], c["d"], self.kda.KDA_DTYPE_BF16,
+                                              self.dev, segment_chunks)
+        for _ in range(warmup):
+            self.case_call(c, ws=ws)
+        torch.cuda.synchronize()
+        a, b = self.event(), self.event()
+        a.record(self.stream)
+        for _ in range(steps):
+            self.case_call(c, ws=ws)
+        b.record(self.stream)
+        torch.cuda.synchronize()
+        st = self.kda.kda_read_device_status(ws.data_ptr(), self.sh)
+        if st != self.kda.KDA_OK:
+            raise self.kda.KdaError(st, "kda_prefill, bounded records (device status)")
+        return a.elapsed_time(b) / steps, ws.numel()
 
     def time_case(self, c, steps, warmup):
         """Per-call event times (ms) of kda_prefill on one workload, and the per-kernel split
@@ -532,6 +556,9 @@ def run_gpu(args):
             c = g.setup_case(case_ws[name][0])
             barrier()
             case_ms[name] = (c, g.time_case(c, CASE_STEPS, max(3, args.warmup)))
+            if name == "long_prefill":  # the same call with records for BOUNDED_CHUNKS chunks at a time
+                c["bounded"] = g.time_bounded(c, BOUNDED_CHUNKS, CASE_STEPS, max(3, args.warmup))
+                c["full_ws_bytes"] = c["ws"].numel()
             c["with_init"] = c["inp"]["init_state"] is not None
             # the oracle's sample is cut out now; the full host inputs are dropped
             c["cpu_sample"] = case_sample(c["w"], c["inp"])
@@ -593,6 +620,15 @@ def run_gpu(args):
                "gpu_launches": 3 * len(call_ms),
                "roofline": prefill_roofline(T, H, d, N, c["with_init"], ms,
                                             stage_mean, peaks, case_ws[name][1])}
+        if "bounded" in c:
+            bms, bws = c["bounded"]
+            bms = reduce_max(bms)
+            blk["bounded_records"] = {
+                "segment_chunks": BOUNDED_CHUNKS, "workspace_bytes": bws, "full_workspace_bytes": c["full_ws_bytes"],
+                "value": aggregate_rate(T, world, 1, bms), "ms_per_call": bms, "steps": CASE_STEPS,
+                "note": "kda_prefill with a workspace from kda_prefill_workspace_size_segmented: the chunk and "
+                        "state kernels run over segments of that many packed chunks (results bit for bit those "
+                        "of the full workspace without the sequence split)"}
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             blk["cpu_baseline"] = cpu_baseline_case(w, c["cpu_sample"])
         line[name] = blk

@@ -84,6 +84,29 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
                                   int32_t d_k, int32_t d_v, kda_dtype_t dtype);
 
 /*
+ * Workspace bytes for the two-kernel prefill with its per-chunk records bounded (the
+ * chunkwise form of "From 124M to 2.8T", chapter 3, run over a bounded window of chunks
+ * at a time).  kda_prefill_workspace_size covers the records of every packed 64-token
+ * chunk, about 1.16 KB per token-head (a one-million-token, 32-head prompt would need
+ * about 39 GB).  With this size instead the records cover at most segment_chunks packed
+ * chunks: kda_prefill then runs the chunk kernel and the state pass one segment of
+ * packed chunks after the other, and a sequence cut at a segment boundary carries its
+ * fp32 state to the next segment in the workspace (two [num_heads, 128, 128] fp32
+ * buffers).  The results are bit for bit those of the full workspace without the
+ * sequence split (KDA_FLAG_NO_SEQ_SPLIT); each extra segment costs two more launches.
+ * Any workspace between this size for segment_chunks = 1 and kda_prefill_workspace_size
+ * runs segmented, with as many chunks per segment as its records fit.
+ *
+ *  segment_chunks  >= 1; values past the packed chunk bound (total_tokens / 64 +
+ *                  num_seqs) are clamped to it.
+ *  Returns 0 for invalid arguments and for shapes the two-kernel path does not run
+ *  (anything but bf16, d_k = d_v = 128, total_tokens > 0).
+ */
+size_t kda_prefill_workspace_size_segmented(int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                                            int32_t d_k, int32_t d_v, kda_dtype_t dtype,
+                                            int64_t segment_chunks);
+
+/*
  * Chunkwise prefill over packed variable-length sequences ("K3 attention,
  * three-piece set": chunkwise-parallel form with WY representation and UT
  * transform; "From 124M to 2.8T", chapter 3: parallel inside a chunk, serial
@@ -106,8 +129,10 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
  *  workspace   device buffer owned by the caller, 256-byte aligned, reused by every
  *              call.  With kda_prefill_workspace_size(...) bytes or more the bf16,
  *              d = 128 prefill runs as two kernels (chunk-local products for all
- *              chunks at once, then the serial state pass); with at least
- *              KDA_PREFILL_MIN_WORKSPACE(num_seqs) bytes it runs as one fused
+ *              chunks at once, then the serial state pass); with less, but at least
+ *              kda_prefill_workspace_size_segmented(..., 1) bytes, as the same two
+ *              kernels over segments of chunks (bounded records, identical results);
+ *              with at least KDA_PREFILL_MIN_WORKSPACE(num_seqs) bytes as one fused
  *              kernel (same results up to rounding order, slower).  Smaller
  *              workspaces are rejected.
  *  q, k, v, log_alpha and beta may be NULL when total_tokens == 0.

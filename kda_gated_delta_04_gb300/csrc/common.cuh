@@ -72,7 +72,21 @@ struct PrefillProblem {
     StateSlots slots;           // state pool indices, or none (dense states)
     SeqSplit split;             // sequence-split state pass, or none
     bool qk_l2norm = false;     // q, k rows are normalised in the kernels
+    // bounded records (two-kernel path): records for seg_chunks packed chunks at a time, the
+    // pass run segment by segment; a sequence cut at a segment boundary carries its state in
+    // carry (two [num_heads, d, d] fp32 buffers, alternating by segment).  0: unsegmented.
+    int seg_chunks = 0;
+    float *carry = nullptr;
     cudaStream_t stream;
+};
+
+// The part of the packed chunk range one launch of the state pass walks: chunks
+// [g_lo, g_hi) (records indexed from g_lo); a sequence that began in an earlier segment
+// starts from carry_in[head], one that goes on past g_hi ends in carry_out[head].
+struct StateSegment {
+    int g_lo = 0, g_hi = 0x7fffffff;
+    const float *carry_in = nullptr;
+    float *carry_out = nullptr;
 };
 
 struct DecodeProblem {
@@ -99,6 +113,8 @@ bool prefill_tc_supported(const PrefillProblem &p);  // bf16, d = 128, 0 < total
 cudaError_t launch_prefill_tc(const PrefillProblem &p);
 // Two-kernel tensor-core prefill (needs p.cc and p.records).
 size_t prefill_split_records_bytes(int64_t total_tokens, int num_seqs, int num_heads);
+// bytes of one (chunk, head) record of the two-kernel path
+size_t prefill_split_record_bytes();
 // `mid` (may be null) is recorded on p.stream between the chunk kernel and the state kernel.
 cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records,
                                  cudaEvent_t mid = nullptr);

@@ -63,6 +63,14 @@ size_t ws_split_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
     return ws_records_bytes(num_seqs, total_tokens, num_heads) +
            kda::seqsplit_bytes(num_seqs, total_tokens, num_heads);
 }
+// the two-kernel path with bounded records: schedule, chunk numbering, descriptors, two
+// carried states per head ([num_heads, 128, 128] fp32 each) and records for seg_chunks chunks
+size_t ws_carry_bytes(int32_t num_heads) { return round_up((size_t)2 * num_heads * 128 * 128 * sizeof(float), 256); }
+size_t ws_segmented_fixed(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
+{
+    return ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) + ws_desc_bytes(num_seqs, total_tokens) +
+           ws_carry_bytes(num_heads);
+}
 
 kda_status_t check_shape(int32_t d_k, int32_t d_v, kda_dtype_t dtype)
 {
@@ -86,6 +94,18 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
     if (split_shape(num_seqs, total_tokens, num_heads, d_k, d_v, dtype))
         return ws_split_bytes(num_seqs, total_tokens, num_heads);
     return ws_min_bytes(num_seqs);
+}
+
+size_t kda_prefill_workspace_size_segmented(int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                                            int32_t d_k, int32_t d_v, kda_dtype_t dtype,
+                                            int64_t segment_chunks)
+{
+    if (num_seqs < 0 || total_tokens < 0 || num_heads <= 0 || segment_chunks < 1) return 0;
+    if (!split_shape(num_seqs, total_tokens, num_heads, d_k, d_v, dtype)) return 0;
+    const int64_t bound = chunk_bound(num_seqs, total_tokens);
+    const int64_t seg = segment_chunks < bound ? segment_chunks : bound;
+    return ws_segmented_fixed(num_seqs, total_tokens, num_heads) +
+           (size_t)seg * (size_t)num_heads * kda::prefill_split_record_bytes();
 }
 
 namespace {
@@ -136,17 +156,31 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     p.order = reinterpret_cast<int32_t *>(ws + kda::kWorkspaceHeader);
     p.stream = strm;
     // bf16 at d = 128 runs on the tensor cores: as the chunk / state kernel pair when the
-    // workspace holds the per-chunk records, else as the single fused kernel.  fp32 I/O
-    // (the exact path) and d = 64 run the CUDA-core chunk kernel.
-    const bool split = split_shape(num_seqs, total_tokens, num_heads, d_k, d_v, dtype) &&
-                       workspace_bytes >= ws_records_bytes(num_seqs, total_tokens, num_heads);
+    // workspace holds the per-chunk records (all of them, or those of a bounded number of
+    // chunks at a time, the pass then run in segments), else as the single fused kernel.
+    // fp32 I/O (the exact path) and d = 64 run the CUDA-core chunk kernel.
+    const bool split_ok = split_shape(num_seqs, total_tokens, num_heads, d_k, d_v, dtype);
+    const bool full = split_ok && workspace_bytes >= ws_records_bytes(num_seqs, total_tokens, num_heads);
+    const size_t rec_chunk = (size_t)num_heads * kda::prefill_split_record_bytes();
+    const size_t seg_fixed = split_ok ? ws_segmented_fixed(num_seqs, total_tokens, num_heads) : 0;
+    const bool segmented = split_ok && !full && workspace_bytes >= seg_fixed + rec_chunk;
+    const bool split = full || segmented;
     p.cc = split ? reinterpret_cast<int32_t *>(ws + ws_min_bytes(num_seqs)) : nullptr;
     p.desc = split ? reinterpret_cast<int2 *>(ws + ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs)) : nullptr;
     p.chunk_bound = split ? (int)chunk_bound(num_seqs, total_tokens) : 0;
-    p.records = split ? ws + ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) + ws_desc_bytes(num_seqs, total_tokens)
-                      : nullptr;
+    const size_t after_desc = ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) + ws_desc_bytes(num_seqs, total_tokens);
+    if (full) {
+        p.records = ws + after_desc;
+    } else if (segmented) {
+        p.carry = reinterpret_cast<float *>(ws + after_desc);
+        p.records = ws + seg_fixed;
+        const size_t fit = (workspace_bytes - seg_fixed) / rec_chunk;
+        p.seg_chunks = fit < (size_t)p.chunk_bound ? (int)fit : p.chunk_bound;
+    } else {
+        p.records = nullptr;
+    }
     // few (sequence, head) units: the state pass runs each sequence in segments
-    if (split && !(flags & KDA_FLAG_NO_SEQ_SPLIT) &&
+    if (full && !(flags & KDA_FLAG_NO_SEQ_SPLIT) &&
         workspace_bytes >= ws_split_bytes(num_seqs, total_tokens, num_heads))
         kda::seqsplit_carve(p.split, num_seqs, total_tokens, num_heads,
                             static_cast<char *>(p.records) +

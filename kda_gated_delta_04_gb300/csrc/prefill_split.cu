@@ -308,7 +308,7 @@ __global__ void __launch_bounds__(kChunkThreads, 2)
 prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_la, const float *__restrict__ log_alpha,
                      const float *__restrict__ beta,
-                     const int2 *__restrict__ desc, int H, int chunk_bound,
+                     const int2 *__restrict__ desc, int H, int g_base, int seg_chunks,
                      unsigned char *__restrict__ records, uint32_t *status, bool with_o, bool scalar_gate)
 {
     using L = ChunkLayout;
@@ -330,14 +330,15 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     const int tid = threadIdx.x, warp = tid >> 5;
     const bool compute = tid < kChunkCompute, issuer = tid == kChunkIssuer;
     constexpr int kIssueWarp = kChunkIssuer / 32;
-    // Persistent: item = (chunk, head), heads fastest, chunks last to first; this CTA takes
-    // items blockIdx.x, blockIdx.x + gridDim.x, ...  Items past the last packed chunk (the
-    // chunk count is an upper bound) are skipped.
-    const int items = chunk_bound * H;
+    // Persistent: item = (chunk, head) over the packed chunks g_base .. g_base + seg_chunks - 1,
+    // heads fastest, chunks last to first; this CTA takes items blockIdx.x, blockIdx.x +
+    // gridDim.x, ...  Items past the last packed chunk (the chunk count is an upper bound)
+    // are skipped.  Records are indexed from g_base.
+    const int items = seg_chunks * H;
     auto next_item = [&](int it, int &h, int &g, int2 &dsc) -> int {
         for (; it < items; it += (int)gridDim.x) {
             h = it % H;
-            g = chunk_bound - 1 - it / H;
+            g = g_base + seg_chunks - 1 - it / H;
             dsc = desc[g];  // first token and row count of packed chunk g
             if (dsc.y > 0) break;
         }
@@ -375,7 +376,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     for (; it < items; ++n) {
         const int64_t c0 = dsc.x;
         const int len = dsc.y;
-        unsigned char *rec = records + ((size_t)g * H + h) * kRecBytes;
+        unsigned char *rec = records + ((size_t)(g - g_base) * H + h) * kRecBytes;
         // the next item, so that its descriptor load overlaps this item's work
         int hn = 0, gn = 0;
         int2 dn = make_int2(0, 0);
@@ -589,7 +590,8 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
                      const int32_t *__restrict__ cu, int64_t total, int H, const int32_t *__restrict__ cc,
                      const unsigned char *__restrict__ records, const float *init_state,
                      __nv_bfloat16 *__restrict__ o, float *final_state, uint32_t *status,
-                     const int32_t *__restrict__ order, StateSlots slots, int z_ident, float *final_ident)
+                     const int32_t *__restrict__ order, StateSlots slots, int z_ident, float *final_ident,
+                     StateSegment seg)
 {
     using Sh = StateShape<SV>;
     using L = Sh;
@@ -612,15 +614,31 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     const int j0 = blockIdx.x * SV, h = blockIdx.y, n = order[ident ? blockIdx.z - z_ident : blockIdx.z];
     int64_t t0, t1;
     seq_range(cu, n, total, t0, t1);
-    const int nchunks = (int)((t1 - t0 + kC - 1) / kC);
+    int nchunks = (int)((t1 - t0 + kC - 1) / kC);
+    // the sequence's packed chunks inside this launch's segment [seg.g_lo, seg.g_hi)
+    const int cn0 = cc[n], ca = cn0 > seg.g_lo ? cn0 : seg.g_lo;
+    const int cb = cn0 + nchunks < seg.g_hi ? cn0 + nchunks : seg.g_hi;
+    bool from_carry = false, to_carry = false;
+    if (nchunks == 0) {
+        if (seg.g_lo != 0) return;  // an empty sequence is settled by the first segment
+    } else {
+        if (cb <= ca) return;       // none of its chunks in this segment
+        from_carry = cn0 < seg.g_lo;
+        to_carry = cn0 + nchunks > seg.g_hi;
+        const int64_t s0 = t0;
+        t0 = s0 + (int64_t)(ca - cn0) * kC;
+        if (to_carry) t1 = s0 + (int64_t)(cb - cn0) * kC;
+        nchunks = cb - ca;
+    }
     int64_t si, sf;
     if (!state_entries(slots, n, !ident && init_state != nullptr, si, sf) && tid == 0)
         atomicOr(status, DEV_ERR_SLOT);
     if (ident) o = nullptr;
-    if (sf < 0 && (o == nullptr || nchunks == 0)) return;  // nothing to store or write
+    const bool store_end = to_carry || sf >= 0;
+    if (!store_end && (o == nullptr || nchunks == 0)) return;  // nothing to store or write
     float *const fpool = ident ? final_ident : final_state;
     const CUtensorMap *const tmv = ident ? &tm_v_zero : &tm_v;
-    const unsigned char *rec0 = records + ((size_t)cc[n] * H + h) * kRecBytes;
+    const unsigned char *rec0 = records + ((size_t)(ca - seg.g_lo) * H + h) * kRecBytes;
     const size_t rec_stride = (size_t)H * kRecBytes;
 
     // copies: issued by lane 0 of the copy warp only, which alone keeps these counts
@@ -661,10 +679,11 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
         if (ident) {
 #pragma unroll
             for (int j = 0; j < kSCols; ++j) S[j] = i_row == j0 + jp + j ? 1.f : 0.f;
-        } else if (si >= 0) {
+        } else if (from_carry || si >= 0) {
+            const float *src = from_carry ? seg.carry_in + st_off : init_state + si * st_entry + st_off;
 #pragma unroll
             for (int q = 0; q < kSCols / 4; ++q) {
-                const float4 x = *reinterpret_cast<const float4 *>(init_state + si * st_entry + st_off + 4 * q);
+                const float4 x = *reinterpret_cast<const float4 *>(src + 4 * q);
                 S[4 * q] = x.x; S[4 * q + 1] = x.y; S[4 * q + 2] = x.z; S[4 * q + 3] = x.w;
             }
         } else {
@@ -831,8 +850,8 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
             (void)mbar_wait_ns(&bar_rec[k & 1], (uint32_t)((k >> 1) & 1), kWaitNs);
         for (int k = v_issued > kVRing ? v_issued - kVRing : 0; k < v_issued; ++k)
             (void)mbar_wait_ns(&bar_v[k % kVRing], (uint32_t)((k / kVRing) & 1), kWaitNs);
-    } else if (state_warp && sf >= 0) {
-        float *dst = fpool + sf * st_entry + st_off;
+    } else if (state_warp && store_end) {
+        float *dst = to_carry ? seg.carry_out + st_off : fpool + sf * st_entry + st_off;
 #pragma unroll
         for (int q = 0; q < kSCols / 4; ++q)
             *reinterpret_cast<float4 *>(dst + 4 * q) = make_float4(S[4 * q], S[4 * q + 1], S[4 * q + 2], S[4 * q + 3]);
@@ -958,6 +977,8 @@ cudaError_t diag_tensor_phases(int pass, int reps, uint32_t *status, cudaStream_
                      : run_tensor_phases<1>(reps, status, stream, tflops);
 }
 
+size_t prefill_split_record_bytes() { return kRecBytes; }
+
 size_t prefill_split_records_bytes(int64_t total_tokens, int num_seqs, int num_heads)
 {
     return (size_t)(total_tokens / kC + num_seqs) * (size_t)num_heads * kRecBytes;
@@ -968,7 +989,7 @@ namespace {
 // The state pass with SV-column value slices (the chunk kernel has run before it).
 template <int SV>
 cudaError_t launch_state_pass(const PrefillProblem &p, const int32_t *cc, const unsigned char *rec,
-                              cudaLaunchConfig_t cfg)
+                              cudaLaunchConfig_t cfg, StateSegment seg)
 {
     using Sh = StateShape<SV>;
     static int dev_state = -1;
@@ -984,7 +1005,7 @@ cudaError_t launch_state_pass(const PrefillProblem &p, const int32_t *cc, const 
         cfg.gridDim = dim3(kD / SV, p.num_heads, p.num_seqs);
         return cudaLaunchKernelEx(&cfg, prefill_state_kernel<SV>, tv, tv, p.cu_seqlens, p.total_tokens, p.num_heads,
                                   cc, rec, p.init_state, o, p.final_state, p.status,
-                                  static_cast<const int32_t *>(p.order), p.slots, INT_MAX, (float *)nullptr);
+                                  static_cast<const int32_t *>(p.order), p.slots, INT_MAX, (float *)nullptr, seg);
     }
     // sequence split: transition pass (R for grid z < nv_max, M above), start states, state pass
     const SeqSplit &s = p.split;
@@ -997,7 +1018,8 @@ cudaError_t launch_state_pass(const PrefillProblem &p, const int32_t *cc, const 
     cfg.gridDim = dim3(kD / SV, p.num_heads, 2 * s.nv_max);
     err = cudaLaunchKernelEx(&cfg, prefill_state_kernel<SV>, tv, tz, (const int32_t *)s.vcu, p.total_tokens,
                              p.num_heads, (const int32_t *)s.vcc, rec, (const float *)nullptr,
-                             (__nv_bfloat16 *)nullptr, s.R, p.status, (const int32_t *)s.vorder, sa, s.nv_max, s.M);
+                             (__nv_bfloat16 *)nullptr, s.R, p.status, (const int32_t *)s.vorder, sa, s.nv_max, s.M,
+                             StateSegment());
     if (err != cudaSuccess) return err;
     if ((err = launch_seqsplit_combine(p)) != cudaSuccess) return err;
     StateSlots sc;
@@ -1008,7 +1030,7 @@ cudaError_t launch_state_pass(const PrefillProblem &p, const int32_t *cc, const 
     cfg.gridDim = dim3(kD / SV, p.num_heads, s.nv_max);
     return cudaLaunchKernelEx(&cfg, prefill_state_kernel<SV>, tv, tv, (const int32_t *)s.vcu, p.total_tokens,
                               p.num_heads, (const int32_t *)s.vcc, rec, (const float *)s.start, o, p.final_state,
-                              p.status, (const int32_t *)s.vorder, sc, INT_MAX, (float *)nullptr);
+                              p.status, (const int32_t *)s.vorder, sc, INT_MAX, (float *)nullptr, StateSegment());
 }
 
 // SMs of the current device (cached per device).
@@ -1049,26 +1071,43 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
     pdl.val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
-    // persistent: two CTAs per SM (or one per item when there are fewer)
-    const int64_t items = chunk_bound * p.num_heads, slots = 2 * (int64_t)sm_count();
-    cfg.gridDim = dim3((unsigned)(items < slots || slots <= 0 ? items : slots));
-    cfg.blockDim = dim3(kChunkThreads);
-    cfg.dynamicSmemBytes = kChunkSmem;
     cfg.stream = p.stream;
     cfg.attrs = &pdl;
     cfg.numAttrs = 1;
-    err = cudaLaunchKernelEx(&cfg, chunk_kernel, tq, tk, tla, p.log_alpha, p.beta, (const int2 *)p.desc,
-                             p.num_heads, (int)chunk_bound, static_cast<unsigned char *>(records), p.status, p.o != nullptr,
-                             p.scalar_gate);
-    if (err != cudaSuccess) return err;
-    if (mid && (err = cudaEventRecord(mid, p.stream)) != cudaSuccess) return err;
-    // 32-column slices while every (sequence, head, slice) of the pass fits in one wave of
-    // SMs (their chain per chunk is shorter); 64-column slices beyond that, and for the
+    // 32-column state slices while every (sequence, head, slice) of the pass fits in one wave
+    // of SMs (their chain per chunk is shorter); 64-column slices beyond that, and for the
     // sequence split, whose transition pass is sized for them
     const unsigned char *rec = static_cast<const unsigned char *>(records);
     const int64_t slices32 = (int64_t)p.num_seqs * p.num_heads * (kD / 32);
-    if (p.split.lseg == 0 && slices32 <= sm_count()) return launch_state_pass<32>(p, cc, rec, cfg);
-    return launch_state_pass<64>(p, cc, rec, cfg);
+    const bool narrow = p.split.lseg == 0 && slices32 <= sm_count();
+    // the records cover seg packed chunks at a time: all of them, or (bounded workspace)
+    // segments of p.seg_chunks chunks walked one after the other
+    const bool segmented = p.seg_chunks > 0 && p.seg_chunks < chunk_bound;
+    const int seg = segmented ? p.seg_chunks : (int)chunk_bound;
+    const size_t carry_entry = (size_t)p.num_heads * kD * kD;
+    for (int g_lo = 0, k = 0; g_lo < chunk_bound; g_lo += seg, ++k) {
+        const int g_hi = g_lo + seg < chunk_bound ? g_lo + seg : (int)chunk_bound;
+        // persistent: two CTAs per SM (or one per item when there are fewer)
+        const int64_t items = (int64_t)(g_hi - g_lo) * p.num_heads, slots = 2 * (int64_t)sm_count();
+        cfg.gridDim = dim3((unsigned)(items < slots || slots <= 0 ? items : slots));
+        cfg.blockDim = dim3(kChunkThreads);
+        cfg.dynamicSmemBytes = kChunkSmem;
+        err = cudaLaunchKernelEx(&cfg, chunk_kernel, tq, tk, tla, p.log_alpha, p.beta, (const int2 *)p.desc,
+                                 p.num_heads, g_lo, g_hi - g_lo, static_cast<unsigned char *>(records), p.status,
+                                 p.o != nullptr, p.scalar_gate);
+        if (err != cudaSuccess) return err;
+        if (mid && k == 0 && (err = cudaEventRecord(mid, p.stream)) != cudaSuccess) return err;
+        StateSegment sg;
+        if (segmented) {
+            sg.g_lo = g_lo;
+            sg.g_hi = g_hi;
+            sg.carry_in = k > 0 ? p.carry + ((k - 1) & 1) * carry_entry : nullptr;
+            sg.carry_out = p.carry + (k & 1) * carry_entry;
+        }
+        err = narrow ? launch_state_pass<32>(p, cc, rec, cfg, sg) : launch_state_pass<64>(p, cc, rec, cfg, sg);
+        if (err != cudaSuccess) return err;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace kda

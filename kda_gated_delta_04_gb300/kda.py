@@ -38,6 +38,8 @@ _DECODE_ARGS = [_VP, _VP, _VP, _VP, _VP, _c.c_int32, _c.c_int32, _c.c_int32, _c.
 EXPORTS = {
     "kda_prefill_workspace_size": (_c.c_size_t, [_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
                                                  _c.c_int32, _c.c_int]),
+    "kda_prefill_workspace_size_segmented": (_c.c_size_t, [_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
+                                                           _c.c_int32, _c.c_int, _c.c_int64]),
     "kda_prefill": (_c.c_int, _PREFILL_ARGS),
     "kda_decode_step": (_c.c_int, _DECODE_ARGS),
     "kda_read_device_status": (_c.c_int, [_VP, _VP]),
@@ -86,6 +88,12 @@ def lib():
 # ------------------------------------------------------------------ raw C entry points
 def kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, d_k, d_v, dtype):
     return lib().kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, d_k, d_v, dtype)
+
+
+def kda_prefill_workspace_size_segmented(num_seqs, total_tokens, num_heads, d_k, d_v, dtype,
+                                         segment_chunks):
+    return lib().kda_prefill_workspace_size_segmented(num_seqs, total_tokens, num_heads, d_k, d_v,
+                                                      dtype, segment_chunks)
 
 
 def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
@@ -238,6 +246,17 @@ def workspace_for(num_seqs, total_tokens, num_heads, d, dtype_code, device):
     torch = _torch()
     nbytes = kda_prefill_workspace_size(num_seqs, total_tokens, num_heads, d, d, dtype_code)
     # every byte the kernels read is written first in the same call
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def segmented_workspace_for(num_seqs, total_tokens, num_heads, d, dtype_code, device, segment_chunks):
+    """A workspace whose per-chunk records cover at most `segment_chunks` packed chunks: the
+    two-kernel prefill then runs segment by segment (kda_prefill_workspace_size_segmented)."""
+    torch = _torch()
+    nbytes = kda_prefill_workspace_size_segmented(num_seqs, total_tokens, num_heads, d, d, dtype_code,
+                                                  segment_chunks)
+    if nbytes == 0:
+        raise KdaError(KDA_ERR_UNSUPPORTED, "kda_prefill_workspace_size_segmented")
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 

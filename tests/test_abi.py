@@ -53,6 +53,29 @@ def test_workspace_size(kda):
     assert kda.kda_prefill_workspace_size(-1, 0, 1, 64, 64, 1) == 0
 
 
+def test_segmented_workspace_size(kda):
+    """Bounded records: a fixed part (schedule, chunk numbering, descriptors and two carried
+    [H, 128, 128] fp32 states) plus one 74,240-byte record per (chunk, head) of a segment,
+    never more than the full two-kernel workspace without the sequence split."""
+    H, T, N = 32, 65536, 1
+    one = kda.kda_prefill_workspace_size_segmented(N, T, H, 128, 128, 0, 1)
+    two = kda.kda_prefill_workspace_size_segmented(N, T, H, 128, 128, 0, 2)
+    assert one > 2 * H * 128 * 128 * 4 and one % 256 == 0
+    assert two - one == H * 74240
+    bound = T // 64 + N
+    full_seg = kda.kda_prefill_workspace_size_segmented(N, T, H, 128, 128, 0, bound)
+    assert kda.kda_prefill_workspace_size_segmented(N, T, H, 128, 128, 0, 10 * bound) == full_seg
+    assert full_seg - one == (bound - 1) * H * 74240
+    # the records of every chunk, as in the full workspace (this shape has no sequence split),
+    # plus the two carried states
+    assert full_seg - kda.kda_prefill_workspace_size(N, T, H, 128, 128, 0) == 2 * H * 128 * 128 * 4
+    for bad in (dict(seg=0), dict(dtype=1), dict(d=64), dict(T=0), dict(H=0)):
+        a = dict(N=N, T=T, H=H, d=128, dtype=0, seg=4)
+        a.update(bad)
+        assert kda.kda_prefill_workspace_size_segmented(a["N"], a["T"], a["H"], a["d"], a["d"], a["dtype"],
+                                                        a["seg"]) == 0
+
+
 FAKE = 1 << 20  # 16-byte aligned dummy address; never dereferenced (rejected first)
 
 

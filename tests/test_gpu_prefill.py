@@ -586,6 +586,53 @@ def test_more_items_than_resident_chunk_ctas(scalar, qkn):
     assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, "bf16", w.name)
 
 
+@pytest.mark.parametrize("seg_chunks", [1, 3, 17])
+def test_bounded_records_run_in_segments(seg_chunks):
+    """A workspace whose records cover only `seg_chunks` packed chunks: the chunk and state
+    kernels run segment by segment, each sequence cut at a boundary carrying its state in
+    the workspace.  Ragged sequences (a zero-length one, one shorter than a chunk, several
+    spanning many segments) from initial states, two heads: o and the final states bit for
+    bit those of the full workspace without the sequence split, and within the bar of the
+    oracle; the final state may alias the initial state."""
+    w = PrefillWorkload(f"segmented_{seg_chunks}", 170 + seg_chunks, 2, 128, "bf16",
+                        (300, 0, 1000, 40, 129, 700), 6, init_state=True)
+    inp = synth.prefill_inputs(w)
+    d = to_device(inp)
+    T, H = inp["q"].shape[:2]
+    o_ref_gpu, fs_ref_gpu = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
+                                        d["init_state"], check_status=True, seq_split=False)
+    ws = kda.segmented_workspace_for(6, T, H, 128, kda.KDA_DTYPE_BF16, "cuda", seg_chunks)
+    assert ws.numel() < kda.kda_prefill_workspace_size(6, T, H, 128, 128, kda.KDA_DTYPE_BF16)
+    o, fs = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"],
+                        workspace=ws, check_status=True)
+    fs_inplace = d["init_state"].clone()
+    o2, _ = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], fs_inplace,
+                        final_state=fs_inplace, workspace=ws, check_status=True)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(synth.to_f64(o), synth.to_f64(o_ref_gpu))
+    np.testing.assert_array_equal(synth.to_f64(fs), synth.to_f64(fs_ref_gpu))
+    np.testing.assert_array_equal(synth.to_f64(o2), synth.to_f64(o_ref_gpu))
+    np.testing.assert_array_equal(synth.to_f64(fs_inplace), synth.to_f64(fs_ref_gpu))
+    o_ref, fs_ref = oracle_prefill(inp)
+    assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, "bf16", w.name)
+
+
+def test_bounded_records_at_full_size():
+    """T = 65536, H = 32 from initial states with the records of 128 chunks at a time (8
+    segments, 304 MB of records instead of 2.4 GB): bit for bit the full workspace."""
+    w = synth.PREFILL_64K
+    inp = synth.prefill_inputs(w)
+    d = to_device(inp)
+    T, H = inp["q"].shape[:2]
+    o_full, fs_full = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
+                                  d["init_state"], check_status=True, seq_split=False)
+    ws = kda.segmented_workspace_for(1, T, H, 128, kda.KDA_DTYPE_BF16, "cuda", 128)
+    o, fs = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"],
+                        workspace=ws, check_status=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o, o_full) and torch.equal(fs, fs_full)
+
+
 def test_split_prefill_into_a_pool_then_paged_decode():
     """A long prompt with few heads goes through the sequence-split pass straight into a
     state pool; paged decode continues from it within the bar of the oracle."""
