@@ -101,15 +101,25 @@ def executed_tensor_flops(T, H, d, C=64):
     return chunks * H * (chunk_groups + state_groups)
 
 
-def prefill_roofline(T, H, d, N, with_init, call_ms, stage_ms, peaks, traffic_key):
+PATH_NAMES = {0: "cuda_core", 1: "fused", 2: "two_kernel", 3: "seq_split", 4: "segmented", 5: "streamed"}
+PATH_STREAMED = 5
+
+
+def prefill_roofline(T, H, d, N, with_init, call_ms, stage_ms, peaks, traffic_key, path):
     """Roofline object of one prefill workload: the dominant (longest) kernel against its
     share of the algorithmic bytes, and the whole call against all of them.  call_ms: mean
-    event time of one kda_prefill; stage_ms: mean event times of schedule, chunk and state
-    kernel from kda_prefill_events."""
+    event time of one kda_prefill; stage_ms: mean event times of the stages kda_prefill_events
+    marks (schedule kernel, chunk kernel, state pass; on the streamed path the schedule
+    kernel and the streamed kernel, which moves every algorithmic byte, the third stage
+    empty).  path: kda_prefill_path of the call."""
     alg_bytes = prefill_algorithmic_bytes(T, H, d, N, 2, with_init)
     achieved = alg_bytes / (call_ms / 1e3) / 1e9
-    names = ("prefill_prep_kernel", "prefill_chunk_kernel", "prefill_state_kernel")
-    stage_bytes = prefill_stage_bytes(T, H, d, N, 2, with_init)
+    if path == PATH_STREAMED:
+        names = ("prefill_prep_kernel", "prefill_stream_kernel")
+        stage_bytes = {"prefill_stream_kernel": alg_bytes}
+    else:
+        names = ("prefill_prep_kernel", "prefill_chunk_kernel", "prefill_state_kernel")
+        stage_bytes = prefill_stage_bytes(T, H, d, N, 2, with_init)
     kernels = {}
     for name, ms in zip(names, stage_ms):
         kb = stage_bytes.get(name)
@@ -125,6 +135,7 @@ def prefill_roofline(T, H, d, N, with_init, call_ms, stage_ms, peaks, traffic_ke
             "traffic": profiled_traffic(dom + "_" + traffic_key),
             "peak_source": peaks["source"],
             "algorithmic_bytes_per_launch": stage_bytes[dom],
+            "kernel_path": PATH_NAMES.get(path, str(path)),
             "kernels": kernels,
             "path": {"achieved": achieved, "frac": achieved / peaks["hbm_gbs"],
                      "algorithmic_bytes_per_launch": alg_bytes,
@@ -254,15 +265,22 @@ class _Gpu:
         self.fs = torch.empty((1, self.H, self.d, self.d), dtype=torch.float32, device=self.dev)
         self.ws = kda.workspace_for(1, self.T, self.H, self.d, kda.KDA_DTYPE_BF16, self.dev)
 
-    def prefill_call(self, events=None):
+    def prefill_path(self, flags=0):
+        return self.kda.kda_prefill_path(1, self.T, self.H, self.d, self.d, self.kda.KDA_DTYPE_BF16,
+                                         self.ws.numel(), flags)
+
+    def prefill_call(self, events=None, flags=0):
         """One kda_prefill through the C ABI; with `events` (four CUDA events) the
-        kda_prefill_events variant, which also marks the stages."""
+        kda_prefill_events variant, which also marks the stages; with `flags` kda_prefill_ex."""
         kda, x = self.kda, self.x
         args = (x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), x["log_alpha"].data_ptr(),
                 x["beta"].data_ptr(), x["cu_seqlens"].data_ptr(), 1, self.T, self.H, self.d, self.d,
                 kda.KDA_DTYPE_BF16, None, self.o.data_ptr(), self.fs.data_ptr(), self.ws.data_ptr(),
                 self.ws.numel(), self.sh)
-        st = kda.kda_prefill(*args) if events is None else kda.kda_prefill_events(*args, events)
+        if flags:
+            st = kda.kda_prefill_ex(*args, flags)
+        else:
+            st = kda.kda_prefill(*args) if events is None else kda.kda_prefill_events(*args, events)
         if st != kda.KDA_OK:
             raise kda.KdaError(st, "kda_prefill")
 
@@ -303,6 +321,22 @@ class _Gpu:
         stages = [[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev]
         return whole, stages
 
+    def time_prefill_flags(self, steps, warmup, flags):
+        """Per-step event times (ms) of kda_prefill_ex with `flags`, L2 flushed before each."""
+        torch = self.torch
+        for _ in range(warmup):
+            self.flush.zero_()
+            self.prefill_call(flags=flags)
+        torch.cuda.synchronize()
+        outer = [(self.event(), self.event()) for _ in range(steps)]
+        for a, b in outer:
+            self.flush.zero_()
+            a.record(self.stream)
+            self.prefill_call(flags=flags)
+            b.record(self.stream)
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) for a, b in outer]
+
     def time_prefill_e2e(self, steps, warmup):
         """Host-to-host through kda_prefill_host: pinned inputs in, o and the final state out,
         the copies of later segments overlapped with the prefill of earlier ones."""
@@ -321,7 +355,12 @@ class _Gpu:
         nseg = kda.kda_prefill_host_segments(cu_host.data_ptr(), 1, self.T, bounds.data_ptr(), 64)
         if nseg < 1:
             raise kda.KdaError(kda.KDA_ERR_INVALID_ARG, "kda_prefill_host_segments")
-        self.e2e_launches = 4 * nseg  # per segment: schedule, chunk, state kernel and the error word
+        # per segment: the schedule kernel, the streamed kernel (or the chunk kernel and the
+        # state pass) and the error word
+        seg_path = kda.kda_prefill_path(1, max(1, self.T // nseg), self.H, self.d, self.d, kda.KDA_DTYPE_BF16,
+                                        kda.kda_prefill_workspace_size(1, max(1, self.T // nseg), self.H,
+                                                                       self.d, self.d, kda.KDA_DTYPE_BF16), 0)
+        self.e2e_launches = (3 if seg_path == PATH_STREAMED else 4) * nseg
 
         def step():
             st = kda.kda_prefill_host(pin["q"].data_ptr(), pin["k"].data_ptr(), pin["v"].data_ptr(),
@@ -405,6 +444,7 @@ class _Gpu:
              "o": torch.empty((T, H, d), dtype=torch.bfloat16, device=self.dev),
              "fs": torch.empty((N, H, d, d), dtype=torch.float32, device=self.dev),
              "ws": kda.workspace_for(N, T, H, d, kda.KDA_DTYPE_BF16, self.dev)}
+        c["path"] = kda.kda_prefill_path(N, T, H, d, d, kda.KDA_DTYPE_BF16, c["ws"].numel(), 0)
         return c
 
     def case_call(self, c, events=None, ws=None):
@@ -547,10 +587,14 @@ def run_gpu(args):
     with clocks:
         if do_prefill:
             step_ms, stage_ms = g.time_prefill(args.steps, args.warmup, barrier)
+            prefill_path = g.prefill_path()
+            # the same call with the chunk work and the state walk in one launch
+            stream_ms = g.time_prefill_flags(args.steps, args.warmup, g.kda.KDA_FLAG_STREAM)
             e2e_ms = g.time_prefill_e2e(args.steps, args.warmup)
             # the prefill kernels' tensor-core product groups on their own (resident operands)
             phase_tflops = {name: g.kda.diag_tensor_phases(i, 2000, g.ws)
-                            for i, name in enumerate(("chunk_kernel_products", "state_kernel_products"))}
+                            for i, name in enumerate(("chunk_kernel_products", "state_kernel_products",
+                                                      "stream_walk_products"))}
         for name in do_cases:
             # one workload on the device at a time (the varlen pack holds about 20 GB)
             c = g.setup_case(case_ws[name][0])
@@ -576,14 +620,20 @@ def run_gpu(args):
         T, H, d = g.T, g.H, g.d
         # per kernel: mean event time (max over ranks) and its share of the algorithmic bytes
         stage_mean = [reduce_max(sum(s[i] for s in stage_ms)) / args.steps for i in range(3)]
-        roof = prefill_roofline(T, H, d, 1, False, mean_step_ms, stage_mean, peaks, "4k")
+        roof = prefill_roofline(T, H, d, 1, False, mean_step_ms, stage_mean, peaks, "4k", prefill_path)
         roof["path"]["executed_tensor_flops_per_call"] = executed_tensor_flops(T, H, d)
         roof["gemm_phases"] = dict(
             {name: {"achieved": tf, "unit": "TFLOP/s", "peak": peaks["bf16_tflops"],
                     "frac": tf / peaks["bf16_tflops"]} for name, tf in phase_tflops.items()},
             note="kda_diag_tensor_phases: each kernel's product groups issued back to back by "
                  "its own issue routines on operands resident in shared memory (executed "
-                 "FLOPs, bf16/fp16 inputs, fp32 accumulate), 2000 repetitions per CTA")
+                 "FLOPs, bf16/fp16 inputs, fp32 accumulate), 2000 repetitions per CTA: the "
+                 "chunk work's groups (both paths), the state kernel's groups (64-column "
+                 "slice, two-kernel path) and the streamed kernel's walk (whole head)")
+        sm_ms = reduce_max(sum(stream_ms)) / args.steps
+        roof["streamed_form"] = {
+            "ms_per_call": sm_ms, "value": aggregate_rate(T, world, 1, sm_ms),
+            "note": "the same call with KDA_FLAG_STREAM: chunk work and state walk in one launch"}
         roof["note"] = ("kernel durations from the four CUDA events kda_prefill_events records on "
                         "the launching stream around its kernels (a separate timed pass); the "
                         "dominant (longest) kernel is measured against its share of the path's "
@@ -605,7 +655,8 @@ def run_gpu(args):
                             "those of kda_prefill)",
                     "link_gbs": (g.h2d + g.d2h) / (e2e_total / args.steps / 1e3) / 1e9,
                     "gpu_launches_per_step": g.e2e_launches},
-            "gpu_launches": 3 * args.steps,  # schedule, chunk and state kernel per step
+            # schedule kernel and streamed kernel (or chunk kernel and state pass) per step
+            "gpu_launches": (2 if prefill_path == PATH_STREAMED else 3) * args.steps,
         })
     line["clocks"] = clocks.summary()
     for name, (c, (call_ms, stages)) in case_ms.items():
@@ -617,9 +668,9 @@ def run_gpu(args):
                "num_seqs": N, "total_tokens": T, "num_heads": H, "d_k": d, "d_v": d,
                "init_state": c["with_init"],
                "l2": "inputs larger than L2 (no flush)",
-               "gpu_launches": 3 * len(call_ms),
+               "gpu_launches": (2 if c["path"] == PATH_STREAMED else 3) * len(call_ms),
                "roofline": prefill_roofline(T, H, d, N, c["with_init"], ms,
-                                            stage_mean, peaks, case_ws[name][1])}
+                                            stage_mean, peaks, case_ws[name][1], c["path"])}
         if "bounded" in c:
             bms, bws = c["bounded"]
             bms = reduce_max(bms)
@@ -628,7 +679,7 @@ def run_gpu(args):
                 "value": aggregate_rate(T, world, 1, bms), "ms_per_call": bms, "steps": CASE_STEPS,
                 "note": "kda_prefill with a workspace from kda_prefill_workspace_size_segmented: the chunk and "
                         "state kernels run over segments of that many packed chunks (results bit for bit those "
-                        "of the full workspace without the sequence split)"}
+                        "of the full workspace)"}
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             blk["cpu_baseline"] = cpu_baseline_case(w, c["cpu_sample"])
         line[name] = blk

@@ -107,6 +107,30 @@ size_t kda_prefill_workspace_size_segmented(int32_t num_seqs, int64_t total_toke
                                             int64_t segment_chunks);
 
 /*
+ * The kernels a kda_prefill_ex call with these arguments runs (the path it takes).
+ *  KDA_PATH_CUDA_CORE  fp32 I/O or d = 64: the exact CUDA-core chunk kernel
+ *  KDA_PATH_FUSED      bf16, d = 128, workspace below the bounded-records size: one
+ *                      tensor-core kernel per (sequence, head, value slice)
+ *  KDA_PATH_TWO_KERNEL the chunk kernel, then the state pass
+ *  KDA_PATH_SEQ_SPLIT  the chunk kernel, then the sequence-split state pass
+ *  KDA_PATH_SEGMENTED  the chunk kernel and the state pass over segments of records
+ *  KDA_PATH_STREAMED   chunk work and state walk in one launch (KDA_FLAG_STREAM)
+ * Host arithmetic plus one device-attribute query (the SM count of the current
+ * device); returns a negative kda_status_t for arguments kda_prefill_ex rejects on
+ * the host.  Each path also runs the schedule kernel first.
+ */
+typedef enum {
+    KDA_PATH_CUDA_CORE = 0,
+    KDA_PATH_FUSED = 1,
+    KDA_PATH_TWO_KERNEL = 2,
+    KDA_PATH_SEQ_SPLIT = 3,
+    KDA_PATH_SEGMENTED = 4,
+    KDA_PATH_STREAMED = 5
+} kda_prefill_path_t;
+int32_t kda_prefill_path(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int32_t d_k,
+                         int32_t d_v, kda_dtype_t dtype, size_t workspace_bytes, uint32_t flags);
+
+/*
  * Chunkwise prefill over packed variable-length sequences ("K3 attention,
  * three-piece set": chunkwise-parallel form with WY representation and UT
  * transform; "From 124M to 2.8T", chapter 3: parallel inside a chunk, serial
@@ -129,7 +153,9 @@ size_t kda_prefill_workspace_size_segmented(int32_t num_seqs, int64_t total_toke
  *  workspace   device buffer owned by the caller, 256-byte aligned, reused by every
  *              call.  With kda_prefill_workspace_size(...) bytes or more the bf16,
  *              d = 128 prefill runs as two kernels (chunk-local products for all
- *              chunks at once, then the serial state pass); with less, but at least
+ *              chunks at once, then the serial state pass; with KDA_FLAG_STREAM and
+ *              few (sequence, head) units, both in one launch; kda_prefill_path tells
+ *              which); with less, but at least
  *              kda_prefill_workspace_size_segmented(..., 1) bytes, as the same two
  *              kernels over segments of chunks (bounded records, identical results);
  *              with at least KDA_PREFILL_MIN_WORKSPACE(num_seqs) bytes as one fused
@@ -220,6 +246,18 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
  *                        state, and the segments then run at once.  The results agree
  *                        with the unsplit pass to within rounding, not bit for bit. */
 #define KDA_FLAG_NO_SEQ_SPLIT 4u
+/*  KDA_FLAG_STREAM        run the chunk work and the state pass in one launch: when a
+ *                        bf16 d = 128 problem has at most 64 (sequence, head) units, no
+ *                        sequence split and a workspace that holds every record, a few
+ *                        CTAs walk the state of one unit each while the others do the
+ *                        chunk work, and each record is handed over through a ready flag
+ *                        in the workspace as soon as its stores are complete (otherwise
+ *                        the flag changes nothing).  The two forms agree to within
+ *                        rounding, not bit for bit (the streamed walk forms its products
+ *                        transposed).  Off by default: on one GB300 the walk, one chunk
+ *                        after another, is slower than the separate state pass (T = 4096,
+ *                        H = 32: 0.185 against 0.161 ms per call). */
+#define KDA_FLAG_STREAM 8u
 
 /* kda_prefill with options (flags above); flags = 0 is kda_prefill. */
 kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -398,8 +436,12 @@ int32_t kda_prefill_host_segments(const int32_t *cu_seqlens, int32_t num_seqs, i
  * prefill's GEMM phases, apart from the work between them.
  *  pass  0: the chunk kernel's groups of one (chunk, head) item (k-k and q-k, W, P2, the
  *           three-term P, N, Q''), 9,961,472 executed FLOP per repetition, two CTAs per SM;
- *        1: the state kernel's chain and output groups of one chunk and 32-column value
- *           slice (P V, N S, P2 V, Q' S), 2,359,296 FLOP per repetition, one CTA per SM
+ *        1: the state kernel's chain and output groups of one chunk and 64-column value
+ *           slice (P V, N S, P2 V, Q' S), 4,718,592 FLOP per repetition, one CTA per SM,
+ *           each group issued by a thread of its own warp;
+ *        2: the streamed kernel's walk group of one chunk and a whole head (the same four
+ *           products transposed, S^T read from TMEM, as one N = 192 group), 9,437,184 FLOP
+ *           per repetition, one CTA per SM, one issuing thread
  *  reps      repetitions per CTA, 1 .. 2^20
  *  workspace 256-byte aligned device memory of at least 4 bytes (status word, cleared)
  *  tflops    receives the executed TFLOP/s over the whole GPU (CUDA events on `stream`)

@@ -77,6 +77,10 @@ struct PrefillProblem {
     // carry (two [num_heads, d, d] fp32 buffers, alternating by segment).  0: unsegmented.
     int seg_chunks = 0;
     float *carry = nullptr;
+    // one ready flag per chunk-head record ([chunk_bound, num_heads]) and one item counter
+    // after them, zeroed by the schedule kernel: the streamed prefill publishes each record
+    // through its flag.  Null: no streaming.
+    int *flags = nullptr;
     cudaStream_t stream;
 };
 
@@ -115,9 +119,16 @@ cudaError_t launch_prefill_tc(const PrefillProblem &p);
 size_t prefill_split_records_bytes(int64_t total_tokens, int num_seqs, int num_heads);
 // bytes of one (chunk, head) record of the two-kernel path
 size_t prefill_split_record_bytes();
-// `mid` (may be null) is recorded on p.stream between the chunk kernel and the state kernel.
+// `mid` (may be null) is recorded on p.stream between the chunk kernel and the state kernel
+// (after the streamed kernel, when that one runs).
 cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records,
                                  cudaEvent_t mid = nullptr);
+// Whether launch_prefill_split tries the streamed kernel (chunk work and state walk in one
+// grid) for p: ready flags given, no sequence split, no segments, few (sequence, head) units.
+bool prefill_stream_eligible(const PrefillProblem &p);
+// Whether `units` (sequence, head) units are few enough for the streamed kernel on the
+// current device (one walker CTA each, beside at least one worker CTA per SM).
+bool prefill_stream_fits(int64_t units);
 cudaError_t launch_decode(const DecodeProblem &p);
 // Measurement only: the tensor-core product groups of the chunk kernel (pass 0) or the state
 // kernel (pass 1) back to back on resident operands; synchronises `stream`; executed TFLOP/s.

@@ -33,7 +33,9 @@ kda_status_t check_device()
 size_t round_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace layout: status header | sequence order | first chunk of each sequence
-// | per chunk-head records (the last two only for the two-kernel tensor-core path).
+// | per-chunk descriptors | per chunk-head ready flags | per chunk-head records (the last
+// four only for the two-kernel tensor-core path; the bounded-records layout carries two
+// states per head instead of the flags, and records for a segment of chunks).
 size_t ws_order_bytes(int32_t num_seqs) { return round_up((size_t)num_seqs * sizeof(int32_t) + 1, 256); }
 size_t ws_min_bytes(int32_t num_seqs) { return kda::kWorkspaceHeader + ws_order_bytes(num_seqs); }
 size_t ws_cc_bytes(int32_t num_seqs) { return round_up(((size_t)num_seqs + 1) * sizeof(int32_t), 256); }
@@ -51,10 +53,16 @@ bool split_shape(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int3
            total_tokens <= 0x7fffffffll &&
            (total_tokens / KDA_CHUNK + num_seqs) * (int64_t)num_heads <= 0x7fffffffll;
 }
-// the two-kernel path: schedule, chunk numbering and records
+// one ready flag (int32) per chunk-head record and an item counter, for the streamed prefill
+size_t ws_flags_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
+{
+    return round_up(((size_t)chunk_bound(num_seqs, total_tokens) * (size_t)num_heads + 1) * sizeof(int32_t), 256);
+}
+// the two-kernel path: schedule, chunk numbering, descriptors, ready flags and records
 size_t ws_records_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
 {
     return ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) + ws_desc_bytes(num_seqs, total_tokens) +
+           ws_flags_bytes(num_seqs, total_tokens, num_heads) +
            kda::prefill_split_records_bytes(total_tokens, num_seqs, num_heads);
 }
 // ... plus the sequence-split state pass where the shape calls for it
@@ -72,6 +80,28 @@ size_t ws_segmented_fixed(int32_t num_seqs, int64_t total_tokens, int32_t num_he
            ws_carry_bytes(num_heads);
 }
 
+// The path kda_prefill_ex takes for a call with these arguments (kda_prefill_path_t): the
+// decisions of prefill_impl below, in the same order.
+int32_t path_for(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                 kda_dtype_t dtype, size_t workspace_bytes, uint32_t flags)
+{
+    const bool split_ok = split_shape(num_seqs, total_tokens, num_heads, d_k, d_v, dtype);
+    const bool full = split_ok && workspace_bytes >= ws_records_bytes(num_seqs, total_tokens, num_heads);
+    if (full) {
+        if (!(flags & KDA_FLAG_NO_SEQ_SPLIT) && workspace_bytes >= ws_split_bytes(num_seqs, total_tokens, num_heads) &&
+            kda::seqsplit_lseg(num_seqs, total_tokens, num_heads) > 0)
+            return KDA_PATH_SEQ_SPLIT;
+        if ((flags & KDA_FLAG_STREAM) && kda::prefill_stream_fits((int64_t)num_seqs * num_heads))
+            return KDA_PATH_STREAMED;
+        return KDA_PATH_TWO_KERNEL;
+    }
+    const size_t rec_chunk = (size_t)num_heads * kda::prefill_split_record_bytes();
+    if (split_ok && workspace_bytes >= ws_segmented_fixed(num_seqs, total_tokens, num_heads) + rec_chunk)
+        return KDA_PATH_SEGMENTED;
+    const bool tc = dtype == KDA_DTYPE_BF16 && d_k == 128 && total_tokens > 0 && total_tokens <= 0x7fffffffll;
+    return tc ? KDA_PATH_FUSED : KDA_PATH_CUDA_CORE;
+}
+
 kda_status_t check_shape(int32_t d_k, int32_t d_v, kda_dtype_t dtype)
 {
     if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
@@ -83,7 +113,8 @@ kda_status_t check_shape(int32_t d_k, int32_t d_v, kda_dtype_t dtype)
 }  // namespace
 
 // every option bit of the _ex / _slots calls
-constexpr uint32_t kKnownFlags = KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM | KDA_FLAG_NO_SEQ_SPLIT;
+constexpr uint32_t kKnownFlags =
+    KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM | KDA_FLAG_NO_SEQ_SPLIT | KDA_FLAG_STREAM;
 
 extern "C" {
 
@@ -106,6 +137,19 @@ size_t kda_prefill_workspace_size_segmented(int32_t num_seqs, int64_t total_toke
     const int64_t seg = segment_chunks < bound ? segment_chunks : bound;
     return ws_segmented_fixed(num_seqs, total_tokens, num_heads) +
            (size_t)seg * (size_t)num_heads * kda::prefill_split_record_bytes();
+}
+
+int32_t kda_prefill_path(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int32_t d_k,
+                         int32_t d_v, kda_dtype_t dtype, size_t workspace_bytes, uint32_t flags)
+{
+    if (flags & ~kKnownFlags) return -(int32_t)KDA_ERR_INVALID_ARG;
+    const kda_status_t st = check_shape(d_k, d_v, dtype);
+    if (st != KDA_OK) return -(int32_t)st;
+    if (num_seqs < 0 || total_tokens < 0 || num_heads <= 0 || (num_seqs == 0 && total_tokens != 0))
+        return -(int32_t)KDA_ERR_INVALID_ARG;
+    if (num_seqs > 65535 || num_heads > 65535) return -(int32_t)KDA_ERR_UNSUPPORTED;
+    if (workspace_bytes < ws_min_bytes(num_seqs)) return -(int32_t)KDA_ERR_INVALID_ARG;
+    return path_for(num_seqs, total_tokens, num_heads, d_k, d_v, dtype, workspace_bytes, flags);
 }
 
 namespace {
@@ -170,7 +214,8 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     p.chunk_bound = split ? (int)chunk_bound(num_seqs, total_tokens) : 0;
     const size_t after_desc = ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) + ws_desc_bytes(num_seqs, total_tokens);
     if (full) {
-        p.records = ws + after_desc;
+        if (flags & KDA_FLAG_STREAM) p.flags = reinterpret_cast<int *>(ws + after_desc);
+        p.records = ws + after_desc + ws_flags_bytes(num_seqs, total_tokens, num_heads);
     } else if (segmented) {
         p.carry = reinterpret_cast<float *>(ws + after_desc);
         p.records = ws + seg_fixed;

@@ -39,10 +39,11 @@ constexpr int kPrepStaged = 4096;  // sequences whose boundaries and chunk offse
 
 __global__ void prefill_prep_kernel(const int32_t *__restrict__ cu, int num_seqs, int64_t total,
                                     uint32_t *status, int32_t *order, int32_t *cc, int2 *desc,
-                                    int chunk_bound)
+                                    int chunk_bound, int *flags, int64_t num_flags)
 {
     // the chunk kernel may be scheduled now; it waits for this kernel's results itself
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    for (int64_t e = threadIdx.x; e < num_flags; e += blockDim.x) flags[e] = 0;  // no record published yet
     __shared__ int bad;
     // up to kPrepStaged sequences: cu (clamped as seq_range clamps it) and the chunk offsets
     // cc are kept here, so the sort and the descriptor search read no global memory
@@ -373,8 +374,11 @@ cudaError_t launch_simt(const PrefillProblem &p)
 
 cudaError_t launch_prefill_prep(const PrefillProblem &p)
 {
+    // the ready flag of every chunk-head record and, after them, the streamed kernel's claim counter
+    const int64_t num_flags = p.flags ? (int64_t)p.chunk_bound * p.num_heads + 1 : 0;
     prefill_prep_kernel<<<1, 1024, 0, p.stream>>>(p.cu_seqlens, p.num_seqs, p.total_tokens,
-                                                  p.status, p.order, p.cc, p.desc, p.chunk_bound);
+                                                  p.status, p.order, p.cc, p.desc, p.chunk_bound,
+                                                  p.flags, num_flags);
     return cudaGetLastError();
 }
 

@@ -302,14 +302,23 @@ __device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, un
     }
 }
 
+// The chunk work: items it0, it0 + stride, ... of the seg_chunks x H (chunk, head) items
+// over the packed chunks g_base .. g_base + seg_chunks - 1, heads fastest.  Run by the
+// chunk kernel (chunks last to first) and by the worker CTAs of the streamed kernel
+// (STREAM: chunks first to last, each record published by a release store of its flag,
+// flags[g * H + h] = 1, once its bulk stores are complete).  Items past the last packed
+// chunk (the chunk count is an upper bound) are skipped.  Records are indexed from g_base.
+// With STREAM the items are not strided but claimed in order from the counter *claim (one
+// item ahead of the one in work), so the items taken are always the earliest not yet taken,
+// whichever CTAs are resident.
 // NORM: q and k arrive raw and are L2-normalised here (KDA_FLAG_QK_L2NORM).
-template <bool NORM>
-__global__ void __launch_bounds__(kChunkThreads, 2)
-prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                     const __grid_constant__ CUtensorMap tm_la, const float *__restrict__ log_alpha,
-                     const float *__restrict__ beta,
-                     const int2 *__restrict__ desc, int H, int g_base, int seg_chunks,
-                     unsigned char *__restrict__ records, uint32_t *status, bool with_o, bool scalar_gate)
+template <bool NORM, bool STREAM>
+__device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
+                                            const CUtensorMap &tm_la, const float *__restrict__ log_alpha,
+                                            const float *__restrict__ beta, const int2 *__restrict__ desc, int H,
+                                            int g_base, int seg_chunks, unsigned char *__restrict__ records,
+                                            uint32_t *status, bool with_o, bool scalar_gate, int it0, int stride,
+                                            int *flags, int *claim)
 {
     using L = ChunkLayout;
     constexpr int NT = kChunkCompute;  // the compute threads' mappings are over 256 threads
@@ -318,35 +327,35 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     __shared__ uint32_t tmem_holder;
     __shared__ __align__(16) float s_beta[kC];
     __shared__ float s_rn[2 * kC];  // reciprocal k, q row norms (NORM)
+    __shared__ int s_claim[2];      // STREAM: the item in work and the next one claimed
 
-    // launched with programmatic stream serialization behind the schedule kernel:
-    // nothing that kernel writes (cc, the status word) is touched before pdl_wait.  The
-    // state kernel may be scheduled once every CTA is past this point, so it can read the
-    // schedule (complete by then) before it waits for this kernel's records.
-    pdl_wait();
-    pdl_launch_dependents();
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5;
     const bool compute = tid < kChunkCompute, issuer = tid == kChunkIssuer;
     constexpr int kIssueWarp = kChunkIssuer / 32;
-    // Persistent: item = (chunk, head) over the packed chunks g_base .. g_base + seg_chunks - 1,
-    // heads fastest, chunks last to first; this CTA takes items blockIdx.x, blockIdx.x +
-    // gridDim.x, ...  Items past the last packed chunk (the chunk count is an upper bound)
-    // are skipped.  Records are indexed from g_base.
     const int items = seg_chunks * H;
     auto next_item = [&](int it, int &h, int &g, int2 &dsc) -> int {
-        for (; it < items; it += (int)gridDim.x) {
+        for (; it < items; it += stride) {
             h = it % H;
-            g = g_base + seg_chunks - 1 - it / H;
+            g = STREAM ? g_base + it / H : g_base + seg_chunks - 1 - it / H;
             dsc = desc[g];  // first token and row count of packed chunk g
             if (dsc.y > 0) break;
+            if (STREAM) return items;  // claimed in order: no packed chunk follows this one
         }
         return it;
     };
     int h = 0, g = 0;
     int2 dsc = make_int2(0, 0);
-    int it = next_item((int)blockIdx.x, h, g, dsc);
+    if (STREAM) {
+        if (tid == 0) {
+            s_claim[0] = atomicAdd(claim, 1);
+            s_claim[1] = atomicAdd(claim, 1);
+        }
+        __syncthreads();
+        it0 = s_claim[0];
+    }
+    int it = next_item(it0, h, g, dsc);
     // q and k boxes, and (per-channel gate) the log_alpha box into O1, which is free until
     // the decayed operands are written there
     const uint32_t tma_bytes = 16384 + 16384 + (scalar_gate ? 0u : 32768u);
@@ -380,7 +389,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
         // the next item, so that its descriptor load overlaps this item's work
         int hn = 0, gn = 0;
         int2 dn = make_int2(0, 0);
-        const int itn = next_item(it + (int)gridDim.x, hn, gn, dn);
+        const int itn = next_item(STREAM ? s_claim[1] : it + stride, hn, gn, dn);
         const uint32_t pm = (3u * n) & 1u;  // bar_mma completes three times per item
         if (tid < kC) s_beta[tid] = tid < len ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
         float2 gl[4096 / NT];
@@ -394,6 +403,8 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
             prefix_scan<NT>(reinterpret_cast<const float *>(sm + L::O1), kD, len, s_tot, gl, gmin, gmax);
         // every thread is past its reads of the log_alpha box and s_tot is complete
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
+        // every thread has read the claim of the next item: claim the one after it
+        if (STREAM && tid == 0) s_claim[1] = atomicAdd(claim, 1);
         if (NORM) {
             if (compute) qk_row_inv_norms<NT>(sm + L::IN_K, sm + L::IN_Q, s_rn);
             __syncthreads();
@@ -485,6 +496,11 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
                 tma_load_3d(sm + L::IN_Q, &tm_q, &bar_tma, 0, hn, dn.x);
                 tma_load_3d(sm + L::IN_K, &tm_k, &bar_tma, 0, hn, dn.x);
             }
+            if (STREAM) {  // the record is complete in global memory: publish it
+                bulk_wait_all();
+                fence_proxy_async_global();
+                st_release_gpu(flags + (size_t)g * H + h, 1);
+            }
         }
         it = itn;
         h = hn;
@@ -508,6 +524,25 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     tc_fence_before_sync();
     __syncthreads();
     if (warp == kIssueWarp) tmem_dealloc(tmem, kChunkTmem);
+}
+
+template <bool NORM>
+__global__ void __launch_bounds__(kChunkThreads, 2)
+prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_la, const float *__restrict__ log_alpha,
+                     const float *__restrict__ beta,
+                     const int2 *__restrict__ desc, int H, int g_base, int seg_chunks,
+                     unsigned char *__restrict__ records, uint32_t *status, bool with_o, bool scalar_gate)
+{
+    // launched with programmatic stream serialization behind the schedule kernel:
+    // nothing that kernel writes (cc, the status word) is touched before pdl_wait.  The
+    // state kernel may be scheduled once every CTA is past this point, so it can read the
+    // schedule (complete by then) before it waits for this kernel's records.
+    pdl_wait();
+    pdl_launch_dependents();
+    // persistent: this CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...
+    chunk_items<NORM, false>(tm_q, tm_k, tm_la, log_alpha, beta, desc, H, g_base, seg_chunks, records, status,
+                             with_o, scalar_gate, (int)blockIdx.x, (int)gridDim.x, nullptr, nullptr);
 }
 
 // ============================================================== state kernel
@@ -862,6 +897,412 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
     if (warp == 0) tmem_dealloc(tmem, Sh::TMEM);
 }
 
+// ============================================================== streamed prefill
+// One launch of two CTAs per SM.  CTAs [0, n_walk) each walk the state of one (sequence,
+// head) unit through its chunks; the others run the chunk work (chunk_items, chunks first
+// to last, items claimed in order from a counter) and publish every record with a release
+// store of its flag.  A walker copies a record only after an acquire load has seen its
+// flag, so the serial pass follows the chunk work closely, its records come back from L2,
+// and the serial chain overlaps the chunk work instead of following it.
+//
+// Progress does not depend on which CTAs are resident: only walkers wait, and only for
+// records; a worker never waits for another CTA, and the items are claimed in order by
+// workers that are running, so the earliest unpublished record is always in work.  The
+// walkers (at most kMaxWalkers) are fewer than the CTAs that one wave holds, so workers
+// always run beside them.  Every wait is bounded all the same (a flag that does not come
+// up within the limit is recorded as KDA_ERR_TIMEOUT and the CTA unwinds).
+//
+// The walker forms the transposed products, so that a whole head fits in a CTA of the
+// chunk work's size.  With S^T (value column j x key row i) as the A operand, the state
+// update and the outputs share their A operands and run as one product group:
+//   [S_{c+1}^T | o_c^T] = [gamma_c . S_c^T | 0] + V_c^T [P_c^T | P2_c^T] + S_c^T [N_c^T | Q'_c^T]
+// (M = 128 rows j; N = 128 key rows i for the state and 64 tokens t for the outputs, 192 in
+// all).  The record's P, P2, N and Q' images (rows over their first index, K-major over
+// the second) are the B operands; the walker copies them so that P and P2, and each K panel
+// of N and Q', sit back to back as 192-row operands.  TMEM holds the state itself: the
+// accumulator's first 128 columns (fp32, lane j, column i), into which the state warps store
+// gamma_c . S_c (and zeros into the output columns) before the products accumulate onto
+// them; and S_c^T in bf16 as the A operand of the N, Q' products.  V_c^T (fp16, K-major) is
+// in shared memory.
+struct WalkLayout {
+    // the record in use: [N panel 0 | Q' panel 0 | N panel 1 | Q' panel 1 | P | P2]
+    static constexpr uint32_t NQ = 0, NQ_PANEL = 24576;  // 192 rows x 128 bytes per K panel
+    static constexpr uint32_t PP = 2 * NQ_PANEL;         // P (128 rows) then P2 (64 rows)
+    static constexpr uint32_t VT = PP + 24576;           // V^T fp16, 128 rows (j) x K 64 (t)
+    static constexpr uint32_t VBOX = VT + kC * kD * 2;   // raw v box [64 tokens][128] bf16
+    static constexpr uint32_t GAM = VBOX + kC * kD * 2;  // gamma of two chunks, 2 x 128 fp32
+    static constexpr uint32_t USED = GAM + 2 * kD * 4;
+};
+static_assert(WalkLayout::NQ_PANEL % 1024 == 0 && WalkLayout::PP % 1024 == 0 && WalkLayout::VT % 1024 == 0 &&
+                  WalkLayout::VBOX % 128 == 0,
+              "walker layout alignment");
+static_assert(R_P2 == R_P + 16384, "P2 follows P in the record");
+constexpr uint32_t kStreamSmem =
+    (WalkLayout::USED > ChunkLayout::USED ? WalkLayout::USED : ChunkLayout::USED) + 1024;
+// walker TMEM columns: accumulator (state 0-127, outputs 128-191), bf16 S^T
+constexpr uint32_t TW_D = 0, TW_O = 128, TW_A = 192, kWalkTmem = 256;
+constexpr int kWalkStateWarps = 8;
+constexpr int kMaxWalkers = 64;  // (sequence, head) units the streamed prefill takes at most
+
+// The product group of one chunk: D += V^T [P^T | P2^T] (fp16) + S^T [N^T | Q'^T] (bf16, S^T
+// from TMEM), N = 192, or N = 128 (state only) without the outputs.
+__device__ __forceinline__ void issue_walk(uint32_t tmem, uint32_t sb, bool with_o)
+{
+    const uint32_t id_pv = with_o ? idesc_f16(128, 192, false, false) : idesc_f16(128, 128, false, false);
+    const uint32_t id_ns = with_o ? idesc_bf16(128, 192, false, false) : idesc_bf16(128, 128, false, false);
+    const uint64_t dvt = kdesc(sb + WalkLayout::VT), dp = kdesc(sb + WalkLayout::PP), dn = kdesc(sb + WalkLayout::NQ);
+#pragma unroll
+    for (int s = 0; s < 4; ++s) mma_bf16(tmem + TW_D, dvt + 2 * s, dp + 2 * s, id_pv, 1);
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+        mma_tmem_a(tmem + TW_D, tmem + TW_A + 8 * s, dn + (((s >> 2) * WalkLayout::NQ_PANEL + (s & 3) * 32) >> 4),
+                   id_ns, 1);
+}
+
+// One walker CTA over one unit.  Warps 0-7 move the state through TMEM (value column j =
+// 32 (warp & 3) + lane, key rows 64 (warp >> 2) .. + 63), write the outputs and convert
+// the v boxes; lane 0 of warp 8 waits for the records' flags, copies the records and issues
+// the product group.  Per chunk c:
+//   warp 8    waits ready(c) and record c; loads the v box of c + 1; issues the group (commit
+//             w_mma); copies record c + 1 once w_mma(c) holds (its flag was seen a chunk
+//             earlier); then waits for the flag of record c + 2 and copies its gamma.
+//   warps 0-7 wait w_mma(c); read o_c into registers and zero the output columns; read
+//             S_{c+1} from D, store bf16(S_{c+1}) and gamma_{c+1} . S_{c+1} back; convert the
+//             v box of c + 1; arrive on ready(c + 1); then store o_c while the next group runs.
+// Every barrier's producer stays within one phase of its consumers (each refill waits for
+// the consumption of what it overwrites), so no wait is ever more than one phase behind.
+__device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, const int32_t *__restrict__ cu,
+                                          int64_t total, int H, const int32_t *__restrict__ cc,
+                                          const unsigned char *__restrict__ records, const int *flags,
+                                          const float *init_state, __nv_bfloat16 *__restrict__ o, float *final_state,
+                                          uint32_t *status, const StateSlots &slots)
+{
+    using L = WalkLayout;
+    extern __shared__ unsigned char smem_raw[];
+    __shared__ __align__(8) uint64_t w_ready, w_mma, w_rec, w_v, w_vfree, w_g[2], w_drain;
+    __shared__ uint32_t w_tmem;
+    unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    const uint32_t sb = smem_u32(sm);
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const bool state_warp = warp < kWalkStateWarps, ctl_warp = warp == kWalkStateWarps;
+    const int n = unit / H, h = unit % H;
+    int64_t t0, t1;
+    seq_range(cu, n, total, t0, t1);
+    const int nch = (int)((t1 - t0 + kC - 1) / kC);
+    int64_t si, sf;
+    if (!state_entries(slots, n, init_state != nullptr, si, sf) && tid == 0) atomicOr(status, DEV_ERR_SLOT);
+    const int jrow = (warp & 3) * 32 + lane, ib = 64 * ((warp >> 2) & 1);
+    const size_t st_entry = (size_t)H * kD * kD, st_head = (size_t)h * kD * kD;
+    if (nch == 0) {  // no tokens: the final state is the initial one
+        if (state_warp && sf >= 0)
+            for (int i = ib; i < ib + 64; ++i)
+                final_state[sf * st_entry + st_head + (size_t)i * kD + jrow] =
+                    si >= 0 ? init_state[si * st_entry + st_head + (size_t)i * kD + jrow] : 0.f;
+        return;
+    }
+    if (sf < 0 && o == nullptr) return;  // nothing to store and no outputs
+    const unsigned char *rec0 = records + ((size_t)cc[n] * H + h) * kRecBytes;
+    const size_t rec_stride = (size_t)H * kRecBytes;
+    const int *flag0 = flags + (size_t)cc[n] * H + h;
+    if (tid == 0) {
+        mbar_init(&w_ready, kWalkStateWarps);
+        mbar_init(&w_mma, 1);
+        mbar_init(&w_rec, 1);
+        mbar_init(&w_v, 1);
+        mbar_init(&w_vfree, kWalkStateWarps);
+        mbar_init(&w_g[0], 1);
+        mbar_init(&w_g[1], 1);
+        mbar_init(&w_drain, 1);
+        fence_mbar_init();
+    }
+    if (warp == 0) {
+        tmem_alloc(&w_tmem, kWalkTmem);
+        tmem_relinquish();
+    }
+    tc_fence_before_sync();
+    __syncthreads();  // barriers initialised, TMEM allocated
+    tc_fence_after_sync();
+    const uint32_t tmem = w_tmem;
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+
+    // copies: issued by lane 0 of warp 8 only, which alone keeps these counts
+    int rec_issued = 0, v_issued = 0, g_issued = 0;
+    auto wait_flag = [&](int c) -> bool {  // record c is complete in global memory
+        const int *f = flag0 + (size_t)c * H;
+        if (ld_acquire_gpu(f) == 0) {
+            const uint64_t ts = globaltimer_ns();
+            for (;;) {
+                __nanosleep(128);
+                if (ld_acquire_gpu(f) != 0) break;
+                if (globaltimer_ns() - ts > kWaitNs) return false;
+            }
+        }
+        fence_proxy_async_global();  // the bulk copies below read what the flag published
+        return true;
+    };
+    auto load_gamma = [&](int c) {
+        mbar_arrive_expect_tx(&w_g[c & 1], kD * 4);
+        bulk_load(sm + L::GAM + (c & 1) * kD * 4, rec0 + (size_t)c * rec_stride + R_GM, kD * 4, &w_g[c & 1]);
+        g_issued = c + 1;
+    };
+    auto load_record = [&](int c) {  // N, P (and with outputs Q', P2) as the group's operands
+        const unsigned char *r = rec0 + (size_t)c * rec_stride;
+        mbar_arrive_expect_tx(&w_rec, o ? 73728u : 49152u);
+        bulk_load(sm + L::NQ, r + R_N, 16384, &w_rec);
+        bulk_load(sm + L::NQ + L::NQ_PANEL, r + R_N + 16384, 16384, &w_rec);
+        bulk_load(sm + L::PP, r + R_P, 16384, &w_rec);
+        if (o) {
+            bulk_load(sm + L::NQ + 16384, r + R_Q, 8192, &w_rec);
+            bulk_load(sm + L::NQ + L::NQ_PANEL + 16384, r + R_Q + 8192, 8192, &w_rec);
+            bulk_load(sm + L::PP + 16384, r + R_P2, 8192, &w_rec);
+        }
+        rec_issued = c + 1;
+    };
+    auto load_v = [&](int c) {
+        mbar_arrive_expect_tx(&w_v, kC * kD * 2);
+        tma_load_3d(sm + L::VBOX, &tm_v, &w_v, 0, h, (int)(t0 + (int64_t)c * kC));
+        v_issued = c + 1;
+    };
+    bool range_ok = true;
+    // state warps (whole warps; every wait result is made uniform over the warp, as the
+    // TMEM loads and stores are warp-collective): the v box of chunk c -> V^T fp16, K-major
+    // rows j, 128-byte swizzle; rows past the unit's last token read as zero
+    // The box is read into registers (vt) as soon as it arrives, and the warp then
+    // arrives on w_vfree; the registers go to the V^T image once the products reading it
+    // are done.
+    const int vj = tid & (kD - 1), vs0 = (tid >> 7) * 32;  // V^T row j, tokens vs0 .. vs0 + 31
+    auto read_v = [&](int c, uint4 (&vt)[4]) -> bool {
+        if (!__all_sync(0xffffffffu, mbar_wait_ns(&w_v, (uint32_t)(c & 1), kWaitNs))) return false;
+        const int64_t cs = t0 + (int64_t)c * kC;
+        const int lenc = (t1 - cs) < kC ? (int)(t1 - cs) : kC;
+        const unsigned char *box = sm + L::VBOX;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            float x[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int s = vs0 + 8 * q + u;
+                x[u] = s < lenc ? bf16_at(box + (s * kD + vj) * 2) : 0.f;
+                range_ok &= fabsf(x[u]) <= 65504.f;
+            }
+            vt[q] = pack_f16x8_plain(x);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&w_vfree);  // this warp is done with the box
+        return true;
+    };
+    auto store_v = [&](const uint4 (&vt)[4]) {
+#pragma unroll
+        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4 *>(sm + L::VT + km16(vj, vs0 + 8 * q, kD)) = vt[q];
+    };
+    // state warps: 16 key rows i0 .. i0 + 15 of column j: bf16(S) into the A operand,
+    // gamma . S (fp32) into D
+    auto put_state = [&](int i0, float (&x)[16], const float *gam) {
+        uint32_t pk[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) pk[u] = pack_bf16x2(x[2 * u], x[2 * u + 1]);
+        tmem_st8(tmem + lane_off + TW_A + i0 / 2, pk);
+#pragma unroll
+        for (int u = 0; u < 16; u += 4) {
+            const float4 g = *reinterpret_cast<const float4 *>(gam + i0 + u);
+            x[u] *= g.x;
+            x[u + 1] *= g.y;
+            x[u + 2] *= g.z;
+            x[u + 3] *= g.w;
+        }
+        tmem_st16(tmem + lane_off + TW_D + i0, x);
+    };
+    // state warps: zeros into this thread's 32 output columns (the group accumulates onto D)
+    auto zero_out = [&]() {
+        float z[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) z[u] = 0.f;
+        tmem_st16(tmem + lane_off + TW_O + ib / 2, z);
+        tmem_st16(tmem + lane_off + TW_O + ib / 2 + 16, z);
+    };
+
+    bool ok = true;
+    if (ctl_warp) {
+        if (lane == 0) {
+            load_v(0);
+            ok = wait_flag(0);
+            if (ok) {
+                load_gamma(0);
+                load_record(0);
+            }
+            if (ok && nch > 1) {
+                ok = wait_flag(1);
+                if (ok) load_gamma(1);
+            }
+            if (ok && nch > 1) {  // the box of chunk 1, once chunk 0's is read
+                ok = mbar_wait_ns(&w_vfree, 0, kWaitNs);
+                if (ok) load_v(1);
+            }
+        }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+    } else if (state_warp) {  // S_0: gamma_0 . S_0 into D, bf16(S_0) into the A operand
+        ok = __all_sync(0xffffffffu, mbar_wait_ns(&w_g[0], 0, kWaitNs));
+        const float *gam = reinterpret_cast<const float *>(sm + L::GAM);
+        if (ok) {
+#pragma unroll 1
+            for (int q = 0; q < 4; ++q) {
+                const int i0 = ib + 16 * q;
+                float x[16];
+#pragma unroll
+                for (int u = 0; u < 16; ++u)
+                    x[u] = si >= 0 ? init_state[si * st_entry + st_head + (size_t)(i0 + u) * kD + jrow] : 0.f;
+                put_state(i0, x, gam);
+            }
+            if (o) zero_out();
+            uint4 vt[4];
+            ok = read_v(0, vt);
+            if (ok) store_v(vt);
+        }
+        tmem_st_wait();
+        fence_proxy_async_smem();
+        tc_fence_before_sync();
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok && lane == 0) mbar_arrive(&w_ready);
+    }
+    if (ctl_warp) {
+        for (int c = 0; ok && c < nch; ++c) {
+            if (lane == 0) {  // polls (the only thread of its warp at work: the chain's issuer)
+                ok = mbar_wait_spin_ns(&w_ready, (uint32_t)(c & 1), kWaitNs) &&
+                     mbar_wait_spin_ns(&w_rec, (uint32_t)(c & 1), kWaitNs);
+                if (ok) {
+                    tc_fence_after_sync();
+                    issue_walk(tmem, sb, o != nullptr);
+                    mma_commit(&w_mma);
+                }
+                if (ok && c + 2 < nch) {  // the box of chunk c + 2, once that of c + 1 is read
+                    ok = mbar_wait_ns(&w_vfree, (uint32_t)((c + 1) & 1), kWaitNs);
+                    if (ok) load_v(c + 2);
+                }
+                if (ok && c + 1 < nch) {
+                    ok = mbar_wait_spin_ns(&w_mma, (uint32_t)(c & 1), kWaitNs);  // record c is read
+                    if (ok) load_record(c + 1);  // its flag was seen a chunk ago
+                    if (ok && c + 2 < nch) {
+                        ok = wait_flag(c + 2);
+                        if (ok) {
+                            load_gamma(c + 2);
+                            // record c + 2 into L2 now (it may have left L2 since it was written)
+                            bulk_prefetch_l2(rec0 + (size_t)(c + 2) * rec_stride, kRecBytes);
+                        }
+                    }
+                }
+            }
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+        }
+    } else if (state_warp) {
+        const int par = lane & 1;  // lane pairs (j, j ^ 1) store two columns of one token
+        uint32_t opk[16];          // o_c, paired bf16 columns, 16 tokens x 2 halves
+        // o_c^T (lane j, tokens ib / 2 ..) into registers, paired over lanes j, j ^ 1; then
+        // zeros into the output columns for the next group
+        auto read_o = [&]() {
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                float v[16];
+                tmem_ld16(tmem + lane_off + TW_O + ib / 2 + 16 * hh, v);
+                tmem_ld_wait();
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    // even lane: (own, partner's) at token 2k; odd lane: (partner's, own) at 2k + 1
+                    const float mine = par ? v[2 * k + 1] : v[2 * k];
+                    const float other = __shfl_xor_sync(0xffffffffu, par ? v[2 * k] : v[2 * k + 1], 1);
+                    opk[8 * hh + k] = par ? pack_bf16x2(other, mine) : pack_bf16x2(mine, other);
+                }
+            }
+            zero_out();
+        };
+        for (int c = 0; ok && c < nch; ++c) {
+            const int64_t cs = t0 + (int64_t)c * kC;
+            uint4 vt[4];  // the next chunk's V^T, read while this chunk's products run
+            if (c + 1 < nch) ok = read_v(c + 1, vt);
+            ok = ok && __all_sync(0xffffffffu, mbar_wait_ns(&w_mma, (uint32_t)(c & 1), kWaitNs));
+            tc_fence_after_sync();
+            if (ok && c + 1 < nch) store_v(vt);  // V^T of chunk c is no longer read
+            if (c + 1 < nch) {
+                if (ok) ok = __all_sync(0xffffffffu, mbar_wait_ns(&w_g[(c + 1) & 1], (uint32_t)(((c + 1) >> 1) & 1), kWaitNs));
+                if (ok) {
+                    const float *gam = reinterpret_cast<const float *>(sm + L::GAM + ((c + 1) & 1) * kD * 4);
+#pragma unroll 1
+                    for (int q = 0; q < 4; ++q) {
+                        const int i0 = ib + 16 * q;
+                        float x[16];
+                        tmem_ld16(tmem + lane_off + TW_D + i0, x);
+                        tmem_ld_wait();
+                        put_state(i0, x, gam);
+                    }
+                }
+                if (ok && o) read_o();
+                tmem_st_wait();
+                fence_proxy_async_smem();
+                tc_fence_before_sync();
+                ok = __all_sync(0xffffffffu, ok);
+                if (ok && lane == 0) mbar_arrive(&w_ready);
+            } else if (ok) {
+                if (o) read_o();
+#pragma unroll 1
+                for (int q = 0; q < 4 && sf >= 0; ++q) {  // the final state S_T is D
+                    const int i0 = ib + 16 * q;
+                    float x[16];
+                    tmem_ld16(tmem + lane_off + TW_D + i0, x);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int u = 0; u < 16; ++u) final_state[sf * st_entry + st_head + (size_t)(i0 + u) * kD + jrow] = x[u];
+                }
+            }
+            if (ok && o) {  // the outputs of chunk c, while the next chunk's products run
+                __nv_bfloat16 *orow = o + (size_t)h * kD + (jrow & ~1);
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                    const int64_t t = cs + ib / 2 + 16 * (e >> 3) + 2 * (e & 7) + par;
+                    if (t < t1) *reinterpret_cast<uint32_t *>(orow + (size_t)t * H * kD) = opk[e];
+                }
+            }
+        }
+    }
+    const bool timed_out = __syncthreads_or(!ok);  // every role has finished or given up
+    if (timed_out) {
+        if (tid == 0) atomicOr(status, DEV_ERR_TIMEOUT);
+        if (ctl_warp && lane == 0) {
+            mma_commit(&w_drain);  // completes once every MMA issued so far has
+            (void)mbar_wait_ns(&w_drain, 0, kWaitNs);
+            // our own copies still in flight: the last phase of each barrier
+            if (rec_issued > 0) (void)mbar_wait_ns(&w_rec, (uint32_t)((rec_issued - 1) & 1), kWaitNs);
+            if (v_issued > 0) (void)mbar_wait_ns(&w_v, (uint32_t)((v_issued - 1) & 1), kWaitNs);
+            for (int k = g_issued > 2 ? g_issued - 2 : 0; k < g_issued; ++k)
+                (void)mbar_wait_ns(&w_g[k & 1], (uint32_t)((k >> 1) & 1), kWaitNs);
+        }
+    }
+    if (!range_ok) atomicOr(status, DEV_ERR_RANGE);
+    tc_fence_before_sync();
+    __syncthreads();
+    if (warp == 0) tmem_dealloc(tmem, kWalkTmem);
+}
+
+// The streamed prefill: walkers (blockIdx.x < n_walk) and chunk workers in one grid.
+template <bool NORM>
+__global__ void __launch_bounds__(kChunkThreads, 2)
+prefill_stream_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                      const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_v,
+                      const float *__restrict__ log_alpha, const float *__restrict__ beta,
+                      const int2 *__restrict__ desc, int H, int chunks, unsigned char *records, int *flags,
+                      uint32_t *status, bool scalar_gate, const int32_t *__restrict__ cu, int64_t total,
+                      const int32_t *__restrict__ cc, const float *init_state, __nv_bfloat16 *o,
+                      float *final_state, StateSlots slots, int n_walk)
+{
+    // launched with programmatic stream serialization behind the schedule kernel, which
+    // zeroes the flags and the claim counter: nothing it writes is read before this wait
+    pdl_wait();
+    pdl_launch_dependents();
+    if ((int)blockIdx.x < n_walk)
+        walk_unit((int)blockIdx.x, tm_v, cu, total, H, cc, records, flags, init_state, o, final_state, status, slots);
+    else
+        chunk_items<NORM, true>(tm_q, tm_k, tm_la, log_alpha, beta, desc, H, 0, chunks, records, status,
+                                o != nullptr, scalar_gate, 0, 1, flags, flags + (size_t)chunks * H);
+}
+
 // ============================================================== product-group diagnostic
 // Measurement only.  The tensor-core product groups of one prefill kernel, issued back to
 // back `reps` times per CTA by the same routines the kernels use, on a constant operand
@@ -870,9 +1311,12 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
 // P2, the three-term P, N, Q''), issued by one thread, two CTAs per SM as that kernel runs.
 // PASS 1: the state kernel's chain and output groups of one chunk and 64-column slice,
 // one CTA per SM, each group issued by a thread of its own warp as in that kernel.
-constexpr uint64_t kDiagFlops[2] = {
+// PASS 2: the streamed kernel's walk group of one chunk (whole head, S^T from TMEM, the
+// state and output products as one N = 192 group), one CTA per SM, one issuing thread.
+constexpr uint64_t kDiagFlops[3] = {
     2ull * (128 * 64 * 128 + 64 * 128 * 64 + 64 * 64 * 64 + 3 * 128 * 64 * 64 + 128 * 128 * 64 + 64 * 128 * 64),
-    2ull * (128 * 64 * 64 + 128 * 64 * 128 + 64 * 64 * 64 + 64 * 64 * 128)};
+    2ull * (128 * 64 * 64 + 128 * 64 * 128 + 64 * 64 * 64 + 64 * 64 * 128),
+    2ull * (128 * 128 * 64 + 128 * 128 * 128 + 128 * 64 * 64 + 128 * 64 * 128)};
 using DiagState = StateShape<64>;  // pass 1 measures the 64-column groups
 
 template <int PASS>
@@ -881,8 +1325,8 @@ __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(in
     extern __shared__ unsigned char smem_raw[];
     __shared__ __align__(8) uint64_t bar[2], bar_drain;
     __shared__ uint32_t tmem_holder;
-    constexpr uint32_t used = PASS == 0 ? ChunkLayout::USED : DiagState::USED;
-    constexpr uint32_t cols = PASS == 0 ? kChunkTmem : DiagState::TMEM;
+    constexpr uint32_t used = PASS == 0 ? ChunkLayout::USED : (PASS == 1 ? DiagState::USED : WalkLayout::USED);
+    constexpr uint32_t cols = PASS == 0 ? kChunkTmem : (PASS == 1 ? DiagState::TMEM : kWalkTmem);
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x;
@@ -893,7 +1337,7 @@ __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(in
     if (tid == 0) {
         mbar_init(&bar[0], 1);
         mbar_init(&bar[1], 1);
-        mbar_init(&bar_drain, PASS == 0 ? 1 : 2);
+        mbar_init(&bar_drain, PASS == 1 ? 2 : 1);  // one commit per issuing thread
         fence_mbar_init();
     }
     if (tid < 32) {
@@ -903,8 +1347,18 @@ __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(in
     __syncthreads();
     tc_fence_after_sync();
     const uint32_t tmem = tmem_holder;
-    // PASS 0: thread 0 issues everything; PASS 1: thread 0 the chain group, thread 128 the
-    // output group
+    if (PASS == 2 && tid < 128) {  // the bf16 S^T operand in TMEM: the same constant
+        float x[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) x[u] = __uint_as_float(0x3c003c00u);
+        for (int c = 0; c < 64; c += 16) tmem_st16(tmem + ((uint32_t)(tid & ~31) << 16) + TW_A + c, x);
+        tmem_st_wait();
+    }
+    tc_fence_before_sync();
+    __syncthreads();
+    tc_fence_after_sync();
+    // PASS 0 and 2: thread 0 issues everything; PASS 1: thread 0 the chain group, thread 128
+    // the output group
     const int issuer = tid == 0 ? 0 : (PASS == 1 && tid == 128 ? 1 : -1);
     if (issuer >= 0) {
         bool ok = true;
@@ -914,6 +1368,8 @@ __global__ void __launch_bounds__(256, PASS == 0 ? 2 : 1) tensor_phase_kernel(in
                 issue_w_p2<ChunkLayout>(sb, tmem, true);
                 issue_p<ChunkLayout>(sb, tmem);
                 issue_n_q<ChunkLayout>(sb, tmem, true);
+            } else if (PASS == 2) {
+                issue_walk(tmem, sb, true);
             } else {
                 const uint64_t dr = kdesc(sb), dv = kdesc(sb + DiagState::VIMG), ds = DiagState::sdesc_s(sb + DiagState::O7);
                 if (issuer == 0)
@@ -942,7 +1398,7 @@ cudaError_t run_tensor_phases(int reps, uint32_t *status, cudaStream_t stream, d
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    const int smem = PASS == 0 ? (int)kChunkSmem : (int)DiagState::SMEM;
+    const int smem = PASS == 0 ? (int)kChunkSmem : (PASS == 1 ? (int)DiagState::SMEM : (int)kStreamSmem);
     if (configured != dev) {
         if ((err = cudaFuncSetAttribute(tensor_phase_kernel<PASS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         smem)) != cudaSuccess ||
@@ -973,8 +1429,9 @@ cudaError_t run_tensor_phases(int reps, uint32_t *status, cudaStream_t stream, d
 
 cudaError_t diag_tensor_phases(int pass, int reps, uint32_t *status, cudaStream_t stream, double *tflops)
 {
-    return pass == 0 ? run_tensor_phases<0>(reps, status, stream, tflops)
-                     : run_tensor_phases<1>(reps, status, stream, tflops);
+    if (pass == 0) return run_tensor_phases<0>(reps, status, stream, tflops);
+    if (pass == 1) return run_tensor_phases<1>(reps, status, stream, tflops);
+    return run_tensor_phases<2>(reps, status, stream, tflops);
 }
 
 size_t prefill_split_record_bytes() { return kRecBytes; }
@@ -1044,7 +1501,51 @@ int sm_count()
     return count[dev];
 }
 
+// The streamed prefill (walkers and chunk workers in one grid of two CTAs per SM), for
+// problems with at most kMaxWalkers (sequence, head) units and every record in the
+// workspace.  cudaErrorNotSupported when the grid would leave fewer worker CTAs than SMs
+// (the caller then runs the two kernels).
+template <bool NORM>
+cudaError_t launch_stream(const PrefillProblem &p, const CUtensorMap &tq, const CUtensorMap &tk,
+                          const CUtensorMap &tla, const int32_t *cc, void *records, int units)
+{
+    static int dev_cfg = -1;
+    cudaError_t err = allow_smem(prefill_stream_kernel<NORM>, (int)kStreamSmem, &dev_cfg);
+    if (err != cudaSuccess) return err;
+    const int sms = sm_count();
+    if (sms <= 0 || 2 * sms - units < sms) return cudaErrorNotSupported;
+    CUtensorMap tv;  // v boxes of 64 tokens x 128 columns
+    if (!make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kD))
+        return cudaErrorInvalidValue;
+    cudaLaunchAttribute pdl;
+    pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl.val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.stream = p.stream;
+    cfg.attrs = &pdl;
+    cfg.numAttrs = 1;
+    cfg.gridDim = dim3(2 * sms);
+    cfg.blockDim = dim3(kChunkThreads);
+    cfg.dynamicSmemBytes = kStreamSmem;
+    return cudaLaunchKernelEx(&cfg, prefill_stream_kernel<NORM>, tq, tk, tla, tv, p.log_alpha, p.beta,
+                              (const int2 *)p.desc, p.num_heads, p.chunk_bound, static_cast<unsigned char *>(records),
+                              p.flags, p.status, p.scalar_gate, p.cu_seqlens, p.total_tokens, cc, p.init_state,
+                              static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.slots, units);
+}
+
 }  // namespace
+
+bool prefill_stream_fits(int64_t units)
+{
+    const int sms = sm_count();  // the walkers leave at least one worker CTA per SM
+    return units >= 1 && units <= kMaxWalkers && sms > 0 && 2 * (int64_t)sms - units >= sms;
+}
+
+bool prefill_stream_eligible(const PrefillProblem &p)
+{
+    return p.flags && p.split.lseg == 0 && p.seg_chunks == 0 &&
+           prefill_stream_fits((int64_t)p.num_seqs * p.num_heads);
+}
 
 cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records, cudaEvent_t mid)
 {
@@ -1077,6 +1578,15 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     // 32-column state slices while every (sequence, head, slice) of the pass fits in one wave
     // of SMs (their chain per chunk is shorter); 64-column slices beyond that, and for the
     // sequence split, whose transition pass is sized for them
+    if (prefill_stream_eligible(p)) {
+        const int units = p.num_seqs * p.num_heads;
+        err = p.qk_l2norm ? launch_stream<true>(p, tq, tk, tla, cc, records, units)
+                          : launch_stream<false>(p, tq, tk, tla, cc, records, units);
+        if (err != cudaErrorNotSupported) {
+            if (err == cudaSuccess && mid) err = cudaEventRecord(mid, p.stream);
+            return err;
+        }
+    }
     const unsigned char *rec = static_cast<const unsigned char *>(records);
     const int64_t slices32 = (int64_t)p.num_seqs * p.num_heads * (kD / 32);
     const bool narrow = p.split.lseg == 0 && slices32 <= sm_count();

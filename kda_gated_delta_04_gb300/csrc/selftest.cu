@@ -45,7 +45,7 @@ extern "C" kda_status_t kda_selftest_bounded_wait(void *workspace, uint64_t limi
 extern "C" kda_status_t kda_diag_tensor_phases(int32_t pass, int32_t reps, void *workspace, void *stream,
                                                double *tflops)
 {
-    if ((pass != 0 && pass != 1) || reps < 1 || reps > (1 << 20) || !tflops) return KDA_ERR_INVALID_ARG;
+    if (pass < 0 || pass > 2 || reps < 1 || reps > (1 << 20) || !tflops) return KDA_ERR_INVALID_ARG;
     if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return KDA_ERR_INVALID_ARG;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(workspace, 0, sizeof(uint32_t), s) != cudaSuccess) return KDA_ERR_CUDA;

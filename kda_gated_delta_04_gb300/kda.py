@@ -24,6 +24,9 @@ KDA_DTYPE_BF16, KDA_DTYPE_F32 = 0, 1
 KDA_FLAG_SCALAR_GATE = 1
 KDA_FLAG_QK_L2NORM = 2
 KDA_FLAG_NO_SEQ_SPLIT = 4
+KDA_FLAG_STREAM = 8
+KDA_PATH_CUDA_CORE, KDA_PATH_FUSED, KDA_PATH_TWO_KERNEL, KDA_PATH_SEQ_SPLIT, KDA_PATH_SEGMENTED, \
+    KDA_PATH_STREAMED = range(6)
 CHUNK = 64
 
 _lib = None
@@ -40,6 +43,8 @@ EXPORTS = {
                                                  _c.c_int32, _c.c_int]),
     "kda_prefill_workspace_size_segmented": (_c.c_size_t, [_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
                                                            _c.c_int32, _c.c_int, _c.c_int64]),
+    "kda_prefill_path": (_c.c_int32, [_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int,
+                                       _c.c_size_t, _c.c_uint32]),
     "kda_prefill": (_c.c_int, _PREFILL_ARGS),
     "kda_decode_step": (_c.c_int, _DECODE_ARGS),
     "kda_read_device_status": (_c.c_int, [_VP, _VP]),
@@ -94,6 +99,10 @@ def kda_prefill_workspace_size_segmented(num_seqs, total_tokens, num_heads, d_k,
                                          segment_chunks):
     return lib().kda_prefill_workspace_size_segmented(num_seqs, total_tokens, num_heads, d_k, d_v,
                                                       dtype, segment_chunks)
+
+
+def kda_prefill_path(num_seqs, total_tokens, num_heads, d_k, d_v, dtype, workspace_bytes, flags=0):
+    return lib().kda_prefill_path(num_seqs, total_tokens, num_heads, d_k, d_v, dtype, workspace_bytes, flags)
 
 
 def kda_prefill(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
@@ -176,8 +185,9 @@ def kda_diag_tensor_phases(pass_, reps, workspace, stream, tflops):
 
 
 def diag_tensor_phases(pass_, reps, workspace, stream=None):
-    """Executed TFLOP/s of the chunk kernel's (pass_ = 0) or state kernel's (pass_ = 1)
-    tensor-core product groups run on their own (see include/kda.h)."""
+    """Executed TFLOP/s of the chunk kernel's (pass_ = 0), the state kernel's (pass_ = 1) or
+    the streamed kernel's walk (pass_ = 2) tensor-core product groups run on their own (see
+    include/kda.h)."""
     out = _c.c_double(0.0)
     st = lib().kda_diag_tensor_phases(pass_, reps, _ptr(workspace, "workspace"),
                                       _stream_handle(stream, workspace.device), _c.byref(out))
@@ -230,10 +240,11 @@ def _ptr(t, name, dtype=None):
     return t.data_ptr()
 
 
-def _flags(log_alpha, qk_l2norm, seq_split=True):
+def _flags(log_alpha, qk_l2norm, seq_split=True, streamed=False):
     """Option bits: a log_alpha without a channel axis is the scalar gate."""
     return ((KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0) |
-            (KDA_FLAG_QK_L2NORM if qk_l2norm else 0) | (0 if seq_split else KDA_FLAG_NO_SEQ_SPLIT))
+            (KDA_FLAG_QK_L2NORM if qk_l2norm else 0) | (0 if seq_split else KDA_FLAG_NO_SEQ_SPLIT) |
+            (KDA_FLAG_STREAM if streamed else 0))
 
 
 def _stream_handle(stream, device):
@@ -268,14 +279,15 @@ def min_workspace_bytes(num_seqs):
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=None,
             final_state=None, workspace=None, stream=None, check_status=False, outputs=True,
-            qk_l2norm=False, seq_split=True):
+            qk_l2norm=False, seq_split=True, streamed=False):
     """KDA prefill over packed sequences.  q, k: [T, H, d]; v: [T, H, d]; log_alpha: [T, H, d]
     fp32; beta: [T, H] fp32; cu_seqlens: int32 [N+1] CUDA tensor or None (one sequence);
     init_state: [N, H, d, d] fp32 or None.  Returns (o, final_state); with outputs=False
     only the final states are computed and o is None.  A log_alpha of shape [T, H] is the
     scalar-gate (Gated DeltaNet) variant: one decay per token-head for every key channel.
     qk_l2norm=True: q and k are raw and the kernels L2-normalise their rows.  seq_split=False
-    keeps each sequence's state pass in one piece (KDA_FLAG_NO_SEQ_SPLIT)."""
+    keeps each sequence's state pass in one piece (KDA_FLAG_NO_SEQ_SPLIT); streamed=True runs
+    the chunk work and the state pass in one launch (KDA_FLAG_STREAM)."""
     torch = _torch()
     T, H, d = q.shape
     dt = _dtype_code(q)
@@ -288,7 +300,7 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
         final_state = torch.empty((N, H, d, v.shape[2]), dtype=torch.float32, device=q.device)
     if workspace is None:
         workspace = workspace_for(N, T, H, d, dt, q.device)
-    flags = _flags(log_alpha, qk_l2norm, seq_split)
+    flags = _flags(log_alpha, qk_l2norm, seq_split, streamed)
     st = kda_prefill_ex(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
                      _ptr(log_alpha, "log_alpha", torch.float32), _ptr(beta, "beta", torch.float32),
                      _ptr(cu_seqlens, "cu_seqlens", torch.int32), N, T, H, d, v.shape[2], dt,
@@ -308,7 +320,7 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
 
 def prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, state_pool, final_slots, init_slots=None, *,
                   o=None, workspace=None, stream=None, check_status=False, outputs=True,
-                  qk_l2norm=False, seq_split=True):
+                  qk_l2norm=False, seq_split=True, streamed=False):
     """Prefill into a paged state cache: sequence n starts from state_pool[init_slots[n]]
     (zero when init_slots is None or the entry is -1) and its final state is written to
     state_pool[final_slots[n]].  state_pool [S, H, d, d] fp32; slots int32 CUDA tensors [N].
@@ -323,7 +335,7 @@ def prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, state_pool, final_slots,
         o = None
     if workspace is None:
         workspace = workspace_for(N, T, H, d, dt, q.device)
-    flags = _flags(log_alpha, qk_l2norm, seq_split)
+    flags = _flags(log_alpha, qk_l2norm, seq_split, streamed)
     st = kda_prefill_slots(_ptr(q, "q", q.dtype), _ptr(k, "k", q.dtype), _ptr(v, "v", q.dtype),
                            _ptr(log_alpha, "log_alpha", torch.float32),
                            _ptr(beta, "beta", torch.float32),
@@ -358,7 +370,8 @@ def _hptr(t, name, dtype=None):
 
 
 def prefill_host(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=None, final_state=None,
-                 device_buffer=None, device=None, stream=None, outputs=True, qk_l2norm=False, seq_split=True):
+                 device_buffer=None, device=None, stream=None, outputs=True, qk_l2norm=False, seq_split=True,
+                 streamed=False):
     """kda_prefill_host: q, k, v, log_alpha, beta, cu_seqlens (int32), init_state and the outputs
     in host memory (pin them for the copies to overlap with the prefill).  Returns (o, final_state)
     as host tensors, valid once `stream` has been synchronised."""
@@ -385,7 +398,8 @@ def prefill_host(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, 
                           _hptr(o, "o", q.dtype), _hptr(final_state, "final_state", torch.float32),
                           _ptr(device_buffer, "device_buffer"),
                           device_buffer.numel() * device_buffer.element_size(),
-                          _stream_handle(stream, device_buffer.device), _flags(log_alpha, qk_l2norm, seq_split))
+                          _stream_handle(stream, device_buffer.device),
+                          _flags(log_alpha, qk_l2norm, seq_split, streamed))
     if st != KDA_OK:
         raise KdaError(st, "kda_prefill_host")
     return o, final_state

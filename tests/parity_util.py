@@ -33,12 +33,13 @@ def to_device(inp, device="cuda"):
     return out
 
 
-def gpu_prefill(inp, device="cuda", init_state_inplace=False, check_status=True):
+def gpu_prefill(inp, device="cuda", init_state_inplace=False, check_status=True, streamed=False):
     d = to_device(inp, device)
     cu = d["cu_seqlens"]
     fs = d["init_state"] if init_state_inplace else None
     o, fs = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], cu_seqlens=cu,
-                        init_state=d["init_state"], final_state=fs, check_status=check_status)
+                        init_state=d["init_state"], final_state=fs, check_status=check_status,
+                        streamed=streamed)
     torch.cuda.synchronize()
     return synth.to_f64(o), synth.to_f64(fs)
 

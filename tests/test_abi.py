@@ -67,13 +67,36 @@ def test_segmented_workspace_size(kda):
     assert kda.kda_prefill_workspace_size_segmented(N, T, H, 128, 128, 0, 10 * bound) == full_seg
     assert full_seg - one == (bound - 1) * H * 74240
     # the records of every chunk, as in the full workspace (this shape has no sequence split),
-    # plus the two carried states
-    assert full_seg - kda.kda_prefill_workspace_size(N, T, H, 128, 128, 0) == 2 * H * 128 * 128 * 4
+    # plus the two carried states, less the full workspace's ready flag per chunk-head record
+    flags = -(-(bound * H + 1) * 4 // 256) * 256
+    assert full_seg - kda.kda_prefill_workspace_size(N, T, H, 128, 128, 0) == 2 * H * 128 * 128 * 4 - flags
     for bad in (dict(seg=0), dict(dtype=1), dict(d=64), dict(T=0), dict(H=0)):
         a = dict(N=N, T=T, H=H, d=128, dtype=0, seg=4)
         a.update(bad)
         assert kda.kda_prefill_workspace_size_segmented(a["N"], a["T"], a["H"], a["d"], a["d"], a["dtype"],
                                                         a["seg"]) == 0
+
+
+def test_prefill_path_query(kda):
+    """kda_prefill_path, on the shapes and workspaces that decide it without the device (the
+    streamed and sequence-split choices are checked on the GPU): fp32 and d = 64 take the
+    CUDA-core kernel, a bf16 d = 128 call with the minimal workspace the fused kernel, with a
+    bounded-records workspace the segmented pass, and with the full workspace the two kernels
+    when the sequence split is turned off.  Rejected arguments give the
+    negated status kda_prefill_ex returns."""
+    N, T, H = 1, 4096, 32
+    full = kda.kda_prefill_workspace_size(N, T, H, 128, 128, 0)
+    seg = kda.kda_prefill_workspace_size_segmented(N, T, H, 128, 128, 0, 4)
+    minimal = kda.min_workspace_bytes(N)
+    off = kda.KDA_FLAG_NO_SEQ_SPLIT
+    assert kda.kda_prefill_path(N, T, H, 128, 128, 1, full, 0) == kda.KDA_PATH_CUDA_CORE
+    assert kda.kda_prefill_path(N, T, H, 64, 64, 0, full, 0) == kda.KDA_PATH_CUDA_CORE
+    assert kda.kda_prefill_path(N, T, H, 128, 128, 0, minimal, 0) == kda.KDA_PATH_FUSED
+    assert kda.kda_prefill_path(N, T, H, 128, 128, 0, seg, 0) == kda.KDA_PATH_SEGMENTED
+    assert kda.kda_prefill_path(N, T, H, 128, 128, 0, full, off) == kda.KDA_PATH_TWO_KERNEL
+    assert kda.kda_prefill_path(N, T, H, 128, 128, 0, minimal - 1, 0) == -kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_prefill_path(N, T, H, 128, 128, 0, full, 1 << 9) == -kda.KDA_ERR_INVALID_ARG
+    assert kda.kda_prefill_path(N, T, H, 96, 96, 0, full, 0) == -kda.KDA_ERR_UNSUPPORTED
 
 
 FAKE = 1 << 20  # 16-byte aligned dummy address; never dereferenced (rejected first)
@@ -154,7 +177,7 @@ def test_slot_calls_reject_bad_arguments_on_host(kda):
 def test_diag_tensor_phases_rejects_bad_arguments_on_host(kda):
     import ctypes
     out = ctypes.c_double(0.0)
-    assert kda.kda_diag_tensor_phases(2, 10, FAKE, None, ctypes.byref(out)) == 1    # no such pass
+    assert kda.kda_diag_tensor_phases(3, 10, FAKE, None, ctypes.byref(out)) == 1    # no such pass
     assert kda.kda_diag_tensor_phases(0, 0, FAKE, None, ctypes.byref(out)) == 1     # no repetition
     assert kda.kda_diag_tensor_phases(0, 10, FAKE + 16, None, ctypes.byref(out)) == 1  # misaligned
     assert kda.kda_diag_tensor_phases(1, 10, None, None, ctypes.byref(out)) == 1    # no workspace

@@ -34,7 +34,7 @@ def test_small_problems_match_oracle(w):
     assert_parity(o, fs, o_ref, fs_ref, w.dtype, w.name)
 
 
-def _whole_tensor_parity(w, group):
+def _whole_tensor_parity(w, group, streamed=False):
     """Run the whole workload on the GPU exactly as the benchmark launches it, then check
     every (sequence, head) unit against the oracle, `group` heads at a time (so host memory
     stays bounded): o element by element (max-abs over the whole output), the final state by
@@ -44,7 +44,7 @@ def _whole_tensor_parity(w, group):
     d = to_device(full)
     o_d, fs_d = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"],
                             cu_seqlens=d["cu_seqlens"], init_state=d["init_state"],
-                            check_status=True)
+                            check_status=True, streamed=streamed)
     torch.cuda.synchronize()
     o, fs = o_d.cpu(), fs_d.cpu()
     del d, o_d, fs_d
@@ -85,6 +85,16 @@ def _whole_tensor_parity(w, group):
 
 def test_prefill_4k_full_size_every_unit():
     _whole_tensor_parity(synth.PREFILL_4K, group=32)
+
+
+def test_prefill_4k_streamed_full_size_every_unit():
+    """The same workload with the chunk work and the state walk in one launch
+    (KDA_FLAG_STREAM)."""
+    _whole_tensor_parity(synth.PREFILL_4K, group=32, streamed=True)
+
+
+def test_prefill_64k_streamed_full_size_every_unit():
+    _whole_tensor_parity(synth.PREFILL_64K, group=8, streamed=True)
 
 
 def test_prefill_64k_with_initial_state_full_size_every_unit():
@@ -592,15 +602,15 @@ def test_bounded_records_run_in_segments(seg_chunks):
     kernels run segment by segment, each sequence cut at a boundary carrying its state in
     the workspace.  Ragged sequences (a zero-length one, one shorter than a chunk, several
     spanning many segments) from initial states, two heads: o and the final states bit for
-    bit those of the full workspace without the sequence split, and within the bar of the
-    oracle; the final state may alias the initial state."""
+    bit those of the full workspace in the same two-kernel form (no sequence split, no
+    streaming), and within the bar of the oracle; the final state may alias the initial state."""
     w = PrefillWorkload(f"segmented_{seg_chunks}", 170 + seg_chunks, 2, 128, "bf16",
                         (300, 0, 1000, 40, 129, 700), 6, init_state=True)
     inp = synth.prefill_inputs(w)
     d = to_device(inp)
     T, H = inp["q"].shape[:2]
     o_ref_gpu, fs_ref_gpu = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
-                                        d["init_state"], check_status=True, seq_split=False)
+                                        d["init_state"], check_status=True, seq_split=False, streamed=False)
     ws = kda.segmented_workspace_for(6, T, H, 128, kda.KDA_DTYPE_BF16, "cuda", seg_chunks)
     assert ws.numel() < kda.kda_prefill_workspace_size(6, T, H, 128, 128, kda.KDA_DTYPE_BF16)
     o, fs = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"],
@@ -619,13 +629,14 @@ def test_bounded_records_run_in_segments(seg_chunks):
 
 def test_bounded_records_at_full_size():
     """T = 65536, H = 32 from initial states with the records of 128 chunks at a time (8
-    segments, 304 MB of records instead of 2.4 GB): bit for bit the full workspace."""
+    segments, 304 MB of records instead of 2.4 GB): bit for bit the full workspace in the
+    same two-kernel form."""
     w = synth.PREFILL_64K
     inp = synth.prefill_inputs(w)
     d = to_device(inp)
     T, H = inp["q"].shape[:2]
     o_full, fs_full = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"],
-                                  d["init_state"], check_status=True, seq_split=False)
+                                  d["init_state"], check_status=True, seq_split=False, streamed=False)
     ws = kda.segmented_workspace_for(1, T, H, 128, kda.KDA_DTYPE_BF16, "cuda", 128)
     o, fs = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"],
                         workspace=ws, check_status=True)

@@ -1,0 +1,116 @@
+"""The streamed prefill (KDA_FLAG_STREAM: chunk work and state walk in one launch) against
+the oracle and against the two-kernel form on the same inputs.
+
+Every shape here has at most 64 (sequence, head) units and no sequence split, so a call with
+streamed=True takes the streamed kernel; the default runs the chunk kernel and then the state
+pass.
+Both are checked element by element against the fp64 oracle; their difference from each
+other is printed (it is rounding only: the walk forms its products transposed)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kda_gated_delta_04_gb300 import kda, synth
+from kda_gated_delta_04_gb300.synth import PrefillWorkload
+from parity_util import TOL, assert_parity, gpu_prefill, maxabs, oracle_prefill, relF, to_device
+
+pytestmark = pytest.mark.gpu
+
+CASES = [
+    PrefillWorkload("stream_T1000_H32", 300, 32, 128, "bf16", (1000,), 1),
+    PrefillWorkload("stream_two_seqs_H32_64_units", 301, 32, 128, "bf16", (300, 129), 2, init_state=True),
+    PrefillWorkload("stream_varlen_edges_H3_state", 302, 3, 128, "bf16", (0, 1, 63, 64, 65, 130), 6,
+                    init_state=True),
+    PrefillWorkload("stream_T64_H20", 303, 20, 128, "bf16", (64,), 1, init_state=True),
+    PrefillWorkload("stream_T4000_H24_state", 304, 24, 128, "bf16", (4000,), 1, init_state=True),
+]
+
+
+@pytest.mark.parametrize("w", CASES, ids=lambda w: w.name)
+def test_streamed_and_two_kernel_forms_match_oracle(w):
+    inp = synth.prefill_inputs(w)
+    o_s, fs_s = gpu_prefill(inp, streamed=True)
+    o_t, fs_t = gpu_prefill(inp, streamed=False)
+    o_ref, fs_ref = oracle_prefill(inp)
+    print(f"[stream] {w.name}: streamed vs two-kernel max|do| = {maxabs(o_s, o_t):.3e}, "
+          f"relF(state) = {relF(fs_s, fs_t):.3e}")
+    assert_parity(o_s, fs_s, o_ref, fs_ref, w.dtype, w.name + " (streamed)")
+    assert_parity(o_t, fs_t, o_ref, fs_ref, w.dtype, w.name + " (two kernels)")
+
+
+@pytest.mark.parametrize("variant", ["state_only", "scalar_gate", "qk_l2norm"])
+def test_streamed_variants(variant):
+    """Final states only (no output products), the scalar gate and in-kernel q/k
+    normalisation, each through the streamed kernel and the two-kernel form, against the
+    oracle."""
+    w = PrefillWorkload(f"stream_{variant}", 310, 16, 128, "bf16", (700, 190), 2, init_state=True,
+                        raw_qk=variant == "qk_l2norm")
+    inp = synth.prefill_inputs(w)
+    d = to_device(inp)
+    la = d["log_alpha"]
+    ref = dict(inp)
+    if variant == "scalar_gate":
+        g = torch.Generator().manual_seed(311)
+        T, H, dk = inp["q"].shape
+        la_s = (-0.05 * torch.nn.functional.softplus(torch.randn(T, H, generator=g))).float().contiguous()
+        la = la_s.cuda()
+        ref["log_alpha"] = la_s[:, :, None].expand(T, H, dk).contiguous()
+    if variant == "qk_l2norm":
+        ref["q"] = oracle.l2_normalize(synth.to_f64(inp["q"]))
+        ref["k"] = oracle.l2_normalize(synth.to_f64(inp["k"]))
+    o_ref, fs_ref = oracle_prefill(ref)
+    for streamed in (True, False):
+        o, fs = kda.prefill(d["q"], d["k"], d["v"], la, d["beta"], cu_seqlens=d["cu_seqlens"],
+                            init_state=d["init_state"], check_status=True, outputs=variant != "state_only",
+                            qk_l2norm=variant == "qk_l2norm", streamed=streamed)
+        torch.cuda.synchronize()
+        label = f"{w.name} ({'streamed' if streamed else 'two kernels'})"
+        if variant == "state_only":
+            assert o is None
+            es = relF(synth.to_f64(fs), fs_ref)
+            print(f"[parity] {label}: relF(state) = {es:.3e}")
+            assert np.isfinite(synth.to_f64(fs)).all() and es <= TOL["bf16"]["state"]
+        else:
+            assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, "bf16", label)
+
+
+def test_streamed_prefill_into_state_pool():
+    """kda_prefill_slots through the streamed kernel: start states from pool slots (one
+    sequence from zero), final states into other slots; untouched slots keep their bytes."""
+    w = PrefillWorkload("stream_slots", 320, 8, 128, "bf16", (200, 77, 130), 3, init_state=True)
+    inp = synth.prefill_inputs(w)
+    d = to_device(inp)
+    S = 7
+    pool = torch.randn((S, 8, 128, 128), generator=torch.Generator().manual_seed(321)).mul_(0.02).cuda()
+    init_slots = torch.tensor([4, -1, 0], dtype=torch.int32, device="cuda")
+    final_slots = torch.tensor([1, 5, 6], dtype=torch.int32, device="cuda")
+    before = pool.clone()
+    o = kda.prefill_slots(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], pool, final_slots,
+                          init_slots, check_status=True, streamed=True)
+    torch.cuda.synchronize()
+    s0 = torch.stack([before[4], torch.zeros_like(before[0]), before[0]]).cpu()
+    ref_inp = dict(inp)
+    ref_inp["init_state"] = s0
+    o_ref, fs_ref = oracle_prefill(ref_inp)
+    fs = torch.stack([pool[1], pool[5], pool[6]])
+    assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, "bf16", w.name)
+    for s in (0, 2, 3, 4):
+        assert torch.equal(pool[s], before[s])
+
+
+def test_prefill_path_of_the_benchmark_shapes():
+    """kda_prefill_path on the device: by default the single-sequence H = 32 workloads run the
+    two kernels and with KDA_FLAG_STREAM stream (32 units); a 16-sequence pack (512 units)
+    runs the two kernels with the flag too, and four heads over 65,536 tokens take the
+    sequence split either way."""
+    def path(N, T, H, flags=0):
+        ws = kda.kda_prefill_workspace_size(N, T, H, 128, 128, kda.KDA_DTYPE_BF16)
+        return kda.kda_prefill_path(N, T, H, 128, 128, kda.KDA_DTYPE_BF16, ws, flags)
+    S = kda.KDA_FLAG_STREAM
+    assert path(1, 4096, 32) == kda.KDA_PATH_TWO_KERNEL
+    assert path(1, 4096, 32, S) == kda.KDA_PATH_STREAMED
+    assert path(1, 65536, 32, S) == kda.KDA_PATH_STREAMED
+    assert path(16, 168023, 32, S) == kda.KDA_PATH_TWO_KERNEL
+    assert path(1, 65536, 4) == kda.KDA_PATH_SEQ_SPLIT
+    assert path(1, 65536, 4, S) == kda.KDA_PATH_SEQ_SPLIT
