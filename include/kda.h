@@ -114,7 +114,7 @@ size_t kda_prefill_workspace_size_segmented(int32_t num_seqs, int64_t total_toke
  *  KDA_PATH_TWO_KERNEL the chunk kernel, then the state pass
  *  KDA_PATH_SEQ_SPLIT  the chunk kernel, then the sequence-split state pass
  *  KDA_PATH_SEGMENTED  the chunk kernel and the state pass over segments of records
- *  KDA_PATH_STREAMED   chunk work and state walk in one launch (KDA_FLAG_STREAM)
+ *  KDA_PATH_STREAMED   chunk work and state walk in one launch (see KDA_FLAG_NO_STREAM)
  * Host arithmetic plus one device-attribute query (the SM count of the current
  * device); returns a negative kda_status_t for arguments kda_prefill_ex rejects on
  * the host.  Each path also runs the schedule kernel first.
@@ -153,8 +153,8 @@ int32_t kda_prefill_path(int32_t num_seqs, int64_t total_tokens, int32_t num_hea
  *  workspace   device buffer owned by the caller, 256-byte aligned, reused by every
  *              call.  With kda_prefill_workspace_size(...) bytes or more the bf16,
  *              d = 128 prefill runs as two kernels (chunk-local products for all
- *              chunks at once, then the serial state pass; with KDA_FLAG_STREAM and
- *              few (sequence, head) units, both in one launch; kda_prefill_path tells
+ *              chunks at once, then the serial state pass; with few (sequence, head)
+ *              units both in one launch, see KDA_FLAG_NO_STREAM; kda_prefill_path tells
  *              which); with less, but at least
  *              kda_prefill_workspace_size_segmented(..., 1) bytes, as the same two
  *              kernels over segments of chunks (bounded records, identical results);
@@ -246,18 +246,16 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
  *                        state, and the segments then run at once.  The results agree
  *                        with the unsplit pass to within rounding, not bit for bit. */
 #define KDA_FLAG_NO_SEQ_SPLIT 4u
-/*  KDA_FLAG_STREAM        run the chunk work and the state pass in one launch: when a
- *                        bf16 d = 128 problem has at most 64 (sequence, head) units, no
- *                        sequence split and a workspace that holds every record, a few
- *                        CTAs walk the state of one unit each while the others do the
- *                        chunk work, and each record is handed over through a ready flag
- *                        in the workspace as soon as its stores are complete (otherwise
- *                        the flag changes nothing).  The two forms agree to within
- *                        rounding, not bit for bit (the streamed walk forms its products
- *                        transposed).  Off by default: on one GB300 the walk, one chunk
- *                        after another, is slower than the separate state pass (T = 4096,
- *                        H = 32: 0.185 against 0.161 ms per call). */
-#define KDA_FLAG_STREAM 8u
+/*  KDA_FLAG_NO_STREAM     run the chunk kernel and the state pass one after the other.
+ *                        By default, when a bf16 d = 128 problem has at most 32 (sequence,
+ *                        head) units, no sequence split and a workspace that holds every
+ *                        record, both run in one launch: two CTAs walk the state of each
+ *                        unit (64 value columns each) while the others do the chunk work,
+ *                        and each record is handed over through a ready flag in the
+ *                        workspace as soon as its stores are complete.  The two forms
+ *                        agree to within rounding, not bit for bit (the walk forms its
+ *                        products transposed). */
+#define KDA_FLAG_NO_STREAM 8u
 
 /* kda_prefill with options (flags above); flags = 0 is kda_prefill. */
 kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, const float *log_alpha,
@@ -439,9 +437,9 @@ int32_t kda_prefill_host_segments(const int32_t *cu_seqlens, int32_t num_seqs, i
  *        1: the state kernel's chain and output groups of one chunk and 64-column value
  *           slice (P V, N S, P2 V, Q' S), 4,718,592 FLOP per repetition, one CTA per SM,
  *           each group issued by a thread of its own warp;
- *        2: the streamed kernel's walk group of one chunk and a whole head (the same four
- *           products transposed, S^T read from TMEM, as one N = 192 group), 9,437,184 FLOP
- *           per repetition, one CTA per SM, one issuing thread
+ *        2: the streamed kernel's walk group of one chunk and 64 value columns (the same
+ *           four products transposed, S^T read from TMEM, as one M = 64, N = 192 group),
+ *           4,718,592 FLOP per repetition, one CTA per SM, one issuing thread
  *  reps      repetitions per CTA, 1 .. 2^20
  *  workspace 256-byte aligned device memory of at least 4 bytes (status word, cleared)
  *  tflops    receives the executed TFLOP/s over the whole GPU (CUDA events on `stream`)

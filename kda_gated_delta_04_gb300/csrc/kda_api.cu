@@ -91,7 +91,7 @@ int32_t path_for(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int3
         if (!(flags & KDA_FLAG_NO_SEQ_SPLIT) && workspace_bytes >= ws_split_bytes(num_seqs, total_tokens, num_heads) &&
             kda::seqsplit_lseg(num_seqs, total_tokens, num_heads) > 0)
             return KDA_PATH_SEQ_SPLIT;
-        if ((flags & KDA_FLAG_STREAM) && kda::prefill_stream_fits((int64_t)num_seqs * num_heads))
+        if (!(flags & KDA_FLAG_NO_STREAM) && kda::prefill_stream_fits((int64_t)num_seqs * num_heads))
             return KDA_PATH_STREAMED;
         return KDA_PATH_TWO_KERNEL;
     }
@@ -114,7 +114,7 @@ kda_status_t check_shape(int32_t d_k, int32_t d_v, kda_dtype_t dtype)
 
 // every option bit of the _ex / _slots calls
 constexpr uint32_t kKnownFlags =
-    KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM | KDA_FLAG_NO_SEQ_SPLIT | KDA_FLAG_STREAM;
+    KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM | KDA_FLAG_NO_SEQ_SPLIT | KDA_FLAG_NO_STREAM;
 
 extern "C" {
 
@@ -214,7 +214,7 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     p.chunk_bound = split ? (int)chunk_bound(num_seqs, total_tokens) : 0;
     const size_t after_desc = ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) + ws_desc_bytes(num_seqs, total_tokens);
     if (full) {
-        if (flags & KDA_FLAG_STREAM) p.flags = reinterpret_cast<int *>(ws + after_desc);
+        if (!(flags & KDA_FLAG_NO_STREAM)) p.flags = reinterpret_cast<int *>(ws + after_desc);
         p.records = ws + after_desc + ws_flags_bytes(num_seqs, total_tokens, num_heads);
     } else if (segmented) {
         p.carry = reinterpret_cast<float *>(ws + after_desc);

@@ -308,9 +308,10 @@ __device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, un
 // (STREAM: chunks first to last, each record published by a release store of its flag,
 // flags[g * H + h] = 1, once its bulk stores are complete).  Items past the last packed
 // chunk (the chunk count is an upper bound) are skipped.  Records are indexed from g_base.
-// With STREAM the items are not strided but claimed in order from the counter *claim (one
-// item ahead of the one in work), so the items taken are always the earliest not yet taken,
-// whichever CTAs are resident.
+// With STREAM the items are not strided but claimed in order from the counter *claim, the
+// next one while the current item is in work (after its first barrier), so the items taken
+// are always the earliest not yet taken, whichever CTAs are resident, and finish about in
+// the order they were claimed.
 // NORM: q and k arrive raw and are L2-normalised here (KDA_FLAG_QK_L2NORM).
 template <bool NORM, bool STREAM>
 __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
@@ -327,7 +328,7 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
     __shared__ uint32_t tmem_holder;
     __shared__ __align__(16) float s_beta[kC];
     __shared__ float s_rn[2 * kC];  // reciprocal k, q row norms (NORM)
-    __shared__ int s_claim[2];      // STREAM: the item in work and the next one claimed
+    __shared__ int s_claim;         // STREAM: the item claimed next
 
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
@@ -348,12 +349,9 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
     int h = 0, g = 0;
     int2 dsc = make_int2(0, 0);
     if (STREAM) {
-        if (tid == 0) {
-            s_claim[0] = atomicAdd(claim, 1);
-            s_claim[1] = atomicAdd(claim, 1);
-        }
+        if (tid == 0) s_claim = atomicAdd(claim, 1);
         __syncthreads();
-        it0 = s_claim[0];
+        it0 = s_claim;
     }
     int it = next_item(it0, h, g, dsc);
     // q and k boxes, and (per-channel gate) the log_alpha box into O1, which is free until
@@ -389,7 +387,7 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
         // the next item, so that its descriptor load overlaps this item's work
         int hn = 0, gn = 0;
         int2 dn = make_int2(0, 0);
-        const int itn = next_item(STREAM ? s_claim[1] : it + stride, hn, gn, dn);
+        int itn = STREAM ? items : next_item(it + stride, hn, gn, dn);
         const uint32_t pm = (3u * n) & 1u;  // bar_mma completes three times per item
         if (tid < kC) s_beta[tid] = tid < len ? beta[(size_t)(c0 + tid) * H + h] : 0.f;
         float2 gl[4096 / NT];
@@ -403,8 +401,7 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
             prefix_scan<NT>(reinterpret_cast<const float *>(sm + L::O1), kD, len, s_tot, gl, gmin, gmax);
         // every thread is past its reads of the log_alpha box and s_tot is complete
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
-        // every thread has read the claim of the next item: claim the one after it
-        if (STREAM && tid == 0) s_claim[1] = atomicAdd(claim, 1);
+        if (STREAM && tid == 0) s_claim = atomicAdd(claim, 1);  // the next item
         if (NORM) {
             if (compute) qk_row_inv_norms<NT>(sm + L::IN_K, sm + L::IN_Q, s_rn);
             __syncthreads();
@@ -416,6 +413,7 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
                                                         s_rn);
         fence_proxy_async_smem();
         __syncthreads();
+        if (STREAM) itn = next_item(s_claim, hn, gn, dn);  // its descriptor, for its boxes at the end
         if (issuer) {
             tc_fence_after_sync();
             issue_g1<L>(sb, tmem);
@@ -912,11 +910,12 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
 // always run beside them.  Every wait is bounded all the same (a flag that does not come
 // up within the limit is recorded as KDA_ERR_TIMEOUT and the CTA unwinds).
 //
-// The walker forms the transposed products, so that a whole head fits in a CTA of the
-// chunk work's size.  With S^T (value column j x key row i) as the A operand, the state
-// update and the outputs share their A operands and run as one product group:
+// Two walkers share a head, each with 64 of its value columns (the columns of S evolve
+// independently), and each forms the transposed products, so that its part fits in a CTA
+// of the chunk work's size.  With S^T (value column j x key row i) as the A operand, the
+// state update and the outputs share their A operands and run as one product group:
 //   [S_{c+1}^T | o_c^T] = [gamma_c . S_c^T | 0] + V_c^T [P_c^T | P2_c^T] + S_c^T [N_c^T | Q'_c^T]
-// (M = 128 rows j; N = 128 key rows i for the state and 64 tokens t for the outputs, 192 in
+// (M = 64 rows j; N = 128 key rows i for the state and 64 tokens t for the outputs, 192 in
 // all).  The record's P, P2, N and Q' images (rows over their first index, K-major over
 // the second) are the B operands; the walker copies them so that P and P2, and each K panel
 // of N and Q', sit back to back as 192-row operands.  TMEM holds the state itself: the
@@ -928,9 +927,9 @@ struct WalkLayout {
     // the record in use: [N panel 0 | Q' panel 0 | N panel 1 | Q' panel 1 | P | P2]
     static constexpr uint32_t NQ = 0, NQ_PANEL = 24576;  // 192 rows x 128 bytes per K panel
     static constexpr uint32_t PP = 2 * NQ_PANEL;         // P (128 rows) then P2 (64 rows)
-    static constexpr uint32_t VT = PP + 24576;           // V^T fp16, 128 rows (j) x K 64 (t)
-    static constexpr uint32_t VBOX = VT + kC * kD * 2;   // raw v box [64 tokens][128] bf16
-    static constexpr uint32_t GAM = VBOX + kC * kD * 2;  // gamma of two chunks, 2 x 128 fp32
+    static constexpr uint32_t VT = PP + 24576;           // V^T fp16, 64 rows (j) x K 64 (t)
+    static constexpr uint32_t VBOX = VT + kC * 64 * 2;   // raw v box [64 tokens][64] bf16
+    static constexpr uint32_t GAM = VBOX + kC * 64 * 2;  // gamma of two chunks, 2 x 128 fp32
     static constexpr uint32_t USED = GAM + 2 * kD * 4;
 };
 static_assert(WalkLayout::NQ_PANEL % 1024 == 0 && WalkLayout::PP % 1024 == 0 && WalkLayout::VT % 1024 == 0 &&
@@ -939,39 +938,57 @@ static_assert(WalkLayout::NQ_PANEL % 1024 == 0 && WalkLayout::PP % 1024 == 0 && 
 static_assert(R_P2 == R_P + 16384, "P2 follows P in the record");
 constexpr uint32_t kStreamSmem =
     (WalkLayout::USED > ChunkLayout::USED ? WalkLayout::USED : ChunkLayout::USED) + 1024;
-// walker TMEM columns: accumulator (state 0-127, outputs 128-191), bf16 S^T
+// walker TMEM columns: accumulator (state 0-127, outputs 128-191), bf16 S^T.  An M = 64
+// operand or accumulator keeps its row r in lane 32 (r / 16) + r % 16 (lanes 0-15 of each
+// lane quarter); the walker's warps reach them with the 16-lane load and store shapes.
 constexpr uint32_t TW_D = 0, TW_O = 128, TW_A = 192, kWalkTmem = 256;
 constexpr int kWalkStateWarps = 8;
-constexpr int kMaxWalkers = 64;  // (sequence, head) units the streamed prefill takes at most
+constexpr int kWalkCols = 64;    // value columns per walker: two walkers per (sequence, head)
+constexpr int kMaxWalkers = 64;  // walker CTAs of the streamed prefill at most (32 units)
 
 // The product group of one chunk: D += V^T [P^T | P2^T] (fp16) + S^T [N^T | Q'^T] (bf16, S^T
-// from TMEM), N = 192, or N = 128 (state only) without the outputs.
-__device__ __forceinline__ void issue_walk(uint32_t tmem, uint32_t sb, bool with_o)
+// from TMEM), M = 64, N = 192, or N = 128 (state only) without the outputs; in two parts,
+// the V^T products first (their operands, P and P2, arrive first).
+__device__ __forceinline__ void issue_walk_pv(uint32_t tmem, uint32_t sb, bool with_o)
 {
-    const uint32_t id_pv = with_o ? idesc_f16(128, 192, false, false) : idesc_f16(128, 128, false, false);
-    const uint32_t id_ns = with_o ? idesc_bf16(128, 192, false, false) : idesc_bf16(128, 128, false, false);
-    const uint64_t dvt = kdesc(sb + WalkLayout::VT), dp = kdesc(sb + WalkLayout::PP), dn = kdesc(sb + WalkLayout::NQ);
+    const uint32_t id_pv = with_o ? idesc_f16(64, 192, false, false) : idesc_f16(64, 128, false, false);
+    const uint64_t dvt = kdesc(sb + WalkLayout::VT), dp = kdesc(sb + WalkLayout::PP);
 #pragma unroll
     for (int s = 0; s < 4; ++s) mma_bf16(tmem + TW_D, dvt + 2 * s, dp + 2 * s, id_pv, 1);
+}
+__device__ __forceinline__ void issue_walk_ns(uint32_t tmem, uint32_t sb, bool with_o)
+{
+    const uint32_t id_ns = with_o ? idesc_bf16(64, 192, false, false) : idesc_bf16(64, 128, false, false);
+    const uint64_t dn = kdesc(sb + WalkLayout::NQ);
 #pragma unroll
     for (int s = 0; s < 8; ++s)
         mma_tmem_a(tmem + TW_D, tmem + TW_A + 8 * s, dn + (((s >> 2) * WalkLayout::NQ_PANEL + (s & 3) * 32) >> 4),
                    id_ns, 1);
 }
+__device__ __forceinline__ void issue_walk(uint32_t tmem, uint32_t sb, bool with_o)
+{
+    issue_walk_pv(tmem, sb, with_o);
+    issue_walk_ns(tmem, sb, with_o);
+}
 
-// One walker CTA over one unit.  Warps 0-7 move the state through TMEM (value column j =
-// 32 (warp & 3) + lane, key rows 64 (warp >> 2) .. + 63), write the outputs and convert
-// the v boxes; lane 0 of warp 8 waits for the records' flags, copies the records and issues
-// the product group.  Per chunk c:
-//   warp 8    waits ready(c) and record c; loads the v box of c + 1; issues the group (commit
-//             w_mma); copies record c + 1 once w_mma(c) holds (its flag was seen a chunk
-//             earlier); then waits for the flag of record c + 2 and copies its gamma.
-//   warps 0-7 wait w_mma(c); read o_c into registers and zero the output columns; read
-//             S_{c+1} from D, store bf16(S_{c+1}) and gamma_{c+1} . S_{c+1} back; convert the
-//             v box of c + 1; arrive on ready(c + 1); then store o_c while the next group runs.
+// One walker CTA over one (sequence, head, value half).  Warps 0-7 move the state through
+// TMEM, write the outputs and convert the v boxes: warp w holds rows r = 16 (w & 3) + l of
+// the half (value column j = 64 half + r) in TMEM lane 32 (w & 3) + l, l = lane & 15, and
+// key rows 64 (w >> 2) + 32 (lane >> 4) .. + 31.  Lane 0 of warp 8 copies the records and
+// the v boxes and issues the product group; lane 0 of warp 0 waits for the records' flags
+// and copies the gammas.  Per chunk c:
+//   warp 8    waits ready(c) and record c (P and P2, then N and Q'); issues the group
+//             (commit w_mma); loads the v box of c + 2 once that of c + 1 is read (w_vfree);
+//             copies record c + 1 once w_mma(c) holds (its flag was seen before ready(c)).
+//   warps 0-7 read the v box of c + 1 into registers (arrive w_vfree); lane 0 of warp 0
+//             waits for record c + 2's flag and, its buffer being free after ready(c), copies
+//             its gamma and prefetches the record into L2; all wait w_mma(c); store V^T of
+//             c + 1; read S_{c+1} from D, store bf16(S_{c+1}) and gamma_{c+1} . S_{c+1} back;
+//             read o_c into registers and zero the output columns; arrive on ready(c + 1);
+//             then store o_c while the next group runs.
 // Every barrier's producer stays within one phase of its consumers (each refill waits for
 // the consumption of what it overwrites), so no wait is ever more than one phase behind.
-__device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, const int32_t *__restrict__ cu,
+__device__ __forceinline__ void walk_unit(int walker, const CUtensorMap &tm_v, const int32_t *__restrict__ cu,
                                           int64_t total, int H, const int32_t *__restrict__ cc,
                                           const unsigned char *__restrict__ records, const int *flags,
                                           const float *init_state, __nv_bfloat16 *__restrict__ o, float *final_state,
@@ -979,23 +996,26 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
 {
     using L = WalkLayout;
     extern __shared__ unsigned char smem_raw[];
-    __shared__ __align__(8) uint64_t w_ready, w_mma, w_rec, w_v, w_vfree, w_g[2], w_drain;
+    __shared__ __align__(8) uint64_t w_ready, w_mma, w_rec, w_pp, w_v, w_vfree, w_g[2], w_drain;
     __shared__ uint32_t w_tmem;
     unsigned char *sm = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(sm);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const bool state_warp = warp < kWalkStateWarps, ctl_warp = warp == kWalkStateWarps;
-    const int n = unit / H, h = unit % H;
+    const int half = walker & 1, unit = walker >> 1, n = unit / H, h = unit % H;
     int64_t t0, t1;
     seq_range(cu, n, total, t0, t1);
     const int nch = (int)((t1 - t0 + kC - 1) / kC);
     int64_t si, sf;
-    if (!state_entries(slots, n, init_state != nullptr, si, sf) && tid == 0) atomicOr(status, DEV_ERR_SLOT);
-    const int jrow = (warp & 3) * 32 + lane, ib = 64 * ((warp >> 2) & 1);
+    if (!state_entries(slots, n, init_state != nullptr, si, sf) && tid == 0 && half == 0)
+        atomicOr(status, DEV_ERR_SLOT);
+    const int part = (warp >> 2) & 1, hs = lane >> 4;
+    const int jrow = kWalkCols * half + 16 * (warp & 3) + (lane & 15);  // this thread's value column
+    const int ib = 64 * part + 32 * hs;                                 // its key rows ib .. ib + 31
     const size_t st_entry = (size_t)H * kD * kD, st_head = (size_t)h * kD * kD;
     if (nch == 0) {  // no tokens: the final state is the initial one
         if (state_warp && sf >= 0)
-            for (int i = ib; i < ib + 64; ++i)
+            for (int i = ib; i < ib + 32; ++i)
                 final_state[sf * st_entry + st_head + (size_t)i * kD + jrow] =
                     si >= 0 ? init_state[si * st_entry + st_head + (size_t)i * kD + jrow] : 0.f;
         return;
@@ -1008,6 +1028,7 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
         mbar_init(&w_ready, kWalkStateWarps);
         mbar_init(&w_mma, 1);
         mbar_init(&w_rec, 1);
+        mbar_init(&w_pp, 1);
         mbar_init(&w_v, 1);
         mbar_init(&w_vfree, kWalkStateWarps);
         mbar_init(&w_g[0], 1);
@@ -1025,7 +1046,8 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
     const uint32_t tmem = w_tmem;
     const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
 
-    // copies: issued by lane 0 of warp 8 only, which alone keeps these counts
+    // copies: the records and v boxes issued by lane 0 of warp 8, the gammas by lane 0 of
+    // warp 0; each keeps its own counts
     int rec_issued = 0, v_issued = 0, g_issued = 0;
     auto wait_flag = [&](int c) -> bool {  // record c is complete in global memory
         const int *f = flag0 + (size_t)c * H;
@@ -1045,44 +1067,45 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
         bulk_load(sm + L::GAM + (c & 1) * kD * 4, rec0 + (size_t)c * rec_stride + R_GM, kD * 4, &w_g[c & 1]);
         g_issued = c + 1;
     };
-    auto load_record = [&](int c) {  // N, P (and with outputs Q', P2) as the group's operands
+    // N, P (and with outputs Q', P2) as the group's operands: P and P2 first (w_pp), then
+    // N and Q' (w_rec)
+    auto load_record = [&](int c) {
         const unsigned char *r = rec0 + (size_t)c * rec_stride;
-        mbar_arrive_expect_tx(&w_rec, o ? 73728u : 49152u);
+        mbar_arrive_expect_tx(&w_pp, o ? 24576u : 16384u);
+        bulk_load(sm + L::PP, r + R_P, o ? 24576u : 16384u, &w_pp);  // P2 follows P in both
+        mbar_arrive_expect_tx(&w_rec, o ? 49152u : 32768u);
         bulk_load(sm + L::NQ, r + R_N, 16384, &w_rec);
         bulk_load(sm + L::NQ + L::NQ_PANEL, r + R_N + 16384, 16384, &w_rec);
-        bulk_load(sm + L::PP, r + R_P, 16384, &w_rec);
         if (o) {
             bulk_load(sm + L::NQ + 16384, r + R_Q, 8192, &w_rec);
             bulk_load(sm + L::NQ + L::NQ_PANEL + 16384, r + R_Q + 8192, 8192, &w_rec);
-            bulk_load(sm + L::PP + 16384, r + R_P2, 8192, &w_rec);
         }
         rec_issued = c + 1;
     };
-    auto load_v = [&](int c) {
-        mbar_arrive_expect_tx(&w_v, kC * kD * 2);
-        tma_load_3d(sm + L::VBOX, &tm_v, &w_v, 0, h, (int)(t0 + (int64_t)c * kC));
+    auto load_v = [&](int c) {  // this half's 64 value columns of the chunk's 64 tokens
+        mbar_arrive_expect_tx(&w_v, kC * kWalkCols * 2);
+        tma_load_3d(sm + L::VBOX, &tm_v, &w_v, kWalkCols * half, h, (int)(t0 + (int64_t)c * kC));
         v_issued = c + 1;
     };
     bool range_ok = true;
-    // state warps (whole warps; every wait result is made uniform over the warp, as the
-    // TMEM loads and stores are warp-collective): the v box of chunk c -> V^T fp16, K-major
-    // rows j, 128-byte swizzle; rows past the unit's last token read as zero
-    // The box is read into registers (vt) as soon as it arrives, and the warp then
-    // arrives on w_vfree; the registers go to the V^T image once the products reading it
-    // are done.
-    const int vj = tid & (kD - 1), vs0 = (tid >> 7) * 32;  // V^T row j, tokens vs0 .. vs0 + 31
-    auto read_v = [&](int c, uint4 (&vt)[4]) -> bool {
+    // State warps (whole warps; every wait result is made uniform over the warp, as the
+    // TMEM loads and stores are warp-collective).  The v box is read into registers (vt) as
+    // soon as it arrives, the warp then arrives on w_vfree, and the registers go to the V^T
+    // image (fp16, K-major rows j, 128-byte swizzle) once the products reading it are done;
+    // rows past the unit's last token read as zero.
+    const int vj = tid & (kWalkCols - 1), vs0 = (tid >> 6) * 16;  // V^T row vj, tokens vs0 .. + 15
+    auto read_v = [&](int c, uint4 (&vt)[2]) -> bool {
         if (!__all_sync(0xffffffffu, mbar_wait_ns(&w_v, (uint32_t)(c & 1), kWaitNs))) return false;
         const int64_t cs = t0 + (int64_t)c * kC;
         const int lenc = (t1 - cs) < kC ? (int)(t1 - cs) : kC;
         const unsigned char *box = sm + L::VBOX;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int q = 0; q < 2; ++q) {
             float x[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int s = vs0 + 8 * q + u;
-                x[u] = s < lenc ? bf16_at(box + (s * kD + vj) * 2) : 0.f;
+                x[u] = s < lenc ? bf16_at(box + (s * kWalkCols + vj) * 2) : 0.f;
                 range_ok &= fabsf(x[u]) <= 65504.f;
             }
             vt[q] = pack_f16x8_plain(x);
@@ -1091,17 +1114,19 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
         if (lane == 0) mbar_arrive(&w_vfree);  // this warp is done with the box
         return true;
     };
-    auto store_v = [&](const uint4 (&vt)[4]) {
+    auto store_v = [&](const uint4 (&vt)[2]) {
 #pragma unroll
-        for (int q = 0; q < 4; ++q) *reinterpret_cast<uint4 *>(sm + L::VT + km16(vj, vs0 + 8 * q, kD)) = vt[q];
+        for (int q = 0; q < 2; ++q)
+            *reinterpret_cast<uint4 *>(sm + L::VT + km16(vj, vs0 + 8 * q, kWalkCols)) = vt[q];
     };
-    // state warps: 16 key rows i0 .. i0 + 15 of column j: bf16(S) into the A operand,
-    // gamma . S (fp32) into D
-    auto put_state = [&](int i0, float (&x)[16], const float *gam) {
+    // 16 key rows ib + 16 k .. + 15 of this thread's column: bf16(S) into the A operand,
+    // gamma . S (fp32) into D (A column c holds key rows 2c, 2c + 1)
+    auto put_state = [&](int k, float (&x)[16], const float *gam) {
         uint32_t pk[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) pk[u] = pack_bf16x2(x[2 * u], x[2 * u + 1]);
-        tmem_st8(tmem + lane_off + TW_A + i0 / 2, pk);
+        tmem_st16x2_x8<16>(tmem + lane_off + TW_A + 32 * part + 8 * k, pk);
+        const int i0 = ib + 16 * k;
 #pragma unroll
         for (int u = 0; u < 16; u += 4) {
             const float4 g = *reinterpret_cast<const float4 *>(gam + i0 + u);
@@ -1110,15 +1135,18 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
             x[u + 2] *= g.z;
             x[u + 3] *= g.w;
         }
-        tmem_st16(tmem + lane_off + TW_D + i0, x);
+        tmem_st16x2_x16<32>(tmem + lane_off + TW_D + 64 * part + 16 * k, x);
     };
-    // state warps: zeros into this thread's 32 output columns (the group accumulates onto D)
+    auto load_state = [&](int k, float (&x)[16]) {  // the same 16 key rows of D
+        tmem_ld16x2_x16<32>(tmem + lane_off + TW_D + 64 * part + 16 * k, x);
+        tmem_ld_wait();
+    };
+    // zeros into this thread's 16 output columns (the group accumulates onto D)
     auto zero_out = [&]() {
         float z[16];
 #pragma unroll
         for (int u = 0; u < 16; ++u) z[u] = 0.f;
-        tmem_st16(tmem + lane_off + TW_O + ib / 2, z);
-        tmem_st16(tmem + lane_off + TW_O + ib / 2 + 16, z);
+        tmem_st16x2_x16<16>(tmem + lane_off + TW_O + 32 * part, z);
     };
 
     bool ok = true;
@@ -1126,14 +1154,7 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
         if (lane == 0) {
             load_v(0);
             ok = wait_flag(0);
-            if (ok) {
-                load_gamma(0);
-                load_record(0);
-            }
-            if (ok && nch > 1) {
-                ok = wait_flag(1);
-                if (ok) load_gamma(1);
-            }
+            if (ok) load_record(0);
             if (ok && nch > 1) {  // the box of chunk 1, once chunk 0's is read
                 ok = mbar_wait_ns(&w_vfree, 0, kWaitNs);
                 if (ok) load_v(1);
@@ -1141,20 +1162,27 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
     } else if (state_warp) {  // S_0: gamma_0 . S_0 into D, bf16(S_0) into the A operand
-        ok = __all_sync(0xffffffffu, mbar_wait_ns(&w_g[0], 0, kWaitNs));
+        if (warp == 0 && lane == 0) {  // lane 0 of warp 0 loads every gamma (its flag seen first)
+            ok = wait_flag(0);
+            if (ok) load_gamma(0);
+            if (ok && nch > 1) {
+                ok = wait_flag(1);
+                if (ok) load_gamma(1);
+            }
+        }
+        ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait_ns(&w_g[0], 0, kWaitNs));
         const float *gam = reinterpret_cast<const float *>(sm + L::GAM);
         if (ok) {
 #pragma unroll 1
-            for (int q = 0; q < 4; ++q) {
-                const int i0 = ib + 16 * q;
+            for (int k = 0; k < 2; ++k) {
                 float x[16];
 #pragma unroll
                 for (int u = 0; u < 16; ++u)
-                    x[u] = si >= 0 ? init_state[si * st_entry + st_head + (size_t)(i0 + u) * kD + jrow] : 0.f;
-                put_state(i0, x, gam);
+                    x[u] = si >= 0 ? init_state[si * st_entry + st_head + (size_t)(ib + 16 * k + u) * kD + jrow] : 0.f;
+                put_state(k, x, gam);
             }
             if (o) zero_out();
-            uint4 vt[4];
+            uint4 vt[2];
             ok = read_v(0, vt);
             if (ok) store_v(vt);
         }
@@ -1166,12 +1194,14 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
     }
     if (ctl_warp) {
         for (int c = 0; ok && c < nch; ++c) {
-            if (lane == 0) {  // polls (the only thread of its warp at work: the chain's issuer)
+            if (lane == 0) {  // polls (the only thread of its warp at work: the group's issuer)
                 ok = mbar_wait_spin_ns(&w_ready, (uint32_t)(c & 1), kWaitNs) &&
-                     mbar_wait_spin_ns(&w_rec, (uint32_t)(c & 1), kWaitNs);
+                     mbar_wait_spin_ns(&w_pp, (uint32_t)(c & 1), kWaitNs);
                 if (ok) {
                     tc_fence_after_sync();
-                    issue_walk(tmem, sb, o != nullptr);
+                    issue_walk_pv(tmem, sb, o != nullptr);
+                    ok = mbar_wait_spin_ns(&w_rec, (uint32_t)(c & 1), kWaitNs);
+                    if (ok) issue_walk_ns(tmem, sb, o != nullptr);
                     mma_commit(&w_mma);
                 }
                 if (ok && c + 2 < nch) {  // the box of chunk c + 2, once that of c + 1 is read
@@ -1180,45 +1210,47 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
                 }
                 if (ok && c + 1 < nch) {
                     ok = mbar_wait_spin_ns(&w_mma, (uint32_t)(c & 1), kWaitNs);  // record c is read
-                    if (ok) load_record(c + 1);  // its flag was seen a chunk ago
-                    if (ok && c + 2 < nch) {
-                        ok = wait_flag(c + 2);
-                        if (ok) {
-                            load_gamma(c + 2);
-                            // record c + 2 into L2 now (it may have left L2 since it was written)
-                            bulk_prefetch_l2(rec0 + (size_t)(c + 2) * rec_stride, kRecBytes);
-                        }
-                    }
+                    // record c + 1's flag was seen (by lane 0 of warp 0) before ready(c)
+                    fence_proxy_async_global();
+                    if (ok) load_record(c + 1);
                 }
             }
             ok = __shfl_sync(0xffffffffu, ok, 0);
         }
     } else if (state_warp) {
         const int par = lane & 1;  // lane pairs (j, j ^ 1) store two columns of one token
-        uint32_t opk[16];          // o_c, paired bf16 columns, 16 tokens x 2 halves
-        // o_c^T (lane j, tokens ib / 2 ..) into registers, paired over lanes j, j ^ 1; then
-        // zeros into the output columns for the next group
+        const int tb = 32 * part + 16 * hs;  // this thread's output tokens tb .. tb + 15
+        uint32_t opk[8];           // o_c, paired bf16 columns, 8 token pairs
+        // o_c^T (row j, tokens tb ..) into registers, paired over lanes j, j ^ 1; then zeros
+        // into the output columns for the next group
         auto read_o = [&]() {
+            float v[16];
+            tmem_ld16x2_x16<16>(tmem + lane_off + TW_O + 32 * part, v);
+            tmem_ld_wait();
 #pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-                float v[16];
-                tmem_ld16(tmem + lane_off + TW_O + ib / 2 + 16 * hh, v);
-                tmem_ld_wait();
-#pragma unroll
-                for (int k = 0; k < 8; ++k) {
-                    // even lane: (own, partner's) at token 2k; odd lane: (partner's, own) at 2k + 1
-                    const float mine = par ? v[2 * k + 1] : v[2 * k];
-                    const float other = __shfl_xor_sync(0xffffffffu, par ? v[2 * k] : v[2 * k + 1], 1);
-                    opk[8 * hh + k] = par ? pack_bf16x2(other, mine) : pack_bf16x2(mine, other);
-                }
+            for (int k = 0; k < 8; ++k) {
+                // even lane: (own, partner's) at token 2k; odd lane: (partner's, own) at 2k + 1
+                const float mine = par ? v[2 * k + 1] : v[2 * k];
+                const float other = __shfl_xor_sync(0xffffffffu, par ? v[2 * k] : v[2 * k + 1], 1);
+                opk[k] = par ? pack_bf16x2(other, mine) : pack_bf16x2(mine, other);
             }
             zero_out();
         };
         for (int c = 0; ok && c < nch; ++c) {
             const int64_t cs = t0 + (int64_t)c * kC;
-            uint4 vt[4];  // the next chunk's V^T, read while this chunk's products run
+            uint4 vt[2];  // the next chunk's V^T, read while this chunk's products run
             if (c + 1 < nch) ok = read_v(c + 1, vt);
-            ok = ok && __all_sync(0xffffffffu, mbar_wait_ns(&w_mma, (uint32_t)(c & 1), kWaitNs));
+            if (ok && warp == 0 && lane == 0 && c + 2 < nch) {
+                // while this chunk's products run: record c + 2's flag, then (its buffer is
+                // free once every state warp is past chunk c - 1: ready(c)) its gamma, and the
+                // record into L2 (it may have left L2 since it was written)
+                ok = wait_flag(c + 2) && mbar_wait_ns(&w_ready, (uint32_t)(c & 1), kWaitNs);
+                if (ok) {
+                    load_gamma(c + 2);
+                    bulk_prefetch_l2(rec0 + (size_t)(c + 2) * rec_stride, kRecBytes);
+                }
+            }
+            ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait_ns(&w_mma, (uint32_t)(c & 1), kWaitNs));
             tc_fence_after_sync();
             if (ok && c + 1 < nch) store_v(vt);  // V^T of chunk c is no longer read
             if (c + 1 < nch) {
@@ -1226,12 +1258,10 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
                 if (ok) {
                     const float *gam = reinterpret_cast<const float *>(sm + L::GAM + ((c + 1) & 1) * kD * 4);
 #pragma unroll 1
-                    for (int q = 0; q < 4; ++q) {
-                        const int i0 = ib + 16 * q;
+                    for (int k = 0; k < 2; ++k) {
                         float x[16];
-                        tmem_ld16(tmem + lane_off + TW_D + i0, x);
-                        tmem_ld_wait();
-                        put_state(i0, x, gam);
+                        load_state(k, x);
+                        put_state(k, x, gam);
                     }
                 }
                 if (ok && o) read_o();
@@ -1243,36 +1273,41 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
             } else if (ok) {
                 if (o) read_o();
 #pragma unroll 1
-                for (int q = 0; q < 4 && sf >= 0; ++q) {  // the final state S_T is D
-                    const int i0 = ib + 16 * q;
+                for (int k = 0; k < 2 && sf >= 0; ++k) {  // the final state S_T is D
                     float x[16];
-                    tmem_ld16(tmem + lane_off + TW_D + i0, x);
-                    tmem_ld_wait();
+                    load_state(k, x);
 #pragma unroll
-                    for (int u = 0; u < 16; ++u) final_state[sf * st_entry + st_head + (size_t)(i0 + u) * kD + jrow] = x[u];
+                    for (int u = 0; u < 16; ++u)
+                        final_state[sf * st_entry + st_head + (size_t)(ib + 16 * k + u) * kD + jrow] = x[u];
                 }
             }
             if (ok && o) {  // the outputs of chunk c, while the next chunk's products run
                 __nv_bfloat16 *orow = o + (size_t)h * kD + (jrow & ~1);
 #pragma unroll
-                for (int e = 0; e < 16; ++e) {
-                    const int64_t t = cs + ib / 2 + 16 * (e >> 3) + 2 * (e & 7) + par;
-                    if (t < t1) *reinterpret_cast<uint32_t *>(orow + (size_t)t * H * kD) = opk[e];
+                for (int k = 0; k < 8; ++k) {
+                    const int64_t t = cs + tb + 2 * k + par;
+                    if (t < t1) *reinterpret_cast<uint32_t *>(orow + (size_t)t * H * kD) = opk[k];
                 }
             }
         }
     }
     const bool timed_out = __syncthreads_or(!ok);  // every role has finished or given up
     if (timed_out) {
-        if (tid == 0) atomicOr(status, DEV_ERR_TIMEOUT);
+        if (tid == 0) {
+            atomicOr(status, DEV_ERR_TIMEOUT);
+            // the gamma copies still in flight (lane 0 of warp 0 issues them all)
+            for (int k = g_issued > 2 ? g_issued - 2 : 0; k < g_issued; ++k)
+                (void)mbar_wait_ns(&w_g[k & 1], (uint32_t)((k >> 1) & 1), kWaitNs);
+        }
         if (ctl_warp && lane == 0) {
             mma_commit(&w_drain);  // completes once every MMA issued so far has
             (void)mbar_wait_ns(&w_drain, 0, kWaitNs);
             // our own copies still in flight: the last phase of each barrier
-            if (rec_issued > 0) (void)mbar_wait_ns(&w_rec, (uint32_t)((rec_issued - 1) & 1), kWaitNs);
+            if (rec_issued > 0) {
+                (void)mbar_wait_ns(&w_rec, (uint32_t)((rec_issued - 1) & 1), kWaitNs);
+                (void)mbar_wait_ns(&w_pp, (uint32_t)((rec_issued - 1) & 1), kWaitNs);
+            }
             if (v_issued > 0) (void)mbar_wait_ns(&w_v, (uint32_t)((v_issued - 1) & 1), kWaitNs);
-            for (int k = g_issued > 2 ? g_issued - 2 : 0; k < g_issued; ++k)
-                (void)mbar_wait_ns(&w_g[k & 1], (uint32_t)((k >> 1) & 1), kWaitNs);
         }
     }
     if (!range_ok) atomicOr(status, DEV_ERR_RANGE);
@@ -1281,7 +1316,8 @@ __device__ __forceinline__ void walk_unit(int unit, const CUtensorMap &tm_v, con
     if (warp == 0) tmem_dealloc(tmem, kWalkTmem);
 }
 
-// The streamed prefill: walkers (blockIdx.x < n_walk) and chunk workers in one grid.
+// The streamed prefill: walkers (blockIdx.x < n_walk, two per (sequence, head)) and chunk
+// workers in one grid.
 template <bool NORM>
 __global__ void __launch_bounds__(kChunkThreads, 2)
 prefill_stream_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
@@ -1311,12 +1347,13 @@ prefill_stream_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
 // P2, the three-term P, N, Q''), issued by one thread, two CTAs per SM as that kernel runs.
 // PASS 1: the state kernel's chain and output groups of one chunk and 64-column slice,
 // one CTA per SM, each group issued by a thread of its own warp as in that kernel.
-// PASS 2: the streamed kernel's walk group of one chunk (whole head, S^T from TMEM, the
-// state and output products as one N = 192 group), one CTA per SM, one issuing thread.
+// PASS 2: the streamed kernel's walk group of one chunk (64 value columns, S^T from TMEM,
+// the state and output products as one M = 64, N = 192 group), one CTA per SM, one issuing
+// thread.
 constexpr uint64_t kDiagFlops[3] = {
     2ull * (128 * 64 * 128 + 64 * 128 * 64 + 64 * 64 * 64 + 3 * 128 * 64 * 64 + 128 * 128 * 64 + 64 * 128 * 64),
     2ull * (128 * 64 * 64 + 128 * 64 * 128 + 64 * 64 * 64 + 64 * 64 * 128),
-    2ull * (128 * 128 * 64 + 128 * 128 * 128 + 128 * 64 * 64 + 128 * 64 * 128)};
+    2ull * (64 * 192 * 64 + 64 * 192 * 128)};
 using DiagState = StateShape<64>;  // pass 1 measures the 64-column groups
 
 template <int PASS>
@@ -1513,9 +1550,9 @@ cudaError_t launch_stream(const PrefillProblem &p, const CUtensorMap &tq, const 
     cudaError_t err = allow_smem(prefill_stream_kernel<NORM>, (int)kStreamSmem, &dev_cfg);
     if (err != cudaSuccess) return err;
     const int sms = sm_count();
-    if (sms <= 0 || 2 * sms - units < sms) return cudaErrorNotSupported;
-    CUtensorMap tv;  // v boxes of 64 tokens x 128 columns
-    if (!make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kD))
+    if (sms <= 0 || 2 * sms - (kD / kWalkCols) * units < sms) return cudaErrorNotSupported;
+    CUtensorMap tv;  // v boxes of 64 tokens x 64 columns (one walker's value half)
+    if (!make_map(&tv, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.v, p.total_tokens, p.num_heads, 2, kWalkCols))
         return cudaErrorInvalidValue;
     cudaLaunchAttribute pdl;
     pdl.id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -1530,7 +1567,7 @@ cudaError_t launch_stream(const PrefillProblem &p, const CUtensorMap &tq, const 
     return cudaLaunchKernelEx(&cfg, prefill_stream_kernel<NORM>, tq, tk, tla, tv, p.log_alpha, p.beta,
                               (const int2 *)p.desc, p.num_heads, p.chunk_bound, static_cast<unsigned char *>(records),
                               p.flags, p.status, p.scalar_gate, p.cu_seqlens, p.total_tokens, cc, p.init_state,
-                              static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.slots, units);
+                              static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.slots, (kD / kWalkCols) * units);
 }
 
 }  // namespace
@@ -1538,7 +1575,8 @@ cudaError_t launch_stream(const PrefillProblem &p, const CUtensorMap &tq, const 
 bool prefill_stream_fits(int64_t units)
 {
     const int sms = sm_count();  // the walkers leave at least one worker CTA per SM
-    return units >= 1 && units <= kMaxWalkers && sms > 0 && 2 * (int64_t)sms - units >= sms;
+    const int64_t walkers = (kD / kWalkCols) * units;
+    return units >= 1 && walkers <= kMaxWalkers && sms > 0 && 2 * (int64_t)sms - walkers >= sms;
 }
 
 bool prefill_stream_eligible(const PrefillProblem &p)

@@ -336,6 +336,29 @@ __device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t (&u)[8])
                  : "memory");
 }
 
+// Stores of the 16-lane shape (the counterpart of tmem_ld16x2_*): thread t < 16 writes lane
+// (quarter base + t) at columns [c, c + N), thread t >= 16 lane (quarter base + t - 16) at
+// columns [c + HALF, c + HALF + N).
+template <int HALF>
+__device__ __forceinline__ void tmem_st16x2_x8(uint32_t taddr, const uint32_t (&u)[8])
+{
+    asm volatile("tcgen05.st.sync.aligned.16x32bx2.x8.b32 [%0], %1, {%2,%3,%4,%5,%6,%7,%8,%9};" ::"r"(taddr),
+                 "n"(HALF), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]),
+                 "r"(u[7])
+                 : "memory");
+}
+template <int HALF>
+__device__ __forceinline__ void tmem_st16x2_x16(uint32_t taddr, const float (&r)[16])
+{
+    const uint32_t *u = reinterpret_cast<const uint32_t *>(r);
+    asm volatile(
+        "tcgen05.st.sync.aligned.16x32bx2.x16.b32 [%0], %1, "
+        "{%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17};" ::"r"(taddr),
+        "n"(HALF), "r"(u[0]), "r"(u[1]), "r"(u[2]), "r"(u[3]), "r"(u[4]), "r"(u[5]), "r"(u[6]), "r"(u[7]),
+        "r"(u[8]), "r"(u[9]), "r"(u[10]), "r"(u[11]), "r"(u[12]), "r"(u[13]), "r"(u[14]), "r"(u[15])
+        : "memory");
+}
+
 __device__ __forceinline__ void tmem_st_wait()
 {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");

@@ -82,13 +82,13 @@ def test_prefill_path_query(kda):
     streamed and sequence-split choices are checked on the GPU): fp32 and d = 64 take the
     CUDA-core kernel, a bf16 d = 128 call with the minimal workspace the fused kernel, with a
     bounded-records workspace the segmented pass, and with the full workspace the two kernels
-    when the sequence split is turned off.  Rejected arguments give the
+    when streaming and the sequence split are turned off.  Rejected arguments give the
     negated status kda_prefill_ex returns."""
     N, T, H = 1, 4096, 32
     full = kda.kda_prefill_workspace_size(N, T, H, 128, 128, 0)
     seg = kda.kda_prefill_workspace_size_segmented(N, T, H, 128, 128, 0, 4)
     minimal = kda.min_workspace_bytes(N)
-    off = kda.KDA_FLAG_NO_SEQ_SPLIT
+    off = kda.KDA_FLAG_NO_STREAM | kda.KDA_FLAG_NO_SEQ_SPLIT
     assert kda.kda_prefill_path(N, T, H, 128, 128, 1, full, 0) == kda.KDA_PATH_CUDA_CORE
     assert kda.kda_prefill_path(N, T, H, 64, 64, 0, full, 0) == kda.KDA_PATH_CUDA_CORE
     assert kda.kda_prefill_path(N, T, H, 128, 128, 0, minimal, 0) == kda.KDA_PATH_FUSED

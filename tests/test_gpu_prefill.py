@@ -34,7 +34,7 @@ def test_small_problems_match_oracle(w):
     assert_parity(o, fs, o_ref, fs_ref, w.dtype, w.name)
 
 
-def _whole_tensor_parity(w, group, streamed=False):
+def _whole_tensor_parity(w, group, streamed=True):
     """Run the whole workload on the GPU exactly as the benchmark launches it, then check
     every (sequence, head) unit against the oracle, `group` heads at a time (so host memory
     stays bounded): o element by element (max-abs over the whole output), the final state by
@@ -87,14 +87,14 @@ def test_prefill_4k_full_size_every_unit():
     _whole_tensor_parity(synth.PREFILL_4K, group=32)
 
 
-def test_prefill_4k_streamed_full_size_every_unit():
-    """The same workload with the chunk work and the state walk in one launch
-    (KDA_FLAG_STREAM)."""
-    _whole_tensor_parity(synth.PREFILL_4K, group=32, streamed=True)
+def test_prefill_4k_two_kernel_form_full_size_every_unit():
+    """The same workload with the chunk kernel and the state pass one after the other
+    (KDA_FLAG_NO_STREAM): the form of every problem with more (sequence, head) units."""
+    _whole_tensor_parity(synth.PREFILL_4K, group=32, streamed=False)
 
 
-def test_prefill_64k_streamed_full_size_every_unit():
-    _whole_tensor_parity(synth.PREFILL_64K, group=8, streamed=True)
+def test_prefill_64k_two_kernel_form_full_size_every_unit():
+    _whole_tensor_parity(synth.PREFILL_64K, group=8, streamed=False)
 
 
 def test_prefill_64k_with_initial_state_full_size_every_unit():

@@ -1,9 +1,8 @@
-"""The streamed prefill (KDA_FLAG_STREAM: chunk work and state walk in one launch) against
-the oracle and against the two-kernel form on the same inputs.
+"""The streamed prefill (chunk work and state walk in one launch) against the oracle and
+against the two-kernel form (KDA_FLAG_NO_STREAM) on the same inputs.
 
-Every shape here has at most 64 (sequence, head) units and no sequence split, so a call with
-streamed=True takes the streamed kernel; the default runs the chunk kernel and then the state
-pass.
+Every shape here has at most 32 (sequence, head) units and no sequence split, so the default
+call takes the streamed kernel; streamed=False runs the chunk kernel and then the state pass.
 Both are checked element by element against the fp64 oracle; their difference from each
 other is printed (it is rounding only: the walk forms its products transposed)."""
 import numpy as np
@@ -19,7 +18,7 @@ pytestmark = pytest.mark.gpu
 
 CASES = [
     PrefillWorkload("stream_T1000_H32", 300, 32, 128, "bf16", (1000,), 1),
-    PrefillWorkload("stream_two_seqs_H32_64_units", 301, 32, 128, "bf16", (300, 129), 2, init_state=True),
+    PrefillWorkload("stream_two_seqs_H16_32_units", 301, 16, 128, "bf16", (300, 129), 2, init_state=True),
     PrefillWorkload("stream_varlen_edges_H3_state", 302, 3, 128, "bf16", (0, 1, 63, 64, 65, 130), 6,
                     init_state=True),
     PrefillWorkload("stream_T64_H20", 303, 20, 128, "bf16", (64,), 1, init_state=True),
@@ -87,7 +86,7 @@ def test_streamed_prefill_into_state_pool():
     final_slots = torch.tensor([1, 5, 6], dtype=torch.int32, device="cuda")
     before = pool.clone()
     o = kda.prefill_slots(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], pool, final_slots,
-                          init_slots, check_status=True, streamed=True)
+                          init_slots, check_status=True)
     torch.cuda.synchronize()
     s0 = torch.stack([before[4], torch.zeros_like(before[0]), before[0]]).cpu()
     ref_inp = dict(inp)
@@ -100,17 +99,14 @@ def test_streamed_prefill_into_state_pool():
 
 
 def test_prefill_path_of_the_benchmark_shapes():
-    """kda_prefill_path on the device: by default the single-sequence H = 32 workloads run the
-    two kernels and with KDA_FLAG_STREAM stream (32 units); a 16-sequence pack (512 units)
-    runs the two kernels with the flag too, and four heads over 65,536 tokens take the
-    sequence split either way."""
+    """kda_prefill_path on the device: the single-sequence H = 32 workloads (32 units) stream
+    unless KDA_FLAG_NO_STREAM; a 16-sequence pack (512 units) runs the two kernels, and four
+    heads over 65,536 tokens take the sequence split."""
     def path(N, T, H, flags=0):
         ws = kda.kda_prefill_workspace_size(N, T, H, 128, 128, kda.KDA_DTYPE_BF16)
         return kda.kda_prefill_path(N, T, H, 128, 128, kda.KDA_DTYPE_BF16, ws, flags)
-    S = kda.KDA_FLAG_STREAM
-    assert path(1, 4096, 32) == kda.KDA_PATH_TWO_KERNEL
-    assert path(1, 4096, 32, S) == kda.KDA_PATH_STREAMED
-    assert path(1, 65536, 32, S) == kda.KDA_PATH_STREAMED
-    assert path(16, 168023, 32, S) == kda.KDA_PATH_TWO_KERNEL
+    assert path(1, 4096, 32) == kda.KDA_PATH_STREAMED
+    assert path(1, 65536, 32) == kda.KDA_PATH_STREAMED
+    assert path(1, 4096, 32, kda.KDA_FLAG_NO_STREAM) == kda.KDA_PATH_TWO_KERNEL
+    assert path(16, 168023, 32) == kda.KDA_PATH_TWO_KERNEL
     assert path(1, 65536, 4) == kda.KDA_PATH_SEQ_SPLIT
-    assert path(1, 65536, 4, S) == kda.KDA_PATH_SEQ_SPLIT
