@@ -247,7 +247,7 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
  *                        with the unsplit pass to within rounding, not bit for bit. */
 #define KDA_FLAG_NO_SEQ_SPLIT 4u
 /*  KDA_FLAG_NO_STREAM     run the chunk kernel and the state pass one after the other.
- *                        By default, when a bf16 d = 128 problem has at most 32 (sequence,
+ *                        By default, when a bf16 d = 128 problem has 20 to 32 (sequence,
  *                        head) units, no sequence split and a workspace that holds every
  *                        record, both run in one launch: two CTAs walk the state of each
  *                        unit (64 value columns each) while the others do the chunk work,

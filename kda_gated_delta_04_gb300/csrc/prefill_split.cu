@@ -945,6 +945,10 @@ constexpr uint32_t TW_D = 0, TW_O = 128, TW_A = 192, kWalkTmem = 256;
 constexpr int kWalkStateWarps = 8;
 constexpr int kWalkCols = 64;    // value columns per walker: two walkers per (sequence, head)
 constexpr int kMaxWalkers = 64;  // walker CTAs of the streamed prefill at most (32 units)
+// Fewest (sequence, head) units the streamed prefill takes: with fewer, the walk (about 1.9 us
+// per chunk) outlasts the chunk work beside it, and the separate state pass (about 1 us per
+// chunk, or the sequence split) is faster.
+constexpr int kMinStreamUnits = 20;
 
 // The product group of one chunk: D += V^T [P^T | P2^T] (fp16) + S^T [N^T | Q'^T] (bf16, S^T
 // from TMEM), M = 64, N = 192, or N = 128 (state only) without the outputs; in two parts,
@@ -1576,7 +1580,7 @@ bool prefill_stream_fits(int64_t units)
 {
     const int sms = sm_count();  // the walkers leave at least one worker CTA per SM
     const int64_t walkers = (kD / kWalkCols) * units;
-    return units >= 1 && walkers <= kMaxWalkers && sms > 0 && 2 * (int64_t)sms - walkers >= sms;
+    return units >= kMinStreamUnits && walkers <= kMaxWalkers && sms > 0 && 2 * (int64_t)sms - walkers >= sms;
 }
 
 bool prefill_stream_eligible(const PrefillProblem &p)

@@ -1,7 +1,7 @@
 """The streamed prefill (chunk work and state walk in one launch) against the oracle and
 against the two-kernel form (KDA_FLAG_NO_STREAM) on the same inputs.
 
-Every shape here has at most 32 (sequence, head) units and no sequence split, so the default
+Every shape here has 20 to 32 (sequence, head) units and no sequence split, so the default
 call takes the streamed kernel; streamed=False runs the chunk kernel and then the state pass.
 Both are checked element by element against the fp64 oracle; their difference from each
 other is printed (it is rounding only: the walk forms its products transposed)."""
@@ -19,7 +19,7 @@ pytestmark = pytest.mark.gpu
 CASES = [
     PrefillWorkload("stream_T1000_H32", 300, 32, 128, "bf16", (1000,), 1),
     PrefillWorkload("stream_two_seqs_H16_32_units", 301, 16, 128, "bf16", (300, 129), 2, init_state=True),
-    PrefillWorkload("stream_varlen_edges_H3_state", 302, 3, 128, "bf16", (0, 1, 63, 64, 65, 130), 6,
+    PrefillWorkload("stream_varlen_edges_H4_state", 302, 4, 128, "bf16", (0, 1, 63, 64, 65, 130), 6,
                     init_state=True),
     PrefillWorkload("stream_T64_H20", 303, 20, 128, "bf16", (64,), 1, init_state=True),
     PrefillWorkload("stream_T4000_H24_state", 304, 24, 128, "bf16", (4000,), 1, init_state=True),
@@ -100,8 +100,9 @@ def test_streamed_prefill_into_state_pool():
 
 def test_prefill_path_of_the_benchmark_shapes():
     """kda_prefill_path on the device: the single-sequence H = 32 workloads (32 units) stream
-    unless KDA_FLAG_NO_STREAM; a 16-sequence pack (512 units) runs the two kernels, and four
-    heads over 65,536 tokens take the sequence split."""
+    unless KDA_FLAG_NO_STREAM; a 16-sequence pack (512 units) runs the two kernels; four heads
+    over 65,536 tokens take the sequence split, and without it the two kernels (too few
+    units to stream)."""
     def path(N, T, H, flags=0):
         ws = kda.kda_prefill_workspace_size(N, T, H, 128, 128, kda.KDA_DTYPE_BF16)
         return kda.kda_prefill_path(N, T, H, 128, 128, kda.KDA_DTYPE_BF16, ws, flags)
@@ -110,3 +111,6 @@ def test_prefill_path_of_the_benchmark_shapes():
     assert path(1, 4096, 32, kda.KDA_FLAG_NO_STREAM) == kda.KDA_PATH_TWO_KERNEL
     assert path(16, 168023, 32) == kda.KDA_PATH_TWO_KERNEL
     assert path(1, 65536, 4) == kda.KDA_PATH_SEQ_SPLIT
+    assert path(1, 65536, 4, kda.KDA_FLAG_NO_SEQ_SPLIT) == kda.KDA_PATH_TWO_KERNEL
+    assert path(1, 4096, 16) != kda.KDA_PATH_STREAMED
+    assert path(1, 4096, 20) == kda.KDA_PATH_STREAMED
