@@ -68,11 +68,13 @@ typedef enum { KDA_DTYPE_BF16 = 0, KDA_DTYPE_F32 = 1 } kda_dtype_t;
 
 /*
  * Bytes of device workspace for the fastest kda_prefill path on this problem.
- * For bf16 q/k/v at d_k = d_v = 128 that is the two-kernel tensor-core path: a
- * status word, a sequence schedule, the first chunk of each sequence, one 8-byte
- * descriptor per chunk and one 74,240-byte record per (64-token chunk, head), at
- * most (total_tokens / 64 + num_seqs) * num_heads records (about 1.2 KB per
- * token per head); when the problem has so few (sequence, head) units that the
+ * For bf16 q/k/v at d_k = d_v = 128 that is the tensor-core path with per-chunk
+ * records: a status word, a sequence schedule, the first chunk of each sequence,
+ * one 8-byte descriptor per chunk, a 4-byte ready flag per record (for the streamed
+ * form, KDA_FLAG_NO_STREAM) and one item counter, and one 74,240-byte record per
+ * (64-token chunk, head), at most (total_tokens / 64 + num_seqs) * num_heads
+ * records (about 1.2 KB per token per head); when the problem has so few
+ * (sequence, head) units that the
  * state pass runs in segments (KDA_FLAG_NO_SEQ_SPLIT), also three fp32 states
  * per segment and head.  For other shapes it equals
  * KDA_PREFILL_MIN_WORKSPACE(num_seqs).
