@@ -114,3 +114,31 @@ def test_prefill_path_of_the_benchmark_shapes():
     assert path(1, 65536, 4, kda.KDA_FLAG_NO_SEQ_SPLIT) == kda.KDA_PATH_TWO_KERNEL
     assert path(1, 4096, 16) != kda.KDA_PATH_STREAMED
     assert path(1, 4096, 20) == kda.KDA_PATH_STREAMED
+
+
+@pytest.mark.parametrize("case", ["decay", "value", "cu_seqlens"])
+def test_streamed_errors_are_reported_not_faulted(case):
+    """Device-side errors through the streamed kernel (3 sequences x 8 heads = 24 units): a
+    decay outside the supported range (found by a worker), a v value outside the fp16 range
+    (found by a walker converting its box) and a cu_seqlens that is not a prefix sum (found by
+    the schedule kernel; the workers and walkers still agree on the clamped ranges).  Each is
+    recorded in the workspace and the call finishes."""
+    lens, H = [100, 50, 50], 8
+    w = PrefillWorkload(f"stream_err_{case}", 330, H, 128, "bf16", tuple(lens), len(lens))
+    inp = synth.prefill_inputs(w)
+    if case == "decay":
+        inp["log_alpha"] = torch.full_like(inp["log_alpha"], -2.0)
+    if case == "value":
+        inp["v"][37, 5, 5] = 1.0e5
+    d = to_device(inp)
+    if case == "cu_seqlens":
+        d["cu_seqlens"] = torch.tensor([0, 100, 60, 200], dtype=torch.int32, device="cuda")
+    T = sum(lens)
+    ws = kda.workspace_for(len(lens), T, H, 128, kda.KDA_DTYPE_BF16, "cuda")
+    assert kda.kda_prefill_path(len(lens), T, H, 128, 128, kda.KDA_DTYPE_BF16, ws.numel(), 0) == kda.KDA_PATH_STREAMED
+    kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], workspace=ws)
+    st = kda.kda_read_device_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
+    expected = {"decay": kda.KDA_ERR_DECAY_RANGE, "value": kda.KDA_ERR_VALUE_RANGE,
+                "cu_seqlens": kda.KDA_ERR_INVALID_ARG}[case]
+    assert st == expected
+    assert kda.kda_read_device_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
