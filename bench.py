@@ -102,7 +102,7 @@ def executed_tensor_flops(T, H, d, C=64):
 
 
 PATH_NAMES = {0: "cuda_core", 1: "fused", 2: "two_kernel", 3: "seq_split", 4: "segmented", 5: "streamed"}
-PATH_STREAMED = 5
+PATH_TWO_KERNEL, PATH_STREAMED = 2, 5
 
 
 def prefill_roofline(T, H, d, N, with_init, call_ms, stage_ms, peaks, traffic_key, path):
@@ -271,16 +271,16 @@ class _Gpu:
 
     def prefill_call(self, events=None, flags=0):
         """One kda_prefill through the C ABI; with `events` (four CUDA events) the
-        kda_prefill_events variant, which also marks the stages; with `flags` kda_prefill_ex."""
+        kda_prefill_events(_ex) variant, which also marks the stages; with `flags` kda_prefill_ex."""
         kda, x = self.kda, self.x
         args = (x["q"].data_ptr(), x["k"].data_ptr(), x["v"].data_ptr(), x["log_alpha"].data_ptr(),
                 x["beta"].data_ptr(), x["cu_seqlens"].data_ptr(), 1, self.T, self.H, self.d, self.d,
                 kda.KDA_DTYPE_BF16, None, self.o.data_ptr(), self.fs.data_ptr(), self.ws.data_ptr(),
                 self.ws.numel(), self.sh)
-        if flags:
-            st = kda.kda_prefill_ex(*args, flags)
+        if events is not None:
+            st = kda.kda_prefill_events_ex(*args, events, flags)
         else:
-            st = kda.kda_prefill(*args) if events is None else kda.kda_prefill_events(*args, events)
+            st = kda.kda_prefill_ex(*args, flags) if flags else kda.kda_prefill(*args)
         if st != kda.KDA_OK:
             raise kda.KdaError(st, "kda_prefill")
 
@@ -322,7 +322,8 @@ class _Gpu:
         return whole, stages
 
     def time_prefill_flags(self, steps, warmup, flags):
-        """Per-step event times (ms) of kda_prefill_ex with `flags`, L2 flushed before each."""
+        """Per-step event times (ms) of kda_prefill_ex with `flags`, L2 flushed before each, and
+        the same number of kda_prefill_events_ex calls split into its stages."""
         torch = self.torch
         for _ in range(warmup):
             self.flush.zero_()
@@ -335,7 +336,17 @@ class _Gpu:
             self.prefill_call(flags=flags)
             b.record(self.stream)
         torch.cuda.synchronize()
-        return [a.elapsed_time(b) for a, b in outer]
+        ev = [[self.event() for _ in range(4)] for _ in range(steps)]
+        for e in ev:
+            for x in e:  # create the handles before they are passed down
+                x.record(self.stream)
+        torch.cuda.synchronize()
+        for e in ev:
+            self.flush.zero_()
+            self.prefill_call([x.cuda_event for x in e], flags=flags)
+        torch.cuda.synchronize()
+        stages = [[e[i].elapsed_time(e[i + 1]) for i in range(3)] for e in ev]
+        return [a.elapsed_time(b) for a, b in outer], stages
 
     def time_prefill_e2e(self, steps, warmup):
         """Host-to-host through kda_prefill_host: pinned inputs in, o and the final state out,
@@ -630,10 +641,16 @@ def run_gpu(args):
                  "FLOPs, bf16/fp16 inputs, fp32 accumulate), 2000 repetitions per CTA: the "
                  "chunk work's groups (both paths), the state kernel's groups (64-column "
                  "slice, two-kernel path) and the streamed kernel's walk (whole head)")
-        tk_ms = reduce_max(sum(two_kernel_ms)) / args.steps
+        tk_whole, tk_stages = two_kernel_ms
+        tk_ms = reduce_max(sum(tk_whole)) / args.steps
+        tk_stage = [reduce_max(sum(s[i] for s in tk_stages)) / args.steps for i in range(3)]
+        tk_roof = prefill_roofline(T, H, d, 1, False, tk_ms, tk_stage, peaks, "4k", PATH_TWO_KERNEL)
         roof["two_kernel_form"] = {
             "ms_per_call": tk_ms, "value": aggregate_rate(T, world, 1, tk_ms),
-            "note": "the same call with KDA_FLAG_NO_STREAM: the chunk kernel, then the state pass"}
+            "kernel": tk_roof["kernel"], "frac": tk_roof["frac"], "traffic": tk_roof["traffic"],
+            "kernels": tk_roof["kernels"], "path_frac": tk_roof["path"]["frac"],
+            "note": "the same call with KDA_FLAG_NO_STREAM: the chunk kernel, then the state pass "
+                    "(kernel split from kda_prefill_events_ex with the same flag)"}
         roof["note"] = ("kernel durations from the four CUDA events kda_prefill_events records on "
                         "the launching stream around its kernels (a separate timed pass); the "
                         "dominant (longest) kernel is measured against its share of the path's "

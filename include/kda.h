@@ -206,7 +206,7 @@ kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, 
  *   events[0]  before the schedule kernel (cu_seqlens check, sequence order),
  *   events[1]  after it,
  *   events[2]  after the chunk-local kernel of the two-kernel path (on the
- *              single-kernel paths directly after events[1]),
+ *              single-kernel paths, the streamed one included, after that kernel),
  *   events[3]  after the last kernel.
  * All four are recorded even when no kernel runs.  num_events must be 4 and no
  * handle NULL, else KDA_ERR_INVALID_ARG before anything is enqueued.
@@ -217,6 +217,14 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
                                 kda_dtype_t dtype, const float *init_state, void *o,
                                 float *final_state, void *workspace, size_t workspace_bytes,
                                 void *stream, void *const *events, int32_t num_events);
+
+/* kda_prefill_events with option flags (as kda_prefill_ex); flags = 0 is kda_prefill_events. */
+kda_status_t kda_prefill_events_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                                   const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                   int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                                   kda_dtype_t dtype, const float *init_state, void *o,
+                                   float *final_state, void *workspace, size_t workspace_bytes,
+                                   void *stream, void *const *events, int32_t num_events, uint32_t flags);
 
 /*
  * Options of kda_prefill_ex / kda_decode_step_ex (bitwise or; other bits are

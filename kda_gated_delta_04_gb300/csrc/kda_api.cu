@@ -288,12 +288,12 @@ kda_status_t kda_prefill_slots(const void *q, const void *k, const void *v, cons
                         workspace_bytes, stream, nullptr, flags, &slots);
 }
 
-kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, const float *log_alpha,
-                                const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
-                                int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
-                                kda_dtype_t dtype, const float *init_state, void *o,
-                                float *final_state, void *workspace, size_t workspace_bytes,
-                                void *stream, void *const *events, int32_t num_events)
+kda_status_t kda_prefill_events_ex(const void *q, const void *k, const void *v, const float *log_alpha,
+                                   const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                   int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                                   kda_dtype_t dtype, const float *init_state, void *o,
+                                   float *final_state, void *workspace, size_t workspace_bytes,
+                                   void *stream, void *const *events, int32_t num_events, uint32_t flags)
 {
     if (!events || num_events != 4) return KDA_ERR_INVALID_ARG;
     cudaEvent_t ev[4];
@@ -302,7 +302,19 @@ kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, con
         ev[i] = static_cast<cudaEvent_t>(events[i]);
     }
     return prefill_impl(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
-                        d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream, ev, 0u);
+                        d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream, ev, flags);
+}
+
+kda_status_t kda_prefill_events(const void *q, const void *k, const void *v, const float *log_alpha,
+                                const float *beta, const int32_t *cu_seqlens, int32_t num_seqs,
+                                int64_t total_tokens, int32_t num_heads, int32_t d_k, int32_t d_v,
+                                kda_dtype_t dtype, const float *init_state, void *o,
+                                float *final_state, void *workspace, size_t workspace_bytes,
+                                void *stream, void *const *events, int32_t num_events)
+{
+    return kda_prefill_events_ex(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads, d_k,
+                                 d_v, dtype, init_state, o, final_state, workspace, workspace_bytes, stream,
+                                 events, num_events, 0u);
 }
 
 kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, const float *log_alpha,

@@ -51,6 +51,7 @@ EXPORTS = {
     "kda_status_string": (_c.c_char_p, [_c.c_int]),
     "kda_prefill_no_alloc": (_c.c_int, _PREFILL_ARGS[:15] + [_VP, _VP]),
     "kda_prefill_events": (_c.c_int, _PREFILL_ARGS + [_c.POINTER(_VP), _c.c_int32]),
+    "kda_prefill_events_ex": (_c.c_int, _PREFILL_ARGS + [_c.POINTER(_VP), _c.c_int32, _c.c_uint32]),
     "kda_selftest_bounded_wait": (_c.c_int, [_VP, _c.c_uint64, _VP]),
     "kda_prefill_ex": (_c.c_int, _PREFILL_ARGS + [_c.c_uint32]),
     "kda_diag_tensor_phases": (_c.c_int, [_c.c_int32, _c.c_int32, _VP, _VP, _c.POINTER(_c.c_double)]),
@@ -149,6 +150,16 @@ def kda_prefill_events(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tok
     return lib().kda_prefill_events(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens,
                                     num_heads, d_k, d_v, dtype, init_state, o, final_state,
                                     workspace, workspace_bytes, stream, arr, len(events))
+
+
+def kda_prefill_events_ex(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens, num_heads,
+                          d_k, d_v, dtype, init_state, o, final_state, workspace, workspace_bytes,
+                          stream, events, flags):
+    """kda_prefill_events with option flags (as kda_prefill_ex)."""
+    arr = (_VP * len(events))(*events)
+    return lib().kda_prefill_events_ex(q, k, v, log_alpha, beta, cu_seqlens, num_seqs, total_tokens,
+                                       num_heads, d_k, d_v, dtype, init_state, o, final_state,
+                                       workspace, workspace_bytes, stream, arr, len(events), flags)
 
 
 def kda_decode_step_slots(q, k, v, log_alpha, beta, batch, num_heads, d_k, d_v, dtype, state_pool,
