@@ -896,7 +896,7 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
 }
 
 // ============================================================== streamed prefill
-// One launch of two CTAs per SM.  CTAs [0, n_walk) each walk the state of one (sequence,
+// One launch of two CTAs per SM.  CTAs [0, n_walk) each walk the state of half a (sequence,
 // head) unit through its chunks; the others run the chunk work (chunk_items, chunks first
 // to last, items claimed in order from a counter) and publish every record with a release
 // store of its flag.  A walker copies a record only after an acquire load has seen its
