@@ -64,10 +64,15 @@ struct ChunkLayout {
     // record images staged for bulk stores, each over bytes dead by then:
     static constexpr uint32_t ST_P = 0;        // P over the k box (after the Kd build)
     static constexpr uint32_t ST_P2 = 90112;   // P2 over T' high (after the P products)
-    static constexpr uint32_t ST_NQ = 0;       // N | Q' over the P image and Kd^T (after N, Q'')
+    // N's two K panels over Kd^T low and over Aqk and T' high (after N, Q''), then Q' over the
+    // first once its store has read it: clear of the next item's boxes (k, q, log_alpha),
+    // which are copied in meanwhile
+    static constexpr uint32_t ST_A = 32768, ST_B = 81920;
     static constexpr uint32_t USED = 106496;
 };
-static_assert(ChunkLayout::ST_NQ + 49152 <= ChunkLayout::O1, "N | Q' staging overlaps O1");
+static_assert(ChunkLayout::ST_A >= ChunkLayout::IN_Q + 16384 && ChunkLayout::ST_A + 16384 <= ChunkLayout::O1 &&
+                  ChunkLayout::ST_B >= ChunkLayout::O1 + 32768 && ChunkLayout::ST_B + 16384 <= ChunkLayout::USED,
+              "record staging overlaps the boxes");
 static_assert(ChunkLayout::SOLVE_X + 32 * kLdX * 4 <= ChunkLayout::O1, "solve scratch overlaps O1");
 
 // State kernel (608 threads: sixteen state warps, two issuing warps, a copy warp) over a
@@ -193,7 +198,8 @@ __device__ __forceinline__ void issue_p(uint32_t sb, uint32_t tmem)
                      (t | s) != 0);
 }
 
-// Round 3: N = Kd^T (-W) (M = 128, N = 128) and, when outputs are wanted, Q'' = Aqk (-W) (M = 64, N = 128).
+// Round 3: N = Kd^T (-W) (M = 128, N = 128) and, when outputs are wanted, Q' = Qg + Aqk (-W)
+// (M = 64, N = 128), accumulated onto Qg, which the compute warps store into its columns.
 template <class L>
 __device__ __forceinline__ void issue_n_q(uint32_t sb, uint32_t tmem, bool with_o)
 {
@@ -204,7 +210,7 @@ __device__ __forceinline__ void issue_n_q(uint32_t sb, uint32_t tmem, bool with_
     if (!with_o) return;
 #pragma unroll
     for (int s = 0; s < 4; ++s)
-        mma_bf16(tmem + TC_Q, kdesc(sb + L::AQ + s * 32), mndesc(sb + L::O1 + s * 2048, 16384), id_q, s > 0);
+        mma_bf16(tmem + TC_Q, kdesc(sb + L::AQ + s * 32), mndesc(sb + L::O1 + s * 2048, 16384), id_q, 1);
 }
 
 // Epilogues into shared-memory images of the record's parts, which one thread
@@ -252,12 +258,16 @@ __device__ __forceinline__ void epi_p(uint32_t tmem, unsigned char *dst, bool &o
     }
 }
 
+// N: the compute warps of part p (warps 4p .. 4p + 3) write K panel p (columns 64p ..) to
+// dst[p], 128 rows of 128 bytes.
 template <int NT>
-__device__ __forceinline__ void epi_n(uint32_t tmem, unsigned char *dst)
+__device__ __forceinline__ void epi_n(uint32_t tmem, unsigned char *dst0, unsigned char *dst1)
 {
-    constexpr int CW = 128 / (NT / 128);
+    static_assert(NT == 256, "one K panel per part");
+    constexpr int CW = 64;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
     const int i = quarter * 32 + lane;
+    unsigned char *dst = part ? dst1 : dst0;
 #pragma unroll
     for (int cb = 0; cb < CW; cb += 16) {
         float v[16];
@@ -268,14 +278,40 @@ __device__ __forceinline__ void epi_n(uint32_t tmem, unsigned char *dst)
             float x[8];
 #pragma unroll
             for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
-            *reinterpret_cast<uint4 *>(dst + km16(i, part * CW + cb + hh * 8, 128)) = pack_bf16x8(x);
+            *reinterpret_cast<uint4 *>(dst + km16(i, cb + hh * 8, 128)) = pack_bf16x8(x);
         }
     }
 }
 
-// Q' = Qg + Aqk (-W); Qg from rows 64..127 of O1.  M = 64: 16-lane loads, as in w_epilogue.
+// Qg (rows 64..127 of O1, bf16) into the Q'' accumulator columns, before the products that
+// add Aqk (-W) onto it.  M = 64: 16-lane stores, the mapping of epi_q.
 template <class L, int NT>
-__device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, unsigned char *dst)
+__device__ __forceinline__ void qg_to_tmem(const unsigned char *sm, uint32_t tmem)
+{
+    constexpr int CW = 128 / (NT / 128), HW = CW / 2;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
+    const int r = quarter * 16 + (lane & 15), c0 = part * CW + (lane >> 4) * HW;
+#pragma unroll
+    for (int cb = 0; cb < HW; cb += 16) {
+        float v[16];
+#pragma unroll
+        for (int hh = 0; hh < 2; ++hh) {
+            const uint4 qraw = *reinterpret_cast<const uint4 *>(sm + L::O1 + km16(64 + r, c0 + cb + hh * 8, 128));
+            const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qw[u]));
+                v[hh * 8 + 2 * u] = qf.x;
+                v[hh * 8 + 2 * u + 1] = qf.y;
+            }
+        }
+        tmem_st16x2_x16<HW>(tmem + TC_Q + ((uint32_t)(quarter * 32) << 16) + part * CW + cb, v);
+    }
+}
+
+// Q' = Qg + Aqk (-W), whole in TMEM.  M = 64: 16-lane loads, as in w_epilogue.
+template <int NT>
+__device__ __forceinline__ void epi_q(uint32_t tmem, unsigned char *dst)
 {
     constexpr int CW = 128 / (NT / 128), HW = CW / 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, quarter = warp & 3, part = warp >> 2;
@@ -287,17 +323,10 @@ __device__ __forceinline__ void epi_q(const unsigned char *sm, uint32_t tmem, un
         tmem_ld_wait();
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
-            const int col = c0 + cb + hh * 8;
-            const uint4 qraw = *reinterpret_cast<const uint4 *>(sm + L::O1 + km16(64 + r, col, 128));
-            const uint32_t qw[4] = {qraw.x, qraw.y, qraw.z, qraw.w};
             float x[8];
 #pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const float2 qf = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&qw[u]));
-                x[2 * u] = qf.x + v[hh * 8 + 2 * u];
-                x[2 * u + 1] = qf.y + v[hh * 8 + 2 * u + 1];
-            }
-            *reinterpret_cast<uint4 *>(dst + km16(r, col, 64)) = pack_bf16x8(x);
+            for (int u = 0; u < 8; ++u) x[u] = v[hh * 8 + u];
+            *reinterpret_cast<uint4 *>(dst + km16(r, c0 + cb + hh * 8, 64)) = pack_bf16x8(x);
         }
     }
 }
@@ -379,8 +408,21 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
     const uint32_t tmem = tmem_holder;
     float *s_tot = reinterpret_cast<float *>(sm + L::AQ);
     bool timed_out = false, decay_bad = false, range_ok = true, stores_pending = false;
+    int pub = -1;    // STREAM: the flag of the record whose last stores are in flight (issuer)
     uint32_t n = 0;  // items done by this CTA: the barriers' phase parities follow it
     for (; it < items; ++n) {
+        // the previous item's N and Q' stores must have read their staging, which the prefix
+        // (s_tot over Aqk) and the decayed operands (Ki over Kd^T low) write next
+        if (n > 0) {
+            if (issuer) bulk_wait_read();
+            __syncthreads();
+        }
+        if (STREAM && issuer && pub >= 0) {  // the previous record, complete in global memory once
+            bulk_wait_all();                   // its stores are: publish it (the compute warps go on)
+            fence_proxy_async_global();
+            st_release_gpu(flags + pub, 1);
+            pub = -1;
+        }
         const int64_t c0 = dsc.x;
         const int len = dsc.y;
         unsigned char *rec = records + ((size_t)(g - g_base) * H + h) * kRecBytes;
@@ -457,6 +499,15 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
                 epi_p<NT>(tmem, sm + L::ST_P, range_ok);    // the k box is dead
                 if (with_o) epi_p2<NT>(tmem, sm + L::ST_P2, range_ok);  // T' (high) is dead: every product reading it is done
             }
+            if (with_o) {  // Qg into the Q'' columns, once every compute warp has read P and P2 from them
+                tc_fence_before_sync();
+                late = bar_sync_or(1, NT, late);
+                tc_fence_after_sync();
+                if (!late) {
+                    qg_to_tmem<L, NT>(sm, tmem);
+                    tmem_st_wait();
+                }
+            }
         }
         fence_proxy_async_smem();
         tc_fence_before_sync();
@@ -472,38 +523,52 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
             mma_commit(&bar_mma);
         }
         ok = mbar_wait_ns(&bar_mma, pm, kWaitNs);
-        if (issuer) bulk_wait_read();  // the P image is overwritten next
+        if (issuer) bulk_wait_read();  // the P and P2 images: the next boxes and the N staging go over them
         if (__syncthreads_or(!ok)) { timed_out = true; break; }
         tc_fence_after_sync();
-        if (compute) {
-            epi_n<NT>(tmem, sm + L::ST_NQ);           // over the P image and Kd^T
-            if (with_o) epi_q<L, NT>(sm, tmem, sm + L::ST_NQ + 32768);
+        if (issuer && itn < items) {
+            // the next item's boxes: every byte they land on is dead now, and N and Q' are
+            // staged clear of them, so the copies run while this item's records go out
+            mbar_arrive_expect_tx(&bar_tma, tma_bytes);
+            if (!scalar_gate) tma_load_3d(sm + L::O1, &tm_la, &bar_tma, 0, hn, dn.x);
+            tma_load_3d(sm + L::IN_Q, &tm_q, &bar_tma, 0, hn, dn.x);
+            tma_load_3d(sm + L::IN_K, &tm_k, &bar_tma, 0, hn, dn.x);
         }
+        if (compute) epi_n<NT>(tmem, sm + L::ST_A, sm + L::ST_B);
         fence_proxy_async_smem();
+        if (with_o) {  // then Q' over N's first panel, once its store has read it
+            __syncthreads();
+            if (issuer) {
+                bulk_store(rec + R_N, sm + L::ST_A, 16384u);
+                bulk_store(rec + R_N + 16384, sm + L::ST_B, 16384u);
+                bulk_commit();
+                bulk_wait_read();
+            }
+            __syncthreads();
+            if (compute) epi_q<NT>(tmem, sm + L::ST_A);
+            fence_proxy_async_smem();
+        }
         tc_fence_before_sync();  // this item's TMEM reads precede the next item's products
         __syncthreads();
         if (issuer) {
-            bulk_store(rec + R_N, sm + L::ST_NQ, with_o ? 49152u : 32768u);  // N | Q'
+            if (with_o) {
+                bulk_store(rec + R_Q, sm + L::ST_A, 16384u);
+            } else {
+                bulk_store(rec + R_N, sm + L::ST_A, 16384u);
+                bulk_store(rec + R_N + 16384, sm + L::ST_B, 16384u);
+            }
             bulk_commit();
-            if (itn < items) {
-                // the next item's boxes: log_alpha into O1 at once (free after Q'), q and k
-                // once the store has read [0, 48 KB), where they land
-                mbar_arrive_expect_tx(&bar_tma, tma_bytes);
-                if (!scalar_gate) tma_load_3d(sm + L::O1, &tm_la, &bar_tma, 0, hn, dn.x);
-                bulk_wait_read();
-                tma_load_3d(sm + L::IN_Q, &tm_q, &bar_tma, 0, hn, dn.x);
-                tma_load_3d(sm + L::IN_K, &tm_k, &bar_tma, 0, hn, dn.x);
-            }
-            if (STREAM) {  // the record is complete in global memory: publish it
-                bulk_wait_all();
-                fence_proxy_async_global();
-                st_release_gpu(flags + (size_t)g * H + h, 1);
-            }
+            if (STREAM) pub = g * H + h;  // published once its stores are complete (next item's start)
         }
         it = itn;
         h = hn;
         g = gn;
         dsc = dn;
+    }
+    if (STREAM && issuer && pub >= 0) {  // the last record: its stores were all issued
+        bulk_wait_all();
+        fence_proxy_async_global();
+        st_release_gpu(flags + pub, 1);
     }
     if (timed_out) {
         if (issuer) {
