@@ -33,9 +33,12 @@ namespace {
 using namespace ptx;
 using namespace tc;
 
-// Record of one chunk-head.
-constexpr uint32_t R_N = 0;        // N  bf16 K-major, 2 panels x 128 rows (rows i, K = j)
-constexpr uint32_t R_Q = 32768;    // Q' bf16 K-major, 2 panels x 64 rows  (rows t, K = j)
+// Record of one chunk-head.  N and Q' interleave by K panel, [N panel 0 | Q' panel 0 |
+// N panel 1 | Q' panel 1], so that each K panel of the two is one 192-row operand image and
+// the pair travels as one copy.
+constexpr uint32_t R_NQ_PANEL = 24576;  // bytes from one K panel of N and Q' to the next
+constexpr uint32_t R_N = 0;        // N  bf16 K-major, 128 rows per panel (rows i, K = j)
+constexpr uint32_t R_Q = 16384;    // Q' bf16 K-major, 64 rows per panel  (rows t, K = j)
 constexpr uint32_t R_P = 49152;    // P  fp16 K-major, 128 rows            (rows i, K = s)
 constexpr uint32_t R_P2 = 65536;   // P2 fp16 K-major, 64 rows             (rows t, K = s)
 constexpr uint32_t R_GM = 73728;   // gamma, 128 fp32
@@ -540,7 +543,7 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
             __syncthreads();
             if (issuer) {
                 bulk_store(rec + R_N, sm + L::ST_A, 16384u);
-                bulk_store(rec + R_N + 16384, sm + L::ST_B, 16384u);
+                bulk_store(rec + R_N + R_NQ_PANEL, sm + L::ST_B, 16384u);
                 bulk_commit();
                 bulk_wait_read();
             }
@@ -551,11 +554,12 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
         tc_fence_before_sync();  // this item's TMEM reads precede the next item's products
         __syncthreads();
         if (issuer) {
-            if (with_o) {
-                bulk_store(rec + R_Q, sm + L::ST_A, 16384u);
+            if (with_o) {  // Q' staged as its two K panels back to back
+                bulk_store(rec + R_Q, sm + L::ST_A, 8192u);
+                bulk_store(rec + R_Q + R_NQ_PANEL, sm + L::ST_A + 8192, 8192u);
             } else {
                 bulk_store(rec + R_N, sm + L::ST_A, 16384u);
-                bulk_store(rec + R_N + 16384, sm + L::ST_B, 16384u);
+                bulk_store(rec + R_N + R_NQ_PANEL, sm + L::ST_B, 16384u);
             }
             bulk_commit();
             if (STREAM) pub = g * H + h;  // published once its stores are complete (next item's start)
@@ -638,7 +642,7 @@ __device__ __forceinline__ void issue_chain(uint32_t acc, uint64_t dr, uint64_t 
         mma_bf16(acc, dr + ((R_P + s * 32) >> 4), dv + ((s * 32) >> 4), Sh::IDESC_PV, s > 0);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {  // + N S_c (bf16)
-        const uint32_t off = (s >> 2) * 16384 + (s & 3) * 32, offs = s * Sh::SK;
+        const uint32_t off = (s >> 2) * R_NQ_PANEL + (s & 3) * 32, offs = s * Sh::SK;
         mma_bf16(acc, dr + ((R_N + off) >> 4), ds + (offs >> 4), Sh::IDESC_NS, 1);
     }
 }
@@ -652,7 +656,7 @@ __device__ __forceinline__ void issue_out(uint32_t acc, uint64_t dr, uint64_t dv
         mma_bf16(acc, dr + ((R_P2 + s * 32) >> 4), dv + ((s * 32) >> 4), Sh::IDESC_P2V, s > 0);
 #pragma unroll
     for (int s = 0; s < 8; ++s) {  // + Q' S_c (bf16)
-        const uint32_t off = (s >> 2) * 8192 + (s & 3) * 32, offs = s * Sh::SK;
+        const uint32_t off = (s >> 2) * R_NQ_PANEL + (s & 3) * 32, offs = s * Sh::SK;
         mma_bf16(acc, dr + ((R_Q + off) >> 4), ds + (offs >> 4), Sh::IDESC_QS, 1);
     }
 }
@@ -982,8 +986,10 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
 //   [S_{c+1}^T | o_c^T] = [gamma_c . S_c^T | 0] + V_c^T [P_c^T | P2_c^T] + S_c^T [N_c^T | Q'_c^T]
 // (M = 64 rows j; N = 128 key rows i for the state and 64 tokens t for the outputs, 192 in
 // all).  The record's P, P2, N and Q' images (rows over their first index, K-major over
-// the second) are the B operands; the walker copies them so that P and P2, and each K panel
-// of N and Q', sit back to back as 192-row operands.  TMEM holds the state itself: the
+// the second) are the B operands: P and P2, and each K panel of N and Q', sit back to back
+// in the record as 192-row operands, so the walker copies them in two pieces as they stand
+// (fewer copies shorten the wait for them: every extra copy per chunk cost about 30 ns of
+// the walk).  TMEM holds the state itself: the
 // accumulator's first 128 columns (fp32, lane j, column i), into which the state warps store
 // gamma_c . S_c (and zeros into the output columns) before the products accumulate onto
 // them; and S_c^T in bf16 as the A operand of the N, Q' products.  V_c^T (fp16, K-major) is
@@ -1001,6 +1007,8 @@ static_assert(WalkLayout::NQ_PANEL % 1024 == 0 && WalkLayout::PP % 1024 == 0 && 
                   WalkLayout::VBOX % 128 == 0,
               "walker layout alignment");
 static_assert(R_P2 == R_P + 16384, "P2 follows P in the record");
+static_assert(WalkLayout::NQ_PANEL == R_NQ_PANEL && R_Q == R_N + 16384 && R_P == R_N + 2 * R_NQ_PANEL,
+              "the walker's N | Q' operand is the record's, copied whole");
 constexpr uint32_t kStreamSmem =
     (WalkLayout::USED > ChunkLayout::USED ? WalkLayout::USED : ChunkLayout::USED) + 1024;
 // walker TMEM columns: accumulator (state 0-127, outputs 128-191), bf16 S^T.  An M = 64
@@ -1143,11 +1151,11 @@ __device__ __forceinline__ void walk_unit(int walker, const CUtensorMap &tm_v, c
         mbar_arrive_expect_tx(&w_pp, o ? 24576u : 16384u);
         bulk_load(sm + L::PP, r + R_P, o ? 24576u : 16384u, &w_pp);  // P2 follows P in both
         mbar_arrive_expect_tx(&w_rec, o ? 49152u : 32768u);
-        bulk_load(sm + L::NQ, r + R_N, 16384, &w_rec);
-        bulk_load(sm + L::NQ + L::NQ_PANEL, r + R_N + 16384, 16384, &w_rec);
-        if (o) {
-            bulk_load(sm + L::NQ + 16384, r + R_Q, 8192, &w_rec);
-            bulk_load(sm + L::NQ + L::NQ_PANEL + 16384, r + R_Q + 8192, 8192, &w_rec);
+        if (o) {  // N and Q' as laid out in the record: one copy
+            bulk_load(sm + L::NQ, r + R_N, 49152u, &w_rec);
+        } else {
+            bulk_load(sm + L::NQ, r + R_N, 16384u, &w_rec);
+            bulk_load(sm + L::NQ + L::NQ_PANEL, r + R_N + R_NQ_PANEL, 16384u, &w_rec);
         }
         rec_issued = c + 1;
     };
