@@ -1022,6 +1022,11 @@ constexpr int kMaxWalkers = 64;  // walker CTAs of the streamed prefill at most 
 // per chunk) outlasts the chunk work beside it, and the separate state pass (about 1 us per
 // chunk, or the sequence split) is faster.
 constexpr int kMinStreamUnits = 20;
+// First chunk whose record a walker prefetches into L2 two chunks ahead.  The walk trails the
+// chunk work by a little more each chunk (about 12 %), so early records are read while still
+// in L2 and the prefetch only costs a copy on the critical path (T = 4096: 1.7 % slower with
+// it); later ones have left L2 by the time they are read (T = 65536: 4 % slower without it).
+constexpr int kWalkPrefetchFrom = 128;
 
 // The product group of one chunk: D += V^T [P^T | P2^T] (fp16) + S^T [N^T | Q'^T] (bf16, S^T
 // from TMEM), M = 64, N = 192, or N = 128 (state only) without the outputs; in two parts,
@@ -1319,12 +1324,12 @@ __device__ __forceinline__ void walk_unit(int walker, const CUtensorMap &tm_v, c
             if (c + 1 < nch) ok = read_v(c + 1, vt);
             if (ok && warp == 0 && lane == 0 && c + 2 < nch) {
                 // while this chunk's products run: record c + 2's flag, then (its buffer is
-                // free once every state warp is past chunk c - 1: ready(c)) its gamma, and the
-                // record into L2 (it may have left L2 since it was written)
+                // free once every state warp is past chunk c - 1: ready(c)) its gamma, and
+                // later in the walk the record into L2 (it may have left L2 since it was written)
                 ok = wait_flag(c + 2) && mbar_wait_ns(&w_ready, (uint32_t)(c & 1), kWaitNs);
                 if (ok) {
                     load_gamma(c + 2);
-                    bulk_prefetch_l2(rec0 + (size_t)(c + 2) * rec_stride, kRecBytes);
+                    if (c + 2 >= kWalkPrefetchFrom) bulk_prefetch_l2(rec0 + (size_t)(c + 2) * rec_stride, kRecBytes);
                 }
             }
             ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait_ns(&w_mma, (uint32_t)(c & 1), kWaitNs));
