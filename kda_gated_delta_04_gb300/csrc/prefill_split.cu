@@ -147,7 +147,8 @@ __device__ __forceinline__ void build_kd(unsigned char *sm, int len, const float
     const int sel = lane & 1;  // odd lanes store their odd channel first (no bank conflicts)
 #pragma unroll
     for (int r8 = 0; r8 < R; r8 += 8) {
-        float hx[8], lx[8], hy[8], ly[8];
+        uint32_t hxy[8];  // the high parts of channels (2cp, 2cp + 1) of row r8 + u
+        float lx[8], ly[8];
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
             const int rr = r8 + u, r = rg * R + rr;
@@ -160,13 +161,15 @@ __device__ __forceinline__ void build_kd(unsigned char *sm, int len, const float
             }
             const float dx = kv.x * exp2_approx(tot.x - (off.x + gl[rr].x));  // log2 units
             const float dy = kv.y * exp2_approx(tot.y - (off.y + gl[rr].y));
-            hx[u] = __bfloat162float(__float2bfloat16_rn(dx));
-            hy[u] = __bfloat162float(__float2bfloat16_rn(dy));
-            lx[u] = dx - hx[u];
-            ly[u] = dy - hy[u];
+            hxy[u] = split_bf16x2(dx, dy, lx[u], ly[u]);
         }
         const int s0 = rg * R + r8;
-        const uint4 hxv = pack_bf16x8(hx), hyv = pack_bf16x8(hy), lxv = pack_bf16x8(lx), lyv = pack_bf16x8(ly);
+        // the high parts regrouped by channel (rows u, u + 1 per word, as pack_bf16x8 packs)
+        const uint4 hxv = make_uint4(__byte_perm(hxy[0], hxy[1], 0x5410), __byte_perm(hxy[2], hxy[3], 0x5410),
+                                     __byte_perm(hxy[4], hxy[5], 0x5410), __byte_perm(hxy[6], hxy[7], 0x5410));
+        const uint4 hyv = make_uint4(__byte_perm(hxy[0], hxy[1], 0x7632), __byte_perm(hxy[2], hxy[3], 0x7632),
+                                     __byte_perm(hxy[4], hxy[5], 0x7632), __byte_perm(hxy[6], hxy[7], 0x7632));
+        const uint4 lxv = pack_bf16x8(lx), lyv = pack_bf16x8(ly);
         *reinterpret_cast<uint4 *>(sm + L::KDH + km16(2 * cp + sel, s0, 128)) = sel ? hyv : hxv;
         *reinterpret_cast<uint4 *>(sm + L::KDH + km16(2 * cp + 1 - sel, s0, 128)) = sel ? hxv : hyv;
         *reinterpret_cast<uint4 *>(sm + L::KDL + km16(2 * cp + sel, s0, 128)) = sel ? lyv : lxv;

@@ -56,6 +56,17 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b)
     return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// The bf16 high parts of a and b (round to nearest even), packed as pack_bf16x2 does, and
+// the fp32 remainders a - hi(a), b - hi(b): one conversion for the pair, the remainders from
+// the packed bits.
+__device__ __forceinline__ uint32_t split_bf16x2(float a, float b, float &ra, float &rb)
+{
+    const uint32_t h = pack_bf16x2(a, b);
+    ra = a - __uint_as_float(h << 16);
+    rb = b - __uint_as_float(h & 0xffff0000u);
+    return h;
+}
+
 // Eight fp16 values (round to nearest even); `ok` is cleared when one of them
 // is outside the fp16 range or not finite.
 __device__ __forceinline__ uint4 pack_f16x8(const float (&x)[8], bool &ok)
@@ -418,13 +429,9 @@ __device__ __forceinline__ void store_tprime_quad(unsigned char *sm, int r, int 
 {
     const float4 bq = *reinterpret_cast<const float4 *>(s_beta + c);
     const float tv[4] = {t.x * bq.x, t.y * bq.y, t.z * bq.z, t.w * bq.w};
-    float hi[4], lo[4];
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-        hi[u] = __bfloat162float(__float2bfloat16_rn(tv[u]));
-        lo[u] = tv[u] - hi[u];
-    }
-    *reinterpret_cast<uint2 *>(sm + L::O4 + km16(r, c, 64)) = make_uint2(pack_bf16x2(hi[0], hi[1]), pack_bf16x2(hi[2], hi[3]));
+    float lo[4];
+    const uint32_t h01 = split_bf16x2(tv[0], tv[1], lo[0], lo[1]), h23 = split_bf16x2(tv[2], tv[3], lo[2], lo[3]);
+    *reinterpret_cast<uint2 *>(sm + L::O4 + km16(r, c, 64)) = make_uint2(h01, h23);
     *reinterpret_cast<uint2 *>(sm + L::TL + km16(r, c, 64)) = make_uint2(pack_bf16x2(lo[0], lo[1]), pack_bf16x2(lo[2], lo[3]));
 }
 
