@@ -142,3 +142,24 @@ def test_streamed_errors_are_reported_not_faulted(case):
                 "cu_seqlens": kda.KDA_ERR_INVALID_ARG}[case]
     assert st == expected
     assert kda.kda_read_device_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream) == 0
+
+
+def test_streamed_results_do_not_depend_on_timing():
+    """The walkers and the workers meet only at the records' flags, and every product and
+    rounding is fixed by the data, so repeated calls give the same bits whatever the order in
+    which CTAs run.  A record read before its stores were complete, or a buffer refilled
+    early, would show up as a difference between calls.  The benchmark workload (T = 4096,
+    H = 32: 64 walkers beside 240 workers), with the L2 flushed before every other call so
+    that the timing varies; the two-kernel form the same way."""
+    w = synth.PREFILL_4K
+    d = to_device(synth.prefill_inputs(w))
+    args = (d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"])
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    for streamed in (True, False):
+        o0, s0 = kda.prefill(*args, check_status=True, streamed=streamed)
+        o0, s0 = o0.clone(), s0.clone()
+        for i in range(16):
+            if i % 2:
+                flush.zero_()
+            o, s = kda.prefill(*args, check_status=True, streamed=streamed)
+            assert torch.equal(o, o0) and torch.equal(s, s0), f"call {i + 1} differs (streamed={streamed})"
