@@ -264,7 +264,12 @@ kda_status_t kda_prefill_events_ex(const void *q, const void *k, const void *v, 
  *                        and each record is handed over through a ready flag in the
  *                        workspace as soon as its stores are complete.  The two forms
  *                        agree to within rounding, not bit for bit (the walk forms its
- *                        products transposed). */
+ *                        products transposed).  The walking CTAs wait for records that
+ *                        the others produce, so the launch needs SM slots for both: if
+ *                        kernels on other streams hold all but a few slots for longer
+ *                        than the device-side wait limit (2 s), the walk gives up with
+ *                        KDA_ERR_TIMEOUT instead of hanging.  The two-kernel form has no
+ *                        such dependence; pass this flag where the GPU is shared that way. */
 #define KDA_FLAG_NO_STREAM 8u
 
 /* kda_prefill with options (flags above); flags = 0 is kda_prefill. */
