@@ -177,7 +177,7 @@ __device__ __forceinline__ void build_kd(unsigned char *sm, int len, const float
     }
 }
 
-// Round 2a: W = T' Kg (M = 64, N = 128) and, when outputs are wanted, P2 = Aqk T' (M = 64, N = 64).
+// Product group 2a: W = T' Kg (M = 64, N = 128) and, when outputs are wanted, P2 = Aqk T' (M = 64, N = 64).
 template <class L>
 __device__ __forceinline__ void issue_w_p2(uint32_t sb, uint32_t tmem, bool with_o)
 {
@@ -189,7 +189,7 @@ __device__ __forceinline__ void issue_w_p2(uint32_t sb, uint32_t tmem, bool with
         mma_bf16(tmem + TC_P2, kdesc(sb + L::AQ + s * 32), mndesc(sb + L::O4 + s * 2048, 8192), idesc, s > 0);
 }
 
-// Round 2b: P = Kd^T T' (M = 128, N = 64) from the three leading terms of the
+// Product group 2b: P = Kd^T T' (M = 128, N = 64) from the three leading terms of the
 // high/low split, hi.hi + hi.lo + lo.hi.
 template <class L>
 __device__ __forceinline__ void issue_p(uint32_t sb, uint32_t tmem)
@@ -204,7 +204,7 @@ __device__ __forceinline__ void issue_p(uint32_t sb, uint32_t tmem)
                      (t | s) != 0);
 }
 
-// Round 3: N = Kd^T (-W) (M = 128, N = 128) and, when outputs are wanted, Q' = Qg + Aqk (-W)
+// Product group 3: N = Kd^T (-W) (M = 128, N = 128) and, when outputs are wanted, Q' = Qg + Aqk (-W)
 // (M = 64, N = 128), accumulated onto Qg, which the compute warps store into its columns.
 template <class L>
 __device__ __forceinline__ void issue_n_q(uint32_t sb, uint32_t tmem, bool with_o)
