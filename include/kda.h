@@ -257,11 +257,13 @@ kda_status_t kda_prefill_events_ex(const void *q, const void *k, const void *v, 
  *                        with the unsplit pass to within rounding, not bit for bit. */
 #define KDA_FLAG_NO_SEQ_SPLIT 4u
 /*  KDA_FLAG_NO_STREAM     run the chunk kernel and the state pass one after the other.
- *                        By default, when a bf16 d = 128 problem has 20 to 32 (sequence,
- *                        head) units, no sequence split and a workspace that holds every
- *                        record, both run in one launch: two CTAs walk the state of each
- *                        unit (64 value columns each) while the others do the chunk work,
- *                        and each record is handed over through a ready flag in the
+ *                        By default, when a bf16 d = 128 problem has no sequence split, a
+ *                        workspace that holds every record, and enough (sequence, head)
+ *                        units for it to be the faster form (at most 32; at least 31 when
+ *                        the sequences average up to 96 chunks of 64 tokens, 27 up to 384,
+ *                        24 beyond), both run in one launch: two CTAs walk the state of
+ *                        each unit (64 value columns each) while the others do the chunk
+ *                        work, and each record is handed over through a ready flag in the
  *                        workspace as soon as its stores are complete.  The two forms
  *                        agree to within rounding, not bit for bit (the walk forms its
  *                        products transposed).  The walking CTAs wait for records that
@@ -271,6 +273,11 @@ kda_status_t kda_prefill_events_ex(const void *q, const void *k, const void *v, 
  *                        KDA_ERR_TIMEOUT instead of hanging.  The two-kernel form has no
  *                        such dependence; pass this flag where the GPU is shared that way. */
 #define KDA_FLAG_NO_STREAM 8u
+/*  KDA_FLAG_STREAM        run both in one launch whenever the launch holds the walking CTAs
+ *                        (1 to 32 units on a 152-SM GB300; same conditions otherwise),
+ *                        however few the units.  Passing it with KDA_FLAG_NO_STREAM is
+ *                        KDA_ERR_INVALID_ARG. */
+#define KDA_FLAG_STREAM 16u
 
 /* kda_prefill with options (flags above); flags = 0 is kda_prefill. */
 kda_status_t kda_prefill_ex(const void *q, const void *k, const void *v, const float *log_alpha,

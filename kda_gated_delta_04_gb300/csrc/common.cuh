@@ -81,6 +81,9 @@ struct PrefillProblem {
     // after them, zeroed by the schedule kernel: the streamed prefill publishes each record
     // through its flag.  Null: no streaming.
     int *flags = nullptr;
+    // stream whenever the launch holds the walkers (KDA_FLAG_STREAM), not only where the
+    // streamed form is the faster one
+    bool stream_force = false;
     cudaStream_t stream;
 };
 
@@ -123,12 +126,17 @@ size_t prefill_split_record_bytes();
 // (after the streamed kernel, when that one runs).
 cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records,
                                  cudaEvent_t mid = nullptr);
-// Whether launch_prefill_split tries the streamed kernel (chunk work and state walk in one
-// grid) for p: ready flags given, no sequence split, no segments, few (sequence, head) units.
+// Whether launch_prefill_split runs the streamed kernel (chunk work and state walk in one
+// grid) for p: ready flags given, no sequence split, no segments, and prefill_stream_fits.
 bool prefill_stream_eligible(const PrefillProblem &p);
-// Whether `units` (sequence, head) units are few enough for the streamed kernel on the
-// current device (one walker CTA each, beside at least one worker CTA per SM).
-bool prefill_stream_fits(int64_t units);
+// Whether the streamed kernel takes a problem of `units` (sequence, head) units of about
+// `chunks_per_unit` chunks each on the current device: the launch holds two walker CTAs per
+// unit beside at least one worker CTA per SM, and (unless `force`) there are enough units
+// for the streamed form to be the faster one at that length.
+bool prefill_stream_fits(int64_t units, int64_t chunks_per_unit, bool force);
+// The mean chunk count of a sequence, ceil(ceil(total_tokens / num_seqs) / 64) (0 with no
+// sequences).
+int64_t mean_chunks_per_sequence(int32_t num_seqs, int64_t total_tokens);
 cudaError_t launch_decode(const DecodeProblem &p);
 // Measurement only: the tensor-core product groups of the chunk kernel (pass 0) or the state
 // kernel (pass 1) back to back on resident operands; synchronises `stream`; executed TFLOP/s.

@@ -91,7 +91,9 @@ int32_t path_for(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int3
         if (!(flags & KDA_FLAG_NO_SEQ_SPLIT) && workspace_bytes >= ws_split_bytes(num_seqs, total_tokens, num_heads) &&
             kda::seqsplit_lseg(num_seqs, total_tokens, num_heads) > 0)
             return KDA_PATH_SEQ_SPLIT;
-        if (!(flags & KDA_FLAG_NO_STREAM) && kda::prefill_stream_fits((int64_t)num_seqs * num_heads))
+        if (!(flags & KDA_FLAG_NO_STREAM) &&
+            kda::prefill_stream_fits((int64_t)num_seqs * num_heads, kda::mean_chunks_per_sequence(num_seqs, total_tokens),
+                                     (flags & KDA_FLAG_STREAM) != 0))
             return KDA_PATH_STREAMED;
         return KDA_PATH_TWO_KERNEL;
     }
@@ -114,7 +116,12 @@ kda_status_t check_shape(int32_t d_k, int32_t d_v, kda_dtype_t dtype)
 
 // every option bit of the _ex / _slots calls
 constexpr uint32_t kKnownFlags =
-    KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM | KDA_FLAG_NO_SEQ_SPLIT | KDA_FLAG_NO_STREAM;
+    KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM | KDA_FLAG_NO_SEQ_SPLIT | KDA_FLAG_NO_STREAM | KDA_FLAG_STREAM;
+// flags valid for a call: known bits, and not both streaming choices
+inline bool flags_valid(uint32_t flags)
+{
+    return !(flags & ~kKnownFlags) && (flags & (KDA_FLAG_STREAM | KDA_FLAG_NO_STREAM)) != (KDA_FLAG_STREAM | KDA_FLAG_NO_STREAM);
+}
 
 extern "C" {
 
@@ -142,7 +149,7 @@ size_t kda_prefill_workspace_size_segmented(int32_t num_seqs, int64_t total_toke
 int32_t kda_prefill_path(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int32_t d_k,
                          int32_t d_v, kda_dtype_t dtype, size_t workspace_bytes, uint32_t flags)
 {
-    if (flags & ~kKnownFlags) return -(int32_t)KDA_ERR_INVALID_ARG;
+    if (!flags_valid(flags)) return -(int32_t)KDA_ERR_INVALID_ARG;
     const kda_status_t st = check_shape(d_k, d_v, dtype);
     if (st != KDA_OK) return -(int32_t)st;
     if (num_seqs < 0 || total_tokens < 0 || num_heads <= 0 || (num_seqs == 0 && total_tokens != 0))
@@ -162,7 +169,7 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
                           void *workspace, size_t workspace_bytes, void *stream, const cudaEvent_t *ev,
                           uint32_t flags, const kda::StateSlots *slots = nullptr)
 {
-    if (flags & ~kKnownFlags) return KDA_ERR_INVALID_ARG;
+    if (!flags_valid(flags)) return KDA_ERR_INVALID_ARG;
     const bool scalar_gate = (flags & KDA_FLAG_SCALAR_GATE) != 0;
     kda_status_t st = check_shape(d_k, d_v, dtype);
     if (st != KDA_OK) return st;
@@ -215,6 +222,7 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     const size_t after_desc = ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) + ws_desc_bytes(num_seqs, total_tokens);
     if (full) {
         if (!(flags & KDA_FLAG_NO_STREAM)) p.flags = reinterpret_cast<int *>(ws + after_desc);
+        p.stream_force = (flags & KDA_FLAG_STREAM) != 0;
         p.records = ws + after_desc + ws_flags_bytes(num_seqs, total_tokens, num_heads);
     } else if (segmented) {
         p.carry = reinterpret_cast<float *>(ws + after_desc);
@@ -323,7 +331,7 @@ kda_status_t kda_decode_step_slots(const void *q, const void *k, const void *v, 
                                    const int32_t *slots, void *o, uint32_t *device_errors, void *stream,
                                    uint32_t flags)
 {
-    if (flags & ~kKnownFlags) return KDA_ERR_INVALID_ARG;
+    if (!flags_valid(flags)) return KDA_ERR_INVALID_ARG;
     const bool scalar_gate = (flags & KDA_FLAG_SCALAR_GATE) != 0;
     kda_status_t st = check_shape(d_k, d_v, dtype);
     if (st != KDA_OK) return st;
@@ -353,7 +361,7 @@ kda_status_t kda_decode_step_ex(const void *q, const void *k, const void *v, con
                                 int32_t d_v, kda_dtype_t dtype, float *state, void *o, void *stream,
                                 uint32_t flags)
 {
-    if (flags & ~kKnownFlags) return KDA_ERR_INVALID_ARG;
+    if (!flags_valid(flags)) return KDA_ERR_INVALID_ARG;
     const bool scalar_gate = (flags & KDA_FLAG_SCALAR_GATE) != 0;
     kda_status_t st = check_shape(d_k, d_v, dtype);
     if (st != KDA_OK) return st;

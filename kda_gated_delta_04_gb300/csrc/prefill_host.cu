@@ -182,7 +182,9 @@ kda_status_t kda_prefill_host(const void *q, const void *k, const void *v, const
     if (dtype != KDA_DTYPE_BF16 && dtype != KDA_DTYPE_F32) return KDA_ERR_INVALID_ARG;
     if (d_k != d_v || (d_k != 64 && d_k != 128)) return KDA_ERR_UNSUPPORTED;
     if (num_seqs > 65535 || num_heads > 65535) return KDA_ERR_UNSUPPORTED;
-    if (flags & ~(uint32_t)(KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM | KDA_FLAG_NO_SEQ_SPLIT | KDA_FLAG_NO_STREAM))
+    if (flags & ~(uint32_t)(KDA_FLAG_SCALAR_GATE | KDA_FLAG_QK_L2NORM | KDA_FLAG_NO_SEQ_SPLIT | KDA_FLAG_NO_STREAM |
+                            KDA_FLAG_STREAM) ||
+        (flags & (KDA_FLAG_STREAM | KDA_FLAG_NO_STREAM)) == (KDA_FLAG_STREAM | KDA_FLAG_NO_STREAM))
         return KDA_ERR_INVALID_ARG;
     if (flags & KDA_FLAG_SCALAR_GATE) return KDA_ERR_UNSUPPORTED;  // log_alpha copies are per channel
     if (total_tokens > 0 && (!q || !k || !v || !log_alpha || !beta)) return KDA_ERR_INVALID_ARG;

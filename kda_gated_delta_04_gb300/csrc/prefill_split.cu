@@ -1021,10 +1021,18 @@ constexpr uint32_t TW_D = 0, TW_O = 128, TW_A = 192, kWalkTmem = 256;
 constexpr int kWalkStateWarps = 8;
 constexpr int kWalkCols = 64;    // value columns per walker: two walkers per (sequence, head)
 constexpr int kMaxWalkers = 64;  // walker CTAs of the streamed prefill at most (32 units)
-// Fewest (sequence, head) units the streamed prefill takes: with fewer, the walk (about 1.9 us
-// per chunk) outlasts the chunk work beside it, and the separate state pass (about 1 us per
-// chunk, or the sequence split) is faster.
-constexpr int kMinStreamUnits = 20;
+// Fewest (sequence, head) units for which the streamed prefill is the faster form, by the
+// chunks per unit.  The walk takes about 1.9 us per chunk whatever the unit count, and the
+// two kernels' time grows with it (the chunk work, before the state pass at about 1 us per
+// chunk); the walk's fixed start (the first records) matters less on longer sequences.
+// Measured crossovers (one sequence): about 31 units at 64 chunks (T = 4096: 0.153 ms as two
+// kernels against 0.158 streamed at 30 units, 0.160 against 0.157 at 32), about 27 at 256
+// (T = 16384: 0.486 against 0.506 ms at 24 units, 0.533 against 0.515 at 28), fewer still at
+// 1024 (T = 65536, 32 units: 2.24 against 2.0 ms).
+inline int min_stream_units(int64_t chunks_per_unit)
+{
+    return chunks_per_unit <= 96 ? 31 : (chunks_per_unit <= 384 ? 27 : 24);
+}
 // First chunk whose record a walker prefetches into L2 two chunks ahead.  The walk trails the
 // chunk work by a little more each chunk (about 12 %), so early records are read while still
 // in L2 and the prefetch only costs a copy on the critical path (T = 4096: 1.7 % slower with
@@ -1657,17 +1665,25 @@ cudaError_t launch_stream(const PrefillProblem &p, const CUtensorMap &tq, const 
 
 }  // namespace
 
-bool prefill_stream_fits(int64_t units)
+int64_t mean_chunks_per_sequence(int32_t num_seqs, int64_t total_tokens)
+{
+    if (num_seqs <= 0 || total_tokens <= 0) return 0;
+    return ((total_tokens + num_seqs - 1) / num_seqs + kC - 1) / kC;
+}
+
+bool prefill_stream_fits(int64_t units, int64_t chunks_per_unit, bool force)
 {
     const int sms = sm_count();  // the walkers leave at least one worker CTA per SM
     const int64_t walkers = (kD / kWalkCols) * units;
-    return units >= kMinStreamUnits && walkers <= kMaxWalkers && sms > 0 && 2 * (int64_t)sms - walkers >= sms;
+    if (units < 1 || walkers > kMaxWalkers || sms <= 0 || 2 * (int64_t)sms - walkers < sms) return false;
+    return force || units >= min_stream_units(chunks_per_unit);
 }
 
 bool prefill_stream_eligible(const PrefillProblem &p)
 {
     return p.flags && p.split.lseg == 0 && p.seg_chunks == 0 &&
-           prefill_stream_fits((int64_t)p.num_seqs * p.num_heads);
+           prefill_stream_fits((int64_t)p.num_seqs * p.num_heads, mean_chunks_per_sequence(p.num_seqs, p.total_tokens),
+                               p.stream_force);
 }
 
 cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, void *records, cudaEvent_t mid)

@@ -25,6 +25,7 @@ KDA_FLAG_SCALAR_GATE = 1
 KDA_FLAG_QK_L2NORM = 2
 KDA_FLAG_NO_SEQ_SPLIT = 4
 KDA_FLAG_NO_STREAM = 8
+KDA_FLAG_STREAM = 16
 KDA_PATH_CUDA_CORE, KDA_PATH_FUSED, KDA_PATH_TWO_KERNEL, KDA_PATH_SEQ_SPLIT, KDA_PATH_SEGMENTED, \
     KDA_PATH_STREAMED = range(6)
 CHUNK = 64
@@ -251,11 +252,13 @@ def _ptr(t, name, dtype=None):
     return t.data_ptr()
 
 
-def _flags(log_alpha, qk_l2norm, seq_split=True, streamed=True):
-    """Option bits: a log_alpha without a channel axis is the scalar gate."""
+def _flags(log_alpha, qk_l2norm, seq_split=True, streamed=None):
+    """Option bits: a log_alpha without a channel axis is the scalar gate; streamed None leaves
+    the streamed form to the library, True asks for it (KDA_FLAG_STREAM), False rules it out
+    (KDA_FLAG_NO_STREAM)."""
     return ((KDA_FLAG_SCALAR_GATE if log_alpha.dim() == 2 else 0) |
             (KDA_FLAG_QK_L2NORM if qk_l2norm else 0) | (0 if seq_split else KDA_FLAG_NO_SEQ_SPLIT) |
-            (0 if streamed else KDA_FLAG_NO_STREAM))
+            (0 if streamed is None else (KDA_FLAG_STREAM if streamed else KDA_FLAG_NO_STREAM)))
 
 
 def _stream_handle(stream, device):
@@ -290,15 +293,18 @@ def min_workspace_bytes(num_seqs):
 
 def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=None,
             final_state=None, workspace=None, stream=None, check_status=False, outputs=True,
-            qk_l2norm=False, seq_split=True, streamed=True):
+            qk_l2norm=False, seq_split=True, streamed=None):
     """KDA prefill over packed sequences.  q, k: [T, H, d]; v: [T, H, d]; log_alpha: [T, H, d]
     fp32; beta: [T, H] fp32; cu_seqlens: int32 [N+1] CUDA tensor or None (one sequence);
     init_state: [N, H, d, d] fp32 or None.  Returns (o, final_state); with outputs=False
     only the final states are computed and o is None.  A log_alpha of shape [T, H] is the
     scalar-gate (Gated DeltaNet) variant: one decay per token-head for every key channel.
     qk_l2norm=True: q and k are raw and the kernels L2-normalise their rows.  seq_split=False
-    keeps each sequence's state pass in one piece (KDA_FLAG_NO_SEQ_SPLIT); streamed=False runs
-    the chunk kernel and the state pass one after the other (KDA_FLAG_NO_STREAM)."""
+    keeps each sequence's state pass in one piece (KDA_FLAG_NO_SEQ_SPLIT).  streamed: None (the
+    default) leaves it to the library whether the chunk work and the state walk share one launch
+    (it does so where that is the faster form); True asks for that whenever the launch holds it
+    (KDA_FLAG_STREAM); False runs the chunk kernel and the state pass one after the other
+    (KDA_FLAG_NO_STREAM)."""
     torch = _torch()
     T, H, d = q.shape
     dt = _dtype_code(q)
@@ -331,7 +337,7 @@ def prefill(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=Non
 
 def prefill_slots(q, k, v, log_alpha, beta, cu_seqlens, state_pool, final_slots, init_slots=None, *,
                   o=None, workspace=None, stream=None, check_status=False, outputs=True,
-                  qk_l2norm=False, seq_split=True, streamed=True):
+                  qk_l2norm=False, seq_split=True, streamed=None):
     """Prefill into a paged state cache: sequence n starts from state_pool[init_slots[n]]
     (zero when init_slots is None or the entry is -1) and its final state is written to
     state_pool[final_slots[n]].  state_pool [S, H, d, d] fp32; slots int32 CUDA tensors [N].
@@ -382,7 +388,7 @@ def _hptr(t, name, dtype=None):
 
 def prefill_host(q, k, v, log_alpha, beta, cu_seqlens=None, init_state=None, *, o=None, final_state=None,
                  device_buffer=None, device=None, stream=None, outputs=True, qk_l2norm=False, seq_split=True,
-                 streamed=True):
+                 streamed=None):
     """kda_prefill_host: q, k, v, log_alpha, beta, cu_seqlens (int32), init_state and the outputs
     in host memory (pin them for the copies to overlap with the prefill).  Returns (o, final_state)
     as host tensors, valid once `stream` has been synchronised."""

@@ -33,7 +33,7 @@ def to_device(inp, device="cuda"):
     return out
 
 
-def gpu_prefill(inp, device="cuda", init_state_inplace=False, check_status=True, streamed=True):
+def gpu_prefill(inp, device="cuda", init_state_inplace=False, check_status=True, streamed=None):
     d = to_device(inp, device)
     cu = d["cu_seqlens"]
     fs = d["init_state"] if init_state_inplace else None

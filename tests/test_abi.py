@@ -96,6 +96,8 @@ def test_prefill_path_query(kda):
     assert kda.kda_prefill_path(N, T, H, 128, 128, 0, full, off) == kda.KDA_PATH_TWO_KERNEL
     assert kda.kda_prefill_path(N, T, H, 128, 128, 0, minimal - 1, 0) == -kda.KDA_ERR_INVALID_ARG
     assert kda.kda_prefill_path(N, T, H, 128, 128, 0, full, 1 << 9) == -kda.KDA_ERR_INVALID_ARG
+    both = kda.KDA_FLAG_STREAM | kda.KDA_FLAG_NO_STREAM  # asking for and ruling out the streamed form
+    assert kda.kda_prefill_path(N, T, H, 128, 128, 0, full, both) == -kda.KDA_ERR_INVALID_ARG
     assert kda.kda_prefill_path(N, T, H, 96, 96, 0, full, 0) == -kda.KDA_ERR_UNSUPPORTED
 
 

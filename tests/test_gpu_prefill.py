@@ -34,7 +34,7 @@ def test_small_problems_match_oracle(w):
     assert_parity(o, fs, o_ref, fs_ref, w.dtype, w.name)
 
 
-def _whole_tensor_parity(w, group, streamed=True):
+def _whole_tensor_parity(w, group, streamed=None):
     """Run the whole workload on the GPU exactly as the benchmark launches it, then check
     every (sequence, head) unit against the oracle, `group` heads at a time (so host memory
     stays bounded): o element by element (max-abs over the whole output), the final state by

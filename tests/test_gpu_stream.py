@@ -1,8 +1,10 @@
 """The streamed prefill (chunk work and state walk in one launch) against the oracle and
 against the two-kernel form (KDA_FLAG_NO_STREAM) on the same inputs.
 
-Every shape here has 20 to 32 (sequence, head) units and no sequence split, so the default
-call takes the streamed kernel; streamed=False runs the chunk kernel and then the state pass.
+streamed=True asks for the streamed kernel (KDA_FLAG_STREAM; every shape here has at most 32
+(sequence, head) units and no sequence split, so the launch holds it), streamed=False runs the
+chunk kernel and then the state pass; the default call takes the streamed form only where it
+is the faster one.
 Both are checked element by element against the fp64 oracle; their difference from each
 other is printed (it is rounding only: the walk forms its products transposed)."""
 import numpy as np
@@ -86,7 +88,7 @@ def test_streamed_prefill_into_state_pool():
     final_slots = torch.tensor([1, 5, 6], dtype=torch.int32, device="cuda")
     before = pool.clone()
     o = kda.prefill_slots(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], pool, final_slots,
-                          init_slots, check_status=True)
+                          init_slots, check_status=True, streamed=True)
     torch.cuda.synchronize()
     s0 = torch.stack([before[4], torch.zeros_like(before[0]), before[0]]).cpu()
     ref_inp = dict(inp)
@@ -101,8 +103,10 @@ def test_streamed_prefill_into_state_pool():
 def test_prefill_path_of_the_benchmark_shapes():
     """kda_prefill_path on the device: the single-sequence H = 32 workloads (32 units) stream
     unless KDA_FLAG_NO_STREAM; a 16-sequence pack (512 units) runs the two kernels; four heads
-    over 65,536 tokens take the sequence split, and without it the two kernels (too few
-    units to stream)."""
+    over 65,536 tokens take the sequence split, and without it the two kernels (too few units
+    for the streamed form to be the faster one) unless KDA_FLAG_STREAM asks for it.  The unit
+    count from which the default call streams falls with the sequence length: 31 at 64 chunks,
+    27 at 256, 24 at 1024."""
     def path(N, T, H, flags=0):
         ws = kda.kda_prefill_workspace_size(N, T, H, 128, 128, kda.KDA_DTYPE_BF16)
         return kda.kda_prefill_path(N, T, H, 128, 128, kda.KDA_DTYPE_BF16, ws, flags)
@@ -112,8 +116,17 @@ def test_prefill_path_of_the_benchmark_shapes():
     assert path(16, 168023, 32) == kda.KDA_PATH_TWO_KERNEL
     assert path(1, 65536, 4) == kda.KDA_PATH_SEQ_SPLIT
     assert path(1, 65536, 4, kda.KDA_FLAG_NO_SEQ_SPLIT) == kda.KDA_PATH_TWO_KERNEL
+    assert path(1, 65536, 4, kda.KDA_FLAG_NO_SEQ_SPLIT | kda.KDA_FLAG_STREAM) == kda.KDA_PATH_STREAMED
     assert path(1, 4096, 16) != kda.KDA_PATH_STREAMED
-    assert path(1, 4096, 20) == kda.KDA_PATH_STREAMED
+    assert path(1, 4096, 30) == kda.KDA_PATH_TWO_KERNEL
+    assert path(1, 4096, 31) == kda.KDA_PATH_STREAMED
+    assert path(1, 4096, 24, kda.KDA_FLAG_STREAM) == kda.KDA_PATH_STREAMED
+    assert path(1, 16384, 26) == kda.KDA_PATH_TWO_KERNEL
+    assert path(1, 16384, 27) == kda.KDA_PATH_STREAMED
+    assert path(1, 65536, 23) == kda.KDA_PATH_TWO_KERNEL
+    assert path(1, 65536, 24) == kda.KDA_PATH_STREAMED
+    assert path(2, 8192, 16) == kda.KDA_PATH_STREAMED       # 32 units of 64 chunks on average
+    assert path(1, 4096, 40, kda.KDA_FLAG_STREAM) == kda.KDA_PATH_TWO_KERNEL  # 80 walkers: no room
 
 
 @pytest.mark.parametrize("case", ["decay", "value", "cu_seqlens"])
@@ -135,8 +148,9 @@ def test_streamed_errors_are_reported_not_faulted(case):
         d["cu_seqlens"] = torch.tensor([0, 100, 60, 200], dtype=torch.int32, device="cuda")
     T = sum(lens)
     ws = kda.workspace_for(len(lens), T, H, 128, kda.KDA_DTYPE_BF16, "cuda")
-    assert kda.kda_prefill_path(len(lens), T, H, 128, 128, kda.KDA_DTYPE_BF16, ws.numel(), 0) == kda.KDA_PATH_STREAMED
-    kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], workspace=ws)
+    assert kda.kda_prefill_path(len(lens), T, H, 128, 128, kda.KDA_DTYPE_BF16, ws.numel(),
+                                kda.KDA_FLAG_STREAM) == kda.KDA_PATH_STREAMED
+    kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], workspace=ws, streamed=True)
     st = kda.kda_read_device_status(ws.data_ptr(), torch.cuda.current_stream().cuda_stream)
     expected = {"decay": kda.KDA_ERR_DECAY_RANGE, "value": kda.KDA_ERR_VALUE_RANGE,
                 "cu_seqlens": kda.KDA_ERR_INVALID_ARG}[case]
@@ -163,3 +177,21 @@ def test_streamed_results_do_not_depend_on_timing():
                 flush.zero_()
             o, s = kda.prefill(*args, check_status=True, streamed=streamed)
             assert torch.equal(o, o0) and torch.equal(s, s0), f"call {i + 1} differs (streamed={streamed})"
+
+
+def test_streamed_form_with_few_units_when_asked():
+    """KDA_FLAG_STREAM with few (sequence, head) units, where the default call would not stream:
+    four heads, then one, over ragged sequences without the sequence split (two walkers per
+    unit, the rest of the grid working), against the oracle."""
+    for name, seed, H, lens in (("stream_forced_H4", 340, 4, (1000, 300)), ("stream_forced_H1", 341, 1, (777,))):
+        w = PrefillWorkload(name, seed, H, 128, "bf16", lens, len(lens), init_state=True)
+        inp = synth.prefill_inputs(w)
+        d = to_device(inp)
+        T = sum(lens)
+        flags = kda.KDA_FLAG_STREAM | kda.KDA_FLAG_NO_SEQ_SPLIT
+        ws = kda.kda_prefill_workspace_size(len(lens), T, H, 128, 128, kda.KDA_DTYPE_BF16)
+        assert kda.kda_prefill_path(len(lens), T, H, 128, 128, kda.KDA_DTYPE_BF16, ws, flags) == kda.KDA_PATH_STREAMED
+        o, fs = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"],
+                            check_status=True, seq_split=False, streamed=True)
+        o_ref, fs_ref = oracle_prefill(inp)
+        assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, w.dtype, name)
