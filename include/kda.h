@@ -247,9 +247,12 @@ kda_status_t kda_prefill_events_ex(const void *q, const void *k, const void *v, 
 #define KDA_FLAG_QK_L2NORM 2u
 /*  KDA_FLAG_NO_SEQ_SPLIT  keep each sequence's serial state pass in one piece.  By
  *                        default, when a bf16 d = 128 problem has so few (sequence,
- *                        head) units that the state pass would leave most SMs idle, and
- *                        the workspace was sized by kda_prefill_workspace_size for that
- *                        shape, every sequence is cut into segments of whole chunks: a
+ *                        head) units that the state pass would leave most SMs idle (at
+ *                        most 19), sequences long enough for the split to pay (on average
+ *                        at least 72 chunks of 64 tokens with up to 8 units, 15 per unit
+ *                        less 50 beyond), and the workspace was sized by
+ *                        kda_prefill_workspace_size for that shape, every sequence is cut
+ *                        into segments of whole chunks: a
  *                        transition pass gives each segment its affine map (the
  *                        chunkwise form makes every chunk's update affine in its start
  *                        state), the maps are chained in fp32 into each segment's start

@@ -191,6 +191,13 @@ int seqsplit_lseg(int num_seqs, int64_t total_tokens, int num_heads)
     // the transition pass runs 4 CTAs (R and M, two 64-column slices each) per segment and head
     const int64_t kmax = 1 + kSplitSMs / (4 * units);
     const int64_t avg = (total_tokens / kChunk + num_seqs) / num_seqs;  // chunks per sequence
+    // The split pays once the serial pass it shortens outweighs the transition pass and the
+    // chaining it adds, which takes longer sequences the more units there are.  Timed on one
+    // sequence (the two kernels against the split): from about 72 chunks with up to 8 units,
+    // about 190 with 16, between 192 and 256 with 19 (T = 4096, 64 chunks: the two kernels
+    // 0.085 against 0.099 ms at 4 heads, 0.124 against 0.152 at 19; T = 16384: the split
+    // 0.199 against 0.320 ms at 4 heads, 0.460 against 0.473 at 19).
+    if (avg < (units <= 8 ? 72 : 15 * units - 50)) return 0;
     int64_t k = avg / kMinSegChunks;
     if (k > kmax) k = kmax;
     if (k < 3) return 0;  // two segments cost as much as they save

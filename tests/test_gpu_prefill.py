@@ -475,8 +475,8 @@ def test_in_kernel_qk_l2_normalisation(case):
 
 
 SPLIT_CASES = [  # few (sequence, head) units: the state pass runs in segments
-    PrefillWorkload("split_H2_T2000_state", 128, 2, 128, "bf16", (2000,), 1, init_state=True),
-    PrefillWorkload("split_H1_varlen_state", 129, 1, 128, "bf16", (2000, 0, 3000, 64, 1), 5,
+    PrefillWorkload("split_H2_T6000_state", 128, 2, 128, "bf16", (6000,), 1, init_state=True),
+    PrefillWorkload("split_H1_varlen_state", 129, 1, 128, "bf16", (10000, 0, 13000, 64, 1), 5,
                     init_state=True),
 ]
 
@@ -496,7 +496,14 @@ def test_sequence_split_state_pass(w):
     o_ref, fs_ref = oracle_prefill(inp)
     assert_parity(synth.to_f64(o_s), synth.to_f64(fs_s), o_ref, fs_ref, "bf16", "split " + w.name)
     assert_parity(synth.to_f64(o_n), synth.to_f64(fs_n), o_ref, fs_ref, "bf16", "unsplit " + w.name)
-    assert not np.array_equal(synth.to_f64(fs_s), synth.to_f64(fs_n))
+    # the split did run: the call takes that path, and the outputs differ from the unsplit
+    # pass by rounding (the final states may not: with segments of 10 chunks the decay leaves
+    # no trace of a start state's rounding by the end of a sequence)
+    T = sum(w.seq_lens)
+    ws_bytes = kda.kda_prefill_workspace_size(len(w.seq_lens), T, w.num_heads, 128, 128, kda.KDA_DTYPE_BF16)
+    assert kda.kda_prefill_path(len(w.seq_lens), T, w.num_heads, 128, 128, kda.KDA_DTYPE_BF16, ws_bytes, 0) == \
+        kda.KDA_PATH_SEQ_SPLIT
+    assert not np.array_equal(synth.to_f64(o_s), synth.to_f64(o_n))
     np.testing.assert_array_equal(synth.to_f64(fs_only), synth.to_f64(fs_s))
     # the same problem against a state pool: start slots reversed, one sequence from zero
     N, H = len(w.seq_lens), w.num_heads
@@ -534,7 +541,7 @@ def test_options_together_on_a_split_problem():
     slot is untouched, and the stored states are within the bar of the oracle run on the
     broadcast gate and fp64-normalised q, k."""
     H = 2
-    w = PrefillWorkload("options_split", 135, H, 128, "bf16", (1500, 900, 40), 3, init_state=True,
+    w = PrefillWorkload("options_split", 135, H, 128, "bf16", (9000, 5400, 240), 3, init_state=True,
                         raw_qk=True)
     inp = synth.prefill_inputs(w)
     la_s, la_full = _scalar_gate(inp, 135)
