@@ -79,7 +79,7 @@ def test_segmented_workspace_size(kda):
 
 def test_prefill_path_query(kda):
     """kda_prefill_path, on the shapes and workspaces that decide it without the device (the
-    streamed and sequence-split choices are checked on the GPU): fp32 and d = 64 take the
+    streamed choice is checked on the GPU, the sequence split below): fp32 and d = 64 take the
     CUDA-core kernel, a bf16 d = 128 call with the minimal workspace the fused kernel, with a
     bounded-records workspace the segmented pass, and with the full workspace the two kernels
     when streaming and the sequence split are turned off.  Rejected arguments give the
@@ -100,6 +100,30 @@ def test_prefill_path_query(kda):
     assert kda.kda_prefill_path(N, T, H, 128, 128, 0, full, both) == -kda.KDA_ERR_INVALID_ARG
     assert kda.kda_prefill_path(N, T, H, 96, 96, 0, full, 0) == -kda.KDA_ERR_UNSUPPORTED
 
+
+
+def test_sequence_split_choice(kda):
+    """Which bf16 d = 128 calls with the full workspace take the sequence-split state pass
+    (decided without the device; KDA_FLAG_NO_STREAM keeps the streamed form out of the
+    answer).  Only up to 19 (sequence, head) units, so that the transition pass fits one
+    wave, and only for sequences long enough for the split to pay, a bound that grows with
+    the unit count.  The cases follow the timings the rule was set from: at 64 chunks per
+    sequence the two kernels are faster at every unit count, at 96 the split is faster with
+    4 and 8 units but not with 16 or 19, at 256 it is faster at every count up to 19."""
+    def path(N, T, H, flags=0):
+        ws = kda.kda_prefill_workspace_size(N, T, H, 128, 128, 0)
+        return kda.kda_prefill_path(N, T, H, 128, 128, 0, ws, flags | kda.KDA_FLAG_NO_STREAM)
+    split, two = kda.KDA_PATH_SEQ_SPLIT, kda.KDA_PATH_TWO_KERNEL
+    for H in (1, 4, 8, 16, 19):
+        assert path(1, 4096, H) == two, H
+        assert path(1, 16384, H) == split, H
+    for H, want in ((4, split), (8, split), (16, two), (19, two)):
+        assert path(1, 6144, H) == want, H
+    assert path(2, 16384, 4) == split            # two sequences of 128 chunks: 8 units
+    assert path(4, 16384, 4) == two              # four of 64 chunks: too short
+    assert path(1, 65536, 20) == two             # 20 units: the transition pass needs two waves
+    assert path(1, 65536, 4, kda.KDA_FLAG_NO_SEQ_SPLIT) == two
+    assert path(1, 256, 1) == two                # 4 chunks: no room for three segments
 
 FAKE = 1 << 20  # 16-byte aligned dummy address; never dereferenced (rejected first)
 

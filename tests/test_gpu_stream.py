@@ -117,7 +117,8 @@ def test_prefill_path_of_the_benchmark_shapes():
     assert path(1, 65536, 4) == kda.KDA_PATH_SEQ_SPLIT
     assert path(1, 65536, 4, kda.KDA_FLAG_NO_SEQ_SPLIT) == kda.KDA_PATH_TWO_KERNEL
     assert path(1, 65536, 4, kda.KDA_FLAG_NO_SEQ_SPLIT | kda.KDA_FLAG_STREAM) == kda.KDA_PATH_STREAMED
-    assert path(1, 4096, 16) != kda.KDA_PATH_STREAMED
+    assert path(1, 4096, 16) == kda.KDA_PATH_TWO_KERNEL   # 64 chunks: too short for the split as well
+    assert path(1, 4096, 4) == kda.KDA_PATH_TWO_KERNEL
     assert path(1, 4096, 30) == kda.KDA_PATH_TWO_KERNEL
     assert path(1, 4096, 31) == kda.KDA_PATH_STREAMED
     assert path(1, 4096, 24, kda.KDA_FLAG_STREAM) == kda.KDA_PATH_STREAMED
