@@ -8,8 +8,9 @@ timed in the same run on its own workload (256 sequences x 32 heads, d=128,
 1000 in-place steps) and reported under "decode".  The two larger prefill
 workloads are timed in the same run, each with its own roofline and oracle
 baseline: one sequence of T=65536 tokens from a nonzero initial state under
-"long_prefill" (beside it, "bounded_records": the same call with a workspace whose
-per-chunk records cover 128 chunks at a time), and 16 packed sequences of
+"long_prefill" (beside it, "bounded_records": the same call in the two-kernel form with a
+workspace whose per-chunk records cover 128 chunks at a time, and "streamed_ring": the
+streamed call with records for a ring of 16 chunks), and 16 packed sequences of
 512..16384 tokens (168,023 in all) under "varlen_prefill".  A long single sequence with few heads (T=65536, H=4),
 where the serial state pass would leave most SMs idle, is timed with and
 without the sequence-split state pass under "long_context".
@@ -53,6 +54,7 @@ METRIC = "KDA prefill tokens/s & decode steps/s (H=32,d=128) and % of roofline"
 L2_FLUSH_BYTES = 256 << 20
 CASE_STEPS = 5  # timed calls of each further prefill workload (2.5 to 10 ms each)
 BOUNDED_CHUNKS = 128  # packed chunks per segment of the bounded-records measurement (T=65536: 8 segments)
+RING_CHUNKS = 16      # packed chunks whose records the streamed-ring measurement keeps
 
 
 def _env_rank():
@@ -458,7 +460,7 @@ class _Gpu:
         c["path"] = kda.kda_prefill_path(N, T, H, d, d, kda.KDA_DTYPE_BF16, c["ws"].numel(), 0)
         return c
 
-    def case_call(self, c, events=None, ws=None):
+    def case_call(self, c, events=None, ws=None, flags=0):
         kda, x = self.kda, c["x"]
         ws = c["ws"] if ws is None else ws
         s0 = None if x["init_state"] is None else x["init_state"].data_ptr()
@@ -466,24 +468,30 @@ class _Gpu:
                 x["beta"].data_ptr(), x["cu_seqlens"].data_ptr(), c["N"], c["T"], c["H"], c["d"],
                 c["d"], kda.KDA_DTYPE_BF16, s0, c["o"].data_ptr(), c["fs"].data_ptr(),
                 ws.data_ptr(), ws.numel(), self.sh)
-        st = kda.kda_prefill(*args) if events is None else kda.kda_prefill_events(*args, events)
+        if flags:
+            st = kda.kda_prefill_ex(*args, flags)
+        else:
+            st = kda.kda_prefill(*args) if events is None else kda.kda_prefill_events(*args, events)
         if st != kda.KDA_OK:
             raise kda.KdaError(st, "kda_prefill")
 
-    def time_bounded(self, c, segment_chunks, steps, warmup):
+    def time_bounded(self, c, chunks, steps, warmup, ring=False):
         """Event time (ms per call) of the same prefill with a workspace whose per-chunk
-        records cover only `segment_chunks` packed chunks (the pass then runs in segments);
-        returns (ms, workspace bytes)."""
+        records cover only `chunks` packed chunks: the two kernels over segments of that many
+        chunks (KDA_FLAG_NO_STREAM), or with ring=True the streamed kernel over a ring of
+        them; returns (ms, workspace bytes)."""
         torch = self.torch
-        ws = self.kda.segmented_workspace_for(c["N"], c["T"], c["H"], c["d"], self.kda.KDA_DTYPE_BF16,
-                                              self.dev, segment_chunks)
+        kda = self.kda
+        make = kda.streamed_workspace_for if ring else kda.segmented_workspace_for
+        ws = make(c["N"], c["T"], c["H"], c["d"], kda.KDA_DTYPE_BF16, self.dev, chunks)
+        flags = 0 if ring else kda.KDA_FLAG_NO_STREAM
         for _ in range(warmup):
-            self.case_call(c, ws=ws)
+            self.case_call(c, ws=ws, flags=flags)
         torch.cuda.synchronize()
         a, b = self.event(), self.event()
         a.record(self.stream)
         for _ in range(steps):
-            self.case_call(c, ws=ws)
+            self.case_call(c, ws=ws, flags=flags)
         b.record(self.stream)
         torch.cuda.synchronize()
         st = self.kda.kda_read_device_status(ws.data_ptr(), self.sh)
@@ -613,6 +621,8 @@ def run_gpu(args):
             case_ms[name] = (c, g.time_case(c, CASE_STEPS, max(3, args.warmup)))
             if name == "long_prefill":  # the same call with records for BOUNDED_CHUNKS chunks at a time
                 c["bounded"] = g.time_bounded(c, BOUNDED_CHUNKS, CASE_STEPS, max(3, args.warmup))
+                if c["path"] == PATH_STREAMED:  # and with the records of a ring of RING_CHUNKS chunks
+                    c["ring"] = g.time_bounded(c, RING_CHUNKS, CASE_STEPS, max(3, args.warmup), ring=True)
                 c["full_ws_bytes"] = c["ws"].numel()
             c["with_init"] = c["inp"]["init_state"] is not None
             # the oracle's sample is cut out now; the full host inputs are dropped
@@ -694,9 +704,22 @@ def run_gpu(args):
             blk["bounded_records"] = {
                 "segment_chunks": BOUNDED_CHUNKS, "workspace_bytes": bws, "full_workspace_bytes": c["full_ws_bytes"],
                 "value": aggregate_rate(T, world, 1, bms), "ms_per_call": bms, "steps": CASE_STEPS,
-                "note": "kda_prefill with a workspace from kda_prefill_workspace_size_segmented: the chunk and "
-                        "state kernels run over segments of that many packed chunks (results bit for bit those "
-                        "of the full workspace in the two-kernel form, KDA_FLAG_NO_STREAM)"}
+                "note": "kda_prefill_ex(KDA_FLAG_NO_STREAM) with a workspace from "
+                        "kda_prefill_workspace_size_segmented: the chunk and state kernels run over segments "
+                        "of that many packed chunks (results bit for bit those of the full workspace in the "
+                        "two-kernel form)"}
+        if "ring" in c:
+            rms, rws = c["ring"]
+            rms = reduce_max(rms)
+            blk["streamed_ring"] = {
+                "ring_chunks": RING_CHUNKS, "workspace_bytes": rws, "full_workspace_bytes": c["full_ws_bytes"],
+                "value": aggregate_rate(T, world, 1, rms), "ms_per_call": rms, "steps": CASE_STEPS,
+                # DRAM bytes per launch (ncu) against the path's algorithmic bytes: the records stay in L2
+                "traffic": profiled_traffic("prefill_stream_kernel_ring%d_64k" % RING_CHUNKS),
+                "algorithmic_bytes_per_launch": blk["roofline"]["algorithmic_bytes_per_launch"],
+                "note": "kda_prefill with a workspace from kda_prefill_workspace_size_streamed: the streamed "
+                        "kernel keeps the records of that many packed chunks, each slot refilled once both "
+                        "walkers have copied its record in (results bit for bit those of the full workspace)"}
         if rank == 0 and world == 1 and not args.no_cpu_baseline:
             blk["cpu_baseline"] = cpu_baseline_case(w, c["cpu_sample"])
         line[name] = blk

@@ -97,7 +97,11 @@ size_t kda_prefill_workspace_size(int32_t num_seqs, int64_t total_tokens, int32_
  * buffers).  The results are bit for bit those of the full workspace without the
  * sequence split (KDA_FLAG_NO_SEQ_SPLIT); each extra segment costs two more launches.
  * Any workspace between this size for segment_chunks = 1 and kda_prefill_workspace_size
- * runs segmented, with as many chunks per segment as its records fit.
+ * runs segmented, with as many chunks per segment as its records fit, when the call runs
+ * the two kernels (KDA_FLAG_NO_STREAM, or too few (sequence, head) units to stream); where
+ * the call would stream, a bounded workspace runs the streamed prefill over a ring of
+ * records instead (kda_prefill_workspace_size_streamed), if it holds those of at least
+ * KDA_STREAM_RING_MIN chunks.
  *
  *  segment_chunks  >= 1; values past the packed chunk bound (total_tokens / 64 +
  *                  num_seqs) are clamped to it.
@@ -109,6 +113,28 @@ size_t kda_prefill_workspace_size_segmented(int32_t num_seqs, int64_t total_toke
                                             int64_t segment_chunks);
 
 /*
+ * Workspace bytes for the streamed prefill (chunk work and state walk in one launch, see
+ * KDA_FLAG_NO_STREAM) with its records kept in a ring of ring_chunks packed chunks: the
+ * record of chunk g (all heads) goes to slot g mod ring_chunks, written only once both
+ * walking CTAs of chunk g - ring_chunks have copied that slot's previous record in.  The
+ * chunk work then leads the walk by at most ring_chunks chunks, and the workspace no
+ * longer grows with the records of every chunk (T = 65536, H = 32: about 39 MB for 16
+ * chunks against 2.44 GB).  The results are bit for bit those of the streamed prefill
+ * with the full workspace.  It is not faster than that: held to the walk's pace, the
+ * chunk work shares the SMs with it to the end.  Any workspace between this size for
+ * KDA_STREAM_RING_MIN chunks and kda_prefill_workspace_size runs this way where the call
+ * streams (kda_prefill_path says so), with as many chunks as its records fit.
+ *
+ *  ring_chunks  >= KDA_STREAM_RING_MIN; values past the packed chunk bound
+ *               (total_tokens / 64 + num_seqs) are clamped to it.
+ *  Returns 0 for invalid arguments and for shapes the streamed prefill does not run
+ *  (anything but bf16, d_k = d_v = 128, total_tokens > 0).
+ */
+#define KDA_STREAM_RING_MIN 8
+size_t kda_prefill_workspace_size_streamed(int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                                           int32_t d_k, int32_t d_v, kda_dtype_t dtype, int64_t ring_chunks);
+
+/*
  * The kernels a kda_prefill_ex call with these arguments runs (the path it takes).
  *  KDA_PATH_CUDA_CORE  fp32 I/O or d = 64: the exact CUDA-core chunk kernel
  *  KDA_PATH_FUSED      bf16, d = 128, workspace below the bounded-records size: one
@@ -116,7 +142,9 @@ size_t kda_prefill_workspace_size_segmented(int32_t num_seqs, int64_t total_toke
  *  KDA_PATH_TWO_KERNEL the chunk kernel, then the state pass
  *  KDA_PATH_SEQ_SPLIT  the chunk kernel, then the sequence-split state pass
  *  KDA_PATH_SEGMENTED  the chunk kernel and the state pass over segments of records
- *  KDA_PATH_STREAMED   chunk work and state walk in one launch (see KDA_FLAG_NO_STREAM)
+ *  KDA_PATH_STREAMED   chunk work and state walk in one launch (see KDA_FLAG_NO_STREAM),
+ *                      with a bounded workspace over a ring of records
+ *                      (kda_prefill_workspace_size_streamed)
  * Host arithmetic plus one device-attribute query (the SM count of the current
  * device); returns a negative kda_status_t for arguments kda_prefill_ex rejects on
  * the host.  Each path also runs the schedule kernel first.
@@ -270,11 +298,14 @@ kda_status_t kda_prefill_events_ex(const void *q, const void *k, const void *v, 
  *                        workspace as soon as its stores are complete.  The two forms
  *                        agree to within rounding, not bit for bit (the walk forms its
  *                        products transposed).  The walking CTAs wait for records that
- *                        the others produce, so the launch needs SM slots for both: if
- *                        kernels on other streams hold all but a few slots for longer
- *                        than the device-side wait limit (2 s), the walk gives up with
+ *                        the others produce (and, over a ring of records, those wait for
+ *                        the walk to free a slot), so the launch needs SM slots for both:
+ *                        if kernels on other streams hold all but a few slots for longer
+ *                        than the device-side wait limit (2 s), the call gives up with
  *                        KDA_ERR_TIMEOUT instead of hanging.  The two-kernel form has no
- *                        such dependence; pass this flag where the GPU is shared that way. */
+ *                        such dependence; pass this flag where the GPU is shared that way
+ *                        (with a bounded workspace it then runs the two kernels in
+ *                        segments). */
 #define KDA_FLAG_NO_STREAM 8u
 /*  KDA_FLAG_STREAM        run both in one launch whenever the launch holds the walking CTAs
  *                        (1 to 32 units on a 152-SM GB300; same conditions otherwise),

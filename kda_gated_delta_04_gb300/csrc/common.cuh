@@ -77,10 +77,14 @@ struct PrefillProblem {
     // carry (two [num_heads, d, d] fp32 buffers, alternating by segment).  0: unsegmented.
     int seg_chunks = 0;
     float *carry = nullptr;
-    // one ready flag per chunk-head record ([chunk_bound, num_heads]) and one item counter
-    // after them, zeroed by the schedule kernel: the streamed prefill publishes each record
-    // through its flag.  Null: no streaming.
+    // a ready flag and a copy count per chunk-head record ([chunk_bound, num_heads] each) and
+    // one item counter after them, zeroed by the schedule kernel: the streamed prefill
+    // publishes each record through its flag and frees its slot through its count.  Null:
+    // no streaming.
     int *flags = nullptr;
+    // streamed prefill: records kept for ring_chunks packed chunks (slot g mod ring_chunks);
+    // 0 or chunk_bound: one slot per chunk (a workspace that holds every record)
+    int ring_chunks = 0;
     // stream whenever the launch holds the walkers (KDA_FLAG_STREAM), not only where the
     // streamed form is the faster one
     bool stream_force = false;
@@ -134,6 +138,9 @@ bool prefill_stream_eligible(const PrefillProblem &p);
 // unit beside at least one worker CTA per SM, and (unless `force`) there are enough units
 // for the streamed form to be the faster one at that length.
 bool prefill_stream_fits(int64_t units, int64_t chunks_per_unit, bool force);
+// Fewest packed chunks whose records a bounded workspace must hold for the streamed prefill
+// to run over a ring of them (fewer: the two kernels in segments).
+constexpr int kStreamRingMin = KDA_STREAM_RING_MIN;
 // The mean chunk count of a sequence, ceil(ceil(total_tokens / num_seqs) / 64) (0 with no
 // sequences).
 int64_t mean_chunks_per_sequence(int32_t num_seqs, int64_t total_tokens);

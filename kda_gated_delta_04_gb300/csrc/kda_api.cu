@@ -53,10 +53,12 @@ bool split_shape(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int3
            total_tokens <= 0x7fffffffll &&
            (total_tokens / KDA_CHUNK + num_seqs) * (int64_t)num_heads <= 0x7fffffffll;
 }
-// one ready flag (int32) per chunk-head record and an item counter, for the streamed prefill
+// a ready flag and a copy count (int32 each) per chunk-head record and an item counter, for
+// the streamed prefill
 size_t ws_flags_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
 {
-    return round_up(((size_t)chunk_bound(num_seqs, total_tokens) * (size_t)num_heads + 1) * sizeof(int32_t), 256);
+    return round_up((2 * (size_t)chunk_bound(num_seqs, total_tokens) * (size_t)num_heads + 1) * sizeof(int32_t),
+                    256);
 }
 // the two-kernel path: schedule, chunk numbering, descriptors, ready flags and records
 size_t ws_records_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
@@ -64,6 +66,24 @@ size_t ws_records_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_head
     return ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) + ws_desc_bytes(num_seqs, total_tokens) +
            ws_flags_bytes(num_seqs, total_tokens, num_heads) +
            kda::prefill_split_records_bytes(total_tokens, num_seqs, num_heads);
+}
+// the streamed prefill over a ring of records: schedule, chunk numbering, descriptors,
+// flags and counts; the records of as many packed chunks as the rest holds follow
+size_t ws_stream_fixed(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
+{
+    return ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs) + ws_desc_bytes(num_seqs, total_tokens) +
+           ws_flags_bytes(num_seqs, total_tokens, num_heads);
+}
+// packed chunks whose records a workspace of that size holds after the streamed prefill's
+// fixed part, up to all of them; 0 when fewer than kStreamRingMin (and not all)
+int64_t stream_ring_chunks(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, size_t workspace_bytes)
+{
+    const size_t fixed = ws_stream_fixed(num_seqs, total_tokens, num_heads);
+    if (workspace_bytes <= fixed) return 0;
+    const int64_t fit = (int64_t)((workspace_bytes - fixed) / ((size_t)num_heads * kda::prefill_split_record_bytes()));
+    const int64_t all = chunk_bound(num_seqs, total_tokens);
+    const int64_t ring = fit < all ? fit : all;
+    return ring >= kda::kStreamRingMin || ring == all ? ring : 0;
 }
 // ... plus the sequence-split state pass where the shape calls for it
 size_t ws_split_bytes(int32_t num_seqs, int64_t total_tokens, int32_t num_heads)
@@ -97,6 +117,13 @@ int32_t path_for(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int3
             return KDA_PATH_STREAMED;
         return KDA_PATH_TWO_KERNEL;
     }
+    // a bounded workspace: the streamed prefill over a ring of records where the call would
+    // stream, else the two kernels in segments
+    if (split_ok && !(flags & KDA_FLAG_NO_STREAM) &&
+        stream_ring_chunks(num_seqs, total_tokens, num_heads, workspace_bytes) > 0 &&
+        kda::prefill_stream_fits((int64_t)num_seqs * num_heads, kda::mean_chunks_per_sequence(num_seqs, total_tokens),
+                                 (flags & KDA_FLAG_STREAM) != 0))
+        return KDA_PATH_STREAMED;
     const size_t rec_chunk = (size_t)num_heads * kda::prefill_split_record_bytes();
     if (split_ok && workspace_bytes >= ws_segmented_fixed(num_seqs, total_tokens, num_heads) + rec_chunk)
         return KDA_PATH_SEGMENTED;
@@ -144,6 +171,17 @@ size_t kda_prefill_workspace_size_segmented(int32_t num_seqs, int64_t total_toke
     const int64_t seg = segment_chunks < bound ? segment_chunks : bound;
     return ws_segmented_fixed(num_seqs, total_tokens, num_heads) +
            (size_t)seg * (size_t)num_heads * kda::prefill_split_record_bytes();
+}
+
+size_t kda_prefill_workspace_size_streamed(int32_t num_seqs, int64_t total_tokens, int32_t num_heads,
+                                           int32_t d_k, int32_t d_v, kda_dtype_t dtype, int64_t ring_chunks)
+{
+    if (num_seqs < 0 || total_tokens < 0 || num_heads <= 0 || ring_chunks < kda::kStreamRingMin) return 0;
+    if (!split_shape(num_seqs, total_tokens, num_heads, d_k, d_v, dtype)) return 0;
+    const int64_t bound = chunk_bound(num_seqs, total_tokens);
+    const int64_t ring = ring_chunks < bound ? ring_chunks : bound;
+    return ws_stream_fixed(num_seqs, total_tokens, num_heads) +
+           (size_t)ring * (size_t)num_heads * kda::prefill_split_record_bytes();
 }
 
 int32_t kda_prefill_path(int32_t num_seqs, int64_t total_tokens, int32_t num_heads, int32_t d_k,
@@ -214,8 +252,17 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
     const bool full = split_ok && workspace_bytes >= ws_records_bytes(num_seqs, total_tokens, num_heads);
     const size_t rec_chunk = (size_t)num_heads * kda::prefill_split_record_bytes();
     const size_t seg_fixed = split_ok ? ws_segmented_fixed(num_seqs, total_tokens, num_heads) : 0;
-    const bool segmented = split_ok && !full && workspace_bytes >= seg_fixed + rec_chunk;
-    const bool split = full || segmented;
+    // a bounded workspace: the streamed prefill over a ring of records where the call would
+    // stream (the same choice as kda_prefill_path), else the two kernels in segments
+    const int64_t ring = split_ok && !full && !(flags & KDA_FLAG_NO_STREAM)
+                             ? stream_ring_chunks(num_seqs, total_tokens, num_heads, workspace_bytes)
+                             : 0;
+    const bool ring_stream =
+        ring > 0 && kda::prefill_stream_fits((int64_t)num_seqs * num_heads,
+                                             kda::mean_chunks_per_sequence(num_seqs, total_tokens),
+                                             (flags & KDA_FLAG_STREAM) != 0);
+    const bool segmented = split_ok && !full && !ring_stream && workspace_bytes >= seg_fixed + rec_chunk;
+    const bool split = full || ring_stream || segmented;
     p.cc = split ? reinterpret_cast<int32_t *>(ws + ws_min_bytes(num_seqs)) : nullptr;
     p.desc = split ? reinterpret_cast<int2 *>(ws + ws_min_bytes(num_seqs) + ws_cc_bytes(num_seqs)) : nullptr;
     p.chunk_bound = split ? (int)chunk_bound(num_seqs, total_tokens) : 0;
@@ -224,6 +271,11 @@ kda_status_t prefill_impl(const void *q, const void *k, const void *v, const flo
         if (!(flags & KDA_FLAG_NO_STREAM)) p.flags = reinterpret_cast<int *>(ws + after_desc);
         p.stream_force = (flags & KDA_FLAG_STREAM) != 0;
         p.records = ws + after_desc + ws_flags_bytes(num_seqs, total_tokens, num_heads);
+    } else if (ring_stream) {
+        p.flags = reinterpret_cast<int *>(ws + after_desc);
+        p.stream_force = (flags & KDA_FLAG_STREAM) != 0;
+        p.records = ws + after_desc + ws_flags_bytes(num_seqs, total_tokens, num_heads);
+        p.ring_chunks = (int)ring;
     } else if (segmented) {
         p.carry = reinterpret_cast<float *>(ws + after_desc);
         p.records = ws + seg_fixed;

@@ -374,8 +374,9 @@ cudaError_t launch_simt(const PrefillProblem &p)
 
 cudaError_t launch_prefill_prep(const PrefillProblem &p)
 {
-    // the ready flag of every chunk-head record and, after them, the streamed kernel's claim counter
-    const int64_t num_flags = p.flags ? (int64_t)p.chunk_bound * p.num_heads + 1 : 0;
+    // the ready flag and the copy count of every chunk-head record and, after them, the
+    // streamed kernel's claim counter
+    const int64_t num_flags = p.flags ? 2 * (int64_t)p.chunk_bound * p.num_heads + 1 : 0;
     prefill_prep_kernel<<<1, 1024, 0, p.stream>>>(p.cu_seqlens, p.num_seqs, p.total_tokens,
                                                   p.status, p.order, p.cc, p.desc, p.chunk_bound,
                                                   p.flags, num_flags);

@@ -337,6 +337,19 @@ __device__ __forceinline__ void epi_q(uint32_t tmem, unsigned char *dst)
     }
 }
 
+// Waits (acquire, GPU scope) until the counter at p reaches v; false once kWaitNs has
+// passed without it.
+__device__ __forceinline__ bool wait_count_at_least(const int *p, int v)
+{
+    if (ld_acquire_gpu(p) >= v) return true;
+    const uint64_t ts = globaltimer_ns();
+    for (;;) {
+        __nanosleep(128);
+        if (ld_acquire_gpu(p) >= v) return true;
+        if (globaltimer_ns() - ts > kWaitNs) return false;
+    }
+}
+
 // The chunk work: items it0, it0 + stride, ... of the seg_chunks x H (chunk, head) items
 // over the packed chunks g_base .. g_base + seg_chunks - 1, heads fastest.  Run by the
 // chunk kernel (chunks last to first) and by the worker CTAs of the streamed kernel
@@ -348,13 +361,15 @@ __device__ __forceinline__ void epi_q(uint32_t tmem, unsigned char *dst)
 // are always the earliest not yet taken, whichever CTAs are resident, and finish about in
 // the order they were claimed.
 // NORM: q and k arrive raw and are L2-normalised here (KDA_FLAG_QK_L2NORM).
-template <bool NORM, bool STREAM>
+// RING (with STREAM): chunk g's record goes to slot g mod ring, once both walkers have
+// counted chunk g - ring's record as copied in (cons[(g - ring) * H + h] == 2).
+template <bool NORM, bool STREAM, bool RING = false>
 __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUtensorMap &tm_k,
                                             const CUtensorMap &tm_la, const float *__restrict__ log_alpha,
                                             const float *__restrict__ beta, const int2 *__restrict__ desc, int H,
                                             int g_base, int seg_chunks, unsigned char *__restrict__ records,
                                             uint32_t *status, bool with_o, bool scalar_gate, int it0, int stride,
-                                            int *flags, int *claim)
+                                            int *flags, const int *cons, int *claim, int ring)
 {
     using L = ChunkLayout;
     constexpr int NT = kChunkCompute;  // the compute threads' mappings are over 256 threads
@@ -431,7 +446,8 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
         }
         const int64_t c0 = dsc.x;
         const int len = dsc.y;
-        unsigned char *rec = records + ((size_t)(g - g_base) * H + h) * kRecBytes;
+        // RING: the ring slot of chunk g (otherwise every chunk has its own)
+        unsigned char *rec = records + ((size_t)(RING ? g % ring : g - g_base) * H + h) * kRecBytes;
         // the next item, so that its descriptor load overlaps this item's work
         int hn = 0, gn = 0;
         int2 dn = make_int2(0, 0);
@@ -444,7 +460,11 @@ __device__ __forceinline__ void chunk_items(const CUtensorMap &tm_q, const CUten
         // values straight from global memory while the boxes fly
         if (compute && scalar_gate)
             prefix_scan<NT>(log_alpha + (size_t)c0 * H + h, H, len, s_tot, gl, gmin, gmax, true);
-        bool ok = !compute || mbar_wait_ns(&bar_tma, n & 1u, kWaitNs);
+        // RING: both walkers of the slot's previous record (chunk g - ring) have copied it in
+        // before anything of this one (its gamma first) is written there; checked while the
+        // boxes are on their way
+        bool ok = !(RING && tid == 0 && g >= ring) || wait_count_at_least(cons + (size_t)(g - ring) * H + h, 2);
+        ok = ok && (!compute || mbar_wait_ns(&bar_tma, n & 1u, kWaitNs));
         if (compute && !scalar_gate && ok)  // the per-channel prefix from the log_alpha box
             prefix_scan<NT>(reinterpret_cast<const float *>(sm + L::O1), kD, len, s_tot, gl, gmin, gmax);
         // every thread is past its reads of the log_alpha box and s_tot is complete
@@ -612,7 +632,7 @@ prefill_chunk_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_cons
     pdl_launch_dependents();
     // persistent: this CTA takes items blockIdx.x, blockIdx.x + gridDim.x, ...
     chunk_items<NORM, false>(tm_q, tm_k, tm_la, log_alpha, beta, desc, H, g_base, seg_chunks, records, status,
-                             with_o, scalar_gate, (int)blockIdx.x, (int)gridDim.x, nullptr, nullptr);
+                             with_o, scalar_gate, (int)blockIdx.x, (int)gridDim.x, nullptr, nullptr, nullptr, 0);
 }
 
 // ============================================================== state kernel
@@ -975,12 +995,26 @@ prefill_state_kernel(const __grid_constant__ CUtensorMap tm_v, const __grid_cons
 // flag, so the serial pass follows the chunk work closely, its records come back from L2,
 // and the serial chain overlaps the chunk work instead of following it.
 //
-// Progress does not depend on which CTAs are resident: only walkers wait, and only for
-// records; a worker never waits for another CTA, and the items are claimed in order by
-// workers that are running, so the earliest unpublished record is always in work.  The
-// walkers (at most kMaxWalkers) are fewer than the CTAs that one wave holds, so workers
-// always run beside them.  Every wait is bounded all the same (a flag that does not come
-// up within the limit is recorded as KDA_ERR_TIMEOUT and the CTA unwinds).
+// With a workspace that holds every record, progress does not depend on which CTAs are
+// resident: only walkers wait, and only for records; a worker never waits for another CTA,
+// and the items are claimed in order by workers that are running, so the earliest
+// unpublished record is always in work.  The walkers (at most kMaxWalkers) are fewer than
+// the CTAs that one wave holds, so workers always run beside them.
+//
+// A bounded workspace holds the records of `ring` packed chunks: chunk g's record goes to
+// slot g mod ring, and its worker writes there only once both walkers of chunk g - ring
+// (the slot's previous record) have copied that one in, which each signals by adding one to
+// the record's copy count.  Every such wait is for an earlier chunk than the waiter's, whose
+// item was claimed earlier, so with the grid resident there is no cycle; the chunk work
+// then leads the walk by at most `ring` chunks, and the records stay in L2 (T = 65536,
+// H = 32, 16 chunks: 1.16 times the path's algorithmic DRAM bytes, against 2.46 with every
+// record).  The ring is the RING instantiation; with every record held the kernel is
+// instantiated without it and no worker waits.  The ring is not the faster form then:
+// workers held to the walk's pace share the SMs with it to the end, where unheld they
+// finish early and leave the walkers their SMs (2.16 ms with 16 chunks, against 1.97).
+//
+// Every wait is bounded (a flag or count that does not come up within the limit is
+// recorded as KDA_ERR_TIMEOUT and the CTA unwinds).
 //
 // Two walkers share a head, each with 64 of its value columns (the columns of S evolve
 // independently), and each forms the transposed products, so that its part fits in a CTA
@@ -1081,11 +1115,12 @@ __device__ __forceinline__ void issue_walk(uint32_t tmem, uint32_t sb, bool with
 //             then store o_c while the next group runs.
 // Every barrier's producer stays within one phase of its consumers (each refill waits for
 // the consumption of what it overwrites), so no wait is ever more than one phase behind.
+template <bool RING>
 __device__ __forceinline__ void walk_unit(int walker, const CUtensorMap &tm_v, const int32_t *__restrict__ cu,
                                           int64_t total, int H, const int32_t *__restrict__ cc,
-                                          const unsigned char *__restrict__ records, const int *flags,
-                                          const float *init_state, __nv_bfloat16 *__restrict__ o, float *final_state,
-                                          uint32_t *status, const StateSlots &slots)
+                                          const unsigned char *__restrict__ records, const int *flags, int *cons,
+                                          int ring, const float *init_state, __nv_bfloat16 *__restrict__ o,
+                                          float *final_state, uint32_t *status, const StateSlots &slots)
 {
     using L = WalkLayout;
     extern __shared__ unsigned char smem_raw[];
@@ -1113,10 +1148,28 @@ __device__ __forceinline__ void walk_unit(int walker, const CUtensorMap &tm_v, c
                     si >= 0 ? init_state[si * st_entry + st_head + (size_t)i * kD + jrow] : 0.f;
         return;
     }
-    if (sf < 0 && o == nullptr) return;  // nothing to store and no outputs
-    const unsigned char *rec0 = records + ((size_t)cc[n] * H + h) * kRecBytes;
+    // record c: chunk cc[n] + c, its ready flag, its copy count and its slot (without RING:
+    // every chunk has its own and no count is kept)
+    const int g0 = cc[n];  // read once: the waits' memory clobbers would reload it at every use
+    const int *flag0 = flags + (size_t)g0 * H + h;
+    int *cons0 = cons + (size_t)g0 * H + h;
+    const unsigned char *rec_h = records + (size_t)h * kRecBytes;
     const size_t rec_stride = (size_t)H * kRecBytes;
-    const int *flag0 = flags + (size_t)cc[n] * H + h;
+    auto rec_at = [&](int c) {
+        const int g = g0 + c;
+        return rec_h + (size_t)(RING ? g % ring : g) * rec_stride;
+    };
+    if (sf < 0 && o == nullptr) {  // nothing to store and no outputs: each slot is free once filled
+        if (RING && tid == 0)
+            for (int c = 0; c < nch; ++c) {
+                if (!wait_count_at_least(flag0 + (size_t)c * H, 1)) {
+                    atomicOr(status, DEV_ERR_TIMEOUT);
+                    break;
+                }
+                red_release_add_gpu(cons0 + (size_t)c * H, 1);
+            }
+        return;
+    }
     if (tid == 0) {
         mbar_init(&w_ready, kWalkStateWarps);
         mbar_init(&w_mma, 1);
@@ -1157,13 +1210,13 @@ __device__ __forceinline__ void walk_unit(int walker, const CUtensorMap &tm_v, c
     };
     auto load_gamma = [&](int c) {
         mbar_arrive_expect_tx(&w_g[c & 1], kD * 4);
-        bulk_load(sm + L::GAM + (c & 1) * kD * 4, rec0 + (size_t)c * rec_stride + R_GM, kD * 4, &w_g[c & 1]);
+        bulk_load(sm + L::GAM + (c & 1) * kD * 4, rec_at(c) + R_GM, kD * 4, &w_g[c & 1]);
         g_issued = c + 1;
     };
     // N, P (and with outputs Q', P2) as the group's operands: P and P2 first (w_pp), then
     // N and Q' (w_rec)
     auto load_record = [&](int c) {
-        const unsigned char *r = rec0 + (size_t)c * rec_stride;
+        const unsigned char *r = rec_at(c);
         mbar_arrive_expect_tx(&w_pp, o ? 24576u : 16384u);
         bulk_load(sm + L::PP, r + R_P, o ? 24576u : 16384u, &w_pp);  // P2 follows P in both
         mbar_arrive_expect_tx(&w_rec, o ? 49152u : 32768u);
@@ -1296,6 +1349,10 @@ __device__ __forceinline__ void walk_unit(int walker, const CUtensorMap &tm_v, c
                     ok = mbar_wait_spin_ns(&w_rec, (uint32_t)(c & 1), kWaitNs);
                     if (ok) issue_walk_ns(tmem, sb, o != nullptr);
                     mma_commit(&w_mma);
+                    // record c is in shared memory (its gamma since ready(c)): every read of its
+                    // slot has completed, so the slot may be refilled.  A relaxed add: a release
+                    // here would wait for this thread's copies in flight, on the walk's chain.
+                    if (RING && ok) red_relaxed_add_gpu(cons0 + (size_t)c * H, 1);
                 }
                 if (ok && c + 2 < nch) {  // the box of chunk c + 2, once that of c + 1 is read
                     ok = mbar_wait_ns(&w_vfree, (uint32_t)((c + 1) & 1), kWaitNs);
@@ -1335,12 +1392,11 @@ __device__ __forceinline__ void walk_unit(int walker, const CUtensorMap &tm_v, c
             if (c + 1 < nch) ok = read_v(c + 1, vt);
             if (ok && warp == 0 && lane == 0 && c + 2 < nch) {
                 // while this chunk's products run: record c + 2's flag, then (its buffer is
-                // free once every state warp is past chunk c - 1: ready(c)) its gamma, and
-                // later in the walk the record into L2 (it may have left L2 since it was written)
+                // free once every state warp is past chunk c - 1: ready(c)) its gamma
                 ok = wait_flag(c + 2) && mbar_wait_ns(&w_ready, (uint32_t)(c & 1), kWaitNs);
                 if (ok) {
                     load_gamma(c + 2);
-                    if (c + 2 >= kWalkPrefetchFrom) bulk_prefetch_l2(rec0 + (size_t)(c + 2) * rec_stride, kRecBytes);
+                    if (c + 2 >= kWalkPrefetchFrom) bulk_prefetch_l2(rec_at(c + 2), kRecBytes);
                 }
             }
             ok = __all_sync(0xffffffffu, ok) && __all_sync(0xffffffffu, mbar_wait_ns(&w_mma, (uint32_t)(c & 1), kWaitNs));
@@ -1411,7 +1467,7 @@ __device__ __forceinline__ void walk_unit(int walker, const CUtensorMap &tm_v, c
 
 // The streamed prefill: walkers (blockIdx.x < n_walk, two per (sequence, head)) and chunk
 // workers in one grid.
-template <bool NORM>
+template <bool NORM, bool RING>
 __global__ void __launch_bounds__(kChunkThreads, 2)
 prefill_stream_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                       const __grid_constant__ CUtensorMap tm_la, const __grid_constant__ CUtensorMap tm_v,
@@ -1419,17 +1475,21 @@ prefill_stream_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_con
                       const int2 *__restrict__ desc, int H, int chunks, unsigned char *records, int *flags,
                       uint32_t *status, bool scalar_gate, const int32_t *__restrict__ cu, int64_t total,
                       const int32_t *__restrict__ cc, const float *init_state, __nv_bfloat16 *o,
-                      float *final_state, StateSlots slots, int n_walk)
+                      float *final_state, StateSlots slots, int n_walk, int ring)
 {
     // launched with programmatic stream serialization behind the schedule kernel, which
-    // zeroes the flags and the claim counter: nothing it writes is read before this wait
+    // zeroes the flags, the copy counts and the claim counter: nothing it writes is read
+    // before this wait
     pdl_wait();
     pdl_launch_dependents();
+    // the workspace's ready flags, then the records' copy counts, then the claim counter
+    int *cons = flags + (size_t)chunks * H, *claim = cons + (size_t)chunks * H;
     if ((int)blockIdx.x < n_walk)
-        walk_unit((int)blockIdx.x, tm_v, cu, total, H, cc, records, flags, init_state, o, final_state, status, slots);
+        walk_unit<RING>((int)blockIdx.x, tm_v, cu, total, H, cc, records, flags, cons, ring, init_state, o,
+                        final_state, status, slots);
     else
-        chunk_items<NORM, true>(tm_q, tm_k, tm_la, log_alpha, beta, desc, H, 0, chunks, records, status,
-                                o != nullptr, scalar_gate, 0, 1, flags, flags + (size_t)chunks * H);
+        chunk_items<NORM, true, RING>(tm_q, tm_k, tm_la, log_alpha, beta, desc, H, 0, chunks, records, status,
+                                o != nullptr, scalar_gate, 0, 1, flags, cons, claim, ring);
 }
 
 // ============================================================== product-group diagnostic
@@ -1633,14 +1693,14 @@ int sm_count()
 
 // The streamed prefill (walkers and chunk workers in one grid of two CTAs per SM), for
 // problems with at most kMaxWalkers (sequence, head) units and every record in the
-// workspace.  cudaErrorNotSupported when the grid would leave fewer worker CTAs than SMs
+// workspace, or (RING) the records of p.ring_chunks chunks as a ring.  cudaErrorNotSupported when the grid would leave fewer worker CTAs than SMs
 // (the caller then runs the two kernels).
-template <bool NORM>
+template <bool NORM, bool RING>
 cudaError_t launch_stream(const PrefillProblem &p, const CUtensorMap &tq, const CUtensorMap &tk,
                           const CUtensorMap &tla, const int32_t *cc, void *records, int units)
 {
     static int dev_cfg = -1;
-    cudaError_t err = allow_smem(prefill_stream_kernel<NORM>, (int)kStreamSmem, &dev_cfg);
+    cudaError_t err = allow_smem(prefill_stream_kernel<NORM, RING>, (int)kStreamSmem, &dev_cfg);
     if (err != cudaSuccess) return err;
     const int sms = sm_count();
     if (sms <= 0 || 2 * sms - (kD / kWalkCols) * units < sms) return cudaErrorNotSupported;
@@ -1657,10 +1717,11 @@ cudaError_t launch_stream(const PrefillProblem &p, const CUtensorMap &tq, const 
     cfg.gridDim = dim3(2 * sms);
     cfg.blockDim = dim3(kChunkThreads);
     cfg.dynamicSmemBytes = kStreamSmem;
-    return cudaLaunchKernelEx(&cfg, prefill_stream_kernel<NORM>, tq, tk, tla, tv, p.log_alpha, p.beta,
+    return cudaLaunchKernelEx(&cfg, prefill_stream_kernel<NORM, RING>, tq, tk, tla, tv, p.log_alpha, p.beta,
                               (const int2 *)p.desc, p.num_heads, p.chunk_bound, static_cast<unsigned char *>(records),
                               p.flags, p.status, p.scalar_gate, p.cu_seqlens, p.total_tokens, cc, p.init_state,
-                              static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.slots, (kD / kWalkCols) * units);
+                              static_cast<__nv_bfloat16 *>(p.o), p.final_state, p.slots, (kD / kWalkCols) * units,
+                              RING ? p.ring_chunks : 0);
 }
 
 }  // namespace
@@ -1717,14 +1778,23 @@ cudaError_t launch_prefill_split(const PrefillProblem &p, const int32_t *cc, voi
     // 32-column state slices while every (sequence, head, slice) of the pass fits in one wave
     // of SMs (their chain per chunk is shorter); 64-column slices beyond that, and for the
     // sequence split, whose transition pass is sized for them
+    // records for only ring_chunks chunks: the streamed kernel or nothing (the two kernels
+    // would need every record)
+    const bool ring_only = p.ring_chunks > 0 && p.ring_chunks < p.chunk_bound;
     if (prefill_stream_eligible(p)) {
         const int units = p.num_seqs * p.num_heads;
-        err = p.qk_l2norm ? launch_stream<true>(p, tq, tk, tla, cc, records, units)
-                          : launch_stream<false>(p, tq, tk, tla, cc, records, units);
-        if (err != cudaErrorNotSupported) {
+        if (ring_only)
+            err = p.qk_l2norm ? launch_stream<true, true>(p, tq, tk, tla, cc, records, units)
+                              : launch_stream<false, true>(p, tq, tk, tla, cc, records, units);
+        else
+            err = p.qk_l2norm ? launch_stream<true, false>(p, tq, tk, tla, cc, records, units)
+                              : launch_stream<false, false>(p, tq, tk, tla, cc, records, units);
+        if (err != cudaErrorNotSupported || ring_only) {
             if (err == cudaSuccess && mid) err = cudaEventRecord(mid, p.stream);
             return err;
         }
+    } else if (ring_only) {
+        return cudaErrorInvalidValue;
     }
     const unsigned char *rec = static_cast<const unsigned char *>(records);
     const int64_t slices32 = (int64_t)p.num_seqs * p.num_heads * (kD / 32);

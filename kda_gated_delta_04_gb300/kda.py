@@ -29,6 +29,7 @@ KDA_FLAG_STREAM = 16
 KDA_PATH_CUDA_CORE, KDA_PATH_FUSED, KDA_PATH_TWO_KERNEL, KDA_PATH_SEQ_SPLIT, KDA_PATH_SEGMENTED, \
     KDA_PATH_STREAMED = range(6)
 CHUNK = 64
+KDA_STREAM_RING_MIN = 8
 
 _lib = None
 _lock = threading.Lock()
@@ -44,6 +45,8 @@ EXPORTS = {
                                                  _c.c_int32, _c.c_int]),
     "kda_prefill_workspace_size_segmented": (_c.c_size_t, [_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
                                                            _c.c_int32, _c.c_int, _c.c_int64]),
+    "kda_prefill_workspace_size_streamed": (_c.c_size_t, [_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32,
+                                                          _c.c_int32, _c.c_int, _c.c_int64]),
     "kda_prefill_path": (_c.c_int32, [_c.c_int32, _c.c_int64, _c.c_int32, _c.c_int32, _c.c_int32, _c.c_int,
                                        _c.c_size_t, _c.c_uint32]),
     "kda_prefill": (_c.c_int, _PREFILL_ARGS),
@@ -101,6 +104,11 @@ def kda_prefill_workspace_size_segmented(num_seqs, total_tokens, num_heads, d_k,
                                          segment_chunks):
     return lib().kda_prefill_workspace_size_segmented(num_seqs, total_tokens, num_heads, d_k, d_v,
                                                       dtype, segment_chunks)
+
+
+def kda_prefill_workspace_size_streamed(num_seqs, total_tokens, num_heads, d_k, d_v, dtype, ring_chunks):
+    return lib().kda_prefill_workspace_size_streamed(num_seqs, total_tokens, num_heads, d_k, d_v, dtype,
+                                                     ring_chunks)
 
 
 def kda_prefill_path(num_seqs, total_tokens, num_heads, d_k, d_v, dtype, workspace_bytes, flags=0):
@@ -282,6 +290,16 @@ def segmented_workspace_for(num_seqs, total_tokens, num_heads, d, dtype_code, de
                                                   segment_chunks)
     if nbytes == 0:
         raise KdaError(KDA_ERR_UNSUPPORTED, "kda_prefill_workspace_size_segmented")
+    return torch.empty(nbytes, dtype=torch.uint8, device=device)
+
+
+def streamed_workspace_for(num_seqs, total_tokens, num_heads, d, dtype_code, device, ring_chunks):
+    """A workspace whose records cover a ring of `ring_chunks` packed chunks: where the call
+    streams, the streamed prefill then reuses their slots (kda_prefill_workspace_size_streamed)."""
+    torch = _torch()
+    nbytes = kda_prefill_workspace_size_streamed(num_seqs, total_tokens, num_heads, d, d, dtype_code, ring_chunks)
+    if nbytes == 0:
+        raise KdaError(KDA_ERR_UNSUPPORTED, "kda_prefill_workspace_size_streamed")
     return torch.empty(nbytes, dtype=torch.uint8, device=device)
 
 

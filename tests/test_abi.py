@@ -67,8 +67,9 @@ def test_segmented_workspace_size(kda):
     assert kda.kda_prefill_workspace_size_segmented(N, T, H, 128, 128, 0, 10 * bound) == full_seg
     assert full_seg - one == (bound - 1) * H * 74240
     # the records of every chunk, as in the full workspace (this shape has no sequence split),
-    # plus the two carried states, less the full workspace's ready flag per chunk-head record
-    flags = -(-(bound * H + 1) * 4 // 256) * 256
+    # plus the two carried states, less the full workspace's ready flag and copy count per
+    # chunk-head record (and its item counter)
+    flags = -(-(2 * bound * H + 1) * 4 // 256) * 256
     assert full_seg - kda.kda_prefill_workspace_size(N, T, H, 128, 128, 0) == 2 * H * 128 * 128 * 4 - flags
     for bad in (dict(seg=0), dict(dtype=1), dict(d=64), dict(T=0), dict(H=0)):
         a = dict(N=N, T=T, H=H, d=128, dtype=0, seg=4)
@@ -76,6 +77,23 @@ def test_segmented_workspace_size(kda):
         assert kda.kda_prefill_workspace_size_segmented(a["N"], a["T"], a["H"], a["d"], a["d"], a["dtype"],
                                                         a["seg"]) == 0
 
+
+def test_streamed_workspace_size(kda):
+    """kda_prefill_workspace_size_streamed: the streamed prefill's fixed part plus the records
+    of ring_chunks packed chunks.  One more chunk adds one chunk's records (the step of the
+    segmented size); clamped to every chunk it is the full workspace of a shape without the
+    sequence split; 0 below KDA_STREAM_RING_MIN chunks and for shapes the tensor-core path
+    does not run; at T = 65536, H = 32 a ring of 16 chunks is under 40 MB."""
+    N, T, H = 1, 4096, 32
+    bound = T // 64 + N
+    size = lambda ring, d=128, dt=0, T=T: kda.kda_prefill_workspace_size_streamed(N, T, H, d, d, dt, ring)
+    seg = lambda c: kda.kda_prefill_workspace_size_segmented(N, T, H, 128, 128, 0, c)
+    assert size(9) - size(8) == seg(2) - seg(1) > 0
+    full = kda.kda_prefill_workspace_size(N, T, H, 128, 128, 0)
+    assert size(bound) == size(10 * bound) == full
+    assert size(kda.KDA_STREAM_RING_MIN) > 0 and size(kda.KDA_STREAM_RING_MIN - 1) == 0
+    assert size(8, dt=1) == 0 and size(8, d=64) == 0 and size(8, T=0) == 0
+    assert 0 < kda.kda_prefill_workspace_size_streamed(1, 65536, 32, 128, 128, 0, 16) < 40e6
 
 def test_prefill_path_query(kda):
     """kda_prefill_path, on the shapes and workspaces that decide it without the device (the

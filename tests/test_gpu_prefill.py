@@ -621,10 +621,10 @@ def test_bounded_records_run_in_segments(seg_chunks):
     ws = kda.segmented_workspace_for(6, T, H, 128, kda.KDA_DTYPE_BF16, "cuda", seg_chunks)
     assert ws.numel() < kda.kda_prefill_workspace_size(6, T, H, 128, 128, kda.KDA_DTYPE_BF16)
     o, fs = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"],
-                        workspace=ws, check_status=True)
+                        workspace=ws, check_status=True, streamed=False)
     fs_inplace = d["init_state"].clone()
     o2, _ = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], fs_inplace,
-                        final_state=fs_inplace, workspace=ws, check_status=True)
+                        final_state=fs_inplace, workspace=ws, check_status=True, streamed=False)
     torch.cuda.synchronize()
     np.testing.assert_array_equal(synth.to_f64(o), synth.to_f64(o_ref_gpu))
     np.testing.assert_array_equal(synth.to_f64(fs), synth.to_f64(fs_ref_gpu))
@@ -636,8 +636,9 @@ def test_bounded_records_run_in_segments(seg_chunks):
 
 def test_bounded_records_at_full_size():
     """T = 65536, H = 32 from initial states with the records of 128 chunks at a time (8
-    segments, 304 MB of records instead of 2.4 GB): bit for bit the full workspace in the
-    same two-kernel form."""
+    segments, 304 MB of records instead of 2.4 GB), in the two-kernel form (KDA_FLAG_NO_STREAM:
+    this shape would otherwise stream over a ring of the same records): bit for bit the full
+    workspace in the same form."""
     w = synth.PREFILL_64K
     inp = synth.prefill_inputs(w)
     d = to_device(inp)
@@ -646,7 +647,7 @@ def test_bounded_records_at_full_size():
                                   d["init_state"], check_status=True, seq_split=False, streamed=False)
     ws = kda.segmented_workspace_for(1, T, H, 128, kda.KDA_DTYPE_BF16, "cuda", 128)
     o, fs = kda.prefill(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"],
-                        workspace=ws, check_status=True)
+                        workspace=ws, check_status=True, streamed=False)
     torch.cuda.synchronize()
     assert torch.equal(o, o_full) and torch.equal(fs, fs_full)
 

@@ -196,3 +196,62 @@ def test_streamed_form_with_few_units_when_asked():
                             check_status=True, seq_split=False, streamed=True)
         o_ref, fs_ref = oracle_prefill(inp)
         assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, w.dtype, name)
+
+
+def test_streamed_over_a_ring_of_records():
+    """A bounded workspace (kda_prefill_workspace_size_streamed) on a call that streams: the
+    streamed kernel keeps the records of only `ring` packed chunks, each slot written again
+    once both walkers of its previous record have copied it in.  o and the final states are
+    bit for bit those of the full workspace: the benchmark shape with rings of 8 and 20
+    chunks (of 64); ragged sequences with a zero-length one and initial states (asked to
+    stream, four heads), also against the oracle; the state-only form; and a state-pool call
+    without outputs in which some sequences store no final state, so that their walkers
+    leave at once and only release the slots.  With KDA_FLAG_NO_STREAM the same workspace
+    runs the two kernels in segments."""
+    def ring_ws(N, T, H, ring):
+        ws = kda.streamed_workspace_for(N, T, H, 128, kda.KDA_DTYPE_BF16, "cuda", ring)
+        assert ws.numel() < kda.kda_prefill_workspace_size(N, T, H, 128, 128, kda.KDA_DTYPE_BF16)
+        return ws
+
+    d = to_device(synth.prefill_inputs(synth.PREFILL_4K))
+    args = (d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"])
+    o_full, fs_full = kda.prefill(*args, check_status=True)
+    _, fs_full_so = kda.prefill(*args, check_status=True, outputs=False)
+    for ring in (8, 20):
+        ws = ring_ws(1, 4096, 32, ring)
+        assert kda.kda_prefill_path(1, 4096, 32, 128, 128, kda.KDA_DTYPE_BF16, ws.numel(), 0) == kda.KDA_PATH_STREAMED
+        assert kda.kda_prefill_path(1, 4096, 32, 128, 128, kda.KDA_DTYPE_BF16, ws.numel(),
+                                    kda.KDA_FLAG_NO_STREAM) == kda.KDA_PATH_SEGMENTED
+        o, fs = kda.prefill(*args, workspace=ws, check_status=True)
+        assert torch.equal(o, o_full) and torch.equal(fs, fs_full), f"ring {ring}"
+        o_none, fs_so = kda.prefill(*args, workspace=ws, check_status=True, outputs=False)
+        assert o_none is None and torch.equal(fs_so, fs_full_so), f"ring {ring}, state only"
+
+    lens = (1000, 0, 300, 2000, 64)
+    w = PrefillWorkload("stream_ring_ragged_H4", 350, 4, 128, "bf16", lens, len(lens), init_state=True)
+    inp = synth.prefill_inputs(w)
+    d = to_device(inp)
+    args = (d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"])
+    T = sum(lens)
+    ws = ring_ws(len(lens), T, 4, 8)
+    assert kda.kda_prefill_path(len(lens), T, 4, 128, 128, kda.KDA_DTYPE_BF16, ws.numel(),
+                                kda.KDA_FLAG_STREAM) == kda.KDA_PATH_STREAMED
+    o_full, fs_full = kda.prefill(*args, check_status=True, seq_split=False, streamed=True)
+    o, fs = kda.prefill(*args, workspace=ws, check_status=True, seq_split=False, streamed=True)
+    assert torch.equal(o, o_full) and torch.equal(fs, fs_full)
+    o_ref, fs_ref = oracle_prefill(inp)
+    assert_parity(synth.to_f64(o), synth.to_f64(fs), o_ref, fs_ref, w.dtype, w.name + " (ring of 8 chunks)")
+
+    # the pool: sequences 1 and 3 store no final state (their walkers only release slots)
+    pool = torch.zeros(len(lens) + 1, 4, 128, 128, dtype=torch.float32, device="cuda")
+    final_slots = torch.tensor([0, -1, 2, -1, 4], dtype=torch.int32, device="cuda")
+    init_slots = torch.full((len(lens),), -1, dtype=torch.int32, device="cuda")
+    pool_full = pool.clone()
+    kda.prefill_slots(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], pool_full, final_slots,
+                      init_slots, check_status=True, outputs=False, seq_split=False, streamed=True)
+    kda.prefill_slots(d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], pool, final_slots,
+                      init_slots, workspace=ring_ws(len(lens), T, 4, 8), check_status=True, outputs=False,
+                      seq_split=False, streamed=True)
+    torch.cuda.synchronize()
+    assert torch.equal(pool, pool_full)
+    assert not pool[0].eq(0).all() and pool[1].eq(0).all() and pool[3].eq(0).all()
