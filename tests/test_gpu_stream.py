@@ -255,3 +255,24 @@ def test_streamed_over_a_ring_of_records():
     torch.cuda.synchronize()
     assert torch.equal(pool, pool_full)
     assert not pool[0].eq(0).all() and pool[1].eq(0).all() and pool[3].eq(0).all()
+
+
+def test_streamed_ring_variants():
+    """The ring of records with the kernel variants: raw q, k normalised in the kernels (the
+    ring's NORM instantiation), with the channel-wise gate and with a scalar gate ([T, H] log
+    decay), each bit for bit the same call with the full workspace."""
+    w = PrefillWorkload("stream_ring_variants", 360, 16, 128, "bf16", (1500, 700), 2, init_state=True,
+                        raw_qk=True)
+    inp = synth.prefill_inputs(w)
+    d = to_device(inp)
+    T, H = sum(w.seq_lens), w.num_heads
+    g = torch.Generator().manual_seed(361)
+    la_s = (-0.05 * torch.nn.functional.softplus(torch.randn(T, H, generator=g))).float().contiguous().cuda()
+    ws = kda.streamed_workspace_for(2, T, H, 128, kda.KDA_DTYPE_BF16, "cuda", 8)
+    for name, la in (("qk_l2norm", d["log_alpha"]), ("qk_l2norm_scalar_gate", la_s)):
+        args = (d["q"], d["k"], d["v"], la, d["beta"])
+        kw = dict(cu_seqlens=d["cu_seqlens"], init_state=d["init_state"], check_status=True, qk_l2norm=True,
+                  seq_split=False, streamed=True)
+        o_full, fs_full = kda.prefill(*args, **kw)
+        o, fs = kda.prefill(*args, workspace=ws, **kw)
+        assert torch.equal(o, o_full) and torch.equal(fs, fs_full), name
