@@ -276,3 +276,17 @@ def test_streamed_ring_variants():
         o_full, fs_full = kda.prefill(*args, **kw)
         o, fs = kda.prefill(*args, workspace=ws, **kw)
         assert torch.equal(o, o_full) and torch.equal(fs, fs_full), name
+
+
+def test_streamed_ring_at_full_size():
+    """T = 65536, H = 32 from initial states with the records of 16 chunks (each slot
+    refilled 64 times, the chunk work held to the walk's pace throughout): o and the final
+    states bit for bit those of the full workspace."""
+    d = to_device(synth.prefill_inputs(synth.PREFILL_64K))
+    T, H = d["q"].shape[:2]
+    args = (d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"])
+    o_full, fs_full = kda.prefill(*args, check_status=True)
+    ws = kda.streamed_workspace_for(1, T, H, 128, kda.KDA_DTYPE_BF16, "cuda", 16)
+    assert kda.kda_prefill_path(1, T, H, 128, 128, kda.KDA_DTYPE_BF16, ws.numel(), 0) == kda.KDA_PATH_STREAMED
+    o, fs = kda.prefill(*args, workspace=ws, check_status=True)
+    assert torch.equal(o, o_full) and torch.equal(fs, fs_full)
