@@ -290,3 +290,24 @@ def test_streamed_ring_at_full_size():
     assert kda.kda_prefill_path(1, T, H, 128, 128, kda.KDA_DTYPE_BF16, ws.numel(), 0) == kda.KDA_PATH_STREAMED
     o, fs = kda.prefill(*args, workspace=ws, check_status=True)
     assert torch.equal(o, o_full) and torch.equal(fs, fs_full)
+
+
+def test_streamed_ring_across_many_short_sequences():
+    """24 short sequences (0 to 300 tokens, some empty) of one head each, asked to stream over a
+    ring of 8 chunks: chunk g's slot is then mostly handed over by another sequence's walkers.
+    o and the final states (and the final states alone) bit for bit the full workspace."""
+    rng = np.random.default_rng(370)
+    lens = tuple(int(x) for x in rng.integers(0, 301, size=24))
+    lens = (0,) + lens[1:12] + (0,) + lens[13:]
+    w = PrefillWorkload("stream_ring_short_seqs", 371, 1, 128, "bf16", lens, len(lens), init_state=True)
+    d = to_device(synth.prefill_inputs(w))
+    T = sum(lens)
+    args = (d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"])
+    ws = kda.streamed_workspace_for(len(lens), T, 1, 128, kda.KDA_DTYPE_BF16, "cuda", 8)
+    assert kda.kda_prefill_path(len(lens), T, 1, 128, 128, kda.KDA_DTYPE_BF16, ws.numel(),
+                                kda.KDA_FLAG_STREAM | kda.KDA_FLAG_NO_SEQ_SPLIT) == kda.KDA_PATH_STREAMED
+    for outputs in (True, False):
+        kw = dict(check_status=True, seq_split=False, streamed=True, outputs=outputs)
+        o_full, fs_full = kda.prefill(*args, **kw)
+        o, fs = kda.prefill(*args, workspace=ws, **kw)
+        assert torch.equal(fs, fs_full) and (o is None if not outputs else torch.equal(o, o_full)), outputs
