@@ -38,6 +38,20 @@ def test_library_exports_every_declared_symbol(kda):
     assert set(declared_functions()) == set(kda.EXPORTS)
 
 
+def test_binding_constants_match_the_header(kda):
+    """Every integer constant the binding restates (status codes, dtypes, option flags, path
+    codes, the ring minimum, device error bits) has the header's value: the header's integer
+    #defines and enumerators, parsed from its text."""
+    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    consts = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(KDA_[A-Z0-9_]+)\s+(\d+)u?\s*$", src, re.M)}
+    consts.update({m.group(1): int(m.group(2)) for m in re.finditer(r"\b(KDA_[A-Z0-9_]+)\s*=\s*(\d+)\b", src)})
+    shared = sorted(n for n in consts if hasattr(kda, n))
+    for n in shared:
+        assert getattr(kda, n) == consts[n], n
+    for required in ("KDA_OK", "KDA_ERR_VALUE_RANGE", "KDA_DTYPE_F32", "KDA_FLAG_STREAM", "KDA_PATH_STREAMED",
+                     "KDA_STREAM_RING_MIN"):
+        assert required in shared, required
+
 def test_status_strings(kda):
     for code in range(7):
         s = kda.status_string(code)
