@@ -154,7 +154,8 @@ def source_sha(files):
     """Hash of the kernel sources a profile was taken on (paths relative to the repo)."""
     h = hashlib.sha256()
     for f in sorted(files):
-        h.update(open(os.path.join(ROOT, f), "rb").read())
+        with open(os.path.join(ROOT, f), "rb") as fh:
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 

@@ -2,6 +2,7 @@
 rejects bad arguments on the host before touching any GPU."""
 import ctypes
 import os
+import pathlib
 import re
 
 import pytest
@@ -19,7 +20,7 @@ def kda():
 
 
 def declared_functions():
-    src = open(HEADER).read()
+    src = pathlib.Path(HEADER).read_text()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(kda_[a-z0-9_]+)\s*\(", src)))
 
@@ -42,7 +43,7 @@ def test_binding_constants_match_the_header(kda):
     """Every integer constant the binding restates (status codes, dtypes, option flags, path
     codes, the ring minimum, device error bits) has the header's value: the header's integer
     #defines and enumerators, parsed from its text."""
-    src = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    src = re.sub(r"/\*.*?\*/", "", pathlib.Path(HEADER).read_text(), flags=re.S)
     consts = {m.group(1): int(m.group(2)) for m in re.finditer(r"#define\s+(KDA_[A-Z0-9_]+)\s+(\d+)u?\s*$", src, re.M)}
     consts.update({m.group(1): int(m.group(2)) for m in re.finditer(r"\b(KDA_[A-Z0-9_]+)\s*=\s*(\d+)\b", src)})
     shared = sorted(n for n in consts if hasattr(kda, n))
@@ -205,7 +206,7 @@ def test_product_path_does_not_import_the_oracle():
     for dirpath, _, files in os.walk(pkg):
         for f in files:
             if f.endswith((".py", ".cu", ".cuh", ".c", ".h")):
-                text = open(os.path.join(dirpath, f)).read()
+                text = pathlib.Path(dirpath, f).read_text()
                 assert "import oracle" not in text and "from oracle" not in text, f
                 assert "kda_oracle" not in text, f
 

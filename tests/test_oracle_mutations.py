@@ -8,6 +8,7 @@ restored afterwards.
 import ctypes
 import inspect
 import os
+import pathlib
 import subprocess
 
 import pytest
@@ -78,7 +79,7 @@ def _pin_functions():
 
 @pytest.mark.parametrize("mutation", sorted(MUTATIONS))
 def test_pins_catch_mutation(mutation, tmp_path):
-    src = open(SRC).read()
+    src = pathlib.Path(SRC).read_text()
     for old, new in MUTATIONS[mutation]:
         assert src.count(old) == 1, f"mutation {mutation} no longer matches the oracle source"
         src = src.replace(old, new)
