@@ -165,19 +165,22 @@ def test_streamed_results_do_not_depend_on_timing():
     which CTAs run.  A record read before its stores were complete, or a buffer refilled
     early, would show up as a difference between calls.  The benchmark workload (T = 4096,
     H = 32: 64 walkers beside 240 workers), with the L2 flushed before every other call so
-    that the timing varies; the two-kernel form the same way."""
+    that the timing varies; the two-kernel form the same way, and the streamed form over a
+    ring of 8 chunks' records (whose slots pass between CTAs as the timing allows)."""
     w = synth.PREFILL_4K
     d = to_device(synth.prefill_inputs(w))
     args = (d["q"], d["k"], d["v"], d["log_alpha"], d["beta"], d["cu_seqlens"], d["init_state"])
     flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
-    for streamed in (True, False):
-        o0, s0 = kda.prefill(*args, check_status=True, streamed=streamed)
+    ring = kda.streamed_workspace_for(1, 4096, 32, 128, kda.KDA_DTYPE_BF16, "cuda", 8)
+    for form, kw in (("streamed", dict(streamed=True)), ("two kernels", dict(streamed=False)),
+                     ("ring of 8 chunks", dict(workspace=ring))):
+        o0, s0 = kda.prefill(*args, check_status=True, **kw)
         o0, s0 = o0.clone(), s0.clone()
         for i in range(16):
             if i % 2:
                 flush.zero_()
-            o, s = kda.prefill(*args, check_status=True, streamed=streamed)
-            assert torch.equal(o, o0) and torch.equal(s, s0), f"call {i + 1} differs (streamed={streamed})"
+            o, s = kda.prefill(*args, check_status=True, **kw)
+            assert torch.equal(o, o0) and torch.equal(s, s0), f"call {i + 1} differs ({form})"
 
 
 def test_streamed_form_with_few_units_when_asked():
